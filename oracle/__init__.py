@@ -1,0 +1,312 @@
+"""Python access to the plain CPU oracle (``mtp_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline leg use it; the CUDA library never does.  The oracle
+is compiled with gcc on first use (``build()``) and loaded through ctypes.  It
+shares no code with the CUDA path; both take their inputs from ``synth``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mtp_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (gcc, OpenMP when available)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-std=c11", "-D_DEFAULT_SOURCE", "-shared", "-fPIC", "-o", _LIB_PATH + ".tmp", _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True)
+    os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
+    return _LIB_PATH
+
+
+class Model(C.Structure):
+    _fields_ = [("d_t", C.c_int32), ("d_a", C.c_int32), ("n_blocks", C.c_int32),
+                ("n_q_heads", C.c_int32), ("head_dim", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("d_ff", C.c_int32), ("vocab", C.c_int32), ("wbf16", C.c_int32), ("pad_", C.c_int32),
+                ("rms_eps", C.c_double), ("attn_scale", C.c_double), ("emb_scale", C.c_double),
+                ("logit_softcap", C.c_double)]
+
+
+class View(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("stride_b", C.c_int64),
+                ("stride_h", C.c_int64), ("stride_t", C.c_int64), ("cap", C.c_int32),
+                ("window", C.c_int32), ("rope_theta", C.c_double)]
+
+
+class SampleParams(C.Structure):
+    _fields_ = [("temp", C.c_double), ("top_p", C.c_double), ("min_p", C.c_double),
+                ("rep_penalty", C.c_double), ("presence_penalty", C.c_double),
+                ("top_k", C.c_int32), ("pad_", C.c_int32)]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = C.CDLL(build())
+            _declare(_lib)
+    return _lib
+
+
+def _declare(L):
+    P, I, D, U64 = C.c_void_p, C.c_int, C.c_double, C.c_uint64
+    L.orc_rmsnorm.argtypes = [P, I, P, D, P]
+    L.orc_matvec.argtypes = [P, I, I, I, P, P]
+    L.orc_gelu_tanh.argtypes = [D]
+    L.orc_gelu_tanh.restype = D
+    L.orc_rope_neox.argtypes = [P, I, C.c_int64, D]
+    L.orc_argmax_f64.argtypes = [P, C.c_int64]
+    L.orc_argmax_f64.restype = C.c_int64
+    L.orc_attend_head.argtypes = [P, P, I, I, I, I, D, I, P]
+    L.orc_philox4x32_10.argtypes = [P, P, P]
+    L.orc_uniform.argtypes = [U64, U64, C.c_uint32, C.c_uint32, C.c_uint32]
+    L.orc_uniform.restype = D
+    L.orc_sample_dist.argtypes = [P, I, P, I, P, P, P, P, P]
+    L.orc_sample_dist.restype = I
+    L.orc_pick.argtypes = [P, P, I, D, D, P]
+    L.orc_pick.restype = C.c_int32
+    L.orc_draft_step.argtypes = [P, P, P, P, I, I, P, I, P, P, P, P]
+    L.orc_draft_step.restype = I
+    L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, P, I, P, P, P, P, P]
+    L.orc_draft_block.restype = I
+    L.orc_verify_greedy.argtypes = [P, I, I, I, I, P, P, P]
+    L.orc_verify_sample.argtypes = [P, P, I, I, I, I, P, P, I, P, U64, U64, P, P, P]
+    L.orc_num_threads.restype = I
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def num_threads() -> int:
+    return int(lib().orc_num_threads())
+
+
+# ----------------------------------------------------------------------------
+# building blocks (exposed for the pins)
+# ----------------------------------------------------------------------------
+
+def rmsnorm(x, g=None, eps=1e-6):
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    g = None if g is None else np.ascontiguousarray(g, dtype=np.float32)
+    y = np.empty_like(x)
+    lib().orc_rmsnorm(_p(x), x.size, _p(g), eps, _p(y))
+    return y
+
+
+def matvec(W, x, bf16=False):
+    W = np.ascontiguousarray(W)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty(W.shape[0], dtype=np.float64)
+    lib().orc_matvec(_p(W), W.shape[0], W.shape[1], int(bf16), _p(x), _p(y))
+    return y
+
+
+def gelu_tanh(x):
+    return np.array([lib().orc_gelu_tanh(float(v)) for v in np.ravel(x)]).reshape(np.shape(x))
+
+
+def rope_neox(q, pos, theta):
+    q = np.array(q, dtype=np.float64, copy=True)
+    lib().orc_rope_neox(_p(q), q.size, int(pos), float(theta))
+    return q
+
+
+def argmax(z):
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    return int(lib().orc_argmax_f64(_p(z), z.size))
+
+
+def attend_head(q, k, v, b, g, kv_len, window=0, scale=None, bf16=False):
+    """k, v: [B, Hkv, cap, hd] arrays (fp32, or uint16 bf16 bits with bf16=True)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    B, H, cap, hd = k.shape
+    vw = View(_p(k).value, _p(v).value, H * cap * hd, cap * hd, hd, cap, window, 0.0)
+    out = np.empty(hd, dtype=np.float64)
+    sc = 1.0 / np.sqrt(hd) if scale is None else scale
+    lib().orc_attend_head(_p(q), C.byref(vw), b, g, hd, kv_len, sc, int(bf16), _p(out))
+    return out
+
+
+def philox4x32_10(ctr, key):
+    c = np.asarray(ctr, dtype=np.uint32)
+    k = np.asarray(key, dtype=np.uint32)
+    o = np.empty(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_p(c), _p(k), _p(o))
+    return o
+
+
+def uniform(seed, offset, b, i, purpose):
+    return float(lib().orc_uniform(seed, offset, b, i, purpose))
+
+
+def make_params(sp) -> SampleParams:
+    return SampleParams(float(sp.temp), float(sp.top_p), float(sp.min_p), float(sp.rep_penalty),
+                        float(getattr(sp, "presence_penalty", 0.0)), int(getattr(sp, "top_k", 0)), 0)
+
+
+def sample_dist(z, pen, sp):
+    """Returns (ids, weights, wsum, margin) of sample_dist(z) in (weight desc, id asc) order."""
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    pen = np.ascontiguousarray(np.asarray(pen, dtype=np.int32).reshape(-1))
+    V = z.size
+    ids = np.empty(V, dtype=np.int32)
+    w = np.empty(V, dtype=np.float64)
+    ws = C.c_double()
+    mg = C.c_double()
+    prm = make_params(sp)
+    n = lib().orc_sample_dist(_p(z), V, _p(pen), pen.size, C.byref(prm), _p(ids), _p(w),
+                              C.byref(ws), C.byref(mg))
+    return ids[:n].copy(), w[:n].copy(), ws.value, mg.value
+
+
+def pick(ids, w, wsum, u):
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    mg = C.c_double()
+    r = lib().orc_pick(_p(ids), _p(w), ids.size, float(wsum), float(u), C.byref(mg))
+    return int(r), mg.value
+
+
+# ----------------------------------------------------------------------------
+# draft block
+# ----------------------------------------------------------------------------
+
+GLOBAL_ORDER = ("tok_embd", "norm_e", "norm_h", "w_pre", "final_norm", "w_post")
+BLOCK_ORDER = ("attn_norm", "w_q", "q_norm", "w_o", "post_attn_norm", "pre_ffn_norm",
+               "w_gate", "w_up", "w_down", "post_ffn_norm")
+
+
+class _Bound:
+    """ctypes views of one workload, restricted to one sequence b (or all)."""
+
+    def __init__(self, w, b=None):
+        m = w.model
+        self.keep = []
+        self.model = Model(m.d_t, m.d_a, m.n_blocks, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff,
+                           m.vocab, 1 if m.dtype == "bf16" else 0, 0, m.rms_eps, m.attn_scale,
+                           m.emb_scale, m.logit_softcap)
+        names = list(GLOBAL_ORDER) + [f"blk{i}.{n}" for i in range(m.n_blocks) for n in BLOCK_ORDER]
+        arrs = [np.ascontiguousarray(w.weights[n]) for n in names]
+        self.keep += arrs
+        self.tensors = (C.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+        self.block_view = np.ascontiguousarray(np.asarray(m.block_view, dtype=np.int32))
+        views = []
+        esz = 2 if m.dtype == "bf16" else 4
+        for vd in w.views:
+            k, v = vd["k"], vd["v"]
+            Bv, H, cap, hd = k.shape
+            off = 0 if b is None else b * H * cap * hd * esz
+            views.append(View(k.ctypes.data + off, v.ctypes.data + off, H * cap * hd, cap * hd, hd,
+                              cap, vd["window"], vd["rope_theta"]))
+            self.keep += [k, v]
+        self.views = (View * len(views))(*views)
+        self.n_views = len(views)
+        sl = slice(None) if b is None else slice(b, b + 1)
+        self.B = w.B if b is None else 1
+        self.kv_len = np.ascontiguousarray(w.kv_len[sl], dtype=np.int32)
+        self.last_tok = np.ascontiguousarray(w.last_tok[sl], dtype=np.int32)
+        self.h_prev = np.ascontiguousarray(w.h_prev[sl], dtype=np.float32)
+        self.hist = np.ascontiguousarray(w.hist[sl], dtype=np.int32)
+
+
+def draft_block(w, sample=None, seed=0, offset=0, force=None, seqs=None, want_logits=True):
+    """Run the oracle draft block over sequences ``seqs`` (default: all).
+
+    ``force`` ([B, N] int32, optional) teacher-forces the token consumed at
+    step k+1 to force[b, k] instead of the oracle's own pick.
+    Returns dict(drafts [S,N] int32, h_last [S,d_t] f64, logits [S,N,V] f64 or
+    None, margin [S,N] f64) for the S selected sequences, in ``seqs`` order.
+    """
+    L = lib()
+    m = w.model
+    seqs = list(range(w.B)) if seqs is None else list(seqs)
+    S, N, V = len(seqs), w.N, m.vocab
+    out_d = np.empty((S, N), dtype=np.int32)
+    out_h = np.empty((S, m.d_t), dtype=np.float64)
+    out_z = np.empty((S, N, V), dtype=np.float64) if want_logits else None
+    out_m = np.empty((S, N), dtype=np.float64)
+    prm = make_params(sample) if sample is not None else None
+    for j, b in enumerate(seqs):
+        bd = _Bound(w, b)
+        f = None if force is None else np.ascontiguousarray(force[b:b + 1], dtype=np.int32)
+        d = np.empty((1, N), dtype=np.int32)
+        h = np.empty((1, m.d_t), dtype=np.float64)
+        z = np.empty((1, N, V), dtype=np.float64) if want_logits else None
+        mg = np.empty((1, N), dtype=np.float64)
+        rc = L.orc_draft_block(C.byref(bd.model), bd.tensors, _p(bd.block_view), bd.views, bd.n_views,
+                               1, N, _p(bd.kv_len), _p(bd.last_tok), _p(bd.h_prev),
+                               C.byref(prm) if prm is not None else None, seed, offset,
+                               _p(bd.hist), bd.hist.shape[1], _p(f), _p(d), _p(h), _p(z), _p(mg))
+        if rc != 0:
+            raise ValueError(f"oracle draft block rejected its inputs (rc={rc})")
+        out_d[j], out_h[j], out_m[j] = d[0], h[0], mg[0]
+        if want_logits:
+            out_z[j] = z[0]
+    return dict(drafts=out_d, h_last=out_h, logits=out_z, margin=out_m)
+
+
+def draft_step(w, b, step, tok, h_prev):
+    """One oracle step for sequence b: returns (h_next [d_t] f64, logits [V] f64)."""
+    L = lib()
+    bd = _Bound(w, b)
+    m = w.model
+    tk = np.array([tok], dtype=np.int32)
+    h = np.ascontiguousarray(np.asarray(h_prev, dtype=np.float64).reshape(1, m.d_t))
+    hn = np.empty((1, m.d_t), dtype=np.float64)
+    z = np.empty((1, m.vocab), dtype=np.float64)
+    rc = L.orc_draft_step(C.byref(bd.model), bd.tensors, _p(bd.block_view), bd.views, bd.n_views, 1,
+                          _p(bd.kv_len), step, _p(tk), _p(h), _p(hn), _p(z))
+    if rc != 0:
+        raise ValueError("oracle draft step rejected its inputs")
+    return hn[0], z[0]
+
+
+# ----------------------------------------------------------------------------
+# verify
+# ----------------------------------------------------------------------------
+
+def verify_greedy(logits, dtype, drafts):
+    logits = np.ascontiguousarray(logits)
+    drafts = np.ascontiguousarray(drafts, dtype=np.int32)
+    B, R, V = logits.shape
+    N = R - 1
+    out = np.empty((B, N + 1), dtype=np.int32)
+    n_acc = np.empty(B, dtype=np.int32)
+    lib().orc_verify_greedy(_p(logits), 1 if dtype == "bf16" else 0, B, N, V, _p(drafts), _p(out), _p(n_acc))
+    return out, n_acc
+
+
+def verify_sample(target, draft, dtype, drafts, hist, params, seed, offset):
+    """Returns (out_tokens [B,1+N], n_accept [B], margin [B])."""
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    drafts = np.ascontiguousarray(drafts, dtype=np.int32)
+    hist = np.ascontiguousarray(hist, dtype=np.int32)
+    B, R, V = target.shape
+    N = R - 1
+    H = hist.shape[1] if hist.ndim == 2 else 0
+    out = np.empty((B, N + 1), dtype=np.int32)
+    n_acc = np.empty(B, dtype=np.int32)
+    mg = np.empty(B, dtype=np.float64)
+    prm = make_params(params)
+    lib().orc_verify_sample(_p(target), _p(draft), 1 if dtype == "bf16" else 0, B, N, V, _p(drafts),
+                            _p(hist), H, C.byref(prm), seed, offset, _p(out), _p(n_acc), _p(mg))
+    return out, n_acc, mg

@@ -1,0 +1,614 @@
+/*
+ * mtp_oracle.c -- plain, slow CPU oracle for the MTP draft block and the
+ * verify-accept step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file: only the test suite, the package's smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or helper with the
+ * CUDA library; the two meet only through the seeded inputs of the `synth`
+ * module.
+ *
+ * Arithmetic is fp64 throughout.  bf16 inputs are widened exactly (bits << 16).
+ * Loops run in the order the definitions are written; the only parallelism is
+ * an OpenMP split of independent output rows / sequences, which does not
+ * change any row's summation order.
+ *
+ * Sources (page title, section):
+ *  [G4]  "Gemma 4 MTP -- Multi-Token Prediction speculative decoding",
+ *        sec. 3 (pre/post projection shapes), sec. 4 "Per-step MTP graph"
+ *        (embedding scale, concat + pre-projection, block order, final norm,
+ *        post-projection, LM head, softcap, in-graph argmax), sec. 5 "KV
+ *        sharing" (mask admits every position <= attn_pos; one mask for all
+ *        steps; draft positions are > attn_pos).
+ *  [NX]  "MTP decoding (--mtp)", "Requirements" (NextN enorm / hnorm / eh_proj:
+ *        separate norms of the token embedding and of the hidden state before
+ *        the projection) and "How it is wired" (accept the longest prefix whose
+ *        argmax matches, the next token comes from the first unverified row).
+ *  [SP]  "opus-mtp-turbo: Track 1 report", item 4 "temp > 0 verification"
+ *        (sample_dist: top-k, penalties over history + input[0..i], temp,
+ *        min-p, top-p; accept with p(x)/q(x); on reject sample
+ *        norm(max(p - q, 0)); a fully accepted window samples its last row).
+ *  [FN]  "Fused NextN draft graph", delta 6 (the fused steps cross-attend the
+ *        frozen prefix read-only; the recurrence is carried by the hidden
+ *        state chain alone).
+ *  [PH]  Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+ *        1, 2, 3" (SC'11): the Philox-4x32-10 counter-based generator.
+ *
+ * Readings taken where the pages are silent (each is also listed in the
+ * design notes): RMSNorm y = x / sqrt(mean(x^2) + eps) * g with the gain g
+ * stored directly; RoPE rotates Q only, NeoX half-split pairs (i, i + hd/2),
+ * angle pos * theta^(-2i/hd), pos = kv_len + step; GQA maps q head h to kv
+ * head h / (Hq / Hkv); GELU is the tanh form; argmax ties go to the lowest
+ * index and NaN never wins; the sliding window reads the last W positions
+ * [kv_len - W, kv_len) at every step; KV views are ring buffers (position t in
+ * slot t % cap).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* types (the oracle's own; the CUDA library declares its own elsewhere)     */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int32_t d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab;
+    int32_t wbf16;        /* 1: weight matrices and KV are bf16 bit patterns; 0: fp32 */
+    int32_t pad_;
+    double rms_eps, attn_scale, emb_scale, logit_softcap;
+} orc_model;
+
+typedef struct {
+    const void *k, *v;
+    int64_t stride_b, stride_h, stride_t;   /* elements; head_dim is contiguous */
+    int32_t cap, window;                    /* ring slots; 0 = full attention */
+    double rope_theta;
+} orc_view;
+
+typedef struct {
+    double temp, top_p, min_p, rep_penalty, presence_penalty;
+    int32_t top_k, pad_;
+} orc_sample_params;
+
+/* tensor table: globals first, then B_COUNT entries per block */
+enum { T_TOK_EMBD, T_NORM_E, T_NORM_H, T_W_PRE, T_FINAL_NORM, T_W_POST, T_GLOBAL_COUNT };
+enum { B_ATTN_NORM, B_W_Q, B_Q_NORM, B_W_O, B_POST_ATTN_NORM, B_PRE_FFN_NORM,
+       B_W_GATE, B_W_UP, B_W_DOWN, B_POST_FFN_NORM, B_COUNT };
+
+/* ------------------------------------------------------------------------ */
+/* element access                                                            */
+/* ------------------------------------------------------------------------ */
+
+static double bf16_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double elem(const void *p, int64_t i, int bf16) {
+    if (bf16) return bf16_to_double(((const uint16_t *)p)[i]);
+    return (double)((const float *)p)[i];
+}
+
+/* ------------------------------------------------------------------------ */
+/* building blocks                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* RMSNorm (reading: y = x / sqrt(mean(x^2) + eps) * g; g == NULL means unit gains) */
+void orc_rmsnorm(const double *x, int n, const float *g, double eps, double *y) {
+    double ss = 0.0;
+    for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+    double r = 1.0 / sqrt(ss / (double)n + eps);
+    for (int i = 0; i < n; ++i) y[i] = x[i] * r * (g ? (double)g[i] : 1.0);
+}
+
+/* y[r] = sum_c W[r, c] * x[c], W row-major [rows, cols]; plain dot per row */
+void orc_matvec(const void *W, int rows, int cols, int bf16, const double *x, double *y) {
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        const int64_t base = (int64_t)r * cols;
+        for (int c = 0; c < cols; ++c) acc += elem(W, base + c, bf16) * x[c];
+        y[r] = acc;
+    }
+}
+
+/* GELU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+double orc_gelu_tanh(double x) {
+    const double k = sqrt(2.0 / M_PI);
+    return 0.5 * x * (1.0 + tanh(k * (x + 0.044715 * x * x * x)));
+}
+
+/* RoPE on one head vector, NeoX half-split pairs (i, i + hd/2) */
+void orc_rope_neox(double *q, int hd, int64_t pos, double theta) {
+    const int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        double ang = (double)pos * pow(theta, -2.0 * (double)i / (double)hd);
+        double c = cos(ang), s = sin(ang);
+        double a = q[i], b = q[i + half];
+        q[i] = a * c - b * s;
+        q[i + half] = a * s + b * c;
+    }
+}
+
+/* first index of the largest value; NaN never wins; all-NaN -> 0 */
+int64_t orc_argmax_f64(const double *z, int64_t n) {
+    int64_t best = -1;
+    double bv = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double v = z[i];
+        if (isnan(v)) continue;
+        if (best < 0 || v > bv) { best = i; bv = v; }
+    }
+    return best < 0 ? 0 : best;
+}
+
+static int64_t argmax_stored(const void *z, int64_t n, int bf16) {
+    int64_t best = -1;
+    double bv = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double v = elem(z, i, bf16);
+        if (isnan(v)) continue;
+        if (best < 0 || v > bv) { best = i; bv = v; }
+    }
+    return best < 0 ? 0 : best;
+}
+
+/* Cross-attention of one query head into one KV view ([G4] sec. 4-5, [FN] delta 6).
+ * Keys: positions t in [lo, kv_len), lo = max(0, kv_len - window) for a sliding
+ * view, 0 for a full one; position t is stored in ring slot t % cap.  V is used
+ * as stored. */
+void orc_attend_head(const double *q, const orc_view *vw, int b, int g, int hd, int kv_len,
+                     double scale, int bf16, double *out) {
+    const int lo = (vw->window > 0 && kv_len > vw->window) ? kv_len - vw->window : 0;
+    const int n = kv_len - lo;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+        int64_t slot = (int64_t)((lo + j) % vw->cap);
+        int64_t base = (int64_t)b * vw->stride_b + (int64_t)g * vw->stride_h + slot * vw->stride_t;
+        double acc = 0.0;
+        for (int d = 0; d < hd; ++d) acc += q[d] * elem(vw->k, base + d, bf16);
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+    }
+    double den = 0.0;
+    for (int d = 0; d < hd; ++d) out[d] = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double w = exp(s[j] - m);
+        den += w;
+        int64_t slot = (int64_t)((lo + j) % vw->cap);
+        int64_t base = (int64_t)b * vw->stride_b + (int64_t)g * vw->stride_h + slot * vw->stride_t;
+        for (int d = 0; d < hd; ++d) out[d] += w * elem(vw->v, base + d, bf16);
+    }
+    for (int d = 0; d < hd; ++d) out[d] /= den;
+    free(s);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Philox-4x32-10 [PH]                                                       */
+/* ------------------------------------------------------------------------ */
+
+static void mulhilo32(uint32_t a, uint32_t b, uint32_t *hi, uint32_t *lo) {
+    uint64_t p = (uint64_t)a * (uint64_t)b;
+    *hi = (uint32_t)(p >> 32);
+    *lo = (uint32_t)p;
+}
+
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; ++r) {
+        uint32_t hi0, lo0, hi1, lo1;
+        mulhilo32(0xD2511F53u, c0, &hi0, &lo0);
+        mulhilo32(0xCD9E8D57u, c2, &hi1, &lo1);
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n1 = lo1;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        uint32_t n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* uniform in [0, 1) for (sequence b, row i, purpose): counter (b, 4 i + purpose,
+ * offset lo, offset hi), key (seed lo, seed hi); u = (word0 >> 8) * 2^-24 */
+double orc_uniform(uint64_t seed, uint64_t offset, uint32_t b, uint32_t i, uint32_t purpose) {
+    uint32_t ctr[4] = { b, i * 4u + purpose, (uint32_t)offset, (uint32_t)(offset >> 32) };
+    uint32_t key[2] = { (uint32_t)seed, (uint32_t)(seed >> 32) };
+    uint32_t out[4];
+    orc_philox4x32_10(ctr, key, out);
+    return (double)(out[0] >> 8) * (1.0 / 16777216.0);
+}
+
+/* ------------------------------------------------------------------------ */
+/* sample_dist [SP item 4]                                                   */
+/* ------------------------------------------------------------------------ */
+
+typedef struct { int id; double w; } cand;
+
+static int cand_cmp(const void *a, const void *b) {
+    const cand *x = (const cand *)a, *y = (const cand *)b;
+    if (x->w > y->w) return -1;
+    if (x->w < y->w) return 1;
+    return (x->id < y->id) ? -1 : (x->id > y->id);
+}
+
+static int raw_cmp(const void *a, const void *b) {   /* value desc, id asc */
+    return cand_cmp(a, b);
+}
+
+/* Builds sample_dist(z) for one row.
+ *   z     raw logits, V entries (double)
+ *   pen   penalty token list (history + this window's inputs); duplicates and
+ *         out-of-range ids are ignored; each distinct token is penalised once
+ *   order top-k (off when top_k <= 0) -> repetition penalty (z > 0: z / r,
+ *         else z * r) and presence penalty (z - pres) -> temperature ->
+ *         min-p (keep exp(l - lmax) >= min_p) -> top-p (sorted by weight desc,
+ *         id asc; keep the shortest prefix whose share of the kept mass reaches
+ *         top_p) -> renormalise.
+ * Output: n kept candidates, ids[] / w[] in (w desc, id asc) order, w[] the
+ * unnormalised weights exp(l - lmax); *wsum their sum in that order.
+ * *margin (optional) receives the smallest relative distance of any keep/cut
+ * decision or ordering tie to its threshold. */
+int orc_sample_dist(const double *z, int V, const int32_t *pen, int n_pen,
+                    const orc_sample_params *sp, int32_t *ids, double *w, double *wsum,
+                    double *margin) {
+    double *l = (double *)malloc(sizeof(double) * (size_t)V);
+    unsigned char *alive = (unsigned char *)malloc((size_t)V);
+    for (int x = 0; x < V; ++x) { l[x] = z[x]; alive[x] = !isnan(z[x]); }
+    double mg = INFINITY;
+
+    if (sp->top_k > 0 && sp->top_k < V) {
+        cand *all = (cand *)malloc(sizeof(cand) * (size_t)V);
+        int na = 0;
+        for (int x = 0; x < V; ++x) if (alive[x]) { all[na].id = x; all[na].w = l[x]; ++na; }
+        qsort(all, (size_t)na, sizeof(cand), raw_cmp);
+        memset(alive, 0, (size_t)V);
+        for (int j = 0; j < na && j < sp->top_k; ++j) alive[all[j].id] = 1;
+        if (na > sp->top_k) {
+            double a = all[sp->top_k - 1].w, c = all[sp->top_k].w;
+            double d = fabs(a - c) / (fabs(a) + 1e-30);
+            if (d > 0.0 && d < mg) mg = d;
+        }
+        free(all);
+    }
+
+    /* penalties, once per distinct token */
+    unsigned char *seen = (unsigned char *)calloc((size_t)V, 1);
+    for (int j = 0; j < n_pen; ++j) {
+        int x = pen[j];
+        if (x < 0 || x >= V || seen[x]) continue;
+        seen[x] = 1;
+        if (l[x] > 0.0) l[x] = l[x] / sp->rep_penalty;
+        else l[x] = l[x] * sp->rep_penalty;
+        l[x] -= sp->presence_penalty;
+    }
+    free(seen);
+
+    /* temperature */
+    for (int x = 0; x < V; ++x) l[x] = l[x] / sp->temp;
+
+    double lmax = -INFINITY;
+    for (int x = 0; x < V; ++x) if (alive[x] && l[x] > lmax) lmax = l[x];
+
+    /* min-p: keep p(x) >= min_p * p_max, i.e. exp(l - lmax) >= min_p */
+    cand *c = (cand *)malloc(sizeof(cand) * (size_t)V);
+    int n = 0;
+    for (int x = 0; x < V; ++x) {
+        if (!alive[x]) continue;
+        double wx = exp(l[x] - lmax);
+        if (sp->min_p > 0.0) {
+            double d = fabs(wx - sp->min_p) / sp->min_p;
+            if (d < mg) mg = d;
+        }
+        if (wx >= sp->min_p) { c[n].id = x; c[n].w = wx; ++n; }
+    }
+    qsort(c, (size_t)n, sizeof(cand), cand_cmp);
+    for (int j = 1; j < n; ++j) {
+        double d = fabs(c[j - 1].w - c[j].w) / (c[j - 1].w + 1e-300);
+        if (d > 0.0 && d < mg) mg = d;   /* exact ties are ordered by id on both sides */
+    }
+
+    /* top-p over the renormalised min-p set */
+    if (sp->top_p < 1.0 && n > 0) {
+        double tot = 0.0;
+        for (int j = 0; j < n; ++j) tot += c[j].w;
+        double cum = 0.0;
+        int keep = n;
+        for (int j = 0; j < n; ++j) {
+            cum += c[j].w;
+            double share = cum / tot;
+            double d = fabs(share - sp->top_p);
+            if (d < mg) mg = d;
+            if (share >= sp->top_p) { keep = j + 1; break; }
+        }
+        n = keep;
+    }
+    double s = 0.0;
+    for (int j = 0; j < n; ++j) { ids[j] = c[j].id; w[j] = c[j].w; s += c[j].w; }
+    *wsum = s;
+    if (margin) *margin = mg;
+    free(c); free(alive); free(l);
+    return n;
+}
+
+/* inverse-CDF pick over candidates in their stored order: the first j with
+ * u * wsum < w[0] + ... + w[j].  *margin receives the distance of u * wsum to
+ * the nearer edge of the chosen interval, relative to wsum. */
+int32_t orc_pick(const int32_t *ids, const double *w, int n, double wsum, double u, double *margin) {
+    double target = u * wsum, acc = 0.0, prev = 0.0;
+    for (int j = 0; j < n; ++j) {
+        prev = acc;
+        acc += w[j];
+        if (target < acc) {
+            double a = target - prev, b = acc - target;
+            if (margin) *margin = (a < b ? a : b) / (wsum > 0.0 ? wsum : 1.0);
+            return ids[j];
+        }
+    }
+    if (margin) *margin = 0.0;   /* fell off the end through rounding: a boundary case */
+    return n > 0 ? ids[n - 1] : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the draft step ([G4] sec. 4, [NX] Requirements)                           */
+/* ------------------------------------------------------------------------ */
+
+#define TT(i) (t[(i)])
+#define BT(blk, i) (t[T_GLOBAL_COUNT + (blk) * B_COUNT + (i)])
+
+/* One draft step for B independent sequences.
+ *   tok[b]      token consumed at this step (the last token for step 0, the
+ *               previous step's draft afterwards)
+ *   h_prev[b]   hidden state carried from the target (step 0) or from the
+ *               previous step's post-projection, [B, d_t]
+ *   step        k: RoPE position of the query is kv_len[b] + k
+ * Outputs h_next [B, d_t] (the next step's h_prev) and logits [B, V]. */
+int orc_draft_step(const orc_model *m, const void *const *t, const int32_t *block_view,
+                   const orc_view *views, int n_views, int B, const int32_t *kv_len, int step,
+                   const int32_t *tok, const double *h_prev, double *h_next, double *logits) {
+    const int d_t = m->d_t, d_a = m->d_a, hd = m->head_dim, Hq = m->n_q_heads, Hkv = m->n_kv_heads;
+    const int qw = Hq * hd, F = m->d_ff, V = m->vocab, bf = m->wbf16;
+    const int grp = Hq / Hkv;
+    double *e = malloc(sizeof(double) * d_t), *u = malloc(sizeof(double) * 2 * d_t);
+    double *x = malloc(sizeof(double) * d_a), *a = malloc(sizeof(double) * d_a);
+    double *q = malloc(sizeof(double) * qw), *o = malloc(sizeof(double) * qw);
+    double *y = malloc(sizeof(double) * (d_a > d_t ? d_a : d_t));
+    double *yn = malloc(sizeof(double) * d_a);
+    double *gt = malloc(sizeof(double) * F), *up = malloc(sizeof(double) * F);
+    for (int b = 0; b < B; ++b) {
+        int32_t tk = tok[b];
+        if (tk < 0 || tk >= V) { free(e); free(u); free(x); free(a); free(q); free(o); free(y); free(yn); free(gt); free(up); return -1; }
+        /* token embedding from the tied table, scaled ([G4] sec. 4 item 2) */
+        for (int c = 0; c < d_t; ++c) e[c] = elem(TT(T_TOK_EMBD), (int64_t)tk * d_t + c, bf) * m->emb_scale;
+        /* separate norms of the embedding and of h_prev, then concat ([NX] Requirements) */
+        orc_rmsnorm(e, d_t, (const float *)TT(T_NORM_E), m->rms_eps, u);
+        orc_rmsnorm(h_prev + (size_t)b * d_t, d_t, (const float *)TT(T_NORM_H), m->rms_eps, u + d_t);
+        /* pre-projection 2 d_t -> d_a ([G4] sec. 4 item 3) */
+        orc_matvec(TT(T_W_PRE), d_a, 2 * d_t, bf, u, x);
+        for (int l = 0; l < m->n_blocks; ++l) {
+            const orc_view *vw = &views[block_view[l]];
+            /* RMSNorm -> Q proj -> Q-norm -> RoPE ([G4] sec. 4 item 4) */
+            orc_rmsnorm(x, d_a, (const float *)BT(l, B_ATTN_NORM), m->rms_eps, a);
+            orc_matvec(BT(l, B_W_Q), qw, d_a, bf, a, q);
+            for (int h = 0; h < Hq; ++h) {
+                double tmp[1024];
+                double *qh = q + (size_t)h * hd;
+                orc_rmsnorm(qh, hd, (const float *)BT(l, B_Q_NORM), m->rms_eps, tmp);
+                memcpy(qh, tmp, sizeof(double) * hd);
+                orc_rope_neox(qh, hd, (int64_t)kv_len[b] + step, vw->rope_theta);
+            }
+            /* cross-attention into the target KV, no draft KV ([G4] sec. 5, [FN] delta 6) */
+            for (int h = 0; h < Hq; ++h)
+                orc_attend_head(q + (size_t)h * hd, vw, b, h / grp, hd, kv_len[b], m->attn_scale, bf,
+                                o + (size_t)h * hd);
+            /* o-projection, post-attention norm, residual ([G4] sec. 4 item 4) */
+            orc_matvec(BT(l, B_W_O), d_a, qw, bf, o, y);
+            orc_rmsnorm(y, d_a, (const float *)BT(l, B_POST_ATTN_NORM), m->rms_eps, yn);
+            for (int c = 0; c < d_a; ++c) x[c] += yn[c];
+            /* pre-FFN norm, GeGLU, post-FFN norm, residual */
+            orc_rmsnorm(x, d_a, (const float *)BT(l, B_PRE_FFN_NORM), m->rms_eps, a);
+            orc_matvec(BT(l, B_W_GATE), F, d_a, bf, a, gt);
+            orc_matvec(BT(l, B_W_UP), F, d_a, bf, a, up);
+            for (int f = 0; f < F; ++f) gt[f] = orc_gelu_tanh(gt[f]) * up[f];
+            orc_matvec(BT(l, B_W_DOWN), d_a, F, bf, gt, y);
+            orc_rmsnorm(y, d_a, (const float *)BT(l, B_POST_FFN_NORM), m->rms_eps, yn);
+            for (int c = 0; c < d_a; ++c) x[c] += yn[c];
+        }
+        /* final norm -> post-projection = next h_prev ([G4] sec. 4 item 5) */
+        orc_rmsnorm(x, d_a, (const float *)TT(T_FINAL_NORM), m->rms_eps, a);
+        double *hn = h_next + (size_t)b * d_t;
+        orc_matvec(TT(T_W_POST), d_t, d_a, bf, a, hn);
+        /* tied dense LM head, optional final-logit softcap ([G4] sec. 4 items 6-7) */
+        double *z = logits + (size_t)b * V;
+        orc_matvec(TT(T_TOK_EMBD), V, d_t, bf, hn, z);
+        if (m->logit_softcap > 0.0)
+            for (int v = 0; v < V; ++v) z[v] = m->logit_softcap * tanh(z[v] / m->logit_softcap);
+    }
+    (void)n_views;
+    free(e); free(u); free(x); free(a); free(q); free(o); free(y); free(yn); free(gt); free(up);
+    return 0;
+}
+
+/* N chained draft steps with the token chosen on "device" each step ([G4]
+ * sec. 4 item 8; [FN] the fused chain: argmax -> embed -> h chain).
+ *   sp == NULL or sp->temp <= 0: greedy (argmax).  Otherwise the token of
+ *   step k is drawn from sample_dist(z_k) with penalty set hist[b] u
+ *   drafts[b][0..k-1] and the uniform of (b, k, purpose 0).
+ * Outputs drafts [B, N], h_last [B, d_t] (optional), logits [B, N, V]
+ * (optional), margin [B, N] (optional: top1 - top2 logit gap of each greedy
+ * step, or the sampling decision's relative margin). */
+int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *block_view,
+                    const orc_view *views, int n_views, int B, int N, const int32_t *kv_len,
+                    const int32_t *last_tok, const float *h_prev, const orc_sample_params *sp,
+                    uint64_t seed, uint64_t offset, const int32_t *hist, int H,
+                    const int32_t *force_tok, int32_t *drafts, double *h_last, double *logits,
+                    double *margin) {
+    const int d_t = m->d_t, V = m->vocab;
+    double *h = malloc(sizeof(double) * (size_t)B * d_t), *hn = malloc(sizeof(double) * (size_t)B * d_t);
+    double *z = malloc(sizeof(double) * (size_t)B * V);
+    int32_t *tok = malloc(sizeof(int32_t) * (size_t)B);
+    int32_t *ids = malloc(sizeof(int32_t) * (size_t)V);
+    double *w = malloc(sizeof(double) * (size_t)V);
+    int32_t *pen = malloc(sizeof(int32_t) * (size_t)(H + N + 1));
+    int rc = 0;
+    for (size_t i = 0; i < (size_t)B * d_t; ++i) h[i] = (double)h_prev[i];
+    for (int b = 0; b < B; ++b) tok[b] = last_tok[b];
+    const int sampling = sp && sp->temp > 0.0;
+    for (int k = 0; k < N && rc == 0; ++k) {
+        rc = orc_draft_step(m, t, block_view, views, n_views, B, kv_len, k, tok, h, hn, z);
+        if (rc) break;
+        for (int b = 0; b < B; ++b) {
+            const double *zb = z + (size_t)b * V;
+            int32_t pick;
+            double mg;
+            if (!sampling) {
+                pick = (int32_t)orc_argmax_f64(zb, V);
+                double second = -INFINITY;
+                for (int v = 0; v < V; ++v) if (v != pick && zb[v] > second) second = zb[v];
+                mg = zb[pick] - second;
+            } else {
+                int np = 0;
+                for (int j = 0; j < H; ++j) pen[np++] = hist[(size_t)b * H + j];
+                for (int j = 0; j < k; ++j) pen[np++] = drafts[(size_t)b * N + j];
+                double ws, m1, m2;
+                int n = orc_sample_dist(zb, V, pen, np, sp, ids, w, &ws, &m1);
+                double u = orc_uniform(seed, offset, (uint32_t)b, (uint32_t)k, 0u);
+                pick = orc_pick(ids, w, n, ws, u, &m2);
+                mg = m1 < m2 ? m1 : m2;
+            }
+            if (margin) margin[(size_t)b * N + k] = mg;
+            if (logits) memcpy(logits + ((size_t)b * N + k) * V, zb, sizeof(double) * (size_t)V);
+            drafts[(size_t)b * N + k] = pick;
+            tok[b] = force_tok ? force_tok[(size_t)b * N + k] : pick;
+        }
+        double *sw = h; h = hn; hn = sw;
+    }
+    if (h_last && rc == 0) memcpy(h_last, h, sizeof(double) * (size_t)B * d_t);
+    free(h); free(hn); free(z); free(tok); free(ids); free(w); free(pen);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* verify-accept                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Greedy verify ([NX] How it is wired): t_i = argmax of target row i (rows
+ * 0..N); n_accept = the largest k with drafts[j] == t_j for all j < k; the
+ * emitted tokens are drafts[0..k-1] followed by the bonus t_k, padded with -1.
+ * logits [B, 1+N, V] (bf16 bits or fp32). */
+void orc_verify_greedy(const void *logits, int bf16, int B, int N, int V, const int32_t *drafts,
+                       int32_t *out_tokens, int32_t *out_n_accept) {
+#pragma omp parallel for schedule(static)
+    for (int b = 0; b < B; ++b) {
+        int k = 0;
+        int32_t *ot = out_tokens + (size_t)b * (N + 1);
+        for (int i = 0; i <= N; ++i) ot[i] = -1;
+        for (;;) {
+            const int64_t row = ((int64_t)b * (N + 1) + k) * V;
+            int32_t tk = (int32_t)argmax_stored((const char *)logits + row * (bf16 ? 2 : 4), V, bf16);
+            if (k < N && drafts[(size_t)b * N + k] == tk) { ot[k] = tk; ++k; continue; }
+            ot[k] = tk;
+            break;
+        }
+        out_n_accept[b] = k;
+    }
+}
+
+/* Exact speculative sampling at temp > 0 ([SP] item 4).
+ * Row i (0..N-1): p_i = sample_dist(target row i), q_i = sample_dist(draft row
+ * i), both with penalty set hist[b] u drafts[b][0..i-1].  The draft x = d_i is
+ * accepted iff u < p_i(x) / q_i(x) (u of (b, i, purpose 1)); on the first
+ * rejection the emitted token is drawn from norm(max(p_i - q_i, 0)) (from p_i
+ * when that residual is empty) with the uniform of (b, i, purpose 2) and the
+ * window ends.  If every draft is accepted, the bonus token is drawn from
+ * p_N (penalty set hist u d_0..d_{N-1}) with the uniform of (b, N, purpose 3).
+ * margin[b] (optional): the smallest relative distance of any decision taken
+ * for sequence b to its threshold. */
+void orc_verify_sample(const void *tgt, const void *dft, int bf16, int B, int N, int V,
+                       const int32_t *drafts, const int32_t *hist, int H,
+                       const orc_sample_params *sp, uint64_t seed, uint64_t offset,
+                       int32_t *out_tokens, int32_t *out_n_accept, double *margin) {
+#pragma omp parallel
+    {
+        double *z = malloc(sizeof(double) * (size_t)V);
+        int32_t *pid = malloc(sizeof(int32_t) * (size_t)V), *qid = malloc(sizeof(int32_t) * (size_t)V);
+        double *pw = malloc(sizeof(double) * (size_t)V), *qw = malloc(sizeof(double) * (size_t)V);
+        double *r = malloc(sizeof(double) * (size_t)V);
+        int32_t *pen = malloc(sizeof(int32_t) * (size_t)(H + N + 1));
+#pragma omp for schedule(dynamic, 64)
+        for (int b = 0; b < B; ++b) {
+            int32_t *ot = out_tokens + (size_t)b * (N + 1);
+            for (int i = 0; i <= N; ++i) ot[i] = -1;
+            double mg = INFINITY, m1;
+            int np = 0;
+            for (int j = 0; j < H; ++j) pen[np++] = hist[(size_t)b * H + j];
+            int i;
+            for (i = 0; i < N; ++i) {
+                const int64_t trow = ((int64_t)b * (N + 1) + i) * V;
+                const int64_t drow = ((int64_t)b * N + i) * V;
+                for (int v = 0; v < V; ++v) z[v] = elem(tgt, trow + v, bf16);
+                double ps, qs;
+                int np_ = orc_sample_dist(z, V, pen, np, sp, pid, pw, &ps, &m1);
+                if (m1 < mg) mg = m1;
+                for (int v = 0; v < V; ++v) z[v] = elem(dft, drow + v, bf16);
+                int nq = orc_sample_dist(z, V, pen, np, sp, qid, qw, &qs, &m1);
+                if (m1 < mg) mg = m1;
+                const int32_t x = drafts[(size_t)b * N + i];
+                double px = 0.0, qx = 0.0;
+                for (int j = 0; j < np_; ++j) if (pid[j] == x) { px = pw[j] / ps; break; }
+                for (int j = 0; j < nq; ++j) if (qid[j] == x) { qx = qw[j] / qs; break; }
+                double u = orc_uniform(seed, offset, (uint32_t)b, (uint32_t)i, 1u);
+                double ratio = px / qx;               /* qx == 0: +inf (px > 0) or NaN */
+                if (!isnan(ratio) && isfinite(ratio)) {
+                    double d = fabs(u - ratio);
+                    if (d < mg) mg = d;
+                }
+                if (u < ratio) { ot[i] = x; pen[np++] = x; continue; }
+                /* residual norm(max(p - q, 0)) over p's support, in p's order */
+                double R = 0.0;
+                for (int j = 0; j < np_; ++j) {
+                    double pj = pw[j] / ps, qj = 0.0;
+                    for (int jj = 0; jj < nq; ++jj) if (qid[jj] == pid[j]) { qj = qw[jj] / qs; break; }
+                    r[j] = pj > qj ? pj - qj : 0.0;
+                    R += r[j];
+                }
+                double u2 = orc_uniform(seed, offset, (uint32_t)b, (uint32_t)i, 2u);
+                if (R > 0.0) ot[i] = orc_pick(pid, r, np_, R, u2, &m1);
+                else ot[i] = orc_pick(pid, pw, np_, ps, u2, &m1);
+                if (m1 < mg) mg = m1;
+                break;
+            }
+            if (i == N) {
+                const int64_t trow = ((int64_t)b * (N + 1) + N) * V;
+                for (int v = 0; v < V; ++v) z[v] = elem(tgt, trow + v, bf16);
+                double ps;
+                int np_ = orc_sample_dist(z, V, pen, np, sp, pid, pw, &ps, &m1);
+                if (m1 < mg) mg = m1;
+                double u3 = orc_uniform(seed, offset, (uint32_t)b, (uint32_t)N, 3u);
+                ot[N] = orc_pick(pid, pw, np_, ps, u3, &m1);
+                if (m1 < mg) mg = m1;
+            }
+            out_n_accept[b] = i;
+            if (margin) margin[b] = mg;
+        }
+        free(z); free(pid); free(qid); free(pw); free(qw); free(r); free(pen);
+    }
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

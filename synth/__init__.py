@@ -1,0 +1,422 @@
+"""Seeded synthetic inputs for the MTP draft block and the verify-accept step.
+
+This module only draws random numbers and arranges them into the shapes the
+draft chain and the verifiers consume.  It holds none of the method's
+arithmetic: the CPU oracle (``oracle/``) and the CUDA library
+(``mtp_speculative_decoding_gb300``) both take their inputs from here and from
+nowhere else, and neither side is imported by this module.
+
+Shapes follow the model the pages describe (Gemma-4 assistant drafter, "Gemma 4
+MTP -- Multi-Token Prediction speculative decoding", sections 3-5): a token
+embedding table shared with the target, a pre-projection of the concatenated
+[token embedding; target hidden state], L assistant blocks that cross-attend into
+the target's last full-attention and last sliding-window KV layers, a
+post-projection back to the backbone width and the tied LM head.
+
+Conventions
+-----------
+* bf16 tensors are returned as ``np.uint16`` bit patterns, rounded from fp32
+  with round-to-nearest-even.  fp32 tensors are ``np.float32``.
+* RMSNorm gains are always fp32 and are drawn as ``1 + N(0, 0.02)``.
+* KV views are ``[B, n_kv_heads, cap, head_dim]`` ring buffers: position ``t``
+  lives in slot ``t % cap``.  Every slot that does not hold a position the
+  drafter may read (beyond ``kv_len`` or before the sliding window) is filled
+  with NaN, so an over-read shows up as a NaN in the output.
+* Every tensor gets its own random stream, keyed by (seed, tensor name, chunk),
+  so its values do not depend on which other tensors were generated or on the
+  number of worker threads.
+"""
+from __future__ import annotations
+
+import concurrent.futures as _cf
+import dataclasses
+import math
+import os
+import zlib
+
+import numpy as np
+
+BF16_NAN = np.uint16(0x7FC0)
+_CHUNK = 1 << 22  # elements per independent random stream
+
+
+# ----------------------------------------------------------------------------
+# random streams and bf16 rounding
+# ----------------------------------------------------------------------------
+
+def _stream(seed: int, name: str, chunk: int) -> np.random.Generator:
+    ss = np.random.SeedSequence([int(seed) & 0xFFFFFFFF, zlib.crc32(name.encode()), int(chunk)])
+    return np.random.Generator(np.random.SFC64(ss))
+
+
+def _threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32)
+    out = np.empty(a.shape, dtype=np.uint16)
+    flat_u = u.reshape(-1)
+    flat_o = out.reshape(-1)
+    n = flat_u.size
+
+    def conv(lo: int, hi: int) -> None:
+        x = flat_u[lo:hi]
+        bias = ((x >> 16) & 1) + np.uint32(0x7FFF)
+        r = ((x + bias) >> 16).astype(np.uint16)
+        nan = (x & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+        if nan.any():
+            r[nan] = BF16_NAN
+        flat_o[lo:hi] = r
+
+    step = 1 << 24
+    if n <= step:
+        conv(0, n)
+    else:
+        with _cf.ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(lambda lo: conv(lo, min(n, lo + step)), range(0, n, step)))
+    return out
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to fp32."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def normal(seed: int, name: str, shape, std: float = 1.0, mean: float = 0.0) -> np.ndarray:
+    """fp32 array of N(mean, std^2) values, one independent stream per chunk."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    out = np.empty(n, dtype=np.float32)
+
+    def fill(c: int) -> None:
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        g = _stream(seed, name, c)
+        g.standard_normal(hi - lo, dtype=np.float32, out=out[lo:hi])
+        if std != 1.0:
+            out[lo:hi] *= np.float32(std)
+        if mean != 0.0:
+            out[lo:hi] += np.float32(mean)
+
+    nch = (n + _CHUNK - 1) // _CHUNK
+    if nch <= 1:
+        for c in range(nch):
+            fill(c)
+    else:
+        with _cf.ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(fill, range(nch)))
+    return out.reshape(shape)
+
+
+def uniform_int(seed: int, name: str, shape, lo: int, hi: int) -> np.ndarray:
+    """int32 array uniform in [lo, hi)."""
+    g = _stream(seed, name, 0)
+    return g.integers(lo, hi, size=shape, dtype=np.int64).astype(np.int32)
+
+
+def _as_dtype(a: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return f32_to_bf16_bits(a)
+    if dtype == "f32":
+        return np.ascontiguousarray(a, dtype=np.float32)
+    raise ValueError(dtype)
+
+
+# ----------------------------------------------------------------------------
+# model / workload description
+# ----------------------------------------------------------------------------
+
+BLOCK_TENSORS = ("attn_norm", "w_q", "q_norm", "w_o", "post_attn_norm",
+                 "pre_ffn_norm", "w_gate", "w_up", "w_down", "post_ffn_norm")
+
+
+@dataclasses.dataclass
+class ModelSpec:
+    d_t: int           # backbone (target) width
+    d_a: int           # assistant width
+    n_blocks: int
+    n_q_heads: int
+    head_dim: int
+    n_kv_heads: int
+    d_ff: int
+    vocab: int
+    dtype: str = "bf16"          # weights and KV: "f32" or "bf16"
+    block_view: tuple = (0,)     # per block: index of the KV view it cross-attends
+    rms_eps: float = 1e-6
+    logit_softcap: float = 0.0
+
+    @property
+    def emb_scale(self) -> float:
+        return math.sqrt(self.d_t)
+
+    @property
+    def attn_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    def params(self) -> int:
+        d_t, d_a, q, F = self.d_t, self.d_a, self.n_q_heads * self.head_dim, self.d_ff
+        per_block = 2 * q * d_a + 3 * F * d_a
+        return self.vocab * d_t + 2 * d_t * d_a + self.n_blocks * per_block + d_t * d_a
+
+
+@dataclasses.dataclass
+class ViewSpec:
+    cap: int             # ring-buffer slots per (sequence, kv head)
+    window: int          # 0 = full attention over [0, kv_len); W > 0 = last W positions
+    rope_theta: float
+
+
+@dataclasses.dataclass
+class DraftWorkload:
+    name: str
+    model: ModelSpec
+    views_spec: list
+    B: int
+    N: int
+    weights: dict        # name -> array; per-block tensors as "blk{i}.{name}"
+    views: list          # list of dict(k, v, cap, window, rope_theta)
+    kv_len: np.ndarray   # int32 [B]
+    last_tok: np.ndarray  # int32 [B]
+    h_prev: np.ndarray   # float32 [B, d_t]
+    hist: np.ndarray     # int32 [B, H] (may be H = 0)
+
+    def weight_bytes(self) -> int:
+        return sum(int(a.nbytes) for a in self.weights.values())
+
+
+def make_model_weights(m: ModelSpec, seed: int, std: float = 0.02) -> dict:
+    q = m.n_q_heads * m.head_dim
+    shapes = {
+        "tok_embd": (m.vocab, m.d_t),
+        "w_pre": (m.d_a, 2 * m.d_t),
+        "w_post": (m.d_t, m.d_a),
+    }
+    norms = {"norm_e": m.d_t, "norm_h": m.d_t, "final_norm": m.d_a}
+    for i in range(m.n_blocks):
+        shapes[f"blk{i}.w_q"] = (q, m.d_a)
+        shapes[f"blk{i}.w_o"] = (m.d_a, q)
+        shapes[f"blk{i}.w_gate"] = (m.d_ff, m.d_a)
+        shapes[f"blk{i}.w_up"] = (m.d_ff, m.d_a)
+        shapes[f"blk{i}.w_down"] = (m.d_a, m.d_ff)
+        norms[f"blk{i}.attn_norm"] = m.d_a
+        norms[f"blk{i}.q_norm"] = m.head_dim
+        norms[f"blk{i}.post_attn_norm"] = m.d_a
+        norms[f"blk{i}.pre_ffn_norm"] = m.d_a
+        norms[f"blk{i}.post_ffn_norm"] = m.d_a
+    w = {}
+    for name, shp in shapes.items():
+        w[name] = _as_dtype(normal(seed, name, shp, std=std), m.dtype)
+    for name, n in norms.items():
+        w[name] = normal(seed, name, (n,), std=std, mean=1.0)
+    return w
+
+
+def view_valid_mask(cap: int, window: int, kv_len: int) -> np.ndarray:
+    """bool [cap]: which ring slots hold a position the drafter may read."""
+    lo = max(0, kv_len - window) if window > 0 else 0
+    mask = np.zeros(cap, dtype=bool)
+    t = np.arange(lo, kv_len)
+    mask[t % cap] = True
+    return mask
+
+
+def make_kv_view(m: ModelSpec, vs: ViewSpec, kv_len: np.ndarray, seed: int, tag: str) -> dict:
+    B = kv_len.shape[0]
+    shape = (B, m.n_kv_heads, vs.cap, m.head_dim)
+    out = {}
+    for which in ("k", "v"):
+        vals = normal(seed, f"{tag}.{which}", shape, std=1.0)
+        arr = _as_dtype(vals, m.dtype)
+        for b in range(B):
+            bad = ~view_valid_mask(vs.cap, vs.window, int(kv_len[b]))
+            if m.dtype == "bf16":
+                arr[b][:, bad, :] = BF16_NAN
+            else:
+                arr[b][:, bad, :] = np.nan
+        out[which] = arr
+    out.update(cap=vs.cap, window=vs.window, rope_theta=vs.rope_theta)
+    return out
+
+
+def make_draft_workload(name: str, m: ModelSpec, views_spec: list, B: int, N: int,
+                        kv_len, seed: int, hist_len: int = 0) -> DraftWorkload:
+    kv_len = np.asarray(kv_len, dtype=np.int32).reshape(B)
+    for vs in views_spec:
+        need = vs.window if vs.window > 0 else int(kv_len.max())
+        if need > vs.cap:
+            raise ValueError(f"view cap {vs.cap} too small for {need} positions")
+    weights = make_model_weights(m, seed)
+    views = [make_kv_view(m, vs, kv_len, seed, f"view{j}") for j, vs in enumerate(views_spec)]
+    last_tok = uniform_int(seed, "last_tok", (B,), 0, m.vocab)
+    h_prev = normal(seed, "h_prev", (B, m.d_t))
+    hist = uniform_int(seed, "hist", (B, hist_len), 0, m.vocab)
+    if hist_len:
+        hist[:, -1] = last_tok  # the newest history entry is the token being consumed
+    return DraftWorkload(name, m, views_spec, B, N, weights, views, kv_len, last_tok, h_prev, hist)
+
+
+# ----------------------------------------------------------------------------
+# the five named workloads
+# ----------------------------------------------------------------------------
+
+def _gemma_assistant(dtype: str = "bf16") -> ModelSpec:
+    return ModelSpec(d_t=5120, d_a=1024, n_blocks=4, n_q_heads=16, head_dim=256, n_kv_heads=4,
+                     d_ff=4096, vocab=262144, dtype=dtype, block_view=(0, 0, 0, 1))
+
+
+def _gemma_views(full_cap: int) -> list:
+    # view 0: the target's last sliding-window layer (bounded ring of 1536 cells, window 1024)
+    # view 1: the target's last full-attention layer
+    return [ViewSpec(cap=1536, window=1024, rope_theta=10000.0),
+            ViewSpec(cap=full_cap, window=0, rope_theta=1000000.0)]
+
+
+WORKLOADS = {
+    0: "tiny-fp32-b1-n3",
+    1: "gemma-assistant-bf16-b1-n3-ctx8192",
+    2: "gemma-assistant-bf16-b16-n4-ragged2k-32k",
+    3: "gemma-assistant-bf16-b64-n2-ctx4096",
+    4: "verify-sample-b32-n3-v248320",
+}
+
+
+def workload_seed(cfg_id: int) -> int:
+    return 1000 + int(cfg_id)
+
+
+def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None) -> DraftWorkload:
+    """Draft-block inputs of one of the named workloads (0-3).
+
+    ``B`` may shrink the batch (the first B sequences' lengths are kept) for
+    parity runs at full model size.
+    """
+    seed = workload_seed(cfg_id) if seed is None else seed
+    name = WORKLOADS[cfg_id]
+    if cfg_id == 0:
+        m = ModelSpec(d_t=256, d_a=128, n_blocks=1, n_q_heads=4, head_dim=32, n_kv_heads=1,
+                      d_ff=512, vocab=4096, dtype="f32", block_view=(0,))
+        views = [ViewSpec(cap=128, window=0, rope_theta=1000000.0)]
+        Bf, N, kv = 1, 3, np.array([128])
+    elif cfg_id == 1:
+        m, views = _gemma_assistant(), _gemma_views(8192)
+        Bf, N, kv = 1, 3, np.array([8192])
+    elif cfg_id == 2:
+        m, views = _gemma_assistant(), _gemma_views(32768)
+        Bf, N = 16, 4
+        kv = uniform_int(seed, "kv_len", (Bf,), 2048, 32769)
+    elif cfg_id == 3:
+        m, views = _gemma_assistant(), _gemma_views(4096)
+        Bf, N, kv = 64, 2, np.full(64, 4096)
+    else:
+        raise ValueError("workload 4 has no draft block")
+    B = Bf if B is None else B
+    kv = np.resize(np.asarray(kv, dtype=np.int32), B) if B != Bf else kv
+    if cfg_id == 2:
+        views = [views[0], ViewSpec(cap=int(kv.max()), window=0, rope_theta=1e6)]
+    return make_draft_workload(name, m, views, B, N, kv, seed, hist_len=64)
+
+
+# ----------------------------------------------------------------------------
+# verify inputs
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class VerifyGreedyInputs:
+    logits: np.ndarray   # [B, 1+N, V] float32 or uint16 (bf16 bits)
+    dtype: str
+    drafts: np.ndarray   # int32 [B, N]
+    planted: np.ndarray  # int32 [B]: the accept length the inputs were built for
+
+
+def plant_greedy_logits(logits32: np.ndarray, drafts: np.ndarray, planted: np.ndarray,
+                        dtype: str) -> np.ndarray:
+    """Make row i's largest value sit at drafts[i] for i < k, and not at drafts[k].
+
+    Works on the values as stored (after bf16 rounding), so the planted rows'
+    maxima are exact in the stored dtype.
+    """
+    B, R, V = logits32.shape
+    N = R - 1
+    store = _as_dtype(logits32, dtype)
+    vals = bf16_bits_to_f32(store) if dtype == "bf16" else store
+    for b in range(B):
+        k = int(planted[b])
+        for i in range(min(k, N)):
+            top = float(np.nanmax(vals[b, i]))
+            new = np.float32(top + 1.0)
+            if dtype == "bf16":
+                bits = f32_to_bf16_bits(np.array([new], dtype=np.float32))[0]
+                store[b, i, drafts[b, i]] = bits
+            else:
+                store[b, i, drafts[b, i]] = new
+        if k < N:
+            row = vals[b, k]
+            d = drafts[b, k]
+            low = np.float32(float(np.nanmin(row)) - 1.0)
+            if dtype == "bf16":
+                store[b, k, d] = f32_to_bf16_bits(np.array([low], dtype=np.float32))[0]
+            else:
+                store[b, k, d] = low
+    return store
+
+
+def make_verify_greedy_inputs(cfg_id: int, seed: int | None = None, B: int | None = None,
+                              N: int | None = None, V: int | None = None,
+                              dtype: str | None = None) -> VerifyGreedyInputs:
+    seed = workload_seed(cfg_id) if seed is None else seed
+    defaults = {0: (1, 3, 4096, "f32"), 1: (1, 3, 262144, "bf16"), 2: (16, 4, 262144, "bf16"),
+                3: (64, 2, 262144, "bf16")}
+    Bd, Nd, Vd, dd = defaults[cfg_id]
+    B = Bd if B is None else B
+    N = Nd if N is None else N
+    V = Vd if V is None else V
+    dtype = dd if dtype is None else dtype
+    logits = normal(seed, "verify.logits", (B, N + 1, V))
+    drafts = uniform_int(seed, "verify.drafts", (B, N), 0, V)
+    planted = uniform_int(seed, "verify.planted", (B,), 0, N + 1)
+    store = plant_greedy_logits(logits, drafts, planted, dtype)
+    return VerifyGreedyInputs(store, dtype, drafts, planted)
+
+
+@dataclasses.dataclass
+class SampleParams:
+    temp: float = 0.6
+    top_p: float = 0.95
+    min_p: float = 0.05
+    rep_penalty: float = 1.08
+    presence_penalty: float = 0.0
+    top_k: int = 0
+
+
+@dataclasses.dataclass
+class VerifySampleInputs:
+    target: np.ndarray   # [B, 1+N, V] (bf16 bits or fp32)
+    draft: np.ndarray    # [B, N, V]
+    dtype: str
+    drafts: np.ndarray   # int32 [B, N]
+    hist: np.ndarray     # int32 [B, H]; newest token last
+    params: SampleParams
+    seed: int
+    offset: int
+
+
+def make_verify_sample_inputs(seed: int | None = None, B: int = 32, N: int = 3, V: int = 248320,
+                              H: int = 64, rho: float = 0.8, std: float = 2.0,
+                              dtype: str = "bf16", params: SampleParams | None = None
+                              ) -> VerifySampleInputs:
+    """Target logits ~N(0, std^2); draft logits rho-correlated with the target rows.
+
+    The drafted token of row i is the draft row's largest logit (a deterministic
+    drafter, the case the temp > 0 audit page treats).
+    """
+    seed = workload_seed(4) if seed is None else seed
+    tgt = normal(seed, "vs.target", (B, N + 1, V), std=std)
+    eps = normal(seed, "vs.eps", (B, N, V), std=std)
+    dft = (np.float32(rho) * tgt[:, :N, :] + np.float32(math.sqrt(1 - rho * rho)) * eps)
+    tgt_s, dft_s = _as_dtype(tgt, dtype), _as_dtype(dft, dtype)
+    dvals = bf16_bits_to_f32(dft_s) if dtype == "bf16" else dft_s
+    drafts = np.argmax(dvals, axis=2).astype(np.int32)
+    hist = uniform_int(seed, "vs.hist", (B, H), 0, V)
+    return VerifySampleInputs(tgt_s, dft_s, dtype, drafts, hist,
+                              params or SampleParams(), seed=seed, offset=0)
