@@ -1,0 +1,381 @@
+#!/usr/bin/env python3
+"""Benchmark of the MTP draft block + verify-accept hot path.
+
+One step = one mtp_draft_block call (N chained draft steps, one persistent
+launch) + one mtp_verify_greedy call on the target's (1+N) x V verify logits,
+for the Gemma-assistant-shaped workload (bf16, d_t 5120, d_a 1024, 4 blocks,
+16 x 256 query heads over 4 KV heads, GeGLU 4096, vocab 262144, B = 1, N = 3,
+8192 cached positions; 3 blocks attend a 1024-window sliding layer, 1 a full
+layer).  Metric: drafted tokens per second = B * N / (draft + verify time).
+
+Prints ONE JSON line.  `--impl reference` times the CPU oracle instead on the
+same workload (a bounded sample per step).  Multi-GPU (torchrun): every rank
+runs an independent replica (the path has no cross-sequence exchange); the
+value is the sum of drafted tokens over the max time across ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "drafted tok/s (MTP draft block + verify) at B=1..64; % of HBM/tensor roofline"
+UNIT = "tok/s"
+WORKLOAD_ID = 1
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[0, 1, 2, 3])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes (the byte floor: every tensor the step must read, once)
+# ----------------------------------------------------------------------------
+
+def kv_bytes_per_step(w) -> int:
+    """Distinct KV bytes one draft step reads: each view's readable positions,
+    K and V, every KV head; a view read by several blocks counts once."""
+    m = w.model
+    esz = 2 if m.dtype == "bf16" else 4
+    used = sorted(set(m.block_view))
+    tot = 0
+    for vi in used:
+        vd = w.views[vi]
+        for b in range(w.B):
+            L = int(w.kv_len[b])
+            n = min(L, vd["window"]) if vd["window"] > 0 else L
+            tot += 2 * n * m.n_kv_heads * m.head_dim * esz
+    return tot
+
+
+def draft_bytes_per_launch(w) -> int:
+    m = w.model
+    esz = 2 if m.dtype == "bf16" else 4
+    per_step = w.weight_bytes() + kv_bytes_per_step(w) + w.B * m.d_t * esz
+    return w.N * per_step
+
+
+def draft_flops_per_launch(w) -> float:
+    m = w.model
+    attn = 0
+    for l in range(m.n_blocks):
+        vd = w.views[m.block_view[l]]
+        for b in range(w.B):
+            L = int(w.kv_len[b])
+            n = min(L, vd["window"]) if vd["window"] > 0 else L
+            attn += 4 * m.n_q_heads * m.head_dim * n
+    return float(w.N * (2 * m.params() * w.B + attn))
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.th:
+            self.th.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# our implementation
+# ----------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    import mtp_speculative_decoding_gb300 as mtp
+    from mtp_speculative_decoding_gb300 import build as mtp_build
+    from mtp_speculative_decoding_gb300.device import to_device, upload_draft
+    mtp_build.build()
+
+    w = synth.make_draft_inputs(args.workload)
+    m = w.model
+    B, N, V = w.B, w.N, m.vocab
+    dev = upload_draft(w, extra_ws_for=(B, N, V))
+    ws = dev.ws
+    drafts = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    h_last = torch.empty((B, m.d_t), dtype=torch.float32, device="cuda")
+    # one untimed draft to plant the verify logits' accept lengths against the real drafts
+    dev.run(drafts, h_last)
+    torch.cuda.synchronize()
+    if mtp.last_error(ws) != 0:
+        raise RuntimeError(f"draft block status {mtp.last_error(ws)}")
+    d_host = drafts.cpu().numpy()
+    vin = synth.make_verify_greedy_inputs(args.workload, B=B, N=N, V=V)
+    logits_np = synth.plant_greedy_logits(
+        synth.bf16_bits_to_f32(vin.logits) if vin.dtype == "bf16" else vin.logits, d_host, vin.planted, vin.dtype)
+    logits = to_device(logits_np, vin.dtype)
+    out_tok = torch.empty((B, N + 1), dtype=torch.int32, device="cuda")
+    n_acc = torch.empty((B,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dev.run(drafts, h_last)
+        mtp.verify_greedy(logits, drafts, out_tok, n_acc, ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert mtp.last_error(ws) == 0
+    got_n = n_acc.cpu().numpy()
+    if not np.array_equal(got_n, vin.planted):
+        raise RuntimeError(f"verify accepted {got_n}, planted {vin.planted}")
+
+    # per-kernel events on the launch stream: draft launch and verify launch separately
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        a, b_, c = ev[i]
+        a.record(stream)
+        dev.run(drafts, h_last)
+        b_.record(stream)
+        mtp.verify_greedy(logits, drafts, out_tok, n_acc, ws)
+        c.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    draft_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    verify_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+        dist.barrier()
+    ms_per_step = total_ms / args.steps
+    value = world * B * N * args.steps / (total_ms / 1e3)
+
+    # end-to-end through the public API with host buffers (pinned), copies inside the timed region
+    h_tok = torch.from_numpy(w.last_tok.copy()).pin_memory()
+    h_h = torch.from_numpy(w.h_prev.copy()).pin_memory()
+    h_kv = torch.from_numpy(w.kv_len.copy()).pin_memory()
+    h_logits = torch.empty(logits.shape, dtype=logits.dtype).pin_memory()
+    h_logits.copy_(logits.cpu())
+    h_out = torch.empty((B, N + 1), dtype=torch.int32).pin_memory()
+    h_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h_dr = torch.empty((B, N), dtype=torch.int32).pin_memory()
+    bi = h_tok.numel() * 4 + h_h.numel() * 4 + h_kv.numel() * 4 + h_logits.numel() * h_logits.element_size()
+    bo = h_out.numel() * 4 + h_n.numel() * 4 + h_dr.numel() * 4
+
+    def e2e_step():
+        dev.last_tok.copy_(h_tok, non_blocking=True)
+        dev.h_prev.copy_(h_h, non_blocking=True)
+        dev.kv_len.copy_(h_kv, non_blocking=True)
+        logits.copy_(h_logits, non_blocking=True)
+        dev.run(drafts, h_last)
+        mtp.verify_greedy(logits, drafts, out_tok, n_acc, ws)
+        h_dr.copy_(drafts, non_blocking=True)
+        h_out.copy_(out_tok, non_blocking=True)
+        h_n.copy_(n_acc, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * B * N * args.steps / (e2e_ms / 1e3)
+    if not np.array_equal(h_n.numpy(), vin.planted):
+        raise RuntimeError("end-to-end verify disagrees with the planted accept lengths")
+
+    peak, peak_kind = measured_peaks()
+    alg = draft_bytes_per_launch(w)
+    draft_avg_s = statistics.mean(draft_ms) / 1e3
+    achieved = alg / draft_avg_s / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if m.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; random-init weights of the workload's shapes)",
+        "config": {"workload": w.name, "B": B, "N": N, "vocab": V, "d_t": m.d_t, "d_a": m.d_a,
+                   "n_blocks": m.n_blocks, "kv_len": int(w.kv_len.max()),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (weights streamed every step), no flush",
+                   "draft_ms_mean": round(statistics.mean(draft_ms), 4),
+                   "verify_ms_mean": round(statistics.mean(verify_ms), 4)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+                "d2h_bytes_per_step": int(bo)},
+        "roofline": {"bound": "hbm", "kernel": "draft_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": alg,
+                     "traffic": None},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def cpu_baseline(w, min_seconds: float = 10.0) -> dict:
+    """The oracle as it stands, timed on this host's cores over a bounded sample:
+    whole draft blocks (N steps, B sequences) + greedy verify, repeated until
+    `min_seconds` of CPU work."""
+    import oracle
+    vin = synth.make_verify_greedy_inputs(WORKLOAD_ID if w.name == synth.WORKLOADS[1] else 0,
+                                          B=w.B, N=w.N, V=w.model.vocab)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.draft_block(w, want_logits=False)
+        oracle.verify_greedy(vin.logits, vin.dtype, vin.drafts)
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(reps * w.B * w.N / dt, 4), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} full draft blocks (B={w.B}, N={w.N}) + greedy verify, {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = synth.make_draft_inputs(args.workload)
+    vin = synth.make_verify_greedy_inputs(args.workload, B=w.B, N=w.N, V=w.model.vocab)
+    for _ in range(args.warmup):
+        oracle.draft_block(w, want_logits=False)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.draft_block(w, want_logits=False)
+        oracle.verify_greedy(vin.logits, vin.dtype, vin.drafts)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = w.B * w.N * args.steps / tot
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": w.name, "B": w.B, "N": w.N},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": f"{args.steps} full draft blocks + greedy verify"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+/*
+ * mtp.h -- C ABI of the GB300 MTP speculative-decoding hot path.
+ *
+ * Three operations, all asynchronous on a caller-supplied CUDA stream:
+ *
+ *   mtp_draft_block    N chained draft steps of an MTP assistant head that
+ *                      cross-attends into the target's KV cache, in ONE
+ *                      persistent launch (token -> embedding -> hidden-state
+ *                      chain stays on the device between steps).
+ *   mtp_verify_greedy  longest greedy-matching prefix + bonus token from the
+ *                      target's (1+N) x V verify logits.
+ *   mtp_verify_sample  exact speculative sampling at temp > 0.
+ *
+ * Definitions are those of the pages this library implements:
+ *   [G4] "Gemma 4 MTP -- Multi-Token Prediction speculative decoding":
+ *        sec. 4 "Per-step MTP graph" (the draft step), sec. 5 "KV sharing"
+ *        (read-only cross-attention, one mask for all steps), sec. 6 (the
+ *        public API this one replaces: llama_decode_mtp_async / _wait).
+ *   [NX] "MTP decoding (--mtp)": "Requirements" (enorm / hnorm / eh_proj) and
+ *        "How it is wired" (greedy longest-prefix accept + bonus token).
+ *   [FN] "Fused NextN draft graph": one launch + one readback for N steps;
+ *        delta 6 (frozen-prefix cross-attention).
+ *   [SP] "opus-mtp-turbo: Track 1 report", item 4 (exact temp > 0
+ *        verification: sample_dist, accept with p/q, residual max(p - q, 0)).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is DEVICE memory owned by the caller, unless its
+ *   comment says "host".  The library never allocates, frees or copies
+ *   buffers of its own, never synchronizes the stream (except
+ *   mtp_last_error, which says so) and keeps no state between calls.
+ * - Scratch space is the caller's workspace `ws` (`ws_bytes` bytes, 256-byte
+ *   aligned, device memory), sized by mtp_workspace_size().  Calls that share
+ *   a workspace must be ordered on one stream.
+ * - Return value: MTP_OK, or a negative MTP_ERR_* code when the arguments are
+ *   rejected on the host (nothing is launched then) or a launch fails.
+ *   Errors found while the kernels run (a grid barrier that timed out, a
+ *   candidate set that overflowed) are written to a status word inside the
+ *   workspace and read back with mtp_last_error().
+ * - Row-major layouts; every row start must be 16-byte aligned (row lengths
+ *   in elements: multiples of 8 for bf16, 4 for fp32).
+ */
+#ifndef MTP_H
+#define MTP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* a cudaStream_t; NULL is the legacy default stream */
+typedef struct CUstream_st *mtp_stream_t;
+
+enum {
+    MTP_OK = 0,
+    MTP_ERR_ARG = -1,          /* a pointer, size or layout argument is invalid */
+    MTP_ERR_UNSUPPORTED = -2,  /* valid, but outside what the kernels implement */
+    MTP_ERR_WORKSPACE = -3,    /* ws is NULL, misaligned or smaller than required */
+    MTP_ERR_CUDA = -4,         /* a CUDA launch failed */
+    MTP_ERR_TIMEOUT = -5,      /* (device status) a grid barrier gave up waiting */
+    MTP_ERR_CAPACITY = -6      /* (device status) a sampling candidate set overflowed */
+};
+
+enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 };
+
+#define MTP_MAX_BLOCKS 8
+#define MTP_MAX_VIEWS 4
+#define MTP_MAX_BATCH 64
+
+/* Sizes and scalars of the assistant head ([G4] sec. 3-4).
+ *   d_t        backbone (target) width: token embedding, h_prev, LM head input
+ *   d_a        assistant width
+ *   n_blocks   assistant blocks (<= MTP_MAX_BLOCKS)
+ *   n_q_heads, head_dim, n_kv_heads   query heads, their width, KV heads of the
+ *              target layers cross-attended (n_q_heads % n_kv_heads == 0)
+ *   d_ff       GeGLU hidden width
+ *   vocab      rows of the tied token-embedding table
+ *   wdtype     MTP_DTYPE_BF16 or MTP_DTYPE_F32: weight matrices and KV
+ *   rms_eps    RMSNorm epsilon; attn_scale softmax scale (usually 1/sqrt(head_dim));
+ *   emb_scale  token-embedding scale (sqrt(d_t) for Gemma);
+ *   logit_softcap  > 0 applies cap * tanh(z / cap) to the logits, 0 = off */
+typedef struct mtp_config {
+    int32_t d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab;
+    int32_t wdtype;
+    float rms_eps, attn_scale, emb_scale, logit_softcap;
+} mtp_config;
+
+/* One assistant block.  Matrices are row-major [out, in] in `wdtype`; RMSNorm
+ * gains are fp32.  kv_view selects which mtp_kv_view the block attends. */
+typedef struct mtp_block_weights {
+    const void *attn_norm;       /* fp32 [d_a] */
+    const void *w_q;             /* [n_q_heads * head_dim, d_a] */
+    const void *q_norm;          /* fp32 [head_dim], shared by all heads */
+    const void *w_o;             /* [d_a, n_q_heads * head_dim] */
+    const void *post_attn_norm;  /* fp32 [d_a] */
+    const void *pre_ffn_norm;    /* fp32 [d_a] */
+    const void *w_gate;          /* [d_ff, d_a] */
+    const void *w_up;            /* [d_ff, d_a] */
+    const void *w_down;          /* [d_a, d_ff] */
+    const void *post_ffn_norm;   /* fp32 [d_a] */
+    int32_t kv_view;
+    int32_t pad_;
+} mtp_block_weights;
+
+typedef struct mtp_weights {
+    const void *tok_embd;    /* [vocab, d_t]: the TARGET's table, also the tied LM head */
+    const void *norm_e;      /* fp32 [d_t]: norm of the scaled token embedding */
+    const void *norm_h;      /* fp32 [d_t]: norm of h_prev */
+    const void *w_pre;       /* [d_a, 2 d_t]: pre-projection of [norm_e(e); norm_h(h)] */
+    const void *final_norm;  /* fp32 [d_a] */
+    const void *w_post;      /* [d_t, d_a]: post-projection -> next h_prev */
+    mtp_block_weights blk[MTP_MAX_BLOCKS];
+} mtp_weights;
+
+/* A read-only view of one target KV layer ([G4] sec. 5).  K and V share the
+ * layout: element (b, kv head g, slot s, d) at b*stride_b + g*stride_h +
+ * s*stride_t + d (elements of `wdtype`; d contiguous).  The view is a ring of
+ * `cap` slots: position t lives in slot t % cap.  window == 0 reads positions
+ * [0, kv_len[b]) (requires kv_len[b] <= cap); window W > 0 reads the last W
+ * positions [max(0, kv_len[b] - W), kv_len[b]) (requires W <= cap).  K is
+ * stored after RoPE; V is used as stored.  rope_theta is the RoPE base of the
+ * target layer type (applied to the drafter's queries). */
+typedef struct mtp_kv_view {
+    const void *k, *v;
+    int64_t stride_b, stride_h, stride_t;
+    int32_t cap, window;
+    float rope_theta;
+    int32_t pad_;
+} mtp_kv_view;
+
+/* sample_dist settings ([SP] item 4): repetition penalty (z > 0: z / r, else
+ * z * r) and presence penalty (z - pres), once per distinct token of the
+ * penalty set, then temperature, min-p (keep p >= min_p * p_max), top-p (keep
+ * the shortest prefix, by probability desc / id asc, whose mass reaches
+ * top_p), renormalising after each cut.  top_k must be 0 (off). */
+typedef struct mtp_sample_params {
+    float temp, top_p, min_p, rep_penalty, presence_penalty;
+    int32_t top_k;
+} mtp_sample_params;
+
+/* Workspace bytes needed by any of the three operations for these sizes.
+ * cfg may be NULL when only the verify calls will use the workspace.  Returns
+ * 0 for invalid sizes. */
+size_t mtp_workspace_size(const mtp_config *cfg, int B, int N, int V);
+
+/* N chained draft steps for B sequences ([G4] sec. 4-5, [NX], [FN]).
+ * Step k of sequence b consumes token tok_k (last_tok[b] for k = 0, the draft
+ * of step k-1 after) and hidden state h_k (h_prev[b] for k = 0, the previous
+ * step's post-projection after):
+ *   e = tok_embd[tok_k] * emb_scale
+ *   x = w_pre [rmsnorm(e; norm_e); rmsnorm(h_k; norm_h)]
+ *   per block: q = rope(qnorm(w_q rmsnorm(x)), pos = kv_len[b] + k);
+ *              o = GQA softmax cross-attention of q into the block's view;
+ *              x += rmsnorm(w_o o); x += rmsnorm(w_down(gelu_tanh(w_gate n) * w_up n)),
+ *              n = rmsnorm(x; pre_ffn_norm)
+ *   h_{k+1} = w_post rmsnorm(x; final_norm);  z = tok_embd h_{k+1} (softcap)
+ *   draft_k = argmax z (lowest index on ties), or, when sp != NULL and
+ *   sp->temp > 0, a draw from sample_dist(z) with penalty set hist[b] u
+ *   {draft_0..draft_{k-1}} and the Philox-4x32-10 uniform of counter
+ *   (b, 4k + 0, offset lo, offset hi), key (seed lo, seed hi).
+ * Arguments:
+ *   views[n_views]       KV views (host array of structs; data on device)
+ *   kv_len [B] int32     attn_pos + 1 of each sequence, >= 1
+ *   last_tok [B] int32   the last accepted token
+ *   h_prev [B, d_t] fp32 the target's hidden state at that token
+ *   sp                   host pointer or NULL (greedy)
+ *   hist [B, H] int32    penalty history (newest last; entries < 0 ignored);
+ *                        used only when sampling; may be NULL when H == 0
+ *   out_drafts [B, N] int32
+ *   out_h_last [B, d_t] fp32, or NULL: h after the last step
+ *   out_logits [B, N, vocab] fp32, or NULL: every step's logits (diagnostic)
+ * B <= MTP_MAX_BATCH, 1 <= N <= 16.  One cooperative launch (plus a 256-byte
+ * workspace memset); no host round-trip between steps. */
+int mtp_draft_block(const mtp_config *cfg, const mtp_weights *w,
+                    const mtp_kv_view *views, int n_views,
+                    const int32_t *kv_len, int B, int N,
+                    const int32_t *last_tok, const float *h_prev,
+                    const mtp_sample_params *sp, uint64_t seed, uint64_t offset,
+                    const int32_t *hist, int H,
+                    int32_t *out_drafts, float *out_h_last, float *out_logits,
+                    void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+/* Greedy verify ([NX] How it is wired).  logits [B, 1+N, V] in ldtype (row i
+ * is the target's distribution after consuming the last token and drafts
+ * 0..i-1); t_i = argmax of row i (lowest index on ties, NaN never wins, an
+ * all-NaN row gives 0).  n_accept[b] = the largest k <= N with
+ * drafts[b, j] == t_j for all j < k; out_tokens[b] = drafts[b, 0..k-1], t_k,
+ * then -1 up to 1+N entries.  drafts [B, N] int32, out_tokens [B, 1+N] int32,
+ * out_n_accept [B] int32.  0 <= N, B >= 1, V >= 1. */
+int mtp_verify_greedy(const void *logits, int ldtype, int B, int N, int V,
+                      const int32_t *drafts, int32_t *out_tokens, int32_t *out_n_accept,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+/* Exact speculative sampling ([SP] item 4).  For row i < N of sequence b:
+ * p_i = sample_dist(target row i), q_i = sample_dist(draft row i), both with
+ * penalty set hist[b] u {drafts[b, 0..i-1]}; x = drafts[b, i] is accepted iff
+ * u < p_i(x) / q_i(x) (u of counter (b, 4i + 1, ...)).  At the first
+ * rejection the emitted token is drawn from norm(max(p_i - q_i, 0)) (from p_i
+ * if that is empty) with u of (b, 4i + 2, ...) and the window ends; when all
+ * N drafts are accepted the bonus token is drawn from p_N with u of
+ * (b, 4N + 3, ...).  Draws walk the candidates in (probability desc, id asc)
+ * order.  Uniforms: Philox-4x32-10, counter (b, 4i + purpose, offset lo,
+ * offset hi), key (seed lo, seed hi), u = (word0 >> 8) * 2^-24.
+ *   tgt_logits [B, 1+N, V], dft_logits [B, N, V] in ldtype; drafts [B, N];
+ *   hist [B, H] int32 (newest last, entries < 0 ignored; NULL when H == 0);
+ *   sp host pointer (temp > 0, top_k == 0); out_tokens [B, 1+N] (-1 padded);
+ *   out_n_accept [B].  A row whose min-p set exceeds 4096 candidates sets
+ *   MTP_ERR_CAPACITY in the status word. */
+int mtp_verify_sample(const void *tgt_logits, const void *dft_logits, int ldtype,
+                      int B, int N, int V, const int32_t *drafts,
+                      const int32_t *hist, int H, const mtp_sample_params *sp,
+                      uint64_t seed, uint64_t offset,
+                      int32_t *out_tokens, int32_t *out_n_accept,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+/* Device status of the most recent call that used `ws`: MTP_OK,
+ * MTP_ERR_TIMEOUT or MTP_ERR_CAPACITY.  SYNCHRONIZES `stream` (a 4-byte
+ * device-to-host copy).  Returns MTP_ERR_CUDA if the copy fails. */
+int mtp_last_error(const void *ws, mtp_stream_t stream);
+
+/* Static description of an error code. */
+const char *mtp_strerror(int code);
+
+/* Fault-detection check: launches the grid barrier of the draft kernel with
+ * an arrival count that can never be reached and a wait limit of
+ * `timeout_us` microseconds (1..1000000).  Every block gives up, the status
+ * word becomes MTP_ERR_TIMEOUT and the kernel returns; the context stays
+ * usable.  For tests of the timeout path; computes nothing. */
+int mtp_debug_barrier_timeout(void *ws, size_t ws_bytes, int timeout_us, mtp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTP_H */

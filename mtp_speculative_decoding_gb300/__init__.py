@@ -1,0 +1,250 @@
+"""Thin Python binding of libmtp.so (the C ABI declared in include/mtp.h).
+
+Argument marshalling only: every step of the draft block and the verifiers
+runs in the library's CUDA kernels.  PyTorch supplies device memory and the
+current stream.  There is no fallback: if the compiled library is missing or
+no CUDA device is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import platform
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", platform.machine(), "libmtp.so")
+
+MTP_OK = 0
+MTP_ERR_ARG = -1
+MTP_ERR_UNSUPPORTED = -2
+MTP_ERR_WORKSPACE = -3
+MTP_ERR_CUDA = -4
+MTP_ERR_TIMEOUT = -5
+MTP_ERR_CAPACITY = -6
+MTP_DTYPE_F32 = 0
+MTP_DTYPE_BF16 = 1
+MTP_MAX_BLOCKS = 8
+MTP_MAX_VIEWS = 4
+MTP_MAX_BATCH = 64
+
+# every entry point include/mtp.h declares
+EXPORTS = ("mtp_workspace_size", "mtp_draft_block", "mtp_verify_greedy", "mtp_verify_sample",
+           "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout")
+
+
+class MTPError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+
+
+class Config(C.Structure):
+    _fields_ = [("d_t", C.c_int32), ("d_a", C.c_int32), ("n_blocks", C.c_int32), ("n_q_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("n_kv_heads", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
+                ("wdtype", C.c_int32), ("rms_eps", C.c_float), ("attn_scale", C.c_float),
+                ("emb_scale", C.c_float), ("logit_softcap", C.c_float)]
+
+
+class BlockWeights(C.Structure):
+    _fields_ = [("attn_norm", C.c_void_p), ("w_q", C.c_void_p), ("q_norm", C.c_void_p), ("w_o", C.c_void_p),
+                ("post_attn_norm", C.c_void_p), ("pre_ffn_norm", C.c_void_p), ("w_gate", C.c_void_p),
+                ("w_up", C.c_void_p), ("w_down", C.c_void_p), ("post_ffn_norm", C.c_void_p),
+                ("kv_view", C.c_int32), ("pad_", C.c_int32)]
+
+
+class Weights(C.Structure):
+    _fields_ = [("tok_embd", C.c_void_p), ("norm_e", C.c_void_p), ("norm_h", C.c_void_p), ("w_pre", C.c_void_p),
+                ("final_norm", C.c_void_p), ("w_post", C.c_void_p), ("blk", BlockWeights * MTP_MAX_BLOCKS)]
+
+
+class KVView(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("stride_b", C.c_int64), ("stride_h", C.c_int64),
+                ("stride_t", C.c_int64), ("cap", C.c_int32), ("window", C.c_int32), ("rope_theta", C.c_float),
+                ("pad_", C.c_int32)]
+
+
+class SampleParams(C.Structure):
+    _fields_ = [("temp", C.c_float), ("top_p", C.c_float), ("min_p", C.c_float), ("rep_penalty", C.c_float),
+                ("presence_penalty", C.c_float), ("top_k", C.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                                   "or python -m mtp_speculative_decoding_gb300.build")
+            L = C.CDLL(LIB_PATH)
+            P, I, Z = C.c_void_p, C.c_int, C.c_size_t
+            L.mtp_workspace_size.argtypes = [P, I, I, I]
+            L.mtp_workspace_size.restype = Z
+            L.mtp_draft_block.argtypes = [P, P, P, I, P, I, I, P, P, P, C.c_uint64, C.c_uint64, P, I, P, P, P, P, Z, P]
+            L.mtp_draft_block.restype = I
+            L.mtp_verify_greedy.argtypes = [P, I, I, I, I, P, P, P, P, Z, P]
+            L.mtp_verify_greedy.restype = I
+            L.mtp_verify_sample.argtypes = [P, P, I, I, I, I, P, P, I, P, C.c_uint64, C.c_uint64, P, P, P, Z, P]
+            L.mtp_verify_sample.restype = I
+            L.mtp_last_error.argtypes = [P, P]
+            L.mtp_last_error.restype = I
+            L.mtp_strerror.argtypes = [I]
+            L.mtp_strerror.restype = C.c_char_p
+            L.mtp_debug_barrier_timeout.argtypes = [P, Z, I, P]
+            L.mtp_debug_barrier_timeout.restype = I
+            _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().mtp_strerror(int(code)).decode()
+    except Exception:  # library not loadable: still give a readable message
+        return f"error {code}"
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != MTP_OK:
+        raise MTPError(rc, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _require_cuda(*tensors):
+    for t in tensors:
+        if t is not None and not t.is_cuda:
+            raise ValueError("every tensor argument must live on the CUDA device")
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return MTP_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return MTP_DTYPE_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+# ----------------------------------------------------------------------------
+# configuration
+# ----------------------------------------------------------------------------
+
+def make_config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab, wdtype="bf16",
+                rms_eps=1e-6, attn_scale=None, emb_scale=None, logit_softcap=0.0) -> Config:
+    import math
+    return Config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab,
+                  MTP_DTYPE_BF16 if wdtype == "bf16" else MTP_DTYPE_F32, rms_eps,
+                  1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale,
+                  math.sqrt(d_t) if emb_scale is None else emb_scale, logit_softcap)
+
+
+def workspace_size(cfg: Config | None, B: int, N: int, V: int) -> int:
+    n = lib().mtp_workspace_size(C.byref(cfg) if cfg is not None else None, B, N, V)
+    if n == 0:
+        raise MTPError(MTP_ERR_ARG, "mtp_workspace_size")
+    return int(n)
+
+
+def alloc_workspace(nbytes: int, device="cuda"):
+    """A device buffer usable as workspace (PyTorch allocations are 256-byte aligned)."""
+    import torch
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------------------
+# draft block
+# ----------------------------------------------------------------------------
+
+GLOBAL_TENSORS = ("tok_embd", "norm_e", "norm_h", "w_pre", "final_norm", "w_post")
+BLOCK_TENSORS = ("attn_norm", "w_q", "q_norm", "w_o", "post_attn_norm", "pre_ffn_norm",
+                 "w_gate", "w_up", "w_down", "post_ffn_norm")
+
+
+def make_weights(tensors: dict, n_blocks: int, block_view) -> Weights:
+    """Pack device tensors (keys: GLOBAL_TENSORS and 'blk{i}.<name>') into mtp_weights."""
+    w = Weights()
+    for n in GLOBAL_TENSORS:
+        setattr(w, n, tensors[n].data_ptr())
+    for i in range(n_blocks):
+        b = w.blk[i]
+        for n in BLOCK_TENSORS:
+            setattr(b, n, tensors[f"blk{i}.{n}"].data_ptr())
+        b.kv_view = int(block_view[i])
+    return w
+
+
+def make_view(k, v, cap: int, window: int, rope_theta: float) -> KVView:
+    """k, v: [B, n_kv_heads, cap, head_dim] device tensors (head_dim contiguous)."""
+    assert k.shape == v.shape and k.stride() == v.stride() and k.stride(-1) == 1
+    sb, sh, st, _ = k.stride()
+    return KVView(k.data_ptr(), v.data_ptr(), sb, sh, st, cap, window, rope_theta, 0)
+
+
+def draft_block(cfg: Config, weights: Weights, views, kv_len, last_tok, h_prev, out_drafts, ws,
+                out_h_last=None, out_logits=None, sample=None, seed: int = 0, offset: int = 0, hist=None,
+                stream=None) -> None:
+    """Launch mtp_draft_block on the current stream (asynchronous)."""
+    _require_cuda(kv_len, last_tok, h_prev, out_drafts, ws, out_h_last, out_logits, hist)
+    B, N = out_drafts.shape
+    arr = (KVView * len(views))(*views)
+    sp = SampleParams(*sample) if sample is not None else None
+    H = 0 if hist is None else int(hist.shape[1])
+    rc = lib().mtp_draft_block(C.byref(cfg), C.byref(weights), arr, len(views), _ptr(kv_len), B, N,
+                               _ptr(last_tok), _ptr(h_prev), C.byref(sp) if sp is not None else None,
+                               seed, offset, _ptr(hist), H, _ptr(out_drafts), _ptr(out_h_last),
+                               _ptr(out_logits), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "mtp_draft_block")
+
+
+# ----------------------------------------------------------------------------
+# verify
+# ----------------------------------------------------------------------------
+
+def verify_greedy(logits, drafts, out_tokens, out_n_accept, ws, stream=None) -> None:
+    """logits [B, 1+N, V] (bf16 or fp32), drafts [B, N] int32 -> out_tokens [B, 1+N], out_n_accept [B]."""
+    _require_cuda(logits, drafts, out_tokens, out_n_accept, ws)
+    B, R, V = logits.shape
+    rc = lib().mtp_verify_greedy(_ptr(logits), _dtype_code(logits), B, R - 1, V, _ptr(drafts),
+                                 _ptr(out_tokens), _ptr(out_n_accept), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "mtp_verify_greedy")
+
+
+def verify_sample(tgt_logits, dft_logits, drafts, hist, params, seed: int, offset: int, out_tokens,
+                  out_n_accept, ws, stream=None) -> None:
+    """params: (temp, top_p, min_p, rep_penalty, presence_penalty, top_k) or an object with those fields."""
+    _require_cuda(tgt_logits, dft_logits, drafts, hist, out_tokens, out_n_accept, ws)
+    B, R, V = tgt_logits.shape
+    if hasattr(params, "temp"):
+        params = (params.temp, params.top_p, params.min_p, params.rep_penalty,
+                  getattr(params, "presence_penalty", 0.0), getattr(params, "top_k", 0))
+    sp = SampleParams(*params)
+    H = 0 if hist is None else int(hist.shape[1])
+    rc = lib().mtp_verify_sample(_ptr(tgt_logits), _ptr(dft_logits), _dtype_code(tgt_logits), B, R - 1, V,
+                                 _ptr(drafts), _ptr(hist), H, C.byref(sp), seed, offset, _ptr(out_tokens),
+                                 _ptr(out_n_accept), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "mtp_verify_sample")
+
+
+def last_error(ws, stream=None) -> int:
+    """Device status word of the last call on `ws` (synchronizes the stream)."""
+    return int(lib().mtp_last_error(_ptr(ws), _stream(stream)))
+
+
+def debug_barrier_timeout(ws, timeout_us: int, stream=None) -> None:
+    _check(lib().mtp_debug_barrier_timeout(_ptr(ws), ws.numel(), int(timeout_us), _stream(stream)),
+           "mtp_debug_barrier_timeout")

@@ -1,0 +1,365 @@
+// api.cu -- the C ABI declared in include/mtp.h: argument checks, workspace
+// layout and launches.  No allocation, no synchronization (except
+// mtp_last_error), no state kept between calls beyond a per-device cache of
+// the SM count.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "draft.cuh"
+#include "mtp.h"
+#include "verify.cuh"
+
+using namespace mtp;
+
+namespace {
+
+constexpr unsigned long long kBarrierLimitNs = 1000000000ull;  // 1 s per barrier wait
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static int cache[64] = {0};
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+struct DraftLayout {
+    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ACT, end;
+    int kmax;
+};
+
+int draft_kmax(const mtp_config* c) {
+    int k = 2 * c->d_t;
+    const int q = c->n_q_heads * c->head_dim;
+    if (c->d_a > k) k = c->d_a;
+    if (q > k) k = q;
+    if (c->d_ff > k) k = c->d_ff;
+    return k;
+}
+
+DraftLayout draft_layout(const mtp_config* c, int B, int N) {
+    DraftLayout L;
+    size_t off = sizeof(WsHeader);
+    const size_t f = sizeof(float);
+    const int grp = c->n_q_heads / c->n_kv_heads;
+    L.kmax = draft_kmax(c);
+    L.att_cnt = off; off = al256(off + (size_t)B * c->n_kv_heads * sizeof(unsigned int));
+    L.amax = off;    off = al256(off + (size_t)N * B * sizeof(unsigned long long));
+    L.XB = off;      off = al256(off + (size_t)B * c->d_a * f);
+    L.XM = off;      off = al256(off + (size_t)B * c->d_a * f);
+    L.QR = off;      off = al256(off + (size_t)B * c->n_q_heads * c->head_dim * f);
+    L.OB = off;      off = al256(off + (size_t)B * c->n_q_heads * c->head_dim * f);
+    L.YB = off;      off = al256(off + (size_t)B * c->d_a * f);
+    L.MB = off;      off = al256(off + (size_t)B * c->d_ff * f);
+    L.Y2 = off;      off = al256(off + (size_t)B * c->d_a * f);
+    L.HN = off;      off = al256(off + (size_t)B * c->d_t * f);
+    const size_t items = 2 * (size_t)kMaxGrid + (size_t)B * c->n_kv_heads;
+    L.PART = off;    off = al256(off + items * grp * (c->head_dim + 2) * f);
+    L.ACT = off;     off = al256(off + (size_t)B * L.kmax * f);
+    L.end = off;
+    return L;
+}
+
+struct GreedyLayout { size_t amax, end; };
+GreedyLayout greedy_layout(int B, int N) {
+    GreedyLayout L;
+    L.amax = sizeof(WsHeader);
+    L.end = al256(L.amax + (size_t)B * (N + 1) * sizeof(unsigned long long));
+    return L;
+}
+
+struct SampleLayout { size_t rowmax, cnt, zero_end, nkeep, wkeep, id, w, resid, end; };
+SampleLayout sample_layout(int B, int N) {
+    SampleLayout L;
+    const size_t rows = (size_t)B * (N + 1) + (size_t)B * N;
+    size_t off = sizeof(WsHeader);
+    L.rowmax = off; off += rows * sizeof(unsigned long long);
+    L.cnt = off;    off += rows * sizeof(unsigned int);
+    L.zero_end = off;
+    off = al256(off);
+    L.nkeep = off;  off = al256(off + rows * sizeof(int32_t));
+    L.wkeep = off;  off = al256(off + rows * sizeof(float));
+    L.id = off;     off = al256(off + rows * kCandCap * sizeof(int32_t));
+    L.w = off;      off = al256(off + rows * kCandCap * sizeof(float));
+    L.resid = off;  off = al256(off + (size_t)B * kCandCap * sizeof(float));
+    L.end = off;
+    return L;
+}
+
+size_t draft_smem(const mtp_config* c, int B, int act_smem) {
+    const size_t wb = c->wdtype == MTP_DTYPE_BF16 ? 2 : 4;
+    const size_t hd = c->head_dim, grp = c->n_q_heads / c->n_kv_heads;
+    const size_t attn = hd / 2 * sizeof(double) + (2 * grp * hd + grp * kAttnKeys + 48) * sizeof(float) +
+                        2 * (size_t)kAttnKeys * (hd * wb + kAttnPad);
+    const size_t kmax = draft_kmax(c);
+    const size_t act = (((size_t)c->d_a + 3) & ~(size_t)3) * sizeof(float) +
+                       (act_smem ? (size_t)B * kmax : kmax) * sizeof(float);
+    return attn > act ? attn : act;
+}
+
+constexpr size_t kSmemLimit = 220 * 1024;
+
+int check_config(const mtp_config* c) {
+    if (!c) return MTP_ERR_ARG;
+    if (c->d_t <= 0 || c->d_a <= 0 || c->n_blocks <= 0 || c->n_q_heads <= 0 || c->head_dim <= 0 ||
+        c->n_kv_heads <= 0 || c->d_ff <= 0 || c->vocab <= 0)
+        return MTP_ERR_ARG;
+    if (c->n_blocks > MTP_MAX_BLOCKS) return MTP_ERR_UNSUPPORTED;
+    if (c->n_q_heads % c->n_kv_heads != 0) return MTP_ERR_ARG;
+    if (c->n_q_heads / c->n_kv_heads > 16) return MTP_ERR_UNSUPPORTED;
+    if (c->wdtype != MTP_DTYPE_F32 && c->wdtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED;
+    const int hd = c->head_dim;
+    if (hd != 32 && hd != 64 && hd != 128 && hd != 256 && hd != 512) return MTP_ERR_UNSUPPORTED;
+    const int m = 8;  // row lengths in elements: 16-byte rows for either dtype
+    if (c->d_t % m || c->d_a % m || c->d_ff % m || (c->n_q_heads * hd) % m) return MTP_ERR_UNSUPPORTED;
+    if (!(c->rms_eps >= 0.f) || !(c->attn_scale > 0.f) || !(c->logit_softcap >= 0.f)) return MTP_ERR_ARG;
+    return MTP_OK;
+}
+
+int check_workspace(const void* ws, size_t ws_bytes, size_t need) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MTP_ERR_WORKSPACE;
+    if (ws_bytes < need) return MTP_ERR_WORKSPACE;
+    return MTP_OK;
+}
+
+int check_sample_params(const mtp_sample_params* sp) {
+    if (!sp) return MTP_ERR_ARG;
+    if (!(sp->temp > 0.f) || !(sp->top_p > 0.f) || !(sp->min_p >= 0.f) || sp->min_p > 1.f ||
+        !(sp->rep_penalty > 0.f) || sp->presence_penalty != sp->presence_penalty)
+        return MTP_ERR_ARG;
+    if (sp->top_k != 0) return MTP_ERR_UNSUPPORTED;
+    return MTP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mtp_workspace_size(const mtp_config* cfg, int B, int N, int V) {
+    if (B <= 0 || B > MTP_MAX_BATCH || N < 0 || N > 16 || V <= 0) return 0;
+    size_t need = al256(greedy_layout(B, N).end);
+    const size_t s = sample_layout(B, N > 0 ? N : 1).end;
+    if (s > need) need = s;
+    if (cfg) {
+        if (check_config(cfg) != MTP_OK || N < 1) return 0;
+        const size_t d = draft_layout(cfg, B, N).end;
+        if (d > need) need = d;
+    }
+    return need;
+}
+
+int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* views, int n_views,
+                    const int32_t* kv_len, int B, int N, const int32_t* last_tok, const float* h_prev,
+                    const mtp_sample_params* sp, uint64_t seed, uint64_t offset, const int32_t* hist, int H,
+                    int32_t* out_drafts, float* out_h_last, float* out_logits, void* ws, size_t ws_bytes,
+                    mtp_stream_t stream) {
+    int rc = check_config(cfg);
+    if (rc != MTP_OK) return rc;
+    if (!w || !views || n_views < 1 || n_views > MTP_MAX_VIEWS) return MTP_ERR_ARG;
+    if (B < 1 || B > MTP_MAX_BATCH || N < 1 || N > 16) return MTP_ERR_ARG;
+    if (!kv_len || !last_tok || !h_prev || !out_drafts) return MTP_ERR_ARG;
+    if (H < 0 || (H > 0 && !hist)) return MTP_ERR_ARG;
+    if (sp && sp->temp > 0.f) return MTP_ERR_UNSUPPORTED;  // sampled drafting: not built yet
+    const bool bf = cfg->wdtype == MTP_DTYPE_BF16;
+    const int esz = bf ? 2 : 4;
+    // weights
+    const void* mats[] = {w->tok_embd, w->w_pre, w->w_post};
+    for (const void* m : mats) if (!m || !aligned16(m)) return MTP_ERR_ARG;
+    if (!w->norm_e || !w->norm_h || !w->final_norm) return MTP_ERR_ARG;
+    for (int l = 0; l < cfg->n_blocks; ++l) {
+        const mtp_block_weights& b = w->blk[l];
+        const void* bm[] = {b.w_q, b.w_o, b.w_gate, b.w_up, b.w_down};
+        for (const void* m : bm) if (!m || !aligned16(m)) return MTP_ERR_ARG;
+        if (!b.attn_norm || !b.q_norm || !b.post_attn_norm || !b.pre_ffn_norm || !b.post_ffn_norm) return MTP_ERR_ARG;
+        if (b.kv_view < 0 || b.kv_view >= n_views) return MTP_ERR_ARG;
+    }
+    for (int v = 0; v < n_views; ++v) {
+        const mtp_kv_view& kv = views[v];
+        if (!kv.k || !kv.v || !aligned16(kv.k) || !aligned16(kv.v)) return MTP_ERR_ARG;
+        if (kv.cap < 1 || kv.window < 0 || kv.window > kv.cap || !(kv.rope_theta > 0.f)) return MTP_ERR_ARG;
+        if (kv.stride_t < cfg->head_dim || kv.stride_b < 0 || kv.stride_h < 0) return MTP_ERR_ARG;
+        if ((kv.stride_t * esz) % 16 || (kv.stride_h * esz) % 16 || (kv.stride_b * esz) % 16) return MTP_ERR_ARG;
+    }
+    const DraftLayout L = draft_layout(cfg, B, N);
+    rc = check_workspace(ws, ws_bytes, L.end);
+    if (rc != MTP_OK) return rc;
+    const int sms = num_sms();
+    if (sms <= 0) return MTP_ERR_CUDA;
+
+    size_t smem = draft_smem(cfg, B, 1);
+    int act_smem = 1;
+    if (smem > kSmemLimit) {
+        act_smem = 0;
+        smem = draft_smem(cfg, B, 0);
+        if (smem > kSmemLimit) return MTP_ERR_UNSUPPORTED;
+    }
+    const int per_sm = bf ? draft_blocks_per_sm_bf16(cfg->head_dim, smem) : draft_blocks_per_sm_f32(cfg->head_dim, smem);
+    if (per_sm < 1) return MTP_ERR_UNSUPPORTED;
+    int grid = sms;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+
+    char* base = static_cast<char*>(ws);
+    DraftParams p;
+    memset(&p, 0, sizeof p);
+    p.d_t = cfg->d_t; p.d_a = cfg->d_a; p.L = cfg->n_blocks; p.Hq = cfg->n_q_heads; p.hd = cfg->head_dim;
+    p.Hkv = cfg->n_kv_heads; p.F = cfg->d_ff; p.V = cfg->vocab; p.B = B; p.N = N;
+    p.eps = cfg->rms_eps; p.attn_scale = cfg->attn_scale; p.emb_scale = cfg->emb_scale; p.softcap = cfg->logit_softcap;
+    p.tok_embd = w->tok_embd;
+    p.norm_e = static_cast<const float*>(w->norm_e);
+    p.norm_h = static_cast<const float*>(w->norm_h);
+    p.w_pre = w->w_pre;
+    p.final_norm = static_cast<const float*>(w->final_norm);
+    p.w_post = w->w_post;
+    for (int l = 0; l < cfg->n_blocks; ++l) {
+        const mtp_block_weights& b = w->blk[l];
+        BlkW& d = p.blk[l];
+        d.w_q = b.w_q; d.w_o = b.w_o; d.w_gate = b.w_gate; d.w_up = b.w_up; d.w_down = b.w_down;
+        d.attn_norm = static_cast<const float*>(b.attn_norm);
+        d.q_norm = static_cast<const float*>(b.q_norm);
+        d.post_attn_norm = static_cast<const float*>(b.post_attn_norm);
+        d.pre_ffn_norm = static_cast<const float*>(b.pre_ffn_norm);
+        d.post_ffn_norm = static_cast<const float*>(b.post_ffn_norm);
+        d.view = b.kv_view;
+    }
+    for (int v = 0; v < n_views; ++v) {
+        KView& d = p.views[v];
+        d.k = views[v].k; d.v = views[v].v;
+        d.sb = views[v].stride_b; d.sh = views[v].stride_h; d.st = views[v].stride_t;
+        d.cap = views[v].cap; d.window = views[v].window; d.theta = views[v].rope_theta;
+    }
+    p.kv_len = kv_len; p.last_tok = last_tok; p.h_prev = h_prev;
+    p.out_drafts = out_drafts; p.out_h_last = out_h_last; p.out_logits = out_logits;
+    p.hdr = reinterpret_cast<WsHeader*>(base);
+    p.att_cnt = reinterpret_cast<unsigned int*>(base + L.att_cnt);
+    p.amax = reinterpret_cast<unsigned long long*>(base + L.amax);
+    p.XB = reinterpret_cast<float*>(base + L.XB);
+    p.XM = reinterpret_cast<float*>(base + L.XM);
+    p.QR = reinterpret_cast<float*>(base + L.QR);
+    p.OB = reinterpret_cast<float*>(base + L.OB);
+    p.YB = reinterpret_cast<float*>(base + L.YB);
+    p.MB = reinterpret_cast<float*>(base + L.MB);
+    p.Y2 = reinterpret_cast<float*>(base + L.Y2);
+    p.HN = reinterpret_cast<float*>(base + L.HN);
+    p.PART = reinterpret_cast<float*>(base + L.PART);
+    p.ACT = reinterpret_cast<float*>(base + L.ACT);
+    p.act_smem = act_smem;
+    p.kmax = L.kmax;
+    p.timeout_ns = kBarrierLimitNs;
+    (void)seed; (void)offset; (void)hist; (void)H;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, L.amax, s) != cudaSuccess) return MTP_ERR_CUDA;
+    cudaError_t e = bf ? launch_draft_bf16(p, grid, smem, s) : launch_draft_f32(p, grid, smem, s);
+    return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
+}
+
+int mtp_verify_greedy(const void* logits, int ldtype, int B, int N, int V, const int32_t* drafts, int32_t* out_tokens,
+                      int32_t* out_n_accept, void* ws, size_t ws_bytes, mtp_stream_t stream) {
+    if (!logits || !out_tokens || !out_n_accept) return MTP_ERR_ARG;
+    if (B < 1 || B > MTP_MAX_BATCH || N < 0 || N > 16 || V < 1) return MTP_ERR_ARG;
+    if (N > 0 && !drafts) return MTP_ERR_ARG;
+    if (ldtype != MTP_DTYPE_F32 && ldtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(logits) & (ldtype == MTP_DTYPE_BF16 ? 1 : 3)) != 0) return MTP_ERR_ARG;
+    const GreedyLayout L = greedy_layout(B, N);
+    int rc = check_workspace(ws, ws_bytes, L.end);
+    if (rc != MTP_OK) return rc;
+    const int sms = num_sms();
+    if (sms <= 0) return MTP_ERR_CUDA;
+    char* base = static_cast<char*>(ws);
+    VerifyGreedyArgs a;
+    a.logits = logits; a.B = B; a.N = N; a.V = V; a.drafts = drafts;
+    a.out_tokens = out_tokens; a.out_n_accept = out_n_accept;
+    a.hdr = reinterpret_cast<WsHeader*>(base);
+    a.amax = reinterpret_cast<unsigned long long*>(base + L.amax);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, L.end, s) != cudaSuccess) return MTP_ERR_CUDA;
+    return launch_verify_greedy(a, ldtype, sms, s) == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
+}
+
+int mtp_verify_sample(const void* tgt_logits, const void* dft_logits, int ldtype, int B, int N, int V,
+                      const int32_t* drafts, const int32_t* hist, int H, const mtp_sample_params* sp, uint64_t seed,
+                      uint64_t offset, int32_t* out_tokens, int32_t* out_n_accept, void* ws, size_t ws_bytes,
+                      mtp_stream_t stream) {
+    if (!tgt_logits || !out_tokens || !out_n_accept) return MTP_ERR_ARG;
+    if (B < 1 || B > MTP_MAX_BATCH || N < 0 || N > 16 || V < 1) return MTP_ERR_ARG;
+    if (N > 0 && (!drafts || !dft_logits)) return MTP_ERR_ARG;
+    if (H < 0 || (H > 0 && !hist)) return MTP_ERR_ARG;
+    if (ldtype != MTP_DTYPE_F32 && ldtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED;
+    const int am = ldtype == MTP_DTYPE_BF16 ? 1 : 3;
+    if ((reinterpret_cast<uintptr_t>(tgt_logits) & am) || (dft_logits && (reinterpret_cast<uintptr_t>(dft_logits) & am)))
+        return MTP_ERR_ARG;
+    int rc = check_sample_params(sp);
+    if (rc != MTP_OK) return rc;
+    const SampleLayout L = sample_layout(B, N);
+    rc = check_workspace(ws, ws_bytes, L.end);
+    if (rc != MTP_OK) return rc;
+    const int sms = num_sms();
+    if (sms <= 0) return MTP_ERR_CUDA;
+    int grid = verify_sample_max_grid(sms);
+    if (grid < 1) return MTP_ERR_UNSUPPORTED;
+    if (grid > sms) grid = sms;
+    char* base = static_cast<char*>(ws);
+    VerifySampleArgs a;
+    memset(&a, 0, sizeof a);
+    a.tgt = tgt_logits; a.dft = dft_logits; a.bf16 = ldtype == MTP_DTYPE_BF16;
+    a.B = B; a.N = N; a.V = V; a.drafts = drafts; a.hist = hist; a.H = H;
+    a.temp = sp->temp; a.top_p = sp->top_p; a.min_p = sp->min_p; a.rep = sp->rep_penalty;
+    a.pres = sp->presence_penalty;
+    a.seed = seed; a.offset = offset;
+    a.out_tokens = out_tokens; a.out_n_accept = out_n_accept;
+    a.hdr = reinterpret_cast<WsHeader*>(base);
+    a.rowmax = reinterpret_cast<unsigned long long*>(base + L.rowmax);
+    a.cand_cnt = reinterpret_cast<unsigned int*>(base + L.cnt);
+    a.n_keep = reinterpret_cast<int32_t*>(base + L.nkeep);
+    a.w_keep = reinterpret_cast<float*>(base + L.wkeep);
+    a.cand_id = reinterpret_cast<int32_t*>(base + L.id);
+    a.cand_w = reinterpret_cast<float*>(base + L.w);
+    a.resid = reinterpret_cast<float*>(base + L.resid);
+    a.timeout_ns = kBarrierLimitNs;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, L.zero_end, s) != cudaSuccess) return MTP_ERR_CUDA;
+    return launch_verify_sample(a, grid, s) == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
+}
+
+int mtp_last_error(const void* ws, mtp_stream_t stream) {
+    if (!ws) return MTP_ERR_WORKSPACE;
+    int st = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const WsHeader* h = static_cast<const WsHeader*>(ws);
+    if (cudaMemcpyAsync(&st, &h->status, sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MTP_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MTP_ERR_CUDA;
+    return st;
+}
+
+const char* mtp_strerror(int code) {
+    switch (code) {
+    case MTP_OK: return "ok";
+    case MTP_ERR_ARG: return "invalid argument";
+    case MTP_ERR_UNSUPPORTED: return "unsupported size, layout or dtype";
+    case MTP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MTP_ERR_CUDA: return "CUDA launch or copy failed";
+    case MTP_ERR_TIMEOUT: return "grid barrier timed out";
+    case MTP_ERR_CAPACITY: return "sampling candidate set exceeded its capacity";
+    default: return "unknown error";
+    }
+}
+
+int mtp_debug_barrier_timeout(void* ws, size_t ws_bytes, int timeout_us, mtp_stream_t stream) {
+    if (check_workspace(ws, ws_bytes, sizeof(WsHeader)) != MTP_OK) return MTP_ERR_WORKSPACE;
+    if (timeout_us < 1 || timeout_us > 1000000) return MTP_ERR_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess) return MTP_ERR_CUDA;
+    cudaError_t e = launch_barrier_timeout_probe(static_cast<WsHeader*>(ws), 1000ull * (unsigned)timeout_us, s);
+    return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
+}
+
+}  // extern "C"

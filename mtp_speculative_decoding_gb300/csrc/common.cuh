@@ -1,0 +1,182 @@
+// common.cuh -- device helpers shared by the draft and verify kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mtp.h"
+
+namespace mtp {
+
+constexpr int kThreads = 512;          // threads per CTA of every kernel here
+constexpr int kWarps = kThreads / 32;
+
+// ---------------------------------------------------------------------------
+// workspace header (first 256 bytes of every workspace; zeroed per call)
+// ---------------------------------------------------------------------------
+struct WsHeader {
+    unsigned int barrier;     // grid-barrier arrival counter
+    int status;               // MTP_OK or a device-side MTP_ERR_* code
+    unsigned int done;        // last-arriver counters of single-launch kernels
+    unsigned int pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// ---------------------------------------------------------------------------
+// loads
+// ---------------------------------------------------------------------------
+
+// 16-byte streaming load of read-only data (weights, logits, KV): no L1
+// allocation, 256-byte L2 prefetch hint.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+// element i of a weight/KV/logit array of either dtype, as fp32
+template <typename WT> __device__ __forceinline__ float ld_elem(const WT* p, long long i);
+template <> __device__ __forceinline__ float ld_elem<float>(const float* p, long long i) { return __ldg(p + i); }
+template <> __device__ __forceinline__ float ld_elem<uint16_t>(const uint16_t* p, long long i) {
+    return bf16_to_f32(__ldg(p + i));
+}
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// Sum over the CTA; every thread gets the result.  `red` is kWarps floats of
+// shared scratch; the function synchronizes the CTA twice.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    v = warp_sum(v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = lane < kWarps ? red[lane] : 0.f;
+    return warp_sum(t);
+}
+
+// ---------------------------------------------------------------------------
+// argmax keys: a total order on (value, index) packed into 64 bits so that an
+// unsigned max picks the largest value and, among equal values, the lowest
+// index.  NaN orders below -inf (never wins); -0 and +0 are equal.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+    if (f != f) return 0u;
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ unsigned long long pack_argmax(float v, uint32_t idx) {
+    return ((unsigned long long)ordered_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ uint32_t unpack_index(unsigned long long p) {
+    return 0xFFFFFFFFu - (uint32_t)(p & 0xFFFFFFFFull);
+}
+
+// ---------------------------------------------------------------------------
+// Philox-4x32-10 (Salmon et al., SC'11): 10 rounds of the 4x32 bijection with
+// multipliers 0xD2511F53 / 0xCD9E8D57 and Weyl key increments 0x9E3779B9 /
+// 0xBB67AE85.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// uniform in [0, 1) for (sequence b, row i, purpose): 24 random bits, exact in fp32
+__device__ __forceinline__ float philox_uniform(unsigned long long seed, unsigned long long offset,
+                                                uint32_t b, uint32_t i, uint32_t purpose) {
+    uint4 c = make_uint4(b, i * 4u + purpose, (uint32_t)offset, (uint32_t)(offset >> 32));
+    uint2 k = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+    uint4 o = philox4x32_10(c, k);
+    return (float)(o.x >> 8) * (1.0f / 16777216.0f);
+}
+
+// ---------------------------------------------------------------------------
+// grid barrier with a time limit
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Every CTA of a co-resident (cooperative) grid calls this the same number of
+// times.  `epoch` counts barriers passed by the calling CTA (thread 0's copy is
+// the one used).  The counter starts at 0 (the host zeroes the header before
+// the launch).  A CTA that waits longer than `limit_ns`, or sees a non-zero
+// status, gives up: it records MTP_ERR_TIMEOUT (first writer wins) and returns
+// false, after which the caller must return without touching shared results.
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned int& epoch, unsigned long long limit_ns,
+                                             unsigned int arrivals_per_epoch) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        epoch += 1;
+        const unsigned int target = epoch * arrivals_per_epoch;
+        __threadfence();
+        atomicAdd(&hdr->barrier, 1u);
+        const unsigned long long t0 = global_ns();
+        int ok = 1;
+        unsigned int spins = 0;
+        while (true) {
+            const unsigned int v = ld_acquire(&hdr->barrier);
+            if ((int)(v - target) >= 0) break;
+            if (ld_relaxed(&hdr->status) != 0) { ok = 0; break; }
+            if ((++spins & 63u) == 0 && global_ns() - t0 > limit_ns) {
+                atomicCAS(&hdr->status, 0, MTP_ERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+}  // namespace mtp

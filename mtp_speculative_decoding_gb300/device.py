@@ -1,0 +1,72 @@
+"""Device-side containers: upload host arrays (numpy, bf16 as uint16 bits) to
+CUDA tensors and keep the C structs that point into them alive together."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+from . import (Config, KVView, Weights, alloc_workspace, draft_block, make_config, make_view, make_weights,
+               workspace_size)
+
+
+def to_device(a: np.ndarray, dtype: str | None = None, device="cuda"):
+    """numpy -> CUDA tensor; uint16 arrays (or dtype='bf16') become bfloat16."""
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16 or dtype == "bf16":
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a)
+    return t.to(device, non_blocking=False)
+
+
+@dataclasses.dataclass
+class DeviceDraft:
+    cfg: Config
+    weights: Weights
+    views: list
+    tensors: dict
+    kv_len: object
+    last_tok: object
+    h_prev: object
+    hist: object
+    B: int
+    N: int
+    V: int
+    d_t: int
+    ws: object
+
+    def run(self, out_drafts, out_h_last=None, out_logits=None, sample=None, seed=0, offset=0, stream=None):
+        draft_block(self.cfg, self.weights, self.views, self.kv_len, self.last_tok, self.h_prev, out_drafts,
+                    self.ws, out_h_last=out_h_last, out_logits=out_logits, sample=sample, seed=seed,
+                    offset=offset, hist=self.hist if sample is not None else None, stream=stream)
+
+
+def upload_draft(w, device="cuda", extra_ws_for=None) -> DeviceDraft:
+    """Upload a ``synth.DraftWorkload`` (or anything with the same fields).
+
+    ``extra_ws_for`` = (B, N, V) of verify calls that will share the workspace.
+    """
+    import torch
+    m = w.model
+    cfg = make_config(m.d_t, m.d_a, m.n_blocks, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff, m.vocab,
+                      wdtype=m.dtype, rms_eps=m.rms_eps, attn_scale=m.attn_scale, emb_scale=m.emb_scale,
+                      logit_softcap=m.logit_softcap)
+    tensors = {n: to_device(a, device=device) for n, a in w.weights.items()}
+    views, keep = [], []
+    for vd in w.views:
+        k, v = to_device(vd["k"], device=device), to_device(vd["v"], device=device)
+        keep += [k, v]
+        views.append(make_view(k, v, vd["cap"], vd["window"], vd["rope_theta"]))
+    tensors["_views"] = keep
+    weights = make_weights(tensors, m.n_blocks, m.block_view)
+    kv_len = torch.from_numpy(np.ascontiguousarray(w.kv_len, dtype=np.int32)).to(device)
+    last_tok = torch.from_numpy(np.ascontiguousarray(w.last_tok, dtype=np.int32)).to(device)
+    h_prev = torch.from_numpy(np.ascontiguousarray(w.h_prev, dtype=np.float32)).to(device)
+    hist = torch.from_numpy(np.ascontiguousarray(w.hist, dtype=np.int32)).to(device) if w.hist.size else None
+    nbytes = workspace_size(cfg, w.B, w.N, m.vocab)
+    if extra_ws_for is not None:
+        nbytes = max(nbytes, workspace_size(None, *extra_ws_for))
+    ws = alloc_workspace(nbytes, device)
+    return DeviceDraft(cfg, weights, views, tensors, kv_len, last_tok, h_prev, hist, w.B, w.N, m.vocab, m.d_t, ws)

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes as C
 import os
+import platform
 import subprocess
 import threading
 
@@ -16,7 +17,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mtp_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_LIB_PATH = os.path.join(_HERE, "_build", platform.machine(), "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -25,6 +26,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/liboracle.so`` (gcc, OpenMP when available)."""
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
     base = ["gcc", "-O2", "-std=c11", "-D_DEFAULT_SOURCE", "-shared", "-fPIC", "-o", _LIB_PATH + ".tmp", _SRC, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)

@@ -239,14 +239,26 @@ def make_kv_view(m: ModelSpec, vs: ViewSpec, kv_len: np.ndarray, seed: int, tag:
     return out
 
 
+_WEIGHT_CACHE: dict = {}
+
+
+def cached_model_weights(m: ModelSpec, seed: int) -> dict:
+    """make_model_weights, memoised for the last model (several workloads share one model)."""
+    key = (dataclasses.astuple(m), seed)
+    if key not in _WEIGHT_CACHE:
+        _WEIGHT_CACHE.clear()
+        _WEIGHT_CACHE[key] = make_model_weights(m, seed)
+    return _WEIGHT_CACHE[key]
+
+
 def make_draft_workload(name: str, m: ModelSpec, views_spec: list, B: int, N: int,
-                        kv_len, seed: int, hist_len: int = 0) -> DraftWorkload:
+                        kv_len, seed: int, hist_len: int = 0, model_seed: int | None = None) -> DraftWorkload:
     kv_len = np.asarray(kv_len, dtype=np.int32).reshape(B)
     for vs in views_spec:
         need = vs.window if vs.window > 0 else int(kv_len.max())
         if need > vs.cap:
             raise ValueError(f"view cap {vs.cap} too small for {need} positions")
-    weights = make_model_weights(m, seed)
+    weights = cached_model_weights(m, seed if model_seed is None else model_seed)
     views = [make_kv_view(m, vs, kv_len, seed, f"view{j}") for j, vs in enumerate(views_spec)]
     last_tok = uniform_int(seed, "last_tok", (B,), 0, m.vocab)
     h_prev = normal(seed, "h_prev", (B, m.d_t))
@@ -314,7 +326,9 @@ def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None
     kv = np.resize(np.asarray(kv, dtype=np.int32), B) if B != Bf else kv
     if cfg_id == 2:
         views = [views[0], ViewSpec(cap=int(kv.max()), window=0, rope_theta=1e6)]
-    return make_draft_workload(name, m, views, B, N, kv, seed, hist_len=64)
+    # workloads 1-3 share one model ("same model as config 1"): its weights use seed 1001
+    model_seed = workload_seed(1) if cfg_id in (1, 2, 3) else seed
+    return make_draft_workload(name, m, views, B, N, kv, seed, hist_len=64, model_seed=model_seed)
 
 
 # ----------------------------------------------------------------------------
