@@ -311,7 +311,7 @@ int mtp_verify_sample(const void* tgt_logits, const void* dft_logits, int ldtype
     VerifySampleArgs a;
     memset(&a, 0, sizeof a);
     a.tgt = tgt_logits; a.dft = dft_logits; a.bf16 = ldtype == MTP_DTYPE_BF16;
-    a.B = B; a.N = N; a.V = V; a.drafts = drafts; a.hist = hist; a.H = H;
+    a.B = B; a.N = N; a.V = V; a.drafts = drafts; a.hist = hist; a.H = H; a.hist_stride = H;
     a.temp = sp->temp; a.top_p = sp->top_p; a.min_p = sp->min_p; a.rep = sp->rep_penalty;
     a.pres = sp->presence_penalty;
     a.seed = seed; a.offset = offset;

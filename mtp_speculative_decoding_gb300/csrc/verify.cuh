@@ -31,6 +31,7 @@ struct VerifySampleArgs {
     const int32_t* drafts;
     const int32_t* hist;
     int H;
+    int hist_stride;             // row stride of hist (>= H)
     float temp, top_p, min_p, rep, pres;
     unsigned long long seed, offset;
     int32_t* out_tokens;

@@ -27,7 +27,7 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-    base = ["gcc", "-O2", "-std=c11", "-D_DEFAULT_SOURCE", "-shared", "-fPIC", "-o", _LIB_PATH + ".tmp", _SRC, "-lm"]
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-D_DEFAULT_SOURCE", "-shared", "-fPIC", "-o", _LIB_PATH + ".tmp", _SRC, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
@@ -312,3 +312,11 @@ def verify_sample(target, draft, dtype, drafts, hist, params, seed, offset):
     lib().orc_verify_sample(_p(target), _p(draft), 1 if dtype == "bf16" else 0, B, N, V, _p(drafts),
                             _p(hist), H, C.byref(prm), seed, offset, _p(out), _p(n_acc), _p(mg))
     return out, n_acc, mg
+
+
+def exp_cw(x):
+    """The sampler's fp32 exp (see orc_exp_cw)."""
+    L = lib()
+    L.orc_exp_cw.argtypes = [C.c_float]
+    L.orc_exp_cw.restype = C.c_float
+    return np.array([L.orc_exp_cw(float(v)) for v in np.ravel(x)], dtype=np.float32).reshape(np.shape(x))

@@ -231,132 +231,180 @@ double orc_uniform(uint64_t seed, uint64_t offset, uint32_t b, uint32_t i, uint3
 
 /* ------------------------------------------------------------------------ */
 /* sample_dist [SP item 4]                                                   */
+/*                                                                          */
+/* The sampler's arithmetic decides integers (kept sets, orders, picks), so */
+/* it is carried out in the kernel's precision, IEEE fp32, with every       */
+/* rounding step written out: penalties, temperature, weights, and every   */
+/* sum taken sequentially in the documented order.  Given the same fp32     */
+/* inputs, any IEEE fp32 implementation of these steps takes the same       */
+/* decisions.                                                               */
 /* ------------------------------------------------------------------------ */
 
-typedef struct { int id; double w; } cand;
+/* exp(x) for x <= 0 in fp32 (Cody and Waite, "Software Manual for the
+ * Elementary Functions", 1980: argument reduction x = k ln2 + r with ln2 split
+ * into a 16-bit head and a tail so that k * head is exact; exp(r) on
+ * |r| <= ln2 / 2 by its Taylor series through r^7, Horner with fused
+ * multiply-adds; the result scaled by 2^k).  Returns 0 below -87. */
+float orc_exp_cw(float x) {
+    if (!(x >= -87.0f)) return 0.0f;
+    const float ln2_hi = 0.693145751953125f;        /* 45426 / 2^16 */
+    const float ln2_lo = 1.42860682030941723e-06f;  /* ln 2 - ln2_hi */
+    const float log2e = 1.44269504088896341f;
+    const float k = rintf(x * log2e);
+    float r = fmaf(-k, ln2_hi, x);
+    r = fmaf(-k, ln2_lo, r);
+    float q = 1.0f / 5040.0f;
+    q = fmaf(q, r, 1.0f / 720.0f);
+    q = fmaf(q, r, 1.0f / 120.0f);
+    q = fmaf(q, r, 1.0f / 24.0f);
+    q = fmaf(q, r, 1.0f / 6.0f);
+    q = fmaf(q, r, 0.5f);
+    q = fmaf(q, r, 1.0f);
+    q = fmaf(q, r, 1.0f);
+    const int ki = (int)k;                          /* -126 <= ki <= 0 here */
+    uint32_t bits = (uint32_t)(ki + 127) << 23;
+    float scale;
+    memcpy(&scale, &bits, sizeof scale);
+    return q * scale;
+}
 
-static int cand_cmp(const void *a, const void *b) {
+typedef struct { int id; float w; } cand;
+
+static int cand_cmp(const void *a, const void *b) {   /* weight desc, id asc */
     const cand *x = (const cand *)a, *y = (const cand *)b;
     if (x->w > y->w) return -1;
     if (x->w < y->w) return 1;
     return (x->id < y->id) ? -1 : (x->id > y->id);
 }
 
-static int raw_cmp(const void *a, const void *b) {   /* value desc, id asc */
-    return cand_cmp(a, b);
+static float rel_gap(float a, float b, float scale) {
+    float d = fabsf(a - b) / (scale > 0.0f ? scale : 1.0f);
+    return d;
 }
 
 /* Builds sample_dist(z) for one row.
- *   z     raw logits, V entries (double)
+ *   z     raw logits, V entries (values exactly representable in fp32)
  *   pen   penalty token list (history + this window's inputs); duplicates and
  *         out-of-range ids are ignored; each distinct token is penalised once
  *   order top-k (off when top_k <= 0) -> repetition penalty (z > 0: z / r,
- *         else z * r) and presence penalty (z - pres) -> temperature ->
- *         min-p (keep exp(l - lmax) >= min_p) -> top-p (sorted by weight desc,
- *         id asc; keep the shortest prefix whose share of the kept mass reaches
- *         top_p) -> renormalise.
- * Output: n kept candidates, ids[] / w[] in (w desc, id asc) order, w[] the
- * unnormalised weights exp(l - lmax); *wsum their sum in that order.
- * *margin (optional) receives the smallest relative distance of any keep/cut
- * decision or ordering tie to its threshold. */
-int orc_sample_dist(const double *z, int V, const int32_t *pen, int n_pen,
-                    const orc_sample_params *sp, int32_t *ids, double *w, double *wsum,
-                    double *margin) {
-    double *l = (double *)malloc(sizeof(double) * (size_t)V);
+ *         else z * r) then presence penalty (- pres) -> temperature (/ temp)
+ *         -> weights w = exp(l - lmax) -> min-p (keep w >= min_p, i.e.
+ *         p >= min_p * p_max) -> sort by (w desc, id asc) -> top-p (keep the
+ *         shortest prefix whose running sum / total reaches top_p, the
+ *         crossing token included) -> the kept weights, renormalised by their
+ *         sequential sum.
+ * Output: n kept candidates, ids[] / w[] in order; *wsum the kept sum.
+ * *margin (optional): the smallest nonzero relative distance of any keep/cut
+ * decision or ordering to its threshold (diagnostic). */
+int orc_sample_dist_f32(const double *z, int V, const int32_t *pen, int n_pen, const orc_sample_params *sp,
+                        int32_t *ids, float *w, float *wsum, double *margin) {
+    const float rep = (float)sp->rep_penalty, pres = (float)sp->presence_penalty;
+    const float temp = (float)sp->temp, min_p = (float)sp->min_p, top_p = (float)sp->top_p;
+    float *l = (float *)malloc(sizeof(float) * (size_t)V);
     unsigned char *alive = (unsigned char *)malloc((size_t)V);
-    for (int x = 0; x < V; ++x) { l[x] = z[x]; alive[x] = !isnan(z[x]); }
+    for (int x = 0; x < V; ++x) { l[x] = (float)z[x]; alive[x] = !isnan(l[x]); }
     double mg = INFINITY;
 
     if (sp->top_k > 0 && sp->top_k < V) {
         cand *all = (cand *)malloc(sizeof(cand) * (size_t)V);
         int na = 0;
         for (int x = 0; x < V; ++x) if (alive[x]) { all[na].id = x; all[na].w = l[x]; ++na; }
-        qsort(all, (size_t)na, sizeof(cand), raw_cmp);
+        qsort(all, (size_t)na, sizeof(cand), cand_cmp);
         memset(alive, 0, (size_t)V);
         for (int j = 0; j < na && j < sp->top_k; ++j) alive[all[j].id] = 1;
-        if (na > sp->top_k) {
-            double a = all[sp->top_k - 1].w, c = all[sp->top_k].w;
-            double d = fabs(a - c) / (fabs(a) + 1e-30);
-            if (d > 0.0 && d < mg) mg = d;
-        }
         free(all);
     }
 
-    /* penalties, once per distinct token */
     unsigned char *seen = (unsigned char *)calloc((size_t)V, 1);
     for (int j = 0; j < n_pen; ++j) {
         int x = pen[j];
         if (x < 0 || x >= V || seen[x]) continue;
         seen[x] = 1;
-        if (l[x] > 0.0) l[x] = l[x] / sp->rep_penalty;
-        else l[x] = l[x] * sp->rep_penalty;
-        l[x] -= sp->presence_penalty;
+        float y = l[x] > 0.0f ? l[x] / rep : l[x] * rep;
+        l[x] = y - pres;
     }
     free(seen);
+    for (int x = 0; x < V; ++x) l[x] = l[x] / temp;
 
-    /* temperature */
-    for (int x = 0; x < V; ++x) l[x] = l[x] / sp->temp;
-
-    double lmax = -INFINITY;
+    float lmax = -INFINITY;
     for (int x = 0; x < V; ++x) if (alive[x] && l[x] > lmax) lmax = l[x];
 
-    /* min-p: keep p(x) >= min_p * p_max, i.e. exp(l - lmax) >= min_p */
     cand *c = (cand *)malloc(sizeof(cand) * (size_t)V);
     int n = 0;
     for (int x = 0; x < V; ++x) {
         if (!alive[x]) continue;
-        double wx = exp(l[x] - lmax);
-        if (sp->min_p > 0.0) {
-            double d = fabs(wx - sp->min_p) / sp->min_p;
-            if (d < mg) mg = d;
+        const float wx = orc_exp_cw(l[x] - lmax);
+        if (min_p > 0.0f) {
+            double d = rel_gap(wx, min_p, min_p);
+            if (d > 0.0 && d < mg) mg = d;
         }
-        if (wx >= sp->min_p) { c[n].id = x; c[n].w = wx; ++n; }
+        if (wx >= min_p) { c[n].id = x; c[n].w = wx; ++n; }
     }
     qsort(c, (size_t)n, sizeof(cand), cand_cmp);
     for (int j = 1; j < n; ++j) {
-        double d = fabs(c[j - 1].w - c[j].w) / (c[j - 1].w + 1e-300);
-        if (d > 0.0 && d < mg) mg = d;   /* exact ties are ordered by id on both sides */
+        double d = rel_gap(c[j - 1].w, c[j].w, c[j - 1].w);
+        if (d > 0.0 && d < mg) mg = d;
     }
-
-    /* top-p over the renormalised min-p set */
-    if (sp->top_p < 1.0 && n > 0) {
-        double tot = 0.0;
+    if (top_p < 1.0f && n > 0) {
+        float tot = 0.0f;
         for (int j = 0; j < n; ++j) tot += c[j].w;
-        double cum = 0.0;
+        float cum = 0.0f;
         int keep = n;
         for (int j = 0; j < n; ++j) {
             cum += c[j].w;
-            double share = cum / tot;
-            double d = fabs(share - sp->top_p);
-            if (d < mg) mg = d;
-            if (share >= sp->top_p) { keep = j + 1; break; }
+            const float share = cum / tot;
+            double d = fabs((double)share - (double)top_p);
+            if (d > 0.0 && d < mg) mg = d;
+            if (share >= top_p) { keep = j + 1; break; }
         }
         n = keep;
     }
-    double s = 0.0;
-    for (int j = 0; j < n; ++j) { ids[j] = c[j].id; w[j] = c[j].w; s += c[j].w; }
-    *wsum = s;
+    float ssum = 0.0f;
+    for (int j = 0; j < n; ++j) { ids[j] = c[j].id; w[j] = c[j].w; ssum += c[j].w; }
+    *wsum = ssum;
     if (margin) *margin = mg;
     free(c); free(alive); free(l);
     return n;
 }
 
-/* inverse-CDF pick over candidates in their stored order: the first j with
- * u * wsum < w[0] + ... + w[j].  *margin receives the distance of u * wsum to
- * the nearer edge of the chosen interval, relative to wsum. */
-int32_t orc_pick(const int32_t *ids, const double *w, int n, double wsum, double u, double *margin) {
-    double target = u * wsum, acc = 0.0, prev = 0.0;
+/* double-typed wrapper for callers outside this file (weights are fp32 values) */
+int orc_sample_dist(const double *z, int V, const int32_t *pen, int n_pen, const orc_sample_params *sp,
+                    int32_t *ids, double *w, double *wsum, double *margin) {
+    float *wf = (float *)malloc(sizeof(float) * (size_t)(V > 0 ? V : 1));
+    float ws;
+    int n = orc_sample_dist_f32(z, V, pen, n_pen, sp, ids, wf, &ws, margin);
+    for (int j = 0; j < n; ++j) w[j] = (double)wf[j];
+    *wsum = (double)ws;
+    free(wf);
+    return n;
+}
+
+/* Inverse-CDF pick over candidates in their stored order: the first j with
+ * u * wsum < w[0] + ... + w[j] (fp32, running sum in order).  *margin: the
+ * distance of u * wsum to the nearer edge of the chosen interval, relative to
+ * wsum (diagnostic). */
+int32_t orc_pick_f32(const int32_t *ids, const float *w, int n, float wsum, float u, double *margin) {
+    const float target = u * wsum;
+    float acc = 0.0f, prev = 0.0f;
     for (int j = 0; j < n; ++j) {
         prev = acc;
         acc += w[j];
         if (target < acc) {
-            double a = target - prev, b = acc - target;
-            if (margin) *margin = (a < b ? a : b) / (wsum > 0.0 ? wsum : 1.0);
+            double a = (double)target - (double)prev, b = (double)acc - (double)target;
+            if (margin) *margin = (a < b ? a : b) / (wsum > 0.0f ? (double)wsum : 1.0);
             return ids[j];
         }
     }
-    if (margin) *margin = 0.0;   /* fell off the end through rounding: a boundary case */
+    if (margin) *margin = 0.0;
     return n > 0 ? ids[n - 1] : 0;
+}
+
+int32_t orc_pick(const int32_t *ids, const double *w, int n, double wsum, double u, double *margin) {
+    float *wf = (float *)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+    for (int j = 0; j < n; ++j) wf[j] = (float)w[j];
+    int32_t r = orc_pick_f32(ids, wf, n, (float)wsum, (float)u, margin);
+    free(wf);
+    return r;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -458,7 +506,7 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
     double *z = malloc(sizeof(double) * (size_t)B * V);
     int32_t *tok = malloc(sizeof(int32_t) * (size_t)B);
     int32_t *ids = malloc(sizeof(int32_t) * (size_t)V);
-    double *w = malloc(sizeof(double) * (size_t)V);
+    float *wf = malloc(sizeof(float) * (size_t)V);
     int32_t *pen = malloc(sizeof(int32_t) * (size_t)(H + N + 1));
     int rc = 0;
     for (size_t i = 0; i < (size_t)B * d_t; ++i) h[i] = (double)h_prev[i];
@@ -480,10 +528,11 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
                 int np = 0;
                 for (int j = 0; j < H; ++j) pen[np++] = hist[(size_t)b * H + j];
                 for (int j = 0; j < k; ++j) pen[np++] = drafts[(size_t)b * N + j];
-                double ws, m1, m2;
-                int n = orc_sample_dist(zb, V, pen, np, sp, ids, w, &ws, &m1);
-                double u = orc_uniform(seed, offset, (uint32_t)b, (uint32_t)k, 0u);
-                pick = orc_pick(ids, w, n, ws, u, &m2);
+                float ws;
+                double m1, m2;
+                int n = orc_sample_dist_f32(zb, V, pen, np, sp, ids, wf, &ws, &m1);
+                float u = (float)orc_uniform(seed, offset, (uint32_t)b, (uint32_t)k, 0u);
+                pick = orc_pick_f32(ids, wf, n, ws, u, &m2);
                 mg = m1 < m2 ? m1 : m2;
             }
             if (margin) margin[(size_t)b * N + k] = mg;
@@ -494,7 +543,7 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
         double *sw = h; h = hn; hn = sw;
     }
     if (h_last && rc == 0) memcpy(h_last, h, sizeof(double) * (size_t)B * d_t);
-    free(h); free(hn); free(z); free(tok); free(ids); free(w); free(pen);
+    free(h); free(hn); free(z); free(tok); free(ids); free(wf); free(pen);
     return rc;
 }
 
@@ -526,14 +575,17 @@ void orc_verify_greedy(const void *logits, int bf16, int B, int N, int V, const 
 
 /* Exact speculative sampling at temp > 0 ([SP] item 4).
  * Row i (0..N-1): p_i = sample_dist(target row i), q_i = sample_dist(draft row
- * i), both with penalty set hist[b] u drafts[b][0..i-1].  The draft x = d_i is
- * accepted iff u < p_i(x) / q_i(x) (u of (b, i, purpose 1)); on the first
- * rejection the emitted token is drawn from norm(max(p_i - q_i, 0)) (from p_i
- * when that residual is empty) with the uniform of (b, i, purpose 2) and the
- * window ends.  If every draft is accepted, the bonus token is drawn from
- * p_N (penalty set hist u d_0..d_{N-1}) with the uniform of (b, N, purpose 3).
- * margin[b] (optional): the smallest relative distance of any decision taken
- * for sequence b to its threshold. */
+ * i), both with penalty set hist[b] u drafts[b][0..i-1].  With x = d_i,
+ * p_i(x) = w_x / W_p and q_i(x) = w'_x / W_q (0 when x is not kept); x is
+ * accepted iff u < p_i(x) / q_i(x) (fp32; q = 0 gives +inf, or NaN -> reject,
+ * when p = 0 too), u of (b, i, purpose 1).  On the first rejection the emitted
+ * token is drawn from r_j = max(p_j - q(id_j), 0) over p's kept candidates in
+ * p's order (from p itself when sum r = 0) with the uniform of (b, i, purpose
+ * 2) and the window ends.  If every draft is accepted, the bonus token is
+ * drawn from p_N (penalty set hist u d_0..d_{N-1}) with the uniform of
+ * (b, N, purpose 3).  Sampler arithmetic is fp32 as in orc_sample_dist_f32.
+ * margin[b] (optional): smallest relative distance of any decision taken for
+ * sequence b to its threshold (diagnostic). */
 void orc_verify_sample(const void *tgt, const void *dft, int bf16, int B, int N, int V,
                        const int32_t *drafts, const int32_t *hist, int H,
                        const orc_sample_params *sp, uint64_t seed, uint64_t offset,
@@ -542,8 +594,8 @@ void orc_verify_sample(const void *tgt, const void *dft, int bf16, int B, int N,
     {
         double *z = malloc(sizeof(double) * (size_t)V);
         int32_t *pid = malloc(sizeof(int32_t) * (size_t)V), *qid = malloc(sizeof(int32_t) * (size_t)V);
-        double *pw = malloc(sizeof(double) * (size_t)V), *qw = malloc(sizeof(double) * (size_t)V);
-        double *r = malloc(sizeof(double) * (size_t)V);
+        float *pw = malloc(sizeof(float) * (size_t)V), *qw = malloc(sizeof(float) * (size_t)V);
+        float *r = malloc(sizeof(float) * (size_t)V);
         int32_t *pen = malloc(sizeof(int32_t) * (size_t)(H + N + 1));
 #pragma omp for schedule(dynamic, 64)
         for (int b = 0; b < B; ++b) {
@@ -557,45 +609,45 @@ void orc_verify_sample(const void *tgt, const void *dft, int bf16, int B, int N,
                 const int64_t trow = ((int64_t)b * (N + 1) + i) * V;
                 const int64_t drow = ((int64_t)b * N + i) * V;
                 for (int v = 0; v < V; ++v) z[v] = elem(tgt, trow + v, bf16);
-                double ps, qs;
-                int np_ = orc_sample_dist(z, V, pen, np, sp, pid, pw, &ps, &m1);
+                float ps, qs;
+                int np_ = orc_sample_dist_f32(z, V, pen, np, sp, pid, pw, &ps, &m1);
                 if (m1 < mg) mg = m1;
                 for (int v = 0; v < V; ++v) z[v] = elem(dft, drow + v, bf16);
-                int nq = orc_sample_dist(z, V, pen, np, sp, qid, qw, &qs, &m1);
+                int nq = orc_sample_dist_f32(z, V, pen, np, sp, qid, qw, &qs, &m1);
                 if (m1 < mg) mg = m1;
                 const int32_t x = drafts[(size_t)b * N + i];
-                double px = 0.0, qx = 0.0;
+                float px = 0.0f, qx = 0.0f;
                 for (int j = 0; j < np_; ++j) if (pid[j] == x) { px = pw[j] / ps; break; }
                 for (int j = 0; j < nq; ++j) if (qid[j] == x) { qx = qw[j] / qs; break; }
-                double u = orc_uniform(seed, offset, (uint32_t)b, (uint32_t)i, 1u);
-                double ratio = px / qx;               /* qx == 0: +inf (px > 0) or NaN */
+                const float u = (float)orc_uniform(seed, offset, (uint32_t)b, (uint32_t)i, 1u);
+                const float ratio = px / qx;
                 if (!isnan(ratio) && isfinite(ratio)) {
-                    double d = fabs(u - ratio);
-                    if (d < mg) mg = d;
+                    double d = fabs((double)u - (double)ratio);
+                    if (d > 0.0 && d < mg) mg = d;
                 }
                 if (u < ratio) { ot[i] = x; pen[np++] = x; continue; }
-                /* residual norm(max(p - q, 0)) over p's support, in p's order */
-                double R = 0.0;
+                float R = 0.0f;
                 for (int j = 0; j < np_; ++j) {
-                    double pj = pw[j] / ps, qj = 0.0;
+                    const float pj = pw[j] / ps;
+                    float qj = 0.0f;
                     for (int jj = 0; jj < nq; ++jj) if (qid[jj] == pid[j]) { qj = qw[jj] / qs; break; }
-                    r[j] = pj > qj ? pj - qj : 0.0;
+                    r[j] = pj > qj ? pj - qj : 0.0f;
                     R += r[j];
                 }
-                double u2 = orc_uniform(seed, offset, (uint32_t)b, (uint32_t)i, 2u);
-                if (R > 0.0) ot[i] = orc_pick(pid, r, np_, R, u2, &m1);
-                else ot[i] = orc_pick(pid, pw, np_, ps, u2, &m1);
+                const float u2 = (float)orc_uniform(seed, offset, (uint32_t)b, (uint32_t)i, 2u);
+                if (R > 0.0f) ot[i] = orc_pick_f32(pid, r, np_, R, u2, &m1);
+                else ot[i] = orc_pick_f32(pid, pw, np_, ps, u2, &m1);
                 if (m1 < mg) mg = m1;
                 break;
             }
             if (i == N) {
                 const int64_t trow = ((int64_t)b * (N + 1) + N) * V;
                 for (int v = 0; v < V; ++v) z[v] = elem(tgt, trow + v, bf16);
-                double ps;
-                int np_ = orc_sample_dist(z, V, pen, np, sp, pid, pw, &ps, &m1);
+                float ps;
+                int np_ = orc_sample_dist_f32(z, V, pen, np, sp, pid, pw, &ps, &m1);
                 if (m1 < mg) mg = m1;
-                double u3 = orc_uniform(seed, offset, (uint32_t)b, (uint32_t)N, 3u);
-                ot[N] = orc_pick(pid, pw, np_, ps, u3, &m1);
+                const float u3 = (float)orc_uniform(seed, offset, (uint32_t)b, (uint32_t)N, 3u);
+                ot[N] = orc_pick_f32(pid, pw, np_, ps, u3, &m1);
                 if (m1 < mg) mg = m1;
             }
             out_n_accept[b] = i;

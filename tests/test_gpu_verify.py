@@ -87,14 +87,16 @@ def gpu_sample(inp, seed, offset, ws=None):
     return out.cpu().numpy(), n.cpu().numpy()
 
 
-def compare_sample(inp, seed, offset, max_boundary_frac=0.05):
+def compare_sample(inp, seed, offset):
+    """Bit-exact: both sides take the sampler's decisions in IEEE fp32 with the
+    same steps, so every sequence must match.  The oracle's margins (distance
+    of each decision to its threshold) are printed for the record."""
     go, gn = gpu_sample(inp, seed, offset)
     oo, on, mg = oracle.verify_sample(inp.target, inp.draft, inp.dtype, inp.drafts, inp.hist, inp.params,
                                       seed, offset)
-    clear = mg > 1e-4
-    assert np.array_equal(go[clear], oo[clear]), np.nonzero((go != oo).any(1) & clear)
-    assert np.array_equal(gn[clear], on[clear])
-    assert (~clear).mean() <= max_boundary_frac
+    print(f"closest decision margin {mg.min():.2e}; sequences within 1e-6: {(mg < 1e-6).sum()} of {mg.size}")
+    bad = np.nonzero((go != oo).any(1) | (gn != on))[0]
+    assert bad.size == 0, f"sequences {bad} differ; their margins {mg[bad]}"
     return gn
 
 

@@ -121,17 +121,17 @@ def test_sample_dist_softmax_min_p_top_p():
     z = [2.0, 1.0, 0.0, -1.0]
     ids, p = probs(z)
     e = np.exp(np.array(z) - 2.0)
-    assert ids == [0, 1, 2, 3] and np.allclose(p, e / e.sum(), rtol=1e-14)
+    assert ids == [0, 1, 2, 3] and np.allclose(p, e / e.sum(), rtol=2e-6)
     # min-p 0.2 keeps p >= 0.2 p_max: e^-1 = 0.368 stays, e^-2 = 0.135 goes
     ids, p = probs(z, min_p=0.2)
-    assert ids == [0, 1] and np.allclose(p, [1 / (1 + math.e ** -1), math.e ** -1 / (1 + math.e ** -1)])
+    assert ids == [0, 1] and np.allclose(p, [1 / (1 + math.e ** -1), math.e ** -1 / (1 + math.e ** -1)], rtol=2e-6)
     # top-p keeps the shortest prefix whose mass reaches top_p (0.731 >= 0.7)
     assert probs(z, min_p=0.2, top_p=0.7)[0] == [0]
     assert probs(z, min_p=0.2, top_p=0.75)[0] == [0, 1]
     # temperature 0.5 doubles every logit gap
     ids, p = probs(z, temp=0.5)
     e2 = np.exp(2 * (np.array(z) - 2.0))
-    assert np.allclose(p, e2 / e2.sum(), rtol=1e-14)
+    assert np.allclose(p, e2 / e2.sum(), rtol=2e-6)
 
 
 def test_sample_dist_penalties():
@@ -142,7 +142,7 @@ def test_sample_dist_penalties():
     l = np.array([2.0 / 2 - 0.1, -1.0 * 2 - 0.1, 0.5, 0.1])
     e = np.exp(l - l.max())
     order = [0, 2, 3, 1]
-    assert ids == order and np.allclose(p, e[order] / e.sum(), rtol=1e-14)
+    assert ids == order and np.allclose(p, e[order] / e.sum(), rtol=2e-6)
     # a unit penalty is a no-op
     assert probs(z, pen=[0, 1], rep_penalty=1.0) == probs(z)
 
@@ -355,7 +355,8 @@ def test_monte_carlo_tv_exact_vs_greedy_match():
     toy = ToySampler(sp)
     h0 = [1, 4, 2, 0]
     exact = _exact_3(toy, h0)
-    assert abs(exact.sum() - 1.0) < 1e-12
+    assert abs(exact.sum() - 1.0) < 1e-6   # fp32 sampler probabilities
+    exact = exact / exact.sum()
     rng = np.random.default_rng(2024)
     direct = np.bincount(rng.choice(216, size=S, p=exact / exact.sum()), minlength=216) / S
     tv_noise = _tv(direct, exact)
@@ -392,3 +393,18 @@ def test_monte_carlo_tv_deterministic_drafter():
     print(f"TV noise {_tv(direct, exact):.4f} exact {_tv(spec, exact):.4f}; tokens/round {tpr:.2f}")
     assert _tv(spec, exact) < 1.5 * _tv(direct, exact) + 0.002
     assert 1.0 < tpr <= 3.0
+
+
+def test_sampler_exp_accuracy_and_exact_points():
+    """The sampler's fp32 exp (Cody-Waite reduction + Taylor polynomial) is
+    within 2 ulp of exp over [-87, 0], exact at 0, monotone, and 0 below -87."""
+    x = np.concatenate([np.linspace(-87.0, 0.0, 200001, dtype=np.float32),
+                        -np.logspace(-8, 1.9, 4001).astype(np.float32)])
+    got = oracle.exp_cw(x).astype(np.float64)
+    ref = np.exp(x.astype(np.float64))
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(got - ref) / ulp) <= 2.0
+    assert oracle.exp_cw(np.float32(0.0)) == 1.0
+    xs = np.sort(x)
+    assert np.all(np.diff(oracle.exp_cw(xs).astype(np.float64)) >= 0)
+    assert oracle.exp_cw(np.float32(-87.5)) == 0.0
