@@ -215,6 +215,24 @@ int mtp_verify_sample(const void *tgt_logits, const void *dft_logits, int ldtype
                       int32_t *out_tokens, int32_t *out_n_accept,
                       void *ws, size_t ws_bytes, mtp_stream_t stream);
 
+/* Greedy verify without a workspace.  The pages have no counterpart of this
+ * call; it exists for callers that may not allocate device memory at all --
+ * for example a serving loop that has already handed every byte of the GPU to
+ * its weights and KV cache and forbids further allocations, or code that must
+ * not call cudaMalloc because it can synchronize the device in the middle of a
+ * decode step.  Same arguments, results and errors as mtp_verify_greedy, minus
+ * `ws` / `ws_bytes`: the scratch is a 4 KiB array built into the library (held
+ * on every GPU that loads it until the process exits), so B * (1 + N) may be
+ * at most 480; larger sizes return MTP_ERR_UNSUPPORTED and launch nothing.
+ * Allocates nothing.  The first call on a device looks up the array's device
+ * address (with that device current); make that first call before any stream
+ * capture.  All calls share the one array and every call clears it first, so
+ * calls that may overlap on the GPU (different streams, or several host
+ * threads) race and must be serialized by the caller. */
+int mtp_verify_greedy_noalloc(const void *logits, int ldtype, int B, int N, int V,
+                              const int32_t *drafts, int32_t *out_tokens, int32_t *out_n_accept,
+                              mtp_stream_t stream);
+
 /* Device status of the most recent call that used `ws`: MTP_OK,
  * MTP_ERR_TIMEOUT or MTP_ERR_CAPACITY.  SYNCHRONIZES `stream` (a 4-byte
  * device-to-host copy).  Returns MTP_ERR_CUDA if the copy fails. */

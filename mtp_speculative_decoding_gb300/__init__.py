@@ -30,7 +30,7 @@ MTP_MAX_BATCH = 64
 
 # every entry point include/mtp.h declares
 EXPORTS = ("mtp_workspace_size", "mtp_draft_block", "mtp_verify_greedy", "mtp_verify_sample",
-           "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout")
+           "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout", "mtp_verify_greedy_noalloc")
 
 
 class MTPError(RuntimeError):
@@ -97,6 +97,8 @@ def lib():
             L.mtp_strerror.restype = C.c_char_p
             L.mtp_debug_barrier_timeout.argtypes = [P, Z, I, P]
             L.mtp_debug_barrier_timeout.restype = I
+            L.mtp_verify_greedy_noalloc.argtypes = [P, I, I, I, I, P, P, P, P]
+            L.mtp_verify_greedy_noalloc.restype = I
             _lib = L
     return _lib
 
@@ -222,6 +224,17 @@ def verify_greedy(logits, drafts, out_tokens, out_n_accept, ws, stream=None) -> 
     rc = lib().mtp_verify_greedy(_ptr(logits), _dtype_code(logits), B, R - 1, V, _ptr(drafts),
                                  _ptr(out_tokens), _ptr(out_n_accept), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "mtp_verify_greedy")
+
+
+def verify_greedy_noalloc(logits, drafts, out_tokens, out_n_accept, stream=None) -> None:
+    """Greedy verify through the library's built-in scratch (no workspace, no
+    allocation): for callers that may not allocate device memory.  Calls on
+    overlapping streams race; B * (1 + N) <= 480."""
+    _require_cuda(logits, drafts, out_tokens, out_n_accept)
+    B, R, V = logits.shape
+    rc = lib().mtp_verify_greedy_noalloc(_ptr(logits), _dtype_code(logits), B, R - 1, V, _ptr(drafts),
+                                         _ptr(out_tokens), _ptr(out_n_accept), _stream(stream))
+    _check(rc, "mtp_verify_greedy_noalloc")
 
 
 def verify_sample(tgt_logits, dft_logits, drafts, hist, params, seed: int, offset: int, out_tokens,
