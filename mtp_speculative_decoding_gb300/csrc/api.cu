@@ -98,8 +98,10 @@ SampleLayout sample_layout(int B, int N) {
 size_t draft_smem(const mtp_config* c, int B, int act_smem) {
     const size_t wb = c->wdtype == MTP_DTYPE_BF16 ? 2 : 4;
     const size_t hd = c->head_dim, grp = c->n_q_heads / c->n_kv_heads;
-    const size_t attn = hd / 2 * sizeof(double) + (2 * grp * hd + grp * kAttnKeys + 48) * sizeof(float) +
-                        2 * (size_t)kAttnKeys * (hd * wb + kAttnPad);
+    const size_t ck = (size_t)attn_keys((int)hd, (int)wb);
+    // RoPE table, q / o / scores / row state, and two K + V sub-chunk buffers
+    const size_t attn = hd / 2 * sizeof(double) + (2 * grp * hd + grp * ck + 48) * sizeof(float) +
+                        2 * 2 * ck * (hd * wb + kAttnPad);
     const size_t kmax = draft_kmax(c);
     const size_t act = (((size_t)c->d_a + 3) & ~(size_t)3) * sizeof(float) +
                        (act_smem ? (size_t)B * kmax : kmax) * sizeof(float);

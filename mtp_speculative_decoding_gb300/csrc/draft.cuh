@@ -8,7 +8,8 @@
 
 namespace mtp {
 
-constexpr int kAttnKeys = 64;      // keys staged per attention sub-chunk
+// keys per staged attention sub-chunk: 64, or 32 for rows above 512 bytes
+__host__ __device__ constexpr int attn_keys(int hd, int wbytes) { return hd * wbytes <= 512 ? 64 : 32; }
 constexpr int kAttnPad = 16;       // bytes of padding per staged K/V row
 constexpr int kMaxGrid = 1024;     // upper bound on CTAs of the persistent grid
 

@@ -229,11 +229,14 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
             for (int i = threadIdx.x; i < n; i += blockDim.x) tmp[i] = __ldcg(p.XB + (long long)b * n + i);
             __syncthreads();
         } else {
-            for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(p.Y2 + (long long)b * n + i);
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                dst[i] = __ldcg(p.Y2 + (long long)b * n + i);
+                tmp[i] = __ldcg(p.XM + (long long)b * n + i);
+            }
             __syncthreads();
             rms_into(dst, p.blk[l - 1].post_ffn_norm, n, p.eps, dst, red);
             for (int i = threadIdx.x; i < n; i += blockDim.x) {
-                const float x = __ldcg(p.XM + (long long)b * n + i) + dst[i];
+                const float x = tmp[i] + dst[i];
                 tmp[i] = x;
                 if (writer) p.XB[(long long)b * n + i] = x;
             }
@@ -244,11 +247,14 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     }
     case PH_FFN1: {
         const int n = p.d_a;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(p.YB + (long long)b * n + i);
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            dst[i] = __ldcg(p.YB + (long long)b * n + i);
+            tmp[i] = __ldcg(p.XB + (long long)b * n + i);
+        }
         __syncthreads();
         rms_into(dst, p.blk[l].post_attn_norm, n, p.eps, dst, red);
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            const float x = __ldcg(p.XB + (long long)b * n + i) + dst[i];
+            const float x = tmp[i] + dst[i];
             tmp[i] = x;
             if (writer) p.XM[(long long)b * n + i] = x;
         }
@@ -258,10 +264,13 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     }
     case PH_POST: {
         const int n = p.d_a;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(p.Y2 + (long long)b * n + i);
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            dst[i] = __ldcg(p.Y2 + (long long)b * n + i);
+            tmp[i] = __ldcg(p.XM + (long long)b * n + i);
+        }
         __syncthreads();
         rms_into(dst, p.blk[p.L - 1].post_ffn_norm, n, p.eps, dst, red);
-        for (int i = threadIdx.x; i < n; i += blockDim.x) tmp[i] = __ldcg(p.XM + (long long)b * n + i) + dst[i];
+        for (int i = threadIdx.x; i < n; i += blockDim.x) tmp[i] += dst[i];
         __syncthreads();
         rms_into(tmp, p.final_norm, n, p.eps, dst, red);
         break;
@@ -337,8 +346,10 @@ __device__ __forceinline__ int view_lo(const KView& v, int kv_len) {
 
 template <typename WT, int HD>
 __device__ void attention_phase(const DraftParams& p, int l, int k, unsigned char* smem) {
-    constexpr int CK = kAttnKeys;
+    constexpr int CK = attn_keys(HD, (int)sizeof(WT));      // keys per staged sub-chunk
     constexpr int ROWB = HD * (int)sizeof(WT) + kAttnPad;   // bytes per staged row
+    constexpr int BUFB = 2 * CK * ROWB;                     // one K + V sub-chunk
+    constexpr int NCP = (2 * CK * (HD * (int)sizeof(WT) / 16) + kThreads - 1) / kThreads;  // copies per thread
     constexpr int CPR = HD * (int)sizeof(WT) / 16;          // 16-byte chunks per row
     constexpr int EPC = 16 / (int)sizeof(WT);
     const KView& vw = p.views[p.blk[l].view];
@@ -352,11 +363,10 @@ __device__ void attention_phase(const DraftParams& p, int l, int k, unsigned cha
     float* mrow = sc + grp * CK;                         // [grp]
     float* lrow = mrow + 16;                             // [grp]
     float* arow = lrow + 16;                             // [grp]
-    unsigned char* ks = reinterpret_cast<unsigned char*>(arow + 16);
-    unsigned char* vs = ks + CK * ROWB;
+    unsigned char* kvbuf = reinterpret_cast<unsigned char*>(arow + 16);  // 2 x (K rows, V rows)
     __shared__ int s_last;
 
-    // keys per item so that the grid gets about two items per CTA
+    // RoPE inverse frequencies, once per phase (fp64 is scarce on this part)
     {
         const double ltheta = log((double)vw.theta);
         for (int i = tid; i < HD / 2; i += blockDim.x) invf[i] = exp(-2.0 * (double)i / (double)HD * ltheta);
@@ -364,7 +374,10 @@ __device__ void attention_phase(const DraftParams& p, int l, int k, unsigned cha
     }
     long long total = 0;
     for (int b = 0; b < p.B; ++b) total += (long long)(p.kv_len[b] - view_lo(vw, p.kv_len[b])) * p.Hkv;
-    long long kpi = (total + 2LL * gridDim.x - 1) / (2LL * gridDim.x);
+    // keys per item: about one item per CTA (two when every CTA would get
+    // more than 512 keys, to even out ragged sequence lengths)
+    const long long target = (total / gridDim.x <= 512) ? gridDim.x : 2LL * gridDim.x;
+    long long kpi = (total + target - 1) / target;
     kpi = ((kpi + CK - 1) / CK) * CK;
     if (kpi < CK) kpi = CK;
     long long n_items = 0;
@@ -391,6 +404,38 @@ __device__ void attention_phase(const DraftParams& p, int l, int k, unsigned cha
         const int lo = view_lo(vw, kv_len);
         const long long t_beg = lo + (long long)s * kpi;
         const long long t_end = (t_beg + kpi < kv_len) ? t_beg + kpi : kv_len;
+
+        // K/V sub-chunks of CK keys go to shared memory through cp.async, two
+        // buffers deep: sub-chunk i + 1 is in flight while i is used.  Rows
+        // past the range are zero-filled so they never carry NaN.
+        const WT* kbase = reinterpret_cast<const WT*>(vw.k) + (long long)b * vw.sb + (long long)g * vw.sh;
+        const WT* vbase = reinterpret_cast<const WT*>(vw.v) + (long long)b * vw.sb + (long long)g * vw.sh;
+        const int nsub = (int)((t_end - t_beg + CK - 1) / CK);
+        auto stage = [&](int i) {
+            const long long t0 = t_beg + (long long)i * CK;
+            const int cnt = (int)((t_end - t0) < CK ? (t_end - t0) : CK);
+            const int s0 = (int)(t0 % vw.cap);
+            unsigned char* buf = kvbuf + (i & 1) * BUFB;
+#pragma unroll
+            for (int u = 0; u < NCP; ++u) {
+                const int c = tid + u * kThreads;
+                if (c < 2 * CK * CPR) {
+                    const int which = c / (CK * CPR);
+                    const int j = (c / CPR) % CK;
+                    const int q = c % CPR;
+                    unsigned char* dst = buf + which * CK * ROWB + j * ROWB + q * 16;
+                    if (j < cnt) {
+                        int slot = s0 + j;
+                        if (slot >= vw.cap) slot %= vw.cap;
+                        cp_async16(dst, (which ? vbase : kbase) + (long long)slot * vw.st + q * EPC);
+                    } else {
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
+            cp_async_commit();
+        };
+        stage(0);
 
         // q-norm + RoPE for the group's heads (warp h handles head h), scaled by attn_scale
         if (warp < grp) {
@@ -438,23 +483,18 @@ __device__ void attention_phase(const DraftParams& p, int l, int k, unsigned cha
         for (int o = tid; o < grp * HD; o += blockDim.x) os[o] = 0.f;
         __syncthreads();
 
-        for (long long t0 = t_beg; t0 < t_end; t0 += CK) {
+        for (int i = 0; i < nsub; ++i) {
+            const long long t0 = t_beg + (long long)i * CK;
             const int cnt = (int)((t_end - t0) < CK ? (t_end - t0) : CK);
-            // stage K and V rows (zero beyond cnt so masked rows never carry NaN)
-            for (int c = tid; c < 2 * CK * CPR; c += blockDim.x) {
-                const int which = c / (CK * CPR);
-                const int j = (c / CPR) % CK;
-                const int q = c % CPR;
-                uint4 val = make_uint4(0u, 0u, 0u, 0u);
-                if (j < cnt) {
-                    const long long slot = (t0 + j) % vw.cap;
-                    const WT* src = reinterpret_cast<const WT*>(which ? vw.v : vw.k) + (long long)b * vw.sb +
-                                    (long long)g * vw.sh + slot * vw.st;
-                    val = ld_stream16(reinterpret_cast<const uint4*>(src) + q);
-                }
-                *reinterpret_cast<uint4*>((which ? vs : ks) + j * ROWB + q * 16) = val;
+            if (i + 1 < nsub) {
+                stage(i + 1);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
             }
             __syncthreads();
+            const unsigned char* ks = kvbuf + (i & 1) * BUFB;
+            const unsigned char* vs = ks + CK * ROWB;
             // scores
             for (int pr = tid; pr < grp * CK; pr += blockDim.x) {
                 const int h = pr / CK, j = pr % CK;
@@ -523,27 +563,52 @@ __device__ void attention_phase(const DraftParams& p, int l, int k, unsigned cha
         __syncthreads();
         if (s_last) {
             __threadfence();
-            // merge the S partials of (b, g) into OB[b, g*grp .. (g+1)*grp)
+            // merge the S partials of (b, g) into OB[b, g*grp .. (g+1)*grp):
+            // warp h finds head h's max and weights with its lanes spread over
+            // the partials; then every output sums the S weighted partials
+            // with independent loads in flight
             float* M = mrow;   // reuse: per-head max and total
             float* Lt = lrow;
-            if (tid < grp) {
+            float* es = reinterpret_cast<float*>(kvbuf);   // [S][grp] merge weights (K/V stage is free now)
+            const bool cached = S * grp <= (long long)(BUFB / sizeof(float));
+            if (warp < grp) {
+                const int h = warp;
                 float mm = -INFINITY;
-                for (long long q = 0; q < S; ++q) mm = fmaxf(mm, __ldcg(p.PART + (bg_base + q) * PSZ + tid));
+                for (long long q = lane; q < S; q += 32) mm = fmaxf(mm, __ldcg(p.PART + (bg_base + q) * PSZ + h));
+                mm = warp_max(mm);
                 float lt = 0.f;
-                for (long long q = 0; q < S; ++q) {
+                for (long long q = lane; q < S; q += 32) {
                     const float* pq = p.PART + (bg_base + q) * PSZ;
-                    lt += expf(__ldcg(pq + tid) - mm) * __ldcg(pq + grp + tid);
+                    const float e = expf(__ldcg(pq + h) - mm);
+                    if (cached) es[q * grp + h] = e;
+                    lt += e * __ldcg(pq + grp + h);
                 }
-                M[tid] = mm;
-                Lt[tid] = lt;
+                lt = warp_sum(lt);
+                if (lane == 0) {
+                    M[h] = mm;
+                    Lt[h] = lt;
+                }
             }
             __syncthreads();
             for (int o = tid; o < grp * HD; o += blockDim.x) {
                 const int h = o / HD;
                 float acc = 0.f;
-                for (long long q = 0; q < S; ++q) {
+                long long q = 0;
+                for (; q + 4 <= S; q += 4) {
+                    float v[4], e[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float* pq = p.PART + (bg_base + q + u) * PSZ;
+                        v[u] = __ldcg(pq + 2 * grp + o);
+                        e[u] = cached ? es[(q + u) * grp + h] : expf(__ldcg(pq + h) - M[h]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) acc = fmaf(e[u], v[u], acc);
+                }
+                for (; q < S; ++q) {
                     const float* pq = p.PART + (bg_base + q) * PSZ;
-                    acc += expf(__ldcg(pq + h) - M[h]) * __ldcg(pq + 2 * grp + o);
+                    const float e = cached ? es[q * grp + h] : expf(__ldcg(pq + h) - M[h]);
+                    acc = fmaf(e, __ldcg(pq + 2 * grp + o), acc);
                 }
                 p.OB[(long long)b * p.Hq * HD + (long long)g * grp * HD + o] = acc / Lt[h];
             }
