@@ -33,7 +33,7 @@ int num_sms() {
 }
 
 struct DraftLayout {
-    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ACT, end;
+    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, ACT, end;
     int kmax;
 };
 
@@ -63,7 +63,9 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     L.Y2 = off;      off = al256(off + (size_t)B * c->d_a * f);
     L.HN = off;      off = al256(off + (size_t)B * c->d_t * f);
     const size_t items = 2 * (size_t)kMaxGrid + (size_t)B * c->n_kv_heads;
-    L.PART = off;    off = al256(off + items * grp * (c->head_dim + 2) * f);
+    L.PART = off;    off = al256(off + items * attn_psz(grp, c->head_dim) * f);
+    L.ROPE = off;    off = al256(off + (size_t)MTP_MAX_VIEWS * (c->head_dim / 2) * sizeof(double));
+    L.ROPEQ = off;   off = al256(off + (size_t)B * MTP_MAX_VIEWS * (c->head_dim / 2) * 2 * f);
     L.ACT = off;     off = al256(off + (size_t)B * L.kmax * f);
     L.end = off;
     return L;
@@ -95,16 +97,18 @@ SampleLayout sample_layout(int B, int N) {
     return L;
 }
 
+// residual scratch plus staged activations of the GEMV phases
+size_t draft_smem_act(const mtp_config* c, int B, int act_smem) {
+    const size_t kmax = draft_kmax(c);
+    return (((size_t)c->d_a + 3) & ~(size_t)3) * sizeof(float) +
+           (act_smem ? (size_t)B * kmax : kmax) * sizeof(float);
+}
+
 size_t draft_smem(const mtp_config* c, int B, int act_smem) {
     const size_t wb = c->wdtype == MTP_DTYPE_BF16 ? 2 : 4;
     const size_t hd = c->head_dim, grp = c->n_q_heads / c->n_kv_heads;
-    const size_t ck = (size_t)attn_keys((int)hd, (int)wb);
-    // RoPE table, q / o / scores / row state, and two K + V sub-chunk buffers
-    const size_t attn = hd / 2 * sizeof(double) + (2 * grp * hd + grp * ck + 48) * sizeof(float) +
-                        2 * 2 * ck * (hd * wb + kAttnPad);
-    const size_t kmax = draft_kmax(c);
-    const size_t act = (((size_t)c->d_a + 3) & ~(size_t)3) * sizeof(float) +
-                       (act_smem ? (size_t)B * kmax : kmax) * sizeof(float);
+    const size_t attn = attn_smem((int)hd, (int)wb, (int)grp);
+    const size_t act = draft_smem_act(c, B, act_smem);
     return attn > act ? attn : act;
 }
 
@@ -252,6 +256,8 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     p.Y2 = reinterpret_cast<float*>(base + L.Y2);
     p.HN = reinterpret_cast<float*>(base + L.HN);
     p.PART = reinterpret_cast<float*>(base + L.PART);
+    p.ROPE = reinterpret_cast<double*>(base + L.ROPE);
+    p.ROPEQ = reinterpret_cast<float2*>(base + L.ROPEQ);
     p.ACT = reinterpret_cast<float*>(base + L.ACT);
     p.act_smem = act_smem;
     p.kmax = L.kmax;

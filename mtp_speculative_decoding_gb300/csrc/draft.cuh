@@ -8,10 +8,36 @@
 
 namespace mtp {
 
-// keys per staged attention sub-chunk: 64, or 32 for rows above 512 bytes
-__host__ __device__ constexpr int attn_keys(int hd, int wbytes) { return hd * wbytes <= 512 ? 64 : 32; }
-constexpr int kAttnPad = 16;       // bytes of padding per staged K/V row
 constexpr int kMaxGrid = 1024;     // upper bound on CTAs of the persistent grid
+
+// Shape of the attention phase for head dimension hd and element size wb.
+// A K or V row is split over LPR lanes, CPL 16-byte chunks each; a warp
+// reads KPW rows side by side and stages R keys (K and V rows, 4 KB) per
+// round in each of kAttnStages ring slots; HG query heads share a pass.
+struct AttnGeom {
+    int RB, CPR, LPR, CPL, KPW, EPC, DPL, R, RL, SB, HG;
+};
+__host__ __device__ constexpr AttnGeom attn_geom(int hd, int wb) {
+    const int RB = hd * wb, CPR = RB / 16, LPR = CPR < 32 ? CPR : 32, CPL = CPR / LPR, KPW = 32 / LPR;
+    const int EPC = 16 / wb, DPL = CPL * EPC, R = 2048 / RB > KPW ? 2048 / RB : KPW;
+    const int HG = 32 / DPL >= 4 ? 4 : (32 / DPL >= 1 ? 32 / DPL : 1);
+    return AttnGeom{RB, CPR, LPR, CPL, KPW, EPC, DPL, R, R / KPW, 2 * R * RB, HG};
+}
+constexpr int kAttnStages = 2;
+
+// floats per attention partial: o[grp][hd], m[grp], l[grp], padded to 16 bytes
+__host__ __device__ constexpr int attn_psz(int grp, int hd) { return (grp * (hd + 2) + 3) & ~3; }
+// float offsets from the rotated queries: warps' (m, l) at grp * hd, merge
+// weights and maxima after them, then (16-byte aligned) the per-warp round
+// probabilities and rescales
+__host__ __device__ constexpr int attn_pb_off(int grp, int hd, int hg) { return (grp * hd + 3 * kWarps * hg + hg + 3) & ~3; }
+// dynamic shared memory of the attention phase: the rings, then the above
+__host__ __device__ constexpr size_t attn_smem(int hd, int wb, int grp) {
+    return (size_t)kWarps * kAttnStages * attn_geom(hd, wb).SB +
+           ((size_t)attn_pb_off(grp, hd, attn_geom(hd, wb).HG) +
+            (size_t)kWarps * ((attn_geom(hd, wb).RL * attn_geom(hd, wb).HG + attn_geom(hd, wb).HG + 3) & ~3)) *
+               sizeof(float);
+}
 
 struct KView {
     const void* k;
@@ -52,6 +78,8 @@ struct DraftParams {
     unsigned long long* amax;    // [N * B] packed argmax keys
     float *XB, *XM, *QR, *OB, *YB, *MB, *Y2, *HN;
     float* PART;                 // attention partials
+    double* ROPE;                // [MTP_MAX_VIEWS][hd / 2] RoPE inverse frequencies (written at kernel start)
+    float2* ROPEQ;               // [B][MTP_MAX_VIEWS][hd / 2] (cos, sin) at the step's query position
     float* ACT;                  // [B, kmax] staged activations (global mode)
     int act_smem;                // 1: activations staged per CTA in shared memory
     int kmax;

@@ -49,6 +49,22 @@ template <> struct Chunk<uint16_t> {
         s = fmaf(bf16_hi(w.w), a1.w, s);
         return s;
     }
+    // dot with 8 values held in registers (constant indices only)
+    static __device__ __forceinline__ float dotr(const uint4& w, const float* a) {
+        float s = bf16_lo(w.x) * a[0];
+        s = fmaf(bf16_hi(w.x), a[1], s);
+        s = fmaf(bf16_lo(w.y), a[2], s);
+        s = fmaf(bf16_hi(w.y), a[3], s);
+        s = fmaf(bf16_lo(w.z), a[4], s);
+        s = fmaf(bf16_hi(w.z), a[5], s);
+        s = fmaf(bf16_lo(w.w), a[6], s);
+        s = fmaf(bf16_hi(w.w), a[7], s);
+        return s;
+    }
+    static __device__ __forceinline__ float elem(const uint4& w, int e) {
+        const uint32_t x = e < 2 ? w.x : e < 4 ? w.y : e < 6 ? w.z : w.w;
+        return (e & 1) ? bf16_hi(x) : bf16_lo(x);
+    }
 };
 template <> struct Chunk<float> {
     static constexpr int EPC = 4;
@@ -59,6 +75,16 @@ template <> struct Chunk<float> {
         s = fmaf(__uint_as_float(w.z), a0.z, s);
         s = fmaf(__uint_as_float(w.w), a0.w, s);
         return s;
+    }
+    static __device__ __forceinline__ float dotr(const uint4& w, const float* a) {
+        float s = __uint_as_float(w.x) * a[0];
+        s = fmaf(__uint_as_float(w.y), a[1], s);
+        s = fmaf(__uint_as_float(w.z), a[2], s);
+        s = fmaf(__uint_as_float(w.w), a[3], s);
+        return s;
+    }
+    static __device__ __forceinline__ float elem(const uint4& w, int e) {
+        return __uint_as_float(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
     }
 };
 
@@ -337,284 +363,570 @@ __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l,
 }
 
 // ---------------------------------------------------------------------------
-// attention (split-K over key ranges, online softmax, last-arriver merge)
+// attention: flash decoding, split over key ranges
 // ---------------------------------------------------------------------------
+// An item is (sequence b, KV head g, key range).  The CTA's warps take R-key
+// slices of the range round-robin; every warp streams its slices through a
+// private two-stage cp.async ring in shared memory and keeps its own
+// online-softmax state (m, l, o) for HG query heads of the group at a time,
+// with the lanes of one K/V row splitting the head dimension.  The warps are
+// merged in shared memory.  An (b, g) with one item writes OB directly;
+// otherwise every item stores its (o, m, l) in PART and counts itself in
+// att_cnt[b, g], and once the CTA has stored all its items it waits for the
+// count of each of them and merges the item's share of the outputs.  No CTA
+// waits before all its own items are stored, so the waits always end.
 
 __device__ __forceinline__ int view_lo(const KView& v, int kv_len) {
     return (v.window > 0 && kv_len > v.window) ? kv_len - v.window : 0;
 }
 
-template <typename WT, int HD>
-__device__ void attention_phase(const DraftParams& p, int l, int k, unsigned char* smem) {
-    constexpr int CK = attn_keys(HD, (int)sizeof(WT));      // keys per staged sub-chunk
-    constexpr int ROWB = HD * (int)sizeof(WT) + kAttnPad;   // bytes per staged row
-    constexpr int BUFB = 2 * CK * ROWB;                     // one K + V sub-chunk
-    constexpr int NCP = (2 * CK * (HD * (int)sizeof(WT) / 16) + kThreads - 1) / kThreads;  // copies per thread
-    constexpr int CPR = HD * (int)sizeof(WT) / 16;          // 16-byte chunks per row
-    constexpr int EPC = 16 / (int)sizeof(WT);
-    const KView& vw = p.views[p.blk[l].view];
-    const int grp = p.Hq / p.Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    double* invf = reinterpret_cast<double*>(smem);     // [HD/2] RoPE inverse frequencies
-    float* qs = reinterpret_cast<float*>(invf + HD / 2);  // [grp][HD]
-    float* os = qs + grp * HD;                           // [grp][HD]
-    float* sc = os + grp * HD;                           // [grp][CK]
-    float* mrow = sc + grp * CK;                         // [grp]
-    float* lrow = mrow + 16;                             // [grp]
-    float* arow = lrow + 16;                             // [grp]
-    unsigned char* kvbuf = reinterpret_cast<unsigned char*>(arow + 16);  // 2 x (K rows, V rows)
-    __shared__ int s_last;
-
-    // RoPE inverse frequencies, once per phase (fp64 is scarce on this part)
-    {
-        const double ltheta = log((double)vw.theta);
-        for (int i = tid; i < HD / 2; i += blockDim.x) invf[i] = exp(-2.0 * (double)i / (double)HD * ltheta);
-        __syncthreads();
-    }
+// Item decomposition of the attention phases, per view (the sequence
+// lengths are fixed for a launch): keys per item, number of items, and per
+// sequence the first item and the items per KV head.
+struct AttnTab {
+    int kpi[MTP_MAX_VIEWS], n_items[MTP_MAX_VIEWS];
+    int first[MTP_MAX_VIEWS][MTP_MAX_BATCH], per_head[MTP_MAX_VIEWS][MTP_MAX_BATCH];
+};
+// thread v < MTP_MAX_VIEWS fills view v (R: keys per warp slice)
+__device__ __forceinline__ void attn_tab_fill(const DraftParams& p, const int* kv, int R, AttnTab& t) {
+    const int v = threadIdx.x;
+    if (v >= MTP_MAX_VIEWS) return;
+    const KView& vw = p.views[v];
     long long total = 0;
-    for (int b = 0; b < p.B; ++b) total += (long long)(p.kv_len[b] - view_lo(vw, p.kv_len[b])) * p.Hkv;
-    // keys per item: about one item per CTA (two when every CTA would get
-    // more than 512 keys, to even out ragged sequence lengths)
+    for (int b = 0; b < p.B; ++b) total += (long long)(kv[b] - view_lo(vw, kv[b])) * p.Hkv;
+    // about one item per CTA (two when every CTA would get more than 512
+    // keys, to even out ragged sequence lengths), at least one slice per warp
     const long long target = (total / gridDim.x <= 512) ? gridDim.x : 2LL * gridDim.x;
     long long kpi = (total + target - 1) / target;
-    kpi = ((kpi + CK - 1) / CK) * CK;
-    if (kpi < CK) kpi = CK;
-    long long n_items = 0;
+    if (kpi < (long long)kWarps * R) kpi = (long long)kWarps * R;
+    kpi = ((kpi + R - 1) / R) * R;
+    const int k32 = (int)kpi;
+    int n = 0;
     for (int b = 0; b < p.B; ++b) {
-        const long long n = p.kv_len[b] - view_lo(vw, p.kv_len[b]);
-        n_items += p.Hkv * ((n + kpi - 1) / kpi);
+        const int S = (kv[b] - view_lo(vw, kv[b]) + k32 - 1) / k32;
+        t.first[v][b] = n;
+        t.per_head[v][b] = S;
+        n += p.Hkv * S;
     }
-    const int PSZ = grp * (HD + 2);  // floats per partial: m[grp], l[grp], o[grp][HD]
+    t.kpi[v] = k32;
+    t.n_items[v] = n;
+}
 
-    for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
-        // item -> (b, g, s)
-        int b = 0;
-        long long base = 0, S = 1;
-        for (b = 0; b < p.B; ++b) {
-            const long long n = p.kv_len[b] - view_lo(vw, p.kv_len[b]);
-            S = (n + kpi - 1) / kpi;
-            if (it < base + p.Hkv * S) break;
-            base += p.Hkv * S;
+struct AttnItem {
+    int b, g, s, S, bg_base, t_beg, t_end;
+};
+__device__ __forceinline__ AttnItem attn_item(const DraftParams& p, const KView& vw, const int* kv,
+                                              const AttnTab& t, int v, int it) {
+    AttnItem r;
+    int b = 0;
+    while (b + 1 < p.B && t.first[v][b + 1] <= it) ++b;
+    const int S = t.per_head[v][b], rel = it - t.first[v][b];
+    r.b = b;
+    r.S = S;
+    r.g = rel / S;
+    r.s = rel - r.g * S;
+    r.bg_base = t.first[v][b] + r.g * S;
+    r.t_beg = view_lo(vw, kv[b]) + r.s * t.kpi[v];
+    r.t_end = r.t_beg + t.kpi[v] < kv[b] ? r.t_beg + t.kpi[v] : kv[b];
+    return r;
+}
+
+// Sum of NV per-lane values over the LPR lanes of a row group, transposed:
+// afterwards value idx = (lane % LPR) >> log2(LPR / NV) holds the group's
+// total (high index bits from the high lane bits).  NV <= LPR, powers of 2.
+template <int NV, int LPR>
+__device__ __forceinline__ float transpose_sum(float (&v)[NV]) {
+    static_assert(NV <= LPR, "transpose_sum needs NV <= LPR");
+    const int lane = threadIdx.x & 31;
+    float x[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) x[i] = v[i];
+    int n = NV;
+#pragma unroll
+    for (int off = LPR / 2; off >= LPR / NV; off >>= 1) {
+        n >>= 1;
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < NV / 2; ++i) {
+            if (i < n) {
+                const float send = up ? x[i] : x[i + n];
+                const float keep = up ? x[i + n] : x[i];
+                x[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
         }
-        const int g = (int)((it - base) / S);
-        const int s = (int)((it - base) % S);
-        const long long bg_base = base + (long long)g * S;
-        const int kv_len = p.kv_len[b];
-        const int lo = view_lo(vw, kv_len);
-        const long long t_beg = lo + (long long)s * kpi;
-        const long long t_end = (t_beg + kpi < kv_len) ? t_beg + kpi : kv_len;
+    }
+    float r = x[0];
+#pragma unroll
+    for (int off = LPR / NV / 2; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+    return r;
+}
 
-        // K/V sub-chunks of CK keys go to shared memory through cp.async, two
-        // buffers deep: sub-chunk i + 1 is in flight while i is used.  Rows
-        // past the range are zero-filled so they never carry NaN.
+// Waits (thread 0) until *cnt reaches target; false when the time limit
+// passed or another CTA reported an error.  Called by the whole CTA.
+__device__ __forceinline__ bool count_wait(const unsigned int* cnt, unsigned int target, WsHeader* hdr,
+                                           unsigned long long limit_ns) {
+    __shared__ int s_ok;
+    if (threadIdx.x == 0) {
+        const unsigned long long t0 = global_ns();
+        int ok = 1;
+        unsigned int spins = 0;
+        while (ld_acquire(cnt) < target) {
+            if (ld_relaxed(&hdr->status) != 0) { ok = 0; break; }
+            if ((++spins & 63u) == 0 && global_ns() - t0 > limit_ns) {
+                atomicCAS(&hdr->status, 0, MTP_ERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+// release-add: the CTA's earlier writes (ordered by the preceding CTA
+// barrier) become visible at GPU scope before the count
+__device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+template <typename WT, int HD>
+__device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem, const int* kv, const AttnTab& tab) {
+    constexpr AttnGeom G = attn_geom(HD, (int)sizeof(WT));
+    constexpr int RB = G.RB, CPR = G.CPR, LPR = G.LPR, CPL = G.CPL, KPW = G.KPW, EPC = G.EPC, DPL = G.DPL;
+    constexpr int R = G.R, RL = G.RL, SB = G.SB, HG = G.HG, NST = kAttnStages;
+    constexpr int RING = kWarps * NST * SB;
+    constexpr int CPT = SB / 16 / 32;   // cp.async chunks per lane and stage
+    constexpr int NV = RL * HG;         // scores per lane and round
+    // one K/V row per warp and NV <= 32: scores summed transposed, softmax on
+    // one lane per score, probabilities broadcast through shared memory
+    constexpr bool TR = KPW == 1 && NV <= LPR;
+    constexpr int SH = TR ? 32 / NV : 1;   // lanes per score in the transposed layout
+    static_assert(SB % (16 * 32) == 0 && R % KPW == 0, "attention stage shape");
+    const int view = p.blk[l].view;
+    const KView& vw = p.views[view];
+    const int grp = p.Hq / p.Hkv;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lg = lane / LPR, lr = lane % LPR;   // row group of the lane, lane within the row
+    const int PSZ = attn_psz(grp, HD);
+
+    unsigned char* myring = smem + warp * NST * SB;                   // [NST][SB] of this warp
+    float* wo = reinterpret_cast<float*>(smem);                        // [kWarps][HG][HD], aliases the rings
+    float* qs = reinterpret_cast<float*>(smem + RING);                 // [grp][HD] rotated queries
+    float* wml = qs + grp * HD;                                        // [kWarps][HG][2] warp (m, l)
+    float* wex = wml + kWarps * HG * 2;                                // [kWarps][HG] merge weights, [HG] maxima
+    constexpr int PBS = (NV + HG + 3) & ~3;                            // floats per warp, 16-byte multiple
+    float* wpb = qs + attn_pb_off(grp, HD, HG);                        // [kWarps][PBS] probabilities, rescales
+    float* mypb = wpb + warp * PBS;
+    const int n_items = tab.n_items[view];
+    bool any_split = false;
+
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const AttnItem A = attn_item(p, vw, kv, tab, view, it);
+        const int b = A.b, g = A.g;
+        const int t_beg = A.t_beg, t_end = A.t_end;
+        const int nrounds = (t_end - t_beg + kWarps * R - 1) / (kWarps * R);
         const WT* kbase = reinterpret_cast<const WT*>(vw.k) + (long long)b * vw.sb + (long long)g * vw.sh;
         const WT* vbase = reinterpret_cast<const WT*>(vw.v) + (long long)b * vw.sb + (long long)g * vw.sh;
-        const int nsub = (int)((t_end - t_beg + CK - 1) / CK);
-        auto stage = [&](int i) {
-            const long long t0 = t_beg + (long long)i * CK;
-            const int cnt = (int)((t_end - t0) < CK ? (t_end - t0) : CK);
-            const int s0 = (int)(t0 % vw.cap);
-            unsigned char* buf = kvbuf + (i & 1) * BUFB;
+
+        // keys of round rd for this warp: [t0, t0 + cnt)
+        auto slice_cnt = [&](int rd, int& t0) {
+            t0 = t_beg + (rd * kWarps + warp) * R;
+            const int c = t_end - t0;
+            return rd < nrounds ? (c < 0 ? 0 : (c < R ? c : R)) : 0;
+        };
+        // one commit group per round and warp (empty past the range)
+        auto issue = [&](int rd) {
+            int t0;
+            const int cnt = slice_cnt(rd, t0);
+            if (cnt > 0) {
+                unsigned char* buf = myring + (rd % NST) * SB;
+                const int s0 = t0 % vw.cap;
 #pragma unroll
-            for (int u = 0; u < NCP; ++u) {
-                const int c = tid + u * kThreads;
-                if (c < 2 * CK * CPR) {
-                    const int which = c / (CK * CPR);
-                    const int j = (c / CPR) % CK;
+                for (int u = 0; u < CPT; ++u) {
+                    const int c = lane + 32 * u;   // chunk of [K rows | V rows]
+                    const int which = c / (R * CPR);
+                    const int r = (c / CPR) % R;
                     const int q = c % CPR;
-                    unsigned char* dst = buf + which * CK * ROWB + j * ROWB + q * 16;
-                    if (j < cnt) {
-                        int slot = s0 + j;
+                    if (r < cnt) {
+                        int slot = s0 + r;
                         if (slot >= vw.cap) slot %= vw.cap;
-                        cp_async16(dst, (which ? vbase : kbase) + (long long)slot * vw.st + q * EPC);
-                    } else {
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+                        cp_async16(buf + which * R * RB + r * RB + q * 16,
+                                   (which ? vbase : kbase) + (long long)slot * vw.st + q * EPC);
                     }
                 }
             }
             cp_async_commit();
         };
-        stage(0);
 
-        // q-norm + RoPE for the group's heads (warp h handles head h), scaled by attn_scale
-        if (warp < grp) {
-            const int h = g * grp + warp;
-            const float* qraw = p.QR + (long long)b * p.Hq * HD + (long long)h * HD;
-            float ss = 0.f;
-            for (int d = lane; d < HD; d += 32) {
-                const float v = __ldcg(qraw + d);
-                qs[warp * HD + d] = v;
-                ss = fmaf(v, v, ss);
-            }
-            ss = warp_sum(ss);
-            const float r = 1.0f / sqrtf(ss / (float)HD + p.eps);
-            const float* gq = p.blk[l].q_norm;
-            __syncwarp();
-            const double pos = (double)kv_len + (double)k;
-            constexpr int PPL = HD / 64 > 0 ? HD / 64 : 1;  // rotation pairs per lane
-            float ra[PPL], rb[PPL];
+        for (int h0 = 0; h0 < grp; h0 += HG) {
+            const int hn = grp - h0 < HG ? grp - h0 : HG;
+            if (h0 == 0) {
+                issue(0);
+                // q-norm + RoPE of the group's heads (warp h: head g * grp + h),
+                // scaled by attn_scale; (cos, sin) of the position come from
+                // the step's table
+                if (warp < grp) {
+                    constexpr int NQ = (HD / 8 + 31) / 32;   // float4 pairs per lane
+                    const float* qraw = p.QR + ((long long)b * p.Hq + (long long)g * grp + warp) * HD;
+                    const float* gq = p.blk[l].q_norm;
+                    const float4* cs = reinterpret_cast<const float4*>(
+                        p.ROPEQ + ((long long)b * MTP_MAX_VIEWS + view) * (HD / 2));
+                    float4 qa[NQ], qb[NQ], ga[NQ], gb[NQ], c0[NQ], c1[NQ];
+                    float ss = 0.f;
 #pragma unroll
-            for (int m = 0; m < PPL; ++m) {
-                const int i = lane + 32 * m;
-                if (i < HD / 2) {
-                    const float a = qs[warp * HD + i] * r * __ldg(gq + i);
-                    const float c = qs[warp * HD + i + HD / 2] * r * __ldg(gq + i + HD / 2);
-                    // angle pos * theta^(-2i/HD) in fp64, reduced to [-pi, pi] before the fp32 sin/cos
-                    double ang = pos * invf[i];
-                    ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
-                    float sn, cs;
-                    sincosf((float)ang, &sn, &cs);
-                    ra[m] = (a * cs - c * sn) * p.attn_scale;
-                    rb[m] = (a * sn + c * cs) * p.attn_scale;
-                }
-            }
-            __syncwarp();
+                    for (int u = 0; u < NQ; ++u) {
+                        const int i4 = lane + 32 * u;
+                        if (i4 < HD / 8) {
+                            qa[u] = __ldcg(reinterpret_cast<const float4*>(qraw) + i4);
+                            qb[u] = __ldcg(reinterpret_cast<const float4*>(qraw + HD / 2) + i4);
+                            ga[u] = __ldg(reinterpret_cast<const float4*>(gq) + i4);
+                            gb[u] = __ldg(reinterpret_cast<const float4*>(gq + HD / 2) + i4);
+                            c0[u] = __ldcg(cs + 2 * i4);
+                            c1[u] = __ldcg(cs + 2 * i4 + 1);
+                            ss += qa[u].x * qa[u].x + qa[u].y * qa[u].y + qa[u].z * qa[u].z + qa[u].w * qa[u].w;
+                            ss += qb[u].x * qb[u].x + qb[u].y * qb[u].y + qb[u].z * qb[u].z + qb[u].w * qb[u].w;
+                        }
+                    }
+                    ss = warp_sum(ss);
+                    const float rn = 1.0f / sqrtf(ss / (float)HD + p.eps);
+                    float* qo = qs + warp * HD;
 #pragma unroll
-            for (int m = 0; m < PPL; ++m) {
-                const int i = lane + 32 * m;
-                if (i < HD / 2) {
-                    qs[warp * HD + i] = ra[m];
-                    qs[warp * HD + i + HD / 2] = rb[m];
+                    for (int u = 0; u < NQ; ++u) {
+                        const int i4 = lane + 32 * u;
+                        if (i4 < HD / 8) {
+                            const float av[4] = {qa[u].x, qa[u].y, qa[u].z, qa[u].w};
+                            const float bv[4] = {qb[u].x, qb[u].y, qb[u].z, qb[u].w};
+                            const float gav[4] = {ga[u].x, ga[u].y, ga[u].z, ga[u].w};
+                            const float gbv[4] = {gb[u].x, gb[u].y, gb[u].z, gb[u].w};
+                            const float cv[4] = {c0[u].x, c0[u].z, c1[u].x, c1[u].z};
+                            const float sv[4] = {c0[u].y, c0[u].w, c1[u].y, c1[u].w};
+                            float ra[4], rb[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float a = av[e] * rn * gav[e];
+                                const float c = bv[e] * rn * gbv[e];
+                                ra[e] = (a * cv[e] - c * sv[e]) * p.attn_scale;
+                                rb[e] = (a * sv[e] + c * cv[e]) * p.attn_scale;
+                            }
+                            reinterpret_cast<float4*>(qo)[i4] = make_float4(ra[0], ra[1], ra[2], ra[3]);
+                            reinterpret_cast<float4*>(qo + HD / 2)[i4] = make_float4(rb[0], rb[1], rb[2], rb[3]);
+                        }
+                    }
                 }
-            }
-            if (lane == 0) { mrow[warp] = -INFINITY; lrow[warp] = 0.f; }
-        }
-        for (int o = tid; o < grp * HD; o += blockDim.x) os[o] = 0.f;
-        __syncthreads();
-
-        for (int i = 0; i < nsub; ++i) {
-            const long long t0 = t_beg + (long long)i * CK;
-            const int cnt = (int)((t_end - t0) < CK ? (t_end - t0) : CK);
-            if (i + 1 < nsub) {
-                stage(i + 1);
-                cp_async_wait<1>();
+                __syncthreads();
             } else {
-                cp_async_wait<0>();
+                __syncthreads();   // the previous pass's warp merge used the rings
+                issue(0);
             }
-            __syncthreads();
-            const unsigned char* ks = kvbuf + (i & 1) * BUFB;
-            const unsigned char* vs = ks + CK * ROWB;
-            // scores
-            for (int pr = tid; pr < grp * CK; pr += blockDim.x) {
-                const int h = pr / CK, j = pr % CK;
-                float sv = -INFINITY;
-                if (j < cnt) {
-                    const float* qh = qs + h * HD;
-                    const unsigned char* kr = ks + j * ROWB;
-                    float acc = 0.f;
-#pragma unroll 4
-                    for (int q = 0; q < CPR; ++q) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(kr + q * 16);
-                        acc += Chunk<WT>::dot(w, qh + q * EPC);
+
+            // this lane's slice of the pass's queries
+            float qr[HG][DPL];
+#pragma unroll
+            for (int hh = 0; hh < HG; ++hh)
+#pragma unroll
+                for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                    for (int e4 = 0; e4 < EPC; e4 += 4) {
+                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (hh < hn) v = *reinterpret_cast<const float4*>(qs + (h0 + hh) * HD + (c * LPR + lr) * EPC + e4);
+                        qr[hh][c * EPC + e4 + 0] = v.x;
+                        qr[hh][c * EPC + e4 + 1] = v.y;
+                        qr[hh][c * EPC + e4 + 2] = v.z;
+                        qr[hh][c * EPC + e4 + 3] = v.w;
                     }
-                    sv = acc;
-                }
-                sc[h * CK + j] = sv;
+            // online-softmax state: o for all HG heads on every lane; (m, l)
+            // per head on every lane, or (transposed) of the lane's own head
+            float o[HG][DPL];
+            float m[TR ? 1 : HG], ls[TR ? 1 : HG];
+#pragma unroll
+            for (int hh = 0; hh < HG; ++hh)
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) o[hh][d] = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < (TR ? 1 : HG); ++hh) {
+                m[hh] = -INFINITY;
+                ls[hh] = 0.f;
             }
-            __syncthreads();
-            // online softmax update (warp h owns head h)
-            if (warp < grp) {
-                float mx = -INFINITY;
-                for (int j = lane; j < CK; j += 32) mx = fmaxf(mx, sc[warp * CK + j]);
-                mx = warp_max(mx);
-                const float m_old = mrow[warp];
-                const float m_new = fmaxf(m_old, mx);
-                const float alpha = expf(m_old - m_new);
-                float ls = 0.f;
-                for (int j = lane; j < CK; j += 32) {
-                    const float e = j < cnt ? expf(sc[warp * CK + j] - m_new) : 0.f;
-                    sc[warp * CK + j] = e;
-                    ls += e;
-                }
-                ls = warp_sum(ls);
+
+            for (int i = 0; i < nrounds; ++i) {
+                issue(i + 1);
+                cp_async_wait<1>();
                 __syncwarp();
-                if (lane == 0) {
-                    mrow[warp] = m_new;
-                    lrow[warp] = lrow[warp] * alpha + ls;
-                    arow[warp] = alpha;
+                int t0;
+                const int cnt = slice_cnt(i, t0);
+                if (cnt > 0) {
+                    const unsigned char* kb = myring + (i % NST) * SB;
+                    const unsigned char* vb = kb + R * RB;
+                    float sc[NV];   // [RL][HG]
+#pragma unroll
+                    for (int x = 0; x < NV; ++x) sc[x] = 0.f;
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                        for (int ii = 0; ii < RL; ++ii) {
+                            const uint4 w = *reinterpret_cast<const uint4*>(kb + (lg + KPW * ii) * RB + (c * LPR + lr) * 16);
+#pragma unroll
+                            for (int hh = 0; hh < HG; ++hh) sc[ii * HG + hh] += Chunk<WT>::dotr(w, &qr[hh][c * EPC]);
+                        }
+                    float pr[NV];   // probabilities of the round, [RL][HG]
+                    float al[HG];   // rescale of the running o per head
+                    if constexpr (TR) {
+                        // lane holds score x = lane / SH: key x / HG, head x % HG
+                        const float sx = transpose_sum<NV, 32>(sc);
+                        const int x = lane / SH, xh = x % HG;
+                        const bool valid = x / HG < cnt;
+                        float mx = valid ? sx : -INFINITY;
+#pragma unroll
+                        for (int off = HG * SH; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                        const float mn = fmaxf(m[0], mx);
+                        const float mu = mn == -INFINITY ? 0.f : mn;
+                        const float a = expf(m[0] - mu);
+                        float pe = valid ? expf(sx - mu) : 0.f;
+                        float ps = pe;
+#pragma unroll
+                        for (int off = HG * SH; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+                        ls[0] = ls[0] * a + ps;
+                        m[0] = mn;
+                        if (lane % SH == 0) {
+                            mypb[x] = pe;
+                            if (x < HG) mypb[NV + x] = a;
+                        }
+                        __syncwarp();
+                        if constexpr (NV % 4 == 0) {
+#pragma unroll
+                            for (int x4 = 0; x4 < NV; x4 += 4) {
+                                const float4 v = *reinterpret_cast<const float4*>(mypb + x4);
+                                pr[x4] = v.x;
+                                pr[x4 + 1] = v.y;
+                                pr[x4 + 2] = v.z;
+                                pr[x4 + 3] = v.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int x4 = 0; x4 < NV; ++x4) pr[x4] = mypb[x4];
+                        }
+#pragma unroll
+                        for (int hh = 0; hh < HG; ++hh) al[hh] = mypb[NV + hh];
+                        __syncwarp();
+                    } else {
+#pragma unroll
+                        for (int off = 1; off < LPR; off <<= 1)
+#pragma unroll
+                            for (int x = 0; x < NV; ++x) sc[x] += __shfl_xor_sync(0xffffffffu, sc[x], off);
+#pragma unroll
+                        for (int hh = 0; hh < HG; ++hh) {
+                            float mx = -INFINITY;
+#pragma unroll
+                            for (int ii = 0; ii < RL; ++ii)
+                                if (lg + KPW * ii < cnt) mx = fmaxf(mx, sc[ii * HG + hh]);
+                            const float mn = fmaxf(m[hh], mx);
+                            const float mu = mn == -INFINITY ? 0.f : mn;
+                            al[hh] = expf(m[hh] - mu);
+                            ls[hh] *= al[hh];
+#pragma unroll
+                            for (int ii = 0; ii < RL; ++ii) {
+                                const float pe = lg + KPW * ii < cnt ? expf(sc[ii * HG + hh] - mu) : 0.f;
+                                pr[ii * HG + hh] = pe;
+                                ls[hh] += pe;
+                            }
+                            m[hh] = mn;
+                        }
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < HG; ++hh)
+#pragma unroll
+                        for (int d = 0; d < DPL; ++d) o[hh][d] *= al[hh];
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                        for (int ii = 0; ii < RL; ++ii) {
+                            if (lg + KPW * ii < cnt) {
+                                const uint4 w = *reinterpret_cast<const uint4*>(vb + (lg + KPW * ii) * RB + (c * LPR + lr) * 16);
+#pragma unroll
+                                for (int e = 0; e < EPC; ++e) {
+                                    const float v = Chunk<WT>::elem(w, e);
+#pragma unroll
+                                    for (int hh = 0; hh < HG; ++hh)
+                                        o[hh][c * EPC + e] = fmaf(pr[ii * HG + hh], v, o[hh][c * EPC + e]);
+                                }
+                            }
+                        }
+                }
+                __syncwarp();
+            }
+
+            // (m, l) of head hh for the warp state: transposed, from the lane
+            // holding key 0 of head hh
+            float mw[HG], lw[HG];
+#pragma unroll
+            for (int hh = 0; hh < HG; ++hh) {
+                if constexpr (TR) {
+                    mw[hh] = __shfl_sync(0xffffffffu, m[0], hh * SH);
+                    lw[hh] = __shfl_sync(0xffffffffu, ls[0], hh * SH);
+                } else {
+                    mw[hh] = m[hh];
+                    lw[hh] = ls[hh];
+                }
+            }
+            // merge the row groups of the warp (rows of one round side by side)
+#pragma unroll
+            for (int off = LPR; off < 32; off <<= 1)
+#pragma unroll
+                for (int hh = 0; hh < HG; ++hh) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, mw[hh], off);
+                    const float l2 = __shfl_xor_sync(0xffffffffu, lw[hh], off);
+                    const float mn = fmaxf(mw[hh], m2);
+                    const float mu = mn == -INFINITY ? 0.f : mn;
+                    const float a1 = expf(mw[hh] - mu), a2 = expf(m2 - mu);
+                    lw[hh] = lw[hh] * a1 + l2 * a2;
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d) {
+                        const float o2 = __shfl_xor_sync(0xffffffffu, o[hh][d], off);
+                        o[hh][d] = o[hh][d] * a1 + o2 * a2;
+                    }
+                    mw[hh] = mn;
+                }
+            __syncthreads();   // every warp is done with its ring
+            if (lg == 0) {
+#pragma unroll
+                for (int hh = 0; hh < HG; ++hh) {
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                        for (int e4 = 0; e4 < EPC; e4 += 4)
+                            *reinterpret_cast<float4*>(wo + (warp * HG + hh) * HD + (c * LPR + lr) * EPC + e4) =
+                                make_float4(o[hh][c * EPC + e4], o[hh][c * EPC + e4 + 1], o[hh][c * EPC + e4 + 2],
+                                            o[hh][c * EPC + e4 + 3]);
+                    if (lr == 0) {
+                        wml[(warp * HG + hh) * 2] = mw[hh];
+                        wml[(warp * HG + hh) * 2 + 1] = lw[hh];
+                    }
                 }
             }
             __syncthreads();
-            // o = o * alpha + P V
-            for (int o = tid; o < grp * HD; o += blockDim.x) {
-                const int h = o / HD, d = o % HD;
-                float acc = os[o] * arow[h];
-                const float* ph = sc + h * CK;
-                for (int j = 0; j < cnt; ++j) {
-                    const WT* vr = reinterpret_cast<const WT*>(vs + j * ROWB);
-                    float vv;
-                    if (sizeof(WT) == 2) vv = bf16_to_f32(reinterpret_cast<const uint16_t*>(vr)[d]);
-                    else vv = reinterpret_cast<const float*>(vr)[d];
-                    acc = fmaf(ph[j], vv, acc);
-                }
-                os[o] = acc;
+            // CTA merge over the warps: weights per (warp, head), then the outputs
+            if (tid < kWarps * HG) {
+                const int hh = tid % HG;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * HG + hh) * 2]);
+                wex[tid] = expf(wml[tid * 2] - (M == -INFINITY ? 0.f : M));
+                if (tid < HG) wex[kWarps * HG + tid] = M;
             }
             __syncthreads();
+            for (int oi = tid; oi < hn * HD; oi += kThreads) {
+                const int hh = oi / HD, d = oi % HD;
+                float Ls = 0.f, O = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const float e = wex[w * HG + hh];
+                    Ls = fmaf(e, wml[(w * HG + hh) * 2 + 1], Ls);
+                    O = fmaf(e, wo[(w * HG + hh) * HD + d], O);
+                }
+                const int h = h0 + hh;
+                if (A.S == 1) {
+                    p.OB[((long long)b * p.Hq + (long long)g * grp + h) * HD + d] = O / Ls;
+                } else {
+                    float* part = p.PART + (long long)it * PSZ;
+                    part[h * HD + d] = O;
+                    if (d == 0) {
+                        part[grp * HD + h] = wex[kWarps * HG + hh];
+                        part[grp * HD + grp + h] = Ls;
+                    }
+                }
+            }
         }
 
-        // partial (m, l, o) of this item
-        float* part = p.PART + it * PSZ;
-        for (int h = tid; h < grp; h += blockDim.x) { part[h] = mrow[h]; part[grp + h] = lrow[h]; }
-        for (int o = tid; o < grp * HD; o += blockDim.x) part[2 * grp + o] = os[o];
-        __threadfence();
         __syncthreads();
-        if (tid == 0) s_last = (atomicAdd(p.att_cnt + b * p.Hkv + g, 1u) == (unsigned)(S - 1));
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            // merge the S partials of (b, g) into OB[b, g*grp .. (g+1)*grp):
-            // warp h finds head h's max and weights with its lanes spread over
-            // the partials; then every output sums the S weighted partials
-            // with independent loads in flight
-            float* M = mrow;   // reuse: per-head max and total
-            float* Lt = lrow;
-            float* es = reinterpret_cast<float*>(kvbuf);   // [S][grp] merge weights (K/V stage is free now)
-            const bool cached = S * grp <= (long long)(BUFB / sizeof(float));
-            if (warp < grp) {
-                const int h = warp;
-                float mm = -INFINITY;
-                for (long long q = lane; q < S; q += 32) mm = fmaxf(mm, __ldcg(p.PART + (bg_base + q) * PSZ + h));
-                mm = warp_max(mm);
-                float lt = 0.f;
-                for (long long q = lane; q < S; q += 32) {
-                    const float* pq = p.PART + (bg_base + q) * PSZ;
-                    const float e = expf(__ldcg(pq + h) - mm);
-                    if (cached) es[q * grp + h] = e;
-                    lt += e * __ldcg(pq + grp + h);
-                }
-                lt = warp_sum(lt);
-                if (lane == 0) {
-                    M[h] = mm;
-                    Lt[h] = lt;
-                }
-            }
-            __syncthreads();
-            for (int o = tid; o < grp * HD; o += blockDim.x) {
-                const int h = o / HD;
-                float acc = 0.f;
-                long long q = 0;
-                for (; q + 4 <= S; q += 4) {
-                    float v[4], e[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float* pq = p.PART + (bg_base + q + u) * PSZ;
-                        v[u] = __ldcg(pq + 2 * grp + o);
-                        e[u] = cached ? es[(q + u) * grp + h] : expf(__ldcg(pq + h) - M[h]);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) acc = fmaf(e[u], v[u], acc);
-                }
-                for (; q < S; ++q) {
-                    const float* pq = p.PART + (bg_base + q) * PSZ;
-                    const float e = cached ? es[q * grp + h] : expf(__ldcg(pq + h) - M[h]);
-                    acc = fmaf(e, __ldcg(pq + 2 * grp + o), acc);
-                }
-                p.OB[(long long)b * p.Hq * HD + (long long)g * grp * HD + o] = acc / Lt[h];
-            }
-            if (tid == 0) p.att_cnt[b * p.Hkv + g] = 0u;
-            __syncthreads();
+        if (A.S > 1) {
+            any_split = true;
+            if (tid == 0) red_release_add(p.att_cnt + b * p.Hkv + g, 1u);
         }
+    }
+    if (!any_split) return true;
+
+    // merge: item s of an (b, g) with S items combines share s of the grp * HD
+    // outputs over all S partials (lanes over partials, warps over outputs,
+    // up to MJ outputs of a warp with their loads in flight together)
+    constexpr int MJ = 4;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const AttnItem A = attn_item(p, vw, kv, tab, view, it);
+        if (A.S == 1) continue;
+        if (!count_wait(p.att_cnt + A.b * p.Hkv + A.g, (unsigned int)A.S, p.hdr, p.timeout_ns)) return false;
+        const int no = grp * HD;
+        const int per = (no + A.S - 1) / A.S;
+        const int o0 = A.s * per, o1 = o0 + per < no ? o0 + per : no;
+        const float* src = p.PART + (long long)A.bg_base * PSZ;
+        float* dst = p.OB + ((long long)A.b * p.Hq + (long long)A.g * grp) * HD;
+        for (int j0 = o0 + warp; j0 < o1; j0 += MJ * kWarps) {
+            float mm[MJ], ll[MJ], oo[MJ];
+#pragma unroll
+            for (int u = 0; u < MJ; ++u) { mm[u] = -INFINITY; ll[u] = 0.f; oo[u] = 0.f; }
+            for (int q = lane; q < A.S; q += 32) {
+                const float* pq = src + (long long)q * PSZ;
+                float mq[MJ], lq[MJ], oq[MJ];
+#pragma unroll
+                for (int u = 0; u < MJ; ++u) {
+                    const int j = j0 + u * kWarps;
+                    mq[u] = -INFINITY; lq[u] = 0.f; oq[u] = 0.f;
+                    if (j < o1) {
+                        mq[u] = __ldcg(pq + grp * HD + j / HD);
+                        lq[u] = __ldcg(pq + grp * HD + grp + j / HD);
+                        oq[u] = __ldcg(pq + j);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < MJ; ++u) {
+                    const float mn = fmaxf(mm[u], mq[u]);
+                    const float mu = mn == -INFINITY ? 0.f : mn;
+                    const float a1 = expf(mm[u] - mu), a2 = expf(mq[u] - mu);
+                    ll[u] = ll[u] * a1 + lq[u] * a2;
+                    oo[u] = oo[u] * a1 + oq[u] * a2;
+                    mm[u] = mn;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < MJ; ++u) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, mm[u], off);
+                    const float l2 = __shfl_xor_sync(0xffffffffu, ll[u], off);
+                    const float o2 = __shfl_xor_sync(0xffffffffu, oo[u], off);
+                    const float mn = fmaxf(mm[u], m2);
+                    const float mu = mn == -INFINITY ? 0.f : mn;
+                    const float a1 = expf(mm[u] - mu), a2 = expf(m2 - mu);
+                    ll[u] = ll[u] * a1 + l2 * a2;
+                    oo[u] = oo[u] * a1 + o2 * a2;
+                    mm[u] = mn;
+                }
+                const int j = j0 + u * kWarps;
+                if (lane == 0 && j < o1) dst[j] = oo[u] / ll[u];
+            }
+        }
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// LM head over the tied token table with the argmax folded in: per lane,
+// per CTA in shared memory, then one atomic per sequence.
+template <typename WT>
+__device__ __forceinline__ void head_phase(const DraftParams& p, int k, const float* a, int lda,
+                                           unsigned long long (*head_best)[32]) {
+    HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull};
+    gemv<WT, 8, false>(reinterpret_cast<const WT*>(p.tok_embd), nullptr, p.V, p.d_t, a, lda, p.B, e);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int c0 = 0; c0 < p.B; c0 += 32) {
+        head_best[warp][lane] = c0 == 0 ? e.best_lo : e.best_hi;   // column c0 + lane
+        __syncthreads();
+        if (threadIdx.x < 32 && c0 + (int)threadIdx.x < p.B) {
+            unsigned long long m = 0ull;
+            for (int w = 0; w < kWarps; ++w) m = head_best[w][threadIdx.x] > m ? head_best[w][threadIdx.x] : m;
+            atomicMax(p.amax + (long long)k * p.B + c0 + threadIdx.x, m);
+        }
+        __syncthreads();
     }
 }
 
@@ -653,6 +965,19 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     // zero the argmax slots of every step (first read after >= 1 barrier)
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < p.N * p.B; i += blockDim.x) p.amax[i] = 0ull;
+    // sequence lengths, read once, and the attention item tables
+    __shared__ int s_kv[MTP_MAX_BATCH];
+    __shared__ AttnTab s_tab;
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) s_kv[b] = p.kv_len[b];
+    __syncthreads();
+    attn_tab_fill(p, s_kv, attn_geom(HD, (int)sizeof(WT)).R, s_tab);
+    __syncthreads();
+    // RoPE inverse frequencies theta^(-2i/hd) of every view, in fp64, spread
+    // over the grid (first read after the first barrier)
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < MTP_MAX_VIEWS * (HD / 2); e += gridDim.x * blockDim.x) {
+        const float th = p.views[e / (HD / 2)].theta;
+        p.ROPE[e] = th > 0.f ? exp(-2.0 * (double)(e % (HD / 2)) / (double)HD * log((double)th)) : 0.0;
+    }
 
     for (int k = 0; k < p.N; ++k) {
         // ---- PRE ----
@@ -670,6 +995,23 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         for (int l = 0; l < p.L; ++l) {
             const BlkW& bw = p.blk[l];
             // ---- Q ----
+            if (l == 0) {
+                // (cos, sin) of this step's query position for every sequence
+                // and view: angle in fp64, reduced to [-pi, pi] before the
+                // fp32 sin/cos (first read after the Q barrier)
+                constexpr int nh = HD / 2;
+                for (int e = threadIdx.x * gridDim.x + blockIdx.x; e < p.B * MTP_MAX_VIEWS * nh;
+                     e += gridDim.x * blockDim.x) {
+                    const double f = __ldcg(p.ROPE + e % (MTP_MAX_VIEWS * nh));
+                    if (f > 0.0) {
+                        double ang = ((double)s_kv[e / (MTP_MAX_VIEWS * nh)] + (double)k) * f;
+                        ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
+                        float sn, cs;
+                        sincosf((float)ang, &sn, &cs);
+                        p.ROPEQ[e] = make_float2(cs, sn);
+                    }
+                }
+            }
             {
                 const float* a = stage_act<WT>(p, PH_Q, k, l, act, tmp, red, epoch, lda, ok);
                 if (!ok) return;
@@ -678,8 +1020,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
             if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
             // ---- ATT ----
-            attention_phase<WT, HD>(p, l, k, smem);
+            if (!attention_phase<WT, HD>(p, l, smem, s_kv, s_tab)) return;
             if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
+            // every CTA has passed its attention waits: reset the item counters
+            if (blockIdx.x == 0)
+                for (int i = threadIdx.x; i < p.B * p.Hkv; i += blockDim.x) p.att_cnt[i] = 0u;
             // ---- O ----
             {
                 const float* a = stage_act<WT>(p, PH_O, k, l, act, tmp, red, epoch, lda, ok);
@@ -718,20 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         {
             const float* a = stage_act<WT>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
             if (!ok) return;
-            HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull};
-            gemv<WT, U, false>(reinterpret_cast<const WT*>(p.tok_embd), nullptr, p.V, p.d_t, a, lda, p.B, e);
-            // fold the per-lane bests: per CTA in shared memory, one atomic per column
-            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-            for (int c0 = 0; c0 < p.B; c0 += 32) {
-                head_best[warp][lane] = c0 == 0 ? e.best_lo : e.best_hi;   // column c0 + lane
-                __syncthreads();
-                if (threadIdx.x < 32 && c0 + (int)threadIdx.x < p.B) {
-                    unsigned long long m = 0ull;
-                    for (int w = 0; w < kWarps; ++w) m = head_best[w][threadIdx.x] > m ? head_best[w][threadIdx.x] : m;
-                    atomicMax(p.amax + (long long)k * p.B + c0 + threadIdx.x, m);
-                }
-                __syncthreads();
-            }
+            head_phase<WT>(p, k, a, lda, head_best);
         }
         if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
     }

@@ -30,6 +30,15 @@ def test_small_parity(dtype):
     check_draft_parity(w, d, h, z, seqs=range(w.B))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_small_single_sequence(dtype):
+    """B = 1 streams every weight share and the LM head through bulk copies;
+    few rows per CTA here, so rows are split across warps."""
+    w = small_workload(dtype, B=1, kv=(77,), V=3001)
+    _, d, h, z = run_gpu_draft(w)
+    check_draft_parity(w, d, h, z, seqs=[0])
+
+
 def test_small_softcap_and_head_dim_64():
     w = small_workload("bf16", softcap=5.0, hd=64, kv=(1, 64, 127))
     _, d, h, z = run_gpu_draft(w)
