@@ -208,10 +208,20 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         smem = draft_smem(cfg, B, 0);
         if (smem > kSmemLimit) return MTP_ERR_UNSUPPORTED;
     }
-    const int per_sm = bf ? draft_blocks_per_sm_bf16(cfg->head_dim, smem) : draft_blocks_per_sm_f32(cfg->head_dim, smem);
-    if (per_sm < 1) return MTP_ERR_UNSUPPORTED;
     int grid = sms;
     if (grid > kMaxGrid) grid = kMaxGrid;
+    // one sequence: LM head rows through bulk-copy slots at offset 0
+    int head_slotb = 0;
+    if (B == 1 && (size_t)cfg->d_t * esz / 16 <= (size_t)kHeadMaxChunks) {
+        const size_t slotb = ((size_t)cfg->d_t * esz + 127) & ~(size_t)127;
+        const size_t ring = (size_t)kHeadGroups * kHeadSlots * slotb;
+        if (ring <= kSmemLimit) {
+            head_slotb = (int)slotb;
+            if (ring > smem) smem = ring;
+        }
+    }
+    const int per_sm = bf ? draft_blocks_per_sm_bf16(cfg->head_dim, smem) : draft_blocks_per_sm_f32(cfg->head_dim, smem);
+    if (per_sm < 1) return MTP_ERR_UNSUPPORTED;
 
     char* base = static_cast<char*>(ws);
     DraftParams p;
@@ -260,6 +270,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     p.ROPEQ = reinterpret_cast<float2*>(base + L.ROPEQ);
     p.ACT = reinterpret_cast<float*>(base + L.ACT);
     p.act_smem = act_smem;
+    p.head_slotb = head_slotb;
     p.kmax = L.kmax;
     p.timeout_ns = kBarrierLimitNs;
     (void)seed; (void)offset; (void)hist; (void)H;

@@ -10,6 +10,9 @@ namespace mtp {
 
 constexpr int kMaxGrid = 1024;     // upper bound on CTAs of the persistent grid
 
+// phases of one draft step
+enum Phase { PH_PRE, PH_Q, PH_O, PH_FFN1, PH_FFN2, PH_POST, PH_HEAD };
+
 // Shape of the attention phase for head dimension hd and element size wb.
 // A K or V row is split over LPR lanes, CPL 16-byte chunks each; a warp
 // reads KPW rows side by side and stages R keys (K and V rows, 4 KB) per
@@ -24,6 +27,11 @@ __host__ __device__ constexpr AttnGeom attn_geom(int hd, int wb) {
     return AttnGeom{RB, CPR, LPR, CPL, KPW, EPC, DPL, R, R / KPW, 2 * R * RB, HG};
 }
 constexpr int kAttnStages = 2;
+// LM head of one sequence: four groups of four warps, each with kHeadSlots
+// one-row slots; rows of up to kHeadMaxChunks 16-byte chunks
+constexpr int kHeadGroups = 4;
+constexpr int kHeadSlots = 3;
+constexpr int kHeadMaxChunks = 640;
 
 // floats per attention partial: o[grp][hd], m[grp], l[grp], padded to 16 bytes
 __host__ __device__ constexpr int attn_psz(int grp, int hd) { return (grp * (hd + 2) + 3) & ~3; }
@@ -82,6 +90,7 @@ struct DraftParams {
     float2* ROPEQ;               // [B][MTP_MAX_VIEWS][hd / 2] (cos, sin) at the step's query position
     float* ACT;                  // [B, kmax] staged activations (global mode)
     int act_smem;                // 1: activations staged per CTA in shared memory
+    int head_slotb;              // > 0: one sequence, LM head rows through bulk-copy slots of this many bytes
     int kmax;
     unsigned long long timeout_ns;
 };

@@ -25,6 +25,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "draft.cuh"
 
@@ -230,8 +232,6 @@ __device__ __forceinline__ int step_token(const DraftParams& p, int b, int k) {
     return t < (uint32_t)p.V ? (int)t : 0;   // every slot holds a row index after its HEAD phase
 }
 
-enum Phase { PH_PRE, PH_Q, PH_O, PH_FFN1, PH_FFN2, PH_POST, PH_HEAD };
-
 // Writes sequence b's input vector for `phase` into dst (length phase_k).
 // `writer` marks the one CTA that also stores residual-stream updates.
 template <typename WT>
@@ -360,6 +360,19 @@ __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l,
     ok = grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
     lda = p.kmax;
     return p.ACT;
+}
+
+// first row of CTA c's block of R rows
+__device__ __forceinline__ int row_lo(int R, int c) { return (int)(((long long)R * c) / gridDim.x); }
+
+// Bounded wait on an mbarrier phase: false once limit_ns passed.
+__device__ __forceinline__ bool mbar_wait_limited(unsigned long long* bar, unsigned int parity,
+                                                  unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -912,11 +925,108 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
 // ---------------------------------------------------------------------------
 // LM head over the tied token table with the argmax folded in: per lane,
 // per CTA in shared memory, then one atomic per sequence.
+// One sequence: CTA c streams its block of rows [V c / grid, V (c + 1) /
+// grid) with four groups of four warps; group q takes rows r0 + q, r0 + q + 4,
+// ...  Every row is one bulk copy into one of the group's kHeadSlots
+// shared-memory slots, so kHeadSlots rows per group are in flight.  The warps
+// of a group split a row's chunks in quarters and hold their quarter of the
+// input in registers; the group's first thread adds the four warp sums, runs
+// the epilogue and refills the slot.  `par` carries the slot phase bits
+// across calls.  False (status set) if a copy did not land in time.
+__device__ __forceinline__ void group_sync(int g) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(kThreads / kHeadGroups) : "memory");
+}
+
+template <typename WT, int CPL>
+__device__ bool head_groups_b1(const DraftParams& p, unsigned char* ring, unsigned long long (*bars)[kHeadSlots],
+                               unsigned int& par, float (*hpart)[kHeadSlots][4], HeadEpi& e) {
+    constexpr int EPC = Chunk<WT>::EPC;
+    const WT* W = reinterpret_cast<const WT*>(p.tok_embd);
+    const int nch = p.d_t / EPC, qch = (nch + 3) / 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int q = warp / 4, wq = warp % 4;
+    const int r0 = row_lo(p.V, blockIdx.x), r1 = row_lo(p.V, blockIdx.x + 1);
+    const int nrow = r1 - r0 > q ? (r1 - r0 - q + 3) / 4 : 0;
+    const unsigned int rowb = (unsigned int)nch * 16u;
+    unsigned char* gring = ring + q * kHeadSlots * p.head_slotb;
+    const bool issuer = wq == 0 && lane == 0;
+    float xr[CPL][EPC];
+#pragma unroll
+    for (int u = 0; u < CPL; ++u) {
+        const int cw = lane + 32 * u, c = wq * qch + cw;
+#pragma unroll
+        for (int e4 = 0; e4 < EPC; e4 += 4) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (cw < qch && c < nch) v = __ldcg(reinterpret_cast<const float4*>(p.HN + c * EPC + e4));
+            xr[u][e4] = v.x;
+            xr[u][e4 + 1] = v.y;
+            xr[u][e4 + 2] = v.z;
+            xr[u][e4 + 3] = v.w;
+        }
+    }
+    auto issue = [&](int j) {
+        const int slot = j % kHeadSlots;
+        mbar_arrive_expect_tx(&bars[q][slot], rowb);
+        bulk_g2s(gring + slot * p.head_slotb, W + (long long)(r0 + q + 4 * j) * nch * EPC, rowb, &bars[q][slot]);
+    };
+    __syncthreads();   // the slots reuse shared memory of earlier phases
+    if (issuer) {
+        fence_proxy_async_smem();
+        for (int j = 0; j < kHeadSlots && j < nrow; ++j) issue(j);
+    }
+    for (int j = 0; j < nrow; ++j) {
+        const int slot = j % kHeadSlots, bit = q * kHeadSlots + slot;
+        if (!mbar_wait_limited(&bars[q][slot], (par >> bit) & 1u, p.timeout_ns)) {
+            if (issuer) atomicCAS(&p.hdr->status, 0, MTP_ERR_TIMEOUT);
+            for (int u = 1; u < kHeadSlots && j + u < nrow; ++u) {
+                const int s2 = (j + u) % kHeadSlots;
+                mbar_wait_limited(&bars[q][s2], (par >> (q * kHeadSlots + s2)) & 1u, p.timeout_ns);
+            }
+            return false;
+        }
+        par ^= 1u << bit;
+        const unsigned char* sp = gring + slot * p.head_slotb;
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) {
+            const int cw = lane + 32 * u, c = wq * qch + cw;
+            if (cw < qch && c < nch) acc += Chunk<WT>::dotr(*reinterpret_cast<const uint4*>(sp + c * 16), xr[u]);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) hpart[q][slot][wq] = acc;
+        group_sync(q);   // the slot is consumed and the four sums are in
+        if (issuer) {
+            const float z[1] = {((hpart[q][slot][0] + hpart[q][slot][1]) + hpart[q][slot][2]) + hpart[q][slot][3]};
+            e.apply(r0 + q + 4 * j, 0, 1, z, z);
+            if (j + kHeadSlots < nrow) {
+                fence_proxy_async_smem();
+                issue(j + kHeadSlots);
+            }
+        }
+    }
+    return true;
+}
+
 template <typename WT>
-__device__ __forceinline__ void head_phase(const DraftParams& p, int k, const float* a, int lda,
-                                           unsigned long long (*head_best)[32]) {
+__device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const float* a, int lda,
+                                           unsigned long long (*head_best)[32], unsigned char* smem,
+                                           unsigned long long (*bars)[kHeadSlots], unsigned int& par,
+                                           float (*hpart)[kHeadSlots][4]) {
     HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull};
-    gemv<WT, 8, false>(reinterpret_cast<const WT*>(p.tok_embd), nullptr, p.V, p.d_t, a, lda, p.B, e);
+    if (p.head_slotb > 0) {
+        const int cpl = (p.d_t / Chunk<WT>::EPC + 127) / 128;
+        bool ok = true;
+        switch (cpl) {
+        case 1: ok = head_groups_b1<WT, 1>(p, smem, bars, par, hpart, e); break;
+        case 2: ok = head_groups_b1<WT, 2>(p, smem, bars, par, hpart, e); break;
+        case 3: ok = head_groups_b1<WT, 3>(p, smem, bars, par, hpart, e); break;
+        case 4: ok = head_groups_b1<WT, 4>(p, smem, bars, par, hpart, e); break;
+        default: ok = head_groups_b1<WT, 5>(p, smem, bars, par, hpart, e); break;
+        }
+        if (!ok) return false;
+    } else {
+        gemv<WT, 8, false>(reinterpret_cast<const WT*>(p.tok_embd), nullptr, p.V, p.d_t, a, lda, p.B, e);
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int c0 = 0; c0 < p.B; c0 += 32) {
         head_best[warp][lane] = c0 == 0 ? e.best_lo : e.best_hi;   // column c0 + lane
@@ -928,6 +1038,7 @@ __device__ __forceinline__ void head_phase(const DraftParams& p, int k, const fl
         }
         __syncthreads();
     }
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -938,12 +1049,14 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ float red[kWarps];
     __shared__ unsigned long long head_best[kWarps][32];
+    __shared__ __align__(8) unsigned long long head_bar[kHeadGroups][kHeadSlots];   // LM head slots
+    __shared__ float head_part[kHeadGroups][kHeadSlots][4];
+    unsigned int head_par = 0;
     unsigned int epoch = 0;
     float* tmp = reinterpret_cast<float*>(smem);                 // [max(d_a)] residual scratch
     float* act = tmp + ((p.d_a + 3) & ~3);                       // activations
     constexpr int U = 8;
     bool ok = true;
-    int lda = 0;
 
     // device-side input checks: every CTA evaluates the same predicate, so on
     // bad inputs all CTAs return before the first barrier
@@ -979,18 +1092,33 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         p.ROPE[e] = th > 0.f ? exp(-2.0 * (double)(e % (HD / 2)) / (double)HD * log((double)th)) : 0.0;
     }
 
+    if (threadIdx.x < kHeadGroups * kHeadSlots) mbar_init(&head_bar[0][0] + threadIdx.x, 1);
+    mbar_fence_init();
+    __syncthreads();
+    // one GEMV phase and the barrier after it
+    auto gemv_step = [&](int phase, int k, int l, const void* W, const void* W2, int R, int K, auto& epi,
+                         auto two) -> bool {
+        constexpr bool TWO = decltype(two)::value;
+        int lda = 0;
+        bool ok = true;
+        const float* a = stage_act<WT>(p, phase, k, l, act, tmp, red, epoch, lda, ok);
+        if (!ok) return false;
+        gemv<WT, TWO ? U / 2 : U, TWO>(reinterpret_cast<const WT*>(W), reinterpret_cast<const WT*>(W2), R, K, a, lda,
+                                       p.B, epi);
+        return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
+    };
+    using One = std::integral_constant<bool, false>;
+    using Two = std::integral_constant<bool, true>;
+
     for (int k = 0; k < p.N; ++k) {
         // ---- PRE ----
         if (blockIdx.x == 0 && k > 0)
             for (int b = threadIdx.x; b < p.B; b += blockDim.x)
                 p.out_drafts[(long long)b * p.N + (k - 1)] = step_token(p, b, k);
         {
-            const float* a = stage_act<WT>(p, PH_PRE, k, 0, act, tmp, red, epoch, lda, ok);
-            if (!ok) return;
             StoreEpi e{p.XB, p.d_a};
-            gemv<WT, U, false>(reinterpret_cast<const WT*>(p.w_pre), nullptr, p.d_a, 2 * p.d_t, a, lda, p.B, e);
+            if (!gemv_step(PH_PRE, k, 0, p.w_pre, nullptr, p.d_a, 2 * p.d_t, e, One{})) return;
         }
-        if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
 
         for (int l = 0; l < p.L; ++l) {
             const BlkW& bw = p.blk[l];
@@ -1013,12 +1141,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
                 }
             }
             {
-                const float* a = stage_act<WT>(p, PH_Q, k, l, act, tmp, red, epoch, lda, ok);
-                if (!ok) return;
                 StoreEpi e{p.QR, p.Hq * p.hd};
-                gemv<WT, U, false>(reinterpret_cast<const WT*>(bw.w_q), nullptr, p.Hq * p.hd, p.d_a, a, lda, p.B, e);
+                if (!gemv_step(PH_Q, k, l, bw.w_q, nullptr, p.Hq * p.hd, p.d_a, e, One{})) return;
             }
-            if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
             // ---- ATT ----
             if (!attention_phase<WT, HD>(p, l, smem, s_kv, s_tab)) return;
             if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
@@ -1027,43 +1152,34 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
                 for (int i = threadIdx.x; i < p.B * p.Hkv; i += blockDim.x) p.att_cnt[i] = 0u;
             // ---- O ----
             {
-                const float* a = stage_act<WT>(p, PH_O, k, l, act, tmp, red, epoch, lda, ok);
-                if (!ok) return;
                 StoreEpi e{p.YB, p.d_a};
-                gemv<WT, U, false>(reinterpret_cast<const WT*>(bw.w_o), nullptr, p.d_a, p.Hq * p.hd, a, lda, p.B, e);
+                if (!gemv_step(PH_O, k, l, bw.w_o, nullptr, p.d_a, p.Hq * p.hd, e, One{})) return;
             }
-            if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
             // ---- FFN1 (gate and up share the input; GeGLU in the epilogue) ----
             {
-                const float* a = stage_act<WT>(p, PH_FFN1, k, l, act, tmp, red, epoch, lda, ok);
-                if (!ok) return;
                 GegluEpi e{p.MB, p.F};
-                gemv<WT, U / 2, true>(reinterpret_cast<const WT*>(bw.w_gate), reinterpret_cast<const WT*>(bw.w_up),
-                                      p.F, p.d_a, a, lda, p.B, e);
+                if (!gemv_step(PH_FFN1, k, l, bw.w_gate, bw.w_up, p.F, p.d_a, e, Two{})) return;
             }
-            if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
             // ---- FFN2 ----
             {
-                const float* a = stage_act<WT>(p, PH_FFN2, k, l, act, tmp, red, epoch, lda, ok);
-                if (!ok) return;
                 StoreEpi e{p.Y2, p.d_a};
-                gemv<WT, U, false>(reinterpret_cast<const WT*>(bw.w_down), nullptr, p.d_a, p.F, a, lda, p.B, e);
+                if (!gemv_step(PH_FFN2, k, l, bw.w_down, nullptr, p.d_a, p.F, e, One{})) return;
             }
-            if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
         }
         // ---- POST ----
         {
-            const float* a = stage_act<WT>(p, PH_POST, k, 0, act, tmp, red, epoch, lda, ok);
-            if (!ok) return;
             StoreEpi e{p.HN, p.d_t};
-            gemv<WT, U, false>(reinterpret_cast<const WT*>(p.w_post), nullptr, p.d_t, p.d_a, a, lda, p.B, e);
+            if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         }
-        if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
         // ---- HEAD ----
         {
-            const float* a = stage_act<WT>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
-            if (!ok) return;
-            head_phase<WT>(p, k, a, lda, head_best);
+            int lda = 0;
+            const float* a = nullptr;
+            if (p.head_slotb == 0) {
+                a = stage_act<WT>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
+                if (!ok) return;
+            }
+            if (!head_phase<WT>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part)) return;
         }
         if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
     }
