@@ -152,6 +152,36 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def kernel_source_hash() -> str:
+    """sha256 prefix over the library's CUDA sources and its public header:
+    ties a recorded ncu traffic figure to the kernel it was taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mtp_speculative_decoding_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(fn.encode())
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(f.read())
+    with open(os.path.join(ROOT, "include", "mtp.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes (read + write) per draft-kernel launch from the committed ncu
+    summary, or None when that capture was taken on other kernel sources or
+    another workload."""
+    p = os.path.join(ROOT, "profiles", "draft_kernel_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        kv = dict(t.split("=", 1) for t in f.read().split() if "=" in t)
+    if kv.get("workload") != workload or kv.get("source_hash") != kernel_source_hash():
+        return None
+    return int(kv["dram_bytes_per_launch"])
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -308,7 +338,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "draft_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": alg,
-                     "traffic": None},
+                     "traffic": recorded_traffic(w.name)},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
     }
