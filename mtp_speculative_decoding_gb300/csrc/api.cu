@@ -2,9 +2,13 @@
 // layout and launches.  No allocation, no synchronization (except
 // mtp_last_error), no state kept between calls beyond a per-device cache of
 // the SM count.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "draft.cuh"
@@ -32,8 +36,12 @@ int num_sms() {
     return n;
 }
 
+// LM head on tensor cores: bf16 weights and a batch of at least kTcMinBatch
+bool tc_head_eligible(const mtp_config* c, int B) { return c->wdtype == MTP_DTYPE_BF16 && B >= kTcMinBatch; }
+int pad16(int B) { return (B + 15) & ~15; }
+
 struct DraftLayout {
-    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, ACT, end;
+    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, XH, XL, ACT, end;
     int kmax;
 };
 
@@ -66,9 +74,42 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     L.PART = off;    off = al256(off + items * attn_psz(grp, c->head_dim) * f);
     L.ROPE = off;    off = al256(off + (size_t)MTP_MAX_VIEWS * (c->head_dim / 2) * sizeof(double));
     L.ROPEQ = off;   off = al256(off + (size_t)B * MTP_MAX_VIEWS * (c->head_dim / 2) * 2 * f);
+    const size_t xb = tc_head_eligible(c, B) ? (size_t)pad16(B) * c->d_t * 2 : 0;
+    L.XH = off;      off = al256(off + xb);
+    L.XL = off;      off = al256(off + xb);
     L.ACT = off;     off = al256(off + (size_t)B * L.kmax * f);
     L.end = off;
     return L;
+}
+
+// cuTensorMapEncodeTiled from the driver, resolved once
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix: box of 64
+// columns (128 bytes, 128-byte swizzle) by box_rows rows; out-of-range rows
+// and columns read as zero
+bool encode_bf16_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct GreedyLayout { size_t amax, end; };
@@ -220,6 +261,19 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
             if (ring > smem) smem = ring;
         }
     }
+    // batch: LM head on tensor cores, operand ring at offset 0 (1024-aligned)
+    const bool tc = tc_head_eligible(cfg, B);
+    int tc_stages = 0, tc_cols = 0;
+    if (tc) {
+        const size_t sbytes = (size_t)kTcTileM * 128 + 2 * (size_t)pad16(B) * 128;
+        tc_stages = (int)(kTcSmemBudget / sbytes);
+        if (tc_stages > kTcMaxStages) tc_stages = kTcMaxStages;
+        if (tc_stages < 2) return MTP_ERR_UNSUPPORTED;
+        const size_t need = (size_t)tc_stages * sbytes + 1024;
+        if (need > smem) smem = need;
+        tc_cols = 32;
+        while (tc_cols < 2 * pad16(B)) tc_cols *= 2;
+    }
     const int per_sm = bf ? draft_blocks_per_sm_bf16(cfg->head_dim, smem) : draft_blocks_per_sm_f32(cfg->head_dim, smem);
     if (per_sm < 1) return MTP_ERR_UNSUPPORTED;
 
@@ -271,6 +325,18 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     p.ACT = reinterpret_cast<float*>(base + L.ACT);
     p.act_smem = act_smem;
     p.head_slotb = head_slotb;
+    if (tc) {
+        p.tc_head = 1;
+        p.Bp = pad16(B);
+        p.tc_stages = tc_stages;
+        p.tc_cols = tc_cols;
+        p.XH = reinterpret_cast<uint16_t*>(base + L.XH);
+        p.XL = reinterpret_cast<uint16_t*>(base + L.XL);
+        if (!encode_bf16_map(&p.tm_embd, w->tok_embd, (uint64_t)cfg->d_t, (uint64_t)cfg->vocab, kTcTileM) ||
+            !encode_bf16_map(&p.tm_xh, p.XH, (uint64_t)cfg->d_t, (uint64_t)p.Bp, (uint32_t)p.Bp) ||
+            !encode_bf16_map(&p.tm_xl, p.XL, (uint64_t)cfg->d_t, (uint64_t)p.Bp, (uint32_t)p.Bp))
+            return MTP_ERR_CUDA;
+    }
     p.kmax = L.kmax;
     p.timeout_ns = kBarrierLimitNs;
     (void)seed; (void)offset; (void)hist; (void)H;

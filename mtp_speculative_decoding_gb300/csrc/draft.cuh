@@ -1,6 +1,7 @@
 // draft.cuh -- argument block of the persistent draft-block kernel (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,6 +33,13 @@ constexpr int kAttnStages = 2;
 constexpr int kHeadGroups = 4;
 constexpr int kHeadSlots = 3;
 constexpr int kHeadMaxChunks = 640;
+// LM head on tensor cores (bf16 weights, B >= kTcMinBatch): 128-row tiles of
+// the token table, K steps of 64, kTcStages-deep operand ring
+constexpr int kTcMinBatch = 8;
+constexpr int kTcTileM = 128;
+constexpr int kTcTileK = 64;
+constexpr int kTcMaxStages = 8;
+constexpr size_t kTcSmemBudget = 128 * 1024;
 
 // floats per attention partial: o[grp][hd], m[grp], l[grp], padded to 16 bytes
 __host__ __device__ constexpr int attn_psz(int grp, int hd) { return (grp * (hd + 2) + 3) & ~3; }
@@ -64,6 +72,10 @@ struct BlkW {
 };
 
 struct DraftParams {
+    // tensor-core LM head: maps of the token table [V, d_t] (box 64 x 128)
+    // and of the bf16 high / low parts of h [Bp, d_t] (box 64 x Bp), all
+    // with 128-byte swizzle
+    CUtensorMap tm_embd, tm_xh, tm_xl;
     int d_t, d_a, L, Hq, hd, Hkv, F, V, B, N;
     float eps, attn_scale, emb_scale, softcap;
     const void* tok_embd;
@@ -91,6 +103,9 @@ struct DraftParams {
     float* ACT;                  // [B, kmax] staged activations (global mode)
     int act_smem;                // 1: activations staged per CTA in shared memory
     int head_slotb;              // > 0: one sequence, LM head rows through bulk-copy slots of this many bytes
+    int tc_head;                 // 1: LM head on tensor cores
+    int Bp, tc_stages, tc_cols;  // batch padded to 16; operand ring depth; tensor-memory columns
+    uint16_t *XH, *XL;           // [Bp, d_t] bf16 high / low parts of h (rows >= B zero)
     int kmax;
     unsigned long long timeout_ns;
 };

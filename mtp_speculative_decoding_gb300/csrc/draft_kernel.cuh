@@ -27,6 +27,8 @@
 
 #include <type_traits>
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "draft.cuh"
 
@@ -161,6 +163,28 @@ struct StoreEpi {
 #pragma unroll
         for (int j = 0; j < NB; ++j)
             if (lane == j && b0 + j < nb) out[(long long)(b0 + j) * ldo + r] = acc[j];
+    }
+};
+
+// out[b * ldo + r] = v, plus the bf16 high and low parts of v (v ~ hi + lo)
+// as the tensor-core operand rows xh[b * ldo + r], xl[b * ldo + r]
+struct StoreHiLoEpi {
+    float* out;
+    int ldo;
+    uint16_t *xh, *xl;
+    template <int NB>
+    __device__ __forceinline__ void apply(int r, int b0, int nb, const float (&acc)[NB], const float (&)[NB]) {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+            if (lane == j && b0 + j < nb) {
+                const long long i = (long long)(b0 + j) * ldo + r;
+                const float v = acc[j];
+                out[i] = v;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                xh[i] = __bfloat16_as_ushort(hi);
+                xl[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+            }
     }
 };
 
@@ -688,7 +712,7 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
                     if constexpr (TR) {
                         // lane holds score x = lane / SH: key x / HG, head x % HG
                         const float sx = transpose_sum<NV, 32>(sc);
-                        const int x = lane / SH, xh = x % HG;
+                        const int x = lane / SH;
                         const bool valid = x / HG < cnt;
                         float mx = valid ? sx : -INFINITY;
 #pragma unroll
@@ -1007,13 +1031,132 @@ __device__ bool head_groups_b1(const DraftParams& p, unsigned char* ring, unsign
     return true;
 }
 
+// Tensor-core LM head (bf16, B >= 8): logits[row, b] = E[row, :] . h[b, :]
+// as D = A B^T with A a 128-row tile of the token table and B the padded
+// batch of h split into bf16 high and low parts (two MMAs per K slice, so
+// the product carries about 16 mantissa bits of h).  CTA c takes row tiles
+// c, c + grid, ...; warp 0 (one lane) streams A and B tiles through a
+// tc_stages-deep ring with tensor copies, warp 1 (one lane) issues the MMAs
+// into one of two tensor-memory accumulators, and warps 4-7 read the
+// accumulator rows (one tensor-memory lane per row) and fold the argmax per
+// sequence.  The barrier phases continue across calls through `ts`.
+struct TcState {
+    unsigned long long *full, *empty, *tfull, *tempty;
+    unsigned int tmem;   // tensor-memory base address
+    unsigned int g, it;  // K steps and tiles this CTA has processed so far
+};
+
+template <typename WT>
+__device__ bool head_tc(const DraftParams& p, int k, unsigned char* smem, TcState& ts, HeadEpi& e) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int Bp = p.Bp, NS = p.tc_stages;
+    const int nks = (p.d_t + kTcTileK - 1) / kTcTileK;
+    const int ntiles = (p.V + kTcTileM - 1) / kTcTileM;
+    const int nit = ntiles > (int)blockIdx.x ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    const uint32_t abytes = kTcTileM * 128, xbytes = (uint32_t)Bp * 128, sbytes = abytes + 2 * xbytes;
+    const uint32_t base = (smem_addr(smem) + 1023u) & ~1023u;   // 1024-byte aligned ring
+    unsigned char* ring = smem + (base - smem_addr(smem));
+    bool ok = true;
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t g = ts.g;
+            for (int j = 0; j < nit && ok; ++j) {
+                const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * kTcTileM;
+                for (int ks = 0; ks < nks; ++ks, ++g) {
+                    const uint32_t st = g % NS;
+                    if (!mbar_wait_limited(&ts.empty[st], ((g / NS) & 1u) ^ 1u, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* sp = ring + st * sbytes;
+                    mbar_arrive_expect_tx(&ts.full[st], sbytes);
+                    tma_load_2d(sp, &p.tm_embd, ks * kTcTileK, row0, &ts.full[st]);
+                    tma_load_2d(sp + abytes, &p.tm_xh, ks * kTcTileK, 0, &ts.full[st]);
+                    tma_load_2d(sp + abytes + xbytes, &p.tm_xl, ks * kTcTileK, 0, &ts.full[st]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t g = ts.g;
+            const uint32_t idesc = umma_idesc_bf16(kTcTileM, Bp);
+            for (int j = 0; j < nit && ok; ++j) {
+                const uint32_t it = ts.it + j, acc = it & 1u;
+                if (!mbar_wait_limited(&ts.tempty[acc], ((it >> 1) & 1u) ^ 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = ts.tmem + acc * (uint32_t)Bp;
+                for (int ks = 0; ks < nks; ++ks, ++g) {
+                    const uint32_t st = g % NS;
+                    if (!mbar_wait_limited(&ts.full[st], (g / NS) & 1u, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + st * sbytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTcTileK / 16; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(sa + kk * 32);
+                        umma_bf16(d, ad, umma_desc_sw128(sa + abytes + kk * 32), idesc, (ks | kk) != 0 ? 1u : 0u);
+                        umma_bf16(d, ad, umma_desc_sw128(sa + abytes + xbytes + kk * 32), idesc, 1u);
+                    }
+                    umma_commit(&ts.empty[st]);
+                }
+                if (!ok) break;
+                umma_commit(&ts.tfull[acc]);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        const int q = warp - 4;   // tensor-memory lane quarter of this warp
+        for (int j = 0; j < nit && ok; ++j) {
+            const uint32_t it = ts.it + j, acc = it & 1u;
+            if (!mbar_wait_limited(&ts.tfull[acc], (it >> 1) & 1u, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int row = ((int)blockIdx.x + j * (int)gridDim.x) * kTcTileM + 32 * q + lane;
+            const uint32_t ta = ts.tmem + ((uint32_t)(32 * q) << 16) + acc * (uint32_t)Bp;
+            for (int c0 = 0; c0 < Bp; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(ta + (uint32_t)c0, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int b = c0 + jj;
+                    if (b < p.B) {
+                        float z = __uint_as_float(r[jj]);
+                        if (p.softcap > 0.f) z = p.softcap * tanhf(z / p.softcap);
+                        if (row < p.V && p.out_logits) p.out_logits[((long long)b * p.N + k) * p.V + row] = z;
+                        const unsigned long long key = warp_max_u64(row < p.V ? pack_argmax(z, (uint32_t)row) : 0ull);
+                        if (lane == (b & 31)) {
+                            if (b < 32) e.best_lo = key > e.best_lo ? key : e.best_lo;
+                            else e.best_hi = key > e.best_hi ? key : e.best_hi;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ts.tempty[acc]);
+        }
+    }
+    ts.g += (uint32_t)(nit * nks);
+    ts.it += (uint32_t)nit;
+    return __syncthreads_and(ok) != 0;
+}
+
 template <typename WT>
 __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const float* a, int lda,
                                            unsigned long long (*head_best)[32], unsigned char* smem,
                                            unsigned long long (*bars)[kHeadSlots], unsigned int& par,
-                                           float (*hpart)[kHeadSlots][4]) {
+                                           float (*hpart)[kHeadSlots][4], TcState& ts) {
     HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull};
-    if (p.head_slotb > 0) {
+    if (p.tc_head) {
+        if (!head_tc<WT>(p, k, smem, ts, e)) return false;
+    } else if (p.head_slotb > 0) {
         const int cpl = (p.d_t / Chunk<WT>::EPC + 127) / 128;
         bool ok = true;
         switch (cpl) {
@@ -1023,7 +1166,7 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
         case 4: ok = head_groups_b1<WT, 4>(p, smem, bars, par, hpart, e); break;
         default: ok = head_groups_b1<WT, 5>(p, smem, bars, par, hpart, e); break;
         }
-        if (!ok) return false;
+        if (!__syncthreads_and(ok)) return false;
     } else {
         gemv<WT, 8, false>(reinterpret_cast<const WT*>(p.tok_embd), nullptr, p.V, p.d_t, a, lda, p.B, e);
     }
@@ -1045,8 +1188,7 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
 // the kernel
 // ---------------------------------------------------------------------------
 template <typename WT, int HD>
-__global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftParams p) {
-    extern __shared__ __align__(16) unsigned char smem[];
+__device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts) {
     __shared__ float red[kWarps];
     __shared__ unsigned long long head_best[kWarps][32];
     __shared__ __align__(8) unsigned long long head_bar[kHeadGroups][kHeadSlots];   // LM head slots
@@ -1078,6 +1220,15 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     // zero the argmax slots of every step (first read after >= 1 barrier)
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < p.N * p.B; i += blockDim.x) p.amax[i] = 0ull;
+    // tensor-core head: zero rows B..Bp-1 of the bf16 parts of h (read by
+    // tensor copies, first after >= 1 barrier)
+    if (p.tc_head && blockIdx.x == 0) {
+        for (long long i = (long long)p.B * p.d_t + threadIdx.x; i < (long long)p.Bp * p.d_t; i += blockDim.x) {
+            p.XH[i] = 0;
+            p.XL[i] = 0;
+        }
+        fence_proxy_async_global();
+    }
     // sequence lengths, read once, and the attention item tables
     __shared__ int s_kv[MTP_MAX_BATCH];
     __shared__ AttnTab s_tab;
@@ -1105,6 +1256,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         if (!ok) return false;
         gemv<WT, TWO ? U / 2 : U, TWO>(reinterpret_cast<const WT*>(W), reinterpret_cast<const WT*>(W2), R, K, a, lda,
                                        p.B, epi);
+        if (p.tc_head && phase == PH_POST) fence_proxy_async_global();   // h parts are read by tensor copies
         return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
     };
     using One = std::integral_constant<bool, false>;
@@ -1167,7 +1319,10 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             }
         }
         // ---- POST ----
-        {
+        if (p.tc_head) {
+            StoreHiLoEpi e{p.HN, p.d_t, p.XH, p.XL};
+            if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
+        } else {
             StoreEpi e{p.HN, p.d_t};
             if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         }
@@ -1175,11 +1330,11 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         {
             int lda = 0;
             const float* a = nullptr;
-            if (p.head_slotb == 0) {
+            if (p.head_slotb == 0 && !p.tc_head) {
                 a = stage_act<WT>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
                 if (!ok) return;
             }
-            if (!head_phase<WT>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part)) return;
+            if (!head_phase<WT>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part, ts)) return;
         }
         if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
     }
@@ -1189,6 +1344,40 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
             p.out_drafts[(long long)b * p.N + (p.N - 1)] = step_token(p, b, p.N);
         if (p.out_h_last)
             for (long long i = threadIdx.x; i < (long long)p.B * p.d_t; i += blockDim.x) p.out_h_last[i] = __ldcg(p.HN + i);
+    }
+}
+
+// The persistent draft kernel: tensor memory (when the LM head runs on tensor
+// cores) is allocated by warp 2 before the body and freed after it; every
+// exit of the body is uniform over the CTA.
+template <typename WT, int HD>
+__global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftParams p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ __align__(8) unsigned long long tc_bar[2 * kTcMaxStages + 4];
+    __shared__ unsigned int tc_tmem;
+    TcState ts{tc_bar, tc_bar + kTcMaxStages, tc_bar + 2 * kTcMaxStages, tc_bar + 2 * kTcMaxStages + 2, 0u, 0u, 0u};
+    const int warp = threadIdx.x >> 5;
+    if (p.tc_head) {
+        // full / empty stage barriers (one arrival each), accumulator full
+        // (one commit) and empty (one arrival per epilogue warp)
+        if (threadIdx.x < 2 * kTcMaxStages + 4)
+            mbar_init(&tc_bar[threadIdx.x], threadIdx.x >= 2 * kTcMaxStages + 2 ? 4u : 1u);
+        if (warp == 2) {
+            tmem_alloc(&tc_tmem, (unsigned int)p.tc_cols);
+            tmem_relinquish();
+        }
+        mbar_fence_init();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        ts.tmem = tc_tmem;
+    }
+    draft_body<WT, HD>(p, smem, ts);
+    if (p.tc_head) {
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 2) tmem_dealloc(ts.tmem, (unsigned int)p.tc_cols);
     }
 }
 
