@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build", platform.machine())
 LIB = os.path.join(BUILD, "libmtp.so")
 
-SOURCES = ["api.cu", "verify.cu", "draft_bf16.cu", "draft_f32.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "verify.cu", "draft_bf16.cu", "draft_bf16_tc.cu", "draft_f32.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -40,8 +40,47 @@ int num_sms() {
 bool tc_head_eligible(const mtp_config* c, int B) { return c->wdtype == MTP_DTYPE_BF16 && B >= kTcMinBatch; }
 int pad16(int B) { return (B + 15) & ~15; }
 
+size_t draft_smem(const mtp_config* c, int B, int act_smem);
+constexpr size_t kSmemLimit = 220 * 1024;
+
+// Projections on tensor cores: eligible for the head path, activations
+// staged in global memory, FFN width a multiple of the 128-row tile (the
+// gate and up rows of one tile come from one matrix)
+bool tc_proj_eligible(const mtp_config* c, int B) {
+    return tc_head_eligible(c, B) && draft_smem(c, B, 1) > kSmemLimit && c->d_ff % kTcTileM == 0;
+}
+
+// split-K factors of the projection phases (PH_PRE .. PH_POST) for a grid of
+// `grid` CTAs, and the floats of the largest split-partial set
+struct TcPlan {
+    int sk[6];
+    size_t pb_floats;
+};
+TcPlan tc_plan(const mtp_config* c, int B, int grid) {
+    TcPlan t;
+    const size_t qd = (size_t)c->n_q_heads * c->head_dim;
+    const size_t R[6] = {(size_t)c->d_a, qd, (size_t)c->d_a, 2 * (size_t)c->d_ff, (size_t)c->d_a, (size_t)c->d_t};
+    const size_t K[6] = {2 * (size_t)c->d_t, (size_t)c->d_a, qd, (size_t)c->d_a, (size_t)c->d_ff, (size_t)c->d_a};
+    t.pb_floats = 0;
+    for (int ph = 0; ph < 6; ++ph) {
+        const int ntiles = (int)((R[ph] + kTcTileM - 1) / kTcTileM), nks = (int)((K[ph] + kTcTileK - 1) / kTcTileK);
+        int S = grid / ntiles;
+        if (S < 1 || ph == PH_POST) S = 1;   // the post-projection writes h directly
+        if (S > nks) S = nks;
+        const int kps = (nks + S - 1) / S;
+        S = (nks + kps - 1) / kps;
+        t.sk[ph] = S;
+        if (ph != PH_POST && (size_t)S * B * R[ph] > t.pb_floats) t.pb_floats = (size_t)S * B * R[ph];
+    }
+    return t;
+}
+int draft_grid() {
+    const int sms = num_sms();
+    return sms < kMaxGrid ? sms : kMaxGrid;
+}
+
 struct DraftLayout {
-    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, XH, XL, ACT, end;
+    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ACT, end;
     int kmax;
 };
 
@@ -77,6 +116,11 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     const size_t xb = tc_head_eligible(c, B) ? (size_t)pad16(B) * c->d_t * 2 : 0;
     L.XH = off;      off = al256(off + xb);
     L.XL = off;      off = al256(off + xb);
+    const bool tcp = tc_proj_eligible(c, B);
+    const size_t xa = tcp ? (size_t)pad16(B) * L.kmax * 2 : 0;
+    L.XA = off;      off = al256(off + xa);
+    L.XAL = off;     off = al256(off + xa);
+    L.PB = off;      off = al256(off + (tcp ? tc_plan(c, B, draft_grid()).pb_floats * f : 0));
     L.ACT = off;     off = al256(off + (size_t)B * L.kmax * f);
     L.end = off;
     return L;
@@ -152,8 +196,6 @@ size_t draft_smem(const mtp_config* c, int B, int act_smem) {
     const size_t act = draft_smem_act(c, B, act_smem);
     return attn > act ? attn : act;
 }
-
-constexpr size_t kSmemLimit = 220 * 1024;
 
 int check_config(const mtp_config* c) {
     if (!c) return MTP_ERR_ARG;
@@ -249,8 +291,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         smem = draft_smem(cfg, B, 0);
         if (smem > kSmemLimit) return MTP_ERR_UNSUPPORTED;
     }
-    int grid = sms;
-    if (grid > kMaxGrid) grid = kMaxGrid;
+    const int grid = draft_grid();
     // one sequence: LM head rows through bulk-copy slots at offset 0
     int head_slotb = 0;
     if (B == 1 && (size_t)cfg->d_t * esz / 16 <= (size_t)kHeadMaxChunks) {
@@ -274,7 +315,9 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         tc_cols = 32;
         while (tc_cols < 2 * pad16(B)) tc_cols *= 2;
     }
-    const int per_sm = bf ? draft_blocks_per_sm_bf16(cfg->head_dim, smem) : draft_blocks_per_sm_f32(cfg->head_dim, smem);
+    const int per_sm = !bf ? draft_blocks_per_sm_f32(cfg->head_dim, smem)
+                       : tc ? draft_blocks_per_sm_bf16_tc(cfg->head_dim, smem)
+                            : draft_blocks_per_sm_bf16_cc(cfg->head_dim, smem);
     if (per_sm < 1) return MTP_ERR_UNSUPPORTED;
 
     char* base = static_cast<char*>(ws);
@@ -336,6 +379,29 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
             !encode_bf16_map(&p.tm_xh, p.XH, (uint64_t)cfg->d_t, (uint64_t)p.Bp, (uint32_t)p.Bp) ||
             !encode_bf16_map(&p.tm_xl, p.XL, (uint64_t)cfg->d_t, (uint64_t)p.Bp, (uint32_t)p.Bp))
             return MTP_ERR_CUDA;
+        if (tc_proj_eligible(cfg, B) && !act_smem) {
+            // projections: weights [R, K] row-major, inputs staged as [Bp, kmax]
+            const TcPlan plan = tc_plan(cfg, B, grid);
+            p.tc_proj = 1;
+            for (int i = 0; i < 6; ++i) p.sk[i] = plan.sk[i];
+            p.XA = reinterpret_cast<uint16_t*>(base + L.XA);
+            p.XAL = reinterpret_cast<uint16_t*>(base + L.XAL);
+            p.PB = reinterpret_cast<float*>(base + L.PB);
+            const uint64_t da = cfg->d_a, dt = cfg->d_t, F = cfg->d_ff, qd = (uint64_t)cfg->n_q_heads * cfg->head_dim;
+            bool okm = encode_bf16_map(&p.tm_xa, p.XA, (uint64_t)L.kmax, (uint64_t)p.Bp, (uint32_t)p.Bp) &&
+                       encode_bf16_map(&p.tm_xal, p.XAL, (uint64_t)L.kmax, (uint64_t)p.Bp, (uint32_t)p.Bp) &&
+                       encode_bf16_map(&p.tm_w[0], w->w_pre, 2 * dt, da, kTcTileM) &&
+                       encode_bf16_map(&p.tm_w[1], w->w_post, da, dt, kTcTileM);
+            for (int l = 0; l < cfg->n_blocks && okm; ++l) {
+                const mtp_block_weights& bw = w->blk[l];
+                CUtensorMap* m = &p.tm_w[2 + 5 * l];
+                okm = encode_bf16_map(m + 0, bw.w_q, da, qd, kTcTileM) && encode_bf16_map(m + 1, bw.w_o, qd, da, kTcTileM) &&
+                      encode_bf16_map(m + 2, bw.w_gate, da, F, kTcTileM) &&
+                      encode_bf16_map(m + 3, bw.w_up, da, F, kTcTileM) &&
+                      encode_bf16_map(m + 4, bw.w_down, F, da, kTcTileM);
+            }
+            if (!okm) return MTP_ERR_CUDA;
+        }
     }
     p.kmax = L.kmax;
     p.timeout_ns = kBarrierLimitNs;
@@ -343,7 +409,9 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, L.amax, s) != cudaSuccess) return MTP_ERR_CUDA;
-    cudaError_t e = bf ? launch_draft_bf16(p, grid, smem, s) : launch_draft_f32(p, grid, smem, s);
+    cudaError_t e = !bf ? launch_draft_f32(p, grid, smem, s)
+                    : p.tc_head ? launch_draft_bf16_tc(p, grid, smem, s)
+                                : launch_draft_bf16_cc(p, grid, smem, s);
     return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
 }
 

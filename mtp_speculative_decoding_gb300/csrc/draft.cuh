@@ -76,6 +76,11 @@ struct DraftParams {
     // and of the bf16 high / low parts of h [Bp, d_t] (box 64 x Bp), all
     // with 128-byte swizzle
     CUtensorMap tm_embd, tm_xh, tm_xl;
+    // projections on tensor cores: the bf16 high / low parts of a phase's
+    // inputs [Bp, kmax] (box 64 x Bp) and every projection weight (box 64 x
+    // 128): pre, post, then per block q, o, gate, up, down
+    CUtensorMap tm_xa, tm_xal;
+    CUtensorMap tm_w[2 + 5 * MTP_MAX_BLOCKS];
     int d_t, d_a, L, Hq, hd, Hkv, F, V, B, N;
     float eps, attn_scale, emb_scale, softcap;
     const void* tok_embd;
@@ -106,14 +111,20 @@ struct DraftParams {
     int tc_head;                 // 1: LM head on tensor cores
     int Bp, tc_stages, tc_cols;  // batch padded to 16; operand ring depth; tensor-memory columns
     uint16_t *XH, *XL;           // [Bp, d_t] bf16 high / low parts of h (rows >= B zero)
+    int tc_proj;                 // 1: projections on tensor cores (activations staged in global memory)
+    int sk[6];                   // split-K factor of each projection phase (PH_PRE .. PH_POST)
+    uint16_t *XA, *XAL;          // [Bp, kmax] bf16 high / low parts of the current phase input
+    float* PB;                   // [S][B][R] split partials of the last projection (FFN1: R = 2 F)
     int kmax;
     unsigned long long timeout_ns;
 };
 
 cudaError_t launch_draft_f32(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
-cudaError_t launch_draft_bf16(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_draft_bf16_cc(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_draft_bf16_tc(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
 int draft_blocks_per_sm_f32(int hd, size_t smem);
-int draft_blocks_per_sm_bf16(int hd, size_t smem);
+int draft_blocks_per_sm_bf16_cc(int hd, size_t smem);
+int draft_blocks_per_sm_bf16_tc(int hd, size_t smem);
 
 cudaError_t launch_barrier_timeout_probe(WsHeader* hdr, unsigned long long limit_ns, cudaStream_t s);
 

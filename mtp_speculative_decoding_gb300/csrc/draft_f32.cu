@@ -5,21 +5,21 @@ namespace mtp {
 
 cudaError_t launch_draft_f32(const DraftParams& p, int grid, size_t smem, cudaStream_t s) {
     switch (p.hd) {
-    case 64: return launch_draft_t<float, 64>(p, grid, smem, s);
-    case 128: return launch_draft_t<float, 128>(p, grid, smem, s);
-    case 256: return launch_draft_t<float, 256>(p, grid, smem, s);
-    case 512: return launch_draft_t<float, 512>(p, grid, smem, s);
-    default: return launch_draft_t<float, 32>(p, grid, smem, s);
+    case 64: return launch_draft_t<float, 64, false>(p, grid, smem, s);
+    case 128: return launch_draft_t<float, 128, false>(p, grid, smem, s);
+    case 256: return launch_draft_t<float, 256, false>(p, grid, smem, s);
+    case 512: return launch_draft_t<float, 512, false>(p, grid, smem, s);
+    default: return launch_draft_t<float, 32, false>(p, grid, smem, s);
     }
 }
 
 int draft_blocks_per_sm_f32(int hd, size_t smem) {
     switch (hd) {
-    case 64: return draft_blocks_per_sm_t<float, 64>(smem);
-    case 128: return draft_blocks_per_sm_t<float, 128>(smem);
-    case 256: return draft_blocks_per_sm_t<float, 256>(smem);
-    case 512: return draft_blocks_per_sm_t<float, 512>(smem);
-    default: return draft_blocks_per_sm_t<float, 32>(smem);
+    case 64: return draft_blocks_per_sm_t<float, 64, false>(smem);
+    case 128: return draft_blocks_per_sm_t<float, 128, false>(smem);
+    case 256: return draft_blocks_per_sm_t<float, 256, false>(smem);
+    case 512: return draft_blocks_per_sm_t<float, 512, false>(smem);
+    default: return draft_blocks_per_sm_t<float, 32, false>(smem);
     }
 }
 

@@ -256,6 +256,29 @@ __device__ __forceinline__ int step_token(const DraftParams& p, int b, int k) {
     return t < (uint32_t)p.V ? (int)t : 0;   // every slot holds a row index after its HEAD phase
 }
 
+// float4 at q summed over S copies st floats apart, in order
+__device__ __forceinline__ float4 ld4_sum(const float* q, int S, long long st) {
+    float4 a = __ldcg(reinterpret_cast<const float4*>(q));
+    for (int s = 1; s < S; ++s) {
+        const float4 c = __ldcg(reinterpret_cast<const float4*>(q + s * st));
+        a.x += c.x;
+        a.y += c.y;
+        a.z += c.z;
+        a.w += c.w;
+    }
+    return a;
+}
+
+// Element i of sequence b's output of a tensor-core projection with R output
+// rows and S split partials: the partials summed in split order.
+__device__ __forceinline__ float part_sum(const DraftParams& p, int S, int R, int b, int i) {
+    const float* q = p.PB + (long long)b * R + i;
+    const long long st = (long long)p.B * R;
+    float v = 0.f;
+    for (int s = 0; s < S; ++s) v += __ldcg(q + s * st);
+    return v;
+}
+
 // Writes sequence b's input vector for `phase` into dst (length phase_k).
 // `writer` marks the one CTA that also stores residual-stream updates.
 template <typename WT>
@@ -276,11 +299,19 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     case PH_Q: {
         const int n = p.d_a;
         if (l == 0) {
-            for (int i = threadIdx.x; i < n; i += blockDim.x) tmp[i] = __ldcg(p.XB + (long long)b * n + i);
+            if (p.tc_proj) {   // the pre-projection's partials form the residual stream
+                for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                    const float x = part_sum(p, p.sk[PH_PRE], n, b, i);
+                    tmp[i] = x;
+                    if (writer) p.XB[(long long)b * n + i] = x;
+                }
+            } else {
+                for (int i = threadIdx.x; i < n; i += blockDim.x) tmp[i] = __ldcg(p.XB + (long long)b * n + i);
+            }
             __syncthreads();
         } else {
             for (int i = threadIdx.x; i < n; i += blockDim.x) {
-                dst[i] = __ldcg(p.Y2 + (long long)b * n + i);
+                dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_FFN2], n, b, i) : __ldcg(p.Y2 + (long long)b * n + i);
                 tmp[i] = __ldcg(p.XM + (long long)b * n + i);
             }
             __syncthreads();
@@ -298,7 +329,7 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     case PH_FFN1: {
         const int n = p.d_a;
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            dst[i] = __ldcg(p.YB + (long long)b * n + i);
+            dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_O], n, b, i) : __ldcg(p.YB + (long long)b * n + i);
             tmp[i] = __ldcg(p.XB + (long long)b * n + i);
         }
         __syncthreads();
@@ -315,7 +346,7 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     case PH_POST: {
         const int n = p.d_a;
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            dst[i] = __ldcg(p.Y2 + (long long)b * n + i);
+            dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_FFN2], n, b, i) : __ldcg(p.Y2 + (long long)b * n + i);
             tmp[i] = __ldcg(p.XM + (long long)b * n + i);
         }
         __syncthreads();
@@ -333,7 +364,12 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     }
     case PH_FFN2: {
         const int n = p.F;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(p.MB + (long long)b * n + i);
+        if (p.tc_proj) {   // GeGLU of the summed gate (rows 0..F-1) and up (rows F..2F-1) partials
+            for (int i = threadIdx.x; i < n; i += blockDim.x)
+                dst[i] = gelu_tanh(part_sum(p, p.sk[PH_FFN1], 2 * n, b, i)) * part_sum(p, p.sk[PH_FFN1], 2 * n, b, n + i);
+        } else {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(p.MB + (long long)b * n + i);
+        }
         __syncthreads();
         break;
     }
@@ -373,12 +409,25 @@ __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l,
         return smem_act;
     }
     // global mode: copy-only inputs are read in place
-    if (phase == PH_O) { lda = K; return p.OB; }
-    if (phase == PH_FFN2) { lda = K; return p.MB; }
-    if (phase == PH_HEAD) { lda = K; return p.HN; }
+    if (!p.tc_proj) {
+        if (phase == PH_O) { lda = K; return p.OB; }
+        if (phase == PH_FFN2) { lda = K; return p.MB; }
+        if (phase == PH_HEAD) { lda = K; return p.HN; }
+    }
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         build_act<WT>(p, phase, k, l, b, smem_act, smem_tmp, true, red);
-        for (int i = threadIdx.x; i < K; i += blockDim.x) p.ACT[(long long)b * p.kmax + i] = smem_act[i];
+        if (p.tc_proj) {
+            // tensor-core operand: bf16 high and low parts, read by tensor copies
+            for (int i = threadIdx.x; i < K; i += blockDim.x) {
+                const float v = smem_act[i];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                p.XA[(long long)b * p.kmax + i] = __bfloat16_as_ushort(hi);
+                p.XAL[(long long)b * p.kmax + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+            }
+            fence_proxy_async_global();
+        } else {
+            for (int i = threadIdx.x; i < K; i += blockDim.x) p.ACT[(long long)b * p.kmax + i] = smem_act[i];
+        }
         __syncthreads();
     }
     ok = grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
@@ -417,55 +466,97 @@ __device__ __forceinline__ int view_lo(const KView& v, int kv_len) {
     return (v.window > 0 && kv_len > v.window) ? kv_len - v.window : 0;
 }
 
-// Item decomposition of the attention phases, per view (the sequence
-// lengths are fixed for a launch): keys per item, number of items, and per
-// sequence the first item and the items per KV head.
+// Key-space partition of an attention phase, per view (the sequence lengths
+// are fixed for a launch): the (sequence b, KV head g) segments lie end to
+// end in b-major order, segment (b, g) holding sequence b's n_b readable
+// keys, T keys in all; CTA c < G takes positions [T c / G, T (c + 1) / G).
+// G is the grid, or fewer CTAs where that would leave each under 16 R keys.
+// A piece is the part of one segment inside one CTA's range.
+// When every segment has the same length and there are no more segments
+// than CTAs, each segment instead gets cseg CTAs of its own (one piece each).
 struct AttnTab {
-    int kpi[MTP_MAX_VIEWS], n_items[MTP_MAX_VIEWS];
-    int first[MTP_MAX_VIEWS][MTP_MAX_BATCH], per_head[MTP_MAX_VIEWS][MTP_MAX_BATCH];
+    long long T[MTP_MAX_VIEWS];
+    int G[MTP_MAX_VIEWS], cseg[MTP_MAX_VIEWS];
+    long long pre[MTP_MAX_VIEWS][MTP_MAX_BATCH + 1];   // positions before sequence b's segments
 };
 // thread v < MTP_MAX_VIEWS fills view v (R: keys per warp slice)
 __device__ __forceinline__ void attn_tab_fill(const DraftParams& p, const int* kv, int R, AttnTab& t) {
     const int v = threadIdx.x;
     if (v >= MTP_MAX_VIEWS) return;
     const KView& vw = p.views[v];
-    long long total = 0;
-    for (int b = 0; b < p.B; ++b) total += (long long)(kv[b] - view_lo(vw, kv[b])) * p.Hkv;
-    // about one item per CTA (two when every CTA would get more than 512
-    // keys, to even out ragged sequence lengths), at least one slice per warp
-    const long long target = (total / gridDim.x <= 512) ? gridDim.x : 2LL * gridDim.x;
-    long long kpi = (total + target - 1) / target;
-    if (kpi < (long long)kWarps * R) kpi = (long long)kWarps * R;
-    kpi = ((kpi + R - 1) / R) * R;
-    const int k32 = (int)kpi;
-    int n = 0;
+    long long T = 0;
     for (int b = 0; b < p.B; ++b) {
-        const int S = (kv[b] - view_lo(vw, kv[b]) + k32 - 1) / k32;
-        t.first[v][b] = n;
-        t.per_head[v][b] = S;
-        n += p.Hkv * S;
+        t.pre[v][b] = T;
+        T += (long long)(kv[b] - view_lo(vw, kv[b])) * p.Hkv;
     }
-    t.kpi[v] = k32;
-    t.n_items[v] = n;
+    t.pre[v][p.B] = T;
+    long long G = T / ((long long)kWarps * R);
+    if (G > (long long)gridDim.x) G = gridDim.x;
+    if (G < 1) G = 1;
+    t.T[v] = T;
+    t.G[v] = (int)G;
+    // equal segments: whole CTAs per segment
+    const int n0 = kv[0] - view_lo(vw, kv[0]), nseg = p.B * p.Hkv;
+    bool equal = true;
+    for (int b = 1; b < p.B; ++b) equal = equal && kv[b] - view_lo(vw, kv[b]) == n0;
+    int c = nseg <= (int)gridDim.x ? (int)gridDim.x / nseg : 0;
+    if (c > n0 / (kWarps * R)) c = n0 / (kWarps * R);
+    t.cseg[v] = equal && c >= 1 ? c : 0;
+}
+// first position of CTA c's range, and the CTA whose range holds position x
+__device__ __forceinline__ long long attn_lo(const AttnTab& t, int v, int c) { return t.T[v] * c / t.G[v]; }
+__device__ __forceinline__ int attn_cta(const AttnTab& t, int v, long long x) {
+    return (int)(((x + 1) * t.G[v] - 1) / t.T[v]);
 }
 
-struct AttnItem {
-    int b, g, s, S, bg_base, t_beg, t_end;
+struct AttnPiece {
+    int b, g, t_beg, t_end;   // keys [t_beg, t_end) of KV head g of sequence b
+    int cf, S;                // first CTA over the segment and their count (S == 1: one piece)
+    int slot;                 // partial slot of this piece: 2 c, or 2 c + 1 for a range's last piece
 };
-__device__ __forceinline__ AttnItem attn_item(const DraftParams& p, const KView& vw, const int* kv,
-                                              const AttnTab& t, int v, int it) {
-    AttnItem r;
+// CTA c's piece starting at position x; `next` = position after it
+__device__ __forceinline__ AttnPiece attn_piece(const DraftParams& p, const KView& vw, const int* kv,
+                                                const AttnTab& t, int v, int c, long long x, long long& next) {
     int b = 0;
-    while (b + 1 < p.B && t.first[v][b + 1] <= it) ++b;
-    const int S = t.per_head[v][b], rel = it - t.first[v][b];
-    r.b = b;
-    r.S = S;
-    r.g = rel / S;
-    r.s = rel - r.g * S;
-    r.bg_base = t.first[v][b] + r.g * S;
-    r.t_beg = view_lo(vw, kv[b]) + r.s * t.kpi[v];
-    r.t_end = r.t_beg + t.kpi[v] < kv[b] ? r.t_beg + t.kpi[v] : kv[b];
-    return r;
+    while (b + 1 < p.B && t.pre[v][b + 1] <= x) ++b;
+    const int lo = view_lo(vw, kv[b]), n = kv[b] - lo;
+    const int g = (int)((x - t.pre[v][b]) / n);
+    const long long s0 = t.pre[v][b] + (long long)g * n, s1 = s0 + n;
+    const long long ce = attn_lo(t, v, c + 1);
+    next = s1 < ce ? s1 : ce;
+    AttnPiece P;
+    P.b = b;
+    P.g = g;
+    P.t_beg = lo + (int)(x - s0);
+    P.t_end = lo + (int)(next - s0);
+    P.cf = attn_cta(t, v, s0);
+    P.S = attn_cta(t, v, s1 - 1) - P.cf + 1;
+    // a split segment is the first piece of every CTA over it but the
+    // first one, whose range began in an earlier segment unless it starts
+    // exactly at the segment
+    P.slot = 2 * c + ((c == P.cf && attn_lo(t, v, c) != s0) ? 1 : 0);
+    return P;
+}
+// equal segments: the piece of CTA c (c < B Hkv cseg)
+__device__ __forceinline__ AttnPiece attn_piece_eq(const DraftParams& p, const KView& vw, const int* kv,
+                                                   const AttnTab& t, int v, int c) {
+    const int cs = t.cseg[v], j = c / cs, sp = c - j * cs;
+    AttnPiece P;
+    P.b = j / p.Hkv;
+    P.g = j - P.b * p.Hkv;
+    // even split: the first n % cs pieces take one key more
+    const int lo = view_lo(vw, kv[P.b]), n = kv[P.b] - lo, q = n / cs, r = n - q * cs;
+    P.t_beg = lo + sp * q + (sp < r ? sp : r);
+    P.t_end = P.t_beg + q + (sp < r ? 1 : 0);
+    P.cf = j * cs;
+    P.S = cs;
+    P.slot = 2 * c;
+    return P;
+}
+// partial slot of the q-th CTA over a split segment starting at position s0
+__device__ __forceinline__ int attn_slot(const AttnTab& t, int v, int cf, int q, long long s0) {
+    if (t.cseg[v] > 0) return 2 * (cf + q);
+    return 2 * (cf + q) + ((q == 0 && attn_lo(t, v, cf) != s0) ? 1 : 0);
 }
 
 // Sum of NV per-lane values over the LPR lanes of a row group, transposed:
@@ -556,11 +647,23 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
     constexpr int PBS = (NV + HG + 3) & ~3;                            // floats per warp, 16-byte multiple
     float* wpb = qs + attn_pb_off(grp, HD, HG);                        // [kWarps][PBS] probabilities, rescales
     float* mypb = wpb + warp * PBS;
-    const int n_items = tab.n_items[view];
+    const int cta = blockIdx.x;
+    const bool eq = tab.cseg[view] > 0;
+    const bool active = eq ? cta < p.B * p.Hkv * tab.cseg[view] : cta < tab.G[view];
+    // the CTA's pieces: one (equal segments) or those of its position range
+    const long long xbeg = active ? (eq ? 0 : attn_lo(tab, view, cta)) : 0;
+    const long long xend = active ? (eq ? 1 : attn_lo(tab, view, cta + 1)) : 0;
+    auto piece = [&](long long x, long long& nx) {
+        if (eq) {
+            nx = 1;
+            return attn_piece_eq(p, vw, kv, tab, view, cta);
+        }
+        return attn_piece(p, vw, kv, tab, view, cta, x, nx);
+    };
     bool any_split = false;
 
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const AttnItem A = attn_item(p, vw, kv, tab, view, it);
+    for (long long x = xbeg, nx = 0; x < xend; x = nx) {
+        const AttnPiece A = piece(x, nx);
         const int b = A.b, g = A.g;
         const int t_beg = A.t_beg, t_end = A.t_end;
         const int nrounds = (t_end - t_beg + kWarps * R - 1) / (kWarps * R);
@@ -606,7 +709,10 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
                 // the step's table
                 if (warp < grp) {
                     constexpr int NQ = (HD / 8 + 31) / 32;   // float4 pairs per lane
-                    const float* qraw = p.QR + ((long long)b * p.Hq + (long long)g * grp + warp) * HD;
+                    // the query projection, or its split partials summed in order
+                    const float* qraw = (p.tc_proj ? p.PB : p.QR) + ((long long)b * p.Hq + (long long)g * grp + warp) * HD;
+                    const int qS = p.tc_proj ? p.sk[PH_Q] : 1;
+                    const long long qst = (long long)p.B * p.Hq * HD;
                     const float* gq = p.blk[l].q_norm;
                     const float4* cs = reinterpret_cast<const float4*>(
                         p.ROPEQ + ((long long)b * MTP_MAX_VIEWS + view) * (HD / 2));
@@ -622,6 +728,24 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
                             gb[u] = __ldg(reinterpret_cast<const float4*>(gq + HD / 2) + i4);
                             c0[u] = __ldcg(cs + 2 * i4);
                             c1[u] = __ldcg(cs + 2 * i4 + 1);
+                        }
+                    }
+                    if (qS > 1) {   // remaining split partials, after the first loads are in flight
+#pragma unroll
+                        for (int u = 0; u < NQ; ++u) {
+                            const int i4 = lane + 32 * u;
+                            if (i4 < HD / 8) {
+                                const float4 a2 = ld4_sum(qraw + qst + 4 * i4, qS - 1, qst);
+                                const float4 b2 = ld4_sum(qraw + qst + HD / 2 + 4 * i4, qS - 1, qst);
+                                qa[u] = make_float4(qa[u].x + a2.x, qa[u].y + a2.y, qa[u].z + a2.z, qa[u].w + a2.w);
+                                qb[u] = make_float4(qb[u].x + b2.x, qb[u].y + b2.y, qb[u].z + b2.z, qb[u].w + b2.w);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < NQ; ++u) {
+                        const int i4 = lane + 32 * u;
+                        if (i4 < HD / 8) {
                             ss += qa[u].x * qa[u].x + qa[u].y * qa[u].y + qa[u].z * qa[u].z + qa[u].w * qa[u].w;
                             ss += qb[u].x * qb[u].x + qb[u].y * qb[u].y + qb[u].z * qb[u].z + qb[u].w * qb[u].w;
                         }
@@ -866,7 +990,7 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
                 if (A.S == 1) {
                     p.OB[((long long)b * p.Hq + (long long)g * grp + h) * HD + d] = O / Ls;
                 } else {
-                    float* part = p.PART + (long long)it * PSZ;
+                    float* part = p.PART + (long long)A.slot * PSZ;
                     part[h * HD + d] = O;
                     if (d == 0) {
                         part[grp * HD + h] = wex[kWarps * HG + hh];
@@ -888,21 +1012,22 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
     // outputs over all S partials (lanes over partials, warps over outputs,
     // up to MJ outputs of a warp with their loads in flight together)
     constexpr int MJ = 4;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const AttnItem A = attn_item(p, vw, kv, tab, view, it);
+    for (long long x = xbeg, nx = 0; x < xend; x = nx) {
+        const AttnPiece A = piece(x, nx);
         if (A.S == 1) continue;
         if (!count_wait(p.att_cnt + A.b * p.Hkv + A.g, (unsigned int)A.S, p.hdr, p.timeout_ns)) return false;
         const int no = grp * HD;
         const int per = (no + A.S - 1) / A.S;
-        const int o0 = A.s * per, o1 = o0 + per < no ? o0 + per : no;
-        const float* src = p.PART + (long long)A.bg_base * PSZ;
+        const int o0 = (cta - A.cf) * per, o1 = o0 + per < no ? o0 + per : no;
+        // the segment's first position (key-space partition)
+        const long long s0 = eq ? 0 : x - (A.t_beg - view_lo(vw, kv[A.b]));
         float* dst = p.OB + ((long long)A.b * p.Hq + (long long)A.g * grp) * HD;
         for (int j0 = o0 + warp; j0 < o1; j0 += MJ * kWarps) {
             float mm[MJ], ll[MJ], oo[MJ];
 #pragma unroll
             for (int u = 0; u < MJ; ++u) { mm[u] = -INFINITY; ll[u] = 0.f; oo[u] = 0.f; }
             for (int q = lane; q < A.S; q += 32) {
-                const float* pq = src + (long long)q * PSZ;
+                const float* pq = p.PART + (long long)attn_slot(tab, view, A.cf, q, s0) * PSZ;
                 float mq[MJ], lq[MJ], oq[MJ];
 #pragma unroll
                 for (int u = 0; u < MJ; ++u) {
@@ -1031,38 +1156,58 @@ __device__ bool head_groups_b1(const DraftParams& p, unsigned char* ring, unsign
     return true;
 }
 
-// Tensor-core LM head (bf16, B >= 8): logits[row, b] = E[row, :] . h[b, :]
-// as D = A B^T with A a 128-row tile of the token table and B the padded
-// batch of h split into bf16 high and low parts (two MMAs per K slice, so
-// the product carries about 16 mantissa bits of h).  CTA c takes row tiles
-// c, c + grid, ...; warp 0 (one lane) streams A and B tiles through a
-// tc_stages-deep ring with tensor copies, warp 1 (one lane) issues the MMAs
-// into one of two tensor-memory accumulators, and warps 4-7 read the
-// accumulator rows (one tensor-memory lane per row) and fold the argmax per
-// sequence.  The barrier phases continue across calls through `ts`.
+// Tensor-core GEMM D[R, Bp] = W[R, K] X[Bp, K]^T (bf16, fp32 accumulate),
+// with X split into bf16 high and low parts (two MMAs per K slice, so the
+// product carries about 16 mantissa bits of X).  Work items are (128-row
+// tile, K split); CTA c takes items c, c + grid, ...  Warp 0 (one lane)
+// streams the W and X tiles by tensor copies through a tc_stages-deep ring,
+// warp 1 (one lane) issues the MMAs into one of two tensor-memory
+// accumulators, and warps 4-7 read the accumulator (one tensor-memory lane
+// per output row, 16 columns at a time) into the epilogue.  Barrier phases
+// continue across calls through `ts`.
 struct TcState {
     unsigned long long *full, *empty, *tfull, *tempty;
     unsigned int tmem;   // tensor-memory base address
-    unsigned int g, it;  // K steps and tiles this CTA has processed so far
+    unsigned int g, it;  // K steps and items this CTA has processed so far
 };
 
-template <typename WT>
-__device__ bool head_tc(const DraftParams& p, int k, unsigned char* smem, TcState& ts, HeadEpi& e) {
+struct TcJob {
+    const CUtensorMap *wa, *wb;   // W rows [0, R1) and [R1, R) (wb: rows counted from R1)
+    const CUtensorMap *xh, *xl;   // X high / low parts, box 64 x Bp
+    int R1, R, nks, S, kps;       // rows, K steps of 64, K splits, K steps per split
+};
+
+template <class Epi>
+__device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsigned char* smem, TcState& ts, Epi& epi) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int Bp = p.Bp, NS = p.tc_stages;
-    const int nks = (p.d_t + kTcTileK - 1) / kTcTileK;
-    const int ntiles = (p.V + kTcTileM - 1) / kTcTileM;
-    const int nit = ntiles > (int)blockIdx.x ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    const int ntiles = (J.R + kTcTileM - 1) / kTcTileM, nitems = ntiles * J.S;
+    const int nit = nitems > (int)blockIdx.x ? (nitems - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     const uint32_t abytes = kTcTileM * 128, xbytes = (uint32_t)Bp * 128, sbytes = abytes + 2 * xbytes;
     const uint32_t base = (smem_addr(smem) + 1023u) & ~1023u;   // 1024-byte aligned ring
     unsigned char* ring = smem + (base - smem_addr(smem));
+    auto ksteps = [&](int item, int& k0) {   // K steps of an item: [k0, k0 + n)
+        k0 = (item % J.S) * J.kps;
+        const int k1 = k0 + J.kps < J.nks ? k0 + J.kps : J.nks;
+        return k1 - k0;
+    };
+    uint32_t nsteps = 0;   // K steps of this CTA's items (same on every thread)
+    for (int j = 0; j < nit; ++j) {
+        int k0;
+        nsteps += (uint32_t)ksteps((int)blockIdx.x + j * (int)gridDim.x, k0);
+    }
     bool ok = true;
     if (warp == 0) {
         if (lane == 0) {
             uint32_t g = ts.g;
             for (int j = 0; j < nit && ok; ++j) {
-                const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * kTcTileM;
-                for (int ks = 0; ks < nks; ++ks, ++g) {
+                const int item = (int)blockIdx.x + j * (int)gridDim.x;
+                const int row0 = (item / J.S) * kTcTileM;
+                const CUtensorMap* wm = row0 < J.R1 ? J.wa : J.wb;
+                const int wy = row0 < J.R1 ? row0 : row0 - J.R1;
+                int k0;
+                const int n = ksteps(item, k0);
+                for (int ks = k0; ks < k0 + n; ++ks, ++g) {
                     const uint32_t st = g % NS;
                     if (!mbar_wait_limited(&ts.empty[st], ((g / NS) & 1u) ^ 1u, p.timeout_ns)) {
                         ok = false;
@@ -1070,9 +1215,9 @@ __device__ bool head_tc(const DraftParams& p, int k, unsigned char* smem, TcStat
                     }
                     unsigned char* sp = ring + st * sbytes;
                     mbar_arrive_expect_tx(&ts.full[st], sbytes);
-                    tma_load_2d(sp, &p.tm_embd, ks * kTcTileK, row0, &ts.full[st]);
-                    tma_load_2d(sp + abytes, &p.tm_xh, ks * kTcTileK, 0, &ts.full[st]);
-                    tma_load_2d(sp + abytes + xbytes, &p.tm_xl, ks * kTcTileK, 0, &ts.full[st]);
+                    tma_load_2d(sp, wm, ks * kTcTileK, wy, &ts.full[st]);
+                    tma_load_2d(sp + abytes, J.xh, ks * kTcTileK, 0, &ts.full[st]);
+                    tma_load_2d(sp + abytes + xbytes, J.xl, ks * kTcTileK, 0, &ts.full[st]);
                 }
             }
         }
@@ -1088,7 +1233,9 @@ __device__ bool head_tc(const DraftParams& p, int k, unsigned char* smem, TcStat
                 }
                 tc_fence_after();
                 const uint32_t d = ts.tmem + acc * (uint32_t)Bp;
-                for (int ks = 0; ks < nks; ++ks, ++g) {
+                int k0;
+                const int n = ksteps((int)blockIdx.x + j * (int)gridDim.x, k0);
+                for (int ks = 0; ks < n; ++ks, ++g) {
                     const uint32_t st = g % NS;
                     if (!mbar_wait_limited(&ts.full[st], (g / NS) & 1u, p.timeout_ns)) {
                         ok = false;
@@ -1117,45 +1264,126 @@ __device__ bool head_tc(const DraftParams& p, int k, unsigned char* smem, TcStat
                 break;
             }
             tc_fence_after();
-            const int row = ((int)blockIdx.x + j * (int)gridDim.x) * kTcTileM + 32 * q + lane;
+            const int item = (int)blockIdx.x + j * (int)gridDim.x;
+            const int row = (item / J.S) * kTcTileM + 32 * q + lane;
             const uint32_t ta = ts.tmem + ((uint32_t)(32 * q) << 16) + acc * (uint32_t)Bp;
             for (int c0 = 0; c0 < Bp; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(ta + (uint32_t)c0, r);
                 tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int b = c0 + jj;
-                    if (b < p.B) {
-                        float z = __uint_as_float(r[jj]);
-                        if (p.softcap > 0.f) z = p.softcap * tanhf(z / p.softcap);
-                        if (row < p.V && p.out_logits) p.out_logits[((long long)b * p.N + k) * p.V + row] = z;
-                        const unsigned long long key = warp_max_u64(row < p.V ? pack_argmax(z, (uint32_t)row) : 0ull);
-                        if (lane == (b & 31)) {
-                            if (b < 32) e.best_lo = key > e.best_lo ? key : e.best_lo;
-                            else e.best_hi = key > e.best_hi ? key : e.best_hi;
-                        }
-                    }
-                }
+                epi.apply(row, item % J.S, c0, r);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ts.tempty[acc]);
         }
     }
-    ts.g += (uint32_t)(nit * nks);
+    ts.g += nsteps;
     ts.it += (uint32_t)nit;
     return __syncthreads_and(ok) != 0;
 }
 
-template <typename WT>
+// epilogue: LM-head logits -> softcap, optional store, per-sequence argmax
+// (all lanes of a warp call it with the same c0)
+struct TcHeadEpi {
+    const DraftParams& p;
+    int k;
+    HeadEpi& e;
+    __device__ __forceinline__ void apply(int row, int, int c0, const uint32_t (&r)[16]) {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int b = c0 + jj;
+            if (b < p.B) {
+                float z = __uint_as_float(r[jj]);
+                if (p.softcap > 0.f) z = p.softcap * tanhf(z / p.softcap);
+                if (row < p.V && p.out_logits) p.out_logits[((long long)b * p.N + k) * p.V + row] = z;
+                const unsigned long long key = warp_max_u64(row < p.V ? pack_argmax(z, (uint32_t)row) : 0ull);
+                if (lane == (b & 31)) {
+                    if (b < 32) e.best_lo = key > e.best_lo ? key : e.best_lo;
+                    else e.best_hi = key > e.best_hi ? key : e.best_hi;
+                }
+            }
+        }
+    }
+};
+
+// epilogue: split partial of a projection, PB[split][b][row]
+struct TcPartEpi {
+    float* PB;
+    int B, R;
+    __device__ __forceinline__ void apply(int row, int split, int c0, const uint32_t (&r)[16]) {
+        if (row >= R) return;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int b = c0 + jj;
+            if (b < B) PB[((long long)split * B + b) * R + row] = __uint_as_float(r[jj]);
+        }
+    }
+};
+
+// epilogue: unsplit post-projection: h and its bf16 high / low parts
+struct TcHnEpi {
+    float* HN;
+    uint16_t *XH, *XL;
+    int B, R;
+    __device__ __forceinline__ void apply(int row, int, int c0, const uint32_t (&r)[16]) {
+        if (row >= R) return;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int b = c0 + jj;
+            if (b < B) {
+                const long long i = (long long)b * R + row;
+                const float v = __uint_as_float(r[jj]);
+                HN[i] = v;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                XH[i] = __bfloat16_as_ushort(hi);
+                XL[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+            }
+        }
+    }
+};
+
+// job of projection phase `phase` of block l over the staged inputs
+__device__ __forceinline__ TcJob tc_job(const DraftParams& p, int phase, int l) {
+    TcJob J;
+    J.xh = &p.tm_xa;
+    J.xl = &p.tm_xal;
+    int K = 0;
+    switch (phase) {
+    case PH_PRE: J.wa = J.wb = &p.tm_w[0]; J.R = p.d_a; K = 2 * p.d_t; break;
+    case PH_Q: J.wa = J.wb = &p.tm_w[2 + 5 * l]; J.R = p.Hq * p.hd; K = p.d_a; break;
+    case PH_O: J.wa = J.wb = &p.tm_w[2 + 5 * l + 1]; J.R = p.d_a; K = p.Hq * p.hd; break;
+    case PH_FFN1: J.wa = &p.tm_w[2 + 5 * l + 2]; J.wb = &p.tm_w[2 + 5 * l + 3]; J.R = 2 * p.F; K = p.d_a; break;
+    case PH_FFN2: J.wa = J.wb = &p.tm_w[2 + 5 * l + 4]; J.R = p.d_a; K = p.F; break;
+    default: J.wa = J.wb = &p.tm_w[1]; J.R = p.d_t; K = p.d_a; break;   // PH_POST
+    }
+    J.R1 = phase == PH_FFN1 ? p.F : J.R;
+    J.nks = (K + kTcTileK - 1) / kTcTileK;
+    J.S = p.sk[phase];
+    J.kps = (J.nks + J.S - 1) / J.S;
+    return J;
+}
+
+template <typename WT, bool TC>
 __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const float* a, int lda,
                                            unsigned long long (*head_best)[32], unsigned char* smem,
                                            unsigned long long (*bars)[kHeadSlots], unsigned int& par,
                                            float (*hpart)[kHeadSlots][4], TcState& ts) {
     HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull};
-    if (p.tc_head) {
-        if (!head_tc<WT>(p, k, smem, ts, e)) return false;
+    if (TC && p.tc_head) {
+        TcJob J;
+        J.wa = J.wb = &p.tm_embd;
+        J.xh = &p.tm_xh;
+        J.xl = &p.tm_xl;
+        J.R1 = J.R = p.V;
+        J.nks = (p.d_t + kTcTileK - 1) / kTcTileK;
+        J.S = 1;
+        J.kps = J.nks;
+        TcHeadEpi he{p, k, e};
+        if constexpr (TC) {
+            if (!tc_gemm(p, J, smem, ts, he)) return false;
+        }
     } else if (p.head_slotb > 0) {
         const int cpl = (p.d_t / Chunk<WT>::EPC + 127) / 128;
         bool ok = true;
@@ -1187,7 +1415,7 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <typename WT, int HD>
+template <typename WT, int HD, bool TC>
 __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts) {
     __shared__ float red[kWarps];
     __shared__ unsigned long long head_best[kWarps][32];
@@ -1222,7 +1450,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         for (int i = threadIdx.x; i < p.N * p.B; i += blockDim.x) p.amax[i] = 0ull;
     // tensor-core head: zero rows B..Bp-1 of the bf16 parts of h (read by
     // tensor copies, first after >= 1 barrier)
-    if (p.tc_head && blockIdx.x == 0) {
+    if (TC && p.tc_head && blockIdx.x == 0) {
         for (long long i = (long long)p.B * p.d_t + threadIdx.x; i < (long long)p.Bp * p.d_t; i += blockDim.x) {
             p.XH[i] = 0;
             p.XL[i] = 0;
@@ -1254,9 +1482,24 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         bool ok = true;
         const float* a = stage_act<WT>(p, phase, k, l, act, tmp, red, epoch, lda, ok);
         if (!ok) return false;
-        gemv<WT, TWO ? U / 2 : U, TWO>(reinterpret_cast<const WT*>(W), reinterpret_cast<const WT*>(W2), R, K, a, lda,
-                                       p.B, epi);
-        if (p.tc_head && phase == PH_POST) fence_proxy_async_global();   // h parts are read by tensor copies
+        if (TC && p.tc_proj) {
+            // tensor cores over the staged bf16 input parts: split partials,
+            // or (post-projection, unsplit) h and its bf16 parts for the head
+            if constexpr (TC) {
+                const TcJob J = tc_job(p, phase, l);
+                if (phase == PH_POST) {
+                    TcHnEpi he{p.HN, p.XH, p.XL, p.B, p.d_t};
+                    if (!tc_gemm(p, J, smem, ts, he)) return false;
+                } else {
+                    TcPartEpi pe{p.PB, p.B, J.R};
+                    if (!tc_gemm(p, J, smem, ts, pe)) return false;
+                }
+            }
+        } else {
+            gemv<WT, TWO ? U / 2 : U, TWO>(reinterpret_cast<const WT*>(W), reinterpret_cast<const WT*>(W2), R, K, a,
+                                           lda, p.B, epi);
+        }
+        if (TC && p.tc_head && phase == PH_POST) fence_proxy_async_global();   // h parts are read by tensor copies
         return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
     };
     using One = std::integral_constant<bool, false>;
@@ -1319,7 +1562,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             }
         }
         // ---- POST ----
-        if (p.tc_head) {
+        if (TC && p.tc_head) {
             StoreHiLoEpi e{p.HN, p.d_t, p.XH, p.XL};
             if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         } else {
@@ -1330,11 +1573,11 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         {
             int lda = 0;
             const float* a = nullptr;
-            if (p.head_slotb == 0 && !p.tc_head) {
+            if (p.head_slotb == 0 && !(TC && p.tc_head)) {
                 a = stage_act<WT>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
                 if (!ok) return;
             }
-            if (!head_phase<WT>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part, ts)) return;
+            if (!head_phase<WT, TC>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part, ts)) return;
         }
         if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
     }
@@ -1347,17 +1590,17 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     }
 }
 
-// The persistent draft kernel: tensor memory (when the LM head runs on tensor
-// cores) is allocated by warp 2 before the body and freed after it; every
-// exit of the body is uniform over the CTA.
-template <typename WT, int HD>
+// The persistent draft kernel.  TC: the variant with the tensor-core paths,
+// whose tensor memory is allocated by warp 2 before the body and freed after
+// it; every exit of the body is uniform over the CTA.
+template <typename WT, int HD, bool TC>
 __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ __align__(8) unsigned long long tc_bar[2 * kTcMaxStages + 4];
     __shared__ unsigned int tc_tmem;
     TcState ts{tc_bar, tc_bar + kTcMaxStages, tc_bar + 2 * kTcMaxStages, tc_bar + 2 * kTcMaxStages + 2, 0u, 0u, 0u};
     const int warp = threadIdx.x >> 5;
-    if (p.tc_head) {
+    if (TC && p.tc_head) {
         // full / empty stage barriers (one arrival each), accumulator full
         // (one commit) and empty (one arrival per epilogue warp)
         if (threadIdx.x < 2 * kTcMaxStages + 4)
@@ -1372,8 +1615,8 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         tc_fence_after();
         ts.tmem = tc_tmem;
     }
-    draft_body<WT, HD>(p, smem, ts);
-    if (p.tc_head) {
+    draft_body<WT, HD, TC>(p, smem, ts);
+    if (TC && p.tc_head) {
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -1381,19 +1624,21 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     }
 }
 
-template <typename WT, int HD>
+template <typename WT, int HD, bool TC>
 cudaError_t launch_draft_t(const DraftParams& p, int grid, size_t smem, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(draft_kernel<WT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(draft_kernel<WT, HD, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<DraftParams*>(&p)};
-    return cudaLaunchCooperativeKernel((const void*)draft_kernel<WT, HD>, dim3(grid), dim3(kThreads), args, smem, s);
+    return cudaLaunchCooperativeKernel((const void*)draft_kernel<WT, HD, TC>, dim3(grid), dim3(kThreads), args, smem, s);
 }
 
-template <typename WT, int HD>
+template <typename WT, int HD, bool TC>
 int draft_blocks_per_sm_t(size_t smem) {
     int n = 0;
-    cudaFuncSetAttribute(draft_kernel<WT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draft_kernel<WT, HD>, kThreads, smem) != cudaSuccess) return 0;
+    cudaFuncSetAttribute(draft_kernel<WT, HD, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draft_kernel<WT, HD, TC>, kThreads, smem) != cudaSuccess)
+        return 0;
     return n;
 }
 
