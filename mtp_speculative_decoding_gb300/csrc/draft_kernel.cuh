@@ -619,13 +619,15 @@ __device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// abar: [kWarps][kAttnStages] stage barriers (one arrival each); apar: the
+// calling warp's stage phase bits, carried across calls.
 template <typename WT, int HD>
-__device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem, const int* kv, const AttnTab& tab) {
+__device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem, const int* kv, const AttnTab& tab,
+                                unsigned long long* abar, unsigned int& apar) {
     constexpr AttnGeom G = attn_geom(HD, (int)sizeof(WT));
-    constexpr int RB = G.RB, CPR = G.CPR, LPR = G.LPR, CPL = G.CPL, KPW = G.KPW, EPC = G.EPC, DPL = G.DPL;
+    constexpr int RB = G.RB, LPR = G.LPR, CPL = G.CPL, KPW = G.KPW, EPC = G.EPC, DPL = G.DPL;
     constexpr int R = G.R, RL = G.RL, SB = G.SB, HG = G.HG, NST = kAttnStages;
     constexpr int RING = kWarps * NST * SB;
-    constexpr int CPT = SB / 16 / 32;   // cp.async chunks per lane and stage
     constexpr int NV = RL * HG;         // scores per lane and round
     // one K/V row per warp and NV <= 32: scores summed transposed, softmax on
     // one lane per score, probabilities broadcast through shared memory
@@ -660,7 +662,11 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
         }
         return attn_piece(p, vw, kv, tab, view, cta, x, nx);
     };
-    bool any_split = false;
+    const bool packed = vw.st == HD;   // consecutive ring slots are contiguous rows
+    bool any_split = false, aok = true;
+    // earlier generic shared-memory accesses before the stage copies
+    fence_proxy_async_smem();
+    __syncthreads();
 
     for (long long x = xbeg, nx = 0; x < xend; x = nx) {
         const AttnPiece A = piece(x, nx);
@@ -676,28 +682,27 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
             const int c = t_end - t0;
             return rd < nrounds ? (c < 0 ? 0 : (c < R ? c : R)) : 0;
         };
-        // one commit group per round and warp (empty past the range)
+        // lane 0: bulk copies of round rd's K and V rows into the warp's
+        // stage rd % NST, one copy per run of consecutive ring slots when
+        // rows are packed, completing on the stage barrier (nothing for an
+        // empty slice: its stage is neither filled nor waited on)
         auto issue = [&](int rd) {
             int t0;
             const int cnt = slice_cnt(rd, t0);
-            if (cnt > 0) {
-                unsigned char* buf = myring + (rd % NST) * SB;
-                const int s0 = t0 % vw.cap;
-#pragma unroll
-                for (int u = 0; u < CPT; ++u) {
-                    const int c = lane + 32 * u;   // chunk of [K rows | V rows]
-                    const int which = c / (R * CPR);
-                    const int r = (c / CPR) % R;
-                    const int q = c % CPR;
-                    if (r < cnt) {
-                        int slot = s0 + r;
-                        if (slot >= vw.cap) slot %= vw.cap;
-                        cp_async16(buf + which * R * RB + r * RB + q * 16,
-                                   (which ? vbase : kbase) + (long long)slot * vw.st + q * EPC);
-                    }
+            if (cnt > 0 && lane == 0) {
+                const int si = rd % NST;
+                unsigned char* buf = myring + si * SB;
+                unsigned long long* bar = abar + warp * NST + si;
+                mbar_arrive_expect_tx(bar, 2u * (unsigned int)cnt * RB);
+                for (int r = 0; r < cnt;) {
+                    const int slot = (t0 + r) % vw.cap;
+                    int run = packed ? cnt - r : 1;
+                    if (run > vw.cap - slot) run = vw.cap - slot;
+                    bulk_g2s(buf + r * RB, kbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar);
+                    bulk_g2s(buf + R * RB + r * RB, vbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar);
+                    r += run;
                 }
             }
-            cp_async_commit();
         };
 
         for (int h0 = 0; h0 < grp; h0 += HG) {
@@ -812,13 +817,14 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
             }
 
             for (int i = 0; i < nrounds; ++i) {
-                issue(i + 1);
-                cp_async_wait<1>();
-                __syncwarp();
+                issue(i + 1);   // its stage was consumed in round i - 1
                 int t0;
                 const int cnt = slice_cnt(i, t0);
                 if (cnt > 0) {
-                    const unsigned char* kb = myring + (i % NST) * SB;
+                    const int si = i % NST;
+                    if (!mbar_wait_limited(abar + warp * NST + si, (apar >> si) & 1u, p.timeout_ns)) aok = false;
+                    apar ^= 1u << si;
+                    const unsigned char* kb = myring + si * SB;
                     const unsigned char* vb = kb + R * RB;
                     float sc[NV];   // [RL][HG]
 #pragma unroll
@@ -1000,11 +1006,16 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
             }
         }
 
+        fence_proxy_async_smem();   // the merge's shared-memory writes before the next stage copies
         __syncthreads();
         if (A.S > 1) {
             any_split = true;
             if (tid == 0) red_release_add(p.att_cnt + b * p.Hkv + g, 1u);
         }
+    }
+    if (!__syncthreads_and(aok)) {
+        if (threadIdx.x == 0) atomicCAS(&p.hdr->status, 0, MTP_ERR_TIMEOUT);
+        return false;
     }
     if (!any_split) return true;
 
@@ -1422,6 +1433,8 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     __shared__ __align__(8) unsigned long long head_bar[kHeadGroups][kHeadSlots];   // LM head slots
     __shared__ float head_part[kHeadGroups][kHeadSlots][4];
     unsigned int head_par = 0;
+    __shared__ __align__(8) unsigned long long attn_bar[kWarps][kAttnStages];   // attention stage barriers
+    unsigned int attn_par = 0;
     unsigned int epoch = 0;
     float* tmp = reinterpret_cast<float*>(smem);                 // [max(d_a)] residual scratch
     float* act = tmp + ((p.d_a + 3) & ~3);                       // activations
@@ -1472,6 +1485,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     }
 
     if (threadIdx.x < kHeadGroups * kHeadSlots) mbar_init(&head_bar[0][0] + threadIdx.x, 1);
+    if (threadIdx.x < kWarps * kAttnStages) mbar_init(&attn_bar[0][0] + threadIdx.x, 1);
     mbar_fence_init();
     __syncthreads();
     // one GEMV phase and the barrier after it
@@ -1540,7 +1554,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 if (!gemv_step(PH_Q, k, l, bw.w_q, nullptr, p.Hq * p.hd, p.d_a, e, One{})) return;
             }
             // ---- ATT ----
-            if (!attention_phase<WT, HD>(p, l, smem, s_kv, s_tab)) return;
+            if (!attention_phase<WT, HD>(p, l, smem, s_kv, s_tab, &attn_bar[0][0], attn_par)) return;
             if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
             // every CTA has passed its attention waits: reset the item counters
             if (blockIdx.x == 0)
