@@ -80,7 +80,7 @@ int draft_grid() {
 }
 
 struct DraftLayout {
-    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ACT, end;
+    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, XH, XA, XAL, PB, ACT, end;
     int kmax;
 };
 
@@ -113,11 +113,11 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     L.PART = off;    off = al256(off + items * attn_psz(grp, c->head_dim) * f);
     L.ROPE = off;    off = al256(off + (size_t)MTP_MAX_VIEWS * (c->head_dim / 2) * sizeof(double));
     L.ROPEQ = off;   off = al256(off + (size_t)B * MTP_MAX_VIEWS * (c->head_dim / 2) * 2 * f);
-    const size_t xb = tc_head_eligible(c, B) ? (size_t)pad16(B) * c->d_t * 2 : 0;
+    // tensor-core operands: K blocks of 64 columns x Bp rows, bf16
+    const size_t xb = tc_head_eligible(c, B) ? (size_t)((c->d_t + 63) / 64) * pad16(B) * 128 : 0;
     L.XH = off;      off = al256(off + xb);
-    L.XL = off;      off = al256(off + xb);
     const bool tcp = tc_proj_eligible(c, B);
-    const size_t xa = tcp ? (size_t)pad16(B) * L.kmax * 2 : 0;
+    const size_t xa = tcp ? (size_t)((L.kmax + 63) / 64) * pad16(B) * 128 : 0;
     L.XA = off;      off = al256(off + xa);
     L.XAL = off;     off = al256(off + xa);
     L.PB = off;      off = al256(off + (tcp ? tc_plan(c, B, draft_grid()).pb_floats * f : 0));
@@ -374,10 +374,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         p.tc_stages = tc_stages;
         p.tc_cols = tc_cols;
         p.XH = reinterpret_cast<uint16_t*>(base + L.XH);
-        p.XL = reinterpret_cast<uint16_t*>(base + L.XL);
-        if (!encode_bf16_map(&p.tm_embd, w->tok_embd, (uint64_t)cfg->d_t, (uint64_t)cfg->vocab, kTcTileM) ||
-            !encode_bf16_map(&p.tm_xh, p.XH, (uint64_t)cfg->d_t, (uint64_t)p.Bp, (uint32_t)p.Bp) ||
-            !encode_bf16_map(&p.tm_xl, p.XL, (uint64_t)cfg->d_t, (uint64_t)p.Bp, (uint32_t)p.Bp))
+        if (!encode_bf16_map(&p.tm_embd, w->tok_embd, (uint64_t)cfg->d_t, (uint64_t)cfg->vocab, kTcTileM))
             return MTP_ERR_CUDA;
         if (tc_proj_eligible(cfg, B) && !act_smem) {
             // projections: weights [R, K] row-major, inputs staged as [Bp, kmax]
@@ -388,9 +385,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
             p.XAL = reinterpret_cast<uint16_t*>(base + L.XAL);
             p.PB = reinterpret_cast<float*>(base + L.PB);
             const uint64_t da = cfg->d_a, dt = cfg->d_t, F = cfg->d_ff, qd = (uint64_t)cfg->n_q_heads * cfg->head_dim;
-            bool okm = encode_bf16_map(&p.tm_xa, p.XA, (uint64_t)L.kmax, (uint64_t)p.Bp, (uint32_t)p.Bp) &&
-                       encode_bf16_map(&p.tm_xal, p.XAL, (uint64_t)L.kmax, (uint64_t)p.Bp, (uint32_t)p.Bp) &&
-                       encode_bf16_map(&p.tm_w[0], w->w_pre, 2 * dt, da, kTcTileM) &&
+            bool okm = encode_bf16_map(&p.tm_w[0], w->w_pre, 2 * dt, da, kTcTileM) &&
                        encode_bf16_map(&p.tm_w[1], w->w_post, da, dt, kTcTileM);
             for (int l = 0; l < cfg->n_blocks && okm; ++l) {
                 const mtp_block_weights& bw = w->blk[l];

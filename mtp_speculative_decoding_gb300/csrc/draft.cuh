@@ -72,14 +72,10 @@ struct BlkW {
 };
 
 struct DraftParams {
-    // tensor-core LM head: maps of the token table [V, d_t] (box 64 x 128)
-    // and of the bf16 high / low parts of h [Bp, d_t] (box 64 x Bp), all
-    // with 128-byte swizzle
-    CUtensorMap tm_embd, tm_xh, tm_xl;
-    // projections on tensor cores: the bf16 high / low parts of a phase's
-    // inputs [Bp, kmax] (box 64 x Bp) and every projection weight (box 64 x
-    // 128): pre, post, then per block q, o, gate, up, down
-    CUtensorMap tm_xa, tm_xal;
+    // tensor-core weights, box 64 x 128 with 128-byte swizzle: the token
+    // table [V, d_t], then the projections: pre, post, per block q, o, gate,
+    // up, down
+    CUtensorMap tm_embd;
     CUtensorMap tm_w[2 + 5 * MTP_MAX_BLOCKS];
     int d_t, d_a, L, Hq, hd, Hkv, F, V, B, N;
     float eps, attn_scale, emb_scale, softcap;
@@ -110,10 +106,10 @@ struct DraftParams {
     int head_slotb;              // > 0: one sequence, LM head rows through bulk-copy slots of this many bytes
     int tc_head;                 // 1: LM head on tensor cores
     int Bp, tc_stages, tc_cols;  // batch padded to 16; operand ring depth; tensor-memory columns
-    uint16_t *XH, *XL;           // [Bp, d_t] bf16 high / low parts of h (rows >= B zero)
+    uint16_t* XH;                // bf16(h) as the head's tiled operand (rows >= B zero)
     int tc_proj;                 // 1: projections on tensor cores (activations staged in global memory)
     int sk[6];                   // split-K factor of each projection phase (PH_PRE .. PH_POST)
-    uint16_t *XA, *XAL;          // [Bp, kmax] bf16 high / low parts of the current phase input
+    uint16_t *XA, *XAL;          // bf16 high / low parts of the current phase input, tiled
     float* PB;                   // [S][B][R] split partials of the last projection (FFN1: R = 2 F)
     int kmax;
     unsigned long long timeout_ns;

@@ -166,24 +166,31 @@ struct StoreEpi {
     }
 };
 
-// out[b * ldo + r] = v, plus the bf16 high and low parts of v (v ~ hi + lo)
-// as the tensor-core operand rows xh[b * ldo + r], xl[b * ldo + r]
-struct StoreHiLoEpi {
+// Tensor-core operand rows (batch b, column k) live in global memory in the
+// shared-memory image of the MMA's K-major 128-byte-swizzled tiles: per K
+// block of 64 columns, Bp rows of 128 bytes with 16-byte chunk c of row b
+// at chunk position c ^ (b % 8), so one bulk copy of a block lands ready
+// for the MMA.  Element index of (b, k):
+__device__ __forceinline__ long long xtile_idx(int b, int k, int Bp) {
+    const int kb = k >> 6, kk = k & 63;
+    return ((long long)kb * Bp + b) * 64 + ((((kk >> 3) ^ (b & 7)) << 3) | (kk & 7));
+}
+
+// out[b * ldo + r] = v, plus bf16(v) as tensor-core operand element (b, r)
+struct StoreXhEpi {
     float* out;
     int ldo;
-    uint16_t *xh, *xl;
+    uint16_t* xh;
+    int Bp;
     template <int NB>
     __device__ __forceinline__ void apply(int r, int b0, int nb, const float (&acc)[NB], const float (&)[NB]) {
         const int lane = threadIdx.x & 31;
 #pragma unroll
         for (int j = 0; j < NB; ++j)
             if (lane == j && b0 + j < nb) {
-                const long long i = (long long)(b0 + j) * ldo + r;
                 const float v = acc[j];
-                out[i] = v;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-                xh[i] = __bfloat16_as_ushort(hi);
-                xl[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+                out[(long long)(b0 + j) * ldo + r] = v;
+                xh[xtile_idx(b0 + j, r, Bp)] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
             }
     }
 };
@@ -421,8 +428,9 @@ __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l,
             for (int i = threadIdx.x; i < K; i += blockDim.x) {
                 const float v = smem_act[i];
                 const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-                p.XA[(long long)b * p.kmax + i] = __bfloat16_as_ushort(hi);
-                p.XAL[(long long)b * p.kmax + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+                const long long xi = xtile_idx(b, i, p.Bp);
+                p.XA[xi] = __bfloat16_as_ushort(hi);
+                p.XAL[xi] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
             }
             fence_proxy_async_global();
         } else {
@@ -1023,6 +1031,7 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
     // outputs over all S partials (lanes over partials, warps over outputs,
     // up to MJ outputs of a warp with their loads in flight together)
     constexpr int MJ = 4;
+    constexpr int kMergeFew = 8;
     for (long long x = xbeg, nx = 0; x < xend; x = nx) {
         const AttnPiece A = piece(x, nx);
         if (A.S == 1) continue;
@@ -1033,6 +1042,38 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
         // the segment's first position (key-space partition)
         const long long s0 = eq ? 0 : x - (A.t_beg - view_lo(vw, kv[A.b]));
         float* dst = p.OB + ((long long)A.b * p.Hq + (long long)A.g * grp) * HD;
+        if (A.S <= kMergeFew) {
+            // few partials: a thread per output, all its partials' loads in flight
+            for (int j = o0 + (int)threadIdx.x; j < o1; j += kThreads) {
+                const int h = j / HD;
+                float mv[kMergeFew], lv[kMergeFew], ov[kMergeFew];
+#pragma unroll
+                for (int q = 0; q < kMergeFew; ++q) {
+                    if (q < A.S) {
+                        const float* pq = p.PART + (long long)attn_slot(tab, view, A.cf, q, s0) * PSZ;
+                        mv[q] = __ldcg(pq + grp * HD + h);
+                        lv[q] = __ldcg(pq + grp * HD + grp + h);
+                        ov[q] = __ldcg(pq + j);
+                    }
+                }
+                float M = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < kMergeFew; ++q)
+                    if (q < A.S) M = fmaxf(M, mv[q]);
+                const float mu = M == -INFINITY ? 0.f : M;
+                float Ls = 0.f, O = 0.f;
+#pragma unroll
+                for (int q = 0; q < kMergeFew; ++q) {
+                    if (q < A.S) {
+                        const float e = expf(mv[q] - mu);
+                        Ls = fmaf(e, lv[q], Ls);
+                        O = fmaf(e, ov[q], O);
+                    }
+                }
+                dst[j] = O / Ls;
+            }
+            continue;
+        }
         for (int j0 = o0 + warp; j0 < o1; j0 += MJ * kWarps) {
             float mm[MJ], ll[MJ], oo[MJ];
 #pragma unroll
@@ -1169,7 +1210,7 @@ __device__ bool head_groups_b1(const DraftParams& p, unsigned char* ring, unsign
 
 // Tensor-core GEMM D[R, Bp] = W[R, K] X[Bp, K]^T (bf16, fp32 accumulate),
 // with X split into bf16 high and low parts (two MMAs per K slice, so the
-// product carries about 16 mantissa bits of X).  Work items are (128-row
+// product carries about 16 mantissa bits of X), or X taken as its high part.  Work items are (128-row
 // tile, K split); CTA c takes items c, c + grid, ...  Warp 0 (one lane)
 // streams the W and X tiles by tensor copies through a tc_stages-deep ring,
 // warp 1 (one lane) issues the MMAs into one of two tensor-memory
@@ -1184,8 +1225,9 @@ struct TcState {
 
 struct TcJob {
     const CUtensorMap *wa, *wb;   // W rows [0, R1) and [R1, R) (wb: rows counted from R1)
-    const CUtensorMap *xh, *xl;   // X high / low parts, box 64 x Bp
+    const uint16_t *xh, *xl;      // X high / low parts, tiled (xtile_idx)
     int R1, R, nks, S, kps;       // rows, K steps of 64, K splits, K steps per split
+    bool lo;                      // also multiply the low part (else X ~ its high part)
 };
 
 template <class Epi>
@@ -1195,6 +1237,7 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
     const int ntiles = (J.R + kTcTileM - 1) / kTcTileM, nitems = ntiles * J.S;
     const int nit = nitems > (int)blockIdx.x ? (nitems - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     const uint32_t abytes = kTcTileM * 128, xbytes = (uint32_t)Bp * 128, sbytes = abytes + 2 * xbytes;
+    const uint32_t tx = abytes + (J.lo ? 2 : 1) * xbytes;       // bytes landing per stage
     const uint32_t base = (smem_addr(smem) + 1023u) & ~1023u;   // 1024-byte aligned ring
     unsigned char* ring = smem + (base - smem_addr(smem));
     auto ksteps = [&](int item, int& k0) {   // K steps of an item: [k0, k0 + n)
@@ -1218,17 +1261,21 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
                 const int wy = row0 < J.R1 ? row0 : row0 - J.R1;
                 int k0;
                 const int n = ksteps(item, k0);
-                for (int ks = k0; ks < k0 + n; ++ks, ++g) {
+                // K steps in a rotated order per CTA, so the CTAs do not all
+                // read the same shared X tile at once
+                const int rot = n > 0 ? (int)blockIdx.x % n : 0;
+                for (int i = 0; i < n; ++i, ++g) {
+                    const int ks = k0 + (i + rot < n ? i + rot : i + rot - n);
                     const uint32_t st = g % NS;
                     if (!mbar_wait_limited(&ts.empty[st], ((g / NS) & 1u) ^ 1u, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     unsigned char* sp = ring + st * sbytes;
-                    mbar_arrive_expect_tx(&ts.full[st], sbytes);
+                    mbar_arrive_expect_tx(&ts.full[st], tx);
                     tma_load_2d(sp, wm, ks * kTcTileK, wy, &ts.full[st]);
-                    tma_load_2d(sp + abytes, J.xh, ks * kTcTileK, 0, &ts.full[st]);
-                    tma_load_2d(sp + abytes + xbytes, J.xl, ks * kTcTileK, 0, &ts.full[st]);
+                    bulk_g2s(sp + abytes, J.xh + (long long)ks * Bp * kTcTileK, xbytes, &ts.full[st]);
+                    if (J.lo) bulk_g2s(sp + abytes + xbytes, J.xl + (long long)ks * Bp * kTcTileK, xbytes, &ts.full[st]);
                 }
             }
         }
@@ -1258,7 +1305,7 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
                     for (int kk = 0; kk < kTcTileK / 16; ++kk) {
                         const uint64_t ad = umma_desc_sw128(sa + kk * 32);
                         umma_bf16(d, ad, umma_desc_sw128(sa + abytes + kk * 32), idesc, (ks | kk) != 0 ? 1u : 0u);
-                        umma_bf16(d, ad, umma_desc_sw128(sa + abytes + xbytes + kk * 32), idesc, 1u);
+                        if (J.lo) umma_bf16(d, ad, umma_desc_sw128(sa + abytes + xbytes + kk * 32), idesc, 1u);
                     }
                     umma_commit(&ts.empty[st]);
                 }
@@ -1333,23 +1380,20 @@ struct TcPartEpi {
     }
 };
 
-// epilogue: unsplit post-projection: h and its bf16 high / low parts
+// epilogue: unsplit post-projection: h and bf16(h) as the head's operand
 struct TcHnEpi {
     float* HN;
-    uint16_t *XH, *XL;
-    int B, R;
+    uint16_t* XH;
+    int B, R, Bp;
     __device__ __forceinline__ void apply(int row, int, int c0, const uint32_t (&r)[16]) {
         if (row >= R) return;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const int b = c0 + jj;
             if (b < B) {
-                const long long i = (long long)b * R + row;
                 const float v = __uint_as_float(r[jj]);
-                HN[i] = v;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-                XH[i] = __bfloat16_as_ushort(hi);
-                XL[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+                HN[(long long)b * R + row] = v;
+                XH[xtile_idx(b, row, Bp)] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
             }
         }
     }
@@ -1358,8 +1402,8 @@ struct TcHnEpi {
 // job of projection phase `phase` of block l over the staged inputs
 __device__ __forceinline__ TcJob tc_job(const DraftParams& p, int phase, int l) {
     TcJob J;
-    J.xh = &p.tm_xa;
-    J.xl = &p.tm_xal;
+    J.xh = p.XA;
+    J.xl = p.XAL;
     int K = 0;
     switch (phase) {
     case PH_PRE: J.wa = J.wb = &p.tm_w[0]; J.R = p.d_a; K = 2 * p.d_t; break;
@@ -1370,6 +1414,7 @@ __device__ __forceinline__ TcJob tc_job(const DraftParams& p, int phase, int l) 
     default: J.wa = J.wb = &p.tm_w[1]; J.R = p.d_t; K = p.d_a; break;   // PH_POST
     }
     J.R1 = phase == PH_FFN1 ? p.F : J.R;
+    J.lo = true;
     J.nks = (K + kTcTileK - 1) / kTcTileK;
     J.S = p.sk[phase];
     J.kps = (J.nks + J.S - 1) / J.S;
@@ -1385,12 +1430,12 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
     if (TC && p.tc_head) {
         TcJob J;
         J.wa = J.wb = &p.tm_embd;
-        J.xh = &p.tm_xh;
-        J.xl = &p.tm_xl;
+        J.xh = J.xl = p.XH;
         J.R1 = J.R = p.V;
         J.nks = (p.d_t + kTcTileK - 1) / kTcTileK;
         J.S = 1;
         J.kps = J.nks;
+        J.lo = false;   // h rounded to bf16 for the head: half the MMAs and operand traffic
         TcHeadEpi he{p, k, e};
         if constexpr (TC) {
             if (!tc_gemm(p, J, smem, ts, he)) return false;
@@ -1463,10 +1508,15 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         for (int i = threadIdx.x; i < p.N * p.B; i += blockDim.x) p.amax[i] = 0ull;
     // tensor-core head: zero rows B..Bp-1 of the bf16 parts of h (read by
     // tensor copies, first after >= 1 barrier)
-    if (TC && p.tc_head && blockIdx.x == 0) {
-        for (long long i = (long long)p.B * p.d_t + threadIdx.x; i < (long long)p.Bp * p.d_t; i += blockDim.x) {
-            p.XH[i] = 0;
-            p.XL[i] = 0;
+    // tensor-core operands: zero once (rows >= B and columns past a row's
+    // length are never written; bulk copies read them from the first phase
+    // on, after >= 1 barrier)
+    if (TC && p.tc_head) {
+        const long long nh = (long long)((p.d_t + 63) / 64) * p.Bp * 64, na = p.tc_proj ? (long long)((p.kmax + 63) / 64) * p.Bp * 64 : 0;
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nh + 2 * na; i += (long long)gridDim.x * blockDim.x) {
+            if (i < nh) p.XH[i] = 0;
+            else if (i < nh + na) p.XA[i - nh] = 0;
+            else p.XAL[i - nh - na] = 0;
         }
         fence_proxy_async_global();
     }
@@ -1502,7 +1552,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             if constexpr (TC) {
                 const TcJob J = tc_job(p, phase, l);
                 if (phase == PH_POST) {
-                    TcHnEpi he{p.HN, p.XH, p.XL, p.B, p.d_t};
+                    TcHnEpi he{p.HN, p.XH, p.B, p.d_t, p.Bp};
                     if (!tc_gemm(p, J, smem, ts, he)) return false;
                 } else {
                     TcPartEpi pe{p.PB, p.B, J.R};
@@ -1577,7 +1627,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         }
         // ---- POST ----
         if (TC && p.tc_head) {
-            StoreHiLoEpi e{p.HN, p.d_t, p.XH, p.XL};
+            StoreXhEpi e{p.HN, p.d_t, p.XH, p.Bp};
             if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         } else {
             StoreEpi e{p.HN, p.d_t};
