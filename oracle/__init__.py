@@ -84,7 +84,7 @@ def _declare(L):
     L.orc_pick.restype = C.c_int32
     L.orc_draft_step.argtypes = [P, P, P, P, I, I, P, I, P, P, P, P]
     L.orc_draft_step.restype = I
-    L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, P, I, P, P, P, P, P]
+    L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, I, P, I, P, P, P, P, P]
     L.orc_draft_block.restype = I
     L.orc_verify_greedy.argtypes = [P, I, I, I, I, P, P, P]
     L.orc_verify_sample.argtypes = [P, P, I, I, I, I, P, P, I, P, U64, U64, P, P, P]
@@ -255,7 +255,7 @@ def draft_block(w, sample=None, seed=0, offset=0, force=None, seqs=None, want_lo
         mg = np.empty((1, N), dtype=np.float64)
         rc = L.orc_draft_block(C.byref(bd.model), bd.tensors, _p(bd.block_view), bd.views, bd.n_views,
                                1, N, _p(bd.kv_len), _p(bd.last_tok), _p(bd.h_prev),
-                               C.byref(prm) if prm is not None else None, seed, offset,
+                               C.byref(prm) if prm is not None else None, seed, offset, b,
                                _p(bd.hist), bd.hist.shape[1], _p(f), _p(d), _p(h), _p(z), _p(mg))
         if rc != 0:
             raise ValueError(f"oracle draft block rejected its inputs (rc={rc})")

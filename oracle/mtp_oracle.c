@@ -491,14 +491,15 @@ int orc_draft_step(const orc_model *m, const void *const *t, const int32_t *bloc
  * sec. 4 item 8; [FN] the fused chain: argmax -> embed -> h chain).
  *   sp == NULL or sp->temp <= 0: greedy (argmax).  Otherwise the token of
  *   step k is drawn from sample_dist(z_k) with penalty set hist[b] u
- *   drafts[b][0..k-1] and the uniform of (b, k, purpose 0).
+ *   drafts[b][0..k-1] and the uniform of (seq0 + b, k, purpose 0): seq0 is
+ *   the batch index of row 0 when the rows are a slice of a larger batch.
  * Outputs drafts [B, N], h_last [B, d_t] (optional), logits [B, N, V]
  * (optional), margin [B, N] (optional: top1 - top2 logit gap of each greedy
  * step, or the sampling decision's relative margin). */
 int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *block_view,
                     const orc_view *views, int n_views, int B, int N, const int32_t *kv_len,
                     const int32_t *last_tok, const float *h_prev, const orc_sample_params *sp,
-                    uint64_t seed, uint64_t offset, const int32_t *hist, int H,
+                    uint64_t seed, uint64_t offset, int seq0, const int32_t *hist, int H,
                     const int32_t *force_tok, int32_t *drafts, double *h_last, double *logits,
                     double *margin) {
     const int d_t = m->d_t, V = m->vocab;
@@ -531,7 +532,7 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
                 float ws;
                 double m1, m2;
                 int n = orc_sample_dist_f32(zb, V, pen, np, sp, ids, wf, &ws, &m1);
-                float u = (float)orc_uniform(seed, offset, (uint32_t)b, (uint32_t)k, 0u);
+                float u = (float)orc_uniform(seed, offset, (uint32_t)(seq0 + b), (uint32_t)k, 0u);
                 pick = orc_pick_f32(ids, wf, n, ws, u, &m2);
                 mg = m1 < m2 ? m1 : m2;
             }
