@@ -165,7 +165,11 @@ size_t mtp_workspace_size(const mtp_config *cfg, int B, int N, int V);
  *   kv_len [B] int32     attn_pos + 1 of each sequence, >= 1
  *   last_tok [B] int32   the last accepted token
  *   h_prev [B, d_t] fp32 the target's hidden state at that token
- *   sp                   host pointer or NULL (greedy)
+ *   sp                   host pointer or NULL (greedy); with temp > 0 the
+ *                        settings are checked as for mtp_verify_sample
+ *                        (MTP_ERR_ARG; top_k != 0: MTP_ERR_UNSUPPORTED), and
+ *                        a kept set over 4096 candidates sets the status word
+ *                        to MTP_ERR_CAPACITY
  *   hist [B, H] int32    penalty history (newest last; entries < 0 ignored);
  *                        used only when sampling; may be NULL when H == 0
  *   out_drafts [B, N] int32

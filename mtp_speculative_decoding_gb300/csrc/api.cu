@@ -80,7 +80,7 @@ int draft_grid() {
 }
 
 struct DraftLayout {
-    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, XH, XA, XAL, PB, ACT, end;
+    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ZB, SROW, SCNT, SNK, SWK, SID, SW, ACT, end;
     int kmax;
 };
 
@@ -116,11 +116,20 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     // tensor-core operands: K blocks of 64 columns x Bp rows, bf16
     const size_t xb = tc_head_eligible(c, B) ? (size_t)((c->d_t + 63) / 64) * pad16(B) * 128 : 0;
     L.XH = off;      off = al256(off + xb);
+    L.XL = off;      off = al256(off + xb);
     const bool tcp = tc_proj_eligible(c, B);
     const size_t xa = tcp ? (size_t)((L.kmax + 63) / 64) * pad16(B) * 128 : 0;
     L.XA = off;      off = al256(off + xa);
     L.XAL = off;     off = al256(off + xa);
     L.PB = off;      off = al256(off + (tcp ? tc_plan(c, B, draft_grid()).pb_floats * f : 0));
+    // sampled drafting: the step's logits and the sampler's per-row state
+    L.ZB = off;      off = al256(off + (size_t)B * c->vocab * f);
+    L.SROW = off;    off = al256(off + (size_t)B * sizeof(unsigned long long));
+    L.SCNT = off;    off = al256(off + (size_t)B * sizeof(unsigned int));
+    L.SNK = off;     off = al256(off + (size_t)B * sizeof(int32_t));
+    L.SWK = off;     off = al256(off + (size_t)B * f);
+    L.SID = off;     off = al256(off + (size_t)B * kCandCap * sizeof(int32_t));
+    L.SW = off;      off = al256(off + (size_t)B * kCandCap * f);
     L.ACT = off;     off = al256(off + (size_t)B * L.kmax * f);
     L.end = off;
     return L;
@@ -257,7 +266,12 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     if (B < 1 || B > MTP_MAX_BATCH || N < 1 || N > 16) return MTP_ERR_ARG;
     if (!kv_len || !last_tok || !h_prev || !out_drafts) return MTP_ERR_ARG;
     if (H < 0 || (H > 0 && !hist)) return MTP_ERR_ARG;
-    if (sp && sp->temp > 0.f) return MTP_ERR_UNSUPPORTED;  // sampled drafting: not built yet
+    const bool sampling = sp && sp->temp > 0.f;
+    if (sampling) {
+        const int rs = check_sample_params(sp);
+        if (rs != MTP_OK) return rs;
+        if (H < 0 || (H > 0 && !hist)) return MTP_ERR_ARG;
+    }
     const bool bf = cfg->wdtype == MTP_DTYPE_BF16;
     const int esz = bf ? 2 : 4;
     // weights
@@ -374,6 +388,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         p.tc_stages = tc_stages;
         p.tc_cols = tc_cols;
         p.XH = reinterpret_cast<uint16_t*>(base + L.XH);
+        p.XL = reinterpret_cast<uint16_t*>(base + L.XL);
         if (!encode_bf16_map(&p.tm_embd, w->tok_embd, (uint64_t)cfg->d_t, (uint64_t)cfg->vocab, kTcTileM))
             return MTP_ERR_CUDA;
         if (tc_proj_eligible(cfg, B) && !act_smem) {
@@ -400,7 +415,19 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     }
     p.kmax = L.kmax;
     p.timeout_ns = kBarrierLimitNs;
-    (void)seed; (void)offset; (void)hist; (void)H;
+    if (sampling) {
+        p.sampling = 1;
+        p.s_temp = sp->temp; p.s_top_p = sp->top_p; p.s_min_p = sp->min_p;
+        p.s_rep = sp->rep_penalty; p.s_pres = sp->presence_penalty;
+        p.seed = seed; p.offset = offset; p.hist = hist; p.H = H;
+        p.ZB = reinterpret_cast<float*>(base + L.ZB);
+        p.S_rowmax = reinterpret_cast<unsigned long long*>(base + L.SROW);
+        p.S_cnt = reinterpret_cast<unsigned int*>(base + L.SCNT);
+        p.S_nkeep = reinterpret_cast<int32_t*>(base + L.SNK);
+        p.S_wkeep = reinterpret_cast<float*>(base + L.SWK);
+        p.S_id = reinterpret_cast<int32_t*>(base + L.SID);
+        p.S_w = reinterpret_cast<float*>(base + L.SW);
+    }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, L.amax, s) != cudaSuccess) return MTP_ERR_CUDA;
@@ -458,6 +485,7 @@ int mtp_verify_sample(const void* tgt_logits, const void* dft_logits, int ldtype
     char* base = static_cast<char*>(ws);
     VerifySampleArgs a;
     memset(&a, 0, sizeof a);
+    a.draft_k = -1;
     a.tgt = tgt_logits; a.dft = dft_logits; a.bf16 = ldtype == MTP_DTYPE_BF16;
     a.B = B; a.N = N; a.V = V; a.drafts = drafts; a.hist = hist; a.H = H; a.hist_stride = H;
     a.temp = sp->temp; a.top_p = sp->top_p; a.min_p = sp->min_p; a.rep = sp->rep_penalty;

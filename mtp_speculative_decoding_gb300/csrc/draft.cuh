@@ -106,13 +106,28 @@ struct DraftParams {
     int head_slotb;              // > 0: one sequence, LM head rows through bulk-copy slots of this many bytes
     int tc_head;                 // 1: LM head on tensor cores
     int Bp, tc_stages, tc_cols;  // batch padded to 16; operand ring depth; tensor-memory columns
-    uint16_t* XH;                // bf16(h) as the head's tiled operand (rows >= B zero)
+    uint16_t *XH, *XL;           // bf16 high / low parts of h as the head's tiled operand (rows >= B zero)
     int tc_proj;                 // 1: projections on tensor cores (activations staged in global memory)
     int sk[6];                   // split-K factor of each projection phase (PH_PRE .. PH_POST)
     uint16_t *XA, *XAL;          // bf16 high / low parts of the current phase input, tiled
     float* PB;                   // [S][B][R] split partials of the last projection (FFN1: R = 2 F)
     int kmax;
     unsigned long long timeout_ns;
+    // sampled drafting (temperature > 0): sample_dist parameters, the
+    // Philox stream, the penalty history [B, H], the step's logits [B, V]
+    // and the sampler's per-row state
+    int sampling;
+    float s_temp, s_top_p, s_min_p, s_rep, s_pres;
+    unsigned long long seed, offset;
+    const int32_t* hist;
+    int H;
+    float* ZB;
+    unsigned long long* S_rowmax;
+    unsigned int* S_cnt;
+    int32_t* S_nkeep;
+    float* S_wkeep;
+    int32_t* S_id;
+    float* S_w;
 };
 
 cudaError_t launch_draft_f32(const DraftParams& p, int grid, size_t smem, cudaStream_t s);

@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "draft.cuh"
+#include "sample.cuh"
 
 namespace mtp {
 
@@ -176,11 +177,12 @@ __device__ __forceinline__ long long xtile_idx(int b, int k, int Bp) {
     return ((long long)kb * Bp + b) * 64 + ((((kk >> 3) ^ (b & 7)) << 3) | (kk & 7));
 }
 
-// out[b * ldo + r] = v, plus bf16(v) as tensor-core operand element (b, r)
+// out[b * ldo + r] = v, plus the bf16 high and low parts of v as
+// tensor-core operand elements (b, r)
 struct StoreXhEpi {
     float* out;
     int ldo;
-    uint16_t* xh;
+    uint16_t *xh, *xl;
     int Bp;
     template <int NB>
     __device__ __forceinline__ void apply(int r, int b0, int nb, const float (&acc)[NB], const float (&)[NB]) {
@@ -190,7 +192,10 @@ struct StoreXhEpi {
             if (lane == j && b0 + j < nb) {
                 const float v = acc[j];
                 out[(long long)(b0 + j) * ldo + r] = v;
-                xh[xtile_idx(b0 + j, r, Bp)] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                const long long xi = xtile_idx(b0 + j, r, Bp);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                xh[xi] = __bfloat16_as_ushort(hi);
+                xl[xi] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
             }
     }
 };
@@ -220,6 +225,7 @@ struct HeadEpi {
     int V, N, step;
     float softcap;
     unsigned long long best_lo, best_hi;
+    float* zb;      // [B, V] the step's logits for the sampler, or null
     template <int NB>
     __device__ __forceinline__ void apply(int r, int b0, int nb, const float (&acc)[NB], const float (&)[NB]) {
         const int lane = threadIdx.x & 31;
@@ -230,6 +236,7 @@ struct HeadEpi {
                 float z = acc[j];
                 if (softcap > 0.f) z = softcap * tanhf(z / softcap);
                 if (logits) logits[((long long)col * N + step) * V + r] = z;
+                if (zb) zb[(long long)col * V + r] = z;
                 const unsigned long long k = pack_argmax(z, (uint32_t)r);
                 if (col < 32) best_lo = k > best_lo ? k : best_lo;
                 else best_hi = k > best_hi ? k : best_hi;
@@ -1356,6 +1363,7 @@ struct TcHeadEpi {
                 float z = __uint_as_float(r[jj]);
                 if (p.softcap > 0.f) z = p.softcap * tanhf(z / p.softcap);
                 if (row < p.V && p.out_logits) p.out_logits[((long long)b * p.N + k) * p.V + row] = z;
+                if (row < p.V && p.ZB) p.ZB[(long long)b * p.V + row] = z;
                 const unsigned long long key = warp_max_u64(row < p.V ? pack_argmax(z, (uint32_t)row) : 0ull);
                 if (lane == (b & 31)) {
                     if (b < 32) e.best_lo = key > e.best_lo ? key : e.best_lo;
@@ -1380,10 +1388,11 @@ struct TcPartEpi {
     }
 };
 
-// epilogue: unsplit post-projection: h and bf16(h) as the head's operand
+// epilogue: unsplit post-projection: h and its bf16 high / low parts as the
+// head's operand
 struct TcHnEpi {
     float* HN;
-    uint16_t* XH;
+    uint16_t *XH, *XL;
     int B, R, Bp;
     __device__ __forceinline__ void apply(int row, int, int c0, const uint32_t (&r)[16]) {
         if (row >= R) return;
@@ -1393,7 +1402,10 @@ struct TcHnEpi {
             if (b < B) {
                 const float v = __uint_as_float(r[jj]);
                 HN[(long long)b * R + row] = v;
-                XH[xtile_idx(b, row, Bp)] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                const long long xi = xtile_idx(b, row, Bp);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                XH[xi] = __bfloat16_as_ushort(hi);
+                XL[xi] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
             }
         }
     }
@@ -1426,16 +1438,20 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
                                            unsigned long long (*head_best)[32], unsigned char* smem,
                                            unsigned long long (*bars)[kHeadSlots], unsigned int& par,
                                            float (*hpart)[kHeadSlots][4], TcState& ts) {
-    HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull};
+    HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull, p.ZB};
     if (TC && p.tc_head) {
         TcJob J;
         J.wa = J.wb = &p.tm_embd;
-        J.xh = J.xl = p.XH;
+        J.xh = p.XH;
+        J.xl = p.XL;
         J.R1 = J.R = p.V;
         J.nks = (p.d_t + kTcTileK - 1) / kTcTileK;
         J.S = 1;
         J.kps = J.nks;
-        J.lo = false;   // h rounded to bf16 for the head: half the MMAs and operand traffic
+        // greedy: h rounded to bf16 (half the MMAs and operand traffic; the
+        // argmax is stable to it); sampling: both parts, so the sampler sees
+        // logits as close as the CUDA-core path's
+        J.lo = p.sampling != 0;
         TcHeadEpi he{p, k, e};
         if constexpr (TC) {
             if (!tc_gemm(p, J, smem, ts, he)) return false;
@@ -1471,6 +1487,64 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+// Sampled drafting, step k: sample_dist over each sequence's logits
+// (penalties over hist[b] and the drafts so far, temperature, min-p, top-p)
+// and a draw with the uniform of (b, k, purpose 0), in the sampler's
+// phases: row maxima, candidates, sorted kept sets, draws.  The token goes
+// to the step's argmax slot, where the next step and the outputs read it.
+static __device__ bool sample_step(const DraftParams& p, int k, unsigned char* smem, unsigned int& epoch) {
+    VerifySampleArgs a;
+    a.tgt = p.ZB;
+    a.dft = nullptr;
+    a.bf16 = 0;
+    a.B = p.B;
+    a.N = p.N;
+    a.V = p.V;
+    a.drafts = p.out_drafts;
+    a.hist = p.hist;
+    a.H = p.H;
+    a.hist_stride = p.H;
+    a.temp = p.s_temp;
+    a.top_p = p.s_top_p;
+    a.min_p = p.s_min_p;
+    a.rep = p.s_rep;
+    a.pres = p.s_pres;
+    a.seed = p.seed;
+    a.offset = p.offset;
+    a.out_tokens = nullptr;
+    a.out_n_accept = nullptr;
+    a.hdr = p.hdr;
+    a.rowmax = p.S_rowmax;
+    a.cand_cnt = p.S_cnt;
+    a.n_keep = p.S_nkeep;
+    a.w_keep = p.S_wkeep;
+    a.cand_id = p.S_id;
+    a.cand_w = p.S_w;
+    a.resid = nullptr;
+    a.timeout_ns = p.timeout_ns;
+    a.draft_k = k;
+    const long long chunks = (p.V + kScanChunk - 1) / kScanChunk, items = (long long)p.B * chunks;
+    uint32_t* bits = reinterpret_cast<uint32_t*>(smem);
+    unsigned long long* red64 = reinterpret_cast<unsigned long long*>(smem + kScanChunk / 8);
+    for (int mode = 0; mode < 2; ++mode) {
+        for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+            const long long c0 = (it % chunks) * kScanChunk;
+            sample_scan_item(a, (int)(it / chunks), c0, c0 + kScanChunk < p.V ? c0 + kScanChunk : p.V, mode, bits, red64);
+        }
+        if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return false;
+    }
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
+    float* wsh = reinterpret_cast<float*>(smem + kCandCap * sizeof(unsigned long long));
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) sample_sort_row(a, b, keys, wsh);
+    if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return false;
+    const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    for (int b = gw; b < p.B; b += gridDim.x * kWarps) {
+        const int32_t t = sample_pick_draft(a, b);
+        if (lane == 0) p.amax[(long long)k * p.B + b] = (1ull << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+    }
+    return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
+}
+
 template <typename WT, int HD, bool TC>
 __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts) {
     __shared__ float red[kWarps];
@@ -1513,10 +1587,12 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     // on, after >= 1 barrier)
     if (TC && p.tc_head) {
         const long long nh = (long long)((p.d_t + 63) / 64) * p.Bp * 64, na = p.tc_proj ? (long long)((p.kmax + 63) / 64) * p.Bp * 64 : 0;
-        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nh + 2 * na; i += (long long)gridDim.x * blockDim.x) {
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * nh + 2 * na;
+             i += (long long)gridDim.x * blockDim.x) {
             if (i < nh) p.XH[i] = 0;
-            else if (i < nh + na) p.XA[i - nh] = 0;
-            else p.XAL[i - nh - na] = 0;
+            else if (i < 2 * nh) p.XL[i - nh] = 0;
+            else if (i < 2 * nh + na) p.XA[i - 2 * nh] = 0;
+            else p.XAL[i - 2 * nh - na] = 0;
         }
         fence_proxy_async_global();
     }
@@ -1552,7 +1628,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             if constexpr (TC) {
                 const TcJob J = tc_job(p, phase, l);
                 if (phase == PH_POST) {
-                    TcHnEpi he{p.HN, p.XH, p.B, p.d_t, p.Bp};
+                    TcHnEpi he{p.HN, p.XH, p.XL, p.B, p.d_t, p.Bp};
                     if (!tc_gemm(p, J, smem, ts, he)) return false;
                 } else {
                     TcPartEpi pe{p.PB, p.B, J.R};
@@ -1571,9 +1647,15 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
 
     for (int k = 0; k < p.N; ++k) {
         // ---- PRE ----
-        if (blockIdx.x == 0 && k > 0)
-            for (int b = threadIdx.x; b < p.B; b += blockDim.x)
-                p.out_drafts[(long long)b * p.N + (k - 1)] = step_token(p, b, k);
+        if (blockIdx.x == 0) {
+            for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+                if (k > 0) p.out_drafts[(long long)b * p.N + (k - 1)] = step_token(p, b, k);
+                if (p.sampling) {   // the sampler's row state of this step (first used after the head)
+                    p.S_rowmax[b] = 0ull;
+                    p.S_cnt[b] = 0u;
+                }
+            }
+        }
         {
             StoreEpi e{p.XB, p.d_a};
             if (!gemv_step(PH_PRE, k, 0, p.w_pre, nullptr, p.d_a, 2 * p.d_t, e, One{})) return;
@@ -1627,7 +1709,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         }
         // ---- POST ----
         if (TC && p.tc_head) {
-            StoreXhEpi e{p.HN, p.d_t, p.XH, p.Bp};
+            StoreXhEpi e{p.HN, p.d_t, p.XH, p.XL, p.Bp};
             if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         } else {
             StoreEpi e{p.HN, p.d_t};
@@ -1644,6 +1726,8 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             if (!head_phase<WT, TC>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part, ts)) return;
         }
         if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
+        // ---- SAMPLE (temperature > 0): sample_dist of the step's logits ----
+        if (p.sampling && !sample_step(p, k, smem, epoch)) return;
     }
     // outputs of the last step
     if (blockIdx.x == 0) {

@@ -48,7 +48,8 @@ __device__ __forceinline__ float scaled_logit(const VerifySampleArgs& a, float z
 }
 
 // Row geometry: rows [0, B(1+N)) are target rows (b, i), rows [B(1+N),
-// B(1+N) + B N) are draft rows (b, i).  Penalty set of (b, i): hist[b][*] u
+// B(1+N) + B N) are draft rows (b, i); in draft sampling (draft_k >= 0) row
+// b is sequence b at step draft_k.  Penalty set of (b, i): hist[b][*] u
 // drafts[b][0..i-1].
 struct RowInfo {
     const void* base;
@@ -59,7 +60,11 @@ __device__ __forceinline__ RowInfo row_info(const VerifySampleArgs& a, int row) 
     RowInfo r;
     const int R = a.N + 1;
     const long long esz = a.bf16 ? 2 : 4;
-    if (row < a.B * R) {
+    if (a.draft_k >= 0) {   // draft sampling: one row per sequence, tgt = [B, V]
+        r.b = row;
+        r.i = a.draft_k;
+        r.base = static_cast<const char*>(a.tgt) + (long long)row * a.V * esz;
+    } else if (row < a.B * R) {
         r.b = row / R;
         r.i = row % R;
         r.base = static_cast<const char*>(a.tgt) + (long long)row * a.V * esz;
@@ -99,7 +104,7 @@ __device__ __forceinline__ float key_to_float(uint32_t key) {
 // Scan of one (row, chunk) item.  mode 0: fold the max scaled logit into
 // rowmax[row]; mode 1: append every token with exp_cw(l - lmax) >= min_p to
 // the row's candidate list.
-__device__ void sample_scan_item(const VerifySampleArgs& a, int row, long long c0, long long c1, int mode,
+static __device__ void sample_scan_item(const VerifySampleArgs& a, int row, long long c0, long long c1, int mode,
                                  uint32_t* bits, unsigned long long* red64) {
     const RowInfo ri = row_info(a, row);
     const int nwords = (int)((c1 - c0 + 31) / 32);
@@ -149,7 +154,7 @@ __device__ void sample_scan_item(const VerifySampleArgs& a, int row, long long c
 
 // Sort one row's candidates by (w desc, id asc), cut by top-p, store ids /
 // weights in order, n_keep and the kept mass.  Sums are sequential (thread 0).
-__device__ void sample_sort_row(const VerifySampleArgs& a, int row, unsigned long long* keys, float* wsh) {
+static __device__ void sample_sort_row(const VerifySampleArgs& a, int row, unsigned long long* keys, float* wsh) {
     unsigned int n = __ldcg(a.cand_cnt + row);
     if (n > (unsigned)kCandCap) n = kCandCap;
     unsigned int P = 32;
@@ -224,7 +229,7 @@ __device__ __forceinline__ int pick_index_seq(int n, float total, float u, WF wf
 }
 
 // One warp walks sequence b's rows (lane 0 takes the decisions).
-__device__ void sample_decide(const VerifySampleArgs& a, int b) {
+static __device__ void sample_decide(const VerifySampleArgs& a, int b) {
     const int lane = threadIdx.x & 31;
     const int R = a.N + 1;
     int32_t* out = a.out_tokens + (long long)b * R;
@@ -272,6 +277,16 @@ __device__ void sample_decide(const VerifySampleArgs& a, int b) {
         for (int j = i + 1; j < R; ++j) out[j] = -1;
         a.out_n_accept[b] = i;
     }
+}
+
+// Draft sampling: one warp draws sequence b's token at step a.draft_k from
+// its sorted row with the uniform of (b, draft_k, purpose 0).
+__device__ __forceinline__ int32_t sample_pick_draft(const VerifySampleArgs& a, int b) {
+    const long long tb = (long long)b * kCandCap;
+    const float u = philox_uniform(a.seed, a.offset, (uint32_t)b, (uint32_t)a.draft_k, 0u);
+    const int j = pick_index_seq(__ldcg(a.n_keep + b), __ldcg(a.w_keep + b), u,
+                                 [&](int jj) { return __ldcg(a.cand_w + tb + jj); });
+    return __ldcg(a.cand_id + tb + j);
 }
 
 }  // namespace mtp

@@ -45,6 +45,7 @@ struct VerifySampleArgs {
     float* cand_w;               // [rows, kCandCap]
     float* resid;                // [B, kCandCap]
     unsigned long long timeout_ns;
+    int draft_k;                 // >= 0: draft sampling, row b = sequence b's logits at draft step draft_k
 };
 
 cudaError_t launch_verify_greedy(const VerifyGreedyArgs& a, int ldtype, int num_sms, cudaStream_t s);

@@ -91,3 +91,86 @@ def test_workload3_b64_sampled_sequences():
     w = synth.make_draft_inputs(3)
     _, d, h, z = run_gpu_draft(w)
     check_draft_parity(w, d, h, z, seqs=[0, 63])
+
+
+# ----------------------------------------------------------------------------
+# sampled drafting (temperature > 0)
+# ----------------------------------------------------------------------------
+
+SP = synth.SampleParams()
+
+
+def run_sampled(w, seed, offset, want_logits=True):
+    import torch
+    from mtp_speculative_decoding_gb300.device import upload_draft
+    import mtp_speculative_decoding_gb300 as mtp
+    dev = upload_draft(w)
+    B, N, V = w.B, w.N, w.model.vocab
+    drafts = torch.full((B, N), -7, dtype=torch.int32, device="cuda")
+    h_last = torch.full((B, w.model.d_t), float("nan"), dtype=torch.float32, device="cuda")
+    logits = torch.full((B, N, V), float("nan"), dtype=torch.float32, device="cuda") if want_logits else None
+    sp = (SP.temp, SP.top_p, SP.min_p, SP.rep_penalty, SP.presence_penalty, SP.top_k)
+    dev.run(drafts, h_last, logits, sample=sp, seed=seed, offset=offset)
+    torch.cuda.synchronize()
+    assert mtp.last_error(dev.ws) == 0
+    return drafts.cpu().numpy(), h_last.cpu().numpy(), (logits.cpu().numpy() if want_logits else None)
+
+
+def check_sampled(w, seed, offset, g_drafts, g_h, g_logits, seqs, margin_min=1e-3):
+    """The oracle follows the GPU's tokens (teacher forcing).  Each step's
+    logits match within the dtype tolerance.  The draws are the same except
+    where a sampler decision (a min-p or top-p cut, the order of two
+    candidates, the inverse-CDF pick) lies within margin_min (relative) of its
+    threshold -- there the last-bit differences of the logits may move it --
+    and such draws are at most a tenth of all.  Returns the matching draws."""
+    from gpu_common import tol_for
+    import oracle
+    tol = tol_for(w)
+    ref = oracle.draft_block(w, sample=SP, seed=seed, offset=offset, seqs=seqs, force=g_drafts)
+    same, total = 0, 0
+    for j, b in enumerate(seqs):
+        for k in range(w.N):
+            assert 0 <= g_drafts[b, k] < w.model.vocab
+            if g_logits is not None:
+                zo, zg = ref["logits"][j, k], g_logits[b, k]
+                rms = float(np.sqrt(np.mean(zo * zo)))
+                assert float(np.max(np.abs(zg - zo))) <= tol * rms
+            total += 1
+            if g_drafts[b, k] == ref["drafts"][j, k]:
+                same += 1
+            else:
+                assert ref["margin"][j, k] < margin_min, f"b={b} k={k}: {g_drafts[b, k]} != {ref['drafts'][j, k]}"
+        ho = ref["h_last"][j]
+        assert np.max(np.abs(g_h[b] - ho)) <= tol * float(np.sqrt(np.mean(ho * ho)))
+    assert total - same <= max(1, total // 10), f"{total - same} of {total} draws differ"
+    return same
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_small_sampled_drafts(dtype):
+    w = small_workload(dtype)
+    d, h, z = run_sampled(w, seed=1234, offset=7)
+    check_sampled(w, 1234, 7, d, h, z, seqs=range(w.B))
+    d2, _, _ = run_sampled(w, seed=1234, offset=7)
+    assert np.array_equal(d, d2)   # same Philox stream -> same draws
+    d3, _, _ = run_sampled(w, seed=1235, offset=7)
+    assert not np.array_equal(d, d3) or w.model.vocab < 4
+
+
+def test_small_sampled_tensor_core_batch():
+    # B = 40 runs the tensor-core head and projections, then the sampler
+    m = synth.ModelSpec(d_t=1024, d_a=256, n_blocks=1, n_q_heads=4, head_dim=64, n_kv_heads=1, d_ff=512,
+                        vocab=2048, dtype="bf16", block_view=(0,))
+    views = [synth.ViewSpec(cap=96, window=0, rope_theta=1e6)]
+    rng = np.random.default_rng(1)
+    kv = rng.integers(1, 97, size=40)
+    w = synth.make_draft_workload("batch40s", m, views, 40, 2, kv, 11, hist_len=4)
+    d, h, z = run_sampled(w, seed=99, offset=3)
+    check_sampled(w, 99, 3, d, h, z, seqs=[0, 21, 39])
+
+
+@pytest.mark.slow
+def test_workload1_sampled():
+    w = synth.make_draft_inputs(1)
+    d, h, z = run_sampled(w, seed=5, offset=0)
+    check_sampled(w, 5, 0, d, h, z, seqs=[0])
