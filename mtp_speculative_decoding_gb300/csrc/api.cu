@@ -201,7 +201,8 @@ size_t draft_smem_act(const mtp_config* c, int B, int act_smem) {
 size_t draft_smem(const mtp_config* c, int B, int act_smem) {
     const size_t wb = c->wdtype == MTP_DTYPE_BF16 ? 2 : 4;
     const size_t hd = c->head_dim, grp = c->n_q_heads / c->n_kv_heads;
-    const size_t attn = attn_smem((int)hd, (int)wb, (int)grp);
+    const int nst = tc_head_eligible(c, B) ? kAttnStagesTc : kAttnStages;   // the kernel variant's ring depth
+    const size_t attn = attn_smem((int)hd, (int)wb, (int)grp, nst);
     const size_t act = draft_smem_act(c, B, act_smem);
     return attn > act ? attn : act;
 }

@@ -27,7 +27,8 @@ __host__ __device__ constexpr AttnGeom attn_geom(int hd, int wb) {
     const int HG = 32 / DPL >= 4 ? 4 : (32 / DPL >= 1 ? 32 / DPL : 1);
     return AttnGeom{RB, CPR, LPR, CPL, KPW, EPC, DPL, R, R / KPW, 2 * R * RB, HG};
 }
-constexpr int kAttnStages = 2;
+constexpr int kAttnStages = 2;     // single-sequence kernel
+constexpr int kAttnStagesTc = 2;   // batched (tensor-core) kernel (three measured no faster)
 // LM head of one sequence: four groups of four warps, each with kHeadSlots
 // one-row slots; rows of up to kHeadMaxChunks 16-byte chunks
 constexpr int kHeadGroups = 4;
@@ -48,8 +49,8 @@ __host__ __device__ constexpr int attn_psz(int grp, int hd) { return (grp * (hd 
 // probabilities and rescales
 __host__ __device__ constexpr int attn_pb_off(int grp, int hd, int hg) { return (grp * hd + 3 * kWarps * hg + hg + 3) & ~3; }
 // dynamic shared memory of the attention phase: the rings, then the above
-__host__ __device__ constexpr size_t attn_smem(int hd, int wb, int grp) {
-    return (size_t)kWarps * kAttnStages * attn_geom(hd, wb).SB +
+__host__ __device__ constexpr size_t attn_smem(int hd, int wb, int grp, int nst) {
+    return (size_t)kWarps * nst * attn_geom(hd, wb).SB +
            ((size_t)attn_pb_off(grp, hd, attn_geom(hd, wb).HG) +
             (size_t)kWarps * ((attn_geom(hd, wb).RL * attn_geom(hd, wb).HG + attn_geom(hd, wb).HG + 3) & ~3)) *
                sizeof(float);

@@ -289,7 +289,15 @@ __device__ __forceinline__ float part_sum(const DraftParams& p, int S, int R, in
     const float* q = p.PB + (long long)b * R + i;
     const long long st = (long long)p.B * R;
     float v = 0.f;
-    for (int s = 0; s < S; ++s) v += __ldcg(q + s * st);
+    int s = 0;
+    for (; s + 8 <= S; s += 8) {   // eight loads in flight, summed in order
+        float t[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) t[u] = __ldcg(q + (s + u) * st);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v += t[u];
+    }
+    for (; s < S; ++s) v += __ldcg(q + s * st);
     return v;
 }
 
@@ -634,14 +642,14 @@ __device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// abar: [kWarps][kAttnStages] stage barriers (one arrival each); apar: the
-// calling warp's stage phase bits, carried across calls.
-template <typename WT, int HD>
+// NST: ring stages per warp.  abar: [kWarps][NST] stage barriers (one arrival
+// each); apar: the calling warp's stage phase bits, carried across calls.
+template <typename WT, int HD, int NST>
 __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem, const int* kv, const AttnTab& tab,
                                 unsigned long long* abar, unsigned int& apar) {
     constexpr AttnGeom G = attn_geom(HD, (int)sizeof(WT));
     constexpr int RB = G.RB, LPR = G.LPR, CPL = G.CPL, KPW = G.KPW, EPC = G.EPC, DPL = G.DPL;
-    constexpr int R = G.R, RL = G.RL, SB = G.SB, HG = G.HG, NST = kAttnStages;
+    constexpr int R = G.R, RL = G.RL, SB = G.SB, HG = G.HG;
     constexpr int RING = kWarps * NST * SB;
     constexpr int NV = RL * HG;         // scores per lane and round
     // one K/V row per warp and NV <= 32: scores summed transposed, softmax on
@@ -723,7 +731,7 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
         for (int h0 = 0; h0 < grp; h0 += HG) {
             const int hn = grp - h0 < HG ? grp - h0 : HG;
             if (h0 == 0) {
-                issue(0);
+                for (int r = 0; r + 1 < NST; ++r) issue(r);
                 // q-norm + RoPE of the group's heads (warp h: head g * grp + h),
                 // scaled by attn_scale; (cos, sin) of the position come from
                 // the step's table
@@ -799,7 +807,7 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
                 __syncthreads();
             } else {
                 __syncthreads();   // the previous pass's warp merge used the rings
-                issue(0);
+                for (int r = 0; r + 1 < NST; ++r) issue(r);
             }
 
             // this lane's slice of the pass's queries
@@ -832,7 +840,7 @@ __device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem
             }
 
             for (int i = 0; i < nrounds; ++i) {
-                issue(i + 1);   // its stage was consumed in round i - 1
+                issue(i + NST - 1);   // its stage was consumed in round i - 1
                 int t0;
                 const int cnt = slice_cnt(i, t0);
                 if (cnt > 0) {
@@ -1552,7 +1560,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     __shared__ __align__(8) unsigned long long head_bar[kHeadGroups][kHeadSlots];   // LM head slots
     __shared__ float head_part[kHeadGroups][kHeadSlots][4];
     unsigned int head_par = 0;
-    __shared__ __align__(8) unsigned long long attn_bar[kWarps][kAttnStages];   // attention stage barriers
+    __shared__ __align__(8) unsigned long long attn_bar[kWarps][kAttnStagesTc];   // attention stage barriers
     unsigned int attn_par = 0;
     unsigned int epoch = 0;
     float* tmp = reinterpret_cast<float*>(smem);                 // [max(d_a)] residual scratch
@@ -1611,7 +1619,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     }
 
     if (threadIdx.x < kHeadGroups * kHeadSlots) mbar_init(&head_bar[0][0] + threadIdx.x, 1);
-    if (threadIdx.x < kWarps * kAttnStages) mbar_init(&attn_bar[0][0] + threadIdx.x, 1);
+    if (threadIdx.x < kWarps * kAttnStagesTc) mbar_init(&attn_bar[0][0] + threadIdx.x, 1);
     mbar_fence_init();
     __syncthreads();
     // one GEMV phase and the barrier after it
@@ -1686,7 +1694,9 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 if (!gemv_step(PH_Q, k, l, bw.w_q, nullptr, p.Hq * p.hd, p.d_a, e, One{})) return;
             }
             // ---- ATT ----
-            if (!attention_phase<WT, HD>(p, l, smem, s_kv, s_tab, &attn_bar[0][0], attn_par)) return;
+            if (!attention_phase<WT, HD, TC ? kAttnStagesTc : kAttnStages>(p, l, smem, s_kv, s_tab, &attn_bar[0][0],
+                                                                          attn_par))
+                return;
             if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
             // every CTA has passed its attention waits: reset the item counters
             if (blockIdx.x == 0)
