@@ -193,9 +193,9 @@ SampleLayout sample_layout(int B, int N) {
 
 // residual scratch plus staged activations of the GEMV phases
 size_t draft_smem_act(const mtp_config* c, int B, int act_smem) {
-    const size_t kmax = draft_kmax(c);
+    const size_t kmax = draft_kmax(c), gmax = (size_t)(c->d_t > c->d_a ? c->d_t : c->d_a);
     return (((size_t)c->d_a + 3) & ~(size_t)3) * sizeof(float) +
-           (act_smem ? (size_t)B * kmax : kmax) * sizeof(float);
+           (act_smem ? (size_t)B * kmax : kmax) * sizeof(float) + 2 * gmax * sizeof(float);   // + the gain stage
 }
 
 size_t draft_smem(const mtp_config* c, int B, int act_smem) {

@@ -263,6 +263,47 @@ __device__ __forceinline__ void rms_into(const float* src, const float* g, int n
     __syncthreads();
 }
 
+// rms_into with the gains already staged in shared memory (gs)
+__device__ __forceinline__ void rms_into_s(const float* src, const float* gs, int n, float eps, float* dst, float* red) {
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const float v = src[i];
+        ss = fmaf(v, v, ss);
+    }
+    ss = block_sum(ss, red);
+    const float r = 1.0f / sqrtf(ss / (float)n + eps);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i] * r * gs[i];
+    __syncthreads();
+}
+
+// Both halves of v[2n] RMS-normalised in place with staged gains gs[2n]
+// (one block reduction for the two sums; red holds 2 kWarps floats).
+__device__ __forceinline__ void rms_pair_s(float* v, const float* gs, int n, float eps, float* red) {
+    float s1 = 0.f, s2 = 0.f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const float a = v[i], c = v[n + i];
+        s1 = fmaf(a, a, s1);
+        s2 = fmaf(c, c, s2);
+    }
+    s1 = warp_sum(s1);
+    s2 = warp_sum(s2);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) {
+        red[warp] = s1;
+        red[kWarps + warp] = s2;
+    }
+    __syncthreads();
+    s1 = warp_sum(lane < kWarps ? red[lane] : 0.f);
+    s2 = warp_sum(lane < kWarps ? red[kWarps + lane] : 0.f);
+    const float r1 = 1.0f / sqrtf(s1 / (float)n + eps), r2 = 1.0f / sqrtf(s2 / (float)n + eps);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        v[i] = v[i] * r1 * gs[i];
+        v[n + i] = v[n + i] * r2 * gs[n + i];
+    }
+    __syncthreads();
+}
+
 // token consumed by sequence b at step k
 __device__ __forceinline__ int step_token(const DraftParams& p, int b, int k) {
     if (k == 0) return p.last_tok[b];
@@ -302,42 +343,65 @@ __device__ __forceinline__ float part_sum(const DraftParams& p, int S, int R, in
 }
 
 // Writes sequence b's input vector for `phase` into dst (length phase_k).
-// `writer` marks the one CTA that also stores residual-stream updates.
+// `writer` marks the one CTA that also stores residual-stream updates.  The
+// norm gains are staged in gs (2 max(d_t, d_a) floats) by the same loops that
+// load the activations, so every load of a prologue is in flight at once.
 template <typename WT>
 __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, float* dst, float* tmp, bool writer,
-                          float* red) {
+                          float* red, float* gs) {
     switch (phase) {
     case PH_PRE: {
+        const int n = p.d_t;
+        constexpr int EPC = 16 / (int)sizeof(WT);
         const int tok = step_token(p, b, k);
-        const WT* er = reinterpret_cast<const WT*>(p.tok_embd) + (long long)tok * p.d_t;
-        for (int i = threadIdx.x; i < p.d_t; i += blockDim.x) dst[i] = ld_elem<WT>(er, i) * p.emb_scale;
-        const float* h = k == 0 ? p.h_prev + (long long)b * p.d_t : p.HN + (long long)b * p.d_t;
-        for (int i = threadIdx.x; i < p.d_t; i += blockDim.x) dst[p.d_t + i] = __ldcg(h + i);
+        const uint4* er = reinterpret_cast<const uint4*>(reinterpret_cast<const WT*>(p.tok_embd) + (long long)tok * n);
+        const float* h = k == 0 ? p.h_prev + (long long)b * n : p.HN + (long long)b * n;
+#pragma unroll 2
+        for (int j = threadIdx.x; j < n / EPC; j += blockDim.x) {   // the embedding row, 16-byte vectors
+            const uint4 w = ld_stream16(er + j);
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) dst[j * EPC + e] = Chunk<WT>::elem(w, e) * p.emb_scale;
+        }
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            dst[n + i] = __ldcg(h + i);
+            gs[i] = __ldg(p.norm_e + i);
+            gs[n + i] = __ldg(p.norm_h + i);
+        }
         __syncthreads();
-        rms_into(dst, p.norm_e, p.d_t, p.eps, dst, red);
-        rms_into(dst + p.d_t, p.norm_h, p.d_t, p.eps, dst + p.d_t, red);
+        rms_pair_s(dst, gs, n, p.eps, red);
         break;
     }
     case PH_Q: {
         const int n = p.d_a;
+        const float* ga = p.blk[l].attn_norm;
         if (l == 0) {
             if (p.tc_proj) {   // the pre-projection's partials form the residual stream
                 for (int i = threadIdx.x; i < n; i += blockDim.x) {
                     const float x = part_sum(p, p.sk[PH_PRE], n, b, i);
                     tmp[i] = x;
+                    gs[i] = __ldg(ga + i);
                     if (writer) p.XB[(long long)b * n + i] = x;
                 }
             } else {
-                for (int i = threadIdx.x; i < n; i += blockDim.x) tmp[i] = __ldcg(p.XB + (long long)b * n + i);
+#pragma unroll 4
+                for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                    tmp[i] = __ldcg(p.XB + (long long)b * n + i);
+                    gs[i] = __ldg(ga + i);
+                }
             }
             __syncthreads();
         } else {
+            const float* gp = p.blk[l - 1].post_ffn_norm;
+#pragma unroll 4
             for (int i = threadIdx.x; i < n; i += blockDim.x) {
                 dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_FFN2], n, b, i) : __ldcg(p.Y2 + (long long)b * n + i);
                 tmp[i] = __ldcg(p.XM + (long long)b * n + i);
+                gs[i] = __ldg(ga + i);
+                gs[n + i] = __ldg(gp + i);
             }
             __syncthreads();
-            rms_into(dst, p.blk[l - 1].post_ffn_norm, n, p.eps, dst, red);
+            rms_into_s(dst, gs + n, n, p.eps, dst, red);
             for (int i = threadIdx.x; i < n; i += blockDim.x) {
                 const float x = tmp[i] + dst[i];
                 tmp[i] = x;
@@ -345,37 +409,45 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
             }
             __syncthreads();
         }
-        rms_into(tmp, p.blk[l].attn_norm, n, p.eps, dst, red);
+        rms_into_s(tmp, gs, n, p.eps, dst, red);
         break;
     }
     case PH_FFN1: {
         const int n = p.d_a;
+        const float *g1 = p.blk[l].post_attn_norm, *g2 = p.blk[l].pre_ffn_norm;
+#pragma unroll 4
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_O], n, b, i) : __ldcg(p.YB + (long long)b * n + i);
             tmp[i] = __ldcg(p.XB + (long long)b * n + i);
+            gs[i] = __ldg(g1 + i);
+            gs[n + i] = __ldg(g2 + i);
         }
         __syncthreads();
-        rms_into(dst, p.blk[l].post_attn_norm, n, p.eps, dst, red);
+        rms_into_s(dst, gs, n, p.eps, dst, red);
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             const float x = tmp[i] + dst[i];
             tmp[i] = x;
             if (writer) p.XM[(long long)b * n + i] = x;
         }
         __syncthreads();
-        rms_into(tmp, p.blk[l].pre_ffn_norm, n, p.eps, dst, red);
+        rms_into_s(tmp, gs + n, n, p.eps, dst, red);
         break;
     }
     case PH_POST: {
         const int n = p.d_a;
+        const float *g1 = p.blk[p.L - 1].post_ffn_norm, *g2 = p.final_norm;
+#pragma unroll 4
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_FFN2], n, b, i) : __ldcg(p.Y2 + (long long)b * n + i);
             tmp[i] = __ldcg(p.XM + (long long)b * n + i);
+            gs[i] = __ldg(g1 + i);
+            gs[n + i] = __ldg(g2 + i);
         }
         __syncthreads();
-        rms_into(dst, p.blk[p.L - 1].post_ffn_norm, n, p.eps, dst, red);
+        rms_into_s(dst, gs, n, p.eps, dst, red);
         for (int i = threadIdx.x; i < n; i += blockDim.x) tmp[i] += dst[i];
         __syncthreads();
-        rms_into(tmp, p.final_norm, n, p.eps, dst, red);
+        rms_into_s(tmp, gs + n, n, p.eps, dst, red);
         break;
     }
     case PH_O: {
@@ -423,10 +495,12 @@ template <typename WT>
 __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l, float* smem_act, float* smem_tmp,
                                   float* red, unsigned int& epoch, int& lda, bool& ok) {
     const int K = phase_k(p, phase);
+    // gain stage after the activation area
+    float* gs = smem_act + (p.act_smem ? (long long)p.B * p.kmax : (long long)p.kmax);
     ok = true;
     if (p.act_smem) {
         for (int b = 0; b < p.B; ++b)
-            build_act<WT>(p, phase, k, l, b, smem_act + (long long)b * K, smem_tmp, blockIdx.x == 0, red);
+            build_act<WT>(p, phase, k, l, b, smem_act + (long long)b * K, smem_tmp, blockIdx.x == 0, red, gs);
         lda = K;
         return smem_act;
     }
@@ -437,7 +511,7 @@ __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l,
         if (phase == PH_HEAD) { lda = K; return p.HN; }
     }
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-        build_act<WT>(p, phase, k, l, b, smem_act, smem_tmp, true, red);
+        build_act<WT>(p, phase, k, l, b, smem_act, smem_tmp, true, red, gs);
         if (p.tc_proj) {
             // tensor-core operand: bf16 high and low parts, read by tensor copies
             for (int i = threadIdx.x; i < K; i += blockDim.x) {
@@ -1555,7 +1629,7 @@ static __device__ bool sample_step(const DraftParams& p, int k, unsigned char* s
 
 template <typename WT, int HD, bool TC>
 __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts) {
-    __shared__ float red[kWarps];
+    __shared__ float red[2 * kWarps];
     __shared__ unsigned long long head_best[kWarps][32];
     __shared__ __align__(8) unsigned long long head_bar[kHeadGroups][kHeadSlots];   // LM head slots
     __shared__ float head_part[kHeadGroups][kHeadSlots][4];
