@@ -35,6 +35,23 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
         : "l"(p));
     return r;
 }
+// L2 policy: evict first (weight streams)
+__device__ __forceinline__ unsigned long long l2_evict_first() {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// ld_stream16 for weight streams read once per step, under an L2 policy
+// from l2_evict_first(): the lines go first when L2 evicts, so the small
+// vectors, gains and attention keys and values that phases re-read keep
+// their places
+__device__ __forceinline__ uint4 ld_weight16(const void* p, unsigned long long pol) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -91,6 +108,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned in
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
 }
+// bulk_g2s with an L2 cache policy
+__device__ __forceinline__ void bulk_g2s_pol(void* dst, const void* src, unsigned int bytes, unsigned long long* bar,
+                                             unsigned long long pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
 // order earlier generic-proxy shared-memory accesses before later bulk-copy writes
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -109,6 +135,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
             smem_addr(dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+// tma_load_2d with an L2 cache policy
+__device__ __forceinline__ void tma_load_2d_pol(void* dst, const void* tmap, int x, int y, unsigned long long* bar,
+                                                unsigned long long pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(pol)
         : "memory");
 }
 
@@ -284,22 +319,25 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned int& epoch,
     if (threadIdx.x == 0) {
         epoch += 1;
         const unsigned int target = epoch * arrivals_per_epoch;
-        __threadfence();
-        atomicAdd(&hdr->barrier, 1u);
+        // release: the CTA's writes (ordered before by the CTA barrier) are
+        // visible at GPU scope before its arrival; the acquire load that sees
+        // every arrival orders the CTA's later reads after them
+        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(&hdr->barrier), "r"(1u) : "memory");
         const unsigned long long t0 = global_ns();
         int ok = 1;
         unsigned int spins = 0;
         while (true) {
             const unsigned int v = ld_acquire(&hdr->barrier);
             if ((int)(v - target) >= 0) break;
-            if (ld_relaxed(&hdr->status) != 0) { ok = 0; break; }
-            if ((++spins & 63u) == 0 && global_ns() - t0 > limit_ns) {
-                atomicCAS(&hdr->status, 0, MTP_ERR_TIMEOUT);
-                ok = 0;
-                break;
+            if ((++spins & 63u) == 0) {   // error status and time limit, every 64 polls
+                if (ld_relaxed(&hdr->status) != 0) { ok = 0; break; }
+                if (global_ns() - t0 > limit_ns) {
+                    atomicCAS(&hdr->status, 0, MTP_ERR_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
             }
         }
-        __threadfence();
         s_ok = ok;
     }
     __syncthreads();

@@ -106,6 +106,7 @@ __device__ __forceinline__ void gemv_rows(const WT* __restrict__ W, const WT* __
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int nw = gridDim.x * kWarps;
+    const unsigned long long pol = l2_evict_first();
     for (int r = gw; r < rows; r += nw) {
         const uint4* wr = reinterpret_cast<const uint4*>(W + (long long)r * K);
         const uint4* wr2 = TWO ? reinterpret_cast<const uint4*>(W2 + (long long)r * K) : nullptr;
@@ -117,8 +118,8 @@ __device__ __forceinline__ void gemv_rows(const WT* __restrict__ W, const WT* __
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + lane + 32 * u;
-                w[u] = c < nch ? ld_stream16(wr + c) : make_uint4(0u, 0u, 0u, 0u);
-                if (TWO) w2[u] = c < nch ? ld_stream16(wr2 + c) : make_uint4(0u, 0u, 0u, 0u);
+                w[u] = c < nch ? ld_weight16(wr + c, pol) : make_uint4(0u, 0u, 0u, 0u);
+                if (TWO) w2[u] = c < nch ? ld_weight16(wr2 + c, pol) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -314,7 +315,20 @@ __device__ __forceinline__ int step_token(const DraftParams& p, int b, int k) {
 // float4 at q summed over S copies st floats apart, in order
 __device__ __forceinline__ float4 ld4_sum(const float* q, int S, long long st) {
     float4 a = __ldcg(reinterpret_cast<const float4*>(q));
-    for (int s = 1; s < S; ++s) {
+    int s = 1;
+    for (; s + 4 <= S; s += 4) {   // four loads in flight, summed in order
+        float4 c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) c[u] = __ldcg(reinterpret_cast<const float4*>(q + (s + u) * st));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            a.x += c[u].x;
+            a.y += c[u].y;
+            a.z += c[u].z;
+            a.w += c[u].w;
+        }
+    }
+    for (; s < S; ++s) {
         const float4 c = __ldcg(reinterpret_cast<const float4*>(q + s * st));
         a.x += c.x;
         a.y += c.y;
@@ -342,10 +356,44 @@ __device__ __forceinline__ float part_sum(const DraftParams& p, int S, int R, in
     return v;
 }
 
+// dst[s][i] = src[s][i] for i < n (n a multiple of 4, 16-byte aligned rows):
+// every load of a thread is issued before its first store.  The stores go
+// through generic pointers the compiler cannot tell apart from the sources,
+// so a loop that stored each element before loading the next would wait for
+// one round trip per element.
+template <int NS>
+struct VecCopy {
+    const float* src[NS];
+    float* dst[NS];
+};
+// (global-memory sources only)
+template <int NS, int MAXV>
+__device__ __forceinline__ void vec_copy(const VecCopy<NS>& c, int n) {
+    const int n4 = n >> 2;
+#pragma unroll 1
+    for (int base = threadIdx.x; base < n4; base += MAXV * kThreads) {
+        float4 v[NS][MAXV];
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+            const int i = base + j * kThreads;
+#pragma unroll
+            for (int s = 0; s < NS; ++s)
+                if (i < n4) v[s][j] = __ldcg(reinterpret_cast<const float4*>(c.src[s]) + i);
+        }
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j) {
+            const int i = base + j * kThreads;
+#pragma unroll
+            for (int s = 0; s < NS; ++s)
+                if (i < n4) reinterpret_cast<float4*>(c.dst[s])[i] = v[s][j];
+        }
+    }
+}
+
 // Writes sequence b's input vector for `phase` into dst (length phase_k).
 // `writer` marks the one CTA that also stores residual-stream updates.  The
 // norm gains are staged in gs (2 max(d_t, d_a) floats) by the same loops that
-// load the activations, so every load of a prologue is in flight at once.
+// load the activations.
 template <typename WT>
 __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, float* dst, float* tmp, bool writer,
                           float* red, float* gs) {
@@ -452,24 +500,30 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     }
     case PH_O: {
         const int n = p.Hq * p.hd;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(p.OB + (long long)b * n + i);
+        vec_copy<1, 1>(VecCopy<1>{{p.OB + (long long)b * n}, {dst}}, n);
         __syncthreads();
         break;
     }
     case PH_FFN2: {
         const int n = p.F;
         if (p.tc_proj) {   // GeGLU of the summed gate (rows 0..F-1) and up (rows F..2F-1) partials
-            for (int i = threadIdx.x; i < n; i += blockDim.x)
-                dst[i] = gelu_tanh(part_sum(p, p.sk[PH_FFN1], 2 * n, b, i)) * part_sum(p, p.sk[PH_FFN1], 2 * n, b, n + i);
+            const long long st = (long long)p.B * 2 * n;
+            const float* q = p.PB + (long long)b * 2 * n;
+            const int S = p.sk[PH_FFN1];
+            for (int i4 = threadIdx.x; i4 < (n >> 2); i4 += kThreads) {
+                const float4 g = ld4_sum(q + 4 * i4, S, st), u = ld4_sum(q + n + 4 * i4, S, st);
+                reinterpret_cast<float4*>(dst)[i4] = make_float4(gelu_tanh(g.x) * u.x, gelu_tanh(g.y) * u.y,
+                                                                 gelu_tanh(g.z) * u.z, gelu_tanh(g.w) * u.w);
+            }
         } else {
-            for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(p.MB + (long long)b * n + i);
+            vec_copy<1, 1>(VecCopy<1>{{p.MB + (long long)b * n}, {dst}}, n);
         }
         __syncthreads();
         break;
     }
     case PH_HEAD: {
         const int n = p.d_t;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(p.HN + (long long)b * n + i);
+        vec_copy<1, 1>(VecCopy<1>{{p.HN + (long long)b * n}, {dst}}, n);
         __syncthreads();
         break;
     }
@@ -1257,7 +1311,8 @@ __device__ bool head_groups_b1(const DraftParams& p, unsigned char* ring, unsign
     auto issue = [&](int j) {
         const int slot = j % kHeadSlots;
         mbar_arrive_expect_tx(&bars[q][slot], rowb);
-        bulk_g2s(gring + slot * p.head_slotb, W + (long long)(r0 + q + 4 * j) * nch * EPC, rowb, &bars[q][slot]);
+        bulk_g2s_pol(gring + slot * p.head_slotb, W + (long long)(r0 + q + 4 * j) * nch * EPC, rowb, &bars[q][slot],
+                     l2_evict_first());
     };
     __syncthreads();   // the slots reuse shared memory of earlier phases
     if (issuer) {
@@ -1343,6 +1398,7 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
     if (warp == 0) {
         if (lane == 0) {
             uint32_t g = ts.g;
+            const unsigned long long pol = l2_evict_first();   // weight tiles: read once per step
             for (int j = 0; j < nit && ok; ++j) {
                 const int item = (int)blockIdx.x + j * (int)gridDim.x;
                 const int row0 = (item / J.S) * kTcTileM;
@@ -1362,7 +1418,7 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
                     }
                     unsigned char* sp = ring + st * sbytes;
                     mbar_arrive_expect_tx(&ts.full[st], tx);
-                    tma_load_2d(sp, wm, ks * kTcTileK, wy, &ts.full[st]);
+                    tma_load_2d_pol(sp, wm, ks * kTcTileK, wy, &ts.full[st], pol);
                     bulk_g2s(sp + abytes, J.xh + (long long)ks * Bp * kTcTileK, xbytes, &ts.full[st]);
                     if (J.lo) bulk_g2s(sp + abytes + xbytes, J.xl + (long long)ks * Bp * kTcTileK, xbytes, &ts.full[st]);
                 }
