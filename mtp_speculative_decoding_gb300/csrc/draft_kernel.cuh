@@ -145,11 +145,97 @@ __device__ __forceinline__ void gemv_rows(const WT* __restrict__ W, const WT* __
     }
 }
 
+// One sequence, fewer rows than half the grid's warps: S warps of a CTA
+// share a row, each over a contiguous 1/S of its chunks, and the partial dot
+// products are added in segment order through `xred` (kWarps floats).
+template <typename WT, int U, int S, class Epi>
+__device__ __forceinline__ void gemv_rows_split(const WT* __restrict__ W, int rows, int K, const float* act, Epi& epi,
+                                                float* xred) {
+    constexpr int EPC = Chunk<WT>::EPC, RPC = kWarps / S;
+    const int nch = K / EPC;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, seg = warp % S;
+    const int c_lo = seg * nch / S, c_hi = (seg + 1) * nch / S;
+    const unsigned long long pol = l2_evict_first();
+    for (int r0 = blockIdx.x * RPC; r0 < rows; r0 += gridDim.x * RPC) {   // the same trip count on every warp
+        const int r = r0 + warp / S;
+        float acc = 0.f;
+        if (r < rows) {
+            const uint4* wr = reinterpret_cast<const uint4*>(W + (long long)r * K);
+            for (int c0 = c_lo; c0 < c_hi; c0 += 32 * U) {
+                uint4 w[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + lane + 32 * u;
+                    w[u] = c < c_hi ? ld_weight16(wr + c, pol) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + lane + 32 * u;
+                    if (c < c_hi) acc += Chunk<WT>::dot(w[u], act + c * EPC);
+                }
+            }
+            acc = warp_sum(acc);
+        }
+        if (seg != 0 && lane == 0) xred[warp] = acc;
+        __syncthreads();
+        if (seg == 0 && r < rows) {
+#pragma unroll
+            for (int q = 1; q < S; ++q) acc += xred[warp + q];
+            const float a[1] = {acc};
+            epi.apply(r, 0, 1, a, a);
+        }
+        __syncthreads();
+    }
+}
+
+// One sequence, rows of at most 16 U chunks: each warp loads two of its
+// grid-strided rows (r and r + the grid's warp count) in one batch.
+template <typename WT, int U, class Epi>
+__device__ __forceinline__ void gemv_rows_pair(const WT* __restrict__ W, int rows, int K, const float* act, Epi& epi) {
+    constexpr int EPC = Chunk<WT>::EPC, UH = U / 2;
+    const int nch = K / EPC;
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int nw = gridDim.x * kWarps;
+    const unsigned long long pol = l2_evict_first();
+    for (int r = gw; r < rows; r += 2 * nw) {
+        const int r2 = r + nw;
+        const bool two = r2 < rows;
+        const uint4* wa = reinterpret_cast<const uint4*>(W + (long long)r * K);
+        const uint4* wb = reinterpret_cast<const uint4*>(W + (long long)(two ? r2 : r) * K);
+        uint4 w[U];
+#pragma unroll
+        for (int u = 0; u < UH; ++u) {
+            const int c = lane + 32 * u;
+            w[u] = c < nch ? ld_weight16(wa + c, pol) : make_uint4(0u, 0u, 0u, 0u);
+            w[UH + u] = c < nch && two ? ld_weight16(wb + c, pol) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int u = 0; u < UH; ++u) {
+            const int c = lane + 32 * u;
+            if (c < nch) {
+                a0 += Chunk<WT>::dot(w[u], act + c * EPC);
+                a1 += Chunk<WT>::dot(w[UH + u], act + c * EPC);
+            }
+        }
+        const float s0[1] = {warp_sum(a0)}, s1[1] = {warp_sum(a1)};
+        epi.apply(r, 0, 1, s0, s0);
+        if (two) epi.apply(r2, 0, 1, s1, s1);
+    }
+}
+
 template <typename WT, int U, bool TWO, class Epi>
 __device__ __forceinline__ void gemv(const WT* W, const WT* W2, int rows, int K, const float* act, int lda, int nb,
-                                     Epi& epi) {
+                                     Epi& epi, float* xred) {
     if (nb == 1) {
-        gemv_rows<WT, U, 1, TWO>(W, W2, rows, K, act, lda, 0, 1, epi);
+        const int nw = gridDim.x * kWarps, nch = K / Chunk<WT>::EPC;
+        if (!TWO && 2 * rows <= nw && nch >= 64)
+            gemv_rows_split<WT, U, 2>(W, rows, K, act, epi, xred);
+        else if (!TWO && rows > nw && 2 * nch <= 32 * U)
+            gemv_rows_pair<WT, U>(W, rows, K, act, epi);
+        else
+            gemv_rows<WT, U, 1, TWO>(W, W2, rows, K, act, lda, 0, 1, epi);
     } else {
         for (int b0 = 0; b0 < nb; b0 += 4) gemv_rows<WT, U, 4, TWO>(W, W2, rows, K, act, lda, b0, nb, epi);
     }
@@ -1606,7 +1692,8 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
         }
         if (!__syncthreads_and(ok)) return false;
     } else {
-        gemv<WT, 8, false>(reinterpret_cast<const WT*>(p.tok_embd), nullptr, p.V, p.d_t, a, lda, p.B, e);
+        gemv<WT, 8, false>(reinterpret_cast<const WT*>(p.tok_embd), nullptr, p.V, p.d_t, a, lda, p.B, e,
+                           &hpart[0][0][0]);   // the slots' partials are free here
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int c0 = 0; c0 < p.B; c0 += 32) {
@@ -1775,7 +1862,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             }
         } else {
             gemv<WT, TWO ? U / 2 : U, TWO>(reinterpret_cast<const WT*>(W), reinterpret_cast<const WT*>(W2), R, K, a,
-                                           lda, p.B, epi);
+                                           lda, p.B, epi, red);
         }
         if (TC && p.tc_head && phase == PH_POST) fence_proxy_async_global();   // h parts are read by tensor copies
         return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);

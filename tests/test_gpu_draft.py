@@ -39,6 +39,19 @@ def test_small_single_sequence(dtype):
     check_draft_parity(w, d, h, z, seqs=[0])
 
 
+def test_single_sequence_split_and_paired_rows():
+    """B = 1 with rows that take the split-row GEMV (fewer rows than half the
+    grid's warps: pre/post-projection, O, FFN2; 250 chunks split unevenly
+    over CTAs of 8 rows) and the paired-row GEMV (4096 query rows of 125
+    chunks, more rows than warps, a ragged second row)."""
+    m = synth.ModelSpec(d_t=1000, d_a=1000, n_blocks=1, n_q_heads=16, head_dim=256, n_kv_heads=4, d_ff=1200,
+                        vocab=3001, dtype="bf16", block_view=(0,))
+    views = [synth.ViewSpec(cap=160, window=0, rope_theta=1e6)]
+    w = synth.make_draft_workload("wide_b1", m, views, 1, 2, [150], 21, hist_len=4)
+    _, d, h, z = run_gpu_draft(w)
+    check_draft_parity(w, d, h, z, seqs=[0])
+
+
 def test_small_softcap_and_head_dim_64():
     w = small_workload("bf16", softcap=5.0, hd=64, kv=(1, 64, 127))
     _, d, h, z = run_gpu_draft(w)
