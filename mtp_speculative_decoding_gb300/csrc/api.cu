@@ -113,8 +113,9 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     L.PART = off;    off = al256(off + items * attn_psz(grp, c->head_dim) * f);
     L.ROPE = off;    off = al256(off + (size_t)MTP_MAX_VIEWS * (c->head_dim / 2) * sizeof(double));
     L.ROPEQ = off;   off = al256(off + (size_t)B * MTP_MAX_VIEWS * (c->head_dim / 2) * 2 * f);
-    // tensor-core operands: K blocks of 64 columns x Bp rows, bf16
-    const size_t xb = tc_head_eligible(c, B) ? (size_t)((c->d_t + 63) / 64) * pad16(B) * 128 : 0;
+    // tensor-core operands: K blocks of 64 columns x (kTcHeadM rows for the
+    // head's h, Bp rows for the projections' inputs), bf16
+    const size_t xb = tc_head_eligible(c, B) ? (size_t)((c->d_t + 63) / 64) * kTcHeadM * 128 : 0;
     L.XH = off;      off = al256(off + xb);
     L.XL = off;      off = al256(off + xb);
     const bool tcp = tc_proj_eligible(c, B);
@@ -319,16 +320,21 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     }
     // batch: LM head on tensor cores, operand ring at offset 0 (1024-aligned)
     const bool tc = tc_head_eligible(cfg, B);
-    int tc_stages = 0, tc_cols = 0;
+    int tc_stages = 0, tc_cols = 0, th_stages = 0;
     if (tc) {
         const size_t sbytes = (size_t)kTcTileM * 128 + 2 * (size_t)pad16(B) * 128;
         tc_stages = (int)(kTcSmemBudget / sbytes);
         if (tc_stages > kTcMaxStages) tc_stages = kTcMaxStages;
         if (tc_stages < 2) return MTP_ERR_UNSUPPORTED;
-        const size_t need = (size_t)tc_stages * sbytes + 1024;
+        size_t need = (size_t)tc_stages * sbytes + 1024;
         if (need > smem) smem = need;
-        tc_cols = 32;
-        while (tc_cols < 2 * pad16(B)) tc_cols *= 2;
+        // the head's ring: a table box and h's high (and, sampling, low) block per stage
+        const size_t hbytes = (size_t)kTcHeadN * 128 + (sampling ? 2 : 1) * (size_t)kTcHeadM * 128;
+        th_stages = (int)(kTcHeadSmemBudget / hbytes);
+        if (th_stages > kTcMaxStages) th_stages = kTcMaxStages;
+        need = (size_t)th_stages * hbytes + 1024;
+        if (need > smem) smem = need;
+        tc_cols = kTcHeadCols;   // the head's two accumulators; the projections use the first 2 Bp columns
     }
     const int per_sm = !bf ? draft_blocks_per_sm_f32(cfg->head_dim, smem)
                        : tc ? draft_blocks_per_sm_bf16_tc(cfg->head_dim, smem)
@@ -387,10 +393,11 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         p.tc_head = 1;
         p.Bp = pad16(B);
         p.tc_stages = tc_stages;
+        p.th_stages = th_stages;
         p.tc_cols = tc_cols;
         p.XH = reinterpret_cast<uint16_t*>(base + L.XH);
         p.XL = reinterpret_cast<uint16_t*>(base + L.XL);
-        if (!encode_bf16_map(&p.tm_embd, w->tok_embd, (uint64_t)cfg->d_t, (uint64_t)cfg->vocab, kTcTileM))
+        if (!encode_bf16_map(&p.tm_embd, w->tok_embd, (uint64_t)cfg->d_t, (uint64_t)cfg->vocab, kTcHeadN))
             return MTP_ERR_CUDA;
         if (tc_proj_eligible(cfg, B) && !act_smem) {
             // projections: weights [R, K] row-major, inputs staged as [Bp, kmax]

@@ -41,6 +41,13 @@ constexpr int kTcTileM = 128;
 constexpr int kTcTileK = 64;
 constexpr int kTcMaxStages = 8;
 constexpr size_t kTcSmemBudget = 128 * 1024;
+// LM head on tensor cores: the batch (rows >= B zero) is the MMA's M = 64
+// side and 256 rows of the token table its N side, so each MMA takes 8 KB of
+// the table; stages of one 64 x 256 table box and the batch's 64 x 64 block(s)
+constexpr int kTcHeadM = 64;
+constexpr int kTcHeadN = 256;
+constexpr size_t kTcHeadSmemBudget = 200 * 1024;
+constexpr int kTcHeadCols = 512;   // tensor-memory columns: two 256-column accumulators
 
 // floats per attention partial: o[grp][hd], m[grp], l[grp], padded to 16 bytes
 __host__ __device__ constexpr int attn_psz(int grp, int hd) { return (grp * (hd + 2) + 3) & ~3; }
@@ -107,7 +114,8 @@ struct DraftParams {
     int head_slotb;              // > 0: one sequence, LM head rows through bulk-copy slots of this many bytes
     int tc_head;                 // 1: LM head on tensor cores
     int Bp, tc_stages, tc_cols;  // batch padded to 16; operand ring depth; tensor-memory columns
-    uint16_t *XH, *XL;           // bf16 high / low parts of h as the head's tiled operand (rows >= B zero)
+    int th_stages;               // LM head ring depth
+    uint16_t *XH, *XL;           // bf16 high / low parts of h as the head's tiled operand (kTcHeadM rows, >= B zero)
     int tc_proj;                 // 1: projections on tensor cores (activations staged in global memory)
     int sk[6];                   // split-K factor of each projection phase (PH_PRE .. PH_POST)
     uint16_t *XA, *XAL;          // bf16 high / low parts of the current phase input, tiled

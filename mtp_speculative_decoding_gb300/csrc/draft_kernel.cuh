@@ -1572,31 +1572,131 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
     return __syncthreads_and(ok) != 0;
 }
 
-// epilogue: LM-head logits -> softcap, optional store, per-sequence argmax
-// (all lanes of a warp call it with the same c0)
-struct TcHeadEpi {
-    const DraftParams& p;
-    int k;
-    HeadEpi& e;
-    __device__ __forceinline__ void apply(int row, int, int c0, const uint32_t (&r)[16]) {
-        const int lane = threadIdx.x & 31;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            const int b = c0 + jj;
-            if (b < p.B) {
-                float z = __uint_as_float(r[jj]);
-                if (p.softcap > 0.f) z = p.softcap * tanhf(z / p.softcap);
-                if (row < p.V && p.out_logits) p.out_logits[((long long)b * p.N + k) * p.V + row] = z;
-                if (row < p.V && p.ZB) p.ZB[(long long)b * p.V + row] = z;
-                const unsigned long long key = warp_max_u64(row < p.V ? pack_argmax(z, (uint32_t)row) : 0ull);
-                if (lane == (b & 31)) {
-                    if (b < 32) e.best_lo = key > e.best_lo ? key : e.best_lo;
-                    else e.best_hi = key > e.best_hi ? key : e.best_hi;
+// LM head on tensor cores, step k: D[b, n] = sum_c h[b, c] E[n, c] over
+// 256-row tiles of the token table E (tile t: rows 256 t ..), tile c,
+// c + grid, ... on CTA c.  The batch block (kTcHeadM rows, zero past B) is
+// the MMA's A operand and the table tile its B operand (M = 64, N = 256), so
+// one MMA takes 8 KB of the table; with the table as the M side (M = 128,
+// N = batch) the same loop issued twice the MMAs per byte and was bound by
+// them.  Warp 0 (one lane) streams a 64 x 256 table box and the batch's
+// bf16 block(s) of each K step through a th_stages-deep ring, warp 1 (one
+// lane) issues the MMAs (greedy: h's high part; sampling: high and low)
+// into one of two 256-column accumulators, and warps 4-7 read them back:
+// accumulator row b lies in tensor-memory lane 32 (b / 16) + b % 16, so lane
+// i < 16 of epilogue warp q owns sequence 16 q + i.  Each owner applies the
+// softcap, stores the logits it is asked for, keeps its argmax key over its
+// tiles and folds it into amax[k, b] once.  Barrier phases continue across
+// steps through `ts` (a ring of its own: its stages differ from the
+// projections').
+static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigned char* smem, TcState& ts) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int NS = p.th_stages;
+    const bool lo = p.sampling != 0;
+    const uint32_t wbytes = kTcHeadN * 128, xbytes = kTcHeadM * 128;
+    const uint32_t sbytes = wbytes + (lo ? 2 : 1) * xbytes;     // stage stride = bytes landing per stage
+    const uint32_t tx = sbytes;
+    const uint32_t base = (smem_addr(smem) + 1023u) & ~1023u;   // 1024-byte aligned ring
+    unsigned char* ring = smem + (base - smem_addr(smem));
+    const int ntiles = (p.V + kTcHeadN - 1) / kTcHeadN, nks = (p.d_t + kTcTileK - 1) / kTcTileK;
+    const int nit = ntiles > (int)blockIdx.x ? (ntiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    bool ok = true;
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t g = ts.g;
+            const unsigned long long pol = l2_evict_first();   // the table: read once per step
+            const int rot = (int)blockIdx.x % nks;               // K order rotated per CTA (the batch blocks are shared)
+            for (int j = 0; j < nit && ok; ++j) {
+                const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * kTcHeadN;
+                for (int i = 0; i < nks; ++i, ++g) {
+                    const int ks = i + rot < nks ? i + rot : i + rot - nks;
+                    const uint32_t st = g % NS;
+                    if (!mbar_wait_limited(&ts.empty[st], ((g / NS) & 1u) ^ 1u, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* sp = ring + st * sbytes;
+                    mbar_arrive_expect_tx(&ts.full[st], tx);
+                    tma_load_2d_pol(sp, &p.tm_embd, ks * kTcTileK, row0, &ts.full[st], pol);
+                    bulk_g2s(sp + wbytes, p.XH + (long long)ks * kTcHeadM * kTcTileK, xbytes, &ts.full[st]);
+                    if (lo) bulk_g2s(sp + wbytes + xbytes, p.XL + (long long)ks * kTcHeadM * kTcTileK, xbytes, &ts.full[st]);
                 }
             }
         }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t g = ts.g;
+            const uint32_t idesc = umma_idesc_bf16(kTcHeadM, kTcHeadN);
+            for (int j = 0; j < nit && ok; ++j) {
+                const uint32_t it = ts.it + j, acc = it & 1u;
+                if (!mbar_wait_limited(&ts.tempty[acc], ((it >> 1) & 1u) ^ 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = ts.tmem + acc * (uint32_t)kTcHeadN;
+                for (int ks = 0; ks < nks; ++ks, ++g) {
+                    const uint32_t st = g % NS;
+                    if (!mbar_wait_limited(&ts.full[st], (g / NS) & 1u, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + st * sbytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTcTileK / 16; ++kk) {
+                        const uint64_t bd = umma_desc_sw128(sa + kk * 32);   // table tile, K slice kk
+                        umma_bf16(d, umma_desc_sw128(sa + wbytes + kk * 32), bd, idesc, (ks | kk) != 0 ? 1u : 0u);
+                        if (lo) umma_bf16(d, umma_desc_sw128(sa + wbytes + xbytes + kk * 32), bd, idesc, 1u);
+                    }
+                    umma_commit(&ts.empty[st]);
+                }
+                if (!ok) break;
+                umma_commit(&ts.tfull[acc]);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        const int q = warp - 4;   // tensor-memory lane quarter of this warp
+        const int b = 16 * q + lane;
+        const bool mine = lane < 16 && b < p.B;
+        unsigned long long best = 0ull;
+        for (int j = 0; j < nit && ok; ++j) {
+            const uint32_t it = ts.it + j, acc = it & 1u;
+            if (!mbar_wait_limited(&ts.tfull[acc], (it >> 1) & 1u, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * kTcHeadN;
+            const uint32_t ta = ts.tmem + ((uint32_t)(32 * q) << 16) + acc * (uint32_t)kTcHeadN;
+            for (int c0 = 0; c0 < kTcHeadN; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(ta + (uint32_t)c0, r);
+                tmem_ld_wait();
+                if (mine) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int row = row0 + c0 + jj;
+                        if (row < p.V) {
+                            float z = __uint_as_float(r[jj]);
+                            if (p.softcap > 0.f) z = p.softcap * tanhf(z / p.softcap);
+                            if (p.out_logits) p.out_logits[((long long)b * p.N + k) * p.V + row] = z;
+                            if (p.ZB) p.ZB[(long long)b * p.V + row] = z;
+                            const unsigned long long key = pack_argmax(z, (uint32_t)row);
+                            best = key > best ? key : best;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ts.tempty[acc]);
+        }
+        if (mine && nit > 0) atomicMax(p.amax + (long long)k * p.B + b, best);
     }
-};
+    ts.g += (uint32_t)(nit * nks);
+    ts.it += (uint32_t)nit;
+    return __syncthreads_and(ok) != 0;
+}
 
 // epilogue: split partial of a projection, PB[split][b][row]
 struct TcPartEpi {
@@ -1664,22 +1764,12 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
                                            float (*hpart)[kHeadSlots][4], TcState& ts) {
     HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull, p.ZB};
     if (TC && p.tc_head) {
-        TcJob J;
-        J.wa = J.wb = &p.tm_embd;
-        J.xh = p.XH;
-        J.xl = p.XL;
-        J.R1 = J.R = p.V;
-        J.nks = (p.d_t + kTcTileK - 1) / kTcTileK;
-        J.S = 1;
-        J.kps = J.nks;
         // greedy: h rounded to bf16 (half the MMAs and operand traffic; the
         // argmax is stable to it); sampling: both parts, so the sampler sees
-        // logits as close as the CUDA-core path's
-        J.lo = p.sampling != 0;
-        TcHeadEpi he{p, k, e};
-        if constexpr (TC) {
-            if (!tc_gemm(p, J, smem, ts, he)) return false;
-        }
+        // logits as close as the CUDA-core path's.  The epilogue folds its
+        // maxima into amax itself.
+        if constexpr (TC) return tc_head(p, k, smem, ts);
+        return false;
     } else if (p.head_slotb > 0) {
         const int cpl = (p.d_t / Chunk<WT>::EPC + 127) / 128;
         bool ok = true;
@@ -1771,7 +1861,7 @@ static __device__ bool sample_step(const DraftParams& p, int k, unsigned char* s
 }
 
 template <typename WT, int HD, bool TC>
-__device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts) {
+__device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts, TcState& hs) {
     __shared__ float red[2 * kWarps];
     __shared__ unsigned long long head_best[kWarps][32];
     __shared__ __align__(8) unsigned long long head_bar[kHeadGroups][kHeadSlots];   // LM head slots
@@ -1811,7 +1901,8 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     // length are never written; bulk copies read them from the first phase
     // on, after >= 1 barrier)
     if (TC && p.tc_head) {
-        const long long nh = (long long)((p.d_t + 63) / 64) * p.Bp * 64, na = p.tc_proj ? (long long)((p.kmax + 63) / 64) * p.Bp * 64 : 0;
+        const long long nh = (long long)((p.d_t + 63) / 64) * kTcHeadM * 64,
+                        na = p.tc_proj ? (long long)((p.kmax + 63) / 64) * p.Bp * 64 : 0;
         for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * nh + 2 * na;
              i += (long long)gridDim.x * blockDim.x) {
             if (i < nh) p.XH[i] = 0;
@@ -1853,7 +1944,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             if constexpr (TC) {
                 const TcJob J = tc_job(p, phase, l);
                 if (phase == PH_POST) {
-                    TcHnEpi he{p.HN, p.XH, p.XL, p.B, p.d_t, p.Bp};
+                    TcHnEpi he{p.HN, p.XH, p.XL, p.B, p.d_t, kTcHeadM};
                     if (!tc_gemm(p, J, smem, ts, he)) return false;
                 } else {
                     TcPartEpi pe{p.PB, p.B, J.R};
@@ -1936,7 +2027,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         }
         // ---- POST ----
         if (TC && p.tc_head) {
-            StoreXhEpi e{p.HN, p.d_t, p.XH, p.XL, p.Bp};
+            StoreXhEpi e{p.HN, p.d_t, p.XH, p.XL, kTcHeadM};
             if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         } else {
             StoreEpi e{p.HN, p.d_t};
@@ -1950,7 +2041,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 a = stage_act<WT>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
                 if (!ok) return;
             }
-            if (!head_phase<WT, TC>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part, ts)) return;
+            if (!head_phase<WT, TC>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part, hs)) return;
         }
         if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
         // ---- SAMPLE (temperature > 0): sample_dist of the step's logits ----
@@ -1971,15 +2062,19 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
 template <typename WT, int HD, bool TC>
 __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long tc_bar[2 * kTcMaxStages + 4];
+    constexpr int NB = 2 * kTcMaxStages + 4;   // barriers of one ring
+    __shared__ __align__(8) unsigned long long tc_bar[2 * NB];   // the projections' ring, then the head's
     __shared__ unsigned int tc_tmem;
     TcState ts{tc_bar, tc_bar + kTcMaxStages, tc_bar + 2 * kTcMaxStages, tc_bar + 2 * kTcMaxStages + 2, 0u, 0u, 0u};
+    unsigned long long* hb = tc_bar + NB;
+    TcState hs{hb, hb + kTcMaxStages, hb + 2 * kTcMaxStages, hb + 2 * kTcMaxStages + 2, 0u, 0u, 0u};
     const int warp = threadIdx.x >> 5;
     if (TC && p.tc_head) {
-        // full / empty stage barriers (one arrival each), accumulator full
-        // (one commit) and empty (one arrival per epilogue warp)
-        if (threadIdx.x < 2 * kTcMaxStages + 4)
-            mbar_init(&tc_bar[threadIdx.x], threadIdx.x >= 2 * kTcMaxStages + 2 ? 4u : 1u);
+        // per ring: full / empty stage barriers (one arrival each),
+        // accumulator full (one commit) and empty (one arrival per epilogue
+        // warp)
+        if (threadIdx.x < 2 * NB)
+            mbar_init(&tc_bar[threadIdx.x], threadIdx.x % NB >= 2 * kTcMaxStages + 2 ? 4u : 1u);
         if (warp == 2) {
             tmem_alloc(&tc_tmem, (unsigned int)p.tc_cols);
             tmem_relinquish();
@@ -1989,8 +2084,9 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         __syncthreads();
         tc_fence_after();
         ts.tmem = tc_tmem;
+        hs.tmem = tc_tmem;
     }
-    draft_body<WT, HD, TC>(p, smem, ts);
+    draft_body<WT, HD, TC>(p, smem, ts, hs);
     if (TC && p.tc_head) {
         tc_fence_before();
         __syncthreads();

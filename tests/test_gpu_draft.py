@@ -70,6 +70,20 @@ def test_small_batch_needs_global_activations():
     check_draft_parity(w, d, h, z, seqs=[0, 17, 39])
 
 
+def test_tensor_core_head_ragged_vocab_softcap():
+    """Smallest tensor-core batch (B = 9): the head's 256-row table tiles end
+    in a partial tile (V = 3001), logits are soft-capped and stored, and the
+    batch block is zero past B."""
+    m = synth.ModelSpec(d_t=1024, d_a=256, n_blocks=1, n_q_heads=4, head_dim=64, n_kv_heads=1, d_ff=512,
+                        vocab=3001, dtype="bf16", block_view=(0,), logit_softcap=8.0)
+    views = [synth.ViewSpec(cap=96, window=0, rope_theta=1e6)]
+    rng = np.random.default_rng(3)
+    kv = rng.integers(1, 97, size=9)
+    w = synth.make_draft_workload("tc_head_v3001", m, views, 9, 2, kv, 13, hist_len=4)
+    _, d, h, z = run_gpu_draft(w)
+    check_draft_parity(w, d, h, z, seqs=[0, 4, 8])
+
+
 def test_workload0_tiny_fp32():
     w = synth.make_draft_inputs(0)
     _, d, h, z = run_gpu_draft(w)
