@@ -8,6 +8,9 @@ for the Gemma-assistant-shaped workload (bf16, d_t 5120, d_a 1024, 4 blocks,
 8192 cached positions; 3 blocks attend a 1024-window sliding layer, 1 a full
 layer).  Metric: drafted tokens per second = B * N / (draft + verify time).
 
+`--workload 4` times exact temp > 0 verification alone (mtp_verify_sample,
+B = 32, N = 3, V = 248320): that configuration has no draft block.
+
 Prints ONE JSON line.  `--impl reference` times the CPU oracle instead on the
 same workload (a bounded sample per step).  Multi-GPU (torchrun): every rank
 runs an independent replica (the path has no cross-sequence exchange); the
@@ -42,7 +45,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[0, 1, 2, 3])
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -348,6 +351,162 @@ def run_ours(args):
         print(json.dumps(result))
 
 
+# ----------------------------------------------------------------------------
+# workload 4: exact temp > 0 verification alone (no draft block in this
+# configuration): B = 32 sequences, N = 3 drafts, V = 248320, bf16 logits
+# ----------------------------------------------------------------------------
+
+L2_FLUSH_BYTES = 256 << 20   # written between timed launches: the 111 MB of logits fit in the 129 MB L2
+
+
+def verify_sample_bytes(inp) -> int:
+    """Algorithmic bytes of one mtp_verify_sample call: one read of the target
+    and draft logits (the history and drafts are a few KB)."""
+    return int(inp.target.nbytes + inp.draft.nbytes)
+
+
+def run_verify_sample(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    import mtp_speculative_decoding_gb300 as mtp
+    from mtp_speculative_decoding_gb300 import build as mtp_build
+    from mtp_speculative_decoding_gb300.device import to_device
+    mtp_build.build()
+
+    inp = synth.make_verify_sample_inputs()
+    B, R, V = inp.target.shape
+    N = R - 1
+    tg, df = to_device(inp.target, inp.dtype), to_device(inp.draft, inp.dtype)
+    dr = torch.from_numpy(np.ascontiguousarray(inp.drafts, dtype=np.int32)).cuda()
+    hi = torch.from_numpy(np.ascontiguousarray(inp.hist, dtype=np.int32)).cuda()
+    out = torch.empty((B, R), dtype=torch.int32, device="cuda")
+    n_acc = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ws = mtp.alloc_workspace(mtp.workspace_size(None, B, N, V))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        mtp.verify_sample(tg, df, dr, hi, inp.params, inp.seed, i, out, n_acc, ws)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    if mtp.last_error(ws) != 0:
+        raise RuntimeError(f"verify_sample status {mtp.last_error(ws)}")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(float(i))   # evict the logits from L2
+        ev[i][0].record(stream)
+        step(1000 + i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if mtp.last_error(ws) != 0:
+        raise RuntimeError(f"verify_sample status {mtp.last_error(ws)}")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(ms)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    value = world * B * N * args.steps / (total_ms / 1e3)
+
+    # end-to-end through the public API with pinned host buffers: the logits,
+    # drafts and history go up, the emitted tokens and accept counts come back
+    h_tg = torch.empty(tg.shape, dtype=tg.dtype).pin_memory()
+    h_tg.copy_(tg.cpu())
+    h_df = torch.empty(df.shape, dtype=df.dtype).pin_memory()
+    h_df.copy_(df.cpu())
+    h_dr = dr.cpu().pin_memory()
+    h_hi = hi.cpu().pin_memory()
+    h_out = torch.empty((B, R), dtype=torch.int32).pin_memory()
+    h_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in (h_tg, h_df, h_dr, h_hi))
+    bo = h_out.numel() * 4 + h_n.numel() * 4
+
+    def e2e_step(i):
+        tg.copy_(h_tg, non_blocking=True)
+        df.copy_(h_df, non_blocking=True)
+        dr.copy_(h_dr, non_blocking=True)
+        hi.copy_(h_hi, non_blocking=True)
+        step(i)
+        h_out.copy_(out, non_blocking=True)
+        h_n.copy_(n_acc, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(2000 + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * B * N * args.steps / (e2e_ms / 1e3)
+
+    peak, peak_kind = measured_peaks()
+    alg = verify_sample_bytes(inp)
+    achieved = alg / (statistics.mean(ms) / 1e3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype,
+        "data": "synthetic (seeded; target logits N(0, 2^2), draft logits correlated at 0.8)",
+        "config": {"workload": synth.WORKLOADS[4], "B": B, "N": N, "vocab": V, "history": int(inp.hist.shape[1]),
+                   "path": "mtp_verify_sample alone (this configuration has no draft block)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"flushed before every timed launch ({L2_FLUSH_BYTES >> 20} MB written)",
+                   "verify_ms_mean": round(statistics.mean(ms), 4),
+                   "n_accept_mean": round(float(n_acc.float().mean().item()), 4)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+                "d2h_bytes_per_step": int(bo)},
+        "roofline": {"bound": "hbm", "kernel": "verify_sample_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": alg, "traffic": None},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_verify_sample(inp)
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def cpu_baseline_verify_sample(inp, min_seconds: float = 10.0) -> dict:
+    """The oracle's exact sampling verify on this host's cores, whole calls
+    repeated until `min_seconds` of CPU work."""
+    import oracle
+    B, R, _ = inp.target.shape
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify_sample(inp.target, inp.draft, inp.dtype, inp.drafts, inp.hist, inp.params, inp.seed, reps)
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(reps * B * (R - 1) / dt, 4), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{reps} full verify_sample calls (B={B}, N={R - 1}), {dt:.1f} s"}
+
+
 def cpu_baseline(w, min_seconds: float = 10.0) -> dict:
     """The oracle as it stands, timed on this host's cores over a bounded sample:
     whole draft blocks (N steps, B sequences) + greedy verify, repeated until
@@ -377,6 +536,27 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
+    if args.workload == 4:
+        inp = synth.make_verify_sample_inputs()
+        B, R, _ = inp.target.shape
+        for i in range(args.warmup):
+            oracle.verify_sample(inp.target, inp.draft, inp.dtype, inp.drafts, inp.hist, inp.params, inp.seed, i)
+        times = []
+        for i in range(args.steps):
+            t0 = time.perf_counter()
+            oracle.verify_sample(inp.target, inp.draft, inp.dtype, inp.drafts, inp.hist, inp.params, inp.seed, 1000 + i)
+            times.append(time.perf_counter() - t0)
+        tot = sum(times)
+        value = B * (R - 1) * args.steps / tot
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 0,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 2),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                          "data": "synthetic (seeded)", "config": {"workload": synth.WORKLOADS[4], "B": B, "N": R - 1},
+                          "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                                           "kind": "oracle", "sample": f"{args.steps} full verify_sample calls"},
+                          "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return
     w = synth.make_draft_inputs(args.workload)
     vin = synth.make_verify_greedy_inputs(args.workload, B=w.B, N=w.N, V=w.model.vocab)
     for _ in range(args.warmup):
@@ -403,6 +583,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == 4:
+        run_verify_sample(args)
     else:
         run_ours(args)
 
