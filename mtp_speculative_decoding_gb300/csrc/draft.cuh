@@ -34,8 +34,8 @@ constexpr int kAttnStagesTc = 2;   // batched (tensor-core) kernel (three measur
 constexpr int kHeadGroups = 4;
 constexpr int kHeadSlots = 3;
 constexpr int kHeadMaxChunks = 640;
-// LM head on tensor cores (bf16 weights, B >= kTcMinBatch): 128-row tiles of
-// the token table, K steps of 64, kTcStages-deep operand ring
+// Batched projections on tensor cores (bf16 weights, B >= kTcMinBatch):
+// 128-row weight tiles, K steps of 64, a tc_stages-deep operand ring
 constexpr int kTcMinBatch = 8;
 constexpr int kTcTileM = 128;
 constexpr int kTcTileK = 64;
