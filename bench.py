@@ -57,6 +57,18 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The largest x over all ranks of the initialised process group (x itself
+    for one rank): the whole-job time of independent replicas."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------
 # algorithmic bytes (the byte floor: every tensor the step must read, once)
 # ----------------------------------------------------------------------------
@@ -269,11 +281,9 @@ def run_ours(args):
     total_ms = t_start.elapsed_time(t_end)
     draft_ms = [e[0].elapsed_time(e[1]) for e in ev]
     verify_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = max_over_ranks(total_ms, world)
     if world > 1:
         import torch.distributed as dist
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
         dist.barrier()
     ms_per_step = total_ms / args.steps
     value = world * B * N * args.steps / (total_ms / 1e3)
@@ -312,11 +322,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_value = world * B * N * args.steps / (e2e_ms / 1e3)
     if not np.array_equal(h_n.numpy(), vin.planted):
         raise RuntimeError("end-to-end verify disagrees with the planted accept lengths")
@@ -417,11 +423,7 @@ def run_verify_sample(args):
         raise RuntimeError(f"verify_sample status {mtp.last_error(ws)}")
     ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(ms)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world)
     value = world * B * N * args.steps / (total_ms / 1e3)
 
     # end-to-end through the public API with pinned host buffers: the logits,
@@ -456,11 +458,7 @@ def run_verify_sample(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_value = world * B * N * args.steps / (e2e_ms / 1e3)
 
     peak, peak_kind = measured_peaks()
