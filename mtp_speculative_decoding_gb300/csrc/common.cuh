@@ -129,15 +129,8 @@ __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // 2-D tiled tensor copy global -> shared through a tensor map (generic
-// address of a __grid_constant__ parameter); x is the innermost coordinate
-__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, unsigned long long* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_addr(dst)),
-        "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
-        : "memory");
-}
-// tma_load_2d with an L2 cache policy
+// address of a __grid_constant__ parameter) under an L2 cache policy; x is
+// the innermost coordinate
 __device__ __forceinline__ void tma_load_2d_pol(void* dst, const void* tmap, int x, int y, unsigned long long* bar,
                                                 unsigned long long pol) {
     asm volatile(

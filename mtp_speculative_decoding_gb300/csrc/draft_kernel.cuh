@@ -336,21 +336,8 @@ struct HeadEpi {
 // prologues: build one sequence's GEMV input vector
 // ---------------------------------------------------------------------------
 
-// dst[i] = src[i] * rsqrt(mean(src^2) + eps) * g[i]; src may alias dst.
-// All threads of the CTA participate.
-__device__ __forceinline__ void rms_into(const float* src, const float* g, int n, float eps, float* dst, float* red) {
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const float v = src[i];
-        ss = fmaf(v, v, ss);
-    }
-    ss = block_sum(ss, red);
-    const float r = 1.0f / sqrtf(ss / (float)n + eps);
-    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i] * r * __ldg(g + i);
-    __syncthreads();
-}
-
-// rms_into with the gains already staged in shared memory (gs)
+// dst[i] = src[i] * rsqrt(mean(src^2) + eps) * gs[i] with the gains staged in
+// shared memory (gs); src may alias dst.  All threads of the CTA participate.
 __device__ __forceinline__ void rms_into_s(const float* src, const float* gs, int n, float eps, float* dst, float* red) {
     float ss = 0.f;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
