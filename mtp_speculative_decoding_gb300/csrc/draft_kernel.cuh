@@ -18,8 +18,11 @@
 //
 // Norms and residual updates run redundantly in every CTA's phase prologue
 // (each CTA needs the whole input vector of its GEMV anyway), so they cost no
-// barrier.  Weights stream through 16-byte no-L1-allocate loads, one warp per
-// output row; activations are fp32 in shared memory.
+// barrier.  Below eight sequences the weights stream through 16-byte
+// no-L1-allocate loads under an L2 evict-first policy, a warp per output row
+// (at one sequence: two warps per row when rows are few, two rows per warp
+// when rows are short); from eight sequences the projections and the LM head
+// run on the tensor cores (tc_gemm, tc_head).  Activations are fp32.
 #pragma once
 
 #include <cuda_runtime.h>
