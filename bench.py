@@ -1,20 +1,23 @@
 #!/usr/bin/env python3
 """Benchmark of the MTP draft block + verify-accept hot path.
 
-One step = one mtp_draft_block call (N chained draft steps, one persistent
-launch) + one mtp_verify_greedy call on the target's (1+N) x V verify logits,
-for the Gemma-assistant-shaped workload (bf16, d_t 5120, d_a 1024, 4 blocks,
-16 x 256 query heads over 4 KV heads, GeGLU 4096, vocab 262144, B = 1, N = 3,
-8192 cached positions; 3 blocks attend a 1024-window sliding layer, 1 a full
-layer).  Metric: drafted tokens per second = B * N / (draft + verify time).
+One step of a draft workload = one mtp_draft_block call (N chained draft
+steps, one persistent launch) + one mtp_verify_greedy call on the target's
+(1+N) x V verify logits.  Metric: drafted tokens per second = B * N / (draft
++ verify time).  The headline is the Gemma-assistant-shaped workload (bf16,
+d_t 5120, d_a 1024, 4 blocks, 16 x 256 query heads over 4 KV heads, GeGLU
+4096, vocab 262144, B = 1, N = 3, 8192 cached positions; 3 blocks attend a
+1024-window sliding layer, 1 a full layer).  The default run also times the
+same model at B = 16 (N = 4, ragged 2k-32k contexts) and B = 64 (N = 2,
+context 4096), and exact temp > 0 verification alone (mtp_verify_sample,
+B = 32, N = 3, V = 248320; that configuration has no draft block), each
+reported under per_workload with its own roofline fraction, end-to-end
+number and CPU baseline.  `--workload K` times one of them alone.
 
-`--workload 4` times exact temp > 0 verification alone (mtp_verify_sample,
-B = 32, N = 3, V = 248320): that configuration has no draft block.
-
-Prints ONE JSON line.  `--impl reference` times the CPU oracle instead on the
-same workload (a bounded sample per step).  Multi-GPU (torchrun): every rank
-runs an independent replica (the path has no cross-sequence exchange); the
-value is the sum of drafted tokens over the max time across ranks.
+Prints ONE JSON line.  `--impl reference` times the CPU oracle instead (a
+bounded sample per step), with the same config.  Multi-GPU (torchrun): every
+rank runs an independent replica (the path has no cross-sequence exchange);
+the value is the sum of drafted tokens over the max time across ranks.
 """
 from __future__ import annotations
 
@@ -36,18 +39,20 @@ import synth  # noqa: E402
 
 METRIC = "drafted tok/s (MTP draft block + verify) at B=1..64; % of HBM/tensor roofline"
 UNIT = "tok/s"
-WORKLOAD_ID = 1
+HEADLINE = 1
+OTHERS = (2, 3, 4)
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4],
+                    help="time this workload alone (default: the headline plus workloads 2-4)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -67,6 +72,32 @@ def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# workloads and their configs (one description for both arms)
+# ----------------------------------------------------------------------------
+
+L2_FLUSH_BYTES = 256 << 20   # written between timed verify-sample launches (its 111 MB of logits fit in L2)
+
+
+def _common(world: int, flushed: bool) -> dict:
+    return {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": (f"flushed before every timed launch ({L2_FLUSH_BYTES >> 20} MB written)" if flushed
+                   else "inputs larger than L2 (weights streamed every step), no flush")}
+
+
+def draft_config(w, world: int = 1) -> dict:
+    m = w.model
+    return dict({"workload": w.name, "B": w.B, "N": w.N, "vocab": m.vocab, "d_t": m.d_t, "d_a": m.d_a,
+                 "n_blocks": m.n_blocks, "kv_len_max": int(w.kv_len.max()), "kv_len_min": int(w.kv_len.min())},
+                **_common(world, False))
+
+
+def sample_config(inp, world: int = 1) -> dict:
+    B, R, V = inp.target.shape
+    return dict({"workload": synth.WORKLOADS[4], "B": B, "N": R - 1, "vocab": V, "history": int(inp.hist.shape[1]),
+                 "path": "mtp_verify_sample alone (this configuration has no draft block)"}, **_common(world, True))
 
 
 # ----------------------------------------------------------------------------
@@ -108,11 +139,19 @@ def draft_flops_per_launch(w) -> float:
     return float(w.N * (2 * m.params() * w.B + attn))
 
 
+def verify_sample_bytes(inp) -> int:
+    """Algorithmic bytes of one mtp_verify_sample call: one read of the target
+    and draft logits (the history and drafts are a few KB)."""
+    return int(inp.target.nbytes + inp.draft.nbytes)
+
+
 # ----------------------------------------------------------------------------
-# clocks during the timed region
+# clocks during the timed regions
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi samples (200 ms) taken only while a timed region runs:
+    start()/pause() bracket each region, summary() covers them all."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -122,6 +161,7 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.th = None
+        self.failed = False
 
     def start(self):
         try:
@@ -130,17 +170,19 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            self.failed = True
             return
-        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th = threading.Thread(target=self._read, args=(self.proc,), daemon=True)
         self.th.start()
+        time.sleep(0.3)
 
-    def _read(self):
-        for line in self.proc.stdout:
+    def _read(self, proc):
+        for line in proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self) -> dict:
+    def pause(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return
         time.sleep(0.25)
         self.proc.terminate()
         try:
@@ -149,6 +191,12 @@ class ClockSampler:
             self.proc.kill()
         if self.th:
             self.th.join(timeout=2)
+        self.proc = None
+
+    def summary(self) -> dict:
+        self.pause()
+        if self.failed and not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -184,17 +232,19 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes (read + write) per draft-kernel launch from the committed ncu
-    summary, or None when that capture was taken on other kernel sources or
-    another workload."""
-    p = os.path.join(ROOT, "profiles", "draft_kernel_traffic.txt")
+    """DRAM bytes (read + write) per launch of the workload's dominant kernel
+    from the committed ncu record (one line per workload), or None when that
+    capture was taken on other kernel sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
+    src = kernel_source_hash()
     with open(p) as f:
-        kv = dict(t.split("=", 1) for t in f.read().split() if "=" in t)
-    if kv.get("workload") != workload or kv.get("source_hash") != kernel_source_hash():
-        return None
-    return int(kv["dram_bytes_per_launch"])
+        for line in f:
+            kv = dict(t.split("=", 1) for t in line.split() if "=" in t)
+            if kv.get("workload") == workload and kv.get("source_hash") == src:
+                return int(kv["dram_bytes_per_launch"])
+    return None
 
 
 def measured_peaks():
@@ -206,26 +256,32 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
 # ----------------------------------------------------------------------------
 # our implementation
 # ----------------------------------------------------------------------------
 
-def run_ours(args):
+def bench_draft(wid, args, world, clocks, reuse=None):
+    """Draft block + greedy verify of workload wid.  Returns (fields, device
+    draft object for reuse, workload)."""
     import torch
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
     import mtp_speculative_decoding_gb300 as mtp
-    from mtp_speculative_decoding_gb300 import build as mtp_build
     from mtp_speculative_decoding_gb300.device import to_device, upload_draft
-    mtp_build.build()
 
-    w = synth.make_draft_inputs(args.workload)
+    w = synth.make_draft_inputs(wid)
     m = w.model
     B, N, V = w.B, w.N, m.vocab
-    dev = upload_draft(w, extra_ws_for=(B, N, V))
+    dev = upload_draft(w, extra_ws_for=(B, N, V), reuse=reuse)
     ws = dev.ws
     drafts = torch.empty((B, N), dtype=torch.int32, device="cuda")
     h_last = torch.empty((B, m.d_t), dtype=torch.float32, device="cuda")
@@ -235,7 +291,7 @@ def run_ours(args):
     if mtp.last_error(ws) != 0:
         raise RuntimeError(f"draft block status {mtp.last_error(ws)}")
     d_host = drafts.cpu().numpy()
-    vin = synth.make_verify_greedy_inputs(args.workload, B=B, N=N, V=V)
+    vin = synth.make_verify_greedy_inputs(wid, B=B, N=N, V=V)
     logits_np = synth.plant_greedy_logits(
         synth.bf16_bits_to_f32(vin.logits) if vin.dtype == "bf16" else vin.logits, d_host, vin.planted, vin.dtype)
     logits = to_device(logits_np, vin.dtype)
@@ -258,13 +314,11 @@ def run_ours(args):
     # per-kernel events on the launch stream: draft launch and verify launch separately
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(local)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -277,7 +331,7 @@ def run_ours(args):
         c.record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clocks.pause()
     total_ms = t_start.elapsed_time(t_end)
     draft_ms = [e[0].elapsed_time(e[1]) for e in ev]
     verify_ms = [e[1].elapsed_time(e[2]) for e in ev]
@@ -316,82 +370,57 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    clocks.start()
     e0.record(stream)
     for _ in range(args.steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_ms = max_over_ranks(e2e_ms, world)
+    clocks.pause()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_value = world * B * N * args.steps / (e2e_ms / 1e3)
     if not np.array_equal(h_n.numpy(), vin.planted):
         raise RuntimeError("end-to-end verify disagrees with the planted accept lengths")
 
     peak, peak_kind = measured_peaks()
     alg = draft_bytes_per_launch(w)
-    draft_avg_s = statistics.mean(draft_ms) / 1e3
-    achieved = alg / draft_avg_s / 1e9
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if m.dtype == "bf16" else "f32",
-        "data": "synthetic (seeded; random-init weights of the workload's shapes)",
-        "config": {"workload": w.name, "B": B, "N": N, "vocab": V, "d_t": m.d_t, "d_a": m.d_a,
-                   "n_blocks": m.n_blocks, "kv_len": int(w.kv_len.max()),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (weights streamed every step), no flush",
-                   "draft_ms_mean": round(statistics.mean(draft_ms), 4),
-                   "verify_ms_mean": round(statistics.mean(verify_ms), 4)},
+    achieved = alg / (statistics.mean(draft_ms) / 1e3) / 1e9
+    fields = {
+        "value": round(value, 2), "ms_per_step": round(ms_per_step, 4),
+        "config": draft_config(w, world),
+        "breakdown": {"draft_ms_mean": round(statistics.mean(draft_ms), 4),
+                      "verify_ms_mean": round(statistics.mean(verify_ms), 4)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(bi),
                 "d2h_bytes_per_step": int(bo)},
-        "roofline": {"bound": "hbm", "kernel": "draft_kernel", "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": alg,
-                     "traffic": recorded_traffic(w.name)},
+        "roofline": {"bound": "hbm", "kernel": "draft_kernel", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": alg, "traffic": recorded_traffic(w.name)},
         "gpu_launches": 2 * args.steps,
-        "clocks": clk,
+        "dtype": "bf16" if m.dtype == "bf16" else "f32",
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w)
-    if rank == 0:
-        print(json.dumps(result))
+    return fields, dev, w
 
 
-# ----------------------------------------------------------------------------
-# workload 4: exact temp > 0 verification alone (no draft block in this
-# configuration): B = 32 sequences, N = 3 drafts, V = 248320, bf16 logits
-# ----------------------------------------------------------------------------
-
-L2_FLUSH_BYTES = 256 << 20   # written between timed launches: the 111 MB of logits fit in the 129 MB L2
-
-
-def verify_sample_bytes(inp) -> int:
-    """Algorithmic bytes of one mtp_verify_sample call: one read of the target
-    and draft logits (the history and drafts are a few KB)."""
-    return int(inp.target.nbytes + inp.draft.nbytes)
-
-
-def run_verify_sample(args):
+def bench_verify_sample(args, world, clocks):
+    """Exact temp > 0 verification alone (workload 4).  Returns (fields, inputs)."""
     import torch
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
     import mtp_speculative_decoding_gb300 as mtp
-    from mtp_speculative_decoding_gb300 import build as mtp_build
     from mtp_speculative_decoding_gb300.device import to_device
-    mtp_build.build()
 
     inp = synth.make_verify_sample_inputs()
     B, R, V = inp.target.shape
     N = R - 1
     tg, df = to_device(inp.target, inp.dtype), to_device(inp.draft, inp.dtype)
-    dr = torch.from_numpy(np.ascontiguousarray(inp.drafts, dtype=np.int32)).cuda()
     hi = torch.from_numpy(np.ascontiguousarray(inp.hist, dtype=np.int32)).cuda()
     out = torch.empty((B, R), dtype=torch.int32, device="cuda")
     n_acc = torch.empty((B,), dtype=torch.int32, device="cuda")
     ws = mtp.alloc_workspace(mtp.workspace_size(None, B, N, V))
+    # the drafter's tokens: draws from q_i = sample_dist(draft row i), untimed
+    dr = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    mtp.sample_drafts(df, hi, inp.params, inp.seed, inp.offset, dr, ws)
+    torch.cuda.synchronize()
+    if mtp.last_error(ws) != 0:
+        raise RuntimeError(f"sample_drafts status {mtp.last_error(ws)}")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -405,25 +434,22 @@ def run_verify_sample(args):
         raise RuntimeError(f"verify_sample status {mtp.last_error(ws)}")
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(local)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
     for i in range(args.steps):
         flush.fill_(float(i))   # evict the logits from L2
         ev[i][0].record(stream)
         step(1000 + i)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clocks.pause()
     if mtp.last_error(ws) != 0:
         raise RuntimeError(f"verify_sample status {mtp.last_error(ws)}")
     ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(ms)
-    total_ms = max_over_ranks(total_ms, world)
+    total_ms = max_over_ranks(sum(ms), world)
     value = world * B * N * args.steps / (total_ms / 1e3)
 
     # end-to-end through the public API with pinned host buffers: the logits,
@@ -452,81 +478,157 @@ def run_verify_sample(args):
         e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
     e0.record(stream)
     for i in range(args.steps):
         e2e_step(2000 + i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_ms = max_over_ranks(e2e_ms, world)
+    clocks.pause()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_value = world * B * N * args.steps / (e2e_ms / 1e3)
 
     peak, peak_kind = measured_peaks()
     alg = verify_sample_bytes(inp)
     achieved = alg / (statistics.mean(ms) / 1e3) / 1e9
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype,
-        "data": "synthetic (seeded; target logits N(0, 2^2), draft logits correlated at 0.8)",
-        "config": {"workload": synth.WORKLOADS[4], "B": B, "N": N, "vocab": V, "history": int(inp.hist.shape[1]),
-                   "path": "mtp_verify_sample alone (this configuration has no draft block)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"flushed before every timed launch ({L2_FLUSH_BYTES >> 20} MB written)",
-                   "verify_ms_mean": round(statistics.mean(ms), 4),
-                   "n_accept_mean": round(float(n_acc.float().mean().item()), 4)},
+    fields = {
+        "value": round(value, 2), "ms_per_step": round(total_ms / args.steps, 4),
+        "config": sample_config(inp, world),
+        "breakdown": {"verify_ms_mean": round(statistics.mean(ms), 4),
+                      "n_accept_mean": round(float(n_acc.float().mean().item()), 4)},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(bi),
                 "d2h_bytes_per_step": int(bo)},
-        "roofline": {"bound": "hbm", "kernel": "verify_sample_kernel", "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": alg, "traffic": None},
+        "roofline": {"bound": "hbm", "kernel": "sample_kernel", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": alg, "traffic": recorded_traffic(synth.WORKLOADS[4])},
         "gpu_launches": args.steps,
-        "clocks": clk,
+        "dtype": inp.dtype,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline_verify_sample(inp)
+    return fields, inp
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample of the workload
+# ----------------------------------------------------------------------------
+
+def _timed_units(run_unit, min_seconds):
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run_unit(reps)
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    return reps, time.perf_counter() - t0
+
+
+def cpu_baseline_draft(w, min_seconds: float = 8.0) -> dict:
+    """Whole draft blocks of single sequences (cycling through the batch, N
+    steps each) + their greedy verify rows, on all host cores until
+    min_seconds of work, then one sequence on one core."""
+    import oracle
+    vin = synth.make_verify_greedy_inputs(0 if w.model.dtype == "f32" else 1, B=1, N=w.N, V=w.model.vocab)
+
+    def unit(r):
+        oracle.draft_block(w, seqs=[r % w.B], want_logits=False)
+        oracle.verify_greedy(vin.logits, vin.dtype, vin.drafts)
+
+    cores = oracle.num_threads()
+    reps, dt = _timed_units(unit, min_seconds)
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        unit(0)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(cores)
+    return {"value": round(reps * w.N / dt, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} single-sequence draft blocks (N={w.N}) + greedy verify, cycling over the "
+                      f"batch's sequences, {dt:.1f} s",
+            "single_thread": {"value": round(w.N / dt1, 4), "cores": 1, "sample": "one sequence's draft block"},
+            "cpu_model": cpu_model()}
+
+
+def cpu_baseline_verify_sample(inp, min_seconds: float = 8.0) -> dict:
+    """The oracle's exact sampling verify, whole calls until min_seconds (the
+    drafter's draws, by the oracle, untimed), then one call on one core."""
+    import oracle
+    inp.drafts, _ = oracle.sample_drafts(inp.draft, inp.dtype, inp.hist, inp.params, inp.seed, inp.offset)
+    B, R, _ = inp.target.shape
+
+    def unit(r):
+        oracle.verify_sample(inp.target, inp.draft, inp.dtype, inp.drafts, inp.hist, inp.params, inp.seed, r)
+
+    cores = oracle.num_threads()
+    reps, dt = _timed_units(unit, min_seconds)
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        unit(0)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(cores)
+    return {"value": round(reps * B * (R - 1) / dt, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} full verify_sample calls (B={B}, N={R - 1}), {dt:.1f} s",
+            "single_thread": {"value": round(B * (R - 1) / dt1, 4), "cores": 1, "sample": "one full call"},
+            "cpu_model": cpu_model()}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from mtp_speculative_decoding_gb300 import build as mtp_build
+    mtp_build.build()
+    clocks = ClockSampler(local)
+    want_cpu = rank == 0 and not args.no_cpu_baseline
+
+    order = [args.workload] if args.workload is not None else [HEADLINE] + list(OTHERS)
+    results = {}
+    reuse = None
+    for wid in order:
+        if wid == 4:
+            fields, inp = bench_verify_sample(args, world, clocks)
+            if want_cpu:
+                fields["cpu_baseline"] = cpu_baseline_verify_sample(inp)
+            del inp
+        else:
+            fields, dev, w = bench_draft(wid, args, world, clocks, reuse=reuse)
+            if want_cpu:
+                fields["cpu_baseline"] = cpu_baseline_draft(w)
+            reuse = dev if w.model.dtype == "bf16" else None
+            del w
+        results[wid] = fields
+        torch.cuda.synchronize()
+    del reuse
+    torch.cuda.empty_cache()
+
+    head = results[order[0]]
+    result = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+        "data": "synthetic (seeded; random-init weights of the workloads' shapes)",
+        "config": head["config"], "e2e": head["e2e"], "roofline": head["roofline"],
+        "breakdown": head["breakdown"],
+        "gpu_launches": sum(r["gpu_launches"] for r in results.values()),
+        "clocks": clocks.summary(),
+    }
+    if len(order) > 1:   # the other workloads, each with the same fields as the headline
+        result["per_workload"] = {results[wid]["config"]["workload"]: {
+            k: results[wid][k] for k in ("value", "ms_per_step", "config", "breakdown", "e2e", "roofline",
+                                         "cpu_baseline", "gpu_launches") if k in results[wid]}
+            for wid in order[1:]}
+    if "cpu_baseline" in head:
+        result["cpu_baseline"] = head["cpu_baseline"]
     if rank == 0:
         print(json.dumps(result))
 
 
-def cpu_baseline_verify_sample(inp, min_seconds: float = 10.0) -> dict:
-    """The oracle's exact sampling verify on this host's cores, whole calls
-    repeated until `min_seconds` of CPU work."""
-    import oracle
-    B, R, _ = inp.target.shape
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.verify_sample(inp.target, inp.draft, inp.dtype, inp.drafts, inp.hist, inp.params, inp.seed, reps)
-        reps += 1
-        if time.perf_counter() - t0 >= min_seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(reps * B * (R - 1) / dt, 4), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": f"{reps} full verify_sample calls (B={B}, N={R - 1}), {dt:.1f} s"}
-
-
-def cpu_baseline(w, min_seconds: float = 10.0) -> dict:
-    """The oracle as it stands, timed on this host's cores over a bounded sample:
-    whole draft blocks (N steps, B sequences) + greedy verify, repeated until
-    `min_seconds` of CPU work."""
-    import oracle
-    vin = synth.make_verify_greedy_inputs(WORKLOAD_ID if w.name == synth.WORKLOADS[1] else 0,
-                                          B=w.B, N=w.N, V=w.model.vocab)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.draft_block(w, want_logits=False)
-        oracle.verify_greedy(vin.logits, vin.dtype, vin.drafts)
-        reps += 1
-        if time.perf_counter() - t0 >= min_seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(reps * w.B * w.N / dt, 4), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{reps} full draft blocks (B={w.B}, N={w.N}) + greedy verify, {dt:.1f} s"}
-
-
 # ----------------------------------------------------------------------------
-# reference arm: the oracle on the host cores
+# reference arm: the oracle on the host cores, same config as ours
 # ----------------------------------------------------------------------------
 
 def run_reference(args):
@@ -534,8 +636,10 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    if args.workload == 4:
+    wid = HEADLINE if args.workload is None else args.workload
+    if wid == 4:
         inp = synth.make_verify_sample_inputs()
+        inp.drafts, _ = oracle.sample_drafts(inp.draft, inp.dtype, inp.hist, inp.params, inp.seed, inp.offset)
         B, R, _ = inp.target.shape
         for i in range(args.warmup):
             oracle.verify_sample(inp.target, inp.draft, inp.dtype, inp.drafts, inp.hist, inp.params, inp.seed, i)
@@ -544,35 +648,34 @@ def run_reference(args):
             t0 = time.perf_counter()
             oracle.verify_sample(inp.target, inp.draft, inp.dtype, inp.drafts, inp.hist, inp.params, inp.seed, 1000 + i)
             times.append(time.perf_counter() - t0)
-        tot = sum(times)
-        value = B * (R - 1) * args.steps / tot
-        print(json.dumps({"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 0,
-                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 2),
-                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-                          "data": "synthetic (seeded)", "config": {"workload": synth.WORKLOADS[4], "B": B, "N": R - 1},
-                          "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
-                                           "kind": "oracle", "sample": f"{args.steps} full verify_sample calls"},
-                          "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
-                                  "d2h_bytes_per_step": 0}}))
-        return
-    w = synth.make_draft_inputs(args.workload)
-    vin = synth.make_verify_greedy_inputs(args.workload, B=w.B, N=w.N, V=w.model.vocab)
-    for _ in range(args.warmup):
-        oracle.draft_block(w, want_logits=False)
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oracle.draft_block(w, want_logits=False)
-        oracle.verify_greedy(vin.logits, vin.dtype, vin.drafts)
-        times.append(time.perf_counter() - t0)
+        units = B * (R - 1) * args.steps
+        config = sample_config(inp, world)
+        sample = f"{args.steps} full verify_sample calls"
+        dtype = "f32"
+    else:
+        w = synth.make_draft_inputs(wid)
+        vin = synth.make_verify_greedy_inputs(0 if w.model.dtype == "f32" else 1, B=1, N=w.N, V=w.model.vocab)
+        # each step: one sequence's draft block (cycling over the batch) + its verify rows
+        for r in range(args.warmup):
+            oracle.draft_block(w, seqs=[r % w.B], want_logits=False)
+        times = []
+        for r in range(args.steps):
+            t0 = time.perf_counter()
+            oracle.draft_block(w, seqs=[r % w.B], want_logits=False)
+            oracle.verify_greedy(vin.logits, vin.dtype, vin.drafts)
+            times.append(time.perf_counter() - t0)
+        units = w.N * args.steps
+        config = draft_config(w, world)
+        sample = f"{args.steps} single-sequence draft blocks + greedy verify, cycling over the batch"
+        dtype = "f64"
     tot = sum(times)
-    value = w.B * w.N * args.steps / tot
+    value = units / tot
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / args.steps, 2),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": {"workload": w.name, "B": w.B, "N": w.N},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic (seeded; random-init weights of the workloads' shapes)", "config": config,
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
-                             "kind": "oracle", "sample": f"{args.steps} full draft blocks + greedy verify"},
+                             "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -581,8 +684,6 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload == 4:
-        run_verify_sample(args)
     else:
         run_ours(args)
 

@@ -1,7 +1,7 @@
 /*
  * mtp.h -- C ABI of the GB300 MTP speculative-decoding hot path.
  *
- * Three operations, all asynchronous on a caller-supplied CUDA stream:
+ * Four operations, all asynchronous on a caller-supplied CUDA stream:
  *
  *   mtp_draft_block    N chained draft steps of an MTP assistant head that
  *                      cross-attends into the target's KV cache, in ONE
@@ -10,6 +10,8 @@
  *   mtp_verify_greedy  longest greedy-matching prefix + bonus token from the
  *                      target's (1+N) x V verify logits.
  *   mtp_verify_sample  exact speculative sampling at temp > 0.
+ *   mtp_sample_drafts  the draws of a sampling drafter from given draft
+ *                      logits (the q the sampling verifier checks against).
  *
  * Definitions are those of the pages this library implements:
  *   [G4] "Gemma 4 MTP -- Multi-Token Prediction speculative decoding":
@@ -67,7 +69,8 @@ enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 };
 
 #define MTP_MAX_BLOCKS 8
 #define MTP_MAX_VIEWS 4
-#define MTP_MAX_BATCH 64
+#define MTP_MAX_BATCH 64            /* sequences of one mtp_draft_block call */
+#define MTP_MAX_VERIFY_BATCH 65536  /* sequences of one verify or draw call */
 
 /* Sizes and scalars of the assistant head ([G4] sec. 3-4).
  *   d_t        backbone (target) width: token embedding, h_prev, LM head input
@@ -140,9 +143,10 @@ typedef struct mtp_sample_params {
     int32_t top_k;
 } mtp_sample_params;
 
-/* Workspace bytes needed by any of the three operations for these sizes.
- * cfg may be NULL when only the verify calls will use the workspace.  Returns
- * 0 for invalid sizes. */
+/* Workspace bytes needed by any of the operations for these sizes (B
+ * sequences, N drafts, vocabulary V).  cfg may be NULL when only the verify
+ * and draw calls will use the workspace (then B <= MTP_MAX_VERIFY_BATCH,
+ * else B <= MTP_MAX_BATCH).  Returns 0 for invalid sizes. */
 size_t mtp_workspace_size(const mtp_config *cfg, int B, int N, int V);
 
 /* N chained draft steps for B sequences ([G4] sec. 4-5, [NX], [FN]).
@@ -175,6 +179,15 @@ size_t mtp_workspace_size(const mtp_config *cfg, int B, int N, int V);
  *   out_drafts [B, N] int32
  *   out_h_last [B, d_t] fp32, or NULL: h after the last step
  *   out_logits [B, N, vocab] fp32, or NULL: every step's logits (diagnostic)
+ *   out_conf [B, N] fp32, or NULL: each step's confidence, the softmax
+ *                        probability of its largest logit, 1 / sum_v
+ *                        exp(z_v - max z) over the step's logits (after the
+ *                        softcap, NaN left out) -- the draft loop's
+ *                        confidence that [NX] "Stopping early when the head
+ *                        is unsure" compares with p_min.  The caller trims a
+ *                        row's drafts at the first step below its p_min
+ *                        before verifying; the drafts themselves do not
+ *                        depend on it.
  * B <= MTP_MAX_BATCH, 1 <= N <= 16.  One cooperative launch (plus a 256-byte
  * workspace memset); no host round-trip between steps. */
 int mtp_draft_block(const mtp_config *cfg, const mtp_weights *w,
@@ -184,9 +197,9 @@ int mtp_draft_block(const mtp_config *cfg, const mtp_weights *w,
                     const mtp_sample_params *sp, uint64_t seed, uint64_t offset,
                     const int32_t *hist, int H,
                     int32_t *out_drafts, float *out_h_last, float *out_logits,
-                    void *ws, size_t ws_bytes, mtp_stream_t stream);
+                    float *out_conf, void *ws, size_t ws_bytes, mtp_stream_t stream);
 
-/* Greedy verify ([NX] How it is wired).  logits [B, 1+N, V] in ldtype (row i
+/* Greedy verify ([NX] How it is wired).  B <= MTP_MAX_VERIFY_BATCH.  logits [B, 1+N, V] in ldtype (row i
  * is the target's distribution after consuming the last token and drafts
  * 0..i-1); t_i = argmax of row i (lowest index on ties, NaN never wins, an
  * all-NaN row gives 0).  n_accept[b] = the largest k <= N with
@@ -197,7 +210,8 @@ int mtp_verify_greedy(const void *logits, int ldtype, int B, int N, int V,
                       const int32_t *drafts, int32_t *out_tokens, int32_t *out_n_accept,
                       void *ws, size_t ws_bytes, mtp_stream_t stream);
 
-/* Exact speculative sampling ([SP] item 4).  For row i < N of sequence b:
+/* Exact speculative sampling ([SP] item 4), B <= MTP_MAX_VERIFY_BATCH
+ * sequences.  For row i < N of sequence b:
  * p_i = sample_dist(target row i), q_i = sample_dist(draft row i), both with
  * penalty set hist[b] u {drafts[b, 0..i-1]}; x = drafts[b, i] is accepted iff
  * u < p_i(x) / q_i(x) (u of counter (b, 4i + 1, ...)).  At the first
@@ -210,13 +224,33 @@ int mtp_verify_greedy(const void *logits, int ldtype, int B, int N, int V,
  *   tgt_logits [B, 1+N, V], dft_logits [B, N, V] in ldtype; drafts [B, N];
  *   hist [B, H] int32 (newest last, entries < 0 ignored; NULL when H == 0);
  *   sp host pointer (temp > 0, top_k == 0); out_tokens [B, 1+N] (-1 padded);
- *   out_n_accept [B].  A row whose min-p set exceeds 4096 candidates sets
- *   MTP_ERR_CAPACITY in the status word. */
+ *   out_n_accept [B].  sample_dist's weights are exp(l - lmax) rounded once
+ *   to fp32 (the exponential in fp64); every other step feeding a decision
+ *   is IEEE fp32 in the order written above, sums sequential in (w desc,
+ *   id asc) order.  A row whose min-p set exceeds 4096 candidates sets
+ *   MTP_ERR_CAPACITY in the status word.  One launch (plus a memset of the
+ *   workspace's counters); one pass over the logits. */
 int mtp_verify_sample(const void *tgt_logits, const void *dft_logits, int ldtype,
                       int B, int N, int V, const int32_t *drafts,
                       const int32_t *hist, int H, const mtp_sample_params *sp,
                       uint64_t seed, uint64_t offset,
                       int32_t *out_tokens, int32_t *out_n_accept,
+                      void *ws, size_t ws_bytes, mtp_stream_t stream);
+
+/* Draws of a sampling drafter ([SP] item 4: the token drafted at window
+ * position i is a draw from q_i = sample_dist(draft row i)).  For every
+ * sequence b and i = 0..N-1 in order: q_i = sample_dist(dft_logits[b, i]) with
+ * penalty set hist[b] u {out_drafts[b, 0..i-1]}, and out_drafts[b, i] = the
+ * inverse-CDF pick of q_i with the uniform of counter (b, 4i + 0, offset lo,
+ * offset hi), key (seed lo, seed hi) -- the same draw mtp_draft_block makes
+ * at temp > 0, so mtp_verify_sample can then check these drafts exactly.
+ *   dft_logits [B, N, V] in ldtype; hist [B, H] int32 (NULL when H == 0);
+ *   sp host pointer (as for mtp_verify_sample); out_drafts [B, N] int32.
+ * 1 <= N <= 16, B <= MTP_MAX_VERIFY_BATCH.  N launches (window position i
+ * depends on the draws before it) plus one workspace memset. */
+int mtp_sample_drafts(const void *dft_logits, int ldtype, int B, int N, int V,
+                      const int32_t *hist, int H, const mtp_sample_params *sp,
+                      uint64_t seed, uint64_t offset, int32_t *out_drafts,
                       void *ws, size_t ws_bytes, mtp_stream_t stream);
 
 /* Greedy verify without a workspace.  The pages have no counterpart of this
@@ -232,7 +266,9 @@ int mtp_verify_sample(const void *tgt_logits, const void *dft_logits, int ldtype
  * address (with that device current); make that first call before any stream
  * capture.  All calls share the one array and every call clears it first, so
  * calls that may overlap on the GPU (different streams, or several host
- * threads) race and must be serialized by the caller. */
+ * threads) race and must be serialized by the caller.  The looked-up address
+ * is kept for the life of the process: do not use this call on a device after
+ * cudaDeviceReset() in the same process. */
 int mtp_verify_greedy_noalloc(const void *logits, int ldtype, int B, int N, int V,
                               const int32_t *drafts, int32_t *out_tokens, int32_t *out_n_accept,
                               mtp_stream_t stream);

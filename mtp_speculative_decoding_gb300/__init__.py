@@ -27,10 +27,12 @@ MTP_DTYPE_BF16 = 1
 MTP_MAX_BLOCKS = 8
 MTP_MAX_VIEWS = 4
 MTP_MAX_BATCH = 64
+MTP_MAX_VERIFY_BATCH = 65536
 
 # every entry point include/mtp.h declares
 EXPORTS = ("mtp_workspace_size", "mtp_draft_block", "mtp_verify_greedy", "mtp_verify_sample",
-           "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout", "mtp_verify_greedy_noalloc")
+           "mtp_sample_drafts", "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout",
+           "mtp_verify_greedy_noalloc")
 
 
 class MTPError(RuntimeError):
@@ -85,7 +87,8 @@ def lib():
             P, I, Z = C.c_void_p, C.c_int, C.c_size_t
             L.mtp_workspace_size.argtypes = [P, I, I, I]
             L.mtp_workspace_size.restype = Z
-            L.mtp_draft_block.argtypes = [P, P, P, I, P, I, I, P, P, P, C.c_uint64, C.c_uint64, P, I, P, P, P, P, Z, P]
+            L.mtp_draft_block.argtypes = [P, P, P, I, P, I, I, P, P, P, C.c_uint64, C.c_uint64, P, I, P, P, P, P, P, Z,
+                                          P]
             L.mtp_draft_block.restype = I
             L.mtp_verify_greedy.argtypes = [P, I, I, I, I, P, P, P, P, Z, P]
             L.mtp_verify_greedy.restype = I
@@ -97,6 +100,8 @@ def lib():
             L.mtp_strerror.restype = C.c_char_p
             L.mtp_debug_barrier_timeout.argtypes = [P, Z, I, P]
             L.mtp_debug_barrier_timeout.restype = I
+            L.mtp_sample_drafts.argtypes = [P, I, I, I, I, P, I, P, C.c_uint64, C.c_uint64, P, P, Z, P]
+            L.mtp_sample_drafts.restype = I
             L.mtp_verify_greedy_noalloc.argtypes = [P, I, I, I, I, P, P, P, P]
             L.mtp_verify_greedy_noalloc.restype = I
             _lib = L
@@ -199,9 +204,10 @@ def make_view(k, v, cap: int, window: int, rope_theta: float) -> KVView:
 
 def draft_block(cfg: Config, weights: Weights, views, kv_len, last_tok, h_prev, out_drafts, ws,
                 out_h_last=None, out_logits=None, sample=None, seed: int = 0, offset: int = 0, hist=None,
-                stream=None) -> None:
-    """Launch mtp_draft_block on the current stream (asynchronous)."""
-    _require_cuda(kv_len, last_tok, h_prev, out_drafts, ws, out_h_last, out_logits, hist)
+                stream=None, out_conf=None) -> None:
+    """Launch mtp_draft_block on the current stream (asynchronous).  out_conf
+    [B, N] fp32 (optional) receives each step's top-1 softmax probability."""
+    _require_cuda(kv_len, last_tok, h_prev, out_drafts, ws, out_h_last, out_logits, hist, out_conf)
     B, N = out_drafts.shape
     arr = (KVView * len(views))(*views)
     sp = SampleParams(*sample) if sample is not None else None
@@ -209,7 +215,7 @@ def draft_block(cfg: Config, weights: Weights, views, kv_len, last_tok, h_prev, 
     rc = lib().mtp_draft_block(C.byref(cfg), C.byref(weights), arr, len(views), _ptr(kv_len), B, N,
                                _ptr(last_tok), _ptr(h_prev), C.byref(sp) if sp is not None else None,
                                seed, offset, _ptr(hist), H, _ptr(out_drafts), _ptr(out_h_last),
-                               _ptr(out_logits), _ptr(ws), ws.numel(), _stream(stream))
+                               _ptr(out_logits), _ptr(out_conf), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "mtp_draft_block")
 
 
@@ -242,15 +248,30 @@ def verify_sample(tgt_logits, dft_logits, drafts, hist, params, seed: int, offse
     """params: (temp, top_p, min_p, rep_penalty, presence_penalty, top_k) or an object with those fields."""
     _require_cuda(tgt_logits, dft_logits, drafts, hist, out_tokens, out_n_accept, ws)
     B, R, V = tgt_logits.shape
-    if hasattr(params, "temp"):
-        params = (params.temp, params.top_p, params.min_p, params.rep_penalty,
-                  getattr(params, "presence_penalty", 0.0), getattr(params, "top_k", 0))
-    sp = SampleParams(*params)
+    sp = _sample_params(params)
     H = 0 if hist is None else int(hist.shape[1])
     rc = lib().mtp_verify_sample(_ptr(tgt_logits), _ptr(dft_logits), _dtype_code(tgt_logits), B, R - 1, V,
                                  _ptr(drafts), _ptr(hist), H, C.byref(sp), seed, offset, _ptr(out_tokens),
                                  _ptr(out_n_accept), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "mtp_verify_sample")
+
+
+def _sample_params(params) -> SampleParams:
+    if hasattr(params, "temp"):
+        params = (params.temp, params.top_p, params.min_p, params.rep_penalty,
+                  getattr(params, "presence_penalty", 0.0), getattr(params, "top_k", 0))
+    return SampleParams(*params)
+
+
+def sample_drafts(dft_logits, hist, params, seed: int, offset: int, out_drafts, ws, stream=None) -> None:
+    """Draws of a sampling drafter: out_drafts[b, i] ~ sample_dist(dft_logits[b, i]) (mtp_sample_drafts)."""
+    _require_cuda(dft_logits, hist, out_drafts, ws)
+    B, N, V = dft_logits.shape
+    sp = _sample_params(params)
+    H = 0 if hist is None else int(hist.shape[1])
+    rc = lib().mtp_sample_drafts(_ptr(dft_logits), _dtype_code(dft_logits), B, N, V, _ptr(hist), H, C.byref(sp),
+                                 seed, offset, _ptr(out_drafts), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "mtp_sample_drafts")
 
 
 def last_error(ws, stream=None) -> int:

@@ -18,7 +18,14 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build", platform.machine())
 LIB = os.path.join(BUILD, "libmtp.so")
 
-SOURCES = ["api.cu", "verify.cu", "draft_bf16.cu", "draft_bf16_tc.cu", "draft_f32.cu", "noalloc.cu"]
+# (object name, source, extra defines): the draft kernel's variants are one
+# source compiled once per (weight type, head dimension, tensor-core paths)
+UNITS = [("api", "api.cu", []), ("verify", "verify.cu", []), ("noalloc", "noalloc.cu", []),
+         ("draft_dispatch", "draft_dispatch.cu", [])]
+for _hd in (32, 64, 128, 256, 512):
+    for _name, _bf, _tc in (("f32", 0, 0), ("bf16_cc", 1, 0), ("bf16_tc", 1, 1)):
+        UNITS.append((f"draft_{_name}_{_hd}", "draft_inst.cu",
+                      [f"-DMTP_WT_BF16={_bf}", f"-DMTP_HD={_hd}", f"-DMTP_TC={_tc}"]))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -47,12 +54,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     jobs = []
-    for s in SOURCES:
+    for name, s, defs in UNITS:
         src = os.path.join(CSRC, s)
-        obj = os.path.join(BUILD, s.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, name + ".o")
         if force or _stale(obj, src):
-            cmd = [nvcc] + _flags() + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", src, "-o", obj]
-            jobs.append((s, cmd))
+            cmd = [nvcc] + _flags() + defs + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", src, "-o", obj]
+            jobs.append((name, cmd))
     if jobs:
         def run(job):
             name, cmd = job
@@ -60,11 +67,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed on {name}:\n{r.stderr}")
             return name, r.stderr
-        with cf.ThreadPoolExecutor(max(1, len(jobs))) as ex:
+        with cf.ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
             for name, err in ex.map(run, jobs):
                 if verbose and err:
                     print(f"--- {name}\n{err}")
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(BUILD, name + ".o") for name, _, _ in UNITS]
     if force or jobs or not os.path.exists(LIB):
         cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", LIB + ".tmp"] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -80,9 +80,13 @@ int draft_grid() {
 }
 
 struct DraftLayout {
-    size_t att_cnt, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ZB, SROW, SCNT, SNK, SWK, SID, SW, ACT, end;
+    size_t att_cnt, SROW, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, CONF, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ZB, SBUF, ACT, end;
     int kmax;
 };
+
+// survivor capacity of a sampled row and kept-set capacity, for V tokens
+int sample_rcap(long long V) { return (int)(V < kRowBufCap ? ((V + 7) & ~7LL) : kRowBufCap); }
+int sample_ccap(long long V) { return (int)(V < kCandCap ? ((V + 7) & ~7LL) : kCandCap); }
 
 int draft_kmax(const mtp_config* c) {
     int k = 2 * c->d_t;
@@ -100,6 +104,7 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     const int grp = c->n_q_heads / c->n_kv_heads;
     L.kmax = draft_kmax(c);
     L.att_cnt = off; off = al256(off + (size_t)B * c->n_kv_heads * sizeof(unsigned int));
+    L.SROW = off;    off = al256(off + 4 * (size_t)B * sizeof(unsigned int));   // zeroed with the header
     L.amax = off;    off = al256(off + (size_t)N * B * sizeof(unsigned long long));
     L.XB = off;      off = al256(off + (size_t)B * c->d_a * f);
     L.XM = off;      off = al256(off + (size_t)B * c->d_a * f);
@@ -111,6 +116,7 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     L.HN = off;      off = al256(off + (size_t)B * c->d_t * f);
     const size_t items = 2 * (size_t)kMaxGrid + (size_t)B * c->n_kv_heads;
     L.PART = off;    off = al256(off + items * attn_psz(grp, c->head_dim) * f);
+    L.CONF = off;    off = al256(off + (size_t)kMaxGrid * B * 2 * f);
     L.ROPE = off;    off = al256(off + (size_t)MTP_MAX_VIEWS * (c->head_dim / 2) * sizeof(double));
     L.ROPEQ = off;   off = al256(off + (size_t)B * MTP_MAX_VIEWS * (c->head_dim / 2) * 2 * f);
     // tensor-core operands: K blocks of 64 columns x (kTcHeadM rows for the
@@ -125,12 +131,7 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     L.PB = off;      off = al256(off + (tcp ? tc_plan(c, B, draft_grid()).pb_floats * f : 0));
     // sampled drafting: the step's logits and the sampler's per-row state
     L.ZB = off;      off = al256(off + (size_t)B * c->vocab * f);
-    L.SROW = off;    off = al256(off + (size_t)B * sizeof(unsigned long long));
-    L.SCNT = off;    off = al256(off + (size_t)B * sizeof(unsigned int));
-    L.SNK = off;     off = al256(off + (size_t)B * sizeof(int32_t));
-    L.SWK = off;     off = al256(off + (size_t)B * f);
-    L.SID = off;     off = al256(off + (size_t)B * kCandCap * sizeof(int32_t));
-    L.SW = off;      off = al256(off + (size_t)B * kCandCap * f);
+    L.SBUF = off;    off = al256(off + (size_t)B * sample_rcap(c->vocab) * sizeof(int2));
     L.ACT = off;     off = al256(off + (size_t)B * L.kmax * f);
     L.end = off;
     return L;
@@ -174,23 +175,27 @@ GreedyLayout greedy_layout(int B, int N) {
     return L;
 }
 
-struct SampleLayout { size_t rowmax, cnt, zero_end, nkeep, wkeep, id, w, resid, end; };
-SampleLayout sample_layout(int B, int N) {
+// Sampler workspace: the per-row state (4 x rows words) and the
+// per-sequence counters, zeroed before a launch, then the survivor buffers
+// and (verification) the kept sets.
+struct SampleLayout { size_t row, seq, zero_end, buf, nkeep, wkeep, id, w, end; };
+SampleLayout sample_layout(long long rows, int B, long long V, bool verify) {
     SampleLayout L;
-    const size_t rows = (size_t)B * (N + 1) + (size_t)B * N;
     size_t off = sizeof(WsHeader);
-    L.rowmax = off; off += rows * sizeof(unsigned long long);
-    L.cnt = off;    off += rows * sizeof(unsigned int);
+    L.row = off;   off += 4 * (size_t)rows * sizeof(unsigned int);
+    L.seq = off;   off += (size_t)B * sizeof(unsigned int);
     L.zero_end = off;
     off = al256(off);
-    L.nkeep = off;  off = al256(off + rows * sizeof(int32_t));
-    L.wkeep = off;  off = al256(off + rows * sizeof(float));
-    L.id = off;     off = al256(off + rows * kCandCap * sizeof(int32_t));
-    L.w = off;      off = al256(off + rows * kCandCap * sizeof(float));
-    L.resid = off;  off = al256(off + (size_t)B * kCandCap * sizeof(float));
+    L.buf = off;   off = al256(off + (size_t)rows * sample_rcap(V) * sizeof(int2));
+    const size_t kr = verify ? (size_t)rows : 0, cc = verify ? (size_t)sample_ccap(V) : 0;
+    L.nkeep = off; off = al256(off + kr * sizeof(int32_t));
+    L.wkeep = off; off = al256(off + kr * sizeof(float));
+    L.id = off;    off = al256(off + kr * cc * sizeof(int32_t));
+    L.w = off;     off = al256(off + kr * cc * sizeof(float));
     L.end = off;
     return L;
 }
+long long verify_rows(int B, int N) { return (long long)B * (N + 1) + (long long)B * N; }
 
 // residual scratch plus staged activations of the GEMV phases
 size_t draft_smem_act(const mtp_config* c, int B, int act_smem) {
@@ -240,14 +245,62 @@ int check_sample_params(const mtp_sample_params* sp) {
     return MTP_OK;
 }
 
+// the sampler's job for either entry point (mode, rows and outputs set by the caller)
+SampleJob sample_job(const void* base0, const void* base1, int ldtype, int B, int N, int V, const int32_t* drafts,
+                     const int32_t* hist, int H, const mtp_sample_params* sp, uint64_t seed, uint64_t offset,
+                     char* ws, const SampleLayout& L, long long rows, int sms) {
+    SampleJob j;
+    memset(&j, 0, sizeof j);
+    j.base0 = base0;
+    j.base1 = base1;
+    j.f32 = ldtype == MTP_DTYPE_F32;
+    j.B = B;
+    j.N = N;
+    j.V = V;
+    j.drafts = drafts;
+    j.drafts_ld = N;
+    j.hist = hist;
+    j.H = H;
+    j.hist_ld = H;
+    j.temp = sp->temp; j.top_p = sp->top_p; j.min_p = sp->min_p; j.rep = sp->rep_penalty;
+    j.pres = sp->presence_penalty;
+    j.seed = seed;
+    j.offset = offset;
+    j.hdr = reinterpret_cast<WsHeader*>(ws);
+    unsigned int* row = reinterpret_cast<unsigned int*>(ws + L.row);
+    j.row_max = row;
+    j.row_cnt = row + rows;
+    j.row_ovf = row + 2 * rows;
+    j.row_done = row + 3 * rows;
+    j.seq_done = reinterpret_cast<unsigned int*>(ws + L.seq);
+    j.row_buf = reinterpret_cast<int2*>(ws + L.buf);
+    j.rcap = sample_rcap(V);
+    j.keep_id = reinterpret_cast<int32_t*>(ws + L.id);
+    j.keep_w = reinterpret_cast<float*>(ws + L.w);
+    j.ccap = sample_ccap(V);
+    j.n_keep = reinterpret_cast<int32_t*>(ws + L.nkeep);
+    j.w_keep = reinterpret_cast<float*>(ws + L.wkeep);
+    const int per_sm = sample_blocks_per_sm();
+    sample_piece_plan(V, rows, (per_sm > 0 ? per_sm : 1) * sms, &j.ppr, &j.piece_len);
+    return j;
+}
+
+int check_logits(const void* a, const void* b, int ldtype) {
+    if (ldtype != MTP_DTYPE_F32 && ldtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED;
+    const uintptr_t am = ldtype == MTP_DTYPE_BF16 ? 1 : 3;
+    if ((reinterpret_cast<uintptr_t>(a) & am) || (b && (reinterpret_cast<uintptr_t>(b) & am))) return MTP_ERR_ARG;
+    return MTP_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t mtp_workspace_size(const mtp_config* cfg, int B, int N, int V) {
-    if (B <= 0 || B > MTP_MAX_BATCH || N < 0 || N > 16 || V <= 0) return 0;
+    if (B <= 0 || B > MTP_MAX_VERIFY_BATCH || N < 0 || N > 16 || V <= 0) return 0;
+    if (cfg && B > MTP_MAX_BATCH) return 0;
     size_t need = al256(greedy_layout(B, N).end);
-    const size_t s = sample_layout(B, N > 0 ? N : 1).end;
+    const size_t s = sample_layout(verify_rows(B, N), B, V, true).end;
     if (s > need) need = s;
     if (cfg) {
         if (check_config(cfg) != MTP_OK || N < 1) return 0;
@@ -260,8 +313,8 @@ size_t mtp_workspace_size(const mtp_config* cfg, int B, int N, int V) {
 int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* views, int n_views,
                     const int32_t* kv_len, int B, int N, const int32_t* last_tok, const float* h_prev,
                     const mtp_sample_params* sp, uint64_t seed, uint64_t offset, const int32_t* hist, int H,
-                    int32_t* out_drafts, float* out_h_last, float* out_logits, void* ws, size_t ws_bytes,
-                    mtp_stream_t stream) {
+                    int32_t* out_drafts, float* out_h_last, float* out_logits, float* out_conf, void* ws,
+                    size_t ws_bytes, mtp_stream_t stream) {
     int rc = check_config(cfg);
     if (rc != MTP_OK) return rc;
     if (!w || !views || n_views < 1 || n_views > MTP_MAX_VIEWS) return MTP_ERR_ARG;
@@ -326,7 +379,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         tc_stages = (int)(kTcSmemBudget / sbytes);
         if (tc_stages > kTcMaxStages) tc_stages = kTcMaxStages;
         if (tc_stages < 2) return MTP_ERR_UNSUPPORTED;
-        size_t need = (size_t)tc_stages * sbytes + 1024;
+        size_t need = (size_t)tc_stages * sbytes + 1024 + kTcStageBytes;   // ring + epilogue staging
         if (need > smem) smem = need;
         // the head's ring: a table box and h's high (and, sampling, low) block per stage
         const size_t hbytes = (size_t)kTcHeadN * 128 + (sampling ? 2 : 1) * (size_t)kTcHeadM * 128;
@@ -371,7 +424,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         d.cap = views[v].cap; d.window = views[v].window; d.theta = views[v].rope_theta;
     }
     p.kv_len = kv_len; p.last_tok = last_tok; p.h_prev = h_prev;
-    p.out_drafts = out_drafts; p.out_h_last = out_h_last; p.out_logits = out_logits;
+    p.out_drafts = out_drafts; p.out_h_last = out_h_last; p.out_logits = out_logits; p.out_conf = out_conf;
     p.hdr = reinterpret_cast<WsHeader*>(base);
     p.att_cnt = reinterpret_cast<unsigned int*>(base + L.att_cnt);
     p.amax = reinterpret_cast<unsigned long long*>(base + L.amax);
@@ -384,6 +437,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     p.Y2 = reinterpret_cast<float*>(base + L.Y2);
     p.HN = reinterpret_cast<float*>(base + L.HN);
     p.PART = reinterpret_cast<float*>(base + L.PART);
+    p.CONF = reinterpret_cast<float2*>(base + L.CONF);
     p.ROPE = reinterpret_cast<double*>(base + L.ROPE);
     p.ROPEQ = reinterpret_cast<float2*>(base + L.ROPEQ);
     p.ACT = reinterpret_cast<float*>(base + L.ACT);
@@ -429,12 +483,11 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         p.s_rep = sp->rep_penalty; p.s_pres = sp->presence_penalty;
         p.seed = seed; p.offset = offset; p.hist = hist; p.H = H;
         p.ZB = reinterpret_cast<float*>(base + L.ZB);
-        p.S_rowmax = reinterpret_cast<unsigned long long*>(base + L.SROW);
-        p.S_cnt = reinterpret_cast<unsigned int*>(base + L.SCNT);
-        p.S_nkeep = reinterpret_cast<int32_t*>(base + L.SNK);
-        p.S_wkeep = reinterpret_cast<float*>(base + L.SWK);
-        p.S_id = reinterpret_cast<int32_t*>(base + L.SID);
-        p.S_w = reinterpret_cast<float*>(base + L.SW);
+        p.S_row = reinterpret_cast<unsigned int*>(base + L.SROW);
+        p.S_buf = reinterpret_cast<int2*>(base + L.SBUF);
+        p.S_rcap = sample_rcap(cfg->vocab);
+        sample_piece_plan(cfg->vocab, B, grid, &p.S_ppr, &p.S_plen);
+        if (smem < kSampleSmem) smem = kSampleSmem;
     }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -448,10 +501,10 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
 int mtp_verify_greedy(const void* logits, int ldtype, int B, int N, int V, const int32_t* drafts, int32_t* out_tokens,
                       int32_t* out_n_accept, void* ws, size_t ws_bytes, mtp_stream_t stream) {
     if (!logits || !out_tokens || !out_n_accept) return MTP_ERR_ARG;
-    if (B < 1 || B > MTP_MAX_BATCH || N < 0 || N > 16 || V < 1) return MTP_ERR_ARG;
+    if (B < 1 || B > MTP_MAX_VERIFY_BATCH || N < 0 || N > 16 || V < 1) return MTP_ERR_ARG;
     if (N > 0 && !drafts) return MTP_ERR_ARG;
-    if (ldtype != MTP_DTYPE_F32 && ldtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(logits) & (ldtype == MTP_DTYPE_BF16 ? 1 : 3)) != 0) return MTP_ERR_ARG;
+    const int lc = check_logits(logits, nullptr, ldtype);
+    if (lc != MTP_OK) return lc;
     const GreedyLayout L = greedy_layout(B, N);
     int rc = check_workspace(ws, ws_bytes, L.end);
     if (rc != MTP_OK) return rc;
@@ -473,45 +526,62 @@ int mtp_verify_sample(const void* tgt_logits, const void* dft_logits, int ldtype
                       uint64_t offset, int32_t* out_tokens, int32_t* out_n_accept, void* ws, size_t ws_bytes,
                       mtp_stream_t stream) {
     if (!tgt_logits || !out_tokens || !out_n_accept) return MTP_ERR_ARG;
-    if (B < 1 || B > MTP_MAX_BATCH || N < 0 || N > 16 || V < 1) return MTP_ERR_ARG;
+    if (B < 1 || B > MTP_MAX_VERIFY_BATCH || N < 0 || N > 16 || V < 1) return MTP_ERR_ARG;
     if (N > 0 && (!drafts || !dft_logits)) return MTP_ERR_ARG;
     if (H < 0 || (H > 0 && !hist)) return MTP_ERR_ARG;
-    if (ldtype != MTP_DTYPE_F32 && ldtype != MTP_DTYPE_BF16) return MTP_ERR_UNSUPPORTED;
-    const int am = ldtype == MTP_DTYPE_BF16 ? 1 : 3;
-    if ((reinterpret_cast<uintptr_t>(tgt_logits) & am) || (dft_logits && (reinterpret_cast<uintptr_t>(dft_logits) & am)))
-        return MTP_ERR_ARG;
-    int rc = check_sample_params(sp);
+    int rc = check_logits(tgt_logits, dft_logits, ldtype);
     if (rc != MTP_OK) return rc;
-    const SampleLayout L = sample_layout(B, N);
+    rc = check_sample_params(sp);
+    if (rc != MTP_OK) return rc;
+    const long long rows = verify_rows(B, N);
+    const SampleLayout L = sample_layout(rows, B, V, true);
     rc = check_workspace(ws, ws_bytes, L.end);
     if (rc != MTP_OK) return rc;
     const int sms = num_sms();
     if (sms <= 0) return MTP_ERR_CUDA;
-    int grid = verify_sample_max_grid(sms);
-    if (grid < 1) return MTP_ERR_UNSUPPORTED;
-    if (grid > sms) grid = sms;
     char* base = static_cast<char*>(ws);
-    VerifySampleArgs a;
-    memset(&a, 0, sizeof a);
-    a.draft_k = -1;
-    a.tgt = tgt_logits; a.dft = dft_logits; a.bf16 = ldtype == MTP_DTYPE_BF16;
-    a.B = B; a.N = N; a.V = V; a.drafts = drafts; a.hist = hist; a.H = H; a.hist_stride = H;
-    a.temp = sp->temp; a.top_p = sp->top_p; a.min_p = sp->min_p; a.rep = sp->rep_penalty;
-    a.pres = sp->presence_penalty;
-    a.seed = seed; a.offset = offset;
-    a.out_tokens = out_tokens; a.out_n_accept = out_n_accept;
-    a.hdr = reinterpret_cast<WsHeader*>(base);
-    a.rowmax = reinterpret_cast<unsigned long long*>(base + L.rowmax);
-    a.cand_cnt = reinterpret_cast<unsigned int*>(base + L.cnt);
-    a.n_keep = reinterpret_cast<int32_t*>(base + L.nkeep);
-    a.w_keep = reinterpret_cast<float*>(base + L.wkeep);
-    a.cand_id = reinterpret_cast<int32_t*>(base + L.id);
-    a.cand_w = reinterpret_cast<float*>(base + L.w);
-    a.resid = reinterpret_cast<float*>(base + L.resid);
-    a.timeout_ns = kBarrierLimitNs;
+    SampleJob j = sample_job(tgt_logits, dft_logits, ldtype, B, N, V, drafts, hist, H, sp, seed, offset, base, L,
+                             rows, sms);
+    j.mode = 0;
+    j.out_tokens = out_tokens;
+    j.out_n_accept = out_n_accept;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, L.zero_end, s) != cudaSuccess) return MTP_ERR_CUDA;
-    return launch_verify_sample(a, grid, s) == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
+    return launch_sample(j, sms, s) == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
+}
+
+int mtp_sample_drafts(const void* dft_logits, int ldtype, int B, int N, int V, const int32_t* hist, int H,
+                      const mtp_sample_params* sp, uint64_t seed, uint64_t offset, int32_t* out_drafts, void* ws,
+                      size_t ws_bytes, mtp_stream_t stream) {
+    if (!dft_logits || !out_drafts) return MTP_ERR_ARG;
+    if (B < 1 || B > MTP_MAX_VERIFY_BATCH || N < 1 || N > 16 || V < 1) return MTP_ERR_ARG;
+    if (H < 0 || (H > 0 && !hist)) return MTP_ERR_ARG;
+    int rc = check_logits(dft_logits, nullptr, ldtype);
+    if (rc != MTP_OK) return rc;
+    rc = check_sample_params(sp);
+    if (rc != MTP_OK) return rc;
+    const SampleLayout L = sample_layout(B, B, V, false);
+    rc = check_workspace(ws, ws_bytes, L.end);
+    if (rc != MTP_OK) return rc;
+    const int sms = num_sms();
+    if (sms <= 0) return MTP_ERR_CUDA;
+    char* base = static_cast<char*>(ws);
+    SampleJob j = sample_job(dft_logits, nullptr, ldtype, B, N, V, out_drafts, hist, H, sp, seed, offset, base, L,
+                             B, sms);
+    j.mode = 1;
+    j.draw_ld = (long long)N * V;
+    j.out_draw = out_drafts;
+    j.out_draw_ld = N;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the row state is zeroed once; every row's finishing CTA re-zeroes it
+    if (cudaMemsetAsync(ws, 0, L.zero_end, s) != cudaSuccess) return MTP_ERR_CUDA;
+    const size_t esz = ldtype == MTP_DTYPE_BF16 ? 2 : 4;
+    for (int i = 0; i < N; ++i) {   // draw i's penalty set holds draws 0..i-1: one launch per window position
+        j.draw_i = i;
+        j.base0 = static_cast<const char*>(dft_logits) + (size_t)i * V * esz;
+        if (launch_sample(j, sms, s) != cudaSuccess) return MTP_ERR_CUDA;
+    }
+    return MTP_OK;
 }
 
 int mtp_last_error(const void* ws, mtp_stream_t stream) {

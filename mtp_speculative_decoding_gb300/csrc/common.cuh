@@ -117,6 +117,27 @@ __device__ __forceinline__ void bulk_g2s_pol(void* dst, const void* src, unsigne
         "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
         : "memory");
 }
+// bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16)
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, unsigned int bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// bulk copy shared -> global (both 16-byte aligned, bytes a multiple of 16),
+// tracked by the issuing thread's bulk groups
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, unsigned int bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's bulk stores are complete (their global writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// L2 prefetch of one box of a 2-D tensor map
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+                 : "memory");
+}
 // order earlier generic-proxy shared-memory accesses before later bulk-copy writes
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 

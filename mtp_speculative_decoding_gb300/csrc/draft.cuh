@@ -48,6 +48,11 @@ constexpr int kTcHeadM = 64;
 constexpr int kTcHeadN = 256;
 constexpr size_t kTcHeadSmemBudget = 200 * 1024;
 constexpr int kTcHeadCols = 512;   // tensor-memory columns: two 256-column accumulators
+// Projection epilogue staging after the operand ring: a 128-row output tile
+// as fp32 [b][128] (512 bytes per sequence), then (post-projection) the
+// tile's two 64-column blocks of h's bf16 high and low parts in the head
+// operand's swizzled layout
+constexpr size_t kTcStageBytes = (size_t)kTcHeadM * kTcTileM * 4 + 2 * 2 * (size_t)kTcHeadM * 128;
 
 // floats per attention partial: o[grp][hd], m[grp], l[grp], padded to 16 bytes
 __host__ __device__ constexpr int attn_psz(int grp, int hd) { return (grp * (hd + 2) + 3) & ~3; }
@@ -101,12 +106,14 @@ struct DraftParams {
     int32_t* out_drafts;
     float* out_h_last;
     float* out_logits;
+    float* out_conf;             // [B, N] per-step top-1 softmax probability, or null
     // workspace
     WsHeader* hdr;
     unsigned int* att_cnt;       // [B * Hkv] last-arriver counters (self-resetting)
     unsigned long long* amax;    // [N * B] packed argmax keys
     float *XB, *XM, *QR, *OB, *YB, *MB, *Y2, *HN;
     float* PART;                 // attention partials
+    float2* CONF;                // [grid][B] per-CTA softmax-denominator partials (max, sum) of the step's logits
     double* ROPE;                // [MTP_MAX_VIEWS][hd / 2] RoPE inverse frequencies (written at kernel start)
     float2* ROPEQ;               // [B][MTP_MAX_VIEWS][hd / 2] (cos, sin) at the step's query position
     float* ACT;                  // [B, kmax] staged activations (global mode)
@@ -124,19 +131,16 @@ struct DraftParams {
     unsigned long long timeout_ns;
     // sampled drafting (temperature > 0): sample_dist parameters, the
     // Philox stream, the penalty history [B, H], the step's logits [B, V]
-    // and the sampler's per-row state
+    // and the sampler's per-row state (zero at launch; see sample.cuh)
     int sampling;
     float s_temp, s_top_p, s_min_p, s_rep, s_pres;
     unsigned long long seed, offset;
     const int32_t* hist;
     int H;
     float* ZB;
-    unsigned long long* S_rowmax;
-    unsigned int* S_cnt;
-    int32_t* S_nkeep;
-    float* S_wkeep;
-    int32_t* S_id;
-    float* S_w;
+    unsigned int* S_row;         // [4][B]: row maximum key, survivor count, overflow flag, pieces done
+    int2* S_buf;                 // [B][S_rcap] survivors
+    int S_rcap, S_plen, S_ppr;   // survivor capacity per row, tokens per piece, pieces per row
 };
 
 cudaError_t launch_draft_f32(const DraftParams& p, int grid, size_t smem, cudaStream_t s);

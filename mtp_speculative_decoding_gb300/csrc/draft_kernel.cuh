@@ -308,14 +308,45 @@ struct GegluEpi {
     }
 };
 
+// Running softmax denominator of a stream of logits: m the largest seen, s
+// the sum of exp(z - m) (NaN left out).  Two partials merge exactly.
+struct SoftDen {
+    float m, s;
+    __device__ __forceinline__ void add(float z) {
+        if (!(z == z)) return;
+        if (z > m) {
+            s = s * expf(m - z) + 1.f;   // m = -inf: s = 0 * 0 + 1
+            m = z;
+        } else {
+            s += expf(z - m);
+        }
+    }
+    __device__ __forceinline__ void merge(float m2, float s2) {
+        if (!(s2 > 0.f)) return;
+        if (!(s > 0.f)) {
+            m = m2;
+            s = s2;
+        } else if (m2 > m) {
+            s = s * expf(m - m2) + s2;
+            m = m2;
+        } else {
+            s += s2 * expf(m2 - m);
+        }
+    }
+};
+__device__ __forceinline__ SoftDen soft_den0() { return SoftDen{-INFINITY, 0.f}; }
+
 // LM head: softcap, optional logits store, running packed argmax per column
-// (lane c & 31 owns column c; two registers cover 64 columns).
+// (lane c & 31 owns column c; two registers cover 64 columns), and with
+// `conf` the columns' running softmax denominators.
 struct HeadEpi {
     float* logits;  // [B, N, V] or null
     int V, N, step;
     float softcap;
     unsigned long long best_lo, best_hi;
     float* zb;      // [B, V] the step's logits for the sampler, or null
+    bool conf;      // keep the softmax denominators (per-step confidence output)
+    SoftDen den_lo, den_hi;
     template <int NB>
     __device__ __forceinline__ void apply(int r, int b0, int nb, const float (&acc)[NB], const float (&)[NB]) {
         const int lane = threadIdx.x & 31;
@@ -330,6 +361,10 @@ struct HeadEpi {
                 const unsigned long long k = pack_argmax(z, (uint32_t)r);
                 if (col < 32) best_lo = k > best_lo ? k : best_lo;
                 else best_hi = k > best_hi ? k : best_hi;
+                if (conf) {
+                    if (col < 32) den_lo.add(z);
+                    else den_hi.add(z);
+                }
             }
         }
     }
@@ -414,22 +449,56 @@ __device__ __forceinline__ float4 ld4_sum(const float* q, int S, long long st) {
     return a;
 }
 
-// Element i of sequence b's output of a tensor-core projection with R output
-// rows and S split partials: the partials summed in split order.
-__device__ __forceinline__ float part_sum(const DraftParams& p, int S, int R, int b, int i) {
-    const float* q = p.PB + (long long)b * R + i;
+// dst[i] = sum over s < S of sequence b's split partial i (tensor-core
+// projection with R output rows), i < n, n a multiple of 4.  The CTA's
+// threads take float4 columns; when there are fewer columns than threads,
+// each column's partials are cut into G contiguous groups summed in order by
+// G threads (up to 8 loads in flight each), and the group sums are added in
+// group order through scratch[G n] -- a fixed order, so the result is
+// deterministic.  Synchronises the CTA.
+static __device__ __noinline__ void part_sum_vec(const DraftParams& p, int S, int R, int b, int n, float* dst,
+                                             float* scratch) {
+    const int ncol = n >> 2;
+    int G = (int)blockDim.x / (ncol > 0 ? ncol : 1);
+    G = G < 1 ? 1 : (G > 4 ? 4 : G);
+    const int per = (S + G - 1) / G;
     const long long st = (long long)p.B * R;
-    float v = 0.f;
-    int s = 0;
-    for (; s + 8 <= S; s += 8) {   // eight loads in flight, summed in order
-        float t[8];
+    const float* base = p.PB + (long long)b * R;
+    for (int t = threadIdx.x; t < ncol * G; t += blockDim.x) {
+        const int c = t % ncol, g = t / ncol;
+        const int s0 = g * per, s1 = s0 + per < S ? s0 + per : S;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sb = s0; sb < s1; sb += 8) {
+            float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) t[u] = __ldcg(q + (s + u) * st);
+            for (int u = 0; u < 8; ++u)
+                if (sb + u < s1) v[u] = __ldcg(reinterpret_cast<const float4*>(base + (sb + u) * st) + c);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v += t[u];
+            for (int u = 0; u < 8; ++u)
+                if (sb + u < s1) {
+                    a.x += v[u].x;
+                    a.y += v[u].y;
+                    a.z += v[u].z;
+                    a.w += v[u].w;
+                }
+        }
+        reinterpret_cast<float4*>(G == 1 ? dst : scratch + (long long)g * n)[c] = a;
     }
-    for (; s < S; ++s) v += __ldcg(q + s * st);
-    return v;
+    __syncthreads();
+    if (G > 1) {
+        for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
+            float4 a = reinterpret_cast<const float4*>(scratch)[c];
+            for (int g = 1; g < G; ++g) {
+                const float4 v = reinterpret_cast<const float4*>(scratch + (long long)g * n)[c];
+                a.x += v.x;
+                a.y += v.y;
+                a.z += v.z;
+                a.w += v.w;
+            }
+            reinterpret_cast<float4*>(dst)[c] = a;
+        }
+        __syncthreads();
+    }
 }
 
 // dst[s][i] = src[s][i] for i < n (n a multiple of 4, 16-byte aligned rows):
@@ -470,7 +539,7 @@ __device__ __forceinline__ void vec_copy(const VecCopy<NS>& c, int n) {
 // `writer` marks the one CTA that also stores residual-stream updates.  The
 // norm gains are staged in gs (2 max(d_t, d_a) floats) by the same loops that
 // load the activations.
-template <typename WT>
+template <typename WT, bool TC>
 __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, float* dst, float* tmp, bool writer,
                           float* red, float* gs) {
     switch (phase) {
@@ -500,12 +569,11 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
         const int n = p.d_a;
         const float* ga = p.blk[l].attn_norm;
         if (l == 0) {
-            if (p.tc_proj) {   // the pre-projection's partials form the residual stream
+            if ((TC && p.tc_proj)) {   // the pre-projection's partials form the residual stream
+                part_sum_vec(p, p.sk[PH_PRE], n, b, n, tmp, dst);
                 for (int i = threadIdx.x; i < n; i += blockDim.x) {
-                    const float x = part_sum(p, p.sk[PH_PRE], n, b, i);
-                    tmp[i] = x;
                     gs[i] = __ldg(ga + i);
-                    if (writer) p.XB[(long long)b * n + i] = x;
+                    if (writer) p.XB[(long long)b * n + i] = tmp[i];
                 }
             } else {
 #pragma unroll 4
@@ -517,9 +585,10 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
             __syncthreads();
         } else {
             const float* gp = p.blk[l - 1].post_ffn_norm;
+            if ((TC && p.tc_proj)) part_sum_vec(p, p.sk[PH_FFN2], n, b, n, dst, dst + n);
 #pragma unroll 4
             for (int i = threadIdx.x; i < n; i += blockDim.x) {
-                dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_FFN2], n, b, i) : __ldcg(p.Y2 + (long long)b * n + i);
+                if (!(TC && p.tc_proj)) dst[i] = __ldcg(p.Y2 + (long long)b * n + i);
                 tmp[i] = __ldcg(p.XM + (long long)b * n + i);
                 gs[i] = __ldg(ga + i);
                 gs[n + i] = __ldg(gp + i);
@@ -539,9 +608,10 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     case PH_FFN1: {
         const int n = p.d_a;
         const float *g1 = p.blk[l].post_attn_norm, *g2 = p.blk[l].pre_ffn_norm;
+        if ((TC && p.tc_proj)) part_sum_vec(p, p.sk[PH_O], n, b, n, dst, dst + n);
 #pragma unroll 4
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_O], n, b, i) : __ldcg(p.YB + (long long)b * n + i);
+            if (!(TC && p.tc_proj)) dst[i] = __ldcg(p.YB + (long long)b * n + i);
             tmp[i] = __ldcg(p.XB + (long long)b * n + i);
             gs[i] = __ldg(g1 + i);
             gs[n + i] = __ldg(g2 + i);
@@ -560,9 +630,10 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     case PH_POST: {
         const int n = p.d_a;
         const float *g1 = p.blk[p.L - 1].post_ffn_norm, *g2 = p.final_norm;
+        if ((TC && p.tc_proj)) part_sum_vec(p, p.sk[PH_FFN2], n, b, n, dst, dst + n);
 #pragma unroll 4
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            dst[i] = p.tc_proj ? part_sum(p, p.sk[PH_FFN2], n, b, i) : __ldcg(p.Y2 + (long long)b * n + i);
+            if (!(TC && p.tc_proj)) dst[i] = __ldcg(p.Y2 + (long long)b * n + i);
             tmp[i] = __ldcg(p.XM + (long long)b * n + i);
             gs[i] = __ldg(g1 + i);
             gs[n + i] = __ldg(g2 + i);
@@ -582,7 +653,7 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     }
     case PH_FFN2: {
         const int n = p.F;
-        if (p.tc_proj) {   // GeGLU of the summed gate (rows 0..F-1) and up (rows F..2F-1) partials
+        if ((TC && p.tc_proj)) {   // GeGLU of the summed gate (rows 0..F-1) and up (rows F..2F-1) partials
             const long long st = (long long)p.B * 2 * n;
             const float* q = p.PB + (long long)b * 2 * n;
             const int S = p.sk[PH_FFN1];
@@ -621,7 +692,7 @@ __device__ __forceinline__ int phase_k(const DraftParams& p, int phase) {
 // CTA c builds sequences b = c, c + grid, ... into p.ACT and a barrier
 // follows.  Returns the activation pointer and stride, or null if a barrier
 // failed.
-template <typename WT>
+template <typename WT, bool TC>
 __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l, float* smem_act, float* smem_tmp,
                                   float* red, unsigned int& epoch, int& lda, bool& ok) {
     const int K = phase_k(p, phase);
@@ -630,26 +701,38 @@ __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l,
     ok = true;
     if (p.act_smem) {
         for (int b = 0; b < p.B; ++b)
-            build_act<WT>(p, phase, k, l, b, smem_act + (long long)b * K, smem_tmp, blockIdx.x == 0, red, gs);
+            build_act<WT, TC>(p, phase, k, l, b, smem_act + (long long)b * K, smem_tmp, blockIdx.x == 0, red, gs);
         lda = K;
         return smem_act;
     }
     // global mode: copy-only inputs are read in place
-    if (!p.tc_proj) {
+    if (!(TC && p.tc_proj)) {
         if (phase == PH_O) { lda = K; return p.OB; }
         if (phase == PH_FFN2) { lda = K; return p.MB; }
         if (phase == PH_HEAD) { lda = K; return p.HN; }
     }
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-        build_act<WT>(p, phase, k, l, b, smem_act, smem_tmp, true, red, gs);
-        if (p.tc_proj) {
-            // tensor-core operand: bf16 high and low parts, read by tensor copies
-            for (int i = threadIdx.x; i < K; i += blockDim.x) {
-                const float v = smem_act[i];
-                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-                const long long xi = xtile_idx(b, i, p.Bp);
-                p.XA[xi] = __bfloat16_as_ushort(hi);
-                p.XAL[xi] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+        build_act<WT, TC>(p, phase, k, l, b, smem_act, smem_tmp, true, red, gs);
+        if ((TC && p.tc_proj)) {
+            // tensor-core operand: bf16 high and low parts, read by tensor
+            // copies; 8 consecutive columns are one 16-byte chunk of the
+            // swizzled tile, stored at once (K is a multiple of 8)
+            for (int c = threadIdx.x; c < K / 8; c += blockDim.x) {
+                const float4 v0 = reinterpret_cast<const float4*>(smem_act)[2 * c];
+                const float4 v1 = reinterpret_cast<const float4*>(smem_act)[2 * c + 1];
+                const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+                    const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * e] - __bfloat162float(h0));
+                    const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1));
+                    hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                    lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                }
+                const long long xi = xtile_idx(b, 8 * c, p.Bp);
+                *reinterpret_cast<uint4*>(p.XA + xi) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(p.XAL + xi) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             fence_proxy_async_global();
         } else {
@@ -849,7 +932,7 @@ __device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v)
 // NST: ring stages per warp.  abar: [kWarps][NST] stage barriers (one arrival
 // each); apar: the calling warp's stage phase bits, carried across calls.
 template <typename WT, int HD, int NST>
-__device__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem, const int* kv, const AttnTab& tab,
+__device__ __noinline__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem, const int* kv, const AttnTab& tab,
                                 unsigned long long* abar, unsigned int& apar) {
     constexpr AttnGeom G = attn_geom(HD, (int)sizeof(WT));
     constexpr int RB = G.RB, LPR = G.LPR, CPL = G.CPL, KPW = G.KPW, EPC = G.EPC, DPL = G.DPL;
@@ -1450,6 +1533,9 @@ struct TcJob {
     bool lo;                      // also multiply the low part (else X ~ its high part)
 };
 
+// The four epilogue warps (4-7) of tc_gemm synchronise among themselves.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 5, 128;" ::: "memory"); }
+
 template <class Epi>
 __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsigned char* smem, TcState& ts, Epi& epi) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1535,7 +1621,13 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
             }
         }
     } else if (warp >= 4 && warp < 8) {
-        const int q = warp - 4;   // tensor-memory lane quarter of this warp
+        // epilogue: accumulator -> shared-memory staging -> bulk stores (a
+        // row segment per sequence), so the 128 threads issue a few copies
+        // instead of one 4-byte store per value
+        const int q = warp - 4;                  // tensor-memory lane quarter of this warp
+        const int et = threadIdx.x - 4 * 32;     // 0..127
+        const int r = 32 * q + lane;             // row of the tile this thread reads
+        unsigned char* stg = ring + (size_t)NS * sbytes;
         for (int j = 0; j < nit && ok; ++j) {
             const uint32_t it = ts.it + j, acc = it & 1u;
             if (!mbar_wait_limited(&ts.tfull[acc], (it >> 1) & 1u, p.timeout_ns)) {
@@ -1544,18 +1636,29 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
             }
             tc_fence_after();
             const int item = (int)blockIdx.x + j * (int)gridDim.x;
-            const int row = (item / J.S) * kTcTileM + 32 * q + lane;
+            const int row0 = (item / J.S) * kTcTileM;
+            if (j > 0) {   // the previous item's stores have read the staging
+                bulk_wait_read();
+                epi_sync();
+            }
             const uint32_t ta = ts.tmem + ((uint32_t)(32 * q) << 16) + acc * (uint32_t)Bp;
             for (int c0 = 0; c0 < Bp; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(ta + (uint32_t)c0, r);
+                uint32_t v[16];
+                tmem_ld16(ta + (uint32_t)c0, v);
                 tmem_ld_wait();
-                epi.apply(row, item % J.S, c0, r);
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) epi.put(stg, row0, r, c0 + jj, __uint_as_float(v[jj]));
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ts.tempty[acc]);
+            fence_proxy_async_smem();   // staging writes before the bulk copies read them
+            epi_sync();
+            epi.store(stg, row0, item % J.S, et);
+            bulk_commit();
         }
+        bulk_wait_all();              // the partials are written ...
+        fence_proxy_async_global();   // ... and ordered before this thread's later generic accesses
     }
     ts.g += nsteps;
     ts.it += (uint32_t)nit;
@@ -1648,7 +1751,9 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
         const int q = warp - 4;   // tensor-memory lane quarter of this warp
         const int b = 16 * q + lane;
         const bool mine = lane < 16 && b < p.B;
+        const bool conf = p.out_conf != nullptr;
         unsigned long long best = 0ull;
+        SoftDen den = soft_den0();
         for (int j = 0; j < nit && ok; ++j) {
             const uint32_t it = ts.it + j, acc = it & 1u;
             if (!mbar_wait_limited(&ts.tfull[acc], (it >> 1) & 1u, p.timeout_ns)) {
@@ -1673,6 +1778,7 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
                             if (p.ZB) p.ZB[(long long)b * p.V + row] = z;
                             const unsigned long long key = pack_argmax(z, (uint32_t)row);
                             best = key > best ? key : best;
+                            if (conf) den.add(z);
                         }
                     }
                 }
@@ -1682,6 +1788,7 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
             if (lane == 0) mbar_arrive(&ts.tempty[acc]);
         }
         if (mine && nit > 0) atomicMax(p.amax + (long long)k * p.B + b, best);
+        if (mine && conf) p.CONF[(long long)blockIdx.x * p.B + b] = make_float2(den.m, den.s);
     }
     ts.g += (uint32_t)(nit * nks);
     ts.it += (uint32_t)nit;
@@ -1692,34 +1799,48 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
 struct TcPartEpi {
     float* PB;
     int B, R;
-    __device__ __forceinline__ void apply(int row, int split, int c0, const uint32_t (&r)[16]) {
-        if (row >= R) return;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            const int b = c0 + jj;
-            if (b < B) PB[((long long)split * B + b) * R + row] = __uint_as_float(r[jj]);
-        }
+    __device__ __forceinline__ void put(unsigned char* stg, int, int r, int b, float v) {
+        reinterpret_cast<float*>(stg)[b * kTcTileM + r] = v;
+    }
+    // thread et < B stores sequence et's row segment
+    __device__ __forceinline__ void store(const unsigned char* stg, int row0, int split, int et) {
+        const int nr = R - row0 < kTcTileM ? R - row0 : kTcTileM;
+        if (et < B && nr > 0)
+            bulk_s2g(PB + ((long long)split * B + et) * R + row0, stg + (size_t)et * kTcTileM * 4, (unsigned)nr * 4u);
     }
 };
 
-// epilogue: unsplit post-projection: h and its bf16 high / low parts as the
-// head's operand
+// epilogue: unsplit post-projection: h, and its bf16 high / low parts as the
+// head's operand (rows of the tile past R give zeros, so the operand's
+// columns past d_t stay zero)
 struct TcHnEpi {
     float* HN;
     uint16_t *XH, *XL;
     int B, R, Bp;
-    __device__ __forceinline__ void apply(int row, int, int c0, const uint32_t (&r)[16]) {
-        if (row >= R) return;
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-            const int b = c0 + jj;
-            if (b < B) {
-                const float v = __uint_as_float(r[jj]);
-                HN[(long long)b * R + row] = v;
-                const long long xi = xtile_idx(b, row, Bp);
-                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-                XH[xi] = __bfloat16_as_ushort(hi);
-                XL[xi] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+    __device__ __forceinline__ void put(unsigned char* stg, int row0, int r, int b, float v) {
+        if (row0 + r >= R) v = 0.f;
+        reinterpret_cast<float*>(stg)[b * kTcTileM + r] = v;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const int kbl = r >> 6, kk = r & 63;
+        const size_t o = (size_t)kbl * kTcHeadM * 128 + (size_t)b * 128 + (size_t)((((kk >> 3) ^ (b & 7)) << 3) | (kk & 7)) * 2;
+        unsigned char* xs = stg + (size_t)kTcHeadM * kTcTileM * 4;
+        *reinterpret_cast<uint16_t*>(xs + o) = __bfloat16_as_ushort(hi);
+        *reinterpret_cast<uint16_t*>(xs + 2 * kTcHeadM * 128 + o) =
+            __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+    }
+    // threads et < B store h's row segments; threads 64..67 the operand blocks
+    __device__ __forceinline__ void store(const unsigned char* stg, int row0, int, int et) {
+        const int nr = R - row0 < kTcTileM ? R - row0 : kTcTileM;
+        if (et < B && nr > 0)
+            bulk_s2g(HN + (long long)et * R + row0, stg + (size_t)et * kTcTileM * 4, (unsigned)nr * 4u);
+        const int w = et - 64;
+        if (w >= 0 && w < 4) {
+            const int kbl = w & 1, kb = row0 / 64 + kbl;
+            if (kb < (R + 63) / 64) {
+                const unsigned char* xs = stg + (size_t)kTcHeadM * kTcTileM * 4 + (size_t)(w >> 1) * 2 * kTcHeadM * 128 +
+                                          (size_t)kbl * kTcHeadM * 128;
+                uint16_t* dst = ((w >> 1) ? XL : XH) + (long long)kb * Bp * 64;
+                bulk_s2g(dst, xs, (unsigned)B * 128u);
             }
         }
     }
@@ -1747,12 +1868,26 @@ __device__ __forceinline__ TcJob tc_job(const DraftParams& p, int phase, int l) 
     return J;
 }
 
+// L2 prefetch of this CTA's weight boxes of job J (thread 0, ahead of the
+// phase's prologue and barrier: the weights do not depend on the phase's
+// input, so their HBM latency hides behind the prologue)
+__device__ __forceinline__ void tc_prefetch(const TcJob& J) {
+    const int ntiles = (J.R + kTcTileM - 1) / kTcTileM, nitems = ntiles * J.S;
+    for (int item = (int)blockIdx.x; item < nitems; item += (int)gridDim.x) {
+        const int row0 = (item / J.S) * kTcTileM;
+        const CUtensorMap* wm = row0 < J.R1 ? J.wa : J.wb;
+        const int wy = row0 < J.R1 ? row0 : row0 - J.R1;
+        const int k0 = (item % J.S) * J.kps, k1 = k0 + J.kps < J.nks ? k0 + J.kps : J.nks;
+        for (int ks = k0; ks < k1; ++ks) tma_prefetch_2d(wm, ks * kTcTileK, wy);
+    }
+}
+
 template <typename WT, bool TC>
 __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const float* a, int lda,
                                            unsigned long long (*head_best)[32], unsigned char* smem,
                                            unsigned long long (*bars)[kHeadSlots], unsigned int& par,
                                            float (*hpart)[kHeadSlots][4], TcState& ts) {
-    HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull, p.ZB};
+    HeadEpi e{p.out_logits, p.V, p.N, k, p.softcap, 0ull, 0ull, p.ZB, p.out_conf != nullptr, soft_den0(), soft_den0()};
     if (TC && p.tc_head) {
         // greedy: h rounded to bf16 (half the MMAs and operand traffic; the
         // argmax is stable to it); sampling: both parts, so the sampler sees
@@ -1785,8 +1920,39 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
             atomicMax(p.amax + (long long)k * p.B + c0 + threadIdx.x, m);
         }
         __syncthreads();
+        if (e.conf) {   // the CTA's softmax-denominator partial of each column
+            float* hm = reinterpret_cast<float*>(&head_best[0][0]);
+            const SoftDen d = c0 == 0 ? e.den_lo : e.den_hi;
+            hm[2 * (warp * 32 + lane)] = d.m;
+            hm[2 * (warp * 32 + lane) + 1] = d.s;
+            __syncthreads();
+            if (threadIdx.x < 32 && c0 + (int)threadIdx.x < p.B) {
+                SoftDen t = soft_den0();
+                for (int w = 0; w < kWarps; ++w) t.merge(hm[2 * (w * 32 + threadIdx.x)], hm[2 * (w * 32 + threadIdx.x) + 1]);
+                p.CONF[(long long)blockIdx.x * p.B + c0 + threadIdx.x] = make_float2(t.m, t.s);
+            }
+            __syncthreads();
+        }
     }
     return true;
+}
+
+// Confidence of step k for sequence b (one warp): the top-1 softmax
+// probability 1 / S, S the merged softmax denominator of the CTAs' partials
+// (relative to their common maximum, the top logit).
+__device__ __forceinline__ void write_conf(const DraftParams& p, int k, int b) {
+    const int lane = threadIdx.x & 31;
+    SoftDen t = soft_den0();
+    for (int c = lane; c < (int)gridDim.x; c += 32) {
+        const float2 v = __ldcg(p.CONF + (long long)c * p.B + b);
+        t.merge(v.x, v.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, t.m, o), s2 = __shfl_xor_sync(0xffffffffu, t.s, o);
+        t.merge(m2, s2);
+    }
+    if (lane == 0) p.out_conf[(long long)b * p.N + k] = t.s > 0.f ? 1.f / t.s : 0.f;
 }
 
 // ---------------------------------------------------------------------------
@@ -1794,59 +1960,57 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
 // ---------------------------------------------------------------------------
 // Sampled drafting, step k: sample_dist over each sequence's logits
 // (penalties over hist[b] and the drafts so far, temperature, min-p, top-p)
-// and a draw with the uniform of (b, k, purpose 0), in the sampler's
-// phases: row maxima, candidates, sorted kept sets, draws.  The token goes
-// to the step's argmax slot, where the next step and the outputs read it.
-static __device__ bool sample_step(const DraftParams& p, int k, unsigned char* smem, unsigned int& epoch) {
-    VerifySampleArgs a;
-    a.tgt = p.ZB;
-    a.dft = nullptr;
-    a.bf16 = 0;
-    a.B = p.B;
-    a.N = p.N;
-    a.V = p.V;
-    a.drafts = p.out_drafts;
-    a.hist = p.hist;
-    a.H = p.H;
-    a.hist_stride = p.H;
-    a.temp = p.s_temp;
-    a.top_p = p.s_top_p;
-    a.min_p = p.s_min_p;
-    a.rep = p.s_rep;
-    a.pres = p.s_pres;
-    a.seed = p.seed;
-    a.offset = p.offset;
-    a.out_tokens = nullptr;
-    a.out_n_accept = nullptr;
-    a.hdr = p.hdr;
-    a.rowmax = p.S_rowmax;
-    a.cand_cnt = p.S_cnt;
-    a.n_keep = p.S_nkeep;
-    a.w_keep = p.S_wkeep;
-    a.cand_id = p.S_id;
-    a.cand_w = p.S_w;
-    a.resid = nullptr;
-    a.timeout_ns = p.timeout_ns;
-    a.draft_k = k;
-    const long long chunks = (p.V + kScanChunk - 1) / kScanChunk, items = (long long)p.B * chunks;
-    uint32_t* bits = reinterpret_cast<uint32_t*>(smem);
-    unsigned long long* red64 = reinterpret_cast<unsigned long long*>(smem + kScanChunk / 8);
-    for (int mode = 0; mode < 2; ++mode) {
-        for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-            const long long c0 = (it % chunks) * kScanChunk;
-            sample_scan_item(a, (int)(it / chunks), c0, c0 + kScanChunk < p.V ? c0 + kScanChunk : p.V, mode, bits, red64);
-        }
-        if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return false;
-    }
-    unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
-    float* wsh = reinterpret_cast<float*>(smem + kCandCap * sizeof(unsigned long long));
-    for (int b = blockIdx.x; b < p.B; b += gridDim.x) sample_sort_row(a, b, keys, wsh);
-    if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return false;
-    const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    for (int b = gw; b < p.B; b += gridDim.x * kWarps) {
-        const int32_t t = sample_pick_draft(a, b);
-        if (lane == 0) p.amax[(long long)k * p.B + b] = (1ull << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
-    }
+// and a draw with the uniform of (b, k, purpose 0): one pass of the
+// sampler's pieces over the grid, the rows' finishing CTAs draw.  The token
+// goes to the step's argmax slot, where the next step and the outputs read
+// it; one grid barrier follows.
+static __device__ __noinline__ bool sample_step(const DraftParams& p, int k, unsigned char* smem, unsigned int& epoch) {
+    SampleJob j;
+    j.base0 = p.ZB;
+    j.base1 = nullptr;
+    j.f32 = 1;
+    j.mode = 1;
+    j.B = p.B;
+    j.N = p.N;
+    j.V = p.V;
+    j.draw_ld = p.V;
+    j.draw_i = k;
+    j.drafts = p.out_drafts;   // drafts 0..k-1 (written by the steps' PRE phases)
+    j.drafts_ld = p.N;
+    j.hist = p.hist;
+    j.H = p.H;
+    j.hist_ld = p.H;
+    j.temp = p.s_temp;
+    j.top_p = p.s_top_p;
+    j.min_p = p.s_min_p;
+    j.rep = p.s_rep;
+    j.pres = p.s_pres;
+    j.seed = p.seed;
+    j.offset = p.offset;
+    j.out_tokens = nullptr;
+    j.out_n_accept = nullptr;
+    j.out_draw = nullptr;
+    j.out_draw_ld = 0;
+    j.out_amax = p.amax + (long long)k * p.B;
+    j.hdr = p.hdr;
+    j.row_max = p.S_row;
+    j.row_cnt = p.S_row + p.B;
+    j.row_ovf = p.S_row + 2 * p.B;
+    j.row_done = p.S_row + 3 * p.B;
+    j.seq_done = nullptr;
+    j.row_buf = p.S_buf;
+    j.rcap = p.S_rcap;
+    j.keep_id = nullptr;
+    j.keep_w = nullptr;
+    j.ccap = 0;
+    j.n_keep = nullptr;
+    j.w_keep = nullptr;
+    j.piece_len = p.S_plen;
+    j.ppr = p.S_ppr;
+    const int total = p.B * p.S_ppr;
+    if (threadIdx.x == 0) prefetch_piece(j, blockIdx.x);
+    for (int pc = blockIdx.x; pc < total; pc += gridDim.x)
+        sample_piece(j, pc, pc + (int)gridDim.x < total ? pc + (int)gridDim.x : -1, smem);
     return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
 }
 
@@ -1926,7 +2090,10 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         constexpr bool TWO = decltype(two)::value;
         int lda = 0;
         bool ok = true;
-        const float* a = stage_act<WT>(p, phase, k, l, act, tmp, red, epoch, lda, ok);
+        if constexpr (TC) {
+            if (p.tc_proj && threadIdx.x == 0) tc_prefetch(tc_job(p, phase, l));
+        }
+        const float* a = stage_act<WT, TC>(p, phase, k, l, act, tmp, red, epoch, lda, ok);
         if (!ok) return false;
         if (TC && p.tc_proj) {
             // tensor cores over the staged bf16 input parts: split partials,
@@ -1956,12 +2123,11 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         if (blockIdx.x == 0) {
             for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
                 if (k > 0) p.out_drafts[(long long)b * p.N + (k - 1)] = step_token(p, b, k);
-                if (p.sampling) {   // the sampler's row state of this step (first used after the head)
-                    p.S_rowmax[b] = 0ull;
-                    p.S_cnt[b] = 0u;
-                }
             }
         }
+        if (k > 0 && p.out_conf)   // the previous step's confidence, a warp per sequence
+            for (int b = blockIdx.x * kWarps + (int)(threadIdx.x >> 5); b < p.B; b += gridDim.x * kWarps)
+                write_conf(p, k - 1, b);
         {
             StoreEpi e{p.XB, p.d_a};
             if (!gemv_step(PH_PRE, k, 0, p.w_pre, nullptr, p.d_a, 2 * p.d_t, e, One{})) return;
@@ -2028,7 +2194,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             int lda = 0;
             const float* a = nullptr;
             if (p.head_slotb == 0 && !(TC && p.tc_head)) {
-                a = stage_act<WT>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
+                a = stage_act<WT, TC>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
                 if (!ok) return;
             }
             if (!head_phase<WT, TC>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part, hs)) return;
@@ -2038,6 +2204,9 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         if (p.sampling && !sample_step(p, k, smem, epoch)) return;
     }
     // outputs of the last step
+    if (p.out_conf)
+        for (int b = blockIdx.x * kWarps + (int)(threadIdx.x >> 5); b < p.B; b += gridDim.x * kWarps)
+            write_conf(p, p.N - 1, b);
     if (blockIdx.x == 0) {
         for (int b = threadIdx.x; b < p.B; b += blockDim.x)
             p.out_drafts[(long long)b * p.N + (p.N - 1)] = step_token(p, b, p.N);

@@ -7,17 +7,14 @@
 // to finish (a counter in the workspace header) turns the row argmaxes into
 // the accepted prefix and the bonus token.
 //
-// Exact sampling ("opus-mtp-turbo: Track 1 report", item 4): one cooperative
-// launch with four phases separated by grid barriers:
-//   1. penalised row maxima           (all rows, V split across CTAs)
-//   2. min-p candidate collection     (all rows, V split across CTAs)
-//   3. sort by (p desc, id asc), top-p cut   (one CTA per row)
-//   4. accept / residual / bonus walk        (one warp per sequence)
+// Exact sampling ("opus-mtp-turbo: Track 1 report", item 4): one plain
+// launch over pieces of every target and draft row; one pass over the
+// logits, the rows' finishing CTAs build the kept sets and the sequences'
+// finishing CTAs take the accept / residual / bonus decisions (sample.cuh).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "common.cuh"
-#include "sample.cuh"
 #include "verify.cuh"
 
 namespace mtp {
@@ -92,10 +89,11 @@ __device__ __forceinline__ void chunk_argmax<float>(const float* row, long long 
 
 template <typename T>
 __global__ void __launch_bounds__(256) verify_greedy_kernel(VerifyGreedyArgs a) {
-    const int row = blockIdx.y;                  // b * (1+N) + i
+    const int split = a.split;
+    const int row = (int)(blockIdx.x / (unsigned)split);   // b * (1+N) + i
     const long long V = a.V;
-    const long long chunk = (V + gridDim.x - 1) / gridDim.x;
-    const long long c0 = (long long)blockIdx.x * chunk;
+    const long long chunk = (V + split - 1) / split;
+    const long long c0 = (long long)(blockIdx.x % (unsigned)split) * chunk;
     const long long c1 = c0 + chunk < V ? c0 + chunk : V;
     const T* rowp = reinterpret_cast<const T*>(a.logits) + (long long)row * V;
 
@@ -112,7 +110,7 @@ __global__ void __launch_bounds__(256) verify_greedy_kernel(VerifyGreedyArgs a) 
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = sbest[w] > m ? sbest[w] : m;
         if (c0 < c1) atomicMax(a.amax + row, m);
         __threadfence();
-        const unsigned int total = gridDim.x * gridDim.y;
+        const unsigned int total = gridDim.x;
         s_last = (atomicAdd(&a.hdr->done, 1u) == total - 1u);
     }
     __syncthreads();
@@ -141,65 +139,80 @@ cudaError_t launch_verify_greedy(const VerifyGreedyArgs& a, int ldtype, int num_
     const long long max_split = (a.V + 2047) / 2048;
     if (split > max_split) split = max_split;
     if (split < 1) split = 1;
-    dim3 grid((unsigned)split, (unsigned)rows);
+    VerifyGreedyArgs b = a;
+    b.split = (int)split;
+    const unsigned int grid = (unsigned int)(split * rows);
     if (ldtype == MTP_DTYPE_BF16)
-        verify_greedy_kernel<uint16_t><<<grid, 256, 0, s>>>(a);
+        verify_greedy_kernel<uint16_t><<<grid, 256, 0, s>>>(b);
     else
-        verify_greedy_kernel<float><<<grid, 256, 0, s>>>(a);
+        verify_greedy_kernel<float><<<grid, 256, 0, s>>>(b);
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// exact sampling (device functions in sample.cuh)
+// sampling: exact speculative verification and draft draws (sample.cuh)
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads, 1) verify_sample_kernel(VerifySampleArgs a) {
+constexpr int kSampThreads = 256;
+
+// Persistent over the pieces: CTA c takes pieces c, c + grid, ... and
+// prefetches each next piece into L2 while it works on the current one.
+__global__ void __launch_bounds__(kSampThreads, 3) sample_kernel(const __grid_constant__ SampleJob j) {
     extern __shared__ __align__(16) unsigned char smem[];
-    unsigned int epoch = 0;
-    const int rows = a.B * (a.N + 1) + a.B * a.N;
-    const long long chunks = (a.V + kScanChunk - 1) / kScanChunk;
-    const long long items = (long long)rows * chunks;
-    uint32_t* bits = reinterpret_cast<uint32_t*>(smem);
-    unsigned long long* red64 = reinterpret_cast<unsigned long long*>(smem + kScanChunk / 8);
-    for (int mode = 0; mode < 2; ++mode) {
-        for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-            const int row = (int)(it / chunks);
-            const long long c0 = (it % chunks) * kScanChunk;
-            const long long c1 = c0 + kScanChunk < a.V ? c0 + kScanChunk : a.V;
-            sample_scan_item(a, row, c0, c1, mode, bits, red64);
-        }
-        if (!grid_barrier(a.hdr, epoch, a.timeout_ns, gridDim.x)) return;
+    const long long total = (long long)sample_rows(j) * j.ppr;
+    if (threadIdx.x == 0) prefetch_piece(j, blockIdx.x);
+    for (long long pc = blockIdx.x; pc < total; pc += gridDim.x)
+        sample_piece(j, (int)pc, pc + gridDim.x < total ? pc + gridDim.x : -1, smem);
+}
+
+void sample_piece_plan(long long V, long long rows, int grid, int* ppr, int* piece_len) {
+    long long lo = (V + kPieceMax - 1) / kPieceMax;   // pieces fit the bitmap
+    long long hi = V / 2048 > lo ? V / 2048 : lo;       // pieces of at least ~2K tokens
+    long long want = (2LL * grid + rows - 1) / rows;    // about two pieces per CTA
+    long long n = want < lo ? lo : (want > hi ? hi : want);
+    long long len = (V + n - 1) / n;
+    len = (len + 255) & ~255LL;
+    if (len > kPieceMax) len = kPieceMax;
+    if (len < 256) len = 256;
+    *piece_len = (int)len;
+    *ppr = (int)((V + len - 1) / len);
+}
+
+// The kernel's shared-memory attribute and occupancy, once per device.
+namespace {
+constexpr int kMaxDev = 64;
+int g_samp_ready[kMaxDev] = {0};
+int g_samp_per_sm[kMaxDev] = {0};
+int sample_setup() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return -1;
+    if (!g_samp_ready[dev]) {
+        if (cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSampleSmem) !=
+            cudaSuccess)
+            return -1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sample_kernel, kSampThreads, kSampleSmem) != cudaSuccess)
+            return -1;
+        g_samp_per_sm[dev] = n;
+        g_samp_ready[dev] = 1;
     }
-    unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
-    float* wsh = reinterpret_cast<float*>(smem + kCandCap * sizeof(unsigned long long));
-    for (int row = blockIdx.x; row < rows; row += gridDim.x) sample_sort_row(a, row, keys, wsh);
-    if (!grid_barrier(a.hdr, epoch, a.timeout_ns, gridDim.x)) return;
-    const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
-    for (int b = gw; b < a.B; b += gridDim.x * kWarps) sample_decide(a, b);
+    return dev;
+}
+}  // namespace
+
+cudaError_t launch_sample(const SampleJob& j, int sms, cudaStream_t s) {
+    const int dev = sample_setup();
+    if (dev < 0) return cudaErrorInvalidValue;
+    const long long total = (long long)sample_rows(j) * j.ppr;
+    const long long resident = (long long)(g_samp_per_sm[dev] > 0 ? g_samp_per_sm[dev] : 1) * (sms > 0 ? sms : 1);
+    const unsigned int grid = (unsigned int)(total < resident ? total : resident);
+    sample_kernel<<<grid, kSampThreads, kSampleSmem, s>>>(j);
+    return cudaGetLastError();
 }
 
-size_t verify_sample_smem_bytes() {
-    const size_t scan = kScanChunk / 8 + kWarps * sizeof(unsigned long long);
-    const size_t sort = kCandCap * (sizeof(unsigned long long) + sizeof(float));
-    return scan > sort ? scan : sort;
-}
-
-cudaError_t launch_verify_sample(const VerifySampleArgs& a, int grid, cudaStream_t s) {
-    const size_t smem = verify_sample_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(verify_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    VerifySampleArgs copy = a;
-    void* args[] = {&copy};
-    return cudaLaunchCooperativeKernel((const void*)verify_sample_kernel, dim3(grid), dim3(kThreads), args, smem, s);
-}
-
-int verify_sample_max_grid(int num_sms) {
-    int per_sm = 0;
-    const size_t smem = verify_sample_smem_bytes();
-    cudaFuncSetAttribute(verify_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_sample_kernel, kThreads, smem) != cudaSuccess)
-        return 0;
-    return per_sm * num_sms;
+int sample_blocks_per_sm() {
+    const int dev = sample_setup();
+    return dev < 0 ? 0 : g_samp_per_sm[dev];
 }
 
 }  // namespace mtp

@@ -37,23 +37,33 @@ class DeviceDraft:
     d_t: int
     ws: object
 
-    def run(self, out_drafts, out_h_last=None, out_logits=None, sample=None, seed=0, offset=0, stream=None):
+    def run(self, out_drafts, out_h_last=None, out_logits=None, sample=None, seed=0, offset=0, stream=None,
+            out_conf=None):
         draft_block(self.cfg, self.weights, self.views, self.kv_len, self.last_tok, self.h_prev, out_drafts,
                     self.ws, out_h_last=out_h_last, out_logits=out_logits, sample=sample, seed=seed,
-                    offset=offset, hist=self.hist if sample is not None else None, stream=stream)
+                    offset=offset, hist=self.hist if sample is not None else None, stream=stream,
+                    out_conf=out_conf)
 
 
-def upload_draft(w, device="cuda", extra_ws_for=None) -> DeviceDraft:
+def upload_draft(w, device="cuda", extra_ws_for=None, reuse: "DeviceDraft | None" = None) -> DeviceDraft:
     """Upload a ``synth.DraftWorkload`` (or anything with the same fields).
 
     ``extra_ws_for`` = (B, N, V) of verify calls that will share the workspace.
+    ``reuse``: an earlier upload of the same model whose weight tensors are
+    shared instead of uploaded again (its views and workspace are not).
     """
     import torch
     m = w.model
     cfg = make_config(m.d_t, m.d_a, m.n_blocks, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff, m.vocab,
                       wdtype=m.dtype, rms_eps=m.rms_eps, attn_scale=m.attn_scale, emb_scale=m.emb_scale,
                       logit_softcap=m.logit_softcap)
-    tensors = {n: to_device(a, device=device) for n, a in w.weights.items()}
+    same = (reuse is not None and bytes(reuse.cfg) == bytes(cfg) and
+            all(n in reuse.tensors and tuple(reuse.tensors[n].shape) == a.shape for n, a in w.weights.items()))
+    if same:
+        tensors = {n: reuse.tensors[n] for n in w.weights}
+        reuse.tensors.pop("_views", None)   # the old views go with the old workload
+    else:
+        tensors = {n: to_device(a, device=device) for n, a in w.weights.items()}
     views, keep = [], []
     for vd in w.views:
         k, v = to_device(vd["k"], device=device), to_device(vd["v"], device=device)

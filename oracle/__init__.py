@@ -84,10 +84,14 @@ def _declare(L):
     L.orc_pick.restype = C.c_int32
     L.orc_draft_step.argtypes = [P, P, P, P, I, I, P, I, P, P, P, P]
     L.orc_draft_step.restype = I
-    L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, I, P, I, P, P, P, P, P]
+    L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, I, P, I, P, P, P, P, P, P]
+    L.orc_top1_prob.argtypes = [P, C.c_int64]
+    L.orc_top1_prob.restype = D
     L.orc_draft_block.restype = I
     L.orc_verify_greedy.argtypes = [P, I, I, I, I, P, P, P]
     L.orc_verify_sample.argtypes = [P, P, I, I, I, I, P, P, I, P, U64, U64, P, P, P]
+    L.orc_sample_drafts.argtypes = [P, I, I, I, I, P, I, P, U64, U64, P, P]
+    L.orc_set_threads.argtypes = [I]
     L.orc_num_threads.restype = I
 
 
@@ -97,6 +101,11 @@ def _p(a):
 
 def num_threads() -> int:
     return int(lib().orc_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on (the CPU baseline's single-core run)."""
+    lib().orc_set_threads(int(n))
 
 
 # ----------------------------------------------------------------------------
@@ -179,6 +188,12 @@ def sample_dist(z, pen, sp):
     return ids[:n].copy(), w[:n].copy(), ws.value, mg.value
 
 
+def top1_prob(z):
+    """The softmax probability of the largest logit (NaN entries left out)."""
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    return float(lib().orc_top1_prob(_p(z), z.size))
+
+
 def pick(ids, w, wsum, u):
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     w = np.ascontiguousarray(w, dtype=np.float64)
@@ -235,7 +250,8 @@ def draft_block(w, sample=None, seed=0, offset=0, force=None, seqs=None, want_lo
     ``force`` ([B, N] int32, optional) teacher-forces the token consumed at
     step k+1 to force[b, k] instead of the oracle's own pick.
     Returns dict(drafts [S,N] int32, h_last [S,d_t] f64, logits [S,N,V] f64 or
-    None, margin [S,N] f64) for the S selected sequences, in ``seqs`` order.
+    None, margin [S,N] f64, conf [S,N] f64: each step's top-1 softmax
+    probability) for the S selected sequences, in ``seqs`` order.
     """
     L = lib()
     m = w.model
@@ -245,6 +261,7 @@ def draft_block(w, sample=None, seed=0, offset=0, force=None, seqs=None, want_lo
     out_h = np.empty((S, m.d_t), dtype=np.float64)
     out_z = np.empty((S, N, V), dtype=np.float64) if want_logits else None
     out_m = np.empty((S, N), dtype=np.float64)
+    out_c = np.empty((S, N), dtype=np.float64)
     prm = make_params(sample) if sample is not None else None
     for j, b in enumerate(seqs):
         bd = _Bound(w, b)
@@ -253,16 +270,17 @@ def draft_block(w, sample=None, seed=0, offset=0, force=None, seqs=None, want_lo
         h = np.empty((1, m.d_t), dtype=np.float64)
         z = np.empty((1, N, V), dtype=np.float64) if want_logits else None
         mg = np.empty((1, N), dtype=np.float64)
+        cf = np.empty((1, N), dtype=np.float64)
         rc = L.orc_draft_block(C.byref(bd.model), bd.tensors, _p(bd.block_view), bd.views, bd.n_views,
                                1, N, _p(bd.kv_len), _p(bd.last_tok), _p(bd.h_prev),
                                C.byref(prm) if prm is not None else None, seed, offset, b,
-                               _p(bd.hist), bd.hist.shape[1], _p(f), _p(d), _p(h), _p(z), _p(mg))
+                               _p(bd.hist), bd.hist.shape[1], _p(f), _p(d), _p(h), _p(z), _p(mg), _p(cf))
         if rc != 0:
             raise ValueError(f"oracle draft block rejected its inputs (rc={rc})")
-        out_d[j], out_h[j], out_m[j] = d[0], h[0], mg[0]
+        out_d[j], out_h[j], out_m[j], out_c[j] = d[0], h[0], mg[0], cf[0]
         if want_logits:
             out_z[j] = z[0]
-    return dict(drafts=out_d, h_last=out_h, logits=out_z, margin=out_m)
+    return dict(drafts=out_d, h_last=out_h, logits=out_z, margin=out_m, conf=out_c)
 
 
 def draft_step(w, b, step, tok, h_prev):
@@ -314,9 +332,17 @@ def verify_sample(target, draft, dtype, drafts, hist, params, seed, offset):
     return out, n_acc, mg
 
 
-def exp_cw(x):
-    """The sampler's fp32 exp (see orc_exp_cw)."""
-    L = lib()
-    L.orc_exp_cw.argtypes = [C.c_float]
-    L.orc_exp_cw.restype = C.c_float
-    return np.array([L.orc_exp_cw(float(v)) for v in np.ravel(x)], dtype=np.float32).reshape(np.shape(x))
+def sample_drafts(draft, dtype, hist, params, seed, offset):
+    """Draws of a sampling drafter: drafts[b, i] ~ sample_dist(draft row (b, i)) with
+    penalty set hist[b] + drafts[b, :i] and the uniform of (b, i, purpose 0).
+    Returns (drafts [B, N] int32, margin [B])."""
+    draft = np.ascontiguousarray(draft)
+    hist = np.ascontiguousarray(hist, dtype=np.int32)
+    B, N, V = draft.shape
+    H = hist.shape[1] if hist.ndim == 2 else 0
+    out = np.empty((B, N), dtype=np.int32)
+    mg = np.empty(B, dtype=np.float64)
+    prm = make_params(params)
+    lib().orc_sample_drafts(_p(draft), 1 if dtype == "bf16" else 0, B, N, V, _p(hist), H, C.byref(prm),
+                            seed, offset, _p(out), _p(mg))
+    return out, mg

@@ -233,42 +233,16 @@ double orc_uniform(uint64_t seed, uint64_t offset, uint32_t b, uint32_t i, uint3
 /* sample_dist [SP item 4]                                                   */
 /*                                                                          */
 /* The sampler's arithmetic decides integers (kept sets, orders, picks), so */
-/* it is carried out in the kernel's precision, IEEE fp32, with every       */
-/* rounding step written out: penalties, temperature, weights, and every   */
-/* sum taken sequentially in the documented order.  Given the same fp32     */
-/* inputs, any IEEE fp32 implementation of these steps takes the same       */
-/* decisions.                                                               */
+/* it is carried out in IEEE fp32 with every rounding step written out:     */
+/* penalties, temperature, the difference l - lmax, and every sum taken     */
+/* sequentially in the documented order.  A weight is exp(l - lmax) rounded */
+/* once to fp32: libm's exp in fp64, then one conversion.  Any other        */
+/* implementation whose weights are the correctly rounded exp takes the     */
+/* same decisions; one whose exp is off by an ulp may differ only where a   */
+/* decision lies within about 1e-6 of its threshold, which *margin reports. */
 /* ------------------------------------------------------------------------ */
 
-/* exp(x) for x <= 0 in fp32 (Cody and Waite, "Software Manual for the
- * Elementary Functions", 1980: argument reduction x = k ln2 + r with ln2 split
- * into a 16-bit head and a tail so that k * head is exact; exp(r) on
- * |r| <= ln2 / 2 by its Taylor series through r^7, Horner with fused
- * multiply-adds; the result scaled by 2^k).  Returns 0 below -87. */
-float orc_exp_cw(float x) {
-    if (!(x >= -87.0f)) return 0.0f;
-    const float ln2_hi = 0.693145751953125f;        /* 45426 / 2^16 */
-    const float ln2_lo = 1.42860682030941723e-06f;  /* ln 2 - ln2_hi */
-    const float log2e = 1.44269504088896341f;
-    const float k = rintf(x * log2e);
-    float r = fmaf(-k, ln2_hi, x);
-    r = fmaf(-k, ln2_lo, r);
-    float q = 1.0f / 5040.0f;
-    q = fmaf(q, r, 1.0f / 720.0f);
-    q = fmaf(q, r, 1.0f / 120.0f);
-    q = fmaf(q, r, 1.0f / 24.0f);
-    q = fmaf(q, r, 1.0f / 6.0f);
-    q = fmaf(q, r, 0.5f);
-    q = fmaf(q, r, 1.0f);
-    q = fmaf(q, r, 1.0f);
-    const int ki = (int)k;                          /* -126 <= ki <= 0 here */
-    uint32_t bits = (uint32_t)(ki + 127) << 23;
-    float scale;
-    memcpy(&scale, &bits, sizeof scale);
-    return q * scale;
-}
-
-typedef struct { int id; float w; } cand;
+typedef struct { int id; float w; float l; } cand;
 
 static int cand_cmp(const void *a, const void *b) {   /* weight desc, id asc */
     const cand *x = (const cand *)a, *y = (const cand *)b;
@@ -333,17 +307,22 @@ int orc_sample_dist_f32(const double *z, int V, const int32_t *pen, int n_pen, c
     int n = 0;
     for (int x = 0; x < V; ++x) {
         if (!alive[x]) continue;
-        const float wx = orc_exp_cw(l[x] - lmax);
+        const float d = l[x] - lmax;
+        const float wx = (float)exp((double)d);
         if (min_p > 0.0f) {
-            double d = rel_gap(wx, min_p, min_p);
-            if (d > 0.0 && d < mg) mg = d;
+            double dd = rel_gap(wx, min_p, min_p);
+            if (dd < mg) mg = dd;
         }
-        if (wx >= min_p) { c[n].id = x; c[n].w = wx; ++n; }
+        if (wx >= min_p) { c[n].id = x; c[n].w = wx; c[n].l = l[x]; ++n; }
     }
     qsort(c, (size_t)n, sizeof(cand), cand_cmp);
+    /* order margins: equal weights of equal scaled logits are ordered by id
+     * on any implementation; equal weights of different logits, or nearly
+     * equal weights, could swap under another exp */
     for (int j = 1; j < n; ++j) {
+        if (c[j - 1].l == c[j].l) continue;
         double d = rel_gap(c[j - 1].w, c[j].w, c[j - 1].w);
-        if (d > 0.0 && d < mg) mg = d;
+        if (d < mg) mg = d;
     }
     if (top_p < 1.0f && n > 0) {
         float tot = 0.0f;
@@ -354,7 +333,7 @@ int orc_sample_dist_f32(const double *z, int V, const int32_t *pen, int n_pen, c
             cum += c[j].w;
             const float share = cum / tot;
             double d = fabs((double)share - (double)top_p);
-            if (d > 0.0 && d < mg) mg = d;
+            if (d < mg) mg = d;
             if (share >= top_p) { keep = j + 1; break; }
         }
         n = keep;
@@ -487,6 +466,20 @@ int orc_draft_step(const orc_model *m, const void *const *t, const int32_t *bloc
     return 0;
 }
 
+/* Confidence of a draft step ("MTP decoding (--mtp)", "Stopping early when the
+ * head is unsure": the draft loop's confidence in the token it proposes, the
+ * probability of the top candidate): the softmax probability of the largest
+ * logit, 1 / sum_v exp(z_v - z_max), over the step's logits z (after the
+ * softcap), NaN entries left out. */
+double orc_top1_prob(const double *z, int64_t n) {
+    double zm = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) if (!isnan(z[i]) && z[i] > zm) zm = z[i];
+    if (!(zm > -INFINITY)) return 0.0;
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) if (!isnan(z[i])) s += exp(z[i] - zm);
+    return 1.0 / s;
+}
+
 /* N chained draft steps with the token chosen on "device" each step ([G4]
  * sec. 4 item 8; [FN] the fused chain: argmax -> embed -> h chain).
  *   sp == NULL or sp->temp <= 0: greedy (argmax).  Otherwise the token of
@@ -495,13 +488,14 @@ int orc_draft_step(const orc_model *m, const void *const *t, const int32_t *bloc
  *   the batch index of row 0 when the rows are a slice of a larger batch.
  * Outputs drafts [B, N], h_last [B, d_t] (optional), logits [B, N, V]
  * (optional), margin [B, N] (optional: top1 - top2 logit gap of each greedy
- * step, or the sampling decision's relative margin). */
+ * step, or the sampling decision's relative margin), conf [B, N] (optional:
+ * the step's confidence, see orc_top1_prob). */
 int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *block_view,
                     const orc_view *views, int n_views, int B, int N, const int32_t *kv_len,
                     const int32_t *last_tok, const float *h_prev, const orc_sample_params *sp,
                     uint64_t seed, uint64_t offset, int seq0, const int32_t *hist, int H,
                     const int32_t *force_tok, int32_t *drafts, double *h_last, double *logits,
-                    double *margin) {
+                    double *margin, double *conf) {
     const int d_t = m->d_t, V = m->vocab;
     double *h = malloc(sizeof(double) * (size_t)B * d_t), *hn = malloc(sizeof(double) * (size_t)B * d_t);
     double *z = malloc(sizeof(double) * (size_t)B * V);
@@ -537,6 +531,7 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
                 mg = m1 < m2 ? m1 : m2;
             }
             if (margin) margin[(size_t)b * N + k] = mg;
+            if (conf) conf[(size_t)b * N + k] = orc_top1_prob(zb, V);
             if (logits) memcpy(logits + ((size_t)b * N + k) * V, zb, sizeof(double) * (size_t)V);
             drafts[(size_t)b * N + k] = pick;
             tok[b] = force_tok ? force_tok[(size_t)b * N + k] : pick;
@@ -656,6 +651,53 @@ void orc_verify_sample(const void *tgt, const void *dft, int bf16, int B, int N,
         }
         free(z); free(pid); free(qid); free(pw); free(qw); free(r); free(pen);
     }
+}
+
+/* Draws of a sampling drafter ([SP] item 4: the drafted token of row i is a
+ * draw from q_i = sample_dist(draft row i)).  For sequence b and row i in
+ * order: q_i = sample_dist(dft row (b, i)) with penalty set hist[b] u
+ * drafts[b][0..i-1], and drafts[b][i] = the inverse-CDF pick of q_i with the
+ * uniform of (b, i, purpose 0).  dft [B, N, V] (bf16 bits or fp32); hist
+ * [B, H]; drafts [B, N] out; margin[b] (optional) the smallest relative
+ * distance of any of the sequence's decisions to its threshold. */
+void orc_sample_drafts(const void *dft, int bf16, int B, int N, int V, const int32_t *hist, int H,
+                       const orc_sample_params *sp, uint64_t seed, uint64_t offset, int32_t *drafts,
+                       double *margin) {
+#pragma omp parallel
+    {
+        double *z = malloc(sizeof(double) * (size_t)V);
+        int32_t *ids = malloc(sizeof(int32_t) * (size_t)V);
+        float *w = malloc(sizeof(float) * (size_t)V);
+        int32_t *pen = malloc(sizeof(int32_t) * (size_t)(H + N + 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b) {
+            double mg = INFINITY, m1, m2;
+            int np = 0;
+            for (int j = 0; j < H; ++j) pen[np++] = hist[(size_t)b * H + j];
+            for (int i = 0; i < N; ++i) {
+                const int64_t row = ((int64_t)b * N + i) * V;
+                for (int v = 0; v < V; ++v) z[v] = elem(dft, row + v, bf16);
+                float ws;
+                const int n = orc_sample_dist_f32(z, V, pen, np, sp, ids, w, &ws, &m1);
+                const float u = (float)orc_uniform(seed, offset, (uint32_t)b, (uint32_t)i, 0u);
+                const int32_t d = orc_pick_f32(ids, w, n, ws, u, &m2);
+                if (m1 < mg) mg = m1;
+                if (m2 < mg) mg = m2;
+                drafts[(size_t)b * N + i] = d;
+                pen[np++] = d;
+            }
+            if (margin) margin[b] = mg;
+        }
+        free(z); free(ids); free(w); free(pen);
+    }
+}
+
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
 }
 
 int orc_num_threads(void) {

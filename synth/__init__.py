@@ -408,11 +408,11 @@ class VerifySampleInputs:
     target: np.ndarray   # [B, 1+N, V] (bf16 bits or fp32)
     draft: np.ndarray    # [B, N, V]
     dtype: str
-    drafts: np.ndarray   # int32 [B, N]
     hist: np.ndarray     # int32 [B, H]; newest token last
     params: SampleParams
     seed: int
     offset: int
+    drafts: np.ndarray | None = None   # int32 [B, N]: filled in by the caller's drafter
 
 
 def make_verify_sample_inputs(seed: int | None = None, B: int = 32, N: int = 3, V: int = 248320,
@@ -421,16 +421,15 @@ def make_verify_sample_inputs(seed: int | None = None, B: int = 32, N: int = 3, 
                               ) -> VerifySampleInputs:
     """Target logits ~N(0, std^2); draft logits rho-correlated with the target rows.
 
-    The drafted token of row i is the draft row's largest logit (a deterministic
-    drafter, the case the temp > 0 audit page treats).
+    The drafted tokens are not part of these inputs: a sampling drafter draws
+    them from its own distribution q_i = sample_dist(draft row i), which is
+    arithmetic of the method, so the caller fills ``drafts`` in (the oracle's
+    draws in the tests, the library's on the GPU).
     """
     seed = workload_seed(4) if seed is None else seed
     tgt = normal(seed, "vs.target", (B, N + 1, V), std=std)
     eps = normal(seed, "vs.eps", (B, N, V), std=std)
     dft = (np.float32(rho) * tgt[:, :N, :] + np.float32(math.sqrt(1 - rho * rho)) * eps)
     tgt_s, dft_s = _as_dtype(tgt, dtype), _as_dtype(dft, dtype)
-    dvals = bf16_bits_to_f32(dft_s) if dtype == "bf16" else dft_s
-    drafts = np.argmax(dvals, axis=2).astype(np.int32)
     hist = uniform_int(seed, "vs.hist", (B, H), 0, V)
-    return VerifySampleInputs(tgt_s, dft_s, dtype, drafts, hist,
-                              params or SampleParams(), seed=seed, offset=0)
+    return VerifySampleInputs(tgt_s, dft_s, dtype, hist, params or SampleParams(), seed=seed, offset=0)

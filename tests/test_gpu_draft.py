@@ -105,19 +105,36 @@ def test_workload1_gemma_b1():
     check_draft_parity(w, d, h, z, seqs=[0])
 
 
+# Sequences of a 64-row batch spread over the tensor-core LM head's four
+# epilogue warps: accumulator row b sits in lane b % 16 of warp b / 16.
+SPREAD64 = [16 * q + i for q in range(4) for i in (0, 5, 10, 15)]
+
+
 @pytest.mark.slow
-def test_workload2_ragged_b16_sampled_sequences():
+def test_workload2_ragged_b16_every_sequence():
     w = synth.make_draft_inputs(2)
     _, d, h, z = run_gpu_draft(w)
-    shortest, longest = int(np.argmin(w.kv_len)), int(np.argmax(w.kv_len))
-    check_draft_parity(w, d, h, z, seqs=sorted({shortest, longest, 7}))
+    check_draft_parity(w, d, h, z, seqs=range(w.B))
 
 
 @pytest.mark.slow
-def test_workload3_b64_sampled_sequences():
+def test_workload3_b64_spread_sequences():
     w = synth.make_draft_inputs(3)
     _, d, h, z = run_gpu_draft(w)
-    check_draft_parity(w, d, h, z, seqs=[0, 63])
+    check_draft_parity(w, d, h, z, seqs=SPREAD64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_timed_path_without_logits(cfg):
+    """The configuration the benchmark times (no logits output) gives the
+    same drafts and h_last, bit for bit, as the run that stores the logits,
+    and matches the oracle."""
+    w = synth.make_draft_inputs(cfg)
+    dev, d0, h0, _ = run_gpu_draft(w, want_logits=False)
+    _, d1, h1, z1 = run_gpu_draft(w, dev=dev)
+    assert np.array_equal(d0, d1) and np.array_equal(h0, h1)
+    check_draft_parity(w, d0, h0, None, seqs=[0] if w.B == 1 else SPREAD64[::2])
 
 
 # ----------------------------------------------------------------------------
@@ -201,3 +218,78 @@ def test_workload1_sampled():
     w = synth.make_draft_inputs(1)
     d, h, z = run_sampled(w, seed=5, offset=0)
     check_sampled(w, 5, 0, d, h, z, seqs=[0])
+
+
+# ----------------------------------------------------------------------------
+# per-step confidence output ("MTP decoding (--mtp)", "Stopping early when the
+# head is unsure"): the top-1 softmax probability of each step's logits
+# ----------------------------------------------------------------------------
+
+def run_conf(w, sample=None):
+    import torch
+    from mtp_speculative_decoding_gb300.device import upload_draft
+    import mtp_speculative_decoding_gb300 as mtp
+    dev = upload_draft(w)
+    B, N, V = w.B, w.N, w.model.vocab
+    drafts = torch.full((B, N), -7, dtype=torch.int32, device="cuda")
+    conf = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
+    logits = torch.full((B, N, V), float("nan"), dtype=torch.float32, device="cuda")
+    kw = {}
+    if sample is not None:
+        kw = dict(sample=(SP.temp, SP.top_p, SP.min_p, SP.rep_penalty, SP.presence_penalty, SP.top_k), seed=3)
+    dev.run(drafts, out_logits=logits, out_conf=conf, **kw)
+    torch.cuda.synchronize()
+    assert mtp.last_error(dev.ws) == 0
+    # the confidence output leaves the drafts unchanged
+    d2 = torch.full((B, N), -7, dtype=torch.int32, device="cuda")
+    dev.run(d2, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(drafts, d2)
+    return drafts.cpu().numpy(), conf.cpu().numpy(), logits.cpu().numpy()
+
+
+def check_conf(w, d, c, z, seqs, sample=None):
+    """The reduction is checked against the GPU's own logits: the softmax
+    probability of their largest entry, within 1e-4 (relative; fp32 sums
+    over the vocabulary).  Against the oracle's top-1 probability of the same
+    step (the oracle follows the GPU's tokens) the bound is the logits' own:
+    1e-3 with fp32 weights; 1e-2 with bf16 weights, since the batched head
+    multiplies bf16(h) and every logit moves by up to ~2^-8 of its size."""
+    import oracle
+    tol = 1e-3 if w.model.dtype == "f32" else 1e-2
+    ref = oracle.draft_block(w, sample=sample, seed=3, seqs=seqs, force=d, want_logits=False)
+    for j, b in enumerate(seqs):
+        for k in range(w.N):
+            own = oracle.top1_prob(z[b, k].astype(np.float64))
+            assert abs(c[b, k] - own) <= 1e-4 * own, f"b={b} k={k}: conf {c[b, k]} vs its logits' {own}"
+            o = ref["conf"][j, k]
+            assert abs(c[b, k] - o) <= tol * o, f"b={b} k={k}: conf {c[b, k]} vs oracle {o}"
+
+
+@pytest.mark.parametrize("dtype,B", [("f32", 3), ("bf16", 3), ("bf16", 1)])
+def test_confidence_small(dtype, B):
+    """CUDA-core heads: the generic GEMV head (B = 3) and the single-sequence
+    bulk-copy head (B = 1)."""
+    w = small_workload(dtype, B=B, kv=(37, 23, 100)[:B], V=3001, softcap=4.0)
+    d, c, z = run_conf(w)
+    check_conf(w, d, c, z, range(B))
+
+
+def test_confidence_tensor_core_head_sampled():
+    """The tensor-core head (B = 9) with sampled drafting: the confidence is
+    the top-1 probability of the raw logits either way."""
+    m = synth.ModelSpec(d_t=1024, d_a=256, n_blocks=1, n_q_heads=4, head_dim=64, n_kv_heads=1, d_ff=512,
+                        vocab=3001, dtype="bf16", block_view=(0,))
+    views = [synth.ViewSpec(cap=96, window=0, rope_theta=1e6)]
+    kv = np.random.default_rng(5).integers(1, 97, size=9)
+    w = synth.make_draft_workload("conf_tc", m, views, 9, 2, kv, 17, hist_len=4)
+    d, c, z = run_conf(w, sample=SP)
+    check_conf(w, d, c, z, range(9), sample=SP)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [1, 3])
+def test_confidence_workloads(cfg):
+    w = synth.make_draft_inputs(cfg)
+    d, c, z = run_conf(w)
+    check_conf(w, d, c, z, [0] if w.B == 1 else SPREAD64[::4])

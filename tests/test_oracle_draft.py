@@ -157,3 +157,35 @@ def test_step_position_is_kv_len_plus_step():
     for step, z in ((0, z0), (1, z1)):
         _, rz = torch_step(w, 0, step, 3, h)
         assert np.allclose(z, rz, rtol=1e-10, atol=1e-10)
+
+
+# ----------------------------------------------------------------------------
+# the per-step confidence ("MTP decoding (--mtp)", "Stopping early when the
+# head is unsure"): the top-1 softmax probability of the step's logits
+# ----------------------------------------------------------------------------
+
+def test_top1_prob_closed_forms():
+    import math
+    assert abs(oracle.top1_prob(np.zeros(4096)) - 1.0 / 4096) < 1e-15
+    a, n = 3.0, 1000
+    z = np.zeros(n)
+    z[17] = a
+    assert abs(oracle.top1_prob(z) - math.exp(a) / (math.exp(a) + n - 1)) < 1e-15
+    assert abs(oracle.top1_prob(np.array([2.0, 2.0, -np.inf])) - 0.5) < 1e-15
+    assert abs(oracle.top1_prob(np.array([1.0, np.nan, 1.0])) - 0.5) < 1e-15
+
+
+def test_top1_prob_is_softmax_max():
+    from scipy.special import softmax
+    rng = np.random.default_rng(4)
+    for scale in (0.1, 1.0, 5.0):
+        z = scale * rng.standard_normal(3001)
+        assert abs(oracle.top1_prob(z) - softmax(z).max()) < 1e-12
+
+
+def test_draft_block_confidence_matches_its_logits():
+    w = synth.make_draft_inputs(0)
+    ref = oracle.draft_block(w)
+    for k in range(w.N):
+        assert ref["conf"][0, k] == oracle.top1_prob(ref["logits"][0, k])
+        assert 1.0 / w.model.vocab <= ref["conf"][0, k] <= 1.0

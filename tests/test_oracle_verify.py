@@ -279,8 +279,10 @@ def _draw(toy, ctxs, which, rng):
     return out
 
 
-def _speculate(toy, h0, S, N, rng, seed, rule="exact", greedy_drafter=False):
-    """Generate 3 tokens per sequence by rounds of N drafts + verify."""
+def _speculate(toy, h0, S, N, rng, seed, rule="exact", greedy_drafter=False, verify=None):
+    """Generate 3 tokens per sequence by rounds of N drafts + verify (the
+    oracle's exact verifier unless `verify` is given, with its signature)."""
+    verify = verify or oracle.verify_sample
     gen = [[] for _ in range(S)]
     rnd = 0
     tokens_per_round = []
@@ -315,7 +317,7 @@ def _speculate(toy, h0, S, N, rng, seed, rule="exact", greedy_drafter=False):
                     dft[j, i] = toy.z_draft(full[:len(c) + i])
             hist[j, H - len(c):] = c
         if rule == "exact":
-            out, n, _ = oracle.verify_sample(tgt, dft, "f32", drafts, hist, toy.sp, seed, rnd)
+            out, n, _ = verify(tgt, dft, "f32", drafts, hist, toy.sp, seed, rnd)
         else:
             # the old rule: keep drafts while they equal the unpenalised target argmax,
             # then sample the stop row from the penalised target distribution
@@ -395,16 +397,74 @@ def test_monte_carlo_tv_deterministic_drafter():
     assert 1.0 < tpr <= 3.0
 
 
-def test_sampler_exp_accuracy_and_exact_points():
-    """The sampler's fp32 exp (Cody-Waite reduction + Taylor polynomial) is
-    within 2 ulp of exp over [-87, 0], exact at 0, monotone, and 0 below -87."""
-    x = np.concatenate([np.linspace(-87.0, 0.0, 200001, dtype=np.float32),
-                        -np.logspace(-8, 1.9, 4001).astype(np.float32)])
-    got = oracle.exp_cw(x).astype(np.float64)
-    ref = np.exp(x.astype(np.float64))
-    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
-    assert np.max(np.abs(got - ref) / ulp) <= 2.0
-    assert oracle.exp_cw(np.float32(0.0)) == 1.0
-    xs = np.sort(x)
-    assert np.all(np.diff(oracle.exp_cw(xs).astype(np.float64)) >= 0)
-    assert oracle.exp_cw(np.float32(-87.5)) == 0.0
+# ----------------------------------------------------------------------------
+# the sampling drafter's draws
+# ----------------------------------------------------------------------------
+
+def test_sample_drafts_min_p_one_is_penalised_argmax_chain():
+    """min-p 1 keeps only the largest penalised logit, so every draw is the
+    row's argmax after penalties over the history and the earlier draws."""
+    rng = np.random.default_rng(7)
+    B, N, V = 6, 4, 50
+    dft = rng.standard_normal((B, N, V)).astype(np.float32)
+    hist = rng.integers(0, V, size=(B, 5)).astype(np.int32)
+    # make the raw argmax of every row a penalised token, so penalties matter
+    for b in range(B):
+        for i in range(N):
+            dft[b, i, hist[b, 0]] = 10.0
+            dft[b, i, (hist[b, 0] + 1) % V] = 9.5
+    sp = P(min_p=1.0, temp=0.9, rep_penalty=2.0)
+    d, _ = oracle.sample_drafts(dft, "f32", hist, sp, 3, 0)
+    for b in range(B):
+        pen = set(int(x) for x in hist[b])
+        for i in range(N):
+            l = dft[b, i].astype(np.float64).copy()
+            for x in pen:
+                l[x] = l[x] / 2.0 if l[x] > 0 else l[x] * 2.0
+            assert d[b, i] == int(np.argmax(l))
+            pen.add(int(d[b, i]))
+
+
+def test_sample_drafts_are_picks_of_their_rows():
+    """Each draw is the inverse-CDF pick of sample_dist of its row with the
+    penalty set grown by the earlier draws and the uniform of (b, i, 0)."""
+    rng = np.random.default_rng(8)
+    B, N, V = 5, 3, 300
+    dft = (2 * rng.standard_normal((B, N, V))).astype(np.float32)
+    hist = rng.integers(0, V, size=(B, 9)).astype(np.int32)
+    sp = P(temp=0.6, top_p=0.95, min_p=0.05, rep_penalty=1.08)
+    d, _ = oracle.sample_drafts(dft, "f32", hist, sp, 12, 34)
+    for b in range(B):
+        pen = list(hist[b])
+        for i in range(N):
+            ids, w, ws, _ = oracle.sample_dist(dft[b, i].astype(np.float64), pen, sp)
+            u = oracle.uniform(12, 34, b, i, 0)
+            assert d[b, i] == oracle.pick(ids, w, ws, u)[0]
+            pen.append(int(d[b, i]))
+
+
+def test_sample_drafts_follow_q():
+    """Over many offsets the first draw's frequencies match q_0 (chi-square)."""
+    from scipy.stats import chisquare
+    z = np.array([[[1.0, 0.3, -0.2, 0.8, -1.5, 0.0, 0.5]]], dtype=np.float32)
+    sp = P(temp=0.8, top_p=0.97, min_p=0.02, rep_penalty=1.0)
+    ids, w, ws, _ = oracle.sample_dist(z[0, 0].astype(np.float64), [], sp)
+    q = np.zeros(7)
+    q[ids] = np.asarray(w) / ws
+    T = 20000
+    zz = np.repeat(z, T, axis=0)
+    d, _ = oracle.sample_drafts(zz, "f32", np.zeros((T, 0), dtype=np.int32), sp, 5, 0)
+    cnt = np.bincount(d[:, 0], minlength=7)
+    keep = q > 0
+    assert np.all(cnt[~keep] == 0)
+    exp_ = q[keep] * cnt[keep].sum() / q[keep].sum()
+    assert chisquare(cnt[keep], exp_).pvalue > 1e-3
+
+
+def test_exact_min_p_boundary_has_zero_margin():
+    """A weight exactly at the min-p cut is kept (w >= min_p) and reported
+    with margin 0: another exp could round it to either side."""
+    l1 = np.float32(-0.6931472)
+    mp = float(np.float32(np.exp(np.float64(l1))))
+    ids, w, ws, mg = oracle.sample_dist(np.array([0.0, float(l1), -3.0]), [], P(min_p=mp))
+    assert list(ids) == [0, 1] and mg == 0.0
