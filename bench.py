@@ -114,8 +114,7 @@ def kv_bytes_per_step(w) -> int:
     for vi in used:
         vd = w.views[vi]
         for b in range(w.B):
-            L = int(w.kv_len[b])
-            n = min(L, vd["window"]) if vd["window"] > 0 else L
+            n = len(synth.view_positions(vd["window"], int(w.kv_len[b]), vd.get("sink", 0)))
             tot += 2 * n * m.n_kv_heads * m.head_dim * esz
     return tot
 
@@ -133,8 +132,7 @@ def draft_flops_per_launch(w) -> float:
     for l in range(m.n_blocks):
         vd = w.views[m.block_view[l]]
         for b in range(w.B):
-            L = int(w.kv_len[b])
-            n = min(L, vd["window"]) if vd["window"] > 0 else L
+            n = len(synth.view_positions(vd["window"], int(w.kv_len[b]), vd.get("sink", 0)))
             attn += 4 * m.n_q_heads * m.head_dim * n
     return float(w.N * (2 * m.params() * w.B + attn))
 

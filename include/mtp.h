@@ -119,18 +119,22 @@ typedef struct mtp_weights {
 
 /* A read-only view of one target KV layer ([G4] sec. 5).  K and V share the
  * layout: element (b, kv head g, slot s, d) at b*stride_b + g*stride_h +
- * s*stride_t + d (elements of `wdtype`; d contiguous).  The view is a ring of
- * `cap` slots: position t lives in slot t % cap.  window == 0 reads positions
- * [0, kv_len[b]) (requires kv_len[b] <= cap); window W > 0 reads the last W
- * positions [max(0, kv_len[b] - W), kv_len[b]) (requires W <= cap).  K is
- * stored after RoPE; V is used as stored.  rope_theta is the RoPE base of the
- * target layer type (applied to the drafter's queries). */
+ * s*stride_t + d (elements of `wdtype`; d contiguous).  window == 0 reads
+ * positions [0, kv_len[b]) (requires kv_len[b] <= cap, sink == 0); window
+ * W > 0 reads the last W positions [lo, kv_len[b]), lo = max(0, kv_len[b] - W),
+ * plus the attention sink [0, min(sink, lo)) ("opus-mtp-turbo: Track 1
+ * report", item 2: the draft attention reads the first `sink` cells and the
+ * window).  Storage: position t lives in slot t for t < sink and in slot
+ * sink + (t - sink) % (cap - sink) from there on (a ring of `cap` slots when
+ * sink == 0); requires W + sink <= cap.  K is stored after RoPE; V is used as
+ * stored.  rope_theta is the RoPE base of the target layer type (applied to
+ * the drafter's queries). */
 typedef struct mtp_kv_view {
     const void *k, *v;
     int64_t stride_b, stride_h, stride_t;
     int32_t cap, window;
     float rope_theta;
-    int32_t pad_;
+    int32_t sink;
 } mtp_kv_view;
 
 /* sample_dist settings ([SP] item 4): repetition penalty (z > 0: z / r, else

@@ -63,7 +63,7 @@ class Weights(C.Structure):
 class KVView(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("stride_b", C.c_int64), ("stride_h", C.c_int64),
                 ("stride_t", C.c_int64), ("cap", C.c_int32), ("window", C.c_int32), ("rope_theta", C.c_float),
-                ("pad_", C.c_int32)]
+                ("sink", C.c_int32)]
 
 
 class SampleParams(C.Structure):
@@ -195,11 +195,12 @@ def make_weights(tensors: dict, n_blocks: int, block_view) -> Weights:
     return w
 
 
-def make_view(k, v, cap: int, window: int, rope_theta: float) -> KVView:
-    """k, v: [B, n_kv_heads, cap, head_dim] device tensors (head_dim contiguous)."""
+def make_view(k, v, cap: int, window: int, rope_theta: float, sink: int = 0) -> KVView:
+    """k, v: [B, n_kv_heads, cap, head_dim] device tensors (head_dim contiguous);
+    sink: attention-sink positions read with a window (see mtp_kv_view)."""
     assert k.shape == v.shape and k.stride() == v.stride() and k.stride(-1) == 1
     sb, sh, st, _ = k.stride()
-    return KVView(k.data_ptr(), v.data_ptr(), sb, sh, st, cap, window, rope_theta, 0)
+    return KVView(k.data_ptr(), v.data_ptr(), sb, sh, st, cap, window, rope_theta, sink)
 
 
 def draft_block(cfg: Config, weights: Weights, views, kv_len, last_tok, h_prev, out_drafts, ws,

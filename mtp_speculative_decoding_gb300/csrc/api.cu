@@ -178,12 +178,13 @@ GreedyLayout greedy_layout(int B, int N) {
 // Sampler workspace: the per-row state (4 x rows words) and the
 // per-sequence counters, zeroed before a launch, then the survivor buffers
 // and (verification) the kept sets.
-struct SampleLayout { size_t row, seq, zero_end, buf, nkeep, wkeep, id, w, end; };
+struct SampleLayout { size_t row, seq, ctr, zero_end, buf, nkeep, wkeep, id, w, end; };
 SampleLayout sample_layout(long long rows, int B, long long V, bool verify) {
     SampleLayout L;
     size_t off = sizeof(WsHeader);
     L.row = off;   off += 4 * (size_t)rows * sizeof(unsigned int);
     L.seq = off;   off += (size_t)B * sizeof(unsigned int);
+    L.ctr = off;   off += sizeof(unsigned int);
     L.zero_end = off;
     off = al256(off);
     L.buf = off;   off = al256(off + (size_t)rows * sample_rcap(V) * sizeof(int2));
@@ -273,6 +274,7 @@ SampleJob sample_job(const void* base0, const void* base1, int ldtype, int B, in
     j.row_ovf = row + 2 * rows;
     j.row_done = row + 3 * rows;
     j.seq_done = reinterpret_cast<unsigned int*>(ws + L.seq);
+    j.next_piece = reinterpret_cast<unsigned int*>(ws + L.ctr);
     j.row_buf = reinterpret_cast<int2*>(ws + L.buf);
     j.rcap = sample_rcap(V);
     j.keep_id = reinterpret_cast<int32_t*>(ws + L.id);
@@ -344,6 +346,8 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         const mtp_kv_view& kv = views[v];
         if (!kv.k || !kv.v || !aligned16(kv.k) || !aligned16(kv.v)) return MTP_ERR_ARG;
         if (kv.cap < 1 || kv.window < 0 || kv.window > kv.cap || !(kv.rope_theta > 0.f)) return MTP_ERR_ARG;
+        if (kv.sink < 0 || (kv.window == 0 && kv.sink != 0) || (long long)kv.window + kv.sink > kv.cap)
+            return MTP_ERR_ARG;
         if (kv.stride_t < cfg->head_dim || kv.stride_b < 0 || kv.stride_h < 0) return MTP_ERR_ARG;
         if ((kv.stride_t * esz) % 16 || (kv.stride_h * esz) % 16 || (kv.stride_b * esz) % 16) return MTP_ERR_ARG;
     }
@@ -421,7 +425,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         KView& d = p.views[v];
         d.k = views[v].k; d.v = views[v].v;
         d.sb = views[v].stride_b; d.sh = views[v].stride_h; d.st = views[v].stride_t;
-        d.cap = views[v].cap; d.window = views[v].window; d.theta = views[v].rope_theta;
+        d.cap = views[v].cap; d.window = views[v].window; d.theta = views[v].rope_theta; d.sink = views[v].sink;
     }
     p.kv_len = kv_len; p.last_tok = last_tok; p.h_prev = h_prev;
     p.out_drafts = out_drafts; p.out_h_last = out_h_last; p.out_logits = out_logits; p.out_conf = out_conf;
@@ -577,6 +581,7 @@ int mtp_sample_drafts(const void* dft_logits, int ldtype, int B, int N, int V, c
     if (cudaMemsetAsync(ws, 0, L.zero_end, s) != cudaSuccess) return MTP_ERR_CUDA;
     const size_t esz = ldtype == MTP_DTYPE_BF16 ? 2 : 4;
     for (int i = 0; i < N; ++i) {   // draw i's penalty set holds draws 0..i-1: one launch per window position
+        if (i > 0 && cudaMemsetAsync(j.next_piece, 0, sizeof(unsigned int), s) != cudaSuccess) return MTP_ERR_CUDA;
         j.draw_i = i;
         j.base0 = static_cast<const char*>(dft_logits) + (size_t)i * V * esz;
         if (launch_sample(j, sms, s) != cudaSuccess) return MTP_ERR_CUDA;

@@ -74,7 +74,7 @@ struct KView {
     long long sb, sh, st;
     int cap, window;
     float theta;
-    int pad_;
+    int sink;   // attention-sink positions read with a window (0: none)
 };
 
 struct BlkW {

@@ -776,6 +776,37 @@ __device__ __forceinline__ int view_lo(const KView& v, int kv_len) {
     return (v.window > 0 && kv_len > v.window) ? kv_len - v.window : 0;
 }
 
+// A sequence's keys in a view ("opus-mtp-turbo: Track 1 report", item 2,
+// sink + window): key index x < s0 is position x (the attention sink,
+// positions [0, min(sink, lo))), key index x >= s0 is position lo + x - s0
+// (the window [lo, kv_len)).  Position t lives in slot t below the sink and
+// in slot sink + (t - sink) % (cap - sink) from it on (a plain ring when
+// sink = 0).
+struct KeyMap {
+    int lo, s0, sink, cap, n;   // window start, sink keys, sink, slots, keys
+};
+__device__ __forceinline__ KeyMap key_map(const KView& v, int kv_len) {
+    KeyMap m;
+    m.lo = view_lo(v, kv_len);
+    m.s0 = v.window > 0 ? (v.sink < m.lo ? v.sink : m.lo) : 0;
+    m.sink = v.window > 0 ? v.sink : 0;
+    m.cap = v.cap;
+    m.n = m.s0 + kv_len - m.lo;
+    return m;
+}
+__device__ __forceinline__ int view_keys(const KView& v, int kv_len) { return key_map(v, kv_len).n; }
+__device__ __forceinline__ int key_slot(const KeyMap& m, int x) {
+    const int t = x < m.s0 ? x : m.lo + (x - m.s0);
+    return t < m.sink ? t : m.sink + (t - m.sink) % (m.cap - m.sink);
+}
+// keys from x on (at most `limit`) whose slots follow one another
+__device__ __forceinline__ int key_run(const KeyMap& m, int x, int limit) {
+    int run = limit;
+    if (x < m.s0 && m.s0 - x < run) run = m.s0 - x;   // the sink keys end
+    const int rs = m.cap - key_slot(m, x);            // the ring wraps
+    return rs < run ? rs : run;
+}
+
 // Key-space partition of an attention phase, per view (the sequence lengths
 // are fixed for a launch): the (sequence b, KV head g) segments lie end to
 // end in b-major order, segment (b, g) holding sequence b's n_b readable
@@ -797,7 +828,7 @@ __device__ __forceinline__ void attn_tab_fill(const DraftParams& p, const int* k
     long long T = 0;
     for (int b = 0; b < p.B; ++b) {
         t.pre[v][b] = T;
-        T += (long long)(kv[b] - view_lo(vw, kv[b])) * p.Hkv;
+        T += (long long)view_keys(vw, kv[b]) * p.Hkv;
     }
     t.pre[v][p.B] = T;
     long long G = T / ((long long)kWarps * R);
@@ -806,9 +837,9 @@ __device__ __forceinline__ void attn_tab_fill(const DraftParams& p, const int* k
     t.T[v] = T;
     t.G[v] = (int)G;
     // equal segments: whole CTAs per segment
-    const int n0 = kv[0] - view_lo(vw, kv[0]), nseg = p.B * p.Hkv;
+    const int n0 = view_keys(vw, kv[0]), nseg = p.B * p.Hkv;
     bool equal = true;
-    for (int b = 1; b < p.B; ++b) equal = equal && kv[b] - view_lo(vw, kv[b]) == n0;
+    for (int b = 1; b < p.B; ++b) equal = equal && view_keys(vw, kv[b]) == n0;
     int c = nseg <= (int)gridDim.x ? (int)gridDim.x / nseg : 0;
     if (c > n0 / (kWarps * R)) c = n0 / (kWarps * R);
     t.cseg[v] = equal && c >= 1 ? c : 0;
@@ -820,7 +851,7 @@ __device__ __forceinline__ int attn_cta(const AttnTab& t, int v, long long x) {
 }
 
 struct AttnPiece {
-    int b, g, t_beg, t_end;   // keys [t_beg, t_end) of KV head g of sequence b
+    int b, g, t_beg, t_end;   // key indices [t_beg, t_end) of KV head g of sequence b (see KeyMap)
     int cf, S;                // first CTA over the segment and their count (S == 1: one piece)
     int slot;                 // partial slot of this piece: 2 c, or 2 c + 1 for a range's last piece
 };
@@ -829,7 +860,7 @@ __device__ __forceinline__ AttnPiece attn_piece(const DraftParams& p, const KVie
                                                 const AttnTab& t, int v, int c, long long x, long long& next) {
     int b = 0;
     while (b + 1 < p.B && t.pre[v][b + 1] <= x) ++b;
-    const int lo = view_lo(vw, kv[b]), n = kv[b] - lo;
+    const int n = view_keys(vw, kv[b]);
     const int g = (int)((x - t.pre[v][b]) / n);
     const long long s0 = t.pre[v][b] + (long long)g * n, s1 = s0 + n;
     const long long ce = attn_lo(t, v, c + 1);
@@ -837,8 +868,8 @@ __device__ __forceinline__ AttnPiece attn_piece(const DraftParams& p, const KVie
     AttnPiece P;
     P.b = b;
     P.g = g;
-    P.t_beg = lo + (int)(x - s0);
-    P.t_end = lo + (int)(next - s0);
+    P.t_beg = (int)(x - s0);
+    P.t_end = (int)(next - s0);
     P.cf = attn_cta(t, v, s0);
     P.S = attn_cta(t, v, s1 - 1) - P.cf + 1;
     // a split segment is the first piece of every CTA over it but the
@@ -855,8 +886,8 @@ __device__ __forceinline__ AttnPiece attn_piece_eq(const DraftParams& p, const K
     P.b = j / p.Hkv;
     P.g = j - P.b * p.Hkv;
     // even split: the first n % cs pieces take one key more
-    const int lo = view_lo(vw, kv[P.b]), n = kv[P.b] - lo, q = n / cs, r = n - q * cs;
-    P.t_beg = lo + sp * q + (sp < r ? sp : r);
+    const int n = view_keys(vw, kv[P.b]), q = n / cs, r = n - q * cs;
+    P.t_beg = sp * q + (sp < r ? sp : r);
     P.t_end = P.t_beg + q + (sp < r ? 1 : 0);
     P.cf = j * cs;
     P.S = cs;
@@ -982,6 +1013,7 @@ __device__ __noinline__ bool attention_phase(const DraftParams& p, int l, unsign
         const AttnPiece A = piece(x, nx);
         const int b = A.b, g = A.g;
         const int t_beg = A.t_beg, t_end = A.t_end;
+        const KeyMap km = key_map(vw, kv[b]);
         const int nrounds = (t_end - t_beg + kWarps * R - 1) / (kWarps * R);
         const WT* kbase = reinterpret_cast<const WT*>(vw.k) + (long long)b * vw.sb + (long long)g * vw.sh;
         const WT* vbase = reinterpret_cast<const WT*>(vw.v) + (long long)b * vw.sb + (long long)g * vw.sh;
@@ -1005,9 +1037,8 @@ __device__ __noinline__ bool attention_phase(const DraftParams& p, int l, unsign
                 unsigned long long* bar = abar + warp * NST + si;
                 mbar_arrive_expect_tx(bar, 2u * (unsigned int)cnt * RB);
                 for (int r = 0; r < cnt;) {
-                    const int slot = (t0 + r) % vw.cap;
-                    int run = packed ? cnt - r : 1;
-                    if (run > vw.cap - slot) run = vw.cap - slot;
+                    const int slot = key_slot(km, t0 + r);
+                    const int run = key_run(km, t0 + r, packed ? cnt - r : 1);
                     bulk_g2s(buf + r * RB, kbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar);
                     bulk_g2s(buf + R * RB + r * RB, vbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar);
                     r += run;
@@ -1342,7 +1373,7 @@ __device__ __noinline__ bool attention_phase(const DraftParams& p, int l, unsign
         const int per = (no + A.S - 1) / A.S;
         const int o0 = (cta - A.cf) * per, o1 = o0 + per < no ? o0 + per : no;
         // the segment's first position (key-space partition)
-        const long long s0 = eq ? 0 : x - (A.t_beg - view_lo(vw, kv[A.b]));
+        const long long s0 = eq ? 0 : x - A.t_beg;
         float* dst = p.OB + ((long long)A.b * p.Hq + (long long)A.g * grp) * HD;
         if (A.S <= kMergeFew) {
             // few partials: a thread per output, all its partials' loads in flight
@@ -2007,6 +2038,7 @@ static __device__ __noinline__ bool sample_step(const DraftParams& p, int k, uns
     j.w_keep = nullptr;
     j.piece_len = p.S_plen;
     j.ppr = p.S_ppr;
+    j.next_piece = nullptr;   // static assignment: CTA c takes pieces c, c + grid, ...
     const int total = p.B * p.S_ppr;
     if (threadIdx.x == 0) prefetch_piece(j, blockIdx.x);
     for (int pc = blockIdx.x; pc < total; pc += gridDim.x)

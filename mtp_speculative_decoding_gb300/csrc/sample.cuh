@@ -37,7 +37,7 @@
 namespace mtp {
 
 constexpr int kCandCap = 4096;     // largest kept (min-p) set of one row
-constexpr int kPieceMax = 32768;   // tokens per piece at most
+constexpr int kPieceMax = 65536;   // tokens per piece at most
 constexpr int kPieceBuf = 4096;    // survivors a piece may hold in shared memory
 constexpr int kRowBufCap = 8192;   // survivors a row may hold in its buffer
 
@@ -46,8 +46,10 @@ constexpr int kRowBufCap = 8192;   // survivors a row may hold in its buffer
 // piece's survivors or the finishing CTA's sort keys (8 bytes each), then the
 // finishing CTA's fp32 weights
 constexpr int kPenMax = 1024;      // penalty-list entries (H + window position) kept in shared memory
+constexpr int kBloomWords = 64;    // a 2048-bit filter over the penalty list (bit = id mod 2048)
 constexpr size_t kSampBitmapBytes = (kPieceMax / 32 + 4) * 4;
-static_assert(kSampBitmapBytes >= (size_t)kPenMax * 4 + 16, "penalty list fits the bitmap area");
+static_assert(kSampBitmapBytes >= (size_t)(kPenMax + kBloomWords) * 4 + 16, "penalty list fits the bitmap area");
+constexpr int kRankSortMax = 512;  // kept sets up to this size are sorted by rank (one pass), larger by bitonic
 constexpr size_t kSampKeyBytes = (size_t)kCandCap * 8 > (size_t)kPieceBuf * 8 ? (size_t)kCandCap * 8 : (size_t)kPieceBuf * 8;
 constexpr size_t kSampleSmem = kSampBitmapBytes + kSampKeyBytes + (size_t)kCandCap * 4;
 
@@ -96,6 +98,7 @@ struct SampleJob {
     float* w_keep;            // mode 0: [rows] kept weight sums
     int piece_len;            // tokens per piece (multiple of 32, <= kPieceMax)
     int ppr;                  // pieces per row
+    unsigned int* next_piece; // standalone launches: pieces handed out so far past the first grid (zeroed)
 };
 
 __host__ __device__ inline int sample_rows(const SampleJob& j) {
@@ -285,18 +288,27 @@ __device__ __forceinline__ void piece_stream(const SampleJob& j, const T* row, l
 }
 
 // Loads (b, i)'s penalty list -- hist[b] then drafts[b][0..i-1], duplicates
-// and out-of-range ids included -- into pen; returns its length, or -1 when
-// it does not fit (kPenMax).  Whole CTA; synchronises.
+// and out-of-range ids included -- into pen, and a 2048-bit filter of it
+// after the list's kPenMax slots; returns the list's length, or -1 when it
+// does not fit (kPenMax).  Whole CTA; synchronises.
 __device__ __forceinline__ int load_penalty_list(const SampleJob& j, int b, int i, int32_t* pen) {
     const int total = j.H + i;
     if (total > kPenMax) return -1;
-    for (int t = threadIdx.x; t < total; t += blockDim.x)
-        pen[t] = t < j.H ? j.hist[(long long)b * j.hist_ld + t] : j.drafts[(long long)b * j.drafts_ld + (t - j.H)];
+    uint32_t* bloom = reinterpret_cast<uint32_t*>(pen + kPenMax);
+    for (int t = threadIdx.x; t < kBloomWords; t += blockDim.x) bloom[t] = 0u;
+    __syncthreads();
+    for (int t = threadIdx.x; t < total; t += blockDim.x) {
+        const int x = t < j.H ? j.hist[(long long)b * j.hist_ld + t] : j.drafts[(long long)b * j.drafts_ld + (t - j.H)];
+        pen[t] = x;
+        atomicOr(&bloom[(x >> 5) & (kBloomWords - 1)], 1u << (x & 31));
+    }
     __syncthreads();
     return total;
 }
 
 __device__ __forceinline__ bool in_list(const int32_t* pen, int n, int x) {
+    const uint32_t* bloom = reinterpret_cast<const uint32_t*>(pen + kPenMax);
+    if (!((bloom[(x >> 5) & (kBloomWords - 1)] >> (x & 31)) & 1u)) return false;
     bool f = false;
     for (int t = 0; t < n; ++t) f |= pen[t] == x;
     return f;
@@ -415,6 +427,30 @@ __device__ __forceinline__ void bitonic_sort(unsigned long long* keys, unsigned 
     }
 }
 
+// Sorts keys[0, n) ascending (keys distinct): by rank (each key counts the
+// keys below it; one pass, tmp[n] holds the result until it is copied back)
+// for n <= kRankSortMax, else bitonic over the next power of two (keys past
+// n set to ~0 by the caller's padding here).  Whole CTA; synchronises.
+__device__ __forceinline__ void sort_keys(unsigned long long* keys, unsigned int n, unsigned long long* tmp) {
+    if (n <= (unsigned)kRankSortMax) {
+        for (unsigned int t = threadIdx.x; t < n; t += blockDim.x) {
+            const unsigned long long k = keys[t];
+            unsigned int r = 0;
+            for (unsigned int u = 0; u < n; ++u) r += keys[u] < k ? 1u : 0u;
+            tmp[r] = k;
+        }
+        __syncthreads();
+        for (unsigned int t = threadIdx.x; t < n; t += blockDim.x) keys[t] = tmp[t];
+        __syncthreads();
+        return;
+    }
+    unsigned int P = 1;
+    while (P < n) P <<= 1;
+    for (unsigned int t = n + threadIdx.x; t < P; t += blockDim.x) keys[t] = ~0ull;
+    __syncthreads();
+    bitonic_sort(keys, P);
+}
+
 // inverse-CDF pick: the first j with u * total < w_0 + ... + w_j, sums in
 // order; n - 1 if none, 0 for an empty set
 template <class WF>
@@ -508,6 +544,7 @@ static __device__ void sample_finish_row(const SampleJob& j, int row, unsigned c
         }
         __syncthreads();
         const float M = fmaxf(Mnp, key_max(s_lp));
+        const float pre = survive_thr(M, log_min_p(j));   // cheap fp32 test before the exact weight
         if (M > -INFINITY) {
             const int2* rbuf = j.row_buf + (long long)row * j.rcap;
             for (unsigned int t = threadIdx.x; t < rc + (unsigned)npen; t += blockDim.x) {
@@ -522,6 +559,7 @@ static __device__ void sample_finish_row(const SampleJob& j, int row, unsigned c
                     l = plv[t - rc];
                     if (!(l == l)) continue;
                 }
+                if (!(l >= pre)) continue;
                 const float w = cand_weight(l, M);
                 if (w >= j.min_p) {
                     const unsigned int s2 = atomicAdd(&s_n, 1u);
@@ -538,11 +576,8 @@ static __device__ void sample_finish_row(const SampleJob& j, int row, unsigned c
         if (threadIdx.x == 0) atomicCAS(&j.hdr->status, 0, MTP_ERR_CAPACITY);
         n = kCandCap;
     }
-    unsigned int P = 1;
-    while (P < n) P <<= 1;
-    for (unsigned int t = n + threadIdx.x; t < P; t += blockDim.x) keys[t] = ~0ull;
     __syncthreads();
-    bitonic_sort(keys, P);
+    sort_keys(keys, n, reinterpret_cast<unsigned long long*>(smem));
     for (unsigned int t = threadIdx.x; t < n; t += blockDim.x) wsh[t] = key_to_float(~(uint32_t)(keys[t] >> 32));
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -643,19 +678,13 @@ static __device__ void sample_walk(const SampleJob& j, int b, unsigned char* sme
         }
         // residual max(p - q, 0) over p's kept set in p's order
         const int np = __ldcg(j.n_keep + trow), nq = __ldcg(j.n_keep + drow);
-        unsigned int P = 1;
-        while (P < (unsigned)nq) P <<= 1;
-        for (unsigned int t = threadIdx.x; t < P; t += blockDim.x) {
-            if (t < (unsigned)nq) {
-                const int32_t id = __ldcg(j.keep_id + (long long)drow * j.ccap + t);
-                const float w = __ldcg(j.keep_w + (long long)drow * j.ccap + t);
-                qk[t] = ((unsigned long long)(uint32_t)id << 32) | __float_as_uint(w);
-            } else {
-                qk[t] = ~0ull;
-            }
+        for (int t = threadIdx.x; t < nq; t += blockDim.x) {
+            const int32_t id = __ldcg(j.keep_id + (long long)drow * j.ccap + t);
+            const float w = __ldcg(j.keep_w + (long long)drow * j.ccap + t);
+            qk[t] = ((unsigned long long)(uint32_t)id << 32) | __float_as_uint(w);
         }
         __syncthreads();
-        bitonic_sort(qk, P);
+        sort_keys(qk, (unsigned)nq, reinterpret_cast<unsigned long long*>(smem));
         for (int t = threadIdx.x; t < np; t += blockDim.x) {
             const uint32_t id = (uint32_t)__ldcg(j.keep_id + (long long)trow * j.ccap + t);
             const float pj = __fdiv_rn(__ldcg(j.keep_w + (long long)trow * j.ccap + t), Wt);

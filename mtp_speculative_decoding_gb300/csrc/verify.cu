@@ -155,14 +155,23 @@ cudaError_t launch_verify_greedy(const VerifyGreedyArgs& a, int ldtype, int num_
 
 constexpr int kSampThreads = 256;
 
-// Persistent over the pieces: CTA c takes pieces c, c + grid, ... and
-// prefetches each next piece into L2 while it works on the current one.
+// Persistent over the pieces: CTA c starts with piece c, then takes the next
+// unclaimed piece from a counter (CTAs that finish a row or a sequence on the
+// way simply take fewer pieces), and prefetches that next piece into L2
+// while it works on the current one.
 __global__ void __launch_bounds__(kSampThreads, 3) sample_kernel(const __grid_constant__ SampleJob j) {
     extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ long long s_next;
     const long long total = (long long)sample_rows(j) * j.ppr;
-    if (threadIdx.x == 0) prefetch_piece(j, blockIdx.x);
-    for (long long pc = blockIdx.x; pc < total; pc += gridDim.x)
-        sample_piece(j, (int)pc, pc + gridDim.x < total ? pc + gridDim.x : -1, smem);
+    long long cur = blockIdx.x;
+    if (threadIdx.x == 0) prefetch_piece(j, cur);
+    while (cur < total) {
+        if (threadIdx.x == 0) s_next = (long long)gridDim.x + atomicAdd(j.next_piece, 1u);
+        __syncthreads();
+        const long long nxt = s_next;   // read before sample_piece's first barrier; rewritten only after it
+        sample_piece(j, (int)cur, nxt < total ? nxt : -1, smem);
+        cur = nxt;
+    }
 }
 
 void sample_piece_plan(long long V, long long rows, int grid, int* ppr, int* piece_len) {

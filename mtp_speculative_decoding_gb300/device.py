@@ -68,7 +68,7 @@ def upload_draft(w, device="cuda", extra_ws_for=None, reuse: "DeviceDraft | None
     for vd in w.views:
         k, v = to_device(vd["k"], device=device), to_device(vd["v"], device=device)
         keep += [k, v]
-        views.append(make_view(k, v, vd["cap"], vd["window"], vd["rope_theta"]))
+        views.append(make_view(k, v, vd["cap"], vd["window"], vd["rope_theta"], vd.get("sink", 0)))
     tensors["_views"] = keep
     weights = make_weights(tensors, m.n_blocks, m.block_view)
     kv_len = torch.from_numpy(np.ascontiguousarray(w.kv_len, dtype=np.int32)).to(device)

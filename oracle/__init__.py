@@ -47,7 +47,7 @@ class Model(C.Structure):
 class View(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("stride_b", C.c_int64),
                 ("stride_h", C.c_int64), ("stride_t", C.c_int64), ("cap", C.c_int32),
-                ("window", C.c_int32), ("rope_theta", C.c_double)]
+                ("window", C.c_int32), ("sink", C.c_int32), ("pad_", C.c_int32), ("rope_theta", C.c_double)]
 
 
 class SampleParams(C.Structure):
@@ -143,13 +143,13 @@ def argmax(z):
     return int(lib().orc_argmax_f64(_p(z), z.size))
 
 
-def attend_head(q, k, v, b, g, kv_len, window=0, scale=None, bf16=False):
+def attend_head(q, k, v, b, g, kv_len, window=0, scale=None, bf16=False, sink=0):
     """k, v: [B, Hkv, cap, hd] arrays (fp32, or uint16 bf16 bits with bf16=True)."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k)
     v = np.ascontiguousarray(v)
     B, H, cap, hd = k.shape
-    vw = View(_p(k).value, _p(v).value, H * cap * hd, cap * hd, hd, cap, window, 0.0)
+    vw = View(_p(k).value, _p(v).value, H * cap * hd, cap * hd, hd, cap, window, sink, 0, 0.0)
     out = np.empty(hd, dtype=np.float64)
     sc = 1.0 / np.sqrt(hd) if scale is None else scale
     lib().orc_attend_head(_p(q), C.byref(vw), b, g, hd, kv_len, sc, int(bf16), _p(out))
@@ -232,7 +232,7 @@ class _Bound:
             Bv, H, cap, hd = k.shape
             off = 0 if b is None else b * H * cap * hd * esz
             views.append(View(k.ctypes.data + off, v.ctypes.data + off, H * cap * hd, cap * hd, hd,
-                              cap, vd["window"], vd["rope_theta"]))
+                              cap, vd["window"], vd.get("sink", 0), 0, vd["rope_theta"]))
             self.keep += [k, v]
         self.views = (View * len(views))(*views)
         self.n_views = len(views)

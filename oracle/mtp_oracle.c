@@ -66,7 +66,8 @@ typedef struct {
 typedef struct {
     const void *k, *v;
     int64_t stride_b, stride_h, stride_t;   /* elements; head_dim is contiguous */
-    int32_t cap, window;                    /* ring slots; 0 = full attention */
+    int32_t cap, window;                    /* slots; 0 = full attention */
+    int32_t sink, pad_;                     /* attention-sink positions read with a window */
     double rope_theta;
 } orc_view;
 
@@ -160,18 +161,29 @@ static int64_t argmax_stored(const void *z, int64_t n, int bf16) {
     return best < 0 ? 0 : best;
 }
 
+/* The slot of position t in a view: t below the sink, then a ring over the
+ * remaining cap - sink slots ("opus-mtp-turbo: Track 1 report", item 2 keeps
+ * the first `sink` cells beside the window). */
+static int64_t view_slot(const orc_view *vw, int64_t t) {
+    const int64_t sk = vw->window > 0 ? vw->sink : 0;
+    return t < sk ? t : sk + (t - sk) % (vw->cap - sk);
+}
+
 /* Cross-attention of one query head into one KV view ([G4] sec. 4-5, [FN] delta 6).
  * Keys: positions t in [lo, kv_len), lo = max(0, kv_len - window) for a sliding
- * view, 0 for a full one; position t is stored in ring slot t % cap.  V is used
- * as stored. */
+ * view, 0 for a full one, and for a sliding view the sink positions
+ * [0, min(sink, lo)) (the sink + window read of "opus-mtp-turbo", item 2).  V is
+ * used as stored. */
 void orc_attend_head(const double *q, const orc_view *vw, int b, int g, int hd, int kv_len,
                      double scale, int bf16, double *out) {
     const int lo = (vw->window > 0 && kv_len > vw->window) ? kv_len - vw->window : 0;
-    const int n = kv_len - lo;
+    const int s0 = vw->window > 0 ? (vw->sink < lo ? vw->sink : lo) : 0;   /* sink keys */
+    const int n = s0 + kv_len - lo;
     double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
     double m = -INFINITY;
     for (int j = 0; j < n; ++j) {
-        int64_t slot = (int64_t)((lo + j) % vw->cap);
+        const int64_t pos = j < s0 ? j : lo + (j - s0);
+        int64_t slot = view_slot(vw, pos);
         int64_t base = (int64_t)b * vw->stride_b + (int64_t)g * vw->stride_h + slot * vw->stride_t;
         double acc = 0.0;
         for (int d = 0; d < hd; ++d) acc += q[d] * elem(vw->k, base + d, bf16);
@@ -183,7 +195,8 @@ void orc_attend_head(const double *q, const orc_view *vw, int b, int g, int hd, 
     for (int j = 0; j < n; ++j) {
         double w = exp(s[j] - m);
         den += w;
-        int64_t slot = (int64_t)((lo + j) % vw->cap);
+        const int64_t pos = j < s0 ? j : lo + (j - s0);
+        int64_t slot = view_slot(vw, pos);
         int64_t base = (int64_t)b * vw->stride_b + (int64_t)g * vw->stride_h + slot * vw->stride_t;
         for (int d = 0; d < hd; ++d) out[d] += w * elem(vw->v, base + d, bf16);
     }

@@ -162,9 +162,10 @@ class ModelSpec:
 
 @dataclasses.dataclass
 class ViewSpec:
-    cap: int             # ring-buffer slots per (sequence, kv head)
+    cap: int             # slots per (sequence, kv head)
     window: int          # 0 = full attention over [0, kv_len); W > 0 = last W positions
     rope_theta: float
+    sink: int = 0        # with a window: positions [0, sink) kept beside it (slots 0..sink-1)
 
 
 @dataclasses.dataclass
@@ -212,12 +213,24 @@ def make_model_weights(m: ModelSpec, seed: int, std: float = 0.02) -> dict:
     return w
 
 
-def view_valid_mask(cap: int, window: int, kv_len: int) -> np.ndarray:
-    """bool [cap]: which ring slots hold a position the drafter may read."""
+def view_positions(window: int, kv_len: int, sink: int = 0) -> np.ndarray:
+    """The positions a drafter reads: the window [lo, kv_len) and, with a
+    window, the sink [0, min(sink, lo))."""
     lo = max(0, kv_len - window) if window > 0 else 0
+    s0 = min(sink, lo) if window > 0 else 0
+    return np.concatenate([np.arange(0, s0), np.arange(lo, kv_len)])
+
+
+def view_slot(t: np.ndarray, cap: int, sink: int = 0) -> np.ndarray:
+    """Slot of position t: t below the sink, then a ring over cap - sink slots."""
+    t = np.asarray(t)
+    return np.where(t < sink, t, sink + (t - sink) % max(1, cap - sink))
+
+
+def view_valid_mask(cap: int, window: int, kv_len: int, sink: int = 0) -> np.ndarray:
+    """bool [cap]: which slots hold a position the drafter may read."""
     mask = np.zeros(cap, dtype=bool)
-    t = np.arange(lo, kv_len)
-    mask[t % cap] = True
+    mask[view_slot(view_positions(window, kv_len, sink), cap, sink if window > 0 else 0)] = True
     return mask
 
 
@@ -229,13 +242,13 @@ def make_kv_view(m: ModelSpec, vs: ViewSpec, kv_len: np.ndarray, seed: int, tag:
         vals = normal(seed, f"{tag}.{which}", shape, std=1.0)
         arr = _as_dtype(vals, m.dtype)
         for b in range(B):
-            bad = ~view_valid_mask(vs.cap, vs.window, int(kv_len[b]))
+            bad = ~view_valid_mask(vs.cap, vs.window, int(kv_len[b]), vs.sink)
             if m.dtype == "bf16":
                 arr[b][:, bad, :] = BF16_NAN
             else:
                 arr[b][:, bad, :] = np.nan
         out[which] = arr
-    out.update(cap=vs.cap, window=vs.window, rope_theta=vs.rope_theta)
+    out.update(cap=vs.cap, window=vs.window, rope_theta=vs.rope_theta, sink=vs.sink)
     return out
 
 
@@ -255,7 +268,7 @@ def make_draft_workload(name: str, m: ModelSpec, views_spec: list, B: int, N: in
                         kv_len, seed: int, hist_len: int = 0, model_seed: int | None = None) -> DraftWorkload:
     kv_len = np.asarray(kv_len, dtype=np.int32).reshape(B)
     for vs in views_spec:
-        need = vs.window if vs.window > 0 else int(kv_len.max())
+        need = vs.window + vs.sink if vs.window > 0 else int(kv_len.max())
         if need > vs.cap:
             raise ValueError(f"view cap {vs.cap} too small for {need} positions")
     weights = cached_model_weights(m, seed if model_seed is None else model_seed)
@@ -297,11 +310,12 @@ def workload_seed(cfg_id: int) -> int:
     return 1000 + int(cfg_id)
 
 
-def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None) -> DraftWorkload:
+def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None, sink: int = 0) -> DraftWorkload:
     """Draft-block inputs of one of the named workloads (0-3).
 
     ``B`` may shrink the batch (the first B sequences' lengths are kept) for
-    parity runs at full model size.
+    parity runs at full model size.  ``sink`` > 0 keeps that many attention-
+    sink positions beside the sliding window (workloads 1-3).
     """
     seed = workload_seed(cfg_id) if seed is None else seed
     name = WORKLOADS[cfg_id]
@@ -326,6 +340,8 @@ def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None
     kv = np.resize(np.asarray(kv, dtype=np.int32), B) if B != Bf else kv
     if cfg_id == 2:
         views = [views[0], ViewSpec(cap=int(kv.max()), window=0, rope_theta=1e6)]
+    if sink and cfg_id in (1, 2, 3):
+        views = [ViewSpec(cap=views[0].cap, window=views[0].window, rope_theta=views[0].rope_theta, sink=sink)] + views[1:]
     # workloads 1-3 share one model ("same model as config 1"): its weights use seed 1001
     model_seed = workload_seed(1) if cfg_id in (1, 2, 3) else seed
     return make_draft_workload(name, m, views, B, N, kv, seed, hist_len=64, model_seed=model_seed)

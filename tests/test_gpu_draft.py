@@ -14,12 +14,13 @@ def _built():
     build.build()
 
 
-def small_workload(dtype, B=3, N=3, seed=5, kv=(37, 23, 100), softcap=0.0, V=1000, hd=32):
+def small_workload(dtype, B=3, N=3, seed=5, kv=(37, 23, 100), softcap=0.0, V=1000, hd=32, sink=0):
     """Several tiles of every phase plus ragged tails: V not a multiple of the
     row split, a sliding ring view with stale (NaN) slots, ragged kv_len."""
     m = synth.ModelSpec(d_t=96, d_a=64, n_blocks=2, n_q_heads=4, head_dim=hd, n_kv_heads=2, d_ff=136,
                         vocab=V, dtype=dtype, block_view=(0, 1), logit_softcap=softcap)
-    views = [synth.ViewSpec(cap=48, window=40, rope_theta=1e4), synth.ViewSpec(cap=128, window=0, rope_theta=1e6)]
+    views = [synth.ViewSpec(cap=48 + sink, window=40, rope_theta=1e4, sink=sink),
+             synth.ViewSpec(cap=128, window=0, rope_theta=1e6)]
     return synth.make_draft_workload("small", m, views, B, N, list(kv)[:B], seed, hist_len=8)
 
 
@@ -50,6 +51,26 @@ def test_single_sequence_split_and_paired_rows():
     w = synth.make_draft_workload("wide_b1", m, views, 1, 2, [150], 21, hist_len=4)
     _, d, h, z = run_gpu_draft(w)
     check_draft_parity(w, d, h, z, seqs=[0])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_small_sink_and_window(dtype):
+    """Attention sink + window ("opus-mtp-turbo", item 2): the sliding view
+    keeps 8 sink positions in slots 0..7 and a 40-slot ring after them; the
+    lengths cover a window past the sink with a ring wrap (100), a window
+    overlapping the sink (45) and no window cut (23)."""
+    w = small_workload(dtype, kv=(100, 45, 23), sink=8)
+    _, d, h, z = run_gpu_draft(w)
+    check_draft_parity(w, d, h, z, seqs=range(w.B))
+
+
+@pytest.mark.slow
+def test_workload2_with_sink_64():
+    """Workload 2 with the page's default of 64 sink positions beside the
+    1024-position sliding window."""
+    w = synth.make_draft_inputs(2, sink=64)
+    _, d, h, z = run_gpu_draft(w)
+    check_draft_parity(w, d, h, z, seqs=[0, 5, 11, 15])
 
 
 def test_small_softcap_and_head_dim_64():

@@ -174,3 +174,60 @@ def test_attention_ignores_poisoned_slots():
     v[0, 0, ~mask] = np.nan
     out = oracle.attend_head(rng.standard_normal(8), k, v, 0, 0, kv_len, W)
     assert np.all(np.isfinite(out))
+
+
+# ----------------------------------------------------------------------------
+# sink + window ("opus-mtp-turbo: Track 1 report", item 2): the draft
+# attention reads the first `sink` positions beside the window; position t is
+# stored in slot t below the sink and in a ring over the other slots above it
+# ----------------------------------------------------------------------------
+
+def _plain_attention(q, keys, vals):
+    s = keys @ q / np.sqrt(q.size)
+    p = np.exp(s - s.max())
+    return (p[:, None] * vals).sum(0) / p.sum()
+
+
+@pytest.mark.parametrize("kv_len,W,S,cap", [(100, 40, 8, 48), (45, 40, 8, 48), (30, 40, 8, 48),
+                                             (200, 16, 16, 40), (9, 4, 4, 8)])
+def test_sink_window_brute_force(kv_len, W, S, cap):
+    """The key set enumerated by hand: [0, min(S, lo)) then [lo, kv_len),
+    gathered from their slots; every other slot holds NaN."""
+    rng = np.random.default_rng(kv_len + S)
+    hd = 16
+    k = np.full((1, 1, cap, hd), np.nan, dtype=np.float32)
+    v = np.full((1, 1, cap, hd), np.nan, dtype=np.float32)
+    lo = max(0, kv_len - W)
+    pos = list(range(min(S, lo))) + list(range(lo, kv_len))
+    slot = [t if t < S else S + (t - S) % (cap - S) for t in pos]
+    assert len(set(slot)) == len(slot)      # every read position has its own slot
+    kk = rng.standard_normal((len(pos), hd)).astype(np.float32)
+    vv = rng.standard_normal((len(pos), hd)).astype(np.float32)
+    k[0, 0, slot] = kk
+    v[0, 0, slot] = vv
+    q = rng.standard_normal(hd)
+    got = oracle.attend_head(q, k, v, 0, 0, kv_len, W, sink=S)
+    assert np.allclose(got, _plain_attention(q, kk.astype(np.float64), vv.astype(np.float64)), atol=1e-12)
+
+
+def test_sink_zero_is_the_plain_window_and_a_wide_sink_the_full_view():
+    rng = np.random.default_rng(11)
+    cap, hd = 64, 8
+    k = rng.standard_normal((1, 1, cap, hd)).astype(np.float32)
+    v = rng.standard_normal((1, 1, cap, hd)).astype(np.float32)
+    q = rng.standard_normal(hd)
+    assert np.array_equal(oracle.attend_head(q, k, v, 0, 0, 50, 20, sink=0),
+                          oracle.attend_head(q, k, v, 0, 0, 50, 20))
+    # kv_len - W <= sink and cap >= kv_len: every position in slot t, all read
+    assert np.allclose(oracle.attend_head(q, k, v, 0, 0, 40, 24, sink=16),
+                       oracle.attend_head(q, k, v, 0, 0, 40, 0), atol=0)
+
+
+def test_synth_sink_layout_matches_the_read_set():
+    m = synth.ModelSpec(d_t=32, d_a=32, n_blocks=1, n_q_heads=2, head_dim=16, n_kv_heads=1, d_ff=64,
+                        vocab=64, dtype="f32", block_view=(0,))
+    vs = synth.ViewSpec(cap=48, window=40, rope_theta=1e4, sink=8)
+    view = synth.make_kv_view(m, vs, np.array([100, 45, 23], dtype=np.int32), 3, "s")
+    for b, L in enumerate((100, 45, 23)):
+        finite = np.isfinite(view["k"][b, 0, :, 0])
+        assert finite.sum() == len(synth.view_positions(40, L, 8))
