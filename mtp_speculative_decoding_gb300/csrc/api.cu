@@ -214,6 +214,12 @@ size_t draft_smem(const mtp_config* c, int B, int act_smem) {
     return attn > act ? attn : act;
 }
 
+// floor(2^32 / n) for n >= 2 (2^32 - 1 for n = 1): the device's
+// multiply-high modulo (ring_mod) is then exact after one correction
+unsigned int mod_magic(unsigned int n) {
+    return n <= 1 ? 0xFFFFFFFFu : (unsigned int)(0x100000000ull / (unsigned long long)n);
+}
+
 int check_config(const mtp_config* c) {
     if (!c) return MTP_ERR_ARG;
     if (c->d_t <= 0 || c->d_a <= 0 || c->n_blocks <= 0 || c->n_q_heads <= 0 || c->head_dim <= 0 ||
@@ -426,6 +432,8 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         d.k = views[v].k; d.v = views[v].v;
         d.sb = views[v].stride_b; d.sh = views[v].stride_h; d.st = views[v].stride_t;
         d.cap = views[v].cap; d.window = views[v].window; d.theta = views[v].rope_theta; d.sink = views[v].sink;
+        d.cap_magic = mod_magic((unsigned int)d.cap);
+        d.ring_magic = mod_magic((unsigned int)(d.cap - (d.window > 0 ? d.sink : 0)));
     }
     p.kv_len = kv_len; p.last_tok = last_tok; p.h_prev = h_prev;
     p.out_drafts = out_drafts; p.out_h_last = out_h_last; p.out_logits = out_logits; p.out_conf = out_conf;

@@ -74,7 +74,9 @@ struct KView {
     long long sb, sh, st;
     int cap, window;
     float theta;
-    int sink;   // attention-sink positions read with a window (0: none)
+    int sink;                 // attention-sink positions read with a window (0: none)
+    unsigned int cap_magic;   // floor(2^32 / cap): slot = position mod cap by a multiply-high
+    unsigned int ring_magic;  // floor(2^32 / (cap - sink)) for the ring above the sink
 };
 
 struct BlkW {

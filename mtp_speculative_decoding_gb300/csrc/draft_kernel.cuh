@@ -784,6 +784,7 @@ __device__ __forceinline__ int view_lo(const KView& v, int kv_len) {
 // sink = 0).
 struct KeyMap {
     int lo, s0, sink, cap, n;   // window start, sink keys, sink, slots, keys
+    unsigned int ring, magic;   // cap - sink and floor(2^32 / ring): d % ring by a multiply-high
 };
 __device__ __forceinline__ KeyMap key_map(const KView& v, int kv_len) {
     KeyMap m;
@@ -792,18 +793,25 @@ __device__ __forceinline__ KeyMap key_map(const KView& v, int kv_len) {
     m.sink = v.window > 0 ? v.sink : 0;
     m.cap = v.cap;
     m.n = m.s0 + kv_len - m.lo;
+    m.ring = (unsigned int)(m.cap - m.sink);
+    m.magic = v.window > 0 ? v.ring_magic : v.cap_magic;
     return m;
 }
 __device__ __forceinline__ int view_keys(const KView& v, int kv_len) { return key_map(v, kv_len).n; }
+// d % ring for 0 <= d < 2^31: the multiply-high quotient is exact or one short
+__device__ __forceinline__ unsigned int ring_mod(const KeyMap& m, unsigned int d) {
+    unsigned int r = d - __umulhi(d, m.magic) * m.ring;
+    return r >= m.ring ? r - m.ring : r;
+}
 __device__ __forceinline__ int key_slot(const KeyMap& m, int x) {
     const int t = x < m.s0 ? x : m.lo + (x - m.s0);
-    return t < m.sink ? t : m.sink + (t - m.sink) % (m.cap - m.sink);
+    return t < m.sink ? t : m.sink + (int)ring_mod(m, (unsigned int)(t - m.sink));
 }
-// keys from x on (at most `limit`) whose slots follow one another
-__device__ __forceinline__ int key_run(const KeyMap& m, int x, int limit) {
+// keys from x on (at most `limit`) whose slots follow one another; `slot` is key x's slot
+__device__ __forceinline__ int key_run(const KeyMap& m, int x, int slot, int limit) {
     int run = limit;
     if (x < m.s0 && m.s0 - x < run) run = m.s0 - x;   // the sink keys end
-    const int rs = m.cap - key_slot(m, x);            // the ring wraps
+    const int rs = m.cap - slot;                      // the ring wraps
     return rs < run ? rs : run;
 }
 
@@ -963,7 +971,7 @@ __device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v)
 // NST: ring stages per warp.  abar: [kWarps][NST] stage barriers (one arrival
 // each); apar: the calling warp's stage phase bits, carried across calls.
 template <typename WT, int HD, int NST>
-__device__ __noinline__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem, const int* kv, const AttnTab& tab,
+__device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsigned char* smem, const int* kv, const AttnTab& tab,
                                 unsigned long long* abar, unsigned int& apar) {
     constexpr AttnGeom G = attn_geom(HD, (int)sizeof(WT));
     constexpr int RB = G.RB, LPR = G.LPR, CPL = G.CPL, KPW = G.KPW, EPC = G.EPC, DPL = G.DPL;
@@ -1038,7 +1046,7 @@ __device__ __noinline__ bool attention_phase(const DraftParams& p, int l, unsign
                 mbar_arrive_expect_tx(bar, 2u * (unsigned int)cnt * RB);
                 for (int r = 0; r < cnt;) {
                     const int slot = key_slot(km, t0 + r);
-                    const int run = key_run(km, t0 + r, packed ? cnt - r : 1);
+                    const int run = key_run(km, t0 + r, slot, packed ? cnt - r : 1);
                     bulk_g2s(buf + r * RB, kbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar);
                     bulk_g2s(buf + R * RB + r * RB, vbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar);
                     r += run;
@@ -1456,6 +1464,22 @@ __device__ __noinline__ bool attention_phase(const DraftParams& p, int l, unsign
     return true;
 }
 
+// The attention phase: out of line in the single-sequence kernel (its
+// register allocation then does not compete with the GEMV phases'), inline
+// in the batched kernel (measured faster there: 3.348 vs 3.396 ms per draft
+// launch at 64 sequences, 1.650 vs 1.684 ms the other way at one sequence).
+template <typename WT, int HD, int NST>
+__device__ __noinline__ bool attention_call(const DraftParams& p, int l, unsigned char* smem, const int* kv,
+                                            const AttnTab& tab, unsigned long long* abar, unsigned int& apar) {
+    return attention_body<WT, HD, NST>(p, l, smem, kv, tab, abar, apar);
+}
+template <typename WT, int HD, int NST, bool TC>
+__device__ __forceinline__ bool attention_phase(const DraftParams& p, int l, unsigned char* smem, const int* kv,
+                                                const AttnTab& tab, unsigned long long* abar, unsigned int& apar) {
+    if constexpr (TC) return attention_body<WT, HD, NST>(p, l, smem, kv, tab, abar, apar);
+    else return attention_call<WT, HD, NST>(p, l, smem, kv, tab, abar, apar);
+}
+
 // ---------------------------------------------------------------------------
 // LM head over the tied token table with the argmax folded in: per lane,
 // per CTA in shared memory, then one atomic per sequence.
@@ -1712,6 +1736,10 @@ __device__ __noinline__ bool tc_gemm(const DraftParams& p, const TcJob& J, unsig
 // tiles and folds it into amax[k, b] once.  Barrier phases continue across
 // steps through `ts` (a ring of its own: its stages differ from the
 // projections').
+// CONF: also keep each sequence's softmax denominator (the confidence
+// output); a separate instantiation, so the plain head's epilogue loop
+// carries none of it.
+template <bool CONF>
 static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigned char* smem, TcState& ts) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int NS = p.th_stages;
@@ -1782,7 +1810,6 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
         const int q = warp - 4;   // tensor-memory lane quarter of this warp
         const int b = 16 * q + lane;
         const bool mine = lane < 16 && b < p.B;
-        const bool conf = p.out_conf != nullptr;
         unsigned long long best = 0ull;
         SoftDen den = soft_den0();
         for (int j = 0; j < nit && ok; ++j) {
@@ -1809,7 +1836,7 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
                             if (p.ZB) p.ZB[(long long)b * p.V + row] = z;
                             const unsigned long long key = pack_argmax(z, (uint32_t)row);
                             best = key > best ? key : best;
-                            if (conf) den.add(z);
+                            if constexpr (CONF) den.add(z);
                         }
                     }
                 }
@@ -1819,7 +1846,7 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
             if (lane == 0) mbar_arrive(&ts.tempty[acc]);
         }
         if (mine && nit > 0) atomicMax(p.amax + (long long)k * p.B + b, best);
-        if (mine && conf) p.CONF[(long long)blockIdx.x * p.B + b] = make_float2(den.m, den.s);
+        if (CONF && mine) p.CONF[(long long)blockIdx.x * p.B + b] = make_float2(den.m, den.s);
     }
     ts.g += (uint32_t)(nit * nks);
     ts.it += (uint32_t)nit;
@@ -1924,7 +1951,7 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
         // argmax is stable to it); sampling: both parts, so the sampler sees
         // logits as close as the CUDA-core path's.  The epilogue folds its
         // maxima into amax itself.
-        if constexpr (TC) return tc_head(p, k, smem, ts);
+        if constexpr (TC) return p.out_conf ? tc_head<true>(p, k, smem, ts) : tc_head<false>(p, k, smem, ts);
         return false;
     } else if (p.head_slotb > 0) {
         const int cpl = (p.d_t / Chunk<WT>::EPC + 127) / 128;
@@ -2190,8 +2217,8 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 if (!gemv_step(PH_Q, k, l, bw.w_q, nullptr, p.Hq * p.hd, p.d_a, e, One{})) return;
             }
             // ---- ATT ----
-            if (!attention_phase<WT, HD, TC ? kAttnStagesTc : kAttnStages>(p, l, smem, s_kv, s_tab, &attn_bar[0][0],
-                                                                          attn_par))
+            if (!attention_phase<WT, HD, TC ? kAttnStagesTc : kAttnStages, TC>(p, l, smem, s_kv, s_tab,
+                                                                              &attn_bar[0][0], attn_par))
                 return;
             if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
             // every CTA has passed its attention waits: reset the item counters
