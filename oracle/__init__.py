@@ -39,7 +39,8 @@ def build(force: bool = False) -> str:
 class Model(C.Structure):
     _fields_ = [("d_t", C.c_int32), ("d_a", C.c_int32), ("n_blocks", C.c_int32),
                 ("n_q_heads", C.c_int32), ("head_dim", C.c_int32), ("n_kv_heads", C.c_int32),
-                ("d_ff", C.c_int32), ("vocab", C.c_int32), ("wbf16", C.c_int32), ("pad_", C.c_int32),
+                ("d_ff", C.c_int32), ("vocab", C.c_int32), ("wbf16", C.c_int32), ("n_centroids", C.c_int32),
+                ("centroid_top_k", C.c_int32), ("pad_", C.c_int32),
                 ("rms_eps", C.c_double), ("attn_scale", C.c_double), ("emb_scale", C.c_double),
                 ("logit_softcap", C.c_double)]
 
@@ -85,6 +86,8 @@ def _declare(L):
     L.orc_draft_step.argtypes = [P, P, P, P, I, I, P, I, P, P, P, P]
     L.orc_draft_step.restype = I
     L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, I, P, I, P, P, P, P, P, P]
+    L.orc_centroid_head.argtypes = [P, P, P, P, P, P]
+    L.orc_centroid_head.restype = I
     L.orc_top1_prob.argtypes = [P, C.c_int64]
     L.orc_top1_prob.restype = D
     L.orc_draft_block.restype = I
@@ -206,9 +209,31 @@ def pick(ids, w, wsum, u):
 # draft block
 # ----------------------------------------------------------------------------
 
-GLOBAL_ORDER = ("tok_embd", "norm_e", "norm_h", "w_pre", "final_norm", "w_post")
+GLOBAL_ORDER = ("tok_embd", "norm_e", "norm_h", "w_pre", "final_norm", "w_post", "centroids", "token_ordering")
 BLOCK_ORDER = ("attn_norm", "w_q", "q_norm", "w_o", "post_attn_norm", "pre_ffn_norm",
                "w_gate", "w_up", "w_down", "post_ffn_norm")
+
+
+def _model(m) -> Model:
+    return Model(m.d_t, m.d_a, m.n_blocks, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff, m.vocab,
+                 1 if m.dtype == "bf16" else 0, getattr(m, "n_centroids", 0), getattr(m, "centroid_top_k", 0), 0,
+                 m.rms_eps, m.attn_scale, m.emb_scale, m.logit_softcap)
+
+
+def centroid_head(m, centroids, ordering, tok_embd, h):
+    """The centroid-routed head's full logit row [V] (f64) for one hidden state h [d_t].
+
+    ``m``: a model spec with n_centroids / centroid_top_k / vocab / d_t / dtype /
+    logit_softcap; matrices fp32, or uint16 bf16 bits when m.dtype == 'bf16'."""
+    c = np.ascontiguousarray(centroids)
+    o = np.ascontiguousarray(ordering, dtype=np.int32)
+    e = np.ascontiguousarray(tok_embd)
+    h = np.ascontiguousarray(h, dtype=np.float64)
+    z = np.empty(m.vocab, dtype=np.float64)
+    mdl = _model(m)
+    if lib().orc_centroid_head(C.byref(mdl), _p(c), _p(o), _p(e), _p(h), _p(z)) != 0:
+        raise ValueError("oracle centroid head rejected its inputs")
+    return z
 
 
 class _Bound:
@@ -217,13 +242,12 @@ class _Bound:
     def __init__(self, w, b=None):
         m = w.model
         self.keep = []
-        self.model = Model(m.d_t, m.d_a, m.n_blocks, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff,
-                           m.vocab, 1 if m.dtype == "bf16" else 0, 0, m.rms_eps, m.attn_scale,
-                           m.emb_scale, m.logit_softcap)
+        self.model = _model(m)
         names = list(GLOBAL_ORDER) + [f"blk{i}.{n}" for i in range(m.n_blocks) for n in BLOCK_ORDER]
-        arrs = [np.ascontiguousarray(w.weights[n]) for n in names]
-        self.keep += arrs
-        self.tensors = (C.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+        # the centroid head's tensors exist only for centroid-head models (NULL otherwise)
+        arrs = [np.ascontiguousarray(w.weights[n]) if n in w.weights else None for n in names]
+        self.keep += [a for a in arrs if a is not None]
+        self.tensors = (C.c_void_p * len(arrs))(*[None if a is None else a.ctypes.data for a in arrs])
         self.block_view = np.ascontiguousarray(np.asarray(m.block_view, dtype=np.int32))
         views = []
         esz = 2 if m.dtype == "bf16" else 4

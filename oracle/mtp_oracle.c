@@ -15,7 +15,8 @@
  *
  * Sources (page title, section):
  *  [G4]  "Gemma 4 MTP -- Multi-Token Prediction speculative decoding",
- *        sec. 3 (pre/post projection shapes), sec. 4 "Per-step MTP graph"
+ *        sec. 3 (pre/post projection shapes; the centroid / ordered-embeddings
+ *        LM head), sec. 4 "Per-step MTP graph"
  *        (embedding scale, concat + pre-projection, block order, final norm,
  *        post-projection, LM head, softcap, in-graph argmax), sec. 5 "KV
  *        sharing" (mask admits every position <= attn_pos; one mask for all
@@ -59,7 +60,8 @@
 typedef struct {
     int32_t d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab;
     int32_t wbf16;        /* 1: weight matrices and KV are bf16 bit patterns; 0: fp32 */
-    int32_t pad_;
+    int32_t n_centroids;  /* 0: dense tied LM head; > 0: centroid-routed head */
+    int32_t centroid_top_k, pad_;
     double rms_eps, attn_scale, emb_scale, logit_softcap;
 } orc_model;
 
@@ -77,7 +79,8 @@ typedef struct {
 } orc_sample_params;
 
 /* tensor table: globals first, then B_COUNT entries per block */
-enum { T_TOK_EMBD, T_NORM_E, T_NORM_H, T_W_PRE, T_FINAL_NORM, T_W_POST, T_GLOBAL_COUNT };
+enum { T_TOK_EMBD, T_NORM_E, T_NORM_H, T_W_PRE, T_FINAL_NORM, T_W_POST, T_CENTROIDS, T_ORDERING,
+       T_GLOBAL_COUNT };
 enum { B_ATTN_NORM, B_W_Q, B_Q_NORM, B_W_O, B_POST_ATTN_NORM, B_PRE_FFN_NORM,
        B_W_GATE, B_W_UP, B_W_DOWN, B_POST_FFN_NORM, B_COUNT };
 
@@ -400,6 +403,57 @@ int32_t orc_pick(const int32_t *ids, const double *w, int n, double wsum, double
 }
 
 /* ------------------------------------------------------------------------ */
+/* centroid-routed LM head ([G4] sec. 3, "Centroid / ordered-embeddings LM  */
+/* head", steps 1-5)                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* The full-vocabulary logit row of the centroid-routed head for one hidden
+ * state h [d_t]:
+ *   1. centroid logits c_j = centroids[j] . h, j < n_c (centroids [n_c, d_t]);
+ *   2. the top_k centroids by c_j (reading: ties go to the lower centroid id;
+ *      the chosen set is all that matters, not its order);
+ *   3. token_ordering [V] int32 read as n_c consecutive lists of
+ *      vsc = V / n_c token ids, list j belonging to centroid j (reading of
+ *      the [vsc, n_c] view: vsc is the contiguous dimension, get_rows takes
+ *      one list per chosen centroid); the chosen lists are the candidates;
+ *   4. each candidate t gets the dense head's logit tok_embd[t] . h, with the
+ *      same final softcap (reading: the cap applies to the candidates'
+ *      logits, before the scatter);
+ *   5. every other entry of the row holds -1e30.
+ * Returns 0, or -1 for invalid sizes or an ordering entry outside [0, V). */
+int orc_centroid_head(const orc_model *m, const void *centroids, const int32_t *ordering,
+                      const void *tok_embd, const double *h, double *z) {
+    const int nc = m->n_centroids, kc = m->centroid_top_k, V = m->vocab, d_t = m->d_t, bf = m->wbf16;
+    if (nc <= 0 || kc <= 0 || kc > nc || V % nc != 0) return -1;
+    const int vsc = V / nc;
+    double *cl = malloc(sizeof(double) * (size_t)nc);
+    char *taken = calloc((size_t)nc, 1);
+    orc_matvec(centroids, nc, d_t, bf, h, cl);
+    for (int v = 0; v < V; ++v) z[v] = -1e30;
+    int rc = 0;
+    for (int r = 0; r < kc && rc == 0; ++r) {
+        /* the next centroid: largest remaining logit, lowest id on ties, NaN last */
+        int best = -1;
+        for (int j = 0; j < nc; ++j) {
+            if (taken[j]) continue;
+            if (best < 0 || (isnan(cl[best]) && !isnan(cl[j])) || cl[j] > cl[best]) best = j;
+        }
+        taken[best] = 1;
+        for (int i = 0; i < vsc; ++i) {
+            const int32_t tk = ordering[(size_t)best * vsc + i];
+            if (tk < 0 || tk >= V) { rc = -1; break; }
+            double acc = 0.0;
+            for (int c = 0; c < d_t; ++c) acc += elem(tok_embd, (int64_t)tk * d_t + c, bf) * h[c];
+            if (m->logit_softcap > 0.0) acc = m->logit_softcap * tanh(acc / m->logit_softcap);
+            z[tk] = acc;
+        }
+    }
+    free(cl);
+    free(taken);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
 /* the draft step ([G4] sec. 4, [NX] Requirements)                           */
 /* ------------------------------------------------------------------------ */
 
@@ -468,11 +522,19 @@ int orc_draft_step(const orc_model *m, const void *const *t, const int32_t *bloc
         orc_rmsnorm(x, d_a, (const float *)TT(T_FINAL_NORM), m->rms_eps, a);
         double *hn = h_next + (size_t)b * d_t;
         orc_matvec(TT(T_W_POST), d_t, d_a, bf, a, hn);
-        /* tied dense LM head, optional final-logit softcap ([G4] sec. 4 items 6-7) */
         double *z = logits + (size_t)b * V;
-        orc_matvec(TT(T_TOK_EMBD), V, d_t, bf, hn, z);
-        if (m->logit_softcap > 0.0)
-            for (int v = 0; v < V; ++v) z[v] = m->logit_softcap * tanh(z[v] / m->logit_softcap);
+        if (m->n_centroids > 0) {
+            /* centroid-routed head ([G4] sec. 3) */
+            if (orc_centroid_head(m, TT(T_CENTROIDS), (const int32_t *)TT(T_ORDERING), TT(T_TOK_EMBD), hn, z)) {
+                free(e); free(u); free(x); free(a); free(q); free(o); free(y); free(yn); free(gt); free(up);
+                return -1;
+            }
+        } else {
+            /* tied dense LM head, optional final-logit softcap ([G4] sec. 4 items 6-7) */
+            orc_matvec(TT(T_TOK_EMBD), V, d_t, bf, hn, z);
+            if (m->logit_softcap > 0.0)
+                for (int v = 0; v < V; ++v) z[v] = m->logit_softcap * tanh(z[v] / m->logit_softcap);
+        }
     }
     (void)n_views;
     free(e); free(u); free(x); free(a); free(q); free(o); free(y); free(yn); free(gt); free(up);

@@ -115,6 +115,11 @@ def uniform_int(seed: int, name: str, shape, lo: int, hi: int) -> np.ndarray:
     return g.integers(lo, hi, size=shape, dtype=np.int64).astype(np.int32)
 
 
+def permutation(seed: int, name: str, n: int) -> np.ndarray:
+    """int32 uniformly random permutation of 0..n-1."""
+    return _stream(seed, name, 0).permutation(n).astype(np.int32)
+
+
 def _as_dtype(a: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return f32_to_bf16_bits(a)
@@ -145,6 +150,8 @@ class ModelSpec:
     block_view: tuple = (0,)     # per block: index of the KV view it cross-attends
     rms_eps: float = 1e-6
     logit_softcap: float = 0.0
+    n_centroids: int = 0         # > 0: centroid-routed LM head over n_centroids lists of vocab / n_centroids ids
+    centroid_top_k: int = 0      # centroids whose lists are scored per step
 
     @property
     def emb_scale(self) -> float:
@@ -205,11 +212,16 @@ def make_model_weights(m: ModelSpec, seed: int, std: float = 0.02) -> dict:
         norms[f"blk{i}.post_attn_norm"] = m.d_a
         norms[f"blk{i}.pre_ffn_norm"] = m.d_a
         norms[f"blk{i}.post_ffn_norm"] = m.d_a
+    if m.n_centroids:
+        shapes["centroids"] = (m.n_centroids, m.d_t)
     w = {}
     for name, shp in shapes.items():
         w[name] = _as_dtype(normal(seed, name, shp, std=std), m.dtype)
     for name, n in norms.items():
         w[name] = normal(seed, name, (n,), std=std, mean=1.0)
+    if m.n_centroids:
+        # ordered embeddings: every token in exactly one centroid's list
+        w["token_ordering"] = permutation(seed, "token_ordering", m.vocab)
     return w
 
 
