@@ -1012,7 +1012,7 @@ __device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsi
         return attn_piece(p, vw, kv, tab, view, cta, x, nx);
     };
     const bool packed = vw.st == HD;   // consecutive ring slots are contiguous rows
-    bool any_split = false, aok = true;
+    bool any_split = false, aok = true;   // aok: warp-uniform, false once a stage wait of the warp gave up
     // earlier generic shared-memory accesses before the stage copies
     fence_proxy_async_smem();
     __syncthreads();
@@ -1035,11 +1035,12 @@ __device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsi
         // lane 0: bulk copies of round rd's K and V rows into the warp's
         // stage rd % NST, one copy per run of consecutive ring slots when
         // rows are packed, completing on the stage barrier (nothing for an
-        // empty slice: its stage is neither filled nor waited on)
+        // empty slice: its stage is neither filled nor waited on; nothing
+        // once a wait of the warp gave up)
         auto issue = [&](int rd) {
             int t0;
             const int cnt = slice_cnt(rd, t0);
-            if (cnt > 0 && lane == 0) {
+            if (cnt > 0 && lane == 0 && aok) {
                 const int si = rd % NST;
                 unsigned char* buf = myring + si * SB;
                 unsigned long long* bar = abar + warp * NST + si;
@@ -1165,13 +1166,24 @@ __device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsi
                 ls[hh] = 0.f;
             }
 
-            for (int i = 0; i < nrounds; ++i) {
+            for (int i = 0; i < nrounds && aok; ++i) {
                 issue(i + NST - 1);   // its stage was consumed in round i - 1
                 int t0;
                 const int cnt = slice_cnt(i, t0);
                 if (cnt > 0) {
                     const int si = i % NST;
-                    if (!mbar_wait_limited(abar + warp * NST + si, (apar >> si) & 1u, p.timeout_ns)) aok = false;
+                    if (!__all_sync(0xffffffffu, mbar_wait_limited(abar + warp * NST + si, (apar >> si) & 1u, p.timeout_ns))) {
+                        // give up the pass: first wait (bounded again) for this
+                        // round's and the issued later rounds' copies, so that
+                        // none lands in shared memory afterwards
+                        for (int r = i; r < i + NST && r < nrounds; ++r) {
+                            int tr;
+                            if (slice_cnt(r, tr) > 0)
+                                mbar_wait_limited(abar + warp * NST + r % NST, (apar >> (r % NST)) & 1u, p.timeout_ns);
+                        }
+                        aok = false;
+                        break;
+                    }
                     apar ^= 1u << si;
                     const unsigned char* kb = myring + si * SB;
                     const unsigned char* vb = kb + R * RB;
@@ -1810,6 +1822,12 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
         const int q = warp - 4;   // tensor-memory lane quarter of this warp
         const int b = 16 * q + lane;
         const bool mine = lane < 16 && b < p.B;
+        const int V = p.V;
+        const float sc = p.softcap;
+        float* const lg = p.out_logits ? p.out_logits + (long long)b * p.N * V + (long long)k * V : nullptr;
+        float* const zb = p.ZB ? p.ZB + (long long)b * V : nullptr;
+        // nothing to store, no softcap, no denominators: only the argmax
+        const bool plain = !CONF && lg == nullptr && zb == nullptr && !(sc > 0.f);
         unsigned long long best = 0ull;
         SoftDen den = soft_den0();
         for (int j = 0; j < nit && ok; ++j) {
@@ -1821,23 +1839,44 @@ static __device__ __noinline__ bool tc_head(const DraftParams& p, int k, unsigne
             tc_fence_after();
             const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * kTcHeadN;
             const uint32_t ta = ts.tmem + ((uint32_t)(32 * q) << 16) + acc * (uint32_t)kTcHeadN;
-            for (int c0 = 0; c0 < kTcHeadN; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(ta + (uint32_t)c0, r);
+            for (int c0 = 0; c0 < kTcHeadN; c0 += 32) {
+                uint32_t ra[16], rb[16];   // two loads in flight, one wait
+                tmem_ld16(ta + (uint32_t)c0, ra);
+                tmem_ld16(ta + (uint32_t)c0 + 16u, rb);
                 tmem_ld_wait();
-                if (mine) {
+                auto val = [&](int jj) { return __uint_as_float(jj < 16 ? ra[jj] : rb[jj - 16]); };
+                if (!mine) continue;
+                if (plain && row0 + c0 + 32 <= V) {
+                    // the chunk's maximum by a tree, then its first position:
+                    // the same key as the element-wise packed maximum (NaN
+                    // only if all are NaN: key 0 at the first index; -0 and
+                    // +0 compare equal)
+                    float t[16];
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int row = row0 + c0 + jj;
-                        if (row < p.V) {
-                            float z = __uint_as_float(r[jj]);
-                            if (p.softcap > 0.f) z = p.softcap * tanhf(z / p.softcap);
-                            if (p.out_logits) p.out_logits[((long long)b * p.N + k) * p.V + row] = z;
-                            if (p.ZB) p.ZB[(long long)b * p.V + row] = z;
-                            const unsigned long long key = pack_argmax(z, (uint32_t)row);
-                            best = key > best ? key : best;
-                            if constexpr (CONF) den.add(z);
-                        }
+                    for (int jj = 0; jj < 16; ++jj) t[jj] = fmaxf(val(jj), val(jj + 16));
+#pragma unroll
+                    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                        for (int jj = 0; jj < w; ++jj) t[jj] = fmaxf(t[jj], t[jj + w]);
+                    const float m = t[0];
+                    int ci = 0;
+#pragma unroll
+                    for (int jj = 31; jj >= 0; --jj) ci = val(jj) == m ? jj : ci;
+                    const unsigned long long key = pack_argmax(m, (uint32_t)(row0 + c0 + ci));
+                    best = key > best ? key : best;
+                    continue;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int row = row0 + c0 + jj;
+                    if (row < V) {
+                        float z = val(jj);
+                        if (sc > 0.f) z = sc * tanhf(z / sc);
+                        if (lg) lg[row] = z;
+                        if (zb) zb[row] = z;
+                        const unsigned long long key = pack_argmax(z, (uint32_t)row);
+                        best = key > best ? key : best;
+                        if constexpr (CONF) den.add(z);
                     }
                 }
             }
