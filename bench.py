@@ -9,8 +9,9 @@ d_t 5120, d_a 1024, 4 blocks, 16 x 256 query heads over 4 KV heads, GeGLU
 4096, vocab 262144, B = 1, N = 3, 8192 cached positions; 3 blocks attend a
 1024-window sliding layer, 1 a full layer).  The default run also times the
 same model at B = 16 (N = 4, ragged 2k-32k contexts) and B = 64 (N = 2,
-context 4096), and exact temp > 0 verification alone (mtp_verify_sample,
-B = 32, N = 3, V = 248320; that configuration has no draft block), each
+context 4096), exact temp > 0 verification alone (mtp_verify_sample,
+B = 32, N = 3, V = 248320; that configuration has no draft block), and an
+Edge-shaped drafter with the centroid-routed LM head (B = 1, N = 3), each
 reported under per_workload with its own roofline fraction, end-to-end
 number and CPU baseline.  `--workload K` times one of them alone.
 
@@ -40,7 +41,7 @@ import synth  # noqa: E402
 METRIC = "drafted tok/s (MTP draft block + verify) at B=1..64; % of HBM/tensor roofline"
 UNIT = "tok/s"
 HEADLINE = 1
-OTHERS = (2, 3, 4)
+OTHERS = (2, 3, 4, 5)
 
 
 def parse(argv=None):
@@ -49,8 +50,8 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4],
-                    help="time this workload alone (default: the headline plus workloads 2-4)")
+    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4, 5],
+                    help="time this workload alone (default: the headline plus workloads 2-5)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
 
@@ -89,9 +90,11 @@ def _common(world: int, flushed: bool) -> dict:
 
 def draft_config(w, world: int = 1) -> dict:
     m = w.model
+    head = (f"centroid-routed: {m.n_centroids} lists of {m.vocab // m.n_centroids}, top {m.centroid_top_k}"
+            if m.n_centroids else "dense tied")
     return dict({"workload": w.name, "B": w.B, "N": w.N, "vocab": m.vocab, "d_t": m.d_t, "d_a": m.d_a,
-                 "n_blocks": m.n_blocks, "kv_len_max": int(w.kv_len.max()), "kv_len_min": int(w.kv_len.min())},
-                **_common(world, False))
+                 "n_blocks": m.n_blocks, "kv_len_max": int(w.kv_len.max()), "kv_len_min": int(w.kv_len.min()),
+                 "lm_head": head}, **_common(world, False))
 
 
 def sample_config(inp, world: int = 1) -> dict:
@@ -119,10 +122,27 @@ def kv_bytes_per_step(w) -> int:
     return tot
 
 
-def draft_bytes_per_launch(w) -> int:
+def head_bytes_per_step(w) -> int:
+    """The LM head's bytes: the dense head reads the whole table; the
+    centroid-routed head the centroids, and per sequence the top_k lists'
+    ids and their table rows."""
     m = w.model
     esz = 2 if m.dtype == "bf16" else 4
-    per_step = w.weight_bytes() + kv_bytes_per_step(w) + w.B * m.d_t * esz
+    if not m.n_centroids:
+        return m.vocab * m.d_t * esz
+    cand = m.centroid_top_k * (m.vocab // m.n_centroids)
+    return m.n_centroids * m.d_t * esz + w.B * cand * (m.d_t * esz + 4)
+
+
+def draft_bytes_per_launch(w) -> int:
+    """Weights (the head's share per head_bytes_per_step), each view's KV
+    once, and the consumed tokens' embedding rows, per step."""
+    m = w.model
+    esz = 2 if m.dtype == "bf16" else 4
+    head_w = m.vocab * m.d_t * esz + sum(int(w.weights[n].nbytes) for n in ("centroids", "token_ordering")
+                                         if n in w.weights)
+    per_step = (w.weight_bytes() - head_w + head_bytes_per_step(w) + kv_bytes_per_step(w) +
+                w.B * m.d_t * esz)
     return w.N * per_step
 
 

@@ -71,6 +71,7 @@ enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 };
 #define MTP_MAX_VIEWS 4
 #define MTP_MAX_BATCH 64            /* sequences of one mtp_draft_block call */
 #define MTP_MAX_VERIFY_BATCH 65536  /* sequences of one verify or draw call */
+#define MTP_MAX_CENTROIDS 8192      /* centroids of a centroid-routed LM head */
 
 /* Sizes and scalars of the assistant head ([G4] sec. 3-4).
  *   d_t        backbone (target) width: token embedding, h_prev, LM head input
@@ -83,11 +84,19 @@ enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 };
  *   wdtype     MTP_DTYPE_BF16 or MTP_DTYPE_F32: weight matrices and KV
  *   rms_eps    RMSNorm epsilon; attn_scale softmax scale (usually 1/sqrt(head_dim));
  *   emb_scale  token-embedding scale (sqrt(d_t) for Gemma);
- *   logit_softcap  > 0 applies cap * tanh(z / cap) to the logits, 0 = off */
+ *   logit_softcap  > 0 applies cap * tanh(z / cap) to the logits, 0 = off
+ *   n_centroids    0: the dense tied LM head.  > 0: the centroid-routed head
+ *                  of ordered-embedding models ([G4] sec. 3 "Centroid /
+ *                  ordered-embeddings LM head"), n_centroids <=
+ *                  MTP_MAX_CENTROIDS dividing vocab (MTP_ERR_ARG otherwise;
+ *                  above the maximum MTP_ERR_UNSUPPORTED)
+ *   centroid_top_k centroids whose candidate lists are scored per step,
+ *                  1..n_centroids (ignored for the dense head, must be >= 0) */
 typedef struct mtp_config {
     int32_t d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab;
     int32_t wdtype;
     float rms_eps, attn_scale, emb_scale, logit_softcap;
+    int32_t n_centroids, centroid_top_k;
 } mtp_config;
 
 /* One assistant block.  Matrices are row-major [out, in] in `wdtype`; RMSNorm
@@ -115,6 +124,11 @@ typedef struct mtp_weights {
     const void *final_norm;  /* fp32 [d_a] */
     const void *w_post;      /* [d_t, d_a]: post-projection -> next h_prev */
     mtp_block_weights blk[MTP_MAX_BLOCKS];
+    /* centroid-routed head only (NULL for the dense head): */
+    const void *centroids;           /* [n_centroids, d_t] in wdtype, 16-byte aligned */
+    const int32_t *token_ordering;   /* [vocab]: n_centroids consecutive lists of
+                                      * vocab / n_centroids token ids, list j the
+                                      * candidates of centroid j */
 } mtp_weights;
 
 /* A read-only view of one target KV layer ([G4] sec. 5).  K and V share the
@@ -164,6 +178,11 @@ size_t mtp_workspace_size(const mtp_config *cfg, int B, int N, int V);
  *              x += rmsnorm(w_o o); x += rmsnorm(w_down(gelu_tanh(w_gate n) * w_up n)),
  *              n = rmsnorm(x; pre_ffn_norm)
  *   h_{k+1} = w_post rmsnorm(x; final_norm);  z = tok_embd h_{k+1} (softcap)
+ *   (centroid-routed head, cfg->n_centroids > 0: z is -1e30 except at the
+ *   candidates, the lists of the centroid_top_k centroids with the largest
+ *   centroids[j] . h_{k+1} (lower j on ties), where z_t = tok_embd[t] h_{k+1}
+ *   (softcap); an ordering entry outside [0, vocab) is skipped and sets the
+ *   status word to MTP_ERR_ARG)
  *   draft_k = argmax z (lowest index on ties), or, when sp != NULL and
  *   sp->temp > 0, a draw from sample_dist(z) with penalty set hist[b] u
  *   {draft_0..draft_{k-1}} and the Philox-4x32-10 uniform of counter

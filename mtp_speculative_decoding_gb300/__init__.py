@@ -45,7 +45,8 @@ class Config(C.Structure):
     _fields_ = [("d_t", C.c_int32), ("d_a", C.c_int32), ("n_blocks", C.c_int32), ("n_q_heads", C.c_int32),
                 ("head_dim", C.c_int32), ("n_kv_heads", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
                 ("wdtype", C.c_int32), ("rms_eps", C.c_float), ("attn_scale", C.c_float),
-                ("emb_scale", C.c_float), ("logit_softcap", C.c_float)]
+                ("emb_scale", C.c_float), ("logit_softcap", C.c_float), ("n_centroids", C.c_int32),
+                ("centroid_top_k", C.c_int32)]
 
 
 class BlockWeights(C.Structure):
@@ -57,7 +58,8 @@ class BlockWeights(C.Structure):
 
 class Weights(C.Structure):
     _fields_ = [("tok_embd", C.c_void_p), ("norm_e", C.c_void_p), ("norm_h", C.c_void_p), ("w_pre", C.c_void_p),
-                ("final_norm", C.c_void_p), ("w_post", C.c_void_p), ("blk", BlockWeights * MTP_MAX_BLOCKS)]
+                ("final_norm", C.c_void_p), ("w_post", C.c_void_p), ("blk", BlockWeights * MTP_MAX_BLOCKS),
+                ("centroids", C.c_void_p), ("token_ordering", C.c_void_p)]
 
 
 class KVView(C.Structure):
@@ -152,12 +154,13 @@ def _dtype_code(t) -> int:
 # ----------------------------------------------------------------------------
 
 def make_config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab, wdtype="bf16",
-                rms_eps=1e-6, attn_scale=None, emb_scale=None, logit_softcap=0.0) -> Config:
+                rms_eps=1e-6, attn_scale=None, emb_scale=None, logit_softcap=0.0, n_centroids=0,
+                centroid_top_k=0) -> Config:
     import math
     return Config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab,
                   MTP_DTYPE_BF16 if wdtype == "bf16" else MTP_DTYPE_F32, rms_eps,
                   1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale,
-                  math.sqrt(d_t) if emb_scale is None else emb_scale, logit_softcap)
+                  math.sqrt(d_t) if emb_scale is None else emb_scale, logit_softcap, n_centroids, centroid_top_k)
 
 
 def workspace_size(cfg: Config | None, B: int, N: int, V: int) -> int:
@@ -183,10 +186,14 @@ BLOCK_TENSORS = ("attn_norm", "w_q", "q_norm", "w_o", "post_attn_norm", "pre_ffn
 
 
 def make_weights(tensors: dict, n_blocks: int, block_view) -> Weights:
-    """Pack device tensors (keys: GLOBAL_TENSORS and 'blk{i}.<name>') into mtp_weights."""
+    """Pack device tensors (keys: GLOBAL_TENSORS, 'blk{i}.<name>' and, for a
+    centroid-routed head, 'centroids' and 'token_ordering') into mtp_weights."""
     w = Weights()
     for n in GLOBAL_TENSORS:
         setattr(w, n, tensors[n].data_ptr())
+    for n in ("centroids", "token_ordering"):
+        if n in tensors:
+            setattr(w, n, tensors[n].data_ptr())
     for i in range(n_blocks):
         b = w.blk[i]
         for n in BLOCK_TENSORS:

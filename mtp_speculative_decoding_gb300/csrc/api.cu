@@ -36,8 +36,19 @@ int num_sms() {
     return n;
 }
 
-// LM head on tensor cores: bf16 weights and a batch of at least kTcMinBatch
-bool tc_head_eligible(const mtp_config* c, int B) { return c->wdtype == MTP_DTYPE_BF16 && B >= kTcMinBatch; }
+// LM head on tensor cores: the dense head, bf16 weights and a batch of at
+// least kTcMinBatch
+bool tc_head_eligible(const mtp_config* c, int B) {
+    return c->wdtype == MTP_DTYPE_BF16 && B >= kTcMinBatch && c->n_centroids == 0;
+}
+
+// centroid-routed head: shared memory of its per-CTA sort (keys over n_c
+// rounded up to a power of two, the rank sort's scratch, the selection)
+size_t cent_smem(const mtp_config* c) {
+    size_t P = 1;
+    while (P < (size_t)c->n_centroids) P <<= 1;
+    return (P + kRankSortMax) * sizeof(unsigned long long) + (size_t)c->centroid_top_k * sizeof(int);
+}
 int pad16(int B) { return (B + 15) & ~15; }
 
 size_t draft_smem(const mtp_config* c, int B, int act_smem);
@@ -80,7 +91,7 @@ int draft_grid() {
 }
 
 struct DraftLayout {
-    size_t att_cnt, SROW, amax, XB, XM, QR, OB, YB, MB, Y2, HN, PART, CONF, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ZB, SBUF, ACT, end;
+    size_t att_cnt, SROW, amax, XB, XM, QR, OB, YB, MB, Y2, HN, CL, PART, CONF, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ZB, SBUF, ACT, end;
     int kmax;
 };
 
@@ -114,6 +125,7 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     L.MB = off;      off = al256(off + (size_t)B * c->d_ff * f);
     L.Y2 = off;      off = al256(off + (size_t)B * c->d_a * f);
     L.HN = off;      off = al256(off + (size_t)B * c->d_t * f);
+    L.CL = off;      off = al256(off + (size_t)B * c->n_centroids * f);
     const size_t items = 2 * (size_t)kMaxGrid + (size_t)B * c->n_kv_heads;
     L.PART = off;    off = al256(off + items * attn_psz(grp, c->head_dim) * f);
     L.CONF = off;    off = al256(off + (size_t)kMaxGrid * B * 2 * f);
@@ -234,6 +246,11 @@ int check_config(const mtp_config* c) {
     const int m = 8;  // row lengths in elements: 16-byte rows for either dtype
     if (c->d_t % m || c->d_a % m || c->d_ff % m || (c->n_q_heads * hd) % m) return MTP_ERR_UNSUPPORTED;
     if (!(c->rms_eps >= 0.f) || !(c->attn_scale > 0.f) || !(c->logit_softcap >= 0.f)) return MTP_ERR_ARG;
+    if (c->n_centroids < 0 || c->centroid_top_k < 0) return MTP_ERR_ARG;
+    if (c->n_centroids > 0) {
+        if (c->n_centroids > MTP_MAX_CENTROIDS) return MTP_ERR_UNSUPPORTED;
+        if (c->centroid_top_k < 1 || c->centroid_top_k > c->n_centroids || c->vocab % c->n_centroids) return MTP_ERR_ARG;
+    }
     return MTP_OK;
 }
 
@@ -340,6 +357,10 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     // weights
     const void* mats[] = {w->tok_embd, w->w_pre, w->w_post};
     for (const void* m : mats) if (!m || !aligned16(m)) return MTP_ERR_ARG;
+    const bool cent = cfg->n_centroids > 0;
+    if (cent && (!w->centroids || !aligned16(w->centroids) || !w->token_ordering ||
+                 (reinterpret_cast<uintptr_t>(w->token_ordering) & 3)))
+        return MTP_ERR_ARG;
     if (!w->norm_e || !w->norm_h || !w->final_norm) return MTP_ERR_ARG;
     for (int l = 0; l < cfg->n_blocks; ++l) {
         const mtp_block_weights& b = w->blk[l];
@@ -373,7 +394,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     const int grid = draft_grid();
     // one sequence: LM head rows through bulk-copy slots at offset 0
     int head_slotb = 0;
-    if (B == 1 && (size_t)cfg->d_t * esz / 16 <= (size_t)kHeadMaxChunks) {
+    if (!cent && B == 1 && (size_t)cfg->d_t * esz / 16 <= (size_t)kHeadMaxChunks) {
         const size_t slotb = ((size_t)cfg->d_t * esz + 127) & ~(size_t)127;
         const size_t ring = (size_t)kHeadGroups * kHeadSlots * slotb;
         if (ring <= kSmemLimit) {
@@ -399,6 +420,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         if (need > smem) smem = need;
         tc_cols = kTcHeadCols;   // the head's two accumulators; the projections use the first 2 Bp columns
     }
+    if (cent && cent_smem(cfg) > smem) smem = cent_smem(cfg);   // at most 100 KB (n_c <= MTP_MAX_CENTROIDS)
     const int per_sm = !bf ? draft_blocks_per_sm_f32(cfg->head_dim, smem)
                        : tc ? draft_blocks_per_sm_bf16_tc(cfg->head_dim, smem)
                             : draft_blocks_per_sm_bf16_cc(cfg->head_dim, smem);
@@ -453,6 +475,13 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     p.ROPE = reinterpret_cast<double*>(base + L.ROPE);
     p.ROPEQ = reinterpret_cast<float2*>(base + L.ROPEQ);
     p.ACT = reinterpret_cast<float*>(base + L.ACT);
+    if (cent) {
+        p.n_cent = cfg->n_centroids;
+        p.cent_k = cfg->centroid_top_k;
+        p.cent = w->centroids;
+        p.cord = w->token_ordering;
+        p.CL = reinterpret_cast<float*>(base + L.CL);
+    }
     p.act_smem = act_smem;
     p.head_slotb = head_slotb;
     if (tc) {

@@ -143,6 +143,12 @@ struct DraftParams {
     unsigned int* S_row;         // [4][B]: row maximum key, survivor count, overflow flag, pieces done
     int2* S_buf;                 // [B][S_rcap] survivors
     int S_rcap, S_plen, S_ppr;   // survivor capacity per row, tokens per piece, pieces per row
+    // centroid-routed LM head (n_cent > 0): centroids [n_cent, d_t] (weight
+    // type), token ordering [V] int32, the step's centroid logits [B, n_cent]
+    int n_cent, cent_k;
+    const void* cent;
+    const int32_t* cord;
+    float* CL;
 };
 
 cudaError_t launch_draft_f32(const DraftParams& p, int grid, size_t smem, cudaStream_t s);

@@ -2034,6 +2034,129 @@ __device__ __forceinline__ bool head_phase(const DraftParams& p, int k, const fl
     return true;
 }
 
+// ---------------------------------------------------------------------------
+// centroid-routed LM head (Gemma 4 MTP page, sec. 3 "Centroid / ordered-
+// embeddings LM head")
+// ---------------------------------------------------------------------------
+// Step k's logits over the candidates of each sequence's top_k centroids.
+//   pass 1 (grid): CL[b, j] = centroids[j] . h_b over the n_c rows, and the
+//     logit rows asked for (out_logits row (b, k), the sampler's ZB row b)
+//     set to -1e30; a grid barrier.
+//   pass 2 (no barrier): CTA c serves sequence b = c % B (b = c, c + G, ...
+//     when the grid G is smaller than B).  It sorts b's n_c centroid keys
+//     (value desc, id asc, NaN last) in shared memory, takes the first
+//     top_k, and scores its share of their top_k * vsc candidates (centroid
+//     j's list: the vsc ids at token_ordering[j vsc ...]):
+//     z = softcap(tok_embd[t] . h_b), stored at t in the rows asked for,
+//     folded into amax[k, b] and, with confidence, into the CTA's softmax
+//     partial of b.  The CTAs serving one sequence each sort its keys (a few
+//     microseconds) instead of meeting at a second barrier.
+// An ordering entry outside [0, V) is skipped and sets the status to
+// MTP_ERR_ARG.  Shared memory: (P + kRankSortMax) 8-byte keys (P = n_c
+// rounded up to a power of two) and top_k ints.
+template <typename WT>
+static __device__ __noinline__ bool centroid_head(const DraftParams& p, int k, unsigned char* smem, float* red,
+                                                  unsigned long long (*head_best)[32], unsigned int& epoch) {
+    constexpr int EPC = Chunk<WT>::EPC, U = 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nc = p.n_cent, kc = p.cent_k, vsc = p.V / nc, B = p.B, G = (int)gridDim.x;
+    const long long V = p.V;
+    {
+        StoreEpi e{p.CL, nc};
+        gemv<WT, 8, false>(reinterpret_cast<const WT*>(p.cent), nullptr, nc, p.d_t, p.HN, p.d_t, B, e, red);
+    }
+    const long long nl = p.out_logits ? (long long)B * V : 0, nz = p.ZB ? (long long)B * V : 0;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nl + nz; i += (long long)G * blockDim.x) {
+        if (i < nl) {
+            const long long b = i / V;
+            p.out_logits[(b * p.N + k) * V + (i - b * V)] = -1e30f;
+        } else {
+            p.ZB[i - nl] = -1e30f;
+        }
+    }
+    if (!grid_barrier(p.hdr, epoch, p.timeout_ns, G)) return false;
+
+    unsigned int P = 1;
+    while (P < (unsigned int)nc) P <<= 1;
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
+    unsigned long long* tmp = keys + P;
+    int* sel = reinterpret_cast<int*>(tmp + kRankSortMax);
+    if (p.out_conf)   // partials of the sequences this CTA does not serve stay empty
+        for (int b = threadIdx.x; b < B; b += blockDim.x) p.CONF[(long long)blockIdx.x * B + b] = make_float2(-INFINITY, 0.f);
+    const int nch = p.d_t / EPC, nrow = kc * vsc;
+    const float sc = p.softcap;
+    const unsigned long long pol = l2_evict_first();
+    const bool wide = G >= B;
+    for (int b = wide ? (int)blockIdx.x % B : (int)blockIdx.x; b < B; b += wide ? B : G) {
+        const int gi = wide ? (int)blockIdx.x / B : 0, gn = wide ? (G - b + B - 1) / B : 1;
+        const float* cl = p.CL + (long long)b * nc;
+        __syncthreads();   // the previous sequence's keys and selection are consumed
+        for (int j = threadIdx.x; j < nc; j += blockDim.x)
+            keys[j] = ((unsigned long long)(~ordered_key(__ldcg(cl + j))) << 32) | (unsigned int)j;
+        __syncthreads();
+        sort_keys(keys, (unsigned int)nc, tmp);
+        for (int r = threadIdx.x; r < kc; r += blockDim.x) sel[r] = (int)(keys[r] & 0xFFFFFFFFull);
+        __syncthreads();
+        const int lo = (int)((long long)nrow * gi / gn), hi = (int)((long long)nrow * (gi + 1) / gn);
+        const float* h = p.HN + (long long)b * p.d_t;
+        float* lg = p.out_logits ? p.out_logits + ((long long)b * p.N + k) * V : nullptr;
+        float* zb = p.ZB ? p.ZB + (long long)b * V : nullptr;
+        unsigned long long best = 0ull;
+        SoftDen den = soft_den0();
+        for (int r = lo + warp; r < hi; r += kWarps) {
+            const int t = __ldg(p.cord + (long long)sel[r / vsc] * vsc + (r % vsc));
+            if (t < 0 || (long long)t >= V) {
+                if (lane == 0) atomicCAS(&p.hdr->status, 0, MTP_ERR_ARG);
+                continue;
+            }
+            const uint4* wr = reinterpret_cast<const uint4*>(reinterpret_cast<const WT*>(p.tok_embd) + (long long)t * p.d_t);
+            float acc = 0.f;
+            for (int c0 = 0; c0 < nch; c0 += 32 * U) {
+                uint4 w[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + lane + 32 * u;
+                    w[u] = c < nch ? ld_weight16(wr + c, pol) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + lane + 32 * u;
+                    if (c < nch) acc += Chunk<WT>::dot(w[u], h + c * EPC);
+                }
+            }
+            float z = warp_sum(acc);   // every lane holds the row's logit
+            if (sc > 0.f) z = sc * tanhf(z / sc);
+            if (lane == 0) {
+                if (lg) lg[t] = z;
+                if (zb) zb[t] = z;
+            }
+            const unsigned long long key = pack_argmax(z, (uint32_t)t);
+            best = key > best ? key : best;
+            if (p.out_conf) den.add(z);
+        }
+        // the CTA's merge: one key and one softmax partial per warp
+        float* hm = reinterpret_cast<float*>(&head_best[warp][1]);
+        if (lane == 0) {
+            head_best[warp][0] = best;
+            hm[0] = den.m;
+            hm[1] = den.s;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned long long m = 0ull;
+            SoftDen t = soft_den0();
+            for (int w = 0; w < kWarps; ++w) {
+                m = head_best[w][0] > m ? head_best[w][0] : m;
+                const float* hw = reinterpret_cast<const float*>(&head_best[w][1]);
+                t.merge(hw[0], hw[1]);
+            }
+            if (hi > lo) atomicMax(p.amax + (long long)k * B + b, m);
+            if (p.out_conf) p.CONF[(long long)blockIdx.x * B + b] = make_float2(t.m, t.s);
+        }
+    }
+    return true;
+}
+
 // Confidence of step k for sequence b (one warp): the top-1 softmax
 // probability 1 / S, S the merged softmax denominator of the CTAs' partials
 // (relative to their common maximum, the top logit).
@@ -2288,7 +2411,9 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         }
         // ---- HEAD ----
-        {
+        if (p.n_cent > 0) {
+            if (!centroid_head<WT>(p, k, smem, red, head_best, epoch)) return;
+        } else {
             int lda = 0;
             const float* a = nullptr;
             if (p.head_slotb == 0 && !(TC && p.tc_head)) {

@@ -56,7 +56,8 @@ def upload_draft(w, device="cuda", extra_ws_for=None, reuse: "DeviceDraft | None
     m = w.model
     cfg = make_config(m.d_t, m.d_a, m.n_blocks, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff, m.vocab,
                       wdtype=m.dtype, rms_eps=m.rms_eps, attn_scale=m.attn_scale, emb_scale=m.emb_scale,
-                      logit_softcap=m.logit_softcap)
+                      logit_softcap=m.logit_softcap, n_centroids=getattr(m, "n_centroids", 0),
+                      centroid_top_k=getattr(m, "centroid_top_k", 0))
     same = (reuse is not None and bytes(reuse.cfg) == bytes(cfg) and
             all(n in reuse.tensors and tuple(reuse.tensors[n].shape) == a.shape for n, a in w.weights.items()))
     if same:

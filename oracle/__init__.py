@@ -83,10 +83,10 @@ def _declare(L):
     L.orc_sample_dist.restype = I
     L.orc_pick.argtypes = [P, P, I, D, D, P]
     L.orc_pick.restype = C.c_int32
-    L.orc_draft_step.argtypes = [P, P, P, P, I, I, P, I, P, P, P, P]
+    L.orc_draft_step.argtypes = [P, P, P, P, I, I, P, I, P, P, P, P, P]
     L.orc_draft_step.restype = I
-    L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, I, P, I, P, P, P, P, P, P]
-    L.orc_centroid_head.argtypes = [P, P, P, P, P, P]
+    L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, I, P, I, P, P, P, P, P, P, P]
+    L.orc_centroid_head.argtypes = [P, P, P, P, P, P, P, P]
     L.orc_centroid_head.restype = I
     L.orc_top1_prob.argtypes = [P, C.c_int64]
     L.orc_top1_prob.restype = D
@@ -220,8 +220,10 @@ def _model(m) -> Model:
                  m.rms_eps, m.attn_scale, m.emb_scale, m.logit_softcap)
 
 
-def centroid_head(m, centroids, ordering, tok_embd, h):
-    """The centroid-routed head's full logit row [V] (f64) for one hidden state h [d_t].
+def centroid_head(m, centroids, ordering, tok_embd, h, full=False):
+    """The centroid-routed head's full logit row [V] (f64) for one hidden state h [d_t];
+    with ``full``, (row, cgap, centroid logits [n_c]), cgap the set margin
+    relative to the centroid logits' standard deviation.
 
     ``m``: a model spec with n_centroids / centroid_top_k / vocab / d_t / dtype /
     logit_softcap; matrices fp32, or uint16 bf16 bits when m.dtype == 'bf16'."""
@@ -231,9 +233,11 @@ def centroid_head(m, centroids, ordering, tok_embd, h):
     h = np.ascontiguousarray(h, dtype=np.float64)
     z = np.empty(m.vocab, dtype=np.float64)
     mdl = _model(m)
-    if lib().orc_centroid_head(C.byref(mdl), _p(c), _p(o), _p(e), _p(h), _p(z)) != 0:
+    gap = C.c_double()
+    cl = np.empty(max(1, m.n_centroids), dtype=np.float64)
+    if lib().orc_centroid_head(C.byref(mdl), _p(c), _p(o), _p(e), _p(h), _p(z), C.byref(gap), _p(cl)) != 0:
         raise ValueError("oracle centroid head rejected its inputs")
-    return z
+    return (z, gap.value, cl) if full else z
 
 
 class _Bound:
@@ -275,7 +279,8 @@ def draft_block(w, sample=None, seed=0, offset=0, force=None, seqs=None, want_lo
     step k+1 to force[b, k] instead of the oracle's own pick.
     Returns dict(drafts [S,N] int32, h_last [S,d_t] f64, logits [S,N,V] f64 or
     None, margin [S,N] f64, conf [S,N] f64: each step's top-1 softmax
-    probability) for the S selected sequences, in ``seqs`` order.
+    probability, cgap [S,N] f64: the centroid-routed head's set margin, +inf
+    for the dense head) for the S selected sequences, in ``seqs`` order.
     """
     L = lib()
     m = w.model
@@ -286,6 +291,7 @@ def draft_block(w, sample=None, seed=0, offset=0, force=None, seqs=None, want_lo
     out_z = np.empty((S, N, V), dtype=np.float64) if want_logits else None
     out_m = np.empty((S, N), dtype=np.float64)
     out_c = np.empty((S, N), dtype=np.float64)
+    out_g = np.empty((S, N), dtype=np.float64)
     prm = make_params(sample) if sample is not None else None
     for j, b in enumerate(seqs):
         bd = _Bound(w, b)
@@ -295,16 +301,17 @@ def draft_block(w, sample=None, seed=0, offset=0, force=None, seqs=None, want_lo
         z = np.empty((1, N, V), dtype=np.float64) if want_logits else None
         mg = np.empty((1, N), dtype=np.float64)
         cf = np.empty((1, N), dtype=np.float64)
+        cg = np.empty((1, N), dtype=np.float64)
         rc = L.orc_draft_block(C.byref(bd.model), bd.tensors, _p(bd.block_view), bd.views, bd.n_views,
                                1, N, _p(bd.kv_len), _p(bd.last_tok), _p(bd.h_prev),
                                C.byref(prm) if prm is not None else None, seed, offset, b,
-                               _p(bd.hist), bd.hist.shape[1], _p(f), _p(d), _p(h), _p(z), _p(mg), _p(cf))
+                               _p(bd.hist), bd.hist.shape[1], _p(f), _p(d), _p(h), _p(z), _p(mg), _p(cf), _p(cg))
         if rc != 0:
             raise ValueError(f"oracle draft block rejected its inputs (rc={rc})")
-        out_d[j], out_h[j], out_m[j], out_c[j] = d[0], h[0], mg[0], cf[0]
+        out_d[j], out_h[j], out_m[j], out_c[j], out_g[j] = d[0], h[0], mg[0], cf[0], cg[0]
         if want_logits:
             out_z[j] = z[0]
-    return dict(drafts=out_d, h_last=out_h, logits=out_z, margin=out_m, conf=out_c)
+    return dict(drafts=out_d, h_last=out_h, logits=out_z, margin=out_m, conf=out_c, cgap=out_g)
 
 
 def draft_step(w, b, step, tok, h_prev):
@@ -317,7 +324,7 @@ def draft_step(w, b, step, tok, h_prev):
     hn = np.empty((1, m.d_t), dtype=np.float64)
     z = np.empty((1, m.vocab), dtype=np.float64)
     rc = L.orc_draft_step(C.byref(bd.model), bd.tensors, _p(bd.block_view), bd.views, bd.n_views, 1,
-                          _p(bd.kv_len), step, _p(tk), _p(h), _p(hn), _p(z))
+                          _p(bd.kv_len), step, _p(tk), _p(h), _p(hn), _p(z), None)
     if rc != 0:
         raise ValueError("oracle draft step rejected its inputs")
     return hn[0], z[0]

@@ -420,9 +420,13 @@ int32_t orc_pick(const int32_t *ids, const double *w, int n, double wsum, double
  *      same final softcap (reading: the cap applies to the candidates'
  *      logits, before the scatter);
  *   5. every other entry of the row holds -1e30.
+ * cgap (optional): the chosen set's margin, the top_k-th largest centroid
+ * logit minus the next one, over the population standard deviation of the
+ * centroid logits (+inf when top_k = n_c or that deviation is 0).
+ * cl (optional): the centroid logits [n_c].
  * Returns 0, or -1 for invalid sizes or an ordering entry outside [0, V). */
 int orc_centroid_head(const orc_model *m, const void *centroids, const int32_t *ordering,
-                      const void *tok_embd, const double *h, double *z) {
+                      const void *tok_embd, const double *h, double *z, double *cgap, double *cl_out) {
     const int nc = m->n_centroids, kc = m->centroid_top_k, V = m->vocab, d_t = m->d_t, bf = m->wbf16;
     if (nc <= 0 || kc <= 0 || kc > nc || V % nc != 0) return -1;
     const int vsc = V / nc;
@@ -431,6 +435,7 @@ int orc_centroid_head(const orc_model *m, const void *centroids, const int32_t *
     orc_matvec(centroids, nc, d_t, bf, h, cl);
     for (int v = 0; v < V; ++v) z[v] = -1e30;
     int rc = 0;
+    double last = INFINITY;
     for (int r = 0; r < kc && rc == 0; ++r) {
         /* the next centroid: largest remaining logit, lowest id on ties, NaN last */
         int best = -1;
@@ -439,6 +444,7 @@ int orc_centroid_head(const orc_model *m, const void *centroids, const int32_t *
             if (best < 0 || (isnan(cl[best]) && !isnan(cl[j])) || cl[j] > cl[best]) best = j;
         }
         taken[best] = 1;
+        last = cl[best];
         for (int i = 0; i < vsc; ++i) {
             const int32_t tk = ordering[(size_t)best * vsc + i];
             if (tk < 0 || tk >= V) { rc = -1; break; }
@@ -448,6 +454,19 @@ int orc_centroid_head(const orc_model *m, const void *centroids, const int32_t *
             z[tk] = acc;
         }
     }
+    if (cgap) {
+        double next = -INFINITY, mean = 0.0, var = 0.0;
+        int cnt = 0;
+        for (int j = 0; j < nc; ++j) {
+            if (!taken[j] && cl[j] > next) next = cl[j];
+            if (!isnan(cl[j])) { mean += cl[j]; ++cnt; }
+        }
+        mean = cnt ? mean / cnt : 0.0;
+        for (int j = 0; j < nc; ++j) if (!isnan(cl[j])) var += (cl[j] - mean) * (cl[j] - mean);
+        const double sd = cnt ? sqrt(var / cnt) : 0.0;
+        *cgap = kc < nc && sd > 0.0 ? (last - next) / sd : INFINITY;
+    }
+    if (cl_out) memcpy(cl_out, cl, sizeof(double) * (size_t)nc);
     free(cl);
     free(taken);
     return rc;
@@ -466,10 +485,11 @@ int orc_centroid_head(const orc_model *m, const void *centroids, const int32_t *
  *   h_prev[b]   hidden state carried from the target (step 0) or from the
  *               previous step's post-projection, [B, d_t]
  *   step        k: RoPE position of the query is kv_len[b] + k
- * Outputs h_next [B, d_t] (the next step's h_prev) and logits [B, V]. */
+ * Outputs h_next [B, d_t] (the next step's h_prev), logits [B, V] and, for a
+ * centroid-routed head, cgap [B] (optional; see orc_centroid_head). */
 int orc_draft_step(const orc_model *m, const void *const *t, const int32_t *block_view,
                    const orc_view *views, int n_views, int B, const int32_t *kv_len, int step,
-                   const int32_t *tok, const double *h_prev, double *h_next, double *logits) {
+                   const int32_t *tok, const double *h_prev, double *h_next, double *logits, double *cgap) {
     const int d_t = m->d_t, d_a = m->d_a, hd = m->head_dim, Hq = m->n_q_heads, Hkv = m->n_kv_heads;
     const int qw = Hq * hd, F = m->d_ff, V = m->vocab, bf = m->wbf16;
     const int grp = Hq / Hkv;
@@ -525,7 +545,8 @@ int orc_draft_step(const orc_model *m, const void *const *t, const int32_t *bloc
         double *z = logits + (size_t)b * V;
         if (m->n_centroids > 0) {
             /* centroid-routed head ([G4] sec. 3) */
-            if (orc_centroid_head(m, TT(T_CENTROIDS), (const int32_t *)TT(T_ORDERING), TT(T_TOK_EMBD), hn, z)) {
+            if (orc_centroid_head(m, TT(T_CENTROIDS), (const int32_t *)TT(T_ORDERING), TT(T_TOK_EMBD), hn, z,
+                                  cgap ? cgap + b : NULL, NULL)) {
                 free(e); free(u); free(x); free(a); free(q); free(o); free(y); free(yn); free(gt); free(up);
                 return -1;
             }
@@ -564,13 +585,14 @@ double orc_top1_prob(const double *z, int64_t n) {
  * Outputs drafts [B, N], h_last [B, d_t] (optional), logits [B, N, V]
  * (optional), margin [B, N] (optional: top1 - top2 logit gap of each greedy
  * step, or the sampling decision's relative margin), conf [B, N] (optional:
- * the step's confidence, see orc_top1_prob). */
+ * the step's confidence, see orc_top1_prob), cgap [B, N] (optional: the
+ * centroid-routed head's set margin, see orc_centroid_head). */
 int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *block_view,
                     const orc_view *views, int n_views, int B, int N, const int32_t *kv_len,
                     const int32_t *last_tok, const float *h_prev, const orc_sample_params *sp,
                     uint64_t seed, uint64_t offset, int seq0, const int32_t *hist, int H,
                     const int32_t *force_tok, int32_t *drafts, double *h_last, double *logits,
-                    double *margin, double *conf) {
+                    double *margin, double *conf, double *cgap) {
     const int d_t = m->d_t, V = m->vocab;
     double *h = malloc(sizeof(double) * (size_t)B * d_t), *hn = malloc(sizeof(double) * (size_t)B * d_t);
     double *z = malloc(sizeof(double) * (size_t)B * V);
@@ -578,12 +600,13 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
     int32_t *ids = malloc(sizeof(int32_t) * (size_t)V);
     float *wf = malloc(sizeof(float) * (size_t)V);
     int32_t *pen = malloc(sizeof(int32_t) * (size_t)(H + N + 1));
+    double *cg = malloc(sizeof(double) * (size_t)B);
     int rc = 0;
     for (size_t i = 0; i < (size_t)B * d_t; ++i) h[i] = (double)h_prev[i];
     for (int b = 0; b < B; ++b) tok[b] = last_tok[b];
     const int sampling = sp && sp->temp > 0.0;
     for (int k = 0; k < N && rc == 0; ++k) {
-        rc = orc_draft_step(m, t, block_view, views, n_views, B, kv_len, k, tok, h, hn, z);
+        rc = orc_draft_step(m, t, block_view, views, n_views, B, kv_len, k, tok, h, hn, z, cg);
         if (rc) break;
         for (int b = 0; b < B; ++b) {
             const double *zb = z + (size_t)b * V;
@@ -607,6 +630,7 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
             }
             if (margin) margin[(size_t)b * N + k] = mg;
             if (conf) conf[(size_t)b * N + k] = orc_top1_prob(zb, V);
+            if (cgap) cgap[(size_t)b * N + k] = m->n_centroids > 0 ? cg[b] : INFINITY;
             if (logits) memcpy(logits + ((size_t)b * N + k) * V, zb, sizeof(double) * (size_t)V);
             drafts[(size_t)b * N + k] = pick;
             tok[b] = force_tok ? force_tok[(size_t)b * N + k] : pick;
@@ -614,7 +638,7 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
         double *sw = h; h = hn; hn = sw;
     }
     if (h_last && rc == 0) memcpy(h_last, h, sizeof(double) * (size_t)B * d_t);
-    free(h); free(hn); free(z); free(tok); free(ids); free(wf); free(pen);
+    free(h); free(hn); free(z); free(tok); free(ids); free(wf); free(pen); free(cg);
     return rc;
 }
 

@@ -302,6 +302,16 @@ def _gemma_assistant(dtype: str = "bf16") -> ModelSpec:
                      d_ff=4096, vocab=262144, dtype=dtype, block_view=(0, 0, 0, 1))
 
 
+def _edge_assistant() -> ModelSpec:
+    """An Edge-shaped assistant with the centroid-routed head (synthetic sizes:
+    the pages give the head's steps, not an Edge model's dimensions): 2048-wide
+    backbone, 512-wide assistant, 4 blocks, 8 query heads x 256 against 2 KV
+    heads, GeGLU 2048, the 262144-token table in 2048 lists of 128 ids, 32
+    lists scored per step."""
+    return ModelSpec(d_t=2048, d_a=512, n_blocks=4, n_q_heads=8, head_dim=256, n_kv_heads=2, d_ff=2048,
+                     vocab=262144, dtype="bf16", block_view=(0, 0, 0, 1), n_centroids=2048, centroid_top_k=32)
+
+
 def _gemma_views(full_cap: int) -> list:
     # view 0: the target's last sliding-window layer (bounded ring of 1536 cells, window 1024)
     # view 1: the target's last full-attention layer
@@ -315,6 +325,7 @@ WORKLOADS = {
     2: "gemma-assistant-bf16-b16-n4-ragged2k-32k",
     3: "gemma-assistant-bf16-b64-n2-ctx4096",
     4: "verify-sample-b32-n3-v248320",
+    5: "edge-centroid-bf16-b1-n3-ctx4096",
 }
 
 
@@ -323,7 +334,10 @@ def workload_seed(cfg_id: int) -> int:
 
 
 def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None, sink: int = 0) -> DraftWorkload:
-    """Draft-block inputs of one of the named workloads (0-3).
+    """Draft-block inputs of one of the named workloads (0-3, 5).
+
+    Workload 5 is the Edge-shaped model with the centroid-routed head, batch
+    1, N = 3, a sliding layer (window 512) and a full layer of 4096 positions.
 
     ``B`` may shrink the batch (the first B sequences' lengths are kept) for
     parity runs at full model size.  ``sink`` > 0 keeps that many attention-
@@ -346,6 +360,10 @@ def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None
     elif cfg_id == 3:
         m, views = _gemma_assistant(), _gemma_views(4096)
         Bf, N, kv = 64, 2, np.full(64, 4096)
+    elif cfg_id == 5:
+        m = _edge_assistant()
+        views = [ViewSpec(cap=768, window=512, rope_theta=10000.0), ViewSpec(cap=4096, window=0, rope_theta=1000000.0)]
+        Bf, N, kv = 1, 3, np.array([4096])
     else:
         raise ValueError("workload 4 has no draft block")
     B = Bf if B is None else B
@@ -408,7 +426,7 @@ def make_verify_greedy_inputs(cfg_id: int, seed: int | None = None, B: int | Non
                               dtype: str | None = None) -> VerifyGreedyInputs:
     seed = workload_seed(cfg_id) if seed is None else seed
     defaults = {0: (1, 3, 4096, "f32"), 1: (1, 3, 262144, "bf16"), 2: (16, 4, 262144, "bf16"),
-                3: (64, 2, 262144, "bf16")}
+                3: (64, 2, 262144, "bf16"), 5: (1, 3, 262144, "bf16")}
     Bd, Nd, Vd, dd = defaults[cfg_id]
     B = Bd if B is None else B
     N = Nd if N is None else N

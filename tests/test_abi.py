@@ -3,6 +3,7 @@ include/mtp.h declares (no GPU needed: nothing is called)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -36,13 +37,32 @@ def test_binding_loads_library():
     assert mtp.strerror(0) == "ok"
 
 
-def test_struct_layouts_match_header_sizes():
-    # sizes the C compiler gives the header's structs (x86-64 and aarch64 agree)
-    assert ctypes.sizeof(mtp.Config) == 13 * 4
-    assert ctypes.sizeof(mtp.BlockWeights) == 10 * 8 + 8
-    assert ctypes.sizeof(mtp.Weights) == 6 * 8 + mtp.MTP_MAX_BLOCKS * (10 * 8 + 8)
-    assert ctypes.sizeof(mtp.KVView) == 2 * 8 + 3 * 8 + 4 * 4
-    assert ctypes.sizeof(mtp.SampleParams) == 6 * 4
+_STRUCTS = (("mtp_config", "Config"), ("mtp_block_weights", "BlockWeights"), ("mtp_weights", "Weights"),
+            ("mtp_kv_view", "KVView"), ("mtp_sample_params", "SampleParams"))
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """Every binding struct has the size and field offsets the C compiler gives
+    the header's struct of the same name."""
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "mtp.h"', "int main(void) {"]
+    for cname, pname in _STRUCTS:
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in getattr(mtp, pname)._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for ln in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        *key, val = ln.split()
+        got[tuple(key)] = int(val)
+    for cname, pname in _STRUCTS:
+        S = getattr(mtp, pname)
+        assert got[(cname, "size")] == ctypes.sizeof(S), cname
+        for f, _ in S._fields_:
+            assert got[(cname, f)] == getattr(S, f).offset, (cname, f)
 
 
 def test_workspace_size_host_only():

@@ -97,7 +97,8 @@ def test_all_centroids_is_the_dense_head(dtype, softcap):
     h = synth.normal(5, "h", (d,)).astype(np.float64)
     E = synth.f32_to_bf16_bits(E32) if dtype == "bf16" else E32
     C = synth.f32_to_bf16_bits(C32) if dtype == "bf16" else C32
-    z = oracle.centroid_head(m, C, order, E, h)
+    z, gap, _ = oracle.centroid_head(m, C, order, E, h, full=True)
+    assert gap == np.inf
     Ew = synth.bf16_bits_to_f32(E).astype(np.float64) if dtype == "bf16" else E32.astype(np.float64)
     dense = Ew @ h
     if softcap:
@@ -114,9 +115,12 @@ def test_candidate_set_is_the_top_centroids_lists():
     C = synth.normal(6, "C", (nc, d))
     order = synth.permutation(6, "order", V)
     h = synth.normal(6, "h", (d,)).astype(np.float64)
-    z = oracle.centroid_head(m, C, order, E, h)
+    z, gap, clo = oracle.centroid_head(m, C, order, E, h, full=True)
     cl = C.astype(np.float64) @ h
+    np.testing.assert_allclose(clo, cl, rtol=1e-12, atol=1e-12)
     top = sorted(range(nc), key=lambda j: (-cl[j], j))[:kc]
+    srt = np.sort(cl)[::-1]
+    assert gap == pytest.approx((srt[kc - 1] - srt[kc]) / np.std(cl), rel=1e-9)
     vsc = V // nc
     cand = set(int(t) for j in top for t in order[j * vsc:(j + 1) * vsc])
     assert set(np.flatnonzero(z > FILL).tolist()) == cand
