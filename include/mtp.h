@@ -82,8 +82,9 @@ enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 };
  *   d_ff       GeGLU hidden width
  *   vocab      rows of the tied token-embedding table
  *   wdtype     MTP_DTYPE_BF16 or MTP_DTYPE_F32: weight matrices and KV
- *   rms_eps    RMSNorm epsilon; attn_scale softmax scale (usually 1/sqrt(head_dim));
- *   emb_scale  token-embedding scale (sqrt(d_t) for Gemma);
+ *   rms_eps    RMSNorm epsilon; attn_scale softmax scale, 0 = the default
+ *              1/sqrt(head_dim) (rounded to fp32);
+ *   emb_scale  token-embedding scale, 0 = the default sqrt(d_t) (Gemma's);
  *   logit_softcap  > 0 applies cap * tanh(z / cap) to the logits, 0 = off
  *   n_centroids    0: the dense tied LM head.  > 0: the centroid-routed head
  *                  of ordered-embedding models ([G4] sec. 3 "Centroid /

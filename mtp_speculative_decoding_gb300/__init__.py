@@ -156,11 +156,11 @@ def _dtype_code(t) -> int:
 def make_config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab, wdtype="bf16",
                 rms_eps=1e-6, attn_scale=None, emb_scale=None, logit_softcap=0.0, n_centroids=0,
                 centroid_top_k=0) -> Config:
-    import math
+    # None -> 0: the library's documented defaults (1/sqrt(head_dim), sqrt(d_t))
     return Config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab,
                   MTP_DTYPE_BF16 if wdtype == "bf16" else MTP_DTYPE_F32, rms_eps,
-                  1.0 / math.sqrt(head_dim) if attn_scale is None else attn_scale,
-                  math.sqrt(d_t) if emb_scale is None else emb_scale, logit_softcap, n_centroids, centroid_top_k)
+                  0.0 if attn_scale is None else attn_scale, 0.0 if emb_scale is None else emb_scale,
+                  logit_softcap, n_centroids, centroid_top_k)
 
 
 def workspace_size(cfg: Config | None, B: int, N: int, V: int) -> int:

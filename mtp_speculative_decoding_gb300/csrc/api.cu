@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <math.h>
 #include <string.h>
 
 #include <mutex>
@@ -245,7 +246,8 @@ int check_config(const mtp_config* c) {
     if (hd != 32 && hd != 64 && hd != 128 && hd != 256 && hd != 512) return MTP_ERR_UNSUPPORTED;
     const int m = 8;  // row lengths in elements: 16-byte rows for either dtype
     if (c->d_t % m || c->d_a % m || c->d_ff % m || (c->n_q_heads * hd) % m) return MTP_ERR_UNSUPPORTED;
-    if (!(c->rms_eps >= 0.f) || !(c->attn_scale > 0.f) || !(c->logit_softcap >= 0.f)) return MTP_ERR_ARG;
+    if (!(c->rms_eps >= 0.f) || !(c->attn_scale >= 0.f) || !(c->emb_scale >= 0.f) || !(c->logit_softcap >= 0.f))
+        return MTP_ERR_ARG;
     if (c->n_centroids < 0 || c->centroid_top_k < 0) return MTP_ERR_ARG;
     if (c->n_centroids > 0) {
         if (c->n_centroids > MTP_MAX_CENTROIDS) return MTP_ERR_UNSUPPORTED;
@@ -431,7 +433,10 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     memset(&p, 0, sizeof p);
     p.d_t = cfg->d_t; p.d_a = cfg->d_a; p.L = cfg->n_blocks; p.Hq = cfg->n_q_heads; p.hd = cfg->head_dim;
     p.Hkv = cfg->n_kv_heads; p.F = cfg->d_ff; p.V = cfg->vocab; p.B = B; p.N = N;
-    p.eps = cfg->rms_eps; p.attn_scale = cfg->attn_scale; p.emb_scale = cfg->emb_scale; p.softcap = cfg->logit_softcap;
+    p.eps = cfg->rms_eps; p.softcap = cfg->logit_softcap;
+    // 0 selects the defaults the header documents: 1/sqrt(head_dim), sqrt(d_t)
+    p.attn_scale = cfg->attn_scale > 0.f ? cfg->attn_scale : (float)(1.0 / sqrt((double)cfg->head_dim));
+    p.emb_scale = cfg->emb_scale > 0.f ? cfg->emb_scale : (float)sqrt((double)cfg->d_t);
     p.tok_embd = w->tok_embd;
     p.norm_e = static_cast<const float*>(w->norm_e);
     p.norm_h = static_cast<const float*>(w->norm_h);

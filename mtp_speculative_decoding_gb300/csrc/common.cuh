@@ -43,7 +43,7 @@ __device__ __forceinline__ unsigned long long l2_evict_first() {
 }
 // ld_stream16 for weight streams read once per step, under an L2 policy
 // from l2_evict_first(): the lines go first when L2 evicts, so the small
-// vectors, gains and attention keys and values that phases re-read keep
+// vectors, gains and split partials that phases re-read keep
 // their places
 __device__ __forceinline__ uint4 ld_weight16(const void* p, unsigned long long pol) {
     uint4 r;

@@ -866,8 +866,13 @@ struct AttnPiece {
 // CTA c's piece starting at position x; `next` = position after it
 __device__ __forceinline__ AttnPiece attn_piece(const DraftParams& p, const KView& vw, const int* kv,
                                                 const AttnTab& t, int v, int c, long long x, long long& next) {
+    // the sequence holding x: the last b with pre[b] <= x (binary search)
     int b = 0;
-    while (b + 1 < p.B && t.pre[v][b + 1] <= x) ++b;
+    for (int hi = p.B - 1; b < hi;) {
+        const int mid = (b + hi + 1) >> 1;
+        if (t.pre[v][mid] <= x) b = mid;
+        else hi = mid - 1;
+    }
     const int n = view_keys(vw, kv[b]);
     const int g = (int)((x - t.pre[v][b]) / n);
     const long long s0 = t.pre[v][b] + (long long)g * n, s1 = s0 + n;
@@ -1012,6 +1017,9 @@ __device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsi
         return attn_piece(p, vw, kv, tab, view, cta, x, nx);
     };
     const bool packed = vw.st == HD;   // consecutive ring slots are contiguous rows
+    // keys and values stream evict-first, like the weights: the lines that phases
+    // re-read (activations, partials, gains, prefetched weight boxes) keep their places
+    const unsigned long long kvpol = l2_evict_first();
     bool any_split = false, aok = true;   // aok: warp-uniform, false once a stage wait of the warp gave up
     // earlier generic shared-memory accesses before the stage copies
     fence_proxy_async_smem();
@@ -1048,8 +1056,9 @@ __device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsi
                 for (int r = 0; r < cnt;) {
                     const int slot = key_slot(km, t0 + r);
                     const int run = key_run(km, t0 + r, slot, packed ? cnt - r : 1);
-                    bulk_g2s(buf + r * RB, kbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar);
-                    bulk_g2s(buf + R * RB + r * RB, vbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar);
+                    bulk_g2s_pol(buf + r * RB, kbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar, kvpol);
+                    bulk_g2s_pol(buf + R * RB + r * RB, vbase + (long long)slot * vw.st, (unsigned int)(run * RB), bar,
+                                 kvpol);
                     r += run;
                 }
             }

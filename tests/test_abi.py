@@ -73,6 +73,10 @@ def test_workspace_size_host_only():
     assert mtp.workspace_size(None, 32, 3, 248320) > 0
     with pytest.raises(mtp.MTPError):
         mtp.workspace_size(cfg, 65, 3, 262144)
+    assert mtp.workspace_size(mtp.make_config(5120, 1024, 4, 16, 256, 4, 4096, 262144, attn_scale=0.0,
+                                              emb_scale=0.0), 1, 3, 262144) == n   # 0: the defaults
+    with pytest.raises(mtp.MTPError):
+        mtp.workspace_size(mtp.make_config(5120, 1024, 4, 16, 256, 4, 4096, 262144, attn_scale=-1.0), 1, 3, 262144)
     bad = mtp.make_config(5120, 1024, 4, 16, 96, 4, 4096, 262144)   # head_dim 96 unsupported
     with pytest.raises(mtp.MTPError):
         mtp.workspace_size(bad, 1, 3, 262144)

@@ -119,6 +119,19 @@ def test_deterministic_and_workspace_reuse():
     assert np.array_equal(d1, d2) and np.array_equal(h1, h2) and np.array_equal(z1, z2)
 
 
+def test_default_scales_are_the_documented_ones():
+    """attn_scale = emb_scale = 0 selects 1/sqrt(head_dim) and sqrt(d_t): the
+    same outputs, bit for bit, as the explicit values."""
+    import ctypes
+    w = small_workload("f32", softcap=3.0)
+    dev, d1, h1, z1 = run_gpu_draft(w)
+    dev.cfg.attn_scale = 0.0
+    dev.cfg.emb_scale = 0.0
+    _, d2, h2, z2 = run_gpu_draft(w, dev=dev)
+    assert np.array_equal(d1, d2) and np.array_equal(h1, h2) and np.array_equal(z1, z2)
+    assert ctypes.c_float(w.model.attn_scale).value == ctypes.c_float(1.0 / np.sqrt(w.model.head_dim)).value
+
+
 @pytest.mark.slow
 def test_workload1_gemma_b1():
     w = synth.make_draft_inputs(1)
