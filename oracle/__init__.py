@@ -88,6 +88,8 @@ def _declare(L):
     L.orc_draft_block.argtypes = [P, P, P, P, I, I, I, P, P, P, P, U64, U64, I, P, I, P, P, P, P, P, P, P]
     L.orc_centroid_head.argtypes = [P, P, P, P, P, P, P, P]
     L.orc_centroid_head.restype = I
+    L.orc_quantize_q8_0.argtypes = [P, C.c_int64, C.c_int64, P, P]
+    L.orc_dequantize_q8_0.argtypes = [P, P, C.c_int64, C.c_int64, P]
     L.orc_top1_prob.argtypes = [P, C.c_int64]
     L.orc_top1_prob.restype = D
     L.orc_draft_block.restype = I
@@ -191,6 +193,28 @@ def sample_dist(z, pen, sp):
     return ids[:n].copy(), w[:n].copy(), ws.value, mg.value
 
 
+def quantize_q8_0(w):
+    """Q8_0 codes (int8 [rows, cols]) and block scales (binary16 bits [rows, cols / 32]) of an fp32 matrix."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    if cols % 32:
+        raise ValueError("Q8_0 needs a multiple of 32 columns")
+    q = np.empty((rows, cols), dtype=np.int8)
+    d = np.empty((rows, cols // 32), dtype=np.uint16)
+    lib().orc_quantize_q8_0(_p(w), rows, cols, _p(q), _p(d))
+    return q, d
+
+
+def dequantize_q8_0(q, d):
+    """The fp32 weights Q8_0 codes and scales stand for."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    d = np.ascontiguousarray(d, dtype=np.uint16)
+    rows, cols = q.shape
+    w = np.empty((rows, cols), dtype=np.float32)
+    lib().orc_dequantize_q8_0(_p(q), _p(d), rows, cols, _p(w))
+    return w
+
+
 def top1_prob(z):
     """The softmax probability of the largest logit (NaN entries left out)."""
     z = np.ascontiguousarray(z, dtype=np.float64)
@@ -240,6 +264,18 @@ def centroid_head(m, centroids, ordering, tok_embd, h, full=False):
     return (z, gap.value, cl) if full else z
 
 
+def _projection_names(m):
+    return ("w_pre", "w_post") + tuple(f"blk{i}.{n}" for i in range(m.n_blocks)
+                                       for n in ("w_q", "w_o", "w_gate", "w_up", "w_down"))
+
+
+def _widen(a):
+    """bf16 bit patterns (uint16) to fp32, exactly; other arrays unchanged."""
+    if a.dtype == np.uint16:
+        return np.ascontiguousarray((a.astype(np.uint32) << 16).view(np.float32))
+    return a
+
+
 class _Bound:
     """ctypes views of one workload, restricted to one sequence b (or all)."""
 
@@ -250,13 +286,22 @@ class _Bound:
         names = list(GLOBAL_ORDER) + [f"blk{i}.{n}" for i in range(m.n_blocks) for n in BLOCK_ORDER]
         # the centroid head's tensors exist only for centroid-head models (NULL otherwise)
         arrs = [np.ascontiguousarray(w.weights[n]) if n in w.weights else None for n in names]
+        q8 = getattr(m, "wquant", "none") == "q8_0"
+        if q8:
+            # Q8_0 projections: the weights the codes stand for (exact in fp32); the
+            # table and the KV widened from bf16 exactly, and the step run in fp32
+            proj = set(_projection_names(m))
+            arrs = [None if a is None else
+                    dequantize_q8_0(*quantize_q8_0(a)) if n in proj else
+                    _widen(a) for n, a in zip(names, arrs)]
+            self.model.wbf16 = 0
         self.keep += [a for a in arrs if a is not None]
         self.tensors = (C.c_void_p * len(arrs))(*[None if a is None else a.ctypes.data for a in arrs])
         self.block_view = np.ascontiguousarray(np.asarray(m.block_view, dtype=np.int32))
         views = []
-        esz = 2 if m.dtype == "bf16" else 4
+        esz = 2 if m.dtype == "bf16" and not q8 else 4
         for vd in w.views:
-            k, v = vd["k"], vd["v"]
+            k, v = (_widen(vd["k"]), _widen(vd["v"])) if q8 else (vd["k"], vd["v"])
             Bv, H, cap, hd = k.shape
             off = 0 if b is None else b * H * cap * hd * esz
             views.append(View(k.ctypes.data + off, v.ctypes.data + off, H * cap * hd, cap * hd, hd,

@@ -32,6 +32,8 @@
  *  [FN]  "Fused NextN draft graph", delta 6 (the fused steps cross-attend the
  *        frozen prefix read-only; the recurrence is carried by the hidden
  *        state chain alone).
+ *        Item 3 "Q4_0 / Q5_0 draft weights": the Q8_0 weight format of its
+ *        quantisation-error table (ggml's rule, see orc_quantize_q8_0).
  *  [PH]  Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
  *        1, 2, 3" (SC'11): the Philox-4x32-10 counter-based generator.
  *
@@ -400,6 +402,69 @@ int32_t orc_pick(const int32_t *ids, const double *w, int n, double wsum, double
     int32_t r = orc_pick_f32(ids, wf, n, (float)wsum, (float)u, margin);
     free(wf);
     return r;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q8_0 drafter weights ([SP] item 3)                                        */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE binary16 from a float, round to nearest even (subnormals kept,
+ * overflow to infinity), and back. */
+static uint16_t f32_to_f16(float xf) {
+    double x = xf;
+    uint16_t sign = 0;
+    if (signbit(x)) { sign = 0x8000; x = -x; }
+    if (isnan(x)) return 0x7e00;
+    if (x >= 65520.0) return sign | 0x7c00;                 /* rounds past the largest finite */
+    if (x < ldexp(1.0, -14)) {                              /* subnormal: steps of 2^-24 */
+        const double r = nearbyint(x / ldexp(1.0, -24));    /* 1024 is the smallest normal */
+        return sign | (uint16_t)r;
+    }
+    int e;
+    frexp(x, &e);
+    e -= 1;                                                 /* x in [2^e, 2^(e+1)) */
+    double m = nearbyint(x / ldexp(1.0, e - 10));           /* 11 significant bits */
+    if (m == 2048.0) { m = 1024.0; e += 1; }
+    if (e > 15) return sign | 0x7c00;
+    return sign | (uint16_t)((e + 15) << 10) | (uint16_t)((int)m - 1024);
+}
+static double f16_to_double(uint16_t h) {
+    const int e = (h >> 10) & 31, m = h & 1023;
+    const double v = e == 0 ? ldexp((double)m, -24) : e == 31 ? (m ? NAN : INFINITY) : ldexp(1024.0 + m, e - 25);
+    return (h & 0x8000) ? -v : v;
+}
+
+/* Q8_0 quantisation of a row-major [rows, cols] fp32 matrix, cols a multiple
+ * of 32 (the Q8_0 format the report's error table measures, ggml's rule):
+ * per block of 32 consecutive weights of a row, d = max |w| / 127 in fp32,
+ * stored as binary16; codes q = round(w * (1 / d)) in fp32, halves away from
+ * zero, all 0 when d = 0.  Codes go to q[rows, cols] (int8), block scales to
+ * d16[rows, cols / 32] (binary16 bits).  The weight a code stands for is
+ * f16(d) * q (f16_to_double). */
+void orc_quantize_q8_0(const float *w, int64_t rows, int64_t cols, int8_t *q, uint16_t *d16) {
+    const int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < nb; ++j) {
+            const float *x = w + r * cols + j * 32;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) amax = fabsf(x[i]) > amax ? fabsf(x[i]) : amax;
+            const float d = amax / 127.0f;
+            const float id = d != 0.0f ? 1.0f / d : 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                const float v = x[i] * id;
+                q[r * cols + j * 32 + i] = (int8_t)roundf(v);
+            }
+            d16[r * nb + j] = f32_to_f16(d);
+        }
+}
+
+/* The weights the codes stand for, fp32 (exact: an 11-bit scale times an
+ * 8-bit code). */
+void orc_dequantize_q8_0(const int8_t *q, const uint16_t *d16, int64_t rows, int64_t cols, float *w) {
+    const int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            w[r * cols + c] = (float)(f16_to_double(d16[r * nb + c / 32]) * (double)q[r * cols + c]);
 }
 
 /* ------------------------------------------------------------------------ */

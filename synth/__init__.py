@@ -152,6 +152,7 @@ class ModelSpec:
     logit_softcap: float = 0.0
     n_centroids: int = 0         # > 0: centroid-routed LM head over n_centroids lists of vocab / n_centroids ids
     centroid_top_k: int = 0      # centroids whose lists are scored per step
+    wquant: str = "none"         # "q8_0": the projections are quantised (generated here in fp32, unrounded)
 
     @property
     def emb_scale(self) -> float:
@@ -193,6 +194,12 @@ class DraftWorkload:
         return sum(int(a.nbytes) for a in self.weights.values())
 
 
+def projection_names(m: ModelSpec) -> tuple:
+    """The drafter's projection matrices (the ones a quantised model quantises)."""
+    return ("w_pre", "w_post") + tuple(f"blk{i}.{n}" for i in range(m.n_blocks)
+                                       for n in ("w_q", "w_o", "w_gate", "w_up", "w_down"))
+
+
 def make_model_weights(m: ModelSpec, seed: int, std: float = 0.02) -> dict:
     q = m.n_q_heads * m.head_dim
     shapes = {
@@ -216,7 +223,8 @@ def make_model_weights(m: ModelSpec, seed: int, std: float = 0.02) -> dict:
         shapes["centroids"] = (m.n_centroids, m.d_t)
     w = {}
     for name, shp in shapes.items():
-        w[name] = _as_dtype(normal(seed, name, shp, std=std), m.dtype)
+        vals = normal(seed, name, shp, std=std)
+        w[name] = vals if m.wquant != "none" and name in projection_names(m) else _as_dtype(vals, m.dtype)
     for name, n in norms.items():
         w[name] = normal(seed, name, (n,), std=std, mean=1.0)
     if m.n_centroids:
