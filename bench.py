@@ -11,7 +11,8 @@ d_t 5120, d_a 1024, 4 blocks, 16 x 256 query heads over 4 KV heads, GeGLU
 same model at B = 16 (N = 4, ragged 2k-32k contexts) and B = 64 (N = 2,
 context 4096), exact temp > 0 verification alone (mtp_verify_sample,
 B = 32, N = 3, V = 248320; that configuration has no draft block), and an
-Edge-shaped drafter with the centroid-routed LM head (B = 1, N = 3), each
+Edge-shaped drafter with the centroid-routed LM head (B = 1, N = 3), and the
+headline workload with Q8_0 projections, each
 reported under per_workload with its own roofline fraction, end-to-end
 number and CPU baseline.  `--workload K` times one of them alone.
 
@@ -41,7 +42,7 @@ import synth  # noqa: E402
 METRIC = "drafted tok/s (MTP draft block + verify) at B=1..64; % of HBM/tensor roofline"
 UNIT = "tok/s"
 HEADLINE = 1
-OTHERS = (2, 3, 4, 5)
+OTHERS = (2, 3, 4, 5, 6)
 
 
 def parse(argv=None):
@@ -50,8 +51,8 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4, 5],
-                    help="time this workload alone (default: the headline plus workloads 2-5)")
+    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4, 5, 6],
+                    help="time this workload alone (default: the headline plus workloads 2-6)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
 
@@ -94,7 +95,8 @@ def draft_config(w, world: int = 1) -> dict:
             if m.n_centroids else "dense tied")
     return dict({"workload": w.name, "B": w.B, "N": w.N, "vocab": m.vocab, "d_t": m.d_t, "d_a": m.d_a,
                  "n_blocks": m.n_blocks, "kv_len_max": int(w.kv_len.max()), "kv_len_min": int(w.kv_len.min()),
-                 "lm_head": head}, **_common(world, False))
+                 "lm_head": head, "projections": "Q8_0 (bf16 table and KV)" if m.wquant == "q8_0" else m.dtype},
+                **_common(world, False))
 
 
 def sample_config(inp, world: int = 1) -> dict:
@@ -141,9 +143,13 @@ def draft_bytes_per_launch(w) -> int:
     esz = 2 if m.dtype == "bf16" else 4
     head_w = m.vocab * m.d_t * esz + sum(int(w.weights[n].nbytes) for n in ("centroids", "token_ordering")
                                          if n in w.weights)
-    per_step = (w.weight_bytes() - head_w + head_bytes_per_step(w) + kv_bytes_per_step(w) +
-                w.B * m.d_t * esz)
-    return w.N * per_step
+    wb = w.weight_bytes()
+    if m.wquant == "q8_0":   # the projections as Q8_0: a byte per weight plus a 2-byte scale per 32
+        for n in synth.projection_names(m):
+            a = w.weights[n]
+            wb += a.size * (1 + 2 / 32) - a.nbytes
+    per_step = (wb - head_w + head_bytes_per_step(w) + kv_bytes_per_step(w) + w.B * m.d_t * esz)
+    return int(w.N * per_step)
 
 
 def draft_flops_per_launch(w) -> float:

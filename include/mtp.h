@@ -66,6 +66,8 @@ enum {
 };
 
 enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 };
+/* projection weight formats (mtp_config.wquant) */
+enum { MTP_WQ_NONE = 0, MTP_WQ_Q8_0 = 1 };
 
 #define MTP_MAX_BLOCKS 8
 #define MTP_MAX_VIEWS 4
@@ -92,12 +94,21 @@ enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 };
  *                  MTP_MAX_CENTROIDS dividing vocab (MTP_ERR_ARG otherwise;
  *                  above the maximum MTP_ERR_UNSUPPORTED)
  *   centroid_top_k centroids whose candidate lists are scored per step,
- *                  1..n_centroids (ignored for the dense head, must be >= 0) */
+ *                  1..n_centroids (ignored for the dense head, must be >= 0)
+ *   wquant         MTP_WQ_NONE: the projections (w_pre, w_post and every
+ *                  block's w_q, w_o, w_gate, w_up, w_down) are in wdtype.
+ *                  MTP_WQ_Q8_0 ("opus-mtp-turbo: Track 1 report", item 3):
+ *                  they are Q8_0 codes, int8 [out, in], each with its
+ *                  block scales, binary16 [out, in / 32] (see
+ *                  mtp_quantize_q8_0); requires wdtype MTP_DTYPE_BF16 (the
+ *                  table and KV), head_dim 64, 128 or 256, every input
+ *                  width a multiple of 32; runs on the CUDA-core paths */
 typedef struct mtp_config {
     int32_t d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab;
     int32_t wdtype;
     float rms_eps, attn_scale, emb_scale, logit_softcap;
     int32_t n_centroids, centroid_top_k;
+    int32_t wquant, pad_;
 } mtp_config;
 
 /* One assistant block.  Matrices are row-major [out, in] in `wdtype`; RMSNorm
@@ -115,6 +126,8 @@ typedef struct mtp_block_weights {
     const void *post_ffn_norm;   /* fp32 [d_a] */
     int32_t kv_view;
     int32_t pad_;
+    /* MTP_WQ_Q8_0 only (NULL otherwise): block scales of w_q, w_o, w_gate, w_up, w_down */
+    const uint16_t *w_q_scale, *w_o_scale, *w_gate_scale, *w_up_scale, *w_down_scale;
 } mtp_block_weights;
 
 typedef struct mtp_weights {
@@ -130,6 +143,8 @@ typedef struct mtp_weights {
     const int32_t *token_ordering;   /* [vocab]: n_centroids consecutive lists of
                                       * vocab / n_centroids token ids, list j the
                                       * candidates of centroid j */
+    /* MTP_WQ_Q8_0 only (NULL otherwise): block scales of w_pre and w_post */
+    const uint16_t *w_pre_scale, *w_post_scale;
 } mtp_weights;
 
 /* A read-only view of one target KV layer ([G4] sec. 5).  K and V share the
@@ -161,6 +176,16 @@ typedef struct mtp_sample_params {
     float temp, top_p, min_p, rep_penalty, presence_penalty;
     int32_t top_k;
 } mtp_sample_params;
+
+/* Q8_0 quantisation of a row-major fp32 matrix [rows, cols] on the host
+ * ("opus-mtp-turbo: Track 1 report", item 3, ggml's Q8_0 rule): per block of
+ * 32 consecutive weights of a row, d = max |w| / 127 (fp32), stored as
+ * binary16 (round to nearest even); codes q = round(w * (1 / d)) in fp32,
+ * halves away from zero, 0 when d = 0.  The weight a code stands for is
+ * binary16(d) * q.  Host pointers: w [rows, cols], codes [rows, cols] int8,
+ * scales [rows, cols / 32].  cols must be a multiple of 32 (MTP_ERR_ARG).
+ * Synchronous, no device work. */
+int mtp_quantize_q8_0(const float *w, int64_t rows, int64_t cols, int8_t *codes, uint16_t *scales);
 
 /* Workspace bytes needed by any of the operations for these sizes (B
  * sequences, N drafts, vocabulary V).  cfg may be NULL when only the verify

@@ -24,6 +24,8 @@ MTP_ERR_TIMEOUT = -5
 MTP_ERR_CAPACITY = -6
 MTP_DTYPE_F32 = 0
 MTP_DTYPE_BF16 = 1
+MTP_WQ_NONE = 0
+MTP_WQ_Q8_0 = 1
 MTP_MAX_BLOCKS = 8
 MTP_MAX_VIEWS = 4
 MTP_MAX_BATCH = 64
@@ -31,7 +33,7 @@ MTP_MAX_VERIFY_BATCH = 65536
 
 # every entry point include/mtp.h declares
 EXPORTS = ("mtp_workspace_size", "mtp_draft_block", "mtp_verify_greedy", "mtp_verify_sample",
-           "mtp_sample_drafts", "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout",
+           "mtp_sample_drafts", "mtp_quantize_q8_0", "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout",
            "mtp_verify_greedy_noalloc")
 
 
@@ -46,20 +48,22 @@ class Config(C.Structure):
                 ("head_dim", C.c_int32), ("n_kv_heads", C.c_int32), ("d_ff", C.c_int32), ("vocab", C.c_int32),
                 ("wdtype", C.c_int32), ("rms_eps", C.c_float), ("attn_scale", C.c_float),
                 ("emb_scale", C.c_float), ("logit_softcap", C.c_float), ("n_centroids", C.c_int32),
-                ("centroid_top_k", C.c_int32)]
+                ("centroid_top_k", C.c_int32), ("wquant", C.c_int32), ("pad_", C.c_int32)]
 
 
 class BlockWeights(C.Structure):
     _fields_ = [("attn_norm", C.c_void_p), ("w_q", C.c_void_p), ("q_norm", C.c_void_p), ("w_o", C.c_void_p),
                 ("post_attn_norm", C.c_void_p), ("pre_ffn_norm", C.c_void_p), ("w_gate", C.c_void_p),
                 ("w_up", C.c_void_p), ("w_down", C.c_void_p), ("post_ffn_norm", C.c_void_p),
-                ("kv_view", C.c_int32), ("pad_", C.c_int32)]
+                ("kv_view", C.c_int32), ("pad_", C.c_int32), ("w_q_scale", C.c_void_p), ("w_o_scale", C.c_void_p),
+                ("w_gate_scale", C.c_void_p), ("w_up_scale", C.c_void_p), ("w_down_scale", C.c_void_p)]
 
 
 class Weights(C.Structure):
     _fields_ = [("tok_embd", C.c_void_p), ("norm_e", C.c_void_p), ("norm_h", C.c_void_p), ("w_pre", C.c_void_p),
                 ("final_norm", C.c_void_p), ("w_post", C.c_void_p), ("blk", BlockWeights * MTP_MAX_BLOCKS),
-                ("centroids", C.c_void_p), ("token_ordering", C.c_void_p)]
+                ("centroids", C.c_void_p), ("token_ordering", C.c_void_p), ("w_pre_scale", C.c_void_p),
+                ("w_post_scale", C.c_void_p)]
 
 
 class KVView(C.Structure):
@@ -106,6 +110,8 @@ def lib():
             L.mtp_sample_drafts.restype = I
             L.mtp_verify_greedy_noalloc.argtypes = [P, I, I, I, I, P, P, P, P]
             L.mtp_verify_greedy_noalloc.restype = I
+            L.mtp_quantize_q8_0.argtypes = [P, C.c_int64, C.c_int64, P, P]
+            L.mtp_quantize_q8_0.restype = I
             _lib = L
     return _lib
 
@@ -155,12 +161,27 @@ def _dtype_code(t) -> int:
 
 def make_config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab, wdtype="bf16",
                 rms_eps=1e-6, attn_scale=None, emb_scale=None, logit_softcap=0.0, n_centroids=0,
-                centroid_top_k=0) -> Config:
+                centroid_top_k=0, wquant="none") -> Config:
     # None -> 0: the library's documented defaults (1/sqrt(head_dim), sqrt(d_t))
     return Config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab,
                   MTP_DTYPE_BF16 if wdtype == "bf16" else MTP_DTYPE_F32, rms_eps,
                   0.0 if attn_scale is None else attn_scale, 0.0 if emb_scale is None else emb_scale,
-                  logit_softcap, n_centroids, centroid_top_k)
+                  logit_softcap, n_centroids, centroid_top_k, MTP_WQ_Q8_0 if wquant == "q8_0" else MTP_WQ_NONE, 0)
+
+
+def quantize_q8_0(w):
+    """Q8_0 codes (int8 [rows, cols]) and block scales (binary16 bits, uint16
+    [rows, cols / 32]) of an fp32 matrix, by mtp_quantize_q8_0 (host)."""
+    import numpy as np
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    q = np.empty((rows, cols), dtype=np.int8)
+    d = np.empty((rows, cols // 32 if cols % 32 == 0 else 0), dtype=np.uint16)
+    rc = lib().mtp_quantize_q8_0(w.ctypes.data_as(C.c_void_p), rows, cols, q.ctypes.data_as(C.c_void_p),
+                                 d.ctypes.data_as(C.c_void_p))
+    if rc != MTP_OK:
+        raise MTPError(rc, "mtp_quantize_q8_0")
+    return q, d
 
 
 def workspace_size(cfg: Config | None, B: int, N: int, V: int) -> int:
@@ -194,10 +215,15 @@ def make_weights(tensors: dict, n_blocks: int, block_view) -> Weights:
     for n in ("centroids", "token_ordering"):
         if n in tensors:
             setattr(w, n, tensors[n].data_ptr())
+    for n in ("w_pre", "w_post"):   # Q8_0 block scales, when the model has them
+        if n + ".scale" in tensors:
+            setattr(w, n + "_scale", tensors[n + ".scale"].data_ptr())
     for i in range(n_blocks):
         b = w.blk[i]
         for n in BLOCK_TENSORS:
             setattr(b, n, tensors[f"blk{i}.{n}"].data_ptr())
+            if f"blk{i}.{n}.scale" in tensors:
+                setattr(b, n + "_scale", tensors[f"blk{i}.{n}.scale"].data_ptr())
         b.kv_view = int(block_view[i])
     return w
 

@@ -3,6 +3,7 @@
 // mtp_last_error), no state kept between calls beyond a per-device cache of
 // the SM count.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -40,7 +41,7 @@ int num_sms() {
 // LM head on tensor cores: the dense head, bf16 weights and a batch of at
 // least kTcMinBatch
 bool tc_head_eligible(const mtp_config* c, int B) {
-    return c->wdtype == MTP_DTYPE_BF16 && B >= kTcMinBatch && c->n_centroids == 0;
+    return c->wdtype == MTP_DTYPE_BF16 && B >= kTcMinBatch && c->n_centroids == 0 && c->wquant == MTP_WQ_NONE;
 }
 
 // centroid-routed head: shared memory of its per-CTA sort (keys over n_c
@@ -249,6 +250,11 @@ int check_config(const mtp_config* c) {
     if (!(c->rms_eps >= 0.f) || !(c->attn_scale >= 0.f) || !(c->emb_scale >= 0.f) || !(c->logit_softcap >= 0.f))
         return MTP_ERR_ARG;
     if (c->n_centroids < 0 || c->centroid_top_k < 0) return MTP_ERR_ARG;
+    if (c->wquant != MTP_WQ_NONE && c->wquant != MTP_WQ_Q8_0) return MTP_ERR_UNSUPPORTED;
+    if (c->wquant == MTP_WQ_Q8_0) {
+        if (c->wdtype != MTP_DTYPE_BF16 || (hd != 64 && hd != 128 && hd != 256)) return MTP_ERR_UNSUPPORTED;
+        if (c->d_t % 32 || c->d_a % 32 || c->d_ff % 32 || (c->n_q_heads * hd) % 32) return MTP_ERR_UNSUPPORTED;
+    }
     if (c->n_centroids > 0) {
         if (c->n_centroids > MTP_MAX_CENTROIDS) return MTP_ERR_UNSUPPORTED;
         if (c->centroid_top_k < 1 || c->centroid_top_k > c->n_centroids || c->vocab % c->n_centroids) return MTP_ERR_ARG;
@@ -323,6 +329,27 @@ int check_logits(const void* a, const void* b, int ldtype) {
 
 extern "C" {
 
+int mtp_quantize_q8_0(const float* w, int64_t rows, int64_t cols, int8_t* codes, uint16_t* scales) {
+    if (!w || !codes || !scales || rows < 0 || cols < 0 || cols % 32) return MTP_ERR_ARG;
+    const int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < nb; ++j) {
+            const float* x = w + r * cols + j * 32;
+            float amax = 0.f;
+            for (int i = 0; i < 32; ++i) {
+                const float a = fabsf(x[i]);
+                if (a > amax) amax = a;
+            }
+            const float d = amax / 127.f;
+            const float inv = d != 0.f ? 1.f / d : 0.f;
+            int8_t* q = codes + r * cols + j * 32;
+            for (int i = 0; i < 32; ++i) q[i] = (int8_t)roundf(x[i] * inv);
+            scales[r * nb + j] = __half_as_ushort(__float2half_rn(d));
+        }
+    }
+    return MTP_OK;
+}
+
 size_t mtp_workspace_size(const mtp_config* cfg, int B, int N, int V) {
     if (B <= 0 || B > MTP_MAX_VERIFY_BATCH || N < 0 || N > 16 || V <= 0) return 0;
     if (cfg && B > MTP_MAX_BATCH) return 0;
@@ -359,6 +386,15 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     // weights
     const void* mats[] = {w->tok_embd, w->w_pre, w->w_post};
     for (const void* m : mats) if (!m || !aligned16(m)) return MTP_ERR_ARG;
+    if (cfg->wquant == MTP_WQ_Q8_0) {
+        const uint16_t* sc[] = {w->w_pre_scale, w->w_post_scale};
+        for (const uint16_t* x : sc) if (!x || (reinterpret_cast<uintptr_t>(x) & 1)) return MTP_ERR_ARG;
+        for (int l = 0; l < cfg->n_blocks; ++l) {
+            const mtp_block_weights& b = w->blk[l];
+            const uint16_t* bs[] = {b.w_q_scale, b.w_o_scale, b.w_gate_scale, b.w_up_scale, b.w_down_scale};
+            for (const uint16_t* x : bs) if (!x || (reinterpret_cast<uintptr_t>(x) & 1)) return MTP_ERR_ARG;
+        }
+    }
     const bool cent = cfg->n_centroids > 0;
     if (cent && (!w->centroids || !aligned16(w->centroids) || !w->token_ordering ||
                  (reinterpret_cast<uintptr_t>(w->token_ordering) & 3)))
@@ -423,8 +459,10 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         tc_cols = kTcHeadCols;   // the head's two accumulators; the projections use the first 2 Bp columns
     }
     if (cent && cent_smem(cfg) > smem) smem = cent_smem(cfg);   // at most 100 KB (n_c <= MTP_MAX_CENTROIDS)
+    const bool q8 = cfg->wquant == MTP_WQ_Q8_0;
     const int per_sm = !bf ? draft_blocks_per_sm_f32(cfg->head_dim, smem)
                        : tc ? draft_blocks_per_sm_bf16_tc(cfg->head_dim, smem)
+                       : q8 ? draft_blocks_per_sm_q8(cfg->head_dim, smem)
                             : draft_blocks_per_sm_bf16_cc(cfg->head_dim, smem);
     if (per_sm < 1) return MTP_ERR_UNSUPPORTED;
 
@@ -443,10 +481,18 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     p.w_pre = w->w_pre;
     p.final_norm = static_cast<const float*>(w->final_norm);
     p.w_post = w->w_post;
+    if (cfg->wquant == MTP_WQ_Q8_0) {
+        p.s_pre = w->w_pre_scale;
+        p.s_post = w->w_post_scale;
+    }
     for (int l = 0; l < cfg->n_blocks; ++l) {
         const mtp_block_weights& b = w->blk[l];
         BlkW& d = p.blk[l];
         d.w_q = b.w_q; d.w_o = b.w_o; d.w_gate = b.w_gate; d.w_up = b.w_up; d.w_down = b.w_down;
+        if (q8) {
+            d.s_q = b.w_q_scale; d.s_o = b.w_o_scale; d.s_gate = b.w_gate_scale; d.s_up = b.w_up_scale;
+            d.s_down = b.w_down_scale;
+        }
         d.attn_norm = static_cast<const float*>(b.attn_norm);
         d.q_norm = static_cast<const float*>(b.q_norm);
         d.post_attn_norm = static_cast<const float*>(b.post_attn_norm);
@@ -540,6 +586,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     if (cudaMemsetAsync(ws, 0, L.amax, s) != cudaSuccess) return MTP_ERR_CUDA;
     cudaError_t e = !bf ? launch_draft_f32(p, grid, smem, s)
                     : p.tc_head ? launch_draft_bf16_tc(p, grid, smem, s)
+                    : q8 ? launch_draft_q8(p, grid, smem, s)
                                 : launch_draft_bf16_cc(p, grid, smem, s);
     return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
 }

@@ -81,6 +81,7 @@ struct KView {
 
 struct BlkW {
     const void *w_q, *w_o, *w_gate, *w_up, *w_down;
+    const uint16_t *s_q, *s_o, *s_gate, *s_up, *s_down;   // Q8_0 block scales (binary16) or null
     const float *attn_norm, *q_norm, *post_attn_norm, *pre_ffn_norm, *post_ffn_norm;
     int view;
     int pad_;
@@ -100,6 +101,7 @@ struct DraftParams {
     const void* w_pre;
     const float* final_norm;
     const void* w_post;
+    const uint16_t *s_pre, *s_post;   // Q8_0 block scales (binary16) or null
     BlkW blk[MTP_MAX_BLOCKS];
     KView views[MTP_MAX_VIEWS];
     const int32_t* kv_len;
@@ -154,6 +156,9 @@ struct DraftParams {
 cudaError_t launch_draft_f32(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_draft_bf16_cc(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_draft_bf16_tc(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
+// bf16 table and KV, Q8_0 projections (CUDA-core paths); head_dim 64, 128 or 256
+cudaError_t launch_draft_q8(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
+int draft_blocks_per_sm_q8(int hd, size_t smem);
 int draft_blocks_per_sm_f32(int hd, size_t smem);
 int draft_blocks_per_sm_bf16_cc(int hd, size_t smem);
 int draft_blocks_per_sm_bf16_tc(int hd, size_t smem);

@@ -13,6 +13,7 @@ namespace mtp {
 MTP_DECL_HDS(f32_)
 MTP_DECL_HDS(bf16_cc_)
 MTP_DECL_HDS(bf16_tc_)
+MTP_DECL_VARIANT(q8_64) MTP_DECL_VARIANT(q8_128) MTP_DECL_VARIANT(q8_256)
 
 #define MTP_SWITCH_HD(pfx, call)        \
     switch (hd) {                       \
@@ -34,6 +35,20 @@ cudaError_t launch_draft_bf16_cc(const DraftParams& p, int grid, size_t smem, cu
 cudaError_t launch_draft_bf16_tc(const DraftParams& p, int grid, size_t smem, cudaStream_t s) {
     const int hd = p.hd;
     MTP_SWITCH_HD(launch_draft_bf16_tc_, (p, grid, smem, s))
+}
+cudaError_t launch_draft_q8(const DraftParams& p, int grid, size_t smem, cudaStream_t s) {
+    switch (p.hd) {
+    case 64: return launch_draft_q8_64(p, grid, smem, s);
+    case 128: return launch_draft_q8_128(p, grid, smem, s);
+    default: return launch_draft_q8_256(p, grid, smem, s);
+    }
+}
+int draft_blocks_per_sm_q8(int hd, size_t smem) {
+    switch (hd) {
+    case 64: return draft_blocks_per_sm_q8_64(smem);
+    case 128: return draft_blocks_per_sm_q8_128(smem);
+    default: return draft_blocks_per_sm_q8_256(smem);
+    }
 }
 int draft_blocks_per_sm_f32(int hd, size_t smem) { MTP_SWITCH_HD(draft_blocks_per_sm_f32_, (smem)) }
 int draft_blocks_per_sm_bf16_cc(int hd, size_t smem) { MTP_SWITCH_HD(draft_blocks_per_sm_bf16_cc_, (smem)) }

@@ -44,6 +44,7 @@ namespace mtp {
 template <typename WT> struct Chunk;
 template <> struct Chunk<uint16_t> {
     static constexpr int EPC = 8;
+    static constexpr bool QUANT = false;
     static __device__ __forceinline__ float dot(const uint4& w, const float* a) {
         const float4 a0 = *reinterpret_cast<const float4*>(a);
         const float4 a1 = *reinterpret_cast<const float4*>(a + 4);
@@ -76,6 +77,7 @@ template <> struct Chunk<uint16_t> {
 };
 template <> struct Chunk<float> {
     static constexpr int EPC = 4;
+    static constexpr bool QUANT = false;
     static __device__ __forceinline__ float dot(const uint4& w, const float* a) {
         const float4 a0 = *reinterpret_cast<const float4*>(a);
         float s = __uint_as_float(w.x) * a0.x;
@@ -96,6 +98,36 @@ template <> struct Chunk<float> {
     }
 };
 
+// Q8_0 codes ("opus-mtp-turbo: Track 1 report", item 3): 16 int8 codes per
+// chunk; the weight is the code times its 32-weight block's binary16 scale,
+// which the GEMVs apply per chunk (chunk_scale)
+template <> struct Chunk<int8_t> {
+    static constexpr int EPC = 16;
+    static constexpr bool QUANT = true;
+    static __device__ __forceinline__ float dot(const uint4& w, const float* a) {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 av = *reinterpret_cast<const float4*>(a + 4 * k);
+            s = fmaf((float)(int8_t)(ws[k] & 0xffu), av.x, s);
+            s = fmaf((float)(int8_t)((ws[k] >> 8) & 0xffu), av.y, s);
+            s = fmaf((float)(int8_t)((ws[k] >> 16) & 0xffu), av.z, s);
+            s = fmaf((float)(int8_t)(ws[k] >> 24), av.w, s);
+        }
+        return s;
+    }
+};
+// scale of chunk c of row r of a [rows, K] weight matrix: 1 unless quantised
+template <typename WT>
+__device__ __forceinline__ float chunk_scale(const uint16_t* S, long long r, int K, int c) {
+    if constexpr (Chunk<WT>::QUANT) {
+        return __half2float(__ushort_as_half(__ldg(S + r * (K / 32) + c / (32 / Chunk<WT>::EPC))));
+    } else {
+        return 1.f;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // GEMV over a row range: out[r, b] = sum_c W[r, c] act[b, c] for b in
 // [b0, b0 + NB) (masked by nb), one warp per row, grid-strided over rows.
@@ -103,7 +135,8 @@ template <> struct Chunk<float> {
 // ---------------------------------------------------------------------------
 template <typename WT, int U, int NB, bool TWO, class Epi>
 __device__ __forceinline__ void gemv_rows(const WT* __restrict__ W, const WT* __restrict__ W2, int rows, int K,
-                                          const float* act, int lda, int b0, int nb, Epi& epi) {
+                                          const float* act, int lda, int b0, int nb, Epi& epi,
+                                          const uint16_t* S = nullptr, const uint16_t* S2 = nullptr) {
     constexpr int EPC = Chunk<WT>::EPC;
     const int nch = K / EPC;
     const int lane = threadIdx.x & 31;
@@ -128,12 +161,14 @@ __device__ __forceinline__ void gemv_rows(const WT* __restrict__ W, const WT* __
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + lane + 32 * u;
                 if (c < nch) {
+                    const float sc = chunk_scale<WT>(S, r, K, c);
+                    const float sc2 = TWO ? chunk_scale<WT>(S2, r, K, c) : 1.f;
 #pragma unroll
                     for (int j = 0; j < NB; ++j) {
                         if (b0 + j < nb) {
                             const float* a = act + (long long)(b0 + j) * lda + c * EPC;
-                            acc[j] += Chunk<WT>::dot(w[u], a);
-                            if (TWO) acc2[j] += Chunk<WT>::dot(w2[u], a);
+                            acc[j] += Chunk<WT>::dot(w[u], a) * sc;
+                            if (TWO) acc2[j] += Chunk<WT>::dot(w2[u], a) * sc2;
                         }
                     }
                 }
@@ -153,7 +188,7 @@ __device__ __forceinline__ void gemv_rows(const WT* __restrict__ W, const WT* __
 // products are added in segment order through `xred` (kWarps floats).
 template <typename WT, int U, int S, class Epi>
 __device__ __forceinline__ void gemv_rows_split(const WT* __restrict__ W, int rows, int K, const float* act, Epi& epi,
-                                                float* xred) {
+                                                float* xred, const uint16_t* SW = nullptr) {
     constexpr int EPC = Chunk<WT>::EPC, RPC = kWarps / S;
     const int nch = K / EPC;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, seg = warp % S;
@@ -174,7 +209,7 @@ __device__ __forceinline__ void gemv_rows_split(const WT* __restrict__ W, int ro
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int c = c0 + lane + 32 * u;
-                    if (c < c_hi) acc += Chunk<WT>::dot(w[u], act + c * EPC);
+                    if (c < c_hi) acc += Chunk<WT>::dot(w[u], act + c * EPC) * chunk_scale<WT>(SW, r, K, c);
                 }
             }
             acc = warp_sum(acc);
@@ -194,7 +229,8 @@ __device__ __forceinline__ void gemv_rows_split(const WT* __restrict__ W, int ro
 // One sequence, rows of at most 16 U chunks: each warp loads two of its
 // grid-strided rows (r and r + the grid's warp count) in one batch.
 template <typename WT, int U, class Epi>
-__device__ __forceinline__ void gemv_rows_pair(const WT* __restrict__ W, int rows, int K, const float* act, Epi& epi) {
+__device__ __forceinline__ void gemv_rows_pair(const WT* __restrict__ W, int rows, int K, const float* act, Epi& epi,
+                                               const uint16_t* SW = nullptr) {
     constexpr int EPC = Chunk<WT>::EPC, UH = U / 2;
     const int nch = K / EPC;
     const int lane = threadIdx.x & 31;
@@ -218,8 +254,8 @@ __device__ __forceinline__ void gemv_rows_pair(const WT* __restrict__ W, int row
         for (int u = 0; u < UH; ++u) {
             const int c = lane + 32 * u;
             if (c < nch) {
-                a0 += Chunk<WT>::dot(w[u], act + c * EPC);
-                a1 += Chunk<WT>::dot(w[UH + u], act + c * EPC);
+                a0 += Chunk<WT>::dot(w[u], act + c * EPC) * chunk_scale<WT>(SW, r, K, c);
+                a1 += Chunk<WT>::dot(w[UH + u], act + c * EPC) * chunk_scale<WT>(SW, two ? r2 : r, K, c);
             }
         }
         const float s0[1] = {warp_sum(a0)}, s1[1] = {warp_sum(a1)};
@@ -228,19 +264,20 @@ __device__ __forceinline__ void gemv_rows_pair(const WT* __restrict__ W, int row
     }
 }
 
+// S, S2: the block scales of W, W2 when WT is a quantised code type (Chunk::QUANT)
 template <typename WT, int U, bool TWO, class Epi>
 __device__ __forceinline__ void gemv(const WT* W, const WT* W2, int rows, int K, const float* act, int lda, int nb,
-                                     Epi& epi, float* xred) {
+                                     Epi& epi, float* xred, const uint16_t* S = nullptr, const uint16_t* S2 = nullptr) {
     if (nb == 1) {
         const int nw = gridDim.x * kWarps, nch = K / Chunk<WT>::EPC;
         if (!TWO && 2 * rows <= nw && nch >= 64)
-            gemv_rows_split<WT, U, 2>(W, rows, K, act, epi, xred);
+            gemv_rows_split<WT, U, 2>(W, rows, K, act, epi, xred, S);
         else if (!TWO && rows > nw && 2 * nch <= 32 * U)
-            gemv_rows_pair<WT, U>(W, rows, K, act, epi);
+            gemv_rows_pair<WT, U>(W, rows, K, act, epi, S);
         else
-            gemv_rows<WT, U, 1, TWO>(W, W2, rows, K, act, lda, 0, 1, epi);
+            gemv_rows<WT, U, 1, TWO>(W, W2, rows, K, act, lda, 0, 1, epi, S, S2);
     } else {
-        for (int b0 = 0; b0 < nb; b0 += 4) gemv_rows<WT, U, 4, TWO>(W, W2, rows, K, act, lda, b0, nb, epi);
+        for (int b0 = 0; b0 < nb; b0 += 4) gemv_rows<WT, U, 4, TWO>(W, W2, rows, K, act, lda, b0, nb, epi, S, S2);
     }
 }
 
@@ -2244,7 +2281,8 @@ static __device__ __noinline__ bool sample_step(const DraftParams& p, int k, uns
     return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
 }
 
-template <typename WT, int HD, bool TC>
+// PT: the projections' weight type (WT, or int8_t for Q8_0 codes with block scales)
+template <typename WT, int HD, bool TC, typename PT>
 __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts, TcState& hs) {
     __shared__ float red[2 * kWarps];
     __shared__ unsigned long long head_best[kWarps][32];
@@ -2315,8 +2353,8 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     mbar_fence_init();
     __syncthreads();
     // one GEMV phase and the barrier after it
-    auto gemv_step = [&](int phase, int k, int l, const void* W, const void* W2, int R, int K, auto& epi,
-                         auto two) -> bool {
+    auto gemv_step = [&](int phase, int k, int l, const void* W, const void* W2, const uint16_t* S,
+                         const uint16_t* S2, int R, int K, auto& epi, auto two) -> bool {
         constexpr bool TWO = decltype(two)::value;
         int lda = 0;
         bool ok = true;
@@ -2339,8 +2377,8 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 }
             }
         } else {
-            gemv<WT, TWO ? U / 2 : U, TWO>(reinterpret_cast<const WT*>(W), reinterpret_cast<const WT*>(W2), R, K, a,
-                                           lda, p.B, epi, red);
+            gemv<PT, TWO ? U / 2 : U, TWO>(reinterpret_cast<const PT*>(W), reinterpret_cast<const PT*>(W2), R, K, a,
+                                           lda, p.B, epi, red, S, S2);
         }
         if (TC && p.tc_head && phase == PH_POST) fence_proxy_async_global();   // h parts are read by tensor copies
         return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
@@ -2360,7 +2398,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 write_conf(p, k - 1, b);
         {
             StoreEpi e{p.XB, p.d_a};
-            if (!gemv_step(PH_PRE, k, 0, p.w_pre, nullptr, p.d_a, 2 * p.d_t, e, One{})) return;
+            if (!gemv_step(PH_PRE, k, 0, p.w_pre, nullptr, p.s_pre, nullptr, p.d_a, 2 * p.d_t, e, One{})) return;
         }
 
         for (int l = 0; l < p.L; ++l) {
@@ -2385,7 +2423,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             }
             {
                 StoreEpi e{p.QR, p.Hq * p.hd};
-                if (!gemv_step(PH_Q, k, l, bw.w_q, nullptr, p.Hq * p.hd, p.d_a, e, One{})) return;
+                if (!gemv_step(PH_Q, k, l, bw.w_q, nullptr, bw.s_q, nullptr, p.Hq * p.hd, p.d_a, e, One{})) return;
             }
             // ---- ATT ----
             if (!attention_phase<WT, HD, TC ? kAttnStagesTc : kAttnStages, TC>(p, l, smem, s_kv, s_tab,
@@ -2398,26 +2436,26 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             // ---- O ----
             {
                 StoreEpi e{p.YB, p.d_a};
-                if (!gemv_step(PH_O, k, l, bw.w_o, nullptr, p.d_a, p.Hq * p.hd, e, One{})) return;
+                if (!gemv_step(PH_O, k, l, bw.w_o, nullptr, bw.s_o, nullptr, p.d_a, p.Hq * p.hd, e, One{})) return;
             }
             // ---- FFN1 (gate and up share the input; GeGLU in the epilogue) ----
             {
                 GegluEpi e{p.MB, p.F};
-                if (!gemv_step(PH_FFN1, k, l, bw.w_gate, bw.w_up, p.F, p.d_a, e, Two{})) return;
+                if (!gemv_step(PH_FFN1, k, l, bw.w_gate, bw.w_up, bw.s_gate, bw.s_up, p.F, p.d_a, e, Two{})) return;
             }
             // ---- FFN2 ----
             {
                 StoreEpi e{p.Y2, p.d_a};
-                if (!gemv_step(PH_FFN2, k, l, bw.w_down, nullptr, p.d_a, p.F, e, One{})) return;
+                if (!gemv_step(PH_FFN2, k, l, bw.w_down, nullptr, bw.s_down, nullptr, p.d_a, p.F, e, One{})) return;
             }
         }
         // ---- POST ----
         if (TC && p.tc_head) {
             StoreXhEpi e{p.HN, p.d_t, p.XH, p.XL, kTcHeadM};
-            if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
+            if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.s_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         } else {
             StoreEpi e{p.HN, p.d_t};
-            if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.d_t, p.d_a, e, One{})) return;
+            if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.s_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         }
         // ---- HEAD ----
         if (p.n_cent > 0) {
@@ -2450,7 +2488,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
 // The persistent draft kernel.  TC: the variant with the tensor-core paths,
 // whose tensor memory is allocated by warp 2 before the body and freed after
 // it; every exit of the body is uniform over the CTA.
-template <typename WT, int HD, bool TC>
+template <typename WT, int HD, bool TC, typename PT>
 __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constant__ DraftParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int NB = 2 * kTcMaxStages + 4;   // barriers of one ring
@@ -2477,7 +2515,7 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
         ts.tmem = tc_tmem;
         hs.tmem = tc_tmem;
     }
-    draft_body<WT, HD, TC>(p, smem, ts, hs);
+    draft_body<WT, HD, TC, PT>(p, smem, ts, hs);
     if (TC && p.tc_head) {
         tc_fence_before();
         __syncthreads();
@@ -2486,20 +2524,22 @@ __global__ void __launch_bounds__(kThreads, 1) draft_kernel(const __grid_constan
     }
 }
 
-template <typename WT, int HD, bool TC>
+template <typename WT, int HD, bool TC, typename PT = WT>
 cudaError_t launch_draft_t(const DraftParams& p, int grid, size_t smem, cudaStream_t s) {
     cudaError_t e =
-        cudaFuncSetAttribute(draft_kernel<WT, HD, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(draft_kernel<WT, HD, TC, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<DraftParams*>(&p)};
-    return cudaLaunchCooperativeKernel((const void*)draft_kernel<WT, HD, TC>, dim3(grid), dim3(kThreads), args, smem, s);
+    return cudaLaunchCooperativeKernel((const void*)draft_kernel<WT, HD, TC, PT>, dim3(grid), dim3(kThreads), args,
+                                       smem, s);
 }
 
-template <typename WT, int HD, bool TC>
+template <typename WT, int HD, bool TC, typename PT = WT>
 int draft_blocks_per_sm_t(size_t smem) {
     int n = 0;
-    cudaFuncSetAttribute(draft_kernel<WT, HD, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draft_kernel<WT, HD, TC>, kThreads, smem) != cudaSuccess)
+    cudaFuncSetAttribute(draft_kernel<WT, HD, TC, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draft_kernel<WT, HD, TC, PT>, kThreads, smem) !=
+        cudaSuccess)
         return 0;
     return n;
 }

@@ -7,7 +7,7 @@ import dataclasses
 import numpy as np
 
 from . import (Config, KVView, Weights, alloc_workspace, draft_block, make_config, make_view, make_weights,
-               workspace_size)
+               quantize_q8_0, workspace_size)
 
 
 def to_device(a: np.ndarray, dtype: str | None = None, device="cuda"):
@@ -57,12 +57,23 @@ def upload_draft(w, device="cuda", extra_ws_for=None, reuse: "DeviceDraft | None
     cfg = make_config(m.d_t, m.d_a, m.n_blocks, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff, m.vocab,
                       wdtype=m.dtype, rms_eps=m.rms_eps, attn_scale=m.attn_scale, emb_scale=m.emb_scale,
                       logit_softcap=m.logit_softcap, n_centroids=getattr(m, "n_centroids", 0),
-                      centroid_top_k=getattr(m, "centroid_top_k", 0))
+                      centroid_top_k=getattr(m, "centroid_top_k", 0), wquant=getattr(m, "wquant", "none"))
     same = (reuse is not None and bytes(reuse.cfg) == bytes(cfg) and
             all(n in reuse.tensors and tuple(reuse.tensors[n].shape) == a.shape for n, a in w.weights.items()))
     if same:
         tensors = {n: reuse.tensors[n] for n in w.weights}
         reuse.tensors.pop("_views", None)   # the old views go with the old workload
+    elif getattr(m, "wquant", "none") == "q8_0":
+        # Q8_0 projections: quantised here by the library's host quantiser,
+        # codes and block scales uploaded side by side
+        tensors = {}
+        for n, a in w.weights.items():
+            if a.dtype == np.float32 and a.ndim == 2 and n.split(".")[-1].startswith("w_"):
+                q, d = quantize_q8_0(a)
+                tensors[n] = torch.from_numpy(q).to(device)
+                tensors[n + ".scale"] = torch.from_numpy(d.view(np.int16)).to(device)
+            else:
+                tensors[n] = to_device(a, device=device)
     else:
         tensors = {n: to_device(a, device=device) for n, a in w.weights.items()}
     views, keep = [], []

@@ -269,11 +269,26 @@ def _projection_names(m):
                                        for n in ("w_q", "w_o", "w_gate", "w_up", "w_down"))
 
 
+_DERIVED: dict = {}   # id(source array) -> (source, derived): widened or dequantised copies, reused
+
+
+def _derived(a, kind):
+    hit = _DERIVED.get((id(a), kind))
+    if hit is not None and hit[0] is a:
+        return hit[1]
+    if kind == "widen":
+        out = np.ascontiguousarray((a.astype(np.uint32) << 16).view(np.float32)) if a.dtype == np.uint16 else a
+    else:
+        out = dequantize_q8_0(*quantize_q8_0(a))
+    if len(_DERIVED) > 64:
+        _DERIVED.clear()
+    _DERIVED[(id(a), kind)] = (a, out)
+    return out
+
+
 def _widen(a):
     """bf16 bit patterns (uint16) to fp32, exactly; other arrays unchanged."""
-    if a.dtype == np.uint16:
-        return np.ascontiguousarray((a.astype(np.uint32) << 16).view(np.float32))
-    return a
+    return _derived(a, "widen")
 
 
 class _Bound:
@@ -292,7 +307,7 @@ class _Bound:
             # table and the KV widened from bf16 exactly, and the step run in fp32
             proj = set(_projection_names(m))
             arrs = [None if a is None else
-                    dequantize_q8_0(*quantize_q8_0(a)) if n in proj else
+                    _derived(a, "q8") if n in proj else
                     _widen(a) for n, a in zip(names, arrs)]
             self.model.wbf16 = 0
         self.keep += [a for a in arrs if a is not None]

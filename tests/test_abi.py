@@ -80,3 +80,27 @@ def test_workspace_size_host_only():
     bad = mtp.make_config(5120, 1024, 4, 16, 96, 4, 4096, 262144)   # head_dim 96 unsupported
     with pytest.raises(mtp.MTPError):
         mtp.workspace_size(bad, 1, 3, 262144)
+
+
+def test_host_q8_0_quantiser_matches_the_oracle():
+    """mtp_quantize_q8_0 (host code of the library) and the oracle's
+    quantiser give the same codes and scales bit for bit (integer output of
+    the same fp32 rule), over Gaussian rows, exact code multiples, zero
+    blocks and extreme ranges."""
+    import numpy as np
+    import oracle
+    import synth
+    mtp_build.build()
+    rng = np.random.default_rng(11)
+    w = synth.normal(12, "hostq8", (96, 512), std=0.02)
+    w[3, :32] = 0.0
+    w[4] *= 1e-6
+    w[5] *= 1e4
+    w[6, :64] = np.arange(-32, 32, dtype=np.float32) * np.float32(2.0 ** -5)
+    w[7] = rng.standard_normal(512).astype(np.float32) * 3e-8   # binary16 subnormal scales
+    q1, d1 = mtp.quantize_q8_0(w)
+    q2, d2 = oracle.quantize_q8_0(w)
+    np.testing.assert_array_equal(q1, q2)
+    np.testing.assert_array_equal(d1, d2)
+    with pytest.raises(mtp.MTPError):
+        mtp.quantize_q8_0(np.zeros((2, 48), dtype=np.float32))
