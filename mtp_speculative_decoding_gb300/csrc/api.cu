@@ -549,6 +549,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
             // projections: weights [R, K] row-major, inputs staged as [Bp, kmax]
             const TcPlan plan = tc_plan(cfg, B, grid);
             p.tc_proj = 1;
+            p.att_fold = 1;   // the O prologue merges split attention segments: one row per CTA, no counter waits
             for (int i = 0; i < 6; ++i) p.sk[i] = plan.sk[i];
             p.XA = reinterpret_cast<uint16_t*>(base + L.XA);
             p.XAL = reinterpret_cast<uint16_t*>(base + L.XAL);

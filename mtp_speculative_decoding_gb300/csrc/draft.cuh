@@ -128,6 +128,7 @@ struct DraftParams {
     int th_stages;               // LM head ring depth
     uint16_t *XH, *XL;           // bf16 high / low parts of h as the head's tiled operand (kTcHeadM rows, >= B zero)
     int tc_proj;                 // 1: projections on tensor cores (activations staged in global memory)
+    int att_fold;                // 1: split attention segments are merged by the O prologue (tc_proj only)
     int sk[6];                   // split-K factor of each projection phase (PH_PRE .. PH_POST)
     uint16_t *XA, *XAL;          // bf16 high / low parts of the current phase input, tiled
     float* PB;                   // [S][B][R] split partials of the last projection (FFN1: R = 2 F)

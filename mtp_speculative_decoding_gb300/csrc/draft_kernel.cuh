@@ -576,9 +576,12 @@ __device__ __forceinline__ void vec_copy(const VecCopy<NS>& c, int n) {
 // `writer` marks the one CTA that also stores residual-stream updates.  The
 // norm gains are staged in gs (2 max(d_t, d_a) floats) by the same loops that
 // load the activations.
+struct AttnTab;
+static __device__ void attn_fold_row(const DraftParams& p, const AttnTab& tab, int l, int b, float* dst);
+
 template <typename WT, bool TC>
 __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, float* dst, float* tmp, bool writer,
-                          float* red, float* gs) {
+                          float* red, float* gs, const AttnTab* tab) {
     switch (phase) {
     case PH_PRE: {
         const int n = p.d_t;
@@ -684,7 +687,8 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     }
     case PH_O: {
         const int n = p.Hq * p.hd;
-        vec_copy<1, 1>(VecCopy<1>{{p.OB + (long long)b * n}, {dst}}, n);
+        if (p.att_fold) attn_fold_row(p, *tab, l, b, dst);   // merges the attention's split partials here
+        else vec_copy<1, 1>(VecCopy<1>{{p.OB + (long long)b * n}, {dst}}, n);
         __syncthreads();
         break;
     }
@@ -731,14 +735,14 @@ __device__ __forceinline__ int phase_k(const DraftParams& p, int phase) {
 // failed.
 template <typename WT, bool TC>
 __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l, float* smem_act, float* smem_tmp,
-                                  float* red, unsigned int& epoch, int& lda, bool& ok) {
+                                  float* red, unsigned int& epoch, int& lda, bool& ok, const AttnTab* tab) {
     const int K = phase_k(p, phase);
     // gain stage after the activation area
     float* gs = smem_act + (p.act_smem ? (long long)p.B * p.kmax : (long long)p.kmax);
     ok = true;
     if (p.act_smem) {
         for (int b = 0; b < p.B; ++b)
-            build_act<WT, TC>(p, phase, k, l, b, smem_act + (long long)b * K, smem_tmp, blockIdx.x == 0, red, gs);
+            build_act<WT, TC>(p, phase, k, l, b, smem_act + (long long)b * K, smem_tmp, blockIdx.x == 0, red, gs, tab);
         lda = K;
         return smem_act;
     }
@@ -749,7 +753,7 @@ __device__ const float* stage_act(const DraftParams& p, int phase, int k, int l,
         if (phase == PH_HEAD) { lda = K; return p.HN; }
     }
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-        build_act<WT, TC>(p, phase, k, l, b, smem_act, smem_tmp, true, red, gs);
+        build_act<WT, TC>(p, phase, k, l, b, smem_act, smem_tmp, true, red, gs, tab);
         if ((TC && p.tc_proj)) {
             // tensor-core operand: bf16 high and low parts, read by tensor
             // copies; 8 consecutive columns are one 16-byte chunk of the
@@ -948,6 +952,71 @@ __device__ __forceinline__ AttnPiece attn_piece_eq(const DraftParams& p, const K
 __device__ __forceinline__ int attn_slot(const AttnTab& t, int v, int cf, int q, long long s0) {
     if (t.cseg[v] > 0) return 2 * (cf + q);
     return 2 * (cf + q) + ((q == 0 && attn_lo(t, v, cf) != s0) ? 1 : 0);
+}
+
+// The attention output of sequence b for block l, [Hq][hd], into dst (whole
+// CTA): per (b, KV head g) segment the finished output when one CTA covered
+// it, else the LSE merge of its CTAs' partials.  Used by the O prologue when
+// the attention phase leaves its split segments unmerged (att_fold).  One
+// warp per head: lanes take the partials' (m, l) in parallel, then the
+// head's hd outputs (hd / 32 per lane) accumulate over the partials with
+// every lane's loads of a partial in flight together.
+static __device__ void attn_fold_row(const DraftParams& p, const AttnTab& tab, int l, int b, float* dst) {
+    const int view = p.blk[l].view, HD = p.hd, grp = p.Hq / p.Hkv, PSZ = attn_psz(grp, HD);
+    const int n = view_keys(p.views[view], __ldg(p.kv_len + b));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5, DL = HD / 32;
+    for (int h = warp; h < p.Hq; h += nw) {
+        const int g = h / grp, hh = h - g * grp;
+        long long s0;
+        int cf, S;
+        if (tab.cseg[view] > 0) {
+            const int cs = tab.cseg[view];
+            cf = (b * p.Hkv + g) * cs;
+            S = cs;
+            s0 = 0;
+        } else {
+            s0 = tab.pre[view][b] + (long long)g * n;
+            cf = attn_cta(tab, view, s0);
+            S = attn_cta(tab, view, s0 + n - 1) - cf + 1;
+        }
+        float* out = dst + h * HD;
+        if (S == 1) {
+            for (int d = lane; d < HD; d += 32) out[d] = __ldcg(p.OB + ((long long)b * p.Hq + h) * HD + d);
+            continue;
+        }
+        auto part = [&](int q) { return p.PART + (long long)attn_slot(tab, view, cf, q, s0) * PSZ; };
+        float M = -INFINITY;
+        for (int q = lane; q < S; q += 32) M = fmaxf(M, __ldcg(part(q) + grp * HD + hh));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float mu = M == -INFINITY ? 0.f : M;
+        float Ls = 0.f, O[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) O[i] = 0.f;
+        for (int q0 = 0; q0 < S; q0 += 32) {
+            const int q = q0 + lane;
+            float e = 0.f;
+            if (q < S) {
+                const float* pq = part(q);
+                e = expf(__ldcg(pq + grp * HD + hh) - mu);
+                Ls = fmaf(e, __ldcg(pq + grp * HD + grp + hh), Ls);
+            }
+            const int nq = S - q0 < 32 ? S - q0 : 32;
+#pragma unroll 2
+            for (int j = 0; j < nq; ++j) {
+                const float ej = __shfl_sync(0xffffffffu, e, j);
+                const float* oq = part(q0 + j) + hh * HD + lane;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i < DL) O[i] = fmaf(ej, __ldcg(oq + 32 * i), O[i]);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < DL) out[lane + 32 * i] = O[i] / Ls;
+    }
 }
 
 // Sum of NV per-lane values over the LPR lanes of a row group, transposed:
@@ -1415,7 +1484,7 @@ __device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsi
 
         fence_proxy_async_smem();   // the merge's shared-memory writes before the next stage copies
         __syncthreads();
-        if (A.S > 1) {
+        if (A.S > 1 && !p.att_fold) {   // folded: the O prologue merges the partials after the barrier
             any_split = true;
             if (tid == 0) red_release_add(p.att_cnt + b * p.Hkv + g, 1u);
         }
@@ -2361,7 +2430,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         if constexpr (TC) {
             if (p.tc_proj && threadIdx.x == 0) tc_prefetch(tc_job(p, phase, l));
         }
-        const float* a = stage_act<WT, TC>(p, phase, k, l, act, tmp, red, epoch, lda, ok);
+        const float* a = stage_act<WT, TC>(p, phase, k, l, act, tmp, red, epoch, lda, ok, &s_tab);
         if (!ok) return false;
         if (TC && p.tc_proj) {
             // tensor cores over the staged bf16 input parts: split partials,
@@ -2464,7 +2533,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             int lda = 0;
             const float* a = nullptr;
             if (p.head_slotb == 0 && !(TC && p.tc_head)) {
-                a = stage_act<WT, TC>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok);
+                a = stage_act<WT, TC>(p, PH_HEAD, k, 0, act, tmp, red, epoch, lda, ok, &s_tab);
                 if (!ok) return;
             }
             if (!head_phase<WT, TC>(p, k, a, lda, head_best, smem, head_bar, head_par, head_part, hs)) return;
