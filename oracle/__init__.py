@@ -96,6 +96,12 @@ def _declare(L):
     L.orc_verify_greedy.argtypes = [P, I, I, I, I, P, P, P]
     L.orc_verify_sample.argtypes = [P, P, I, I, I, I, P, P, I, P, U64, U64, P, P, P]
     L.orc_sample_drafts.argtypes = [P, I, I, I, I, P, I, P, U64, U64, P, P]
+    L.orc_silu.argtypes = [D]
+    L.orc_silu.restype = D
+    L.orc_to_bf16.argtypes = [D]
+    L.orc_to_bf16.restype = C.c_uint16
+    L.orc_nextn_draft.argtypes = [P, P, P, I, I, P, I, P, P, P, P, P, P, P, P, P, P, P]
+    L.orc_nextn_draft.restype = I
     L.orc_set_threads.argtypes = [I]
     L.orc_num_threads.restype = I
 
@@ -388,6 +394,78 @@ def draft_step(w, b, step, tok, h_prev):
     if rc != 0:
         raise ValueError("oracle draft step rejected its inputs")
     return hn[0], z[0]
+
+
+# ----------------------------------------------------------------------------
+# the dense NextN drafter
+# ----------------------------------------------------------------------------
+
+NEXTN_ORDER = ("tok_embd", "enorm", "hnorm", "eh_proj", "head_norm", "attn_norm", "w_qkv", "q_norm",
+               "k_norm", "w_o", "ffn_norm", "w_gate", "w_up", "w_down")
+
+
+def silu(x):
+    return np.array([lib().orc_silu(float(v)) for v in np.ravel(x)]).reshape(np.shape(x))
+
+
+def to_bf16(x):
+    """Real values rounded once to bf16 (nearest, ties to even): uint16 bit patterns."""
+    return np.array([lib().orc_to_bf16(float(v)) for v in np.ravel(x)], dtype=np.uint16).reshape(np.shape(x))
+
+
+def nextn_draft(w, force=None, seqs=None, want_logits=True, dkv=None):
+    """One drafting call of the NextN drafter over sequences ``seqs`` (default:
+    all): the catch-up rows, then w.N draft steps (see orc_nextn_draft).
+
+    ``force`` ([B, N] int32) teacher-forces the token consumed at step k+1.
+    ``dkv`` (optional dict with k, v) replaces the workload's drafter KV as the
+    starting state.  The workload's arrays are never modified: the call works
+    on a copy of the KV and returns it.  Returns dict(drafts [S,N], h_last
+    [S,d] f64, logits [S,N,V] f64 or None, margin [S,N], conf [S,N], k, v (the
+    drafter KV after the call, [B, Hkv, cap, hd], all sequences)).
+    """
+    L = lib()
+    m = w.model
+    seqs = list(range(w.B)) if seqs is None else list(seqs)
+    S, N, V, d = len(seqs), w.N, m.vocab, m.d
+    src = w.dkv if dkv is None else dkv
+    k = np.array(src["k"], copy=True, order="C")
+    v = np.array(src["v"], copy=True, order="C")
+    Bv, H, cap, hd = k.shape
+    arrs = [np.ascontiguousarray(w.weights[n]) for n in NEXTN_ORDER]
+    tensors = (C.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    mdl = _model(m)
+    esz = k.itemsize
+    out = dict(drafts=np.empty((S, N), dtype=np.int32), h_last=np.empty((S, d)), margin=np.empty((S, N)),
+               conf=np.empty((S, N)), logits=np.empty((S, N, V)) if want_logits else None)
+    M = max(1, w.M)
+    cu_tok = np.zeros((w.B, M), dtype=np.int32)
+    cu_h = np.zeros((w.B, M, d), dtype=np.float32)
+    cu_tok[:, :w.M] = w.cu_tok
+    cu_h[:, :w.M] = w.cu_h
+    for j, b in enumerate(seqs):
+        off = b * H * cap * hd * esz
+        vw = View(k.ctypes.data + off, v.ctypes.data + off, H * cap * hd, cap * hd, hd, cap, 0, 0, 0,
+                  float(w.dkv["rope_theta"]))
+        f = None if force is None else np.ascontiguousarray(force[b:b + 1], dtype=np.int32)
+        dd = np.empty((1, N), dtype=np.int32)
+        h = np.empty((1, d))
+        z = np.empty((1, N, V)) if want_logits else None
+        mg, cf = np.empty((1, N)), np.empty((1, N))
+        rc = L.orc_nextn_draft(C.byref(mdl), tensors, C.byref(vw), 1, N,
+                               _p(np.ascontiguousarray(w.kv_len[b:b + 1], dtype=np.int32)), M,
+                               _p(np.ascontiguousarray(w.n_cu[b:b + 1], dtype=np.int32)),
+                               _p(np.ascontiguousarray(cu_tok[b:b + 1])), _p(np.ascontiguousarray(cu_h[b:b + 1])),
+                               _p(np.ascontiguousarray(w.last_tok[b:b + 1], dtype=np.int32)),
+                               _p(np.ascontiguousarray(w.h_prev[b:b + 1], dtype=np.float32)), _p(f), _p(dd), _p(h),
+                               _p(z), _p(mg), _p(cf))
+        if rc != 0:
+            raise ValueError(f"oracle NextN drafter rejected its inputs (rc={rc})")
+        out["drafts"][j], out["h_last"][j], out["margin"][j], out["conf"][j] = dd[0], h[0], mg[0], cf[0]
+        if want_logits:
+            out["logits"][j] = z[0]
+    out["k"], out["v"] = k, v
+    return out
 
 
 # ----------------------------------------------------------------------------

@@ -23,8 +23,12 @@
  *        steps; draft positions are > attn_pos).
  *  [NX]  "MTP decoding (--mtp)", "Requirements" (NextN enorm / hnorm / eh_proj:
  *        separate norms of the token embedding and of the hidden state before
- *        the projection) and "How it is wired" (accept the longest prefix whose
- *        argmax matches, the next token comes from the first unverified row).
+ *        the projection; the NextN block's own attention and feed-forward and
+ *        the shared head with its norm), "How it is wired" (accept the longest
+ *        prefix whose argmax matches, the next token comes from the first
+ *        unverified row; the draft context catches up on the accepted rows)
+ *        and "The catch-up runs on the accepted prefix" (the catch-up rows are
+ *        [confirmed token, accepted drafts]; no rollback of the draft KV).
  *  [SP]  "opus-mtp-turbo: Track 1 report", item 4 "temp > 0 verification"
  *        (sample_dist: top-k, penalties over history + input[0..i], temp,
  *        min-p, top-p; accept with p(x)/q(x); on reject sample
@@ -34,6 +38,8 @@
  *        state chain alone).
  *        Item 3 "Q4_0 / Q5_0 draft weights": the Q8_0 weight format of its
  *        quantisation-error table (ggml's rule, see orc_quantize_q8_0).
+ *        "The two MTP lanes": the NextN drafter runs its own block with its own
+ *        (unified) KV, unlike the assistant that reads the target's.
  *  [PH]  Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
  *        1, 2, 3" (SC'11): the Philox-4x32-10 counter-based generator.
  *
@@ -44,7 +50,14 @@
  * head h / (Hq / Hkv); GELU is the tanh form; argmax ties go to the lowest
  * index and NaN never wins; the sliding window reads the last W positions
  * [kv_len - W, kv_len) at every step; KV views are ring buffers (position t in
- * slot t % cap).
+ * slot t % cap).  The NextN drafter (the pages name its tensors, not its
+ * arithmetic): one pre-norm block at the backbone width, x += w_o attn and
+ * x += w_down(silu(w_gate n) * w_up n) with n = ffn_norm(x); a fused query /
+ * key / value projection; per-head q and k norms; NeoX RoPE of queries and
+ * keys at the row's position (the row index in its own KV); causal attention
+ * over rows [0, pos]; keys and values stored rounded to the weights' type;
+ * embedding scale 1; the next step's hidden state is the block output before
+ * head_norm.
  */
 #include <math.h>
 #include <stdint.h>
@@ -704,6 +717,172 @@ int orc_draft_block(const orc_model *m, const void *const *t, const int32_t *blo
     }
     if (h_last && rc == 0) memcpy(h_last, h, sizeof(double) * (size_t)B * d_t);
     free(h); free(hn); free(z); free(tok); free(ids); free(wf); free(pen); free(cg);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the dense NextN drafter ([NX] "Requirements", "How it is wired", "The     */
+/* catch-up runs on the accepted prefix"; [FN] "The two MTP lanes")          */
+/* ------------------------------------------------------------------------ */
+
+/* NextN tensor table: its own order (the assistant's table above is not
+ * used).  One block at the backbone width d = d_t:
+ *   tok_embd [V, d]   the table, also the (shared) LM head
+ *   enorm, hnorm [d]  norms of the token embedding and of the hidden state
+ *   eh_proj [d, 2d]   projection of [enorm(e); hnorm(h)]
+ *   head_norm [d]     the shared head's norm
+ *   attn_norm [d], w_qkv [(Hq + 2 Hkv) hd, d] (query rows, then key rows,
+ *   then value rows), q_norm [hd], k_norm [hd], w_o [d, Hq hd],
+ *   ffn_norm [d], w_gate, w_up [F, d], w_down [d, F] */
+enum { NX_TOK_EMBD, NX_ENORM, NX_HNORM, NX_EH_PROJ, NX_HEAD_NORM, NX_ATTN_NORM, NX_W_QKV, NX_Q_NORM, NX_K_NORM,
+       NX_W_O, NX_FFN_NORM, NX_W_GATE, NX_W_UP, NX_W_DOWN, NX_COUNT };
+
+/* SiLU, the gate of the NextN block's feed-forward (SwiGLU) */
+double orc_silu(double x) { return x / (1.0 + exp(-x)); }
+
+/* A real number rounded once to bf16, nearest with ties to even; returns the
+ * bit pattern.  The drafter stores its own keys and values in the weights'
+ * type, so the oracle writes them rounded the same way. */
+uint16_t orc_to_bf16(double x) {
+    if (isnan(x)) return 0x7FC0;
+    if (x == 0.0) return signbit(x) ? 0x8000 : 0x0000;
+    int e;
+    frexp(x, &e);                      /* |x| in [2^(e-1), 2^e) */
+    int eu = e - 8;                    /* 8 significant bits: ulp 2^(e-8) */
+    if (eu < -133) eu = -133;          /* below the normal range: bf16's subnormal spacing */
+    const double r = rint(ldexp(x, -eu));   /* the default rounding mode: nearest, ties to even */
+    const float y = (float)ldexp(r, eu);    /* exact in fp32 (or infinite past the range) */
+    uint32_t u;
+    memcpy(&u, &y, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+static void store_elem(const void *p, int64_t i, int bf16, double x) {
+    if (bf16) ((uint16_t *)(uintptr_t)p)[i] = orc_to_bf16(x);
+    else ((float *)(uintptr_t)p)[i] = (float)x;
+}
+
+#define NT(i) (t[(i)])
+
+/* One position of the NextN block for sequence b of the drafter's KV `dkv`
+ * (K and V [B][Hkv][cap][hd], position p in slot p).
+ *   tk, hin  the token at position pos and the hidden state paired with it:
+ *            the target's at the previous position (catch-up rows and the
+ *            first draft step), the block's own output after that
+ *   full 0   a catch-up row: its key and value are written at slot pos and
+ *            nothing else is computed (nothing downstream reads the rest)
+ *   full 1   a draft step: also the causal attention over positions
+ *            [0, pos], the feed-forward and the head; hout [d] receives the
+ *            block output (the next step's hidden state) and z [V] the logits
+ * The block follows the NextN layout of [NX] "Requirements" (enorm, hnorm,
+ * eh_proj, one attention + feed-forward block, the shared head with its
+ * norm); the pre-norm residual structure, per-head q/k norms, NeoX RoPE at
+ * the row's position and SwiGLU are the readings listed in the design notes. */
+static int nextn_row(const orc_model *m, const void *const *t, const orc_view *dkv, int b, int32_t tk,
+                     const double *hin, int64_t pos, int full, double *hout, double *z) {
+    const int d = m->d_t, hd = m->head_dim, Hq = m->n_q_heads, Hkv = m->n_kv_heads, F = m->d_ff, V = m->vocab;
+    const int bf = m->wbf16, grp = Hq / Hkv, qkv = (Hq + 2 * Hkv) * hd;
+    if (tk < 0 || tk >= V || pos < 0 || pos >= dkv->cap) return -1;
+    double *e = malloc(sizeof(double) * d), *u = malloc(sizeof(double) * 2 * d);
+    double *x = malloc(sizeof(double) * d), *a = malloc(sizeof(double) * d), *y = malloc(sizeof(double) * d);
+    double *q = malloc(sizeof(double) * qkv), *o = malloc(sizeof(double) * Hq * hd);
+    double *gt = malloc(sizeof(double) * F), *up = malloc(sizeof(double) * F), *tmp = malloc(sizeof(double) * hd);
+    /* [enorm(e); hnorm(h)] -> eh_proj ([NX] Requirements) */
+    for (int c = 0; c < d; ++c) e[c] = elem(NT(NX_TOK_EMBD), (int64_t)tk * d + c, bf) * m->emb_scale;
+    orc_rmsnorm(e, d, (const float *)NT(NX_ENORM), m->rms_eps, u);
+    orc_rmsnorm(hin, d, (const float *)NT(NX_HNORM), m->rms_eps, u + d);
+    orc_matvec(NT(NX_EH_PROJ), d, 2 * d, bf, u, x);
+    /* attention input norm, the fused query / key / value projection */
+    orc_rmsnorm(x, d, (const float *)NT(NX_ATTN_NORM), m->rms_eps, a);
+    orc_matvec(NT(NX_W_QKV), qkv, d, bf, a, q);
+    /* keys: per-head norm, RoPE at pos; key and value stored at slot pos */
+    for (int g = 0; g < Hkv; ++g) {
+        double *kh = q + (size_t)(Hq + g) * hd, *vh = q + (size_t)(Hq + Hkv + g) * hd;
+        orc_rmsnorm(kh, hd, (const float *)NT(NX_K_NORM), m->rms_eps, tmp);
+        orc_rope_neox(tmp, hd, pos, dkv->rope_theta);
+        const int64_t base = (int64_t)b * dkv->stride_b + (int64_t)g * dkv->stride_h + pos * dkv->stride_t;
+        for (int c = 0; c < hd; ++c) {
+            store_elem(dkv->k, base + c, bf, tmp[c]);
+            store_elem(dkv->v, base + c, bf, vh[c]);
+        }
+    }
+    if (full) {
+        /* queries: per-head norm, RoPE at pos; attention over [0, pos] as stored */
+        for (int h = 0; h < Hq; ++h) {
+            double *qh = q + (size_t)h * hd;
+            orc_rmsnorm(qh, hd, (const float *)NT(NX_Q_NORM), m->rms_eps, tmp);
+            orc_rope_neox(tmp, hd, pos, dkv->rope_theta);
+            orc_attend_head(tmp, dkv, b, h / grp, hd, (int)(pos + 1), m->attn_scale, bf, o + (size_t)h * hd);
+        }
+        orc_matvec(NT(NX_W_O), d, Hq * hd, bf, o, y);
+        for (int c = 0; c < d; ++c) x[c] += y[c];
+        /* feed-forward: norm, SwiGLU, residual */
+        orc_rmsnorm(x, d, (const float *)NT(NX_FFN_NORM), m->rms_eps, a);
+        orc_matvec(NT(NX_W_GATE), F, d, bf, a, gt);
+        orc_matvec(NT(NX_W_UP), F, d, bf, a, up);
+        for (int f = 0; f < F; ++f) gt[f] = orc_silu(gt[f]) * up[f];
+        orc_matvec(NT(NX_W_DOWN), d, F, bf, gt, y);
+        for (int c = 0; c < d; ++c) x[c] += y[c];
+        memcpy(hout, x, sizeof(double) * d);
+        /* the shared head: its norm, then the tied table (optional softcap) */
+        orc_rmsnorm(x, d, (const float *)NT(NX_HEAD_NORM), m->rms_eps, a);
+        orc_matvec(NT(NX_TOK_EMBD), V, d, bf, a, z);
+        if (m->logit_softcap > 0.0)
+            for (int v = 0; v < V; ++v) z[v] = m->logit_softcap * tanh(z[v] / m->logit_softcap);
+    }
+    free(e); free(u); free(x); free(a); free(y); free(q); free(o); free(gt); free(up); free(tmp);
+    return 0;
+}
+
+/* One drafting call of the NextN drafter for B sequences ([NX] "How it is
+ * wired": draft from the head, and "The catch-up runs on the accepted
+ * prefix": the draft context re-runs the block on the accepted rows only).
+ * The drafter's KV holds kv_len[b] rows (positions 0..kv_len[b]-1).
+ *   catch-up: rows j < n_cu[b] (0 <= n_cu[b] <= M) consume cu_tok[b, j] with
+ *             the target's hidden state cu_h[b, j] and write their key and
+ *             value at position kv_len[b] + j;
+ *   drafts:   step k consumes tok_k (last_tok[b] for k = 0, then the previous
+ *             draft, or force_tok[b, k-1] when given) with h_k (h_prev[b], the
+ *             target's, for k = 0; the previous step's block output after) at
+ *             position kv_len[b] + n_cu[b] + k, writes its key and value there
+ *             and drafts argmax z (lowest index on ties).
+ * Outputs: drafts [B, N]; optional h_last [B, d] (the last step's block
+ * output), logits [B, N, V], margin [B, N] (top-1 minus top-2 logit), conf
+ * [B, N] (orc_top1_prob).  The rows written beyond the accepted ones (steps
+ * k >= 1) are the drafter's own guesses; the next call's catch-up overwrites
+ * the ones that get accepted. */
+int orc_nextn_draft(const orc_model *m, const void *const *t, const orc_view *dkv, int B, int N,
+                    const int32_t *kv_len, int M, const int32_t *n_cu, const int32_t *cu_tok, const float *cu_h,
+                    const int32_t *last_tok, const float *h_prev, const int32_t *force_tok, int32_t *drafts,
+                    double *h_last, double *logits, double *margin, double *conf) {
+    const int d = m->d_t, V = m->vocab;
+    double *h = malloc(sizeof(double) * d), *hn = malloc(sizeof(double) * d), *z = malloc(sizeof(double) * V);
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        const int nc = n_cu ? n_cu[b] : 0;
+        if (nc < 0 || nc > M || kv_len[b] < 0 || (int64_t)kv_len[b] + nc + N > dkv->cap) { rc = -1; break; }
+        for (int j = 0; j < nc && rc == 0; ++j) {
+            for (int c = 0; c < d; ++c) h[c] = (double)cu_h[((size_t)b * M + j) * d + c];
+            rc = nextn_row(m, t, dkv, b, cu_tok[(size_t)b * M + j], h, (int64_t)kv_len[b] + j, 0, NULL, NULL);
+        }
+        for (int c = 0; c < d; ++c) h[c] = (double)h_prev[(size_t)b * d + c];
+        int32_t tok = last_tok[b];
+        for (int k = 0; k < N && rc == 0; ++k) {
+            rc = nextn_row(m, t, dkv, b, tok, h, (int64_t)kv_len[b] + nc + k, 1, hn, z);
+            if (rc) break;
+            const int32_t pick = (int32_t)orc_argmax_f64(z, V);
+            double second = -INFINITY;
+            for (int v = 0; v < V; ++v) if (v != pick && z[v] > second) second = z[v];
+            if (margin) margin[(size_t)b * N + k] = z[pick] - second;
+            if (conf) conf[(size_t)b * N + k] = orc_top1_prob(z, V);
+            if (logits) memcpy(logits + ((size_t)b * N + k) * V, z, sizeof(double) * (size_t)V);
+            drafts[(size_t)b * N + k] = pick;
+            tok = force_tok ? force_tok[(size_t)b * N + k] : pick;
+            double *sw = h; h = hn; hn = sw;
+        }
+        if (h_last && rc == 0) memcpy(h_last + (size_t)b * d, h, sizeof(double) * d);
+    }
+    free(h); free(hn); free(z);
     return rc;
 }
 

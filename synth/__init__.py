@@ -11,7 +11,9 @@ MTP -- Multi-Token Prediction speculative decoding", sections 3-5): a token
 embedding table shared with the target, a pre-projection of the concatenated
 [token embedding; target hidden state], L assistant blocks that cross-attend into
 the target's last full-attention and last sliding-window KV layers, a
-post-projection back to the backbone width and the tied LM head.
+post-projection back to the backbone width and the tied LM head.  The dense
+NextN drafter ("MTP decoding (--mtp)", "Requirements") is one block at the
+backbone width with its own KV, fed through eh_proj, and the shared head.
 
 Conventions
 -----------
@@ -335,6 +337,7 @@ WORKLOADS = {
     4: "verify-sample-b32-n3-v248320",
     5: "edge-centroid-bf16-b1-n3-ctx4096",
     6: "gemma-assistant-q8-b1-n3-ctx8192",
+    7: "nextn-qwen-dense-bf16-b1-n3-kv4096-catchup2",
 }
 
 
@@ -389,6 +392,145 @@ def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None
     # workload 6 quantises that model's projections (the same fp32 draws)
     model_seed = workload_seed(1) if cfg_id in (1, 2, 3, 6) else seed
     return make_draft_workload(name, m, views, B, N, kv, seed, hist_len=64, model_seed=model_seed)
+
+
+# ----------------------------------------------------------------------------
+# the dense NextN drafter ("MTP decoding (--mtp)", "Requirements"; "Fused
+# NextN draft graph", "The two MTP lanes": its own block and its own KV)
+# ----------------------------------------------------------------------------
+
+NEXTN_TENSORS = ("tok_embd", "enorm", "hnorm", "eh_proj", "head_norm", "attn_norm", "w_qkv", "q_norm",
+                 "k_norm", "w_o", "ffn_norm", "w_gate", "w_up", "w_down")
+
+
+@dataclasses.dataclass
+class NextnSpec:
+    """A dense NextN drafter: one attention + SwiGLU block at the backbone width
+    d with its own KV, fed [enorm(embedding); hnorm(hidden state)] through
+    eh_proj, and the shared head (the tied table after head_norm)."""
+    d: int
+    n_q_heads: int
+    head_dim: int
+    n_kv_heads: int
+    d_ff: int
+    vocab: int
+    dtype: str = "bf16"
+    rms_eps: float = 1e-6
+    logit_softcap: float = 0.0
+    rope_theta: float = 1e7
+
+    # the shapes the oracle's model record shares with the assistant
+    @property
+    def d_t(self) -> int:
+        return self.d
+
+    @property
+    def d_a(self) -> int:
+        return self.d
+
+    n_blocks = 1
+    n_centroids = 0
+    centroid_top_k = 0
+    wquant = "none"
+
+    @property
+    def emb_scale(self) -> float:
+        return 1.0
+
+    @property
+    def attn_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def qkv_rows(self) -> int:
+        return (self.n_q_heads + 2 * self.n_kv_heads) * self.head_dim
+
+    def params(self) -> int:
+        d, F, hq = self.d, self.d_ff, self.n_q_heads * self.head_dim
+        return self.vocab * d + 2 * d * d + self.qkv_rows * d + d * hq + 3 * F * d
+
+
+@dataclasses.dataclass
+class NextnWorkload:
+    name: str
+    model: NextnSpec
+    B: int
+    N: int
+    M: int               # catch-up rows a sequence may bring (the width of cu_tok / cu_h)
+    weights: dict        # NEXTN_TENSORS -> array
+    dkv: dict            # the drafter's KV: k, v [B, Hkv, cap, hd], cap, rope_theta
+    kv_len: np.ndarray   # int32 [B]: rows already in the drafter's KV
+    n_cu: np.ndarray     # int32 [B]: catch-up rows of this call, 0..M
+    cu_tok: np.ndarray   # int32 [B, M]: their tokens (rows j < n_cu[b] used)
+    cu_h: np.ndarray     # float32 [B, M, d]: the target's hidden states paired with them
+    last_tok: np.ndarray  # int32 [B]: the token the first draft step consumes
+    h_prev: np.ndarray   # float32 [B, d]: the target's hidden state paired with it
+
+    def weight_bytes(self) -> int:
+        return sum(int(a.nbytes) for a in self.weights.values())
+
+
+def make_nextn_weights(m: NextnSpec, seed: int, std: float = 0.02) -> dict:
+    d, F, hq = m.d, m.d_ff, m.n_q_heads * m.head_dim
+    shapes = {"tok_embd": (m.vocab, d), "eh_proj": (d, 2 * d), "w_qkv": (m.qkv_rows, d), "w_o": (d, hq),
+              "w_gate": (F, d), "w_up": (F, d), "w_down": (d, F)}
+    norms = {"enorm": d, "hnorm": d, "head_norm": d, "attn_norm": d, "ffn_norm": d,
+             "q_norm": m.head_dim, "k_norm": m.head_dim}
+    w = {}
+    for name, shp in shapes.items():
+        w[name] = _as_dtype(normal(seed, "nextn." + name, shp, std=std), m.dtype)
+    for name, n in norms.items():
+        w[name] = normal(seed, "nextn." + name, (n,), std=std, mean=1.0)
+    return w
+
+
+def make_nextn_workload(name: str, m: NextnSpec, B: int, N: int, M: int, kv_len, n_cu, seed: int,
+                        cap: int | None = None, model_seed: int | None = None) -> NextnWorkload:
+    """The drafter's KV holds kv_len[b] rows of N(0, 1) keys and values (what
+    earlier calls wrote); every slot from kv_len[b] on is NaN, so a read of a
+    row this call has not written shows up as a NaN."""
+    kv_len = np.asarray(kv_len, dtype=np.int32).reshape(B)
+    n_cu = np.asarray(n_cu, dtype=np.int32).reshape(B)
+    need = int((kv_len + n_cu).max()) + N
+    cap = need if cap is None else cap
+    if need > cap or n_cu.min() < 0 or n_cu.max() > M:
+        raise ValueError("drafter KV capacity or catch-up rows out of range")
+    key = ("nextn", dataclasses.astuple(m), seed if model_seed is None else model_seed)
+    if key not in _WEIGHT_CACHE:
+        _WEIGHT_CACHE.clear()
+        _WEIGHT_CACHE[key] = make_nextn_weights(m, seed if model_seed is None else model_seed)
+    weights = _WEIGHT_CACHE[key]
+    shape = (B, m.n_kv_heads, cap, m.head_dim)
+    dkv = {}
+    for which in ("k", "v"):
+        arr = _as_dtype(normal(seed, "nextn.dkv." + which, shape), m.dtype)
+        for b in range(B):
+            arr[b][:, int(kv_len[b]):, :] = BF16_NAN if m.dtype == "bf16" else np.nan
+        dkv[which] = arr
+    dkv.update(cap=cap, rope_theta=m.rope_theta)
+    cu_tok = uniform_int(seed, "nextn.cu_tok", (B, max(M, 1)), 0, m.vocab)[:, :M].copy()
+    cu_h = normal(seed, "nextn.cu_h", (B, max(M, 1), m.d))[:, :M].copy()
+    last_tok = uniform_int(seed, "nextn.last_tok", (B,), 0, m.vocab)
+    h_prev = normal(seed, "nextn.h_prev", (B, m.d))
+    return NextnWorkload(name, m, B, N, M, weights, dkv, kv_len, n_cu, cu_tok, cu_h, last_tok, h_prev)
+
+
+def _qwen_nextn() -> NextnSpec:
+    """A Qwen3.5-9B-shaped dense NextN block (synthetic sizes: the pages name
+    the model family and its tensors, not their dimensions): width 4096, 16
+    query heads x 256 against 4 KV heads, SwiGLU 12288, a 248320-token table."""
+    return NextnSpec(d=4096, n_q_heads=16, head_dim=256, n_kv_heads=4, d_ff=12288, vocab=248320, dtype="bf16")
+
+
+def make_nextn_inputs(cfg_id: int = 7, seed: int | None = None, B: int | None = None) -> NextnWorkload:
+    """Workload 7: the Qwen-shaped NextN drafter, batch 1, N = 3 drafts, 4096
+    rows already in its KV, two catch-up rows (the accepted drafts of the
+    previous window) before the drafts."""
+    if cfg_id != 7:
+        raise ValueError("workload 7 is the NextN drafter")
+    seed = workload_seed(cfg_id) if seed is None else seed
+    B = 1 if B is None else B
+    return make_nextn_workload(WORKLOADS[7], _qwen_nextn(), B, 3, 3, np.full(B, 4096), np.full(B, 2), seed)
 
 
 # ----------------------------------------------------------------------------
