@@ -1,7 +1,7 @@
 /*
  * mtp.h -- C ABI of the GB300 MTP speculative-decoding hot path.
  *
- * Four operations, all asynchronous on a caller-supplied CUDA stream:
+ * Five operations, all asynchronous on a caller-supplied CUDA stream:
  *
  *   mtp_draft_block    N chained draft steps of an MTP assistant head that
  *                      cross-attends into the target's KV cache, in ONE
@@ -12,6 +12,9 @@
  *   mtp_verify_sample  exact speculative sampling at temp > 0.
  *   mtp_sample_drafts  the draws of a sampling drafter from given draft
  *                      logits (the q the sampling verifier checks against).
+ *   mtp_nextn_draft    the dense NextN self-speculation drafter: its own
+ *                      block and its own KV, the catch-up on the accepted
+ *                      rows, then N chained draft steps, in ONE launch.
  *
  * Definitions are those of the pages this library implements:
  *   [G4] "Gemma 4 MTP -- Multi-Token Prediction speculative decoding":
@@ -74,6 +77,7 @@ enum { MTP_WQ_NONE = 0, MTP_WQ_Q8_0 = 1 };
 #define MTP_MAX_BATCH 64            /* sequences of one mtp_draft_block call */
 #define MTP_MAX_VERIFY_BATCH 65536  /* sequences of one verify or draw call */
 #define MTP_MAX_CENTROIDS 8192      /* centroids of a centroid-routed LM head */
+#define MTP_MAX_CATCHUP 16          /* catch-up rows per sequence of one mtp_nextn_draft call */
 
 /* Sizes and scalars of the assistant head ([G4] sec. 3-4).
  *   d_t        backbone (target) width: token embedding, h_prev, LM head input
@@ -128,6 +132,8 @@ typedef struct mtp_block_weights {
     int32_t pad_;
     /* MTP_WQ_Q8_0 only (NULL otherwise): block scales of w_q, w_o, w_gate, w_up, w_down */
     const uint16_t *w_q_scale, *w_o_scale, *w_gate_scale, *w_up_scale, *w_down_scale;
+    /* mtp_nextn_draft only (NULL otherwise): fp32 [head_dim] key norm, shared by all KV heads */
+    const void *k_norm;
 } mtp_block_weights;
 
 typedef struct mtp_weights {
@@ -248,6 +254,60 @@ int mtp_draft_block(const mtp_config *cfg, const mtp_weights *w,
                     int32_t *out_drafts, float *out_h_last, float *out_logits,
                     float *out_conf, void *ws, size_t ws_bytes, mtp_stream_t stream);
 
+/* The dense NextN drafter ([NX] "Requirements", "How it is wired", "The
+ * catch-up runs on the accepted prefix"; [FN] "The two MTP lanes": NextN runs
+ * its own block over its own KV).  One block at the backbone width d = d_t.
+ * The drafter's KV `dkv` holds kv_len[b] rows of sequence b, the row of
+ * position t in slot t (window 0, sink 0, kv_len[b] + n_cu[b] + N <= cap);
+ * this call WRITES rows kv_len[b] .. kv_len[b] + n_cu[b] + N - 1 of it.
+ * A row consumes a token t at position pos and a hidden state h:
+ *   x = w_pre [rmsnorm(tok_embd[t] * emb_scale; norm_e); rmsnorm(h; norm_h)]
+ *       (w_pre the eh_proj [d, 2d]; emb_scale 0 = the default 1)
+ *   a = rmsnorm(x; attn_norm);  [q; k; v] = w_q a  (w_q [(Hq + 2 Hkv) hd, d]:
+ *       query rows, then key rows, then value rows)
+ *   per KV head: key = rope(rmsnorm(k_g; k_norm), pos), value = v_g, both
+ *       stored at slot pos rounded to wdtype
+ * Catch-up rows stop there.  A draft step goes on:
+ *   per query head: q_h = rope(rmsnorm(q_h; q_norm), pos) attends (GQA,
+ *       scale attn_scale) to the rows [0, pos] of KV head h / (Hq / Hkv)
+ *   x += w_o o;  x += w_down(silu(w_gate n) * w_up n), n = rmsnorm(x; pre_ffn_norm)
+ *   h' = x (the next step's hidden state);  z = tok_embd rmsnorm(x; final_norm)
+ *       (final_norm the shared head's norm; optional softcap); draft = argmax z
+ *       (lowest index on ties)
+ * Rows of sequence b: catch-up row j < n_cu[b] consumes (cu_tok[b, j],
+ * cu_h[b, j]) at position kv_len[b] + j -- the accepted drafts with the
+ * target's hidden states at the positions before them; draft step k consumes
+ * (last_tok[b], h_prev[b]) for k = 0 -- the bonus token with the target's
+ * hidden state before it -- and (draft k-1, h' of step k-1) after, at
+ * position kv_len[b] + n_cu[b] + k.  The next call's kv_len is kv_len +
+ * n_cu + 1: the rows of steps k >= 1 are the drafter's own guesses, and the
+ * next call's catch-up rewrites the accepted ones (no rollback is needed).
+ * Arguments:
+ *   cfg        d_a == d_t, n_blocks == 1, n_centroids == 0, wquant NONE;
+ *              rope_theta comes from dkv
+ *   w          tok_embd, norm_e, norm_h, w_pre (eh_proj), final_norm (head
+ *              norm); blk[0]: attn_norm, w_q (fused), q_norm, k_norm, w_o,
+ *              pre_ffn_norm, w_gate, w_up, w_down (w_post, post_attn_norm,
+ *              post_ffn_norm, centroids and scales unused, may be NULL)
+ *   dkv        host pointer to one view (data on device, written)
+ *   kv_len [B] int32 >= 0;  n_cu [B] int32 in [0, M] (NULL: all 0)
+ *   cu_tok [B, M] int32, cu_h [B, M, d] fp32 (only rows j < n_cu[b] are read;
+ *              NULL when M == 0);  0 <= M <= MTP_MAX_CATCHUP
+ *   last_tok [B] int32;  h_prev [B, d] fp32
+ *   out_drafts [B, N] int32;  out_h_last [B, d] fp32 or NULL: h' of the last
+ *              step;  out_logits [B, N, vocab] fp32 or NULL;  out_conf [B, N]
+ *              fp32 or NULL (as for mtp_draft_block)
+ * Greedy only ([NX]: speculation there requires greedy decoding).  B <=
+ * MTP_MAX_BATCH, 1 <= N <= 16.  Host-checked arguments return MTP_ERR_ARG /
+ * MTP_ERR_UNSUPPORTED; a kv_len, n_cu or token out of range sets the status
+ * word to MTP_ERR_ARG and the kernel returns before writing anything.  One
+ * cooperative launch (plus a 256-byte workspace memset). */
+int mtp_nextn_draft(const mtp_config *cfg, const mtp_weights *w, const mtp_kv_view *dkv,
+                    const int32_t *kv_len, int B, int N,
+                    const int32_t *n_cu, const int32_t *cu_tok, const float *cu_h, int M,
+                    const int32_t *last_tok, const float *h_prev,
+                    int32_t *out_drafts, float *out_h_last, float *out_logits, float *out_conf,
+                    void *ws, size_t ws_bytes, mtp_stream_t stream);
 /* Greedy verify ([NX] How it is wired).  B <= MTP_MAX_VERIFY_BATCH.  logits [B, 1+N, V] in ldtype (row i
  * is the target's distribution after consuming the last token and drafts
  * 0..i-1); t_i = argmax of row i (lowest index on ties, NaN never wins, an

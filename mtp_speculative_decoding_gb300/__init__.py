@@ -30,11 +30,12 @@ MTP_MAX_BLOCKS = 8
 MTP_MAX_VIEWS = 4
 MTP_MAX_BATCH = 64
 MTP_MAX_VERIFY_BATCH = 65536
+MTP_MAX_CATCHUP = 16
 
 # every entry point include/mtp.h declares
 EXPORTS = ("mtp_workspace_size", "mtp_draft_block", "mtp_verify_greedy", "mtp_verify_sample",
            "mtp_sample_drafts", "mtp_quantize_q8_0", "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout",
-           "mtp_verify_greedy_noalloc")
+           "mtp_verify_greedy_noalloc", "mtp_nextn_draft")
 
 
 class MTPError(RuntimeError):
@@ -56,7 +57,8 @@ class BlockWeights(C.Structure):
                 ("post_attn_norm", C.c_void_p), ("pre_ffn_norm", C.c_void_p), ("w_gate", C.c_void_p),
                 ("w_up", C.c_void_p), ("w_down", C.c_void_p), ("post_ffn_norm", C.c_void_p),
                 ("kv_view", C.c_int32), ("pad_", C.c_int32), ("w_q_scale", C.c_void_p), ("w_o_scale", C.c_void_p),
-                ("w_gate_scale", C.c_void_p), ("w_up_scale", C.c_void_p), ("w_down_scale", C.c_void_p)]
+                ("w_gate_scale", C.c_void_p), ("w_up_scale", C.c_void_p), ("w_down_scale", C.c_void_p),
+                ("k_norm", C.c_void_p)]
 
 
 class Weights(C.Structure):
@@ -110,6 +112,8 @@ def lib():
             L.mtp_sample_drafts.restype = I
             L.mtp_verify_greedy_noalloc.argtypes = [P, I, I, I, I, P, P, P, P]
             L.mtp_verify_greedy_noalloc.restype = I
+            L.mtp_nextn_draft.argtypes = [P, P, P, P, I, I, P, P, P, I, P, P, P, P, P, P, P, Z, P]
+            L.mtp_nextn_draft.restype = I
             L.mtp_quantize_q8_0.argtypes = [P, C.c_int64, C.c_int64, P, P]
             L.mtp_quantize_q8_0.restype = I
             _lib = L
@@ -251,6 +255,46 @@ def draft_block(cfg: Config, weights: Weights, views, kv_len, last_tok, h_prev, 
                                seed, offset, _ptr(hist), H, _ptr(out_drafts), _ptr(out_h_last),
                                _ptr(out_logits), _ptr(out_conf), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "mtp_draft_block")
+
+
+# ----------------------------------------------------------------------------
+# the dense NextN drafter
+# ----------------------------------------------------------------------------
+
+# NextN tensor names -> the mtp_weights / mtp_block_weights fields they fill
+NEXTN_FIELDS = {"tok_embd": "tok_embd", "enorm": "norm_e", "hnorm": "norm_h", "eh_proj": "w_pre",
+                "head_norm": "final_norm"}
+NEXTN_BLOCK_FIELDS = {"attn_norm": "attn_norm", "w_qkv": "w_q", "q_norm": "q_norm", "k_norm": "k_norm",
+                      "w_o": "w_o", "ffn_norm": "pre_ffn_norm", "w_gate": "w_gate", "w_up": "w_up",
+                      "w_down": "w_down"}
+
+
+def make_nextn_weights(tensors: dict) -> Weights:
+    """Pack the NextN drafter's device tensors (keys: NEXTN_FIELDS and
+    NEXTN_BLOCK_FIELDS) into mtp_weights: eh_proj is w_pre, head_norm is
+    final_norm, the fused query / key / value projection is blk[0].w_q."""
+    w = Weights()
+    for n, f in NEXTN_FIELDS.items():
+        setattr(w, f, tensors[n].data_ptr())
+    for n, f in NEXTN_BLOCK_FIELDS.items():
+        setattr(w.blk[0], f, tensors[n].data_ptr())
+    return w
+
+
+def nextn_draft(cfg: Config, weights: Weights, dkv: KVView, kv_len, last_tok, h_prev, out_drafts, ws,
+                n_cu=None, cu_tok=None, cu_h=None, out_h_last=None, out_logits=None, out_conf=None,
+                stream=None) -> None:
+    """Launch mtp_nextn_draft on the current stream (asynchronous): the
+    catch-up rows (cu_tok [B, M] int32, cu_h [B, M, d] fp32, n_cu [B] int32),
+    then out_drafts.shape[1] draft steps; writes the drafter's KV in dkv."""
+    _require_cuda(kv_len, last_tok, h_prev, out_drafts, ws, n_cu, cu_tok, cu_h, out_h_last, out_logits, out_conf)
+    B, N = out_drafts.shape
+    M = 0 if cu_tok is None else int(cu_tok.shape[1])
+    rc = lib().mtp_nextn_draft(C.byref(cfg), C.byref(weights), C.byref(dkv), _ptr(kv_len), B, N, _ptr(n_cu),
+                               _ptr(cu_tok), _ptr(cu_h), M, _ptr(last_tok), _ptr(h_prev), _ptr(out_drafts),
+                               _ptr(out_h_last), _ptr(out_logits), _ptr(out_conf), _ptr(ws), ws.numel(),
+                               _stream(stream))
+    _check(rc, "mtp_nextn_draft")
 
 
 # ----------------------------------------------------------------------------

@@ -74,7 +74,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                 if verbose and err:
                     print(f"--- {name}\n{err}")
     objs = [os.path.join(BUILD, name + ".o") for name, _, _ in UNITS]
-    if force or jobs or not os.path.exists(LIB):
+    # relink also when an object is newer than the library (a link that failed after its compiles)
+    if force or jobs or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
         cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", LIB + ".tmp"] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -53,7 +53,7 @@ size_t cent_smem(const mtp_config* c) {
 }
 int pad16(int B) { return (B + 15) & ~15; }
 
-size_t draft_smem(const mtp_config* c, int B, int act_smem);
+size_t draft_smem(const mtp_config* c, int B, int act_smem, bool cc = false);
 constexpr size_t kSmemLimit = 220 * 1024;
 
 // Projections on tensor cores: eligible for the head path, activations
@@ -93,7 +93,8 @@ int draft_grid() {
 }
 
 struct DraftLayout {
-    size_t att_cnt, SROW, amax, XB, XM, QR, OB, YB, MB, Y2, HN, CL, PART, CONF, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ZB, SBUF, ACT, end;
+    size_t att_cnt, SROW, amax, XB, XM, QR, OB, YB, MB, Y2, HN, HX, CL, PART, CONF, ROPE, ROPEQ, XH, XL, XA, XAL, PB, ZB, SBUF,
+        ACT, end;
     int kmax;
 };
 
@@ -121,12 +122,14 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     L.amax = off;    off = al256(off + (size_t)N * B * sizeof(unsigned long long));
     L.XB = off;      off = al256(off + (size_t)B * c->d_a * f);
     L.XM = off;      off = al256(off + (size_t)B * c->d_a * f);
-    L.QR = off;      off = al256(off + (size_t)B * c->n_q_heads * c->head_dim * f);
+    // query rows, and (NextN's fused projection) its key and value rows
+    L.QR = off;      off = al256(off + (size_t)B * (c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim * f);
     L.OB = off;      off = al256(off + (size_t)B * c->n_q_heads * c->head_dim * f);
     L.YB = off;      off = al256(off + (size_t)B * c->d_a * f);
     L.MB = off;      off = al256(off + (size_t)B * c->d_ff * f);
     L.Y2 = off;      off = al256(off + (size_t)B * c->d_a * f);
     L.HN = off;      off = al256(off + (size_t)B * c->d_t * f);
+    L.HX = off;      off = al256(off + (size_t)B * c->d_t * f);   // NextN: the block output chain
     L.CL = off;      off = al256(off + (size_t)B * c->n_centroids * f);
     const size_t items = 2 * (size_t)kMaxGrid + (size_t)B * c->n_kv_heads;
     L.PART = off;    off = al256(off + items * attn_psz(grp, c->head_dim) * f);
@@ -219,10 +222,11 @@ size_t draft_smem_act(const mtp_config* c, int B, int act_smem) {
            (act_smem ? (size_t)B * kmax : kmax) * sizeof(float) + 2 * gmax * sizeof(float);   // + the gain stage
 }
 
-size_t draft_smem(const mtp_config* c, int B, int act_smem) {
+// cc: the CUDA-core kernel variant regardless of the batch (NextN)
+size_t draft_smem(const mtp_config* c, int B, int act_smem, bool cc) {
     const size_t wb = c->wdtype == MTP_DTYPE_BF16 ? 2 : 4;
     const size_t hd = c->head_dim, grp = c->n_q_heads / c->n_kv_heads;
-    const int nst = tc_head_eligible(c, B) ? kAttnStagesTc : kAttnStages;   // the kernel variant's ring depth
+    const int nst = !cc && tc_head_eligible(c, B) ? kAttnStagesTc : kAttnStages;   // the kernel variant's ring depth
     const size_t attn = attn_smem((int)hd, (int)wb, (int)grp, nst);
     const size_t act = draft_smem_act(c, B, act_smem);
     return attn > act ? attn : act;
@@ -364,13 +368,38 @@ size_t mtp_workspace_size(const mtp_config* cfg, int B, int N, int V) {
     return need;
 }
 
-int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* views, int n_views,
-                    const int32_t* kv_len, int B, int N, const int32_t* last_tok, const float* h_prev,
-                    const mtp_sample_params* sp, uint64_t seed, uint64_t offset, const int32_t* hist, int H,
-                    int32_t* out_drafts, float* out_h_last, float* out_logits, float* out_conf, void* ws,
-                    size_t ws_bytes, mtp_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// NextN's extra inputs (null for the assistant)
+struct NextnIn {
+    const int32_t* n_cu;
+    const int32_t* cu_tok;
+    const float* cu_h;
+    int M;
+};
+
+// mtp_draft_block, and mtp_nextn_draft when nx != null: the checks, the
+// parameter block and the launch of the persistent draft kernel
+int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* views, int n_views,
+               const int32_t* kv_len, int B, int N, const int32_t* last_tok, const float* h_prev,
+               const mtp_sample_params* sp, uint64_t seed, uint64_t offset, const int32_t* hist, int H,
+               int32_t* out_drafts, float* out_h_last, float* out_logits, float* out_conf, void* ws,
+               size_t ws_bytes, mtp_stream_t stream, const NextnIn* nx) {
     int rc = check_config(cfg);
     if (rc != MTP_OK) return rc;
+    if (nx) {
+        if (cfg->d_a != cfg->d_t) return MTP_ERR_ARG;
+        if (cfg->n_blocks != 1 || cfg->n_centroids != 0 || cfg->wquant != MTP_WQ_NONE) return MTP_ERR_UNSUPPORTED;
+        if (nx->M < 0 || nx->M > MTP_MAX_CATCHUP) return MTP_ERR_ARG;
+        if (nx->M > 0 && (!nx->cu_tok || !nx->cu_h)) return MTP_ERR_ARG;
+        if ((reinterpret_cast<uintptr_t>(nx->cu_h) & 3) || (reinterpret_cast<uintptr_t>(nx->cu_tok) & 3) ||
+            (reinterpret_cast<uintptr_t>(nx->n_cu) & 3))
+            return MTP_ERR_ARG;
+        if (n_views != 1 || !views || views[0].window != 0 || views[0].sink != 0) return MTP_ERR_ARG;
+        if (sp) return MTP_ERR_ARG;
+    }
     if (!w || !views || n_views < 1 || n_views > MTP_MAX_VIEWS) return MTP_ERR_ARG;
     if (B < 1 || B > MTP_MAX_BATCH || N < 1 || N > 16) return MTP_ERR_ARG;
     if (!kv_len || !last_tok || !h_prev || !out_drafts) return MTP_ERR_ARG;
@@ -384,7 +413,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     const bool bf = cfg->wdtype == MTP_DTYPE_BF16;
     const int esz = bf ? 2 : 4;
     // weights
-    const void* mats[] = {w->tok_embd, w->w_pre, w->w_post};
+    const void* mats[] = {w->tok_embd, w->w_pre, nx ? w->tok_embd : w->w_post};   // NextN has no post-projection
     for (const void* m : mats) if (!m || !aligned16(m)) return MTP_ERR_ARG;
     if (cfg->wquant == MTP_WQ_Q8_0) {
         const uint16_t* sc[] = {w->w_pre_scale, w->w_post_scale};
@@ -404,8 +433,9 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         const mtp_block_weights& b = w->blk[l];
         const void* bm[] = {b.w_q, b.w_o, b.w_gate, b.w_up, b.w_down};
         for (const void* m : bm) if (!m || !aligned16(m)) return MTP_ERR_ARG;
-        if (!b.attn_norm || !b.q_norm || !b.post_attn_norm || !b.pre_ffn_norm || !b.post_ffn_norm) return MTP_ERR_ARG;
-        if (b.kv_view < 0 || b.kv_view >= n_views) return MTP_ERR_ARG;
+        if (!b.attn_norm || !b.q_norm || !b.pre_ffn_norm) return MTP_ERR_ARG;
+        if (nx ? !b.k_norm : (!b.post_attn_norm || !b.post_ffn_norm)) return MTP_ERR_ARG;
+        if (!nx && (b.kv_view < 0 || b.kv_view >= n_views)) return MTP_ERR_ARG;
     }
     for (int v = 0; v < n_views; ++v) {
         const mtp_kv_view& kv = views[v];
@@ -422,11 +452,11 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     const int sms = num_sms();
     if (sms <= 0) return MTP_ERR_CUDA;
 
-    size_t smem = draft_smem(cfg, B, 1);
+    size_t smem = draft_smem(cfg, B, 1, nx != nullptr);
     int act_smem = 1;
     if (smem > kSmemLimit) {
         act_smem = 0;
-        smem = draft_smem(cfg, B, 0);
+        smem = draft_smem(cfg, B, 0, nx != nullptr);
         if (smem > kSmemLimit) return MTP_ERR_UNSUPPORTED;
     }
     const int grid = draft_grid();
@@ -441,7 +471,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         }
     }
     // batch: LM head on tensor cores, operand ring at offset 0 (1024-aligned)
-    const bool tc = tc_head_eligible(cfg, B);
+    const bool tc = !nx && tc_head_eligible(cfg, B);   // NextN runs the CUDA-core variant
     int tc_stages = 0, tc_cols = 0, th_stages = 0;
     if (tc) {
         const size_t sbytes = (size_t)kTcTileM * 128 + 2 * (size_t)pad16(B) * 128;
@@ -474,7 +504,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     p.eps = cfg->rms_eps; p.softcap = cfg->logit_softcap;
     // 0 selects the defaults the header documents: 1/sqrt(head_dim), sqrt(d_t)
     p.attn_scale = cfg->attn_scale > 0.f ? cfg->attn_scale : (float)(1.0 / sqrt((double)cfg->head_dim));
-    p.emb_scale = cfg->emb_scale > 0.f ? cfg->emb_scale : (float)sqrt((double)cfg->d_t);
+    p.emb_scale = cfg->emb_scale > 0.f ? cfg->emb_scale : nx ? 1.f : (float)sqrt((double)cfg->d_t);
     p.tok_embd = w->tok_embd;
     p.norm_e = static_cast<const float*>(w->norm_e);
     p.norm_h = static_cast<const float*>(w->norm_h);
@@ -498,7 +528,8 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         d.post_attn_norm = static_cast<const float*>(b.post_attn_norm);
         d.pre_ffn_norm = static_cast<const float*>(b.pre_ffn_norm);
         d.post_ffn_norm = static_cast<const float*>(b.post_ffn_norm);
-        d.view = b.kv_view;
+        d.k_norm = nx ? static_cast<const float*>(b.k_norm) : nullptr;
+        d.view = nx ? 0 : b.kv_view;
     }
     for (int v = 0; v < n_views; ++v) {
         KView& d = p.views[v];
@@ -509,6 +540,14 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
         d.ring_magic = mod_magic((unsigned int)(d.cap - (d.window > 0 ? d.sink : 0)));
     }
     p.kv_len = kv_len; p.last_tok = last_tok; p.h_prev = h_prev;
+    p.QS = (nx ? cfg->n_q_heads + 2 * cfg->n_kv_heads : cfg->n_q_heads) * cfg->head_dim;
+    if (nx) {
+        p.nextn = 1;
+        p.M = nx->M;
+        p.n_cu = nx->M > 0 ? nx->n_cu : nullptr;
+        p.cu_tok = nx->cu_tok;
+        p.cu_h = nx->cu_h;
+    }
     p.out_drafts = out_drafts; p.out_h_last = out_h_last; p.out_logits = out_logits; p.out_conf = out_conf;
     p.hdr = reinterpret_cast<WsHeader*>(base);
     p.att_cnt = reinterpret_cast<unsigned int*>(base + L.att_cnt);
@@ -521,6 +560,7 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
     p.MB = reinterpret_cast<float*>(base + L.MB);
     p.Y2 = reinterpret_cast<float*>(base + L.Y2);
     p.HN = reinterpret_cast<float*>(base + L.HN);
+    p.HX = reinterpret_cast<float*>(base + L.HX);
     p.PART = reinterpret_cast<float*>(base + L.PART);
     p.CONF = reinterpret_cast<float2*>(base + L.CONF);
     p.ROPE = reinterpret_cast<double*>(base + L.ROPE);
@@ -590,6 +630,29 @@ int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_vi
                     : q8 ? launch_draft_q8(p, grid, smem, s)
                                 : launch_draft_bf16_cc(p, grid, smem, s);
     return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mtp_draft_block(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* views, int n_views,
+                    const int32_t* kv_len, int B, int N, const int32_t* last_tok, const float* h_prev,
+                    const mtp_sample_params* sp, uint64_t seed, uint64_t offset, const int32_t* hist, int H,
+                    int32_t* out_drafts, float* out_h_last, float* out_logits, float* out_conf, void* ws,
+                    size_t ws_bytes, mtp_stream_t stream) {
+    return draft_impl(cfg, w, views, n_views, kv_len, B, N, last_tok, h_prev, sp, seed, offset, hist, H, out_drafts,
+                      out_h_last, out_logits, out_conf, ws, ws_bytes, stream, nullptr);
+}
+
+int mtp_nextn_draft(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* dkv, const int32_t* kv_len, int B,
+                    int N, const int32_t* n_cu, const int32_t* cu_tok, const float* cu_h, int M,
+                    const int32_t* last_tok, const float* h_prev, int32_t* out_drafts, float* out_h_last,
+                    float* out_logits, float* out_conf, void* ws, size_t ws_bytes, mtp_stream_t stream) {
+    if (!dkv) return MTP_ERR_ARG;
+    const NextnIn nx{n_cu, cu_tok, cu_h, M};
+    return draft_impl(cfg, w, dkv, 1, kv_len, B, N, last_tok, h_prev, nullptr, 0, 0, nullptr, 0, out_drafts,
+                      out_h_last, out_logits, out_conf, ws, ws_bytes, stream, &nx);
 }
 
 int mtp_verify_greedy(const void* logits, int ldtype, int B, int N, int V, const int32_t* drafts, int32_t* out_tokens,

@@ -83,6 +83,7 @@ struct BlkW {
     const void *w_q, *w_o, *w_gate, *w_up, *w_down;
     const uint16_t *s_q, *s_o, *s_gate, *s_up, *s_down;   // Q8_0 block scales (binary16) or null
     const float *attn_norm, *q_norm, *post_attn_norm, *pre_ffn_norm, *post_ffn_norm;
+    const float* k_norm;   // NextN: the key norm (null for the assistant)
     int view;
     int pad_;
 };
@@ -152,6 +153,16 @@ struct DraftParams {
     const void* cent;
     const int32_t* cord;
     float* CL;
+    // dense NextN drafter (nextn = 1): one block with a fused query / key /
+    // value projection into QR, its own KV (views[0], written by the kernel),
+    // catch-up rows before the draft steps, the block output as the chain
+    int QS;                      // floats per sequence in QR: Hq hd, or (Hq + 2 Hkv) hd for NextN
+    int nextn;
+    int M;                       // catch-up rows per sequence at most
+    const int32_t* n_cu;         // [B] catch-up rows of each sequence, or null (none)
+    const int32_t* cu_tok;       // [B, M] their tokens
+    const float* cu_h;           // [B, M, d_t] the hidden states paired with them
+    float* HX;                   // [B, d_t] the block output: the next step's hidden state
 };
 
 cudaError_t launch_draft_f32(const DraftParams& p, int grid, size_t smem, cudaStream_t s);

@@ -16,6 +16,17 @@
 //   POST    h = W_post rms(x_m + rms(y2))
 //   HEAD    z = E h (softcap), packed-key argmax folded across the grid
 //
+// The dense NextN drafter ("MTP decoding (--mtp)", "Requirements"; its own
+// block and KV) runs through the same kernel (nextn = 1, one block at the
+// backbone width): PRE is eh_proj; Q is the fused query / key / value
+// projection, after which each (sequence, KV head) key is normed, rotated and
+// stored with its value in the drafter's KV before the causal attention
+// reads it; FFN1 adds the attention output without a norm and gates with
+// SiLU; POST is no projection: h' = x_m + y2 (the next step's hidden state)
+// and the head's input is head_norm(h').  Catch-up rows (the accepted drafts
+// with the target's hidden states) run as iterations k < 0 of PRE and the
+// key / value rows of Q only.
+//
 // Norms and residual updates run redundantly in every CTA's phase prologue
 // (each CTA needs the whole input vector of its GEMV anyway), so they cost no
 // barrier.  Below eight sequences the weights stream through 16-byte
@@ -332,16 +343,20 @@ __device__ __forceinline__ float gelu_tanh(float x) {
     return 0.5f * x * (1.f + tanhf(k0 * (x + 0.044715f * x * x * x)));
 }
 
-// m[b * ldo + r] = gelu_tanh(gate) * up
+__device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
+
+// m[b * ldo + r] = gelu_tanh(gate) * up, or (NextN) silu(gate) * up
 struct GegluEpi {
     float* out;
     int ldo;
+    int swiglu;
     template <int NB>
     __device__ __forceinline__ void apply(int r, int b0, int nb, const float (&g)[NB], const float (&u)[NB]) {
         const int lane = threadIdx.x & 31;
 #pragma unroll
         for (int j = 0; j < NB; ++j)
-            if (lane == j && b0 + j < nb) out[(long long)(b0 + j) * ldo + r] = gelu_tanh(g[j]) * u[j];
+            if (lane == j && b0 + j < nb)
+                out[(long long)(b0 + j) * ldo + r] = (swiglu ? silu(g[j]) : gelu_tanh(g[j])) * u[j];
     }
 };
 
@@ -458,6 +473,20 @@ __device__ __forceinline__ int step_token(const DraftParams& p, int b, int k) {
     if (k == 0) return p.last_tok[b];
     const uint32_t t = unpack_index(__ldcg(p.amax + (long long)(k - 1) * p.B + b));
     return t < (uint32_t)p.V ? (int)t : 0;   // every slot holds a row index after its HEAD phase
+}
+
+// NextN: the catch-up row of sequence b at iteration k < 0 (rows are
+// right-aligned: iteration -1 takes the last), negative if b has none there
+__device__ __forceinline__ int catchup_row(const DraftParams& p, int b, int k) {
+    return (p.n_cu ? __ldg(p.n_cu + b) : 0) + k;
+}
+// Position of sequence b's row at iteration k: the query position
+// kv_len + k of the assistant's draft steps; for NextN the row index in its
+// own KV, kv_len + j for catch-up row j, kv_len + n_cu + k for draft step k
+__device__ __forceinline__ int row_pos(const DraftParams& p, const int* kv, int b, int k) {
+    if (!p.nextn) return kv[b] + k;
+    const int j = catchup_row(p, b, k);
+    return kv[b] + (j > 0 ? j : 0);
 }
 
 // float4 at q summed over S copies st floats apart, in order
@@ -586,9 +615,19 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
     case PH_PRE: {
         const int n = p.d_t;
         constexpr int EPC = 16 / (int)sizeof(WT);
-        const int tok = step_token(p, b, k);
+        int tok;
+        const float* h;
+        if (k < 0) {
+            // NextN catch-up iteration k: row n_cu + k of sequence b, or (none
+            // at this iteration) the first step's inputs, computed and unused
+            const int j = catchup_row(p, b, k);
+            tok = j >= 0 ? __ldg(p.cu_tok + (long long)b * p.M + j) : p.last_tok[b];
+            h = j >= 0 ? p.cu_h + ((long long)b * p.M + j) * n : p.h_prev + (long long)b * n;
+        } else {
+            tok = step_token(p, b, k);
+            h = k == 0 ? p.h_prev + (long long)b * n : (p.nextn ? p.HX : p.HN) + (long long)b * n;
+        }
         const uint4* er = reinterpret_cast<const uint4*>(reinterpret_cast<const WT*>(p.tok_embd) + (long long)tok * n);
-        const float* h = k == 0 ? p.h_prev + (long long)b * n : p.HN + (long long)b * n;
 #pragma unroll 2
         for (int j = threadIdx.x; j < n / EPC; j += blockDim.x) {   // the embedding row, 16-byte vectors
             const uint4 w = ld_stream16(er + j);
@@ -653,11 +692,11 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             if (!(TC && p.tc_proj)) dst[i] = __ldcg(p.YB + (long long)b * n + i);
             tmp[i] = __ldcg(p.XB + (long long)b * n + i);
-            gs[i] = __ldg(g1 + i);
+            if (!p.nextn) gs[i] = __ldg(g1 + i);
             gs[n + i] = __ldg(g2 + i);
         }
         __syncthreads();
-        rms_into_s(dst, gs, n, p.eps, dst, red);
+        if (!p.nextn) rms_into_s(dst, gs, n, p.eps, dst, red);   // NextN: the attention output added as it is
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
             const float x = tmp[i] + dst[i];
             tmp[i] = x;
@@ -1180,7 +1219,8 @@ __device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsi
                 if (warp < grp) {
                     constexpr int NQ = (HD / 8 + 31) / 32;   // float4 pairs per lane
                     // the query projection, or its split partials summed in order
-                    const float* qraw = (p.tc_proj ? p.PB : p.QR) + ((long long)b * p.Hq + (long long)g * grp + warp) * HD;
+                    const float* qraw = (p.tc_proj ? p.PB + (long long)b * p.Hq * HD : p.QR + (long long)b * p.QS) +
+                                        ((long long)g * grp + warp) * HD;
                     const int qS = p.tc_proj ? p.sk[PH_Q] : 1;
                     const long long qst = (long long)p.B * p.Hq * HD;
                     const float* gq = p.blk[l].q_norm;
@@ -2350,6 +2390,74 @@ static __device__ __noinline__ bool sample_step(const DraftParams& p, int k, uns
     return grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x);
 }
 
+// ---------------------------------------------------------------------------
+// NextN: the drafter's own keys and values, and the block output
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void store_kv(float* d, float x) { *d = x; }
+__device__ __forceinline__ void store_kv(uint16_t* d, float x) { *d = __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+// Iteration k's key and value of every sequence with a row there, from the
+// fused projection's key and value rows in QR: per KV head the key RMS-normed
+// over hd with k_norm and rotated at the row position (NeoX pairs, the
+// step's (cos, sin) table of view 0), both stored in the drafter's KV
+// (views[0], slot = position) rounded to the weights' type.  A warp per
+// (sequence, KV head), lanes over hd.  The attention reads these rows with
+// bulk copies, so the writes are fenced for the async proxy; a grid barrier
+// orders them before any read.
+template <typename WT>
+__device__ void nextn_kv_write(const DraftParams& p, int k, const int* kv) {
+    const KView& vw = p.views[0];
+    const int HD = p.hd, nh = HD / 2, lane = threadIdx.x & 31;
+    const int nw = (int)gridDim.x * kWarps;
+    for (int it = (int)blockIdx.x * kWarps + (int)(threadIdx.x >> 5); it < p.B * p.Hkv; it += nw) {
+        const int b = it / p.Hkv, g = it - b * p.Hkv;
+        if (k < 0 && catchup_row(p, b, k) < 0) continue;   // no catch-up row of b at this iteration
+        const long long pos = row_pos(p, kv, b, k);
+        const float* kr = p.QR + (long long)b * p.QS + (long long)(p.Hq + g) * HD;
+        const float* vr = kr + (long long)p.Hkv * HD;
+        float ss = 0.f;
+        for (int d = lane; d < HD; d += 32) {
+            const float x = __ldcg(kr + d);
+            ss = fmaf(x, x, ss);
+        }
+        ss = warp_sum(ss);
+        const float rn = 1.0f / sqrtf(ss / (float)HD + p.eps);
+        const float* gk = p.blk[0].k_norm;
+        const float2* cs = p.ROPEQ + (long long)b * MTP_MAX_VIEWS * nh;   // view 0
+        WT* kd = reinterpret_cast<WT*>(const_cast<void*>(vw.k)) + (long long)b * vw.sb + (long long)g * vw.sh + pos * vw.st;
+        WT* vd = reinterpret_cast<WT*>(const_cast<void*>(vw.v)) + (long long)b * vw.sb + (long long)g * vw.sh + pos * vw.st;
+        for (int i = lane; i < nh; i += 32) {
+            const float a = __ldcg(kr + i) * rn * __ldg(gk + i);
+            const float c = __ldcg(kr + nh + i) * rn * __ldg(gk + nh + i);
+            const float2 t = __ldcg(cs + i);   // (cos, sin)
+            store_kv(kd + i, a * t.x - c * t.y);
+            store_kv(kd + nh + i, a * t.y + c * t.x);
+        }
+        for (int d = lane; d < HD; d += 32) store_kv(vd + d, __ldcg(vr + d));
+    }
+    fence_proxy_async_global();
+}
+
+// The block output h' = x_m + y2 of every sequence (no post-norm, no
+// projection): HX, the next step's hidden state, and HN = head_norm(h'),
+// the LM head's input.  CTA c takes sequences c, c + grid, ...
+static __device__ void nextn_post(const DraftParams& p, float* x, float* gs, float* dst, float* red) {
+    const int n = p.d_t;
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const float v = __ldcg(p.XM + (long long)b * n + i) + __ldcg(p.Y2 + (long long)b * n + i);
+            x[i] = v;
+            p.HX[(long long)b * n + i] = v;
+            gs[i] = __ldg(p.final_norm + i);
+        }
+        __syncthreads();
+        rms_into_s(x, gs, n, p.eps, dst, red);
+        for (int i = threadIdx.x; i < n; i += blockDim.x) p.HN[(long long)b * n + i] = dst[i];
+        __syncthreads();
+    }
+}
+
 // PT: the projections' weight type (WT, or int8_t for Q8_0 codes with block scales)
 template <typename WT, int HD, bool TC, typename PT>
 __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts, TcState& hs) {
@@ -2372,7 +2480,17 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         bool bad = false;
         for (int b = 0; b < p.B; ++b) {
             const int kl = p.kv_len[b], tk = p.last_tok[b];
-            if (kl < 1 || tk < 0 || tk >= p.V) bad = true;
+            if (kl < (p.nextn ? 0 : 1) || tk < 0 || tk >= p.V) bad = true;
+            if (p.nextn) {
+                // the drafter's KV must hold every row this call writes
+                const int nc = p.n_cu ? p.n_cu[b] : 0;
+                if (nc < 0 || nc > p.M || (long long)kl + nc + p.N > p.views[0].cap) bad = true;
+                for (int j = 0; j < nc && !bad; ++j) {
+                    const int t = p.cu_tok[(long long)b * p.M + j];
+                    if (t < 0 || t >= p.V) bad = true;
+                }
+                continue;
+            }
             for (int l = 0; l < p.L; ++l) {
                 const KView& v = p.views[p.blk[l].view];
                 if (v.window == 0 && kl > v.cap) bad = true;
@@ -2405,6 +2523,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     }
     // sequence lengths, read once, and the attention item tables
     __shared__ int s_kv[MTP_MAX_BATCH];
+    __shared__ int s_kx[MTP_MAX_BATCH];   // NextN: keys of the current draft step
     __shared__ AttnTab s_tab;
     for (int b = threadIdx.x; b < p.B; b += blockDim.x) s_kv[b] = p.kv_len[b];
     __syncthreads();
@@ -2455,7 +2574,9 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     using One = std::integral_constant<bool, false>;
     using Two = std::integral_constant<bool, true>;
 
-    for (int k = 0; k < p.N; ++k) {
+    // NextN: iterations -M .. -1 are the catch-up rows (PRE, then the key and
+    // value rows of Q and their store); 0 .. N-1 the draft steps
+    for (int k = p.nextn ? -p.M : 0; k < p.N; ++k) {
         // ---- PRE ----
         if (blockIdx.x == 0) {
             for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
@@ -2482,7 +2603,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                      e += gridDim.x * blockDim.x) {
                     const double f = __ldcg(p.ROPE + e % (MTP_MAX_VIEWS * nh));
                     if (f > 0.0) {
-                        double ang = ((double)s_kv[e / (MTP_MAX_VIEWS * nh)] + (double)k) * f;
+                        double ang = (double)row_pos(p, s_kv, e / (MTP_MAX_VIEWS * nh), k) * f;
                         ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
                         float sn, cs;
                         sincosf((float)ang, &sn, &cs);
@@ -2490,13 +2611,29 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                     }
                 }
             }
-            {
-                StoreEpi e{p.QR, p.Hq * p.hd};
+            if (!p.nextn) {
+                StoreEpi e{p.QR, p.QS};
                 if (!gemv_step(PH_Q, k, l, bw.w_q, nullptr, bw.s_q, nullptr, p.Hq * p.hd, p.d_a, e, One{})) return;
+            } else {
+                // ---- QKV (NextN): the fused projection; a catch-up row needs its key and value rows only ----
+                const int q0 = k < 0 ? p.Hq * p.hd : 0;
+                StoreEpi e{p.QR + q0, p.QS};
+                if (!gemv_step(PH_Q, k, l, reinterpret_cast<const PT*>(bw.w_q) + (long long)q0 * p.d_a, nullptr,
+                               nullptr, nullptr, p.QS - q0, p.d_a, e, One{}))
+                    return;
+                nextn_kv_write<WT>(p, k, s_kv);
+                if (k < 0) break;   // catch-up: the next PRE's barrier orders the stores
+                if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
+                // this step's keys: the rows before it, the catch-up rows, the steps so far and its own
+                for (int b = threadIdx.x; b < p.B; b += blockDim.x)
+                    s_kx[b] = s_kv[b] + (p.n_cu ? __ldg(p.n_cu + b) : 0) + k + 1;
+                __syncthreads();
+                attn_tab_fill(p, s_kx, attn_geom(HD, (int)sizeof(WT)).R, s_tab);
+                __syncthreads();
             }
             // ---- ATT ----
-            if (!attention_phase<WT, HD, TC ? kAttnStagesTc : kAttnStages, TC>(p, l, smem, s_kv, s_tab,
-                                                                              &attn_bar[0][0], attn_par))
+            if (!attention_phase<WT, HD, TC ? kAttnStagesTc : kAttnStages, TC>(p, l, smem, p.nextn ? s_kx : s_kv,
+                                                                              s_tab, &attn_bar[0][0], attn_par))
                 return;
             if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
             // every CTA has passed its attention waits: reset the item counters
@@ -2509,7 +2646,7 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
             }
             // ---- FFN1 (gate and up share the input; GeGLU in the epilogue) ----
             {
-                GegluEpi e{p.MB, p.F};
+                GegluEpi e{p.MB, p.F, p.nextn};
                 if (!gemv_step(PH_FFN1, k, l, bw.w_gate, bw.w_up, bw.s_gate, bw.s_up, p.F, p.d_a, e, Two{})) return;
             }
             // ---- FFN2 ----
@@ -2518,8 +2655,12 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 if (!gemv_step(PH_FFN2, k, l, bw.w_down, nullptr, bw.s_down, nullptr, p.d_a, p.F, e, One{})) return;
             }
         }
+        if (k < 0) continue;   // NextN catch-up iteration: done after its key and value
         // ---- POST ----
-        if (TC && p.tc_head) {
+        if (p.nextn) {
+            nextn_post(p, tmp, act + p.kmax, act, red);
+            if (!grid_barrier(p.hdr, epoch, p.timeout_ns, gridDim.x)) return;
+        } else if (TC && p.tc_head) {
             StoreXhEpi e{p.HN, p.d_t, p.XH, p.XL, kTcHeadM};
             if (!gemv_step(PH_POST, k, 0, p.w_post, nullptr, p.s_post, nullptr, p.d_t, p.d_a, e, One{})) return;
         } else {
@@ -2550,7 +2691,8 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
         for (int b = threadIdx.x; b < p.B; b += blockDim.x)
             p.out_drafts[(long long)b * p.N + (p.N - 1)] = step_token(p, b, p.N);
         if (p.out_h_last)
-            for (long long i = threadIdx.x; i < (long long)p.B * p.d_t; i += blockDim.x) p.out_h_last[i] = __ldcg(p.HN + i);
+            for (long long i = threadIdx.x; i < (long long)p.B * p.d_t; i += blockDim.x)
+                p.out_h_last[i] = __ldcg((p.nextn ? p.HX : p.HN) + i);
     }
 }
 

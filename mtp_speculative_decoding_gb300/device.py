@@ -6,8 +6,8 @@ import dataclasses
 
 import numpy as np
 
-from . import (Config, KVView, Weights, alloc_workspace, draft_block, make_config, make_view, make_weights,
-               quantize_q8_0, workspace_size)
+from . import (Config, KVView, Weights, alloc_workspace, draft_block, make_config, make_nextn_weights, make_view,
+               make_weights, nextn_draft, quantize_q8_0, workspace_size)
 
 
 def to_device(a: np.ndarray, dtype: str | None = None, device="cuda"):
@@ -92,3 +92,53 @@ def upload_draft(w, device="cuda", extra_ws_for=None, reuse: "DeviceDraft | None
         nbytes = max(nbytes, workspace_size(None, *extra_ws_for))
     ws = alloc_workspace(nbytes, device)
     return DeviceDraft(cfg, weights, views, tensors, kv_len, last_tok, h_prev, hist, w.B, w.N, m.vocab, m.d_t, ws)
+
+
+@dataclasses.dataclass
+class DeviceNextn:
+    """A NextN drafter on the device: weights, its own KV (k, v tensors, written
+    by every run), the catch-up rows and the step inputs of one call."""
+    cfg: Config
+    weights: Weights
+    tensors: dict
+    k: object
+    v: object
+    view: KVView
+    kv_len: object
+    n_cu: object
+    cu_tok: object
+    cu_h: object
+    last_tok: object
+    h_prev: object
+    B: int
+    N: int
+    V: int
+    d: int
+    ws: object
+
+    def run(self, out_drafts, out_h_last=None, out_logits=None, out_conf=None, stream=None):
+        nextn_draft(self.cfg, self.weights, self.view, self.kv_len, self.last_tok, self.h_prev, out_drafts, self.ws,
+                    n_cu=self.n_cu, cu_tok=self.cu_tok, cu_h=self.cu_h, out_h_last=out_h_last,
+                    out_logits=out_logits, out_conf=out_conf, stream=stream)
+
+
+def upload_nextn(w, device="cuda") -> DeviceNextn:
+    """Upload a ``synth.NextnWorkload``: the weights, a copy of its drafter KV
+    and the call's inputs."""
+    import torch
+    m = w.model
+    cfg = make_config(m.d, m.d, 1, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff, m.vocab, wdtype=m.dtype,
+                      rms_eps=m.rms_eps, attn_scale=m.attn_scale, emb_scale=m.emb_scale,
+                      logit_softcap=m.logit_softcap)
+    tensors = {n: to_device(a, device=device) for n, a in w.weights.items()}
+    weights = make_nextn_weights(tensors)
+    k, v = to_device(w.dkv["k"], device=device), to_device(w.dkv["v"], device=device)
+    view = make_view(k, v, w.dkv["cap"], 0, w.dkv["rope_theta"])
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+    M = w.M
+    cu_tok = i32(w.cu_tok) if M > 0 else None
+    cu_h = f32(w.cu_h) if M > 0 else None
+    ws = alloc_workspace(workspace_size(cfg, w.B, w.N, m.vocab), device)
+    return DeviceNextn(cfg, weights, tensors, k, v, view, i32(w.kv_len), i32(w.n_cu), cu_tok, cu_h,
+                       i32(w.last_tok), f32(w.h_prev), w.B, w.N, m.vocab, m.d, ws)
