@@ -11,8 +11,10 @@ d_t 5120, d_a 1024, 4 blocks, 16 x 256 query heads over 4 KV heads, GeGLU
 same model at B = 16 (N = 4, ragged 2k-32k contexts) and B = 64 (N = 2,
 context 4096), exact temp > 0 verification alone (mtp_verify_sample,
 B = 32, N = 3, V = 248320; that configuration has no draft block), and an
-Edge-shaped drafter with the centroid-routed LM head (B = 1, N = 3), and the
-headline workload with Q8_0 projections, each
+Edge-shaped drafter with the centroid-routed LM head (B = 1, N = 3), the
+headline workload with Q8_0 projections, and the dense NextN drafter
+(Qwen-shaped, B = 1: two catch-up rows then N = 3 drafts from its own KV of
+4096 rows, one mtp_nextn_draft call + greedy verify), each
 reported under per_workload with its own roofline fraction, end-to-end
 number and CPU baseline.  `--workload K` times one of them alone.
 
@@ -42,7 +44,8 @@ import synth  # noqa: E402
 METRIC = "drafted tok/s (MTP draft block + verify) at B=1..64; % of HBM/tensor roofline"
 UNIT = "tok/s"
 HEADLINE = 1
-OTHERS = (2, 3, 4, 5, 6)
+OTHERS = (2, 3, 4, 5, 6, 7)
+NEXTN = 7
 
 
 def parse(argv=None):
@@ -51,8 +54,8 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4, 5, 6],
-                    help="time this workload alone (default: the headline plus workloads 2-6)")
+    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4, 5, 6, 7],
+                    help="time this workload alone (default: the headline plus workloads 2-7)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
 
@@ -96,6 +99,16 @@ def draft_config(w, world: int = 1) -> dict:
     return dict({"workload": w.name, "B": w.B, "N": w.N, "vocab": m.vocab, "d_t": m.d_t, "d_a": m.d_a,
                  "n_blocks": m.n_blocks, "kv_len_max": int(w.kv_len.max()), "kv_len_min": int(w.kv_len.min()),
                  "lm_head": head, "projections": "Q8_0 (bf16 table and KV)" if m.wquant == "q8_0" else m.dtype},
+                **_common(world, False))
+
+
+def nextn_config(w, world: int = 1) -> dict:
+    m = w.model
+    return dict({"workload": w.name, "B": w.B, "N": w.N, "vocab": m.vocab, "d": m.d, "heads": m.n_q_heads,
+                 "kv_heads": m.n_kv_heads, "head_dim": m.head_dim, "d_ff": m.d_ff,
+                 "drafter_kv_rows": int(w.kv_len.max()), "catch_up_rows": int(w.n_cu.max()),
+                 "lm_head": "dense tied (shared head)", "projections": m.dtype,
+                 "path": "mtp_nextn_draft (catch-up + drafts, one launch) + mtp_verify_greedy"},
                 **_common(world, False))
 
 
@@ -161,6 +174,29 @@ def draft_flops_per_launch(w) -> float:
             n = len(synth.view_positions(vd["window"], int(w.kv_len[b]), vd.get("sink", 0)))
             attn += 4 * m.n_q_heads * m.head_dim * n
     return float(w.N * (2 * m.params() * w.B + attn))
+
+
+def nextn_bytes_per_launch(w) -> int:
+    """The NextN drafter's byte floor for one call.  Weights: every catch-up
+    iteration (as many as the largest catch-up count) reads eh_proj and the
+    key and value rows of w_qkv; every draft step all weights (the table once:
+    it is also the head).  Per sequence: each catch-up row's embedding row and
+    hidden state, each step's embedding row and the drafter KV's rows
+    [0, pos], and the key and value rows the call writes."""
+    m = w.model
+    esz = 2 if m.dtype == "bf16" else 4
+    d, hd, Hkv = m.d, m.head_dim, m.n_kv_heads
+    W = w.weights
+    kv_row = 2 * Hkv * hd * esz
+    tot = int(w.n_cu.max()) * (int(W["eh_proj"].nbytes) + 2 * Hkv * hd * d * esz)
+    tot += w.N * sum(int(a.nbytes) for a in W.values())
+    for b in range(w.B):
+        nc = int(w.n_cu[b])
+        tot += nc * (d * esz + 4 * d)
+        for k in range(w.N):
+            tot += (int(w.kv_len[b]) + nc + k + 1) * kv_row + d * esz
+        tot += (nc + w.N) * kv_row
+    return int(tot)
 
 
 def verify_sample_bytes(inp) -> int:
@@ -425,6 +461,118 @@ def bench_draft(wid, args, world, clocks, reuse=None):
     return fields, dev, w
 
 
+def bench_nextn(args, world, clocks):
+    """The NextN drafter (workload 7): one mtp_nextn_draft call (catch-up rows,
+    then N drafts from its own KV) + greedy verify.  Returns (fields, workload)."""
+    import torch
+    import mtp_speculative_decoding_gb300 as mtp
+    from mtp_speculative_decoding_gb300.device import to_device, upload_nextn
+
+    w = synth.make_nextn_inputs(NEXTN)
+    m = w.model
+    B, N, V = w.B, w.N, m.vocab
+    dev = upload_nextn(w)
+    ws = mtp.alloc_workspace(max(int(dev.ws.numel()), mtp.workspace_size(None, B, N, V)))
+    dev.ws = ws
+    drafts = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    h_last = torch.empty((B, m.d), dtype=torch.float32, device="cuda")
+    # every call writes the same drafter-KV rows (kv_len is not advanced): the timed calls repeat one call
+    dev.run(drafts, h_last)
+    torch.cuda.synchronize()
+    if mtp.last_error(ws) != 0:
+        raise RuntimeError(f"NextN drafter status {mtp.last_error(ws)}")
+    d_host = drafts.cpu().numpy()
+    vin = synth.make_verify_greedy_inputs(NEXTN, B=B, N=N, V=V)
+    logits_np = synth.plant_greedy_logits(synth.bf16_bits_to_f32(vin.logits), d_host, vin.planted, vin.dtype)
+    logits = to_device(logits_np, vin.dtype)
+    out_tok = torch.empty((B, N + 1), dtype=torch.int32, device="cuda")
+    n_acc = torch.empty((B,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        dev.run(drafts, h_last)
+        mtp.verify_greedy(logits, drafts, out_tok, n_acc, ws)
+    torch.cuda.synchronize()
+    assert mtp.last_error(ws) == 0
+    if not np.array_equal(n_acc.cpu().numpy(), vin.planted):
+        raise RuntimeError("NextN verify disagrees with the planted accept lengths")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        a, b_, c = ev[i]
+        a.record(stream)
+        dev.run(drafts, h_last)
+        b_.record(stream)
+        mtp.verify_greedy(logits, drafts, out_tok, n_acc, ws)
+        c.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks.pause()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    draft_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    verify_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    value = world * B * N * args.steps / (total_ms / 1e3)
+
+    # end to end: the call's inputs up from pinned host memory, the tokens back
+    host = {n: getattr(dev, n).cpu().pin_memory() for n in ("last_tok", "h_prev", "kv_len", "n_cu", "cu_tok", "cu_h")}
+    h_logits = torch.empty(logits.shape, dtype=logits.dtype).pin_memory()
+    h_logits.copy_(logits.cpu())
+    h_out = torch.empty((B, N + 1), dtype=torch.int32).pin_memory()
+    h_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h_dr = torch.empty((B, N), dtype=torch.int32).pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in host.values()) + h_logits.numel() * h_logits.element_size()
+    bo = (h_out.numel() + h_n.numel() + h_dr.numel()) * 4
+
+    def e2e_step():
+        for n, t in host.items():
+            getattr(dev, n).copy_(t, non_blocking=True)
+        logits.copy_(h_logits, non_blocking=True)
+        dev.run(drafts, h_last)
+        mtp.verify_greedy(logits, drafts, out_tok, n_acc, ws)
+        h_dr.copy_(drafts, non_blocking=True)
+        h_out.copy_(out_tok, non_blocking=True)
+        h_n.copy_(n_acc, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.pause()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    if not np.array_equal(h_n.numpy(), vin.planted):
+        raise RuntimeError("end-to-end NextN verify disagrees with the planted accept lengths")
+
+    peak, peak_kind = measured_peaks()
+    alg = nextn_bytes_per_launch(w)
+    achieved = alg / (statistics.mean(draft_ms) / 1e3) / 1e9
+    fields = {
+        "value": round(value, 2), "ms_per_step": round(total_ms / args.steps, 4),
+        "config": nextn_config(w, world),
+        "breakdown": {"draft_ms_mean": round(statistics.mean(draft_ms), 4),
+                      "verify_ms_mean": round(statistics.mean(verify_ms), 4)},
+        "e2e": {"value": round(world * B * N * args.steps / (e2e_ms / 1e3), 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)},
+        "roofline": {"bound": "hbm", "kernel": "draft_kernel (NextN)", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": alg, "traffic": recorded_traffic(w.name)},
+        "gpu_launches": 2 * args.steps,
+        "dtype": m.dtype,
+    }
+    return fields, w
+
+
 def bench_verify_sample(args, world, clocks):
     """Exact temp > 0 verification alone (workload 4).  Returns (fields, inputs)."""
     import torch
@@ -572,6 +720,32 @@ def cpu_baseline_draft(w, min_seconds: float = 8.0) -> dict:
             "cpu_model": cpu_model()}
 
 
+def cpu_baseline_nextn(w, min_seconds: float = 8.0) -> dict:
+    """Whole NextN drafting calls of single sequences (catch-up rows + N
+    steps) + their greedy verify rows, on all host cores until min_seconds of
+    work, then one call on one core."""
+    import oracle
+    vin = synth.make_verify_greedy_inputs(NEXTN, B=1, N=w.N, V=w.model.vocab)
+
+    def unit(r):
+        oracle.nextn_draft(w, seqs=[r % w.B], want_logits=False)
+        oracle.verify_greedy(vin.logits, vin.dtype, vin.drafts)
+
+    cores = oracle.num_threads()
+    reps, dt = _timed_units(unit, min_seconds)
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        unit(0)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(cores)
+    return {"value": round(reps * w.N / dt, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} single-sequence NextN calls (catch-up + N={w.N}) + greedy verify, {dt:.1f} s",
+            "single_thread": {"value": round(w.N / dt1, 4), "cores": 1, "sample": "one sequence's call"},
+            "cpu_model": cpu_model()}
+
+
 def cpu_baseline_verify_sample(inp, min_seconds: float = 8.0) -> dict:
     """The oracle's exact sampling verify, whole calls until min_seconds (the
     drafter's draws, by the oracle, untimed), then one call on one core."""
@@ -618,6 +792,13 @@ def run_ours(args):
             if want_cpu:
                 fields["cpu_baseline"] = cpu_baseline_verify_sample(inp)
             del inp
+        elif wid == NEXTN:
+            reuse = None   # a different model: the assistant's weights go
+            torch.cuda.empty_cache()
+            fields, w = bench_nextn(args, world, clocks)
+            if want_cpu:
+                fields["cpu_baseline"] = cpu_baseline_nextn(w)
+            del w
         else:
             fields, dev, w = bench_draft(wid, args, world, clocks, reuse=reuse)
             if want_cpu:
@@ -676,6 +857,21 @@ def run_reference(args):
         config = sample_config(inp, world)
         sample = f"{args.steps} full verify_sample calls"
         dtype = "f32"
+    elif wid == NEXTN:
+        w = synth.make_nextn_inputs(NEXTN)
+        vin = synth.make_verify_greedy_inputs(NEXTN, B=1, N=w.N, V=w.model.vocab)
+        for r in range(args.warmup):
+            oracle.nextn_draft(w, seqs=[r % w.B], want_logits=False)
+        times = []
+        for r in range(args.steps):
+            t0 = time.perf_counter()
+            oracle.nextn_draft(w, seqs=[r % w.B], want_logits=False)
+            oracle.verify_greedy(vin.logits, vin.dtype, vin.drafts)
+            times.append(time.perf_counter() - t0)
+        units = w.N * args.steps
+        config = nextn_config(w, world)
+        sample = f"{args.steps} single-sequence NextN calls + greedy verify"
+        dtype = "f64"
     else:
         w = synth.make_draft_inputs(wid)
         vin = synth.make_verify_greedy_inputs(0 if w.model.dtype == "f32" else 1, B=1, N=w.N, V=w.model.vocab)

@@ -2574,9 +2574,13 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
     using One = std::integral_constant<bool, false>;
     using Two = std::integral_constant<bool, true>;
 
-    // NextN: iterations -M .. -1 are the catch-up rows (PRE, then the key and
-    // value rows of Q and their store); 0 .. N-1 the draft steps
-    for (int k = p.nextn ? -p.M : 0; k < p.N; ++k) {
+    // NextN: iterations -C .. -1 are the catch-up rows, C the largest count
+    // of any sequence (PRE, then the key and value rows of Q and their
+    // store); 0 .. N-1 the draft steps.  Every CTA reads the same counts.
+    int k0 = 0;
+    if (p.nextn && p.n_cu)
+        for (int b = 0; b < p.B; ++b) k0 = max(k0, __ldg(p.n_cu + b));
+    for (int k = -k0; k < p.N; ++k) {
         // ---- PRE ----
         if (blockIdx.x == 0) {
             for (int b = threadIdx.x; b < p.B; b += blockDim.x) {

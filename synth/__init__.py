@@ -582,7 +582,8 @@ def make_verify_greedy_inputs(cfg_id: int, seed: int | None = None, B: int | Non
                               dtype: str | None = None) -> VerifyGreedyInputs:
     seed = workload_seed(cfg_id) if seed is None else seed
     defaults = {0: (1, 3, 4096, "f32"), 1: (1, 3, 262144, "bf16"), 2: (16, 4, 262144, "bf16"),
-                3: (64, 2, 262144, "bf16"), 5: (1, 3, 262144, "bf16"), 6: (1, 3, 262144, "bf16")}
+                3: (64, 2, 262144, "bf16"), 5: (1, 3, 262144, "bf16"), 6: (1, 3, 262144, "bf16"),
+                7: (1, 3, 248320, "bf16")}
     Bd, Nd, Vd, dd = defaults[cfg_id]
     B = Bd if B is None else B
     N = Nd if N is None else N
