@@ -53,7 +53,7 @@ size_t cent_smem(const mtp_config* c) {
 }
 int pad16(int B) { return (B + 15) & ~15; }
 
-size_t draft_smem(const mtp_config* c, int B, int act_smem, bool cc = false);
+size_t draft_smem(const mtp_config* c, int B, int act_smem);
 constexpr size_t kSmemLimit = 220 * 1024;
 
 // Projections on tensor cores: eligible for the head path, activations
@@ -64,15 +64,17 @@ bool tc_proj_eligible(const mtp_config* c, int B) {
 }
 
 // split-K factors of the projection phases (PH_PRE .. PH_POST) for a grid of
-// `grid` CTAs, and the floats of the largest split-partial set
+// `grid` CTAs, and the floats of the largest split-partial set (nextn: the
+// fused query / key / value projection in PH_Q)
 struct TcPlan {
     int sk[6];
     size_t pb_floats;
 };
-TcPlan tc_plan(const mtp_config* c, int B, int grid) {
+TcPlan tc_plan(const mtp_config* c, int B, int grid, bool nextn) {
     TcPlan t;
     const size_t qd = (size_t)c->n_q_heads * c->head_dim;
-    const size_t R[6] = {(size_t)c->d_a, qd, (size_t)c->d_a, 2 * (size_t)c->d_ff, (size_t)c->d_a, (size_t)c->d_t};
+    const size_t qr = (size_t)(nextn ? c->n_q_heads + 2 * c->n_kv_heads : c->n_q_heads) * c->head_dim;   // Q's rows
+    const size_t R[6] = {(size_t)c->d_a, qr, (size_t)c->d_a, 2 * (size_t)c->d_ff, (size_t)c->d_a, (size_t)c->d_t};
     const size_t K[6] = {2 * (size_t)c->d_t, (size_t)c->d_a, qd, (size_t)c->d_a, (size_t)c->d_ff, (size_t)c->d_a};
     t.pb_floats = 0;
     for (int ph = 0; ph < 6; ++ph) {
@@ -145,7 +147,12 @@ DraftLayout draft_layout(const mtp_config* c, int B, int N) {
     const size_t xa = tcp ? (size_t)((L.kmax + 63) / 64) * pad16(B) * 128 : 0;
     L.XA = off;      off = al256(off + xa);
     L.XAL = off;     off = al256(off + xa);
-    L.PB = off;      off = al256(off + (tcp ? tc_plan(c, B, draft_grid()).pb_floats * f : 0));
+    size_t pbf = 0;   // the larger of the assistant's and the NextN drafter's split partials
+    if (tcp) {
+        const size_t a = tc_plan(c, B, draft_grid(), false).pb_floats, n = tc_plan(c, B, draft_grid(), true).pb_floats;
+        pbf = a > n ? a : n;
+    }
+    L.PB = off;      off = al256(off + pbf * f);
     // sampled drafting: the step's logits and the sampler's per-row state
     L.ZB = off;      off = al256(off + (size_t)B * c->vocab * f);
     L.SBUF = off;    off = al256(off + (size_t)B * sample_rcap(c->vocab) * sizeof(int2));
@@ -222,11 +229,10 @@ size_t draft_smem_act(const mtp_config* c, int B, int act_smem) {
            (act_smem ? (size_t)B * kmax : kmax) * sizeof(float) + 2 * gmax * sizeof(float);   // + the gain stage
 }
 
-// cc: the CUDA-core kernel variant regardless of the batch (NextN)
-size_t draft_smem(const mtp_config* c, int B, int act_smem, bool cc) {
+size_t draft_smem(const mtp_config* c, int B, int act_smem) {
     const size_t wb = c->wdtype == MTP_DTYPE_BF16 ? 2 : 4;
     const size_t hd = c->head_dim, grp = c->n_q_heads / c->n_kv_heads;
-    const int nst = !cc && tc_head_eligible(c, B) ? kAttnStagesTc : kAttnStages;   // the kernel variant's ring depth
+    const int nst = tc_head_eligible(c, B) ? kAttnStagesTc : kAttnStages;   // the kernel variant's ring depth
     const size_t attn = attn_smem((int)hd, (int)wb, (int)grp, nst);
     const size_t act = draft_smem_act(c, B, act_smem);
     return attn > act ? attn : act;
@@ -452,11 +458,11 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
     const int sms = num_sms();
     if (sms <= 0) return MTP_ERR_CUDA;
 
-    size_t smem = draft_smem(cfg, B, 1, nx != nullptr);
+    size_t smem = draft_smem(cfg, B, 1);
     int act_smem = 1;
     if (smem > kSmemLimit) {
         act_smem = 0;
-        smem = draft_smem(cfg, B, 0, nx != nullptr);
+        smem = draft_smem(cfg, B, 0);
         if (smem > kSmemLimit) return MTP_ERR_UNSUPPORTED;
     }
     const int grid = draft_grid();
@@ -471,7 +477,7 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
         }
     }
     // batch: LM head on tensor cores, operand ring at offset 0 (1024-aligned)
-    const bool tc = !nx && tc_head_eligible(cfg, B);   // NextN runs the CUDA-core variant
+    const bool tc = tc_head_eligible(cfg, B);
     int tc_stages = 0, tc_cols = 0, th_stages = 0;
     if (tc) {
         const size_t sbytes = (size_t)kTcTileM * 128 + 2 * (size_t)pad16(B) * 128;
@@ -587,7 +593,7 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
             return MTP_ERR_CUDA;
         if (tc_proj_eligible(cfg, B) && !act_smem) {
             // projections: weights [R, K] row-major, inputs staged as [Bp, kmax]
-            const TcPlan plan = tc_plan(cfg, B, grid);
+            const TcPlan plan = tc_plan(cfg, B, grid, nx != nullptr);
             p.tc_proj = 1;
             p.att_fold = 1;   // the O prologue merges split attention segments: one row per CTA, no counter waits
             for (int i = 0; i < 6; ++i) p.sk[i] = plan.sk[i];
@@ -595,12 +601,13 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
             p.XAL = reinterpret_cast<uint16_t*>(base + L.XAL);
             p.PB = reinterpret_cast<float*>(base + L.PB);
             const uint64_t da = cfg->d_a, dt = cfg->d_t, F = cfg->d_ff, qd = (uint64_t)cfg->n_q_heads * cfg->head_dim;
+            const uint64_t qr = (uint64_t)p.QS;   // rows of w_q: NextN's fused projection has the key and value rows too
             bool okm = encode_bf16_map(&p.tm_w[0], w->w_pre, 2 * dt, da, kTcTileM) &&
-                       encode_bf16_map(&p.tm_w[1], w->w_post, da, dt, kTcTileM);
+                       (nx || encode_bf16_map(&p.tm_w[1], w->w_post, da, dt, kTcTileM));   // NextN: no post-projection
             for (int l = 0; l < cfg->n_blocks && okm; ++l) {
                 const mtp_block_weights& bw = w->blk[l];
                 CUtensorMap* m = &p.tm_w[2 + 5 * l];
-                okm = encode_bf16_map(m + 0, bw.w_q, da, qd, kTcTileM) && encode_bf16_map(m + 1, bw.w_o, qd, da, kTcTileM) &&
+                okm = encode_bf16_map(m + 0, bw.w_q, da, qr, kTcTileM) && encode_bf16_map(m + 1, bw.w_o, qd, da, kTcTileM) &&
                       encode_bf16_map(m + 2, bw.w_gate, da, F, kTcTileM) &&
                       encode_bf16_map(m + 3, bw.w_up, da, F, kTcTileM) &&
                       encode_bf16_map(m + 4, bw.w_down, F, da, kTcTileM);

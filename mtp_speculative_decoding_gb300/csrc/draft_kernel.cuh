@@ -739,8 +739,12 @@ __device__ void build_act(const DraftParams& p, int phase, int k, int l, int b, 
             const int S = p.sk[PH_FFN1];
             for (int i4 = threadIdx.x; i4 < (n >> 2); i4 += kThreads) {
                 const float4 g = ld4_sum(q + 4 * i4, S, st), u = ld4_sum(q + n + 4 * i4, S, st);
-                reinterpret_cast<float4*>(dst)[i4] = make_float4(gelu_tanh(g.x) * u.x, gelu_tanh(g.y) * u.y,
-                                                                 gelu_tanh(g.z) * u.z, gelu_tanh(g.w) * u.w);
+                if (p.nextn)
+                    reinterpret_cast<float4*>(dst)[i4] = make_float4(silu(g.x) * u.x, silu(g.y) * u.y, silu(g.z) * u.z,
+                                                                     silu(g.w) * u.w);
+                else
+                    reinterpret_cast<float4*>(dst)[i4] = make_float4(gelu_tanh(g.x) * u.x, gelu_tanh(g.y) * u.y,
+                                                                     gelu_tanh(g.z) * u.z, gelu_tanh(g.w) * u.w);
             }
         } else {
             vec_copy<1, 1>(VecCopy<1>{{p.MB + (long long)b * n}, {dst}}, n);
@@ -1002,7 +1006,8 @@ __device__ __forceinline__ int attn_slot(const AttnTab& t, int v, int cf, int q,
 // every lane's loads of a partial in flight together.
 static __device__ void attn_fold_row(const DraftParams& p, const AttnTab& tab, int l, int b, float* dst) {
     const int view = p.blk[l].view, HD = p.hd, grp = p.Hq / p.Hkv, PSZ = attn_psz(grp, HD);
-    const int n = view_keys(p.views[view], __ldg(p.kv_len + b));
+    // keys per KV head of sequence b, as the attention's table counted them
+    const int n = (int)((tab.pre[view][b + 1] - tab.pre[view][b]) / p.Hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5, DL = HD / 32;
     for (int h = warp; h < p.Hq; h += nw) {
         const int g = h / grp, hh = h - g * grp;
@@ -1219,10 +1224,9 @@ __device__ __forceinline__ bool attention_body(const DraftParams& p, int l, unsi
                 if (warp < grp) {
                     constexpr int NQ = (HD / 8 + 31) / 32;   // float4 pairs per lane
                     // the query projection, or its split partials summed in order
-                    const float* qraw = (p.tc_proj ? p.PB + (long long)b * p.Hq * HD : p.QR + (long long)b * p.QS) +
-                                        ((long long)g * grp + warp) * HD;
+                    const float* qraw = (p.tc_proj ? p.PB : p.QR) + (long long)b * p.QS + ((long long)g * grp + warp) * HD;
                     const int qS = p.tc_proj ? p.sk[PH_Q] : 1;
-                    const long long qst = (long long)p.B * p.Hq * HD;
+                    const long long qst = (long long)p.B * p.QS;
                     const float* gq = p.blk[l].q_norm;
                     const float4* cs = reinterpret_cast<const float4*>(
                         p.ROPEQ + ((long long)b * MTP_MAX_VIEWS + view) * (HD / 2));
@@ -2106,7 +2110,7 @@ __device__ __forceinline__ TcJob tc_job(const DraftParams& p, int phase, int l) 
     int K = 0;
     switch (phase) {
     case PH_PRE: J.wa = J.wb = &p.tm_w[0]; J.R = p.d_a; K = 2 * p.d_t; break;
-    case PH_Q: J.wa = J.wb = &p.tm_w[2 + 5 * l]; J.R = p.Hq * p.hd; K = p.d_a; break;
+    case PH_Q: J.wa = J.wb = &p.tm_w[2 + 5 * l]; J.R = p.QS; K = p.d_a; break;   // NextN: query, key and value rows
     case PH_O: J.wa = J.wb = &p.tm_w[2 + 5 * l + 1]; J.R = p.d_a; K = p.Hq * p.hd; break;
     case PH_FFN1: J.wa = &p.tm_w[2 + 5 * l + 2]; J.wb = &p.tm_w[2 + 5 * l + 3]; J.R = 2 * p.F; K = p.d_a; break;
     case PH_FFN2: J.wa = J.wb = &p.tm_w[2 + 5 * l + 4]; J.R = p.d_a; K = p.F; break;
@@ -2398,7 +2402,8 @@ __device__ __forceinline__ void store_kv(float* d, float x) { *d = x; }
 __device__ __forceinline__ void store_kv(uint16_t* d, float x) { *d = __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
 // Iteration k's key and value of every sequence with a row there, from the
-// fused projection's key and value rows in QR: per KV head the key RMS-normed
+// fused projection's key and value rows (QR, or on the tensor-core path its
+// split-K partials summed in order): per KV head the key RMS-normed
 // over hd with k_norm and rotated at the row position (NeoX pairs, the
 // step's (cos, sin) table of view 0), both stored in the drafter's KV
 // (views[0], slot = position) rounded to the weights' type.  A warp per
@@ -2414,11 +2419,19 @@ __device__ void nextn_kv_write(const DraftParams& p, int k, const int* kv) {
         const int b = it / p.Hkv, g = it - b * p.Hkv;
         if (k < 0 && catchup_row(p, b, k) < 0) continue;   // no catch-up row of b at this iteration
         const long long pos = row_pos(p, kv, b, k);
-        const float* kr = p.QR + (long long)b * p.QS + (long long)(p.Hq + g) * HD;
-        const float* vr = kr + (long long)p.Hkv * HD;
+        // the projection's key and value rows: QR, or the split-K partials summed in order
+        const float* src = (p.tc_proj ? p.PB : p.QR) + (long long)b * p.QS;
+        const int S = p.tc_proj ? p.sk[PH_Q] : 1;
+        const long long st = (long long)p.B * p.QS;
+        auto raw = [&](int off) {
+            float v = __ldcg(src + off);
+            for (int s = 1; s < S; ++s) v += __ldcg(src + s * st + off);
+            return v;
+        };
+        const int ko = (p.Hq + g) * HD, vo = (p.Hq + p.Hkv + g) * HD;
         float ss = 0.f;
         for (int d = lane; d < HD; d += 32) {
-            const float x = __ldcg(kr + d);
+            const float x = raw(ko + d);
             ss = fmaf(x, x, ss);
         }
         ss = warp_sum(ss);
@@ -2428,34 +2441,52 @@ __device__ void nextn_kv_write(const DraftParams& p, int k, const int* kv) {
         WT* kd = reinterpret_cast<WT*>(const_cast<void*>(vw.k)) + (long long)b * vw.sb + (long long)g * vw.sh + pos * vw.st;
         WT* vd = reinterpret_cast<WT*>(const_cast<void*>(vw.v)) + (long long)b * vw.sb + (long long)g * vw.sh + pos * vw.st;
         for (int i = lane; i < nh; i += 32) {
-            const float a = __ldcg(kr + i) * rn * __ldg(gk + i);
-            const float c = __ldcg(kr + nh + i) * rn * __ldg(gk + nh + i);
+            const float a = raw(ko + i) * rn * __ldg(gk + i);
+            const float c = raw(ko + nh + i) * rn * __ldg(gk + nh + i);
             const float2 t = __ldcg(cs + i);   // (cos, sin)
             store_kv(kd + i, a * t.x - c * t.y);
             store_kv(kd + nh + i, a * t.y + c * t.x);
         }
-        for (int d = lane; d < HD; d += 32) store_kv(vd + d, __ldcg(vr + d));
+        for (int d = lane; d < HD; d += 32) store_kv(vd + d, raw(vo + d));
     }
     fence_proxy_async_global();
 }
 
 // The block output h' = x_m + y2 of every sequence (no post-norm, no
-// projection): HX, the next step's hidden state, and HN = head_norm(h'),
-// the LM head's input.  CTA c takes sequences c, c + grid, ...
+// projection; y2 the down projection, or on the tensor-core path its split-K
+// partials summed in order): HX, the next step's hidden state, and HN =
+// head_norm(h'), the LM head's input (with the tensor-core head also as the
+// head operand's bf16 high and low parts).  CTA c takes sequences c,
+// c + grid, ...
 static __device__ void nextn_post(const DraftParams& p, float* x, float* gs, float* dst, float* red) {
     const int n = p.d_t;
+    const int S = p.tc_proj ? p.sk[PH_FFN2] : 1;
+    const float* y2 = p.tc_proj ? p.PB : p.Y2;
+    const long long st = (long long)p.B * n;
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            const float v = __ldcg(p.XM + (long long)b * n + i) + __ldcg(p.Y2 + (long long)b * n + i);
+            float y = __ldcg(y2 + (long long)b * n + i);
+            for (int s = 1; s < S; ++s) y += __ldcg(y2 + s * st + (long long)b * n + i);
+            const float v = __ldcg(p.XM + (long long)b * n + i) + y;
             x[i] = v;
             p.HX[(long long)b * n + i] = v;
             gs[i] = __ldg(p.final_norm + i);
         }
         __syncthreads();
         rms_into_s(x, gs, n, p.eps, dst, red);
-        for (int i = threadIdx.x; i < n; i += blockDim.x) p.HN[(long long)b * n + i] = dst[i];
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const float v = dst[i];
+            p.HN[(long long)b * n + i] = v;
+            if (p.tc_head) {
+                const long long xi = xtile_idx(b, i, kTcHeadM);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                p.XH[xi] = __bfloat16_as_ushort(hi);
+                p.XL[xi] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+            }
+        }
         __syncthreads();
     }
+    if (p.tc_head) fence_proxy_async_global();   // the head operand is read by bulk copies
 }
 
 // PT: the projections' weight type (WT, or int8_t for Q8_0 codes with block scales)
@@ -2620,7 +2651,8 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 if (!gemv_step(PH_Q, k, l, bw.w_q, nullptr, bw.s_q, nullptr, p.Hq * p.hd, p.d_a, e, One{})) return;
             } else {
                 // ---- QKV (NextN): the fused projection; a catch-up row needs its key and value rows only ----
-                const int q0 = k < 0 ? p.Hq * p.hd : 0;
+                // (the tensor-core path runs the whole projection for a catch-up row too)
+                const int q0 = k < 0 && !p.tc_proj ? p.Hq * p.hd : 0;
                 StoreEpi e{p.QR + q0, p.QS};
                 if (!gemv_step(PH_Q, k, l, reinterpret_cast<const PT*>(bw.w_q) + (long long)q0 * p.d_a, nullptr,
                                nullptr, nullptr, p.QS - q0, p.d_a, e, One{}))

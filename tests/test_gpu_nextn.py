@@ -117,12 +117,26 @@ def test_softcap_and_head_dims():
 
 
 def test_batch_sixteen_and_twenty():
-    """At B >= 8 the assistant switches to the tensor-core variant; the NextN
-    drafter stays on the CUDA-core one at every batch."""
+    """B >= 8, bf16: the tensor-core LM head (the projections stay on CUDA
+    cores at these small widths: their inputs fit in shared memory)."""
     for B in (16, 20):
         w = tiny("bf16", B=B, N=2, M=3, kv_len=tuple(range(0, 3 * B, 3)), n_cu=tuple(i % 4 for i in range(B)),
                  seed=B)
         check(w, run(w), seqs=[0, 5, B - 1])
+
+
+@pytest.mark.parametrize("B", [9, 24])
+def test_tensor_core_paths(B):
+    """Width 1024, SwiGLU 4096, bf16: at B = 9 the inputs still fit in shared
+    memory (tensor-core head, CUDA-core projections); at B = 24 they do not,
+    and the projections run as split-K tensor-core GEMMs (the stored keys and
+    values summed from the fused projection's partials, the block output from
+    the down projection's)."""
+    m = synth.NextnSpec(d=1024, n_q_heads=8, head_dim=128, n_kv_heads=2, d_ff=4096, vocab=5000, dtype="bf16",
+                        rope_theta=1e4)
+    w = synth.make_nextn_workload("tc-nextn", m, B, 3, 2, [1 + 7 * i for i in range(B)], [i % 3 for i in range(B)],
+                                  40 + B)
+    check(w, run(w), seqs=[0, B // 2, B - 1])
 
 
 def test_without_logits_and_confidence():
@@ -230,3 +244,10 @@ def test_qwen_shaped_workload():
     w = synth.make_nextn_inputs(7)
     g = run(w)
     check(w, g)
+
+
+@pytest.mark.slow
+def test_qwen_shaped_batch_of_sixteen():
+    w = synth.make_nextn_inputs(7, B=16)
+    g = run(w, want_logits=False)
+    check(w, g, seqs=[0, 15])
