@@ -35,8 +35,11 @@ constexpr int kHeadGroups = 4;
 constexpr int kHeadSlots = 3;
 constexpr int kHeadMaxChunks = 640;
 // Batched projections on tensor cores (bf16 weights, B >= kTcMinBatch):
-// 128-row weight tiles, K steps of 64, a tc_stages-deep operand ring
-constexpr int kTcMinBatch = 8;
+// 128-row weight tiles, K steps of 64, a tc_stages-deep operand ring.  From
+// two sequences the tensor-core head beats the CUDA-core GEMV over B columns
+// (measured, draft launch at the Gemma shape: B = 2 3.29 -> 2.22 ms, B = 4
+// 4.96 -> 2.60, B = 6 10.8 -> 2.47); one sequence keeps the bulk-copy head.
+constexpr int kTcMinBatch = 2;
 constexpr int kTcTileM = 128;
 constexpr int kTcTileK = 64;
 constexpr int kTcMaxStages = 8;

@@ -29,11 +29,13 @@
 //
 // Norms and residual updates run redundantly in every CTA's phase prologue
 // (each CTA needs the whole input vector of its GEMV anyway), so they cost no
-// barrier.  Below eight sequences the weights stream through 16-byte
-// no-L1-allocate loads under an L2 evict-first policy, a warp per output row
-// (at one sequence: two warps per row when rows are few, two rows per warp
-// when rows are short); from eight sequences the projections and the LM head
-// run on the tensor cores (tc_gemm, tc_head).  Activations are fp32.
+// barrier.  At one sequence (and with fp32, Q8_0 or centroid-routed models)
+// the weights stream through 16-byte no-L1-allocate loads under an L2
+// evict-first policy, a warp per output row (at one sequence: two warps per
+// row when rows are few, two rows per warp when rows are short); from two
+// sequences the LM head, and the projections once their inputs no longer fit
+// in shared memory, run on the tensor cores (tc_head, tc_gemm).  Activations
+// are fp32.
 #pragma once
 
 #include <cuda_runtime.h>

@@ -117,7 +117,7 @@ def test_softcap_and_head_dims():
 
 
 def test_batch_sixteen_and_twenty():
-    """B >= 8, bf16: the tensor-core LM head (the projections stay on CUDA
+    """B >= 2, bf16: the tensor-core LM head (the projections stay on CUDA
     cores at these small widths: their inputs fit in shared memory)."""
     for B in (16, 20):
         w = tiny("bf16", B=B, N=2, M=3, kv_len=tuple(range(0, 3 * B, 3)), n_cu=tuple(i % 4 for i in range(B)),
