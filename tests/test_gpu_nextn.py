@@ -251,3 +251,44 @@ def test_qwen_shaped_batch_of_sixteen():
     w = synth.make_nextn_inputs(7, B=16)
     g = run(w, want_logits=False)
     check(w, g, seqs=[0, 15])
+
+
+def test_maximum_catch_up_and_a_full_kv():
+    """M = MTP_MAX_CATCHUP rows (ragged 0..16), and a sequence whose last draft
+    row lands in the KV's last slot (kv_len + n_cu + N == cap)."""
+    import mtp_speculative_decoding_gb300 as mtp
+    M = mtp.MTP_MAX_CATCHUP
+    m = synth.NextnSpec(d=256, n_q_heads=4, head_dim=64, n_kv_heads=2, d_ff=512, vocab=3000, dtype="bf16",
+                        rope_theta=1e4)
+    kv, nc, N = [3, 40, 0, 17], [16, 0, 7, 16], 3
+    cap = max(k + c for k, c in zip(kv, nc)) + N
+    w = synth.make_nextn_workload("max-catchup", m, 4, N, M, kv, nc, 77, cap=cap)
+    assert int((w.kv_len + w.n_cu).max()) + N == w.dkv["cap"]
+    check(w, run(w))
+
+
+def test_batch_of_sixty_four():
+    w = tiny("bf16", B=64, N=2, M=2, kv_len=tuple(range(0, 128, 2)), n_cu=tuple(i % 3 for i in range(64)), seed=64)
+    check(w, run(w, want_logits=False), seqs=[0, 17, 34, 63])
+
+
+def test_null_counts_mean_no_catch_up():
+    """n_cu NULL with catch-up arrays given: no catch-up rows (the header's
+    "NULL: all 0"), the same as counts of zero."""
+    import copy
+    import torch
+    import mtp_speculative_decoding_gb300 as mtp
+    from mtp_speculative_decoding_gb300.device import upload_nextn
+    w = tiny("f32", B=2, kv_len=(4, 6), n_cu=(2, 1), seed=19)
+    w0 = copy.copy(w)
+    w0.n_cu = np.zeros(w.B, np.int32)
+    ref = run(w0)
+    dev = upload_nextn(w)
+    d = torch.full((w.B, w.N), -7, dtype=torch.int32, device="cuda")
+    h = torch.empty((w.B, w.model.d), dtype=torch.float32, device="cuda")
+    mtp.nextn_draft(dev.cfg, dev.weights, dev.view, dev.kv_len, dev.last_tok, dev.h_prev, d, dev.ws, n_cu=None,
+                    cu_tok=dev.cu_tok, cu_h=dev.cu_h, out_h_last=h)
+    torch.cuda.synchronize()
+    assert mtp.last_error(dev.ws) == 0
+    np.testing.assert_array_equal(d.cpu().numpy(), ref["drafts"])
+    np.testing.assert_array_equal(h.cpu().numpy(), ref["h"])
