@@ -40,7 +40,7 @@ class Model(C.Structure):
     _fields_ = [("d_t", C.c_int32), ("d_a", C.c_int32), ("n_blocks", C.c_int32),
                 ("n_q_heads", C.c_int32), ("head_dim", C.c_int32), ("n_kv_heads", C.c_int32),
                 ("d_ff", C.c_int32), ("vocab", C.c_int32), ("wbf16", C.c_int32), ("n_centroids", C.c_int32),
-                ("centroid_top_k", C.c_int32), ("pad_", C.c_int32),
+                ("centroid_top_k", C.c_int32), ("kv_bf16", C.c_int32),
                 ("rms_eps", C.c_double), ("attn_scale", C.c_double), ("emb_scale", C.c_double),
                 ("logit_softcap", C.c_double)]
 
@@ -90,6 +90,8 @@ def _declare(L):
     L.orc_centroid_head.restype = I
     L.orc_quantize_q8_0.argtypes = [P, C.c_int64, C.c_int64, P, P]
     L.orc_dequantize_q8_0.argtypes = [P, P, C.c_int64, C.c_int64, P]
+    L.orc_quantize_q4_0.argtypes = [P, C.c_int64, C.c_int64, P, P]
+    L.orc_dequantize_q4_0.argtypes = [P, P, C.c_int64, C.c_int64, P]
     L.orc_top1_prob.argtypes = [P, C.c_int64]
     L.orc_top1_prob.restype = D
     L.orc_draft_block.restype = I
@@ -221,6 +223,29 @@ def dequantize_q8_0(q, d):
     return w
 
 
+def quantize_q4_0(w):
+    """Q4_0 codes (uint8 [rows, cols / 2], two per byte) and block scales
+    (binary16 bits [rows, cols / 32]) of an fp32 matrix (ggml's scale rule)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    if cols % 32:
+        raise ValueError("Q4_0 needs a multiple of 32 columns")
+    q = np.empty((rows, cols // 2), dtype=np.uint8)
+    d = np.empty((rows, cols // 32), dtype=np.uint16)
+    lib().orc_quantize_q4_0(_p(w), rows, cols, _p(q), _p(d))
+    return q, d
+
+
+def dequantize_q4_0(q, d):
+    """The fp32 weights Q4_0 codes and scales stand for."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    d = np.ascontiguousarray(d, dtype=np.uint16)
+    rows, cols = q.shape[0], q.shape[1] * 2
+    w = np.empty((rows, cols), dtype=np.float32)
+    lib().orc_dequantize_q4_0(_p(q), _p(d), rows, cols, _p(w))
+    return w
+
+
 def top1_prob(z):
     """The softmax probability of the largest logit (NaN entries left out)."""
     z = np.ascontiguousarray(z, dtype=np.float64)
@@ -245,8 +270,9 @@ BLOCK_ORDER = ("attn_norm", "w_q", "q_norm", "w_o", "post_attn_norm", "pre_ffn_n
 
 
 def _model(m) -> Model:
+    bf = 1 if m.dtype == "bf16" else 0
     return Model(m.d_t, m.d_a, m.n_blocks, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff, m.vocab,
-                 1 if m.dtype == "bf16" else 0, getattr(m, "n_centroids", 0), getattr(m, "centroid_top_k", 0), 0,
+                 bf, getattr(m, "n_centroids", 0), getattr(m, "centroid_top_k", 0), bf,
                  m.rms_eps, m.attn_scale, m.emb_scale, m.logit_softcap)
 
 
@@ -284,6 +310,8 @@ def _derived(a, kind):
         return hit[1]
     if kind == "widen":
         out = np.ascontiguousarray((a.astype(np.uint32) << 16).view(np.float32)) if a.dtype == np.uint16 else a
+    elif kind == "q4_0":
+        out = dequantize_q4_0(*quantize_q4_0(a))
     else:
         out = dequantize_q8_0(*quantize_q8_0(a))
     if len(_DERIVED) > 64:
@@ -307,13 +335,15 @@ class _Bound:
         names = list(GLOBAL_ORDER) + [f"blk{i}.{n}" for i in range(m.n_blocks) for n in BLOCK_ORDER]
         # the centroid head's tensors exist only for centroid-head models (NULL otherwise)
         arrs = [np.ascontiguousarray(w.weights[n]) if n in w.weights else None for n in names]
-        q8 = getattr(m, "wquant", "none") == "q8_0"
+        quant = getattr(m, "wquant", "none")
+        q8 = quant in ("q8_0", "q4_0")
         if q8:
-            # Q8_0 projections: the weights the codes stand for (exact in fp32); the
-            # table and the KV widened from bf16 exactly, and the step run in fp32
+            # Q8_0 / Q4_0 projections: the weights the codes stand for (exact in
+            # fp32); the table and the KV widened from bf16 exactly, and the step
+            # run in fp32
             proj = set(_projection_names(m))
             arrs = [None if a is None else
-                    _derived(a, "q8") if n in proj else
+                    _derived(a, quant) if n in proj else
                     _widen(a) for n, a in zip(names, arrs)]
             self.model.wbf16 = 0
         self.keep += [a for a in arrs if a is not None]
@@ -402,6 +432,7 @@ def draft_step(w, b, step, tok, h_prev):
 
 NEXTN_ORDER = ("tok_embd", "enorm", "hnorm", "eh_proj", "head_norm", "attn_norm", "w_qkv", "q_norm",
                "k_norm", "w_o", "ffn_norm", "w_gate", "w_up", "w_down")
+NEXTN_PROJECTIONS = ("eh_proj", "w_qkv", "w_o", "w_gate", "w_up", "w_down")
 
 
 def silu(x):
@@ -433,8 +464,15 @@ def nextn_draft(w, force=None, seqs=None, want_logits=True, dkv=None):
     v = np.array(src["v"], copy=True, order="C")
     Bv, H, cap, hd = k.shape
     arrs = [np.ascontiguousarray(w.weights[n]) for n in NEXTN_ORDER]
-    tensors = (C.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
     mdl = _model(m)
+    quant = getattr(m, "wquant", "none")
+    if quant in ("q8_0", "q4_0"):
+        # quantised projections: the weights the codes stand for, the table
+        # widened, the step in fp32; the drafter's KV stays bf16
+        proj = set(NEXTN_PROJECTIONS)
+        arrs = [_derived(a, quant) if n in proj else _widen(a) for n, a in zip(NEXTN_ORDER, arrs)]
+        mdl.wbf16 = 0
+    tensors = (C.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
     esz = k.itemsize
     out = dict(drafts=np.empty((S, N), dtype=np.int32), h_last=np.empty((S, d)), margin=np.empty((S, N)),
                conf=np.empty((S, N)), logits=np.empty((S, N, V)) if want_logits else None)

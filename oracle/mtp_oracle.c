@@ -76,7 +76,8 @@ typedef struct {
     int32_t d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab;
     int32_t wbf16;        /* 1: weight matrices and KV are bf16 bit patterns; 0: fp32 */
     int32_t n_centroids;  /* 0: dense tied LM head; > 0: centroid-routed head */
-    int32_t centroid_top_k, pad_;
+    int32_t centroid_top_k;
+    int32_t kv_bf16;      /* NextN: 1 when the drafter's own KV is stored as bf16 (its weights may be widened) */
     double rms_eps, attn_scale, emb_scale, logit_softcap;
 } orc_model;
 
@@ -480,6 +481,51 @@ void orc_dequantize_q8_0(const int8_t *q, const uint16_t *d16, int64_t rows, int
             w[r * cols + c] = (float)(f16_to_double(d16[r * nb + c / 32]) * (double)q[r * cols + c]);
 }
 
+/* Q4_0 quantisation of a row-major [rows, cols] fp32 matrix, cols a multiple
+ * of 32 (the Q4_0 format of the report's Q4_0 column, with ggml's rule for
+ * the scale -- the report's own quantiser picks it by Lloyd iterations, which
+ * the page does not spell out): per block of 32 consecutive weights of a row,
+ * m = the weight of largest magnitude (the first on ties), d = m / -8 in fp32,
+ * stored as binary16; codes q = min(15, trunc(w * (1 / d) + 8.5)) in fp32
+ * (all 8 when d = 0), so m itself gets code 0.  The weight a code stands for
+ * is f16(d) * (q - 8).  Storage: 16 bytes per block, byte j holding the code
+ * of weight j in its low four bits and that of weight j + 16 in its high
+ * four: codes go to q[rows, cols / 2] (uint8), block scales to
+ * d16[rows, cols / 32] (binary16 bits). */
+void orc_quantize_q4_0(const float *w, int64_t rows, int64_t cols, uint8_t *q, uint16_t *d16) {
+    const int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < nb; ++j) {
+            const float *x = w + r * cols + j * 32;
+            float amax = 0.0f, m = 0.0f;
+            for (int i = 0; i < 32; ++i)
+                if (fabsf(x[i]) > amax) { amax = fabsf(x[i]); m = x[i]; }
+            const float d = m / -8.0f;
+            const float id = d != 0.0f ? 1.0f / d : 0.0f;
+            int code[32];
+            for (int i = 0; i < 32; ++i) {
+                const int t = (int)(x[i] * id + 8.5f);   /* truncation toward zero; the value lies in [0.5, 16.5] */
+                code[i] = t < 15 ? t : 15;
+            }
+            uint8_t *qb = q + r * (cols / 2) + j * 16;
+            for (int i = 0; i < 16; ++i) qb[i] = (uint8_t)(code[i] | (code[i + 16] << 4));
+            d16[r * nb + j] = f32_to_f16(d);
+        }
+}
+
+/* The weights Q4_0 codes stand for, fp32 (exact: an 11-bit scale times a
+ * small integer). */
+void orc_dequantize_q4_0(const uint8_t *q, const uint16_t *d16, int64_t rows, int64_t cols, float *w) {
+    const int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            const int64_t j = c / 32, i = c % 32;
+            const uint8_t byte = q[r * (cols / 2) + j * 16 + (i % 16)];
+            const int code = i < 16 ? (byte & 15) : (byte >> 4);
+            w[r * cols + c] = (float)(f16_to_double(d16[r * nb + j]) * (double)(code - 8));
+        }
+}
+
 /* ------------------------------------------------------------------------ */
 /* centroid-routed LM head ([G4] sec. 3, "Centroid / ordered-embeddings LM  */
 /* head", steps 1-5)                                                         */
@@ -781,7 +827,7 @@ static void store_elem(const void *p, int64_t i, int bf16, double x) {
 static int nextn_row(const orc_model *m, const void *const *t, const orc_view *dkv, int b, int32_t tk,
                      const double *hin, int64_t pos, int full, double *hout, double *z) {
     const int d = m->d_t, hd = m->head_dim, Hq = m->n_q_heads, Hkv = m->n_kv_heads, F = m->d_ff, V = m->vocab;
-    const int bf = m->wbf16, grp = Hq / Hkv, qkv = (Hq + 2 * Hkv) * hd;
+    const int bf = m->wbf16, kvb = m->kv_bf16, grp = Hq / Hkv, qkv = (Hq + 2 * Hkv) * hd;
     if (tk < 0 || tk >= V || pos < 0 || pos >= dkv->cap) return -1;
     double *e = malloc(sizeof(double) * d), *u = malloc(sizeof(double) * 2 * d);
     double *x = malloc(sizeof(double) * d), *a = malloc(sizeof(double) * d), *y = malloc(sizeof(double) * d);
@@ -802,8 +848,8 @@ static int nextn_row(const orc_model *m, const void *const *t, const orc_view *d
         orc_rope_neox(tmp, hd, pos, dkv->rope_theta);
         const int64_t base = (int64_t)b * dkv->stride_b + (int64_t)g * dkv->stride_h + pos * dkv->stride_t;
         for (int c = 0; c < hd; ++c) {
-            store_elem(dkv->k, base + c, bf, tmp[c]);
-            store_elem(dkv->v, base + c, bf, vh[c]);
+            store_elem(dkv->k, base + c, kvb, tmp[c]);
+            store_elem(dkv->v, base + c, kvb, vh[c]);
         }
     }
     if (full) {
@@ -812,7 +858,7 @@ static int nextn_row(const orc_model *m, const void *const *t, const orc_view *d
             double *qh = q + (size_t)h * hd;
             orc_rmsnorm(qh, hd, (const float *)NT(NX_Q_NORM), m->rms_eps, tmp);
             orc_rope_neox(tmp, hd, pos, dkv->rope_theta);
-            orc_attend_head(tmp, dkv, b, h / grp, hd, (int)(pos + 1), m->attn_scale, bf, o + (size_t)h * hd);
+            orc_attend_head(tmp, dkv, b, h / grp, hd, (int)(pos + 1), m->attn_scale, kvb, o + (size_t)h * hd);
         }
         orc_matvec(NT(NX_W_O), d, Hq * hd, bf, o, y);
         for (int c = 0; c < d; ++c) x[c] += y[c];

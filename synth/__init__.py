@@ -154,7 +154,7 @@ class ModelSpec:
     logit_softcap: float = 0.0
     n_centroids: int = 0         # > 0: centroid-routed LM head over n_centroids lists of vocab / n_centroids ids
     centroid_top_k: int = 0      # centroids whose lists are scored per step
-    wquant: str = "none"         # "q8_0": the projections are quantised (generated here in fp32, unrounded)
+    wquant: str = "none"         # "q8_0" / "q4_0": the projections are quantised (generated here in fp32, unrounded)
 
     @property
     def emb_scale(self) -> float:
@@ -401,6 +401,7 @@ def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None
 
 NEXTN_TENSORS = ("tok_embd", "enorm", "hnorm", "eh_proj", "head_norm", "attn_norm", "w_qkv", "q_norm",
                  "k_norm", "w_o", "ffn_norm", "w_gate", "w_up", "w_down")
+NEXTN_PROJECTIONS = ("eh_proj", "w_qkv", "w_o", "w_gate", "w_up", "w_down")
 
 
 @dataclasses.dataclass
@@ -418,6 +419,7 @@ class NextnSpec:
     rms_eps: float = 1e-6
     logit_softcap: float = 0.0
     rope_theta: float = 1e7
+    wquant: str = "none"         # "q8_0" / "q4_0": the projections quantised (generated here in fp32, unrounded)
 
     # the shapes the oracle's model record shares with the assistant
     @property
@@ -431,7 +433,6 @@ class NextnSpec:
     n_blocks = 1
     n_centroids = 0
     centroid_top_k = 0
-    wquant = "none"
 
     @property
     def emb_scale(self) -> float:
@@ -478,7 +479,8 @@ def make_nextn_weights(m: NextnSpec, seed: int, std: float = 0.02) -> dict:
              "q_norm": m.head_dim, "k_norm": m.head_dim}
     w = {}
     for name, shp in shapes.items():
-        w[name] = _as_dtype(normal(seed, "nextn." + name, shp, std=std), m.dtype)
+        vals = normal(seed, "nextn." + name, shp, std=std)
+        w[name] = vals if m.wquant != "none" and name in NEXTN_PROJECTIONS else _as_dtype(vals, m.dtype)
     for name, n in norms.items():
         w[name] = normal(seed, "nextn." + name, (n,), std=std, mean=1.0)
     return w
