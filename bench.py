@@ -12,7 +12,7 @@ same model at B = 16 (N = 4, ragged 2k-32k contexts) and B = 64 (N = 2,
 context 4096), exact temp > 0 verification alone (mtp_verify_sample,
 B = 32, N = 3, V = 248320; that configuration has no draft block), and an
 Edge-shaped drafter with the centroid-routed LM head (B = 1, N = 3), the
-headline workload with Q8_0 projections, and the dense NextN drafter
+headline workload with Q8_0 and with Q4_0 projections, and the dense NextN drafter
 (Qwen-shaped, B = 1: two catch-up rows then N = 3 drafts from its own KV of
 4096 rows, one mtp_nextn_draft call + greedy verify), each
 reported under per_workload with its own roofline fraction, end-to-end
@@ -44,7 +44,7 @@ import synth  # noqa: E402
 METRIC = "drafted tok/s (MTP draft block + verify) at B=1..64; % of HBM/tensor roofline"
 UNIT = "tok/s"
 HEADLINE = 1
-OTHERS = (2, 3, 4, 5, 6, 7)
+OTHERS = (2, 3, 4, 5, 6, 8, 7)
 NEXTN = 7
 
 
@@ -54,8 +54,8 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4, 5, 6, 7],
-                    help="time this workload alone (default: the headline plus workloads 2-7)")
+    ap.add_argument("--workload", type=int, default=None, choices=[0, 1, 2, 3, 4, 5, 6, 7, 8],
+                    help="time this workload alone (default: the headline plus workloads 2-8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
 
@@ -98,7 +98,9 @@ def draft_config(w, world: int = 1) -> dict:
             if m.n_centroids else "dense tied")
     return dict({"workload": w.name, "B": w.B, "N": w.N, "vocab": m.vocab, "d_t": m.d_t, "d_a": m.d_a,
                  "n_blocks": m.n_blocks, "kv_len_max": int(w.kv_len.max()), "kv_len_min": int(w.kv_len.min()),
-                 "lm_head": head, "projections": "Q8_0 (bf16 table and KV)" if m.wquant == "q8_0" else m.dtype},
+                 "lm_head": head,
+                 "projections": {"q8_0": "Q8_0 (bf16 table and KV)", "q4_0": "Q4_0 (bf16 table and KV)"}.get(m.wquant,
+                                                                                                       m.dtype)},
                 **_common(world, False))
 
 
@@ -157,10 +159,11 @@ def draft_bytes_per_launch(w) -> int:
     head_w = m.vocab * m.d_t * esz + sum(int(w.weights[n].nbytes) for n in ("centroids", "token_ordering")
                                          if n in w.weights)
     wb = w.weight_bytes()
-    if m.wquant == "q8_0":   # the projections as Q8_0: a byte per weight plus a 2-byte scale per 32
+    if m.wquant in ("q8_0", "q4_0"):   # quantised projections: a byte (Q4_0: half) per weight, 2 bytes per 32
+        per = 1 if m.wquant == "q8_0" else 0.5
         for n in synth.projection_names(m):
             a = w.weights[n]
-            wb += a.size * (1 + 2 / 32) - a.nbytes
+            wb += a.size * (per + 2 / 32) - a.nbytes
     per_step = (wb - head_w + head_bytes_per_step(w) + kv_bytes_per_step(w) + w.B * m.d_t * esz)
     return int(w.N * per_step)
 

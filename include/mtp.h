@@ -70,7 +70,7 @@ enum {
 
 enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 };
 /* projection weight formats (mtp_config.wquant) */
-enum { MTP_WQ_NONE = 0, MTP_WQ_Q8_0 = 1 };
+enum { MTP_WQ_NONE = 0, MTP_WQ_Q8_0 = 1, MTP_WQ_Q4_0 = 2 };
 
 #define MTP_MAX_BLOCKS 8
 #define MTP_MAX_VIEWS 4
@@ -106,7 +106,13 @@ enum { MTP_WQ_NONE = 0, MTP_WQ_Q8_0 = 1 };
  *                  block scales, binary16 [out, in / 32] (see
  *                  mtp_quantize_q8_0); requires wdtype MTP_DTYPE_BF16 (the
  *                  table and KV), head_dim 64, 128 or 256, every input
- *                  width a multiple of 32; runs on the CUDA-core paths */
+ *                  width a multiple of 32; runs on the CUDA-core paths.
+ *                  MTP_WQ_Q4_0 (the same item's Q4_0 column): Q4_0 codes,
+ *                  uint8 [out, in / 2] -- per block of 32 weights 16 bytes,
+ *                  byte j holding the code of weight j in its low four bits
+ *                  and of weight j + 16 in its high four; the weight is
+ *                  (code - 8) times the block's binary16 scale [out, in / 32]
+ *                  (see mtp_quantize_q4_0); the same requirements as Q8_0 */
 typedef struct mtp_config {
     int32_t d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab;
     int32_t wdtype;
@@ -192,6 +198,16 @@ typedef struct mtp_sample_params {
  * scales [rows, cols / 32].  cols must be a multiple of 32 (MTP_ERR_ARG).
  * Synchronous, no device work. */
 int mtp_quantize_q8_0(const float *w, int64_t rows, int64_t cols, int8_t *codes, uint16_t *scales);
+/* Q4_0 quantisation on the host ("opus-mtp-turbo: Track 1 report", item 3,
+ * the Q4_0 format; the scale by ggml's rule, where the report's quantiser
+ * picks it by Lloyd iterations): per block of 32 consecutive weights of a row,
+ * m = the weight of largest magnitude (the first on ties), d = m / -8 (fp32),
+ * stored as binary16 (round to nearest even); codes q = min(15, trunc(w * (1 /
+ * d) + 8.5)) in fp32, 8 when d = 0.  Host pointers: w [rows, cols], codes
+ * [rows, cols / 2] uint8 (layout as for MTP_WQ_Q4_0), scales [rows, cols /
+ * 32].  cols must be a multiple of 32 (MTP_ERR_ARG).  Synchronous, no device
+ * work. */
+int mtp_quantize_q4_0(const float *w, int64_t rows, int64_t cols, uint8_t *codes, uint16_t *scales);
 
 /* Workspace bytes needed by any of the operations for these sizes (B
  * sequences, N drafts, vocabulary V).  cfg may be NULL when only the verify

@@ -26,6 +26,7 @@ MTP_DTYPE_F32 = 0
 MTP_DTYPE_BF16 = 1
 MTP_WQ_NONE = 0
 MTP_WQ_Q8_0 = 1
+MTP_WQ_Q4_0 = 2
 MTP_MAX_BLOCKS = 8
 MTP_MAX_VIEWS = 4
 MTP_MAX_BATCH = 64
@@ -35,7 +36,7 @@ MTP_MAX_CATCHUP = 16
 # every entry point include/mtp.h declares
 EXPORTS = ("mtp_workspace_size", "mtp_draft_block", "mtp_verify_greedy", "mtp_verify_sample",
            "mtp_sample_drafts", "mtp_quantize_q8_0", "mtp_last_error", "mtp_strerror", "mtp_debug_barrier_timeout",
-           "mtp_verify_greedy_noalloc", "mtp_nextn_draft")
+           "mtp_verify_greedy_noalloc", "mtp_nextn_draft", "mtp_quantize_q4_0")
 
 
 class MTPError(RuntimeError):
@@ -115,6 +116,8 @@ def lib():
             L.mtp_nextn_draft.argtypes = [P, P, P, P, I, I, P, P, P, I, P, P, P, P, P, P, P, Z, P]
             L.mtp_nextn_draft.restype = I
             L.mtp_quantize_q8_0.argtypes = [P, C.c_int64, C.c_int64, P, P]
+            L.mtp_quantize_q4_0.argtypes = [P, C.c_int64, C.c_int64, P, P]
+            L.mtp_quantize_q4_0.restype = I
             L.mtp_quantize_q8_0.restype = I
             _lib = L
     return _lib
@@ -170,7 +173,8 @@ def make_config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab
     return Config(d_t, d_a, n_blocks, n_q_heads, head_dim, n_kv_heads, d_ff, vocab,
                   MTP_DTYPE_BF16 if wdtype == "bf16" else MTP_DTYPE_F32, rms_eps,
                   0.0 if attn_scale is None else attn_scale, 0.0 if emb_scale is None else emb_scale,
-                  logit_softcap, n_centroids, centroid_top_k, MTP_WQ_Q8_0 if wquant == "q8_0" else MTP_WQ_NONE, 0)
+                  logit_softcap, n_centroids, centroid_top_k,
+                  {"q8_0": MTP_WQ_Q8_0, "q4_0": MTP_WQ_Q4_0}.get(wquant, MTP_WQ_NONE), 0)
 
 
 def quantize_q8_0(w):
@@ -186,6 +190,31 @@ def quantize_q8_0(w):
     if rc != MTP_OK:
         raise MTPError(rc, "mtp_quantize_q8_0")
     return q, d
+
+
+def quantize_q4_0(w):
+    """Q4_0 codes (uint8 [rows, cols / 2], two per byte) and block scales
+    (binary16 bits, uint16 [rows, cols / 32]) of an fp32 matrix, by
+    mtp_quantize_q4_0 (host)."""
+    import numpy as np
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    q = np.empty((rows, cols // 2), dtype=np.uint8)
+    d = np.empty((rows, cols // 32 if cols % 32 == 0 else 0), dtype=np.uint16)
+    rc = lib().mtp_quantize_q4_0(w.ctypes.data_as(C.c_void_p), rows, cols, q.ctypes.data_as(C.c_void_p),
+                                 d.ctypes.data_as(C.c_void_p))
+    if rc != MTP_OK:
+        raise MTPError(rc, "mtp_quantize_q4_0")
+    return q, d
+
+
+def quantize(w, wquant: str):
+    """Codes and block scales of an fp32 projection in the format wquant names."""
+    if wquant == "q8_0":
+        return quantize_q8_0(w)
+    if wquant == "q4_0":
+        return quantize_q4_0(w)
+    raise ValueError(wquant)
 
 
 def workspace_size(cfg: Config | None, B: int, N: int, V: int) -> int:
@@ -271,13 +300,18 @@ NEXTN_BLOCK_FIELDS = {"attn_norm": "attn_norm", "w_qkv": "w_q", "q_norm": "q_nor
 
 def make_nextn_weights(tensors: dict) -> Weights:
     """Pack the NextN drafter's device tensors (keys: NEXTN_FIELDS and
-    NEXTN_BLOCK_FIELDS) into mtp_weights: eh_proj is w_pre, head_norm is
-    final_norm, the fused query / key / value projection is blk[0].w_q."""
+    NEXTN_BLOCK_FIELDS, plus '<name>.scale' for quantised projections) into
+    mtp_weights: eh_proj is w_pre, head_norm is final_norm, the fused query /
+    key / value projection is blk[0].w_q."""
     w = Weights()
     for n, f in NEXTN_FIELDS.items():
         setattr(w, f, tensors[n].data_ptr())
+        if n + ".scale" in tensors:
+            setattr(w, f + "_scale", tensors[n + ".scale"].data_ptr())
     for n, f in NEXTN_BLOCK_FIELDS.items():
         setattr(w.blk[0], f, tensors[n].data_ptr())
+        if n + ".scale" in tensors:
+            setattr(w.blk[0], f + "_scale", tensors[n + ".scale"].data_ptr())
     return w
 
 

@@ -26,8 +26,9 @@ for _hd in (32, 64, 128, 256, 512):
     for _name, _bf, _tc in (("f32", 0, 0), ("bf16_cc", 1, 0), ("bf16_tc", 1, 1)):
         UNITS.append((f"draft_{_name}_{_hd}", "draft_inst.cu",
                       [f"-DMTP_WT_BF16={_bf}", f"-DMTP_HD={_hd}", f"-DMTP_TC={_tc}"]))
-for _hd in (64, 128, 256):   # Q8_0 projections
+for _hd in (64, 128, 256):   # Q8_0 and Q4_0 projections
     UNITS.append((f"draft_q8_{_hd}", "draft_inst.cu", ["-DMTP_WT_BF16=1", f"-DMTP_HD={_hd}", "-DMTP_TC=0", "-DMTP_Q8=1"]))
+    UNITS.append((f"draft_q4_{_hd}", "draft_inst.cu", ["-DMTP_WT_BF16=1", f"-DMTP_HD={_hd}", "-DMTP_TC=0", "-DMTP_Q4=1"]))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -39,7 +40,7 @@ def _nvcc() -> str:
 
 
 def _flags() -> list[str]:
-    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
+    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-ffp-contract=off", "-I", INCLUDE, "-I", CSRC,
                    "--expt-relaxed-constexpr"]
 
 

@@ -260,8 +260,8 @@ int check_config(const mtp_config* c) {
     if (!(c->rms_eps >= 0.f) || !(c->attn_scale >= 0.f) || !(c->emb_scale >= 0.f) || !(c->logit_softcap >= 0.f))
         return MTP_ERR_ARG;
     if (c->n_centroids < 0 || c->centroid_top_k < 0) return MTP_ERR_ARG;
-    if (c->wquant != MTP_WQ_NONE && c->wquant != MTP_WQ_Q8_0) return MTP_ERR_UNSUPPORTED;
-    if (c->wquant == MTP_WQ_Q8_0) {
+    if (c->wquant != MTP_WQ_NONE && c->wquant != MTP_WQ_Q8_0 && c->wquant != MTP_WQ_Q4_0) return MTP_ERR_UNSUPPORTED;
+    if (c->wquant != MTP_WQ_NONE) {
         if (c->wdtype != MTP_DTYPE_BF16 || (hd != 64 && hd != 128 && hd != 256)) return MTP_ERR_UNSUPPORTED;
         if (c->d_t % 32 || c->d_a % 32 || c->d_ff % 32 || (c->n_q_heads * hd) % 32) return MTP_ERR_UNSUPPORTED;
     }
@@ -360,6 +360,33 @@ int mtp_quantize_q8_0(const float* w, int64_t rows, int64_t cols, int8_t* codes,
     return MTP_OK;
 }
 
+int mtp_quantize_q4_0(const float* w, int64_t rows, int64_t cols, uint8_t* codes, uint16_t* scales) {
+    if (!w || !codes || !scales || rows < 0 || cols < 0 || cols % 32) return MTP_ERR_ARG;
+    const int64_t nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < nb; ++j) {
+            const float* x = w + r * cols + j * 32;
+            float amax = 0.f, m = 0.f;   // the first weight of largest magnitude, with its sign
+            for (int i = 0; i < 32; ++i) {
+                const float a = fabsf(x[i]);
+                if (a > amax) {
+                    amax = a;
+                    m = x[i];
+                }
+            }
+            const float d = m / -8.f;
+            const float inv = d != 0.f ? 1.f / d : 0.f;
+            uint8_t* q = codes + r * (cols / 2) + j * 16;
+            for (int i = 0; i < 16; ++i) {
+                const int lo = (int)(x[i] * inv + 8.5f), hi = (int)(x[i + 16] * inv + 8.5f);   // truncations
+                q[i] = (uint8_t)((lo < 15 ? lo : 15) | ((hi < 15 ? hi : 15) << 4));
+            }
+            scales[r * nb + j] = __half_as_ushort(__float2half_rn(d));
+        }
+    }
+    return MTP_OK;
+}
+
 size_t mtp_workspace_size(const mtp_config* cfg, int B, int N, int V) {
     if (B <= 0 || B > MTP_MAX_VERIFY_BATCH || N < 0 || N > 16 || V <= 0) return 0;
     if (cfg && B > MTP_MAX_BATCH) return 0;
@@ -397,7 +424,7 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
     if (rc != MTP_OK) return rc;
     if (nx) {
         if (cfg->d_a != cfg->d_t) return MTP_ERR_ARG;
-        if (cfg->n_blocks != 1 || cfg->n_centroids != 0 || cfg->wquant != MTP_WQ_NONE) return MTP_ERR_UNSUPPORTED;
+        if (cfg->n_blocks != 1 || cfg->n_centroids != 0) return MTP_ERR_UNSUPPORTED;
         if (nx->M < 0 || nx->M > MTP_MAX_CATCHUP) return MTP_ERR_ARG;
         if (nx->M > 0 && (!nx->cu_tok || !nx->cu_h)) return MTP_ERR_ARG;
         if ((reinterpret_cast<uintptr_t>(nx->cu_h) & 3) || (reinterpret_cast<uintptr_t>(nx->cu_tok) & 3) ||
@@ -421,8 +448,8 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
     // weights
     const void* mats[] = {w->tok_embd, w->w_pre, nx ? w->tok_embd : w->w_post};   // NextN has no post-projection
     for (const void* m : mats) if (!m || !aligned16(m)) return MTP_ERR_ARG;
-    if (cfg->wquant == MTP_WQ_Q8_0) {
-        const uint16_t* sc[] = {w->w_pre_scale, w->w_post_scale};
+    if (cfg->wquant != MTP_WQ_NONE) {
+        const uint16_t* sc[] = {w->w_pre_scale, nx ? w->w_pre_scale : w->w_post_scale};   // NextN: no post-projection
         for (const uint16_t* x : sc) if (!x || (reinterpret_cast<uintptr_t>(x) & 1)) return MTP_ERR_ARG;
         for (int l = 0; l < cfg->n_blocks; ++l) {
             const mtp_block_weights& b = w->blk[l];
@@ -495,10 +522,11 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
         tc_cols = kTcHeadCols;   // the head's two accumulators; the projections use the first 2 Bp columns
     }
     if (cent && cent_smem(cfg) > smem) smem = cent_smem(cfg);   // at most 100 KB (n_c <= MTP_MAX_CENTROIDS)
-    const bool q8 = cfg->wquant == MTP_WQ_Q8_0;
+    const bool q8 = cfg->wquant == MTP_WQ_Q8_0, q4 = cfg->wquant == MTP_WQ_Q4_0;
     const int per_sm = !bf ? draft_blocks_per_sm_f32(cfg->head_dim, smem)
                        : tc ? draft_blocks_per_sm_bf16_tc(cfg->head_dim, smem)
                        : q8 ? draft_blocks_per_sm_q8(cfg->head_dim, smem)
+                       : q4 ? draft_blocks_per_sm_q4(cfg->head_dim, smem)
                             : draft_blocks_per_sm_bf16_cc(cfg->head_dim, smem);
     if (per_sm < 1) return MTP_ERR_UNSUPPORTED;
 
@@ -517,15 +545,15 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
     p.w_pre = w->w_pre;
     p.final_norm = static_cast<const float*>(w->final_norm);
     p.w_post = w->w_post;
-    if (cfg->wquant == MTP_WQ_Q8_0) {
+    if (cfg->wquant != MTP_WQ_NONE) {
         p.s_pre = w->w_pre_scale;
-        p.s_post = w->w_post_scale;
+        p.s_post = nx ? nullptr : w->w_post_scale;
     }
     for (int l = 0; l < cfg->n_blocks; ++l) {
         const mtp_block_weights& b = w->blk[l];
         BlkW& d = p.blk[l];
         d.w_q = b.w_q; d.w_o = b.w_o; d.w_gate = b.w_gate; d.w_up = b.w_up; d.w_down = b.w_down;
-        if (q8) {
+        if (q8 || q4) {
             d.s_q = b.w_q_scale; d.s_o = b.w_o_scale; d.s_gate = b.w_gate_scale; d.s_up = b.w_up_scale;
             d.s_down = b.w_down_scale;
         }
@@ -635,6 +663,7 @@ int draft_impl(const mtp_config* cfg, const mtp_weights* w, const mtp_kv_view* v
     cudaError_t e = !bf ? launch_draft_f32(p, grid, smem, s)
                     : p.tc_head ? launch_draft_bf16_tc(p, grid, smem, s)
                     : q8 ? launch_draft_q8(p, grid, smem, s)
+                    : q4 ? launch_draft_q4(p, grid, smem, s)
                                 : launch_draft_bf16_cc(p, grid, smem, s);
     return e == cudaSuccess ? MTP_OK : MTP_ERR_CUDA;
 }

@@ -174,6 +174,9 @@ cudaError_t launch_draft_bf16_tc(const DraftParams& p, int grid, size_t smem, cu
 // bf16 table and KV, Q8_0 projections (CUDA-core paths); head_dim 64, 128 or 256
 cudaError_t launch_draft_q8(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
 int draft_blocks_per_sm_q8(int hd, size_t smem);
+// bf16 table and KV, Q4_0 projections (CUDA-core paths); head_dim 64, 128 or 256
+cudaError_t launch_draft_q4(const DraftParams& p, int grid, size_t smem, cudaStream_t s);
+int draft_blocks_per_sm_q4(int hd, size_t smem);
 int draft_blocks_per_sm_f32(int hd, size_t smem);
 int draft_blocks_per_sm_bf16_cc(int hd, size_t smem);
 int draft_blocks_per_sm_bf16_tc(int hd, size_t smem);

@@ -14,6 +14,7 @@ MTP_DECL_HDS(f32_)
 MTP_DECL_HDS(bf16_cc_)
 MTP_DECL_HDS(bf16_tc_)
 MTP_DECL_VARIANT(q8_64) MTP_DECL_VARIANT(q8_128) MTP_DECL_VARIANT(q8_256)
+MTP_DECL_VARIANT(q4_64) MTP_DECL_VARIANT(q4_128) MTP_DECL_VARIANT(q4_256)
 
 #define MTP_SWITCH_HD(pfx, call)        \
     switch (hd) {                       \
@@ -48,6 +49,20 @@ int draft_blocks_per_sm_q8(int hd, size_t smem) {
     case 64: return draft_blocks_per_sm_q8_64(smem);
     case 128: return draft_blocks_per_sm_q8_128(smem);
     default: return draft_blocks_per_sm_q8_256(smem);
+    }
+}
+cudaError_t launch_draft_q4(const DraftParams& p, int grid, size_t smem, cudaStream_t s) {
+    switch (p.hd) {
+    case 64: return launch_draft_q4_64(p, grid, smem, s);
+    case 128: return launch_draft_q4_128(p, grid, smem, s);
+    default: return launch_draft_q4_256(p, grid, smem, s);
+    }
+}
+int draft_blocks_per_sm_q4(int hd, size_t smem) {
+    switch (hd) {
+    case 64: return draft_blocks_per_sm_q4_64(smem);
+    case 128: return draft_blocks_per_sm_q4_128(smem);
+    default: return draft_blocks_per_sm_q4_256(smem);
     }
 }
 int draft_blocks_per_sm_f32(int hd, size_t smem) { MTP_SWITCH_HD(draft_blocks_per_sm_f32_, (smem)) }

@@ -2,7 +2,7 @@
 //
 // The build compiles this file once per (weight type, head dimension,
 // tensor-core paths) combination, selected by MTP_WT_BF16, MTP_HD and
-// MTP_TC (and MTP_Q8: Q8_0 projections beside a bf16 table and KV), so the
+// MTP_TC (and MTP_Q8 / MTP_Q4: Q8_0 / Q4_0 projections beside a bf16 table and KV), so the
 // kernel variants compile in parallel processes.  Each
 // object defines launch_draft_<variant> and draft_blocks_per_sm_<variant>;
 // draft_dispatch.cu picks one at run time.
@@ -17,10 +17,17 @@
 #if !defined(MTP_Q8)
 #define MTP_Q8 0
 #endif
+#if !defined(MTP_Q4)
+#define MTP_Q4 0
+#endif
 #if MTP_Q8
 #define MTP_WT uint16_t
 #define MTP_PT int8_t
 #define MTP_VAR MTP_CAT(q8_, MTP_HD)
+#elif MTP_Q4
+#define MTP_WT uint16_t
+#define MTP_PT Q4Code
+#define MTP_VAR MTP_CAT(q4_, MTP_HD)
 #elif MTP_WT_BF16
 #define MTP_WT uint16_t
 #if MTP_TC

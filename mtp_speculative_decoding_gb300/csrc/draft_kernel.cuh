@@ -131,6 +131,47 @@ template <> struct Chunk<int8_t> {
         return s;
     }
 };
+// Q4_0 codes (the same report's Q4_0 column, ggml's block format): 16 bytes
+// per block of 32 weights, byte j holding the code of weight j in its low
+// four bits and that of weight j + 16 in its high four; the weight is
+// (code - 8) times the block's binary16 scale (chunk_scale).  One chunk is
+// one block.
+struct Q4Code {
+    uint8_t packed;
+};
+template <> struct Chunk<Q4Code> {
+    static constexpr int EPC = 32;
+    static constexpr bool QUANT = true;
+    static __device__ __forceinline__ float dot(const uint4& w, const float* a) {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 lo = *reinterpret_cast<const float4*>(a + 4 * k);        // weights 4k .. 4k + 3
+            const float4 hi = *reinterpret_cast<const float4*>(a + 16 + 4 * k);   // weights 16 + 4k ..
+            const uint32_t x = ws[k];
+            s = fmaf((float)((int)(x & 15u) - 8), lo.x, s);
+            s = fmaf((float)((int)((x >> 8) & 15u) - 8), lo.y, s);
+            s = fmaf((float)((int)((x >> 16) & 15u) - 8), lo.z, s);
+            s = fmaf((float)((int)((x >> 24) & 15u) - 8), lo.w, s);
+            s = fmaf((float)((int)((x >> 4) & 15u) - 8), hi.x, s);
+            s = fmaf((float)((int)((x >> 12) & 15u) - 8), hi.y, s);
+            s = fmaf((float)((int)((x >> 20) & 15u) - 8), hi.z, s);
+            s = fmaf((float)((int)(x >> 28) - 8), hi.w, s);
+        }
+        return s;
+    }
+};
+// rows [r0, ...) of a [rows, K] weight matrix of type WT: K elements per row,
+// or K / 2 bytes of Q4_0 codes
+template <typename WT>
+__device__ __forceinline__ const WT* weight_rows(const WT* W, long long r0, int K) {
+    return W + r0 * K;
+}
+template <>
+__device__ __forceinline__ const Q4Code* weight_rows<Q4Code>(const Q4Code* W, long long r0, int K) {
+    return W + r0 * (K / 2);
+}
 // scale of chunk c of row r of a [rows, K] weight matrix: 1 unless quantised
 template <typename WT>
 __device__ __forceinline__ float chunk_scale(const uint16_t* S, long long r, int K, int c) {
@@ -157,8 +198,8 @@ __device__ __forceinline__ void gemv_rows(const WT* __restrict__ W, const WT* __
     const int nw = gridDim.x * kWarps;
     const unsigned long long pol = l2_evict_first();
     for (int r = gw; r < rows; r += nw) {
-        const uint4* wr = reinterpret_cast<const uint4*>(W + (long long)r * K);
-        const uint4* wr2 = TWO ? reinterpret_cast<const uint4*>(W2 + (long long)r * K) : nullptr;
+        const uint4* wr = reinterpret_cast<const uint4*>(weight_rows(W, r, K));
+        const uint4* wr2 = TWO ? reinterpret_cast<const uint4*>(weight_rows(W2, r, K)) : nullptr;
         float acc[NB], acc2[NB];
 #pragma unroll
         for (int j = 0; j < NB; ++j) { acc[j] = 0.f; acc2[j] = 0.f; }
@@ -211,7 +252,7 @@ __device__ __forceinline__ void gemv_rows_split(const WT* __restrict__ W, int ro
         const int r = r0 + warp / S;
         float acc = 0.f;
         if (r < rows) {
-            const uint4* wr = reinterpret_cast<const uint4*>(W + (long long)r * K);
+            const uint4* wr = reinterpret_cast<const uint4*>(weight_rows(W, r, K));
             for (int c0 = c_lo; c0 < c_hi; c0 += 32 * U) {
                 uint4 w[U];
 #pragma unroll
@@ -253,8 +294,8 @@ __device__ __forceinline__ void gemv_rows_pair(const WT* __restrict__ W, int row
     for (int r = gw; r < rows; r += 2 * nw) {
         const int r2 = r + nw;
         const bool two = r2 < rows;
-        const uint4* wa = reinterpret_cast<const uint4*>(W + (long long)r * K);
-        const uint4* wb = reinterpret_cast<const uint4*>(W + (long long)(two ? r2 : r) * K);
+        const uint4* wa = reinterpret_cast<const uint4*>(weight_rows(W, r, K));
+        const uint4* wb = reinterpret_cast<const uint4*>(weight_rows(W, two ? r2 : r, K));
         uint4 w[U];
 #pragma unroll
         for (int u = 0; u < UH; ++u) {
@@ -2491,7 +2532,7 @@ static __device__ void nextn_post(const DraftParams& p, float* x, float* gs, flo
     if (p.tc_head) fence_proxy_async_global();   // the head operand is read by bulk copies
 }
 
-// PT: the projections' weight type (WT, or int8_t for Q8_0 codes with block scales)
+// PT: the projections' weight type (WT, or int8_t / Q4Code for Q8_0 / Q4_0 codes with block scales)
 template <typename WT, int HD, bool TC, typename PT>
 __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* smem, TcState& ts, TcState& hs) {
     __shared__ float red[2 * kWarps];
@@ -2656,8 +2697,9 @@ __device__ __forceinline__ void draft_body(const DraftParams& p, unsigned char* 
                 // (the tensor-core path runs the whole projection for a catch-up row too)
                 const int q0 = k < 0 && !p.tc_proj ? p.Hq * p.hd : 0;
                 StoreEpi e{p.QR + q0, p.QS};
-                if (!gemv_step(PH_Q, k, l, reinterpret_cast<const PT*>(bw.w_q) + (long long)q0 * p.d_a, nullptr,
-                               nullptr, nullptr, p.QS - q0, p.d_a, e, One{}))
+                if (!gemv_step(PH_Q, k, l, weight_rows(reinterpret_cast<const PT*>(bw.w_q), q0, p.d_a), nullptr,
+                               bw.s_q ? bw.s_q + (long long)q0 * (p.d_a / 32) : nullptr, nullptr, p.QS - q0, p.d_a, e,
+                               One{}))
                     return;
                 nextn_kv_write<WT>(p, k, s_kv);
                 if (k < 0) break;   // catch-up: the next PRE's barrier orders the stores

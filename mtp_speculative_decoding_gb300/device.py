@@ -7,7 +7,7 @@ import dataclasses
 import numpy as np
 
 from . import (Config, KVView, Weights, alloc_workspace, draft_block, make_config, make_nextn_weights, make_view,
-               make_weights, nextn_draft, quantize_q8_0, workspace_size)
+               make_weights, nextn_draft, quantize, workspace_size)
 
 
 def to_device(a: np.ndarray, dtype: str | None = None, device="cuda"):
@@ -63,13 +63,13 @@ def upload_draft(w, device="cuda", extra_ws_for=None, reuse: "DeviceDraft | None
     if same:
         tensors = {n: reuse.tensors[n] for n in w.weights}
         reuse.tensors.pop("_views", None)   # the old views go with the old workload
-    elif getattr(m, "wquant", "none") == "q8_0":
-        # Q8_0 projections: quantised here by the library's host quantiser,
-        # codes and block scales uploaded side by side
+    elif getattr(m, "wquant", "none") in ("q8_0", "q4_0"):
+        # Q8_0 / Q4_0 projections: quantised here by the library's host
+        # quantiser, codes and block scales uploaded side by side
         tensors = {}
         for n, a in w.weights.items():
             if a.dtype == np.float32 and a.ndim == 2 and n.split(".")[-1].startswith("w_"):
-                q, d = quantize_q8_0(a)
+                q, d = quantize(a, m.wquant)
                 tensors[n] = torch.from_numpy(q).to(device)
                 tensors[n + ".scale"] = torch.from_numpy(d.view(np.int16)).to(device)
             else:
@@ -129,8 +129,16 @@ def upload_nextn(w, device="cuda") -> DeviceNextn:
     m = w.model
     cfg = make_config(m.d, m.d, 1, m.n_q_heads, m.head_dim, m.n_kv_heads, m.d_ff, m.vocab, wdtype=m.dtype,
                       rms_eps=m.rms_eps, attn_scale=m.attn_scale, emb_scale=m.emb_scale,
-                      logit_softcap=m.logit_softcap)
-    tensors = {n: to_device(a, device=device) for n, a in w.weights.items()}
+                      logit_softcap=m.logit_softcap, wquant=m.wquant)
+    tensors = {}
+    for n, a in w.weights.items():
+        if m.wquant != "none" and a.dtype == np.float32 and a.ndim == 2:
+            # a quantised projection: codes and block scales by the library's host quantiser
+            q, d = quantize(a, m.wquant)
+            tensors[n] = torch.from_numpy(q).to(device)
+            tensors[n + ".scale"] = torch.from_numpy(d.view(np.int16)).to(device)
+        else:
+            tensors[n] = to_device(a, device=device)
     weights = make_nextn_weights(tensors)
     k, v = to_device(w.dkv["k"], device=device), to_device(w.dkv["v"], device=device)
     view = make_view(k, v, w.dkv["cap"], 0, w.dkv["rope_theta"])

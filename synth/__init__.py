@@ -338,6 +338,7 @@ WORKLOADS = {
     5: "edge-centroid-bf16-b1-n3-ctx4096",
     6: "gemma-assistant-q8-b1-n3-ctx8192",
     7: "nextn-qwen-dense-bf16-b1-n3-kv4096-catchup2",
+    8: "gemma-assistant-q4-b1-n3-ctx8192",
 }
 
 
@@ -350,7 +351,8 @@ def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None
 
     Workload 5 is the Edge-shaped model with the centroid-routed head, batch
     1, N = 3, a sliding layer (window 512) and a full layer of 4096 positions.
-    Workload 6 is workload 1 with Q8_0 projections (the table and KV bf16).
+    Workload 6 is workload 1 with Q8_0 projections (the table and KV bf16),
+    workload 8 the same with Q4_0 projections.
 
     ``B`` may shrink the batch (the first B sequences' lengths are kept) for
     parity runs at full model size.  ``sink`` > 0 keeps that many attention-
@@ -373,8 +375,9 @@ def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None
     elif cfg_id == 3:
         m, views = _gemma_assistant(), _gemma_views(4096)
         Bf, N, kv = 64, 2, np.full(64, 4096)
-    elif cfg_id == 6:
-        m, views = dataclasses.replace(_gemma_assistant(), wquant="q8_0"), _gemma_views(8192)
+    elif cfg_id in (6, 8):
+        q = "q8_0" if cfg_id == 6 else "q4_0"
+        m, views = dataclasses.replace(_gemma_assistant(), wquant=q), _gemma_views(8192)
         Bf, N, kv = 1, 3, np.array([8192])
     elif cfg_id == 5:
         m = _edge_assistant()
@@ -389,8 +392,8 @@ def make_draft_inputs(cfg_id: int, seed: int | None = None, B: int | None = None
     if sink and cfg_id in (1, 2, 3):
         views = [ViewSpec(cap=views[0].cap, window=views[0].window, rope_theta=views[0].rope_theta, sink=sink)] + views[1:]
     # workloads 1-3 share one model ("same model as config 1"): its weights use seed 1001;
-    # workload 6 quantises that model's projections (the same fp32 draws)
-    model_seed = workload_seed(1) if cfg_id in (1, 2, 3, 6) else seed
+    # workloads 6 and 8 quantise that model's projections (the same fp32 draws)
+    model_seed = workload_seed(1) if cfg_id in (1, 2, 3, 6, 8) else seed
     return make_draft_workload(name, m, views, B, N, kv, seed, hist_len=64, model_seed=model_seed)
 
 
@@ -585,7 +588,7 @@ def make_verify_greedy_inputs(cfg_id: int, seed: int | None = None, B: int | Non
     seed = workload_seed(cfg_id) if seed is None else seed
     defaults = {0: (1, 3, 4096, "f32"), 1: (1, 3, 262144, "bf16"), 2: (16, 4, 262144, "bf16"),
                 3: (64, 2, 262144, "bf16"), 5: (1, 3, 262144, "bf16"), 6: (1, 3, 262144, "bf16"),
-                7: (1, 3, 248320, "bf16")}
+                7: (1, 3, 248320, "bf16"), 8: (1, 3, 262144, "bf16")}
     Bd, Nd, Vd, dd = defaults[cfg_id]
     B = Bd if B is None else B
     N = Nd if N is None else N

@@ -104,3 +104,29 @@ def test_host_q8_0_quantiser_matches_the_oracle():
     np.testing.assert_array_equal(d1, d2)
     with pytest.raises(mtp.MTPError):
         mtp.quantize_q8_0(np.zeros((2, 48), dtype=np.float32))
+
+
+def test_host_q4_0_quantiser_matches_the_oracle():
+    """mtp_quantize_q4_0 (host code of the library) and the oracle's
+    quantiser give the same codes and scales bit for bit, over Gaussian rows,
+    code multiples of a power-of-two scale, zero blocks, opposite extremes of
+    one magnitude (the clamp to 15), ties of the extreme, and extreme ranges."""
+    import numpy as np
+    import oracle
+    import synth
+    mtp_build.build()
+    rng = np.random.default_rng(13)
+    w = synth.normal(14, "hostq4", (96, 512), std=0.02)
+    w[3, :32] = 0.0
+    w[4] *= 1e-6
+    w[5] *= 1e4
+    w[6, :32] = (np.arange(32, dtype=np.float32) % 16 - 8) * np.float32(2.0 ** -5)
+    w[7] = rng.standard_normal(512).astype(np.float32) * 3e-8
+    w[8, :32] = 0.0
+    w[8, 2], w[8, 30] = 0.5, -0.5                  # equal magnitudes: the first is the extreme
+    q1, d1 = mtp.quantize_q4_0(w)
+    q2, d2 = oracle.quantize_q4_0(w)
+    np.testing.assert_array_equal(q1, q2)
+    np.testing.assert_array_equal(d1, d2)
+    with pytest.raises(mtp.MTPError):
+        mtp.quantize_q4_0(np.zeros((2, 48), dtype=np.float32))

@@ -292,3 +292,17 @@ def test_null_counts_mean_no_catch_up():
     assert mtp.last_error(dev.ws) == 0
     np.testing.assert_array_equal(d.cpu().numpy(), ref["drafts"])
     np.testing.assert_array_equal(h.cpu().numpy(), ref["h"])
+
+
+@pytest.mark.parametrize("wquant", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("B", [1, 4])
+def test_quantised_projections(wquant, B):
+    """Q8_0 and Q4_0 projections (eh_proj, the fused query / key / value
+    projection with the catch-up rows' key and value rows at their row and
+    scale offsets, w_o, the SwiGLU matrices) beside the bf16 table and KV; the
+    oracle runs on the weights the codes stand for."""
+    m = synth.NextnSpec(d=512, n_q_heads=4, head_dim=64, n_kv_heads=2, d_ff=1024, vocab=3000, dtype="bf16",
+                        rope_theta=1e4, wquant=wquant)
+    kv, nc = [0, 5, 9, 2][:B], [1, 0, 2, 2][:B]
+    w = synth.make_nextn_workload("q-nextn", m, B, 3, 2, kv, nc, 50 + B)
+    check(w, run(w))

@@ -1,7 +1,7 @@
-"""GPU parity of the draft block with Q8_0 projections ("opus-mtp-turbo:
-Track 1 report", item 3): the codes and scales come from the library's host
-quantiser (bit-identical to the oracle's, checked on the CPU), the table and
-the KV stay bf16.  The oracle runs the chain on the weights the codes stand
+"""GPU parity of the draft block with Q8_0 and Q4_0 projections
+("opus-mtp-turbo: Track 1 report", item 3): the codes and scales come from the
+library's host quantiser (bit-identical to the oracle's, checked on the CPU),
+the table and the KV stay bf16.  The oracle runs the chain on the weights the codes stand
 for (exact in fp32), so the GPU's only departures are fp32 accumulation
 orders: logits and h_last within 1e-3 of the rms, drafts equal wherever the
 top-1 / top-2 margin exceeds 1e-2 of the row's standard deviation.
@@ -24,9 +24,9 @@ def _built():
     build.build()
 
 
-def q8_workload(B=3, N=3, d_t=512, d_a=256, hd=64, V=3000, seed=31, softcap=0.0, views=None, kv=None):
+def q8_workload(B=3, N=3, d_t=512, d_a=256, hd=64, V=3000, seed=31, softcap=0.0, views=None, kv=None, wquant="q8_0"):
     m = synth.ModelSpec(d_t=d_t, d_a=d_a, n_blocks=2, n_q_heads=4, head_dim=hd, n_kv_heads=2, d_ff=512, vocab=V,
-                        dtype="bf16", block_view=(0, 1), logit_softcap=softcap, wquant="q8_0")
+                        dtype="bf16", block_view=(0, 1), logit_softcap=softcap, wquant=wquant)
     views = views or [synth.ViewSpec(cap=96, window=40, rope_theta=1e4), synth.ViewSpec(cap=200, window=0, rope_theta=1e6)]
     kv = np.random.default_rng(seed).integers(1, 201, size=B) if kv is None else kv
     return synth.make_draft_workload("q8-test", m, views, B, N, kv, seed, hist_len=8)
@@ -48,24 +48,27 @@ def check(w, d, h, z, seqs):
         assert np.max(np.abs(h[b] - ho)) <= TOL * float(np.sqrt(np.mean(ho * ho)))
 
 
+@pytest.mark.parametrize("wquant", ["q8_0", "q4_0"])
 @pytest.mark.parametrize("B", [1, 3, 12])
-def test_q8_parity(B):
+def test_q8_parity(B, wquant):
     """B = 1: split and paired single-sequence rows and the bulk-copy head;
     B = 3 and 12: the four-column GEMV rows."""
-    w = q8_workload(B=B, softcap=8.0 if B == 3 else 0.0)
+    w = q8_workload(B=B, softcap=8.0 if B == 3 else 0.0, wquant=wquant)
     _, d, h, z = run_gpu_draft(w)
     check(w, d, h, z, range(B))
 
 
+@pytest.mark.parametrize("wquant", ["q8_0", "q4_0"])
 @pytest.mark.parametrize("hd", [128, 256])
-def test_q8_head_dims(hd):
-    w = q8_workload(B=2, hd=hd, d_a=512)
+def test_q8_head_dims(hd, wquant):
+    w = q8_workload(B=2, hd=hd, d_a=512, wquant=wquant)
     _, d, h, z = run_gpu_draft(w)
     check(w, d, h, z, range(2))
 
 
-def test_q8_timed_path_without_logits():
-    w = q8_workload(B=3, seed=5)
+@pytest.mark.parametrize("wquant", ["q8_0", "q4_0"])
+def test_q8_timed_path_without_logits(wquant):
+    w = q8_workload(B=3, seed=5, wquant=wquant)
     dev, d1, h1, _ = run_gpu_draft(w)
     _, d2, h2, _ = run_gpu_draft(w, want_logits=False, dev=dev)
     np.testing.assert_array_equal(d1, d2)
@@ -100,5 +103,12 @@ def test_q8_missing_scales_rejected():
 @pytest.mark.slow
 def test_q8_gemma_workload():
     w = synth.make_draft_inputs(6)
+    _, d, h, z = run_gpu_draft(w)
+    check(w, d, h, z, [0])
+
+
+@pytest.mark.slow
+def test_q4_gemma_workload():
+    w = synth.make_draft_inputs(8)
     _, d, h, z = run_gpu_draft(w)
     check(w, d, h, z, [0])
