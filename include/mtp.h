@@ -299,12 +299,14 @@ int mtp_draft_block(const mtp_config *cfg, const mtp_weights *w,
  * n_cu + 1: the rows of steps k >= 1 are the drafter's own guesses, and the
  * next call's catch-up rewrites the accepted ones (no rollback is needed).
  * Arguments:
- *   cfg        d_a == d_t, n_blocks == 1, n_centroids == 0, wquant NONE;
- *              rope_theta comes from dkv
+ *   cfg        d_a == d_t, n_blocks == 1, n_centroids == 0; wquant NONE,
+ *              Q8_0 or Q4_0 (then w_pre_scale and blk[0]'s w_q, w_o,
+ *              w_gate, w_up, w_down scales are required); rope_theta comes
+ *              from dkv
  *   w          tok_embd, norm_e, norm_h, w_pre (eh_proj), final_norm (head
  *              norm); blk[0]: attn_norm, w_q (fused), q_norm, k_norm, w_o,
  *              pre_ffn_norm, w_gate, w_up, w_down (w_post, post_attn_norm,
- *              post_ffn_norm, centroids and scales unused, may be NULL)
+ *              post_ffn_norm, centroids and w_post_scale unused, may be NULL)
  *   dkv        host pointer to one view (data on device, written)
  *   kv_len [B] int32 >= 0;  n_cu [B] int32 in [0, M] (NULL: all 0)
  *   cu_tok [B, M] int32, cu_h [B, M, d] fp32 (only rows j < n_cu[b] are read;
