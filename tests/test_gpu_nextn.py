@@ -20,8 +20,6 @@ import synth
 
 pytestmark = pytest.mark.gpu
 
-FILL = np.float32(np.nan)
-
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
@@ -53,13 +51,8 @@ def run(w, dev=None, want_logits=True, conf=False):
     assert mtp.last_error(dev.ws) == 0
     out = dict(dev=dev, drafts=drafts.cpu().numpy(), h=h.cpu().numpy(), z=None if z is None else z.cpu().numpy(),
                conf=None if c is None else c.cpu().numpy())
-    out["k"], out["v"] = _kv_host(dev.k, w), _kv_host(dev.v, w)
+    out["k"], out["v"] = dev.k.float().cpu().numpy(), dev.v.float().cpu().numpy()   # the drafter KV, as fp32
     return out
-
-
-def _kv_host(t, w):
-    a = t.float().cpu().numpy()
-    return a
 
 
 def _widen(a, w):
