@@ -327,3 +327,16 @@ def test_confidence_workloads(cfg):
     w = synth.make_draft_inputs(cfg)
     d, c, z = run_conf(w)
     check_conf(w, d, c, z, [0] if w.B == 1 else SPREAD64[::4])
+
+
+@pytest.mark.parametrize("dtype,B", [("bf16", 1), ("bf16", 3), ("f32", 2)])
+def test_head_dim_512(dtype, B):
+    """head_dim 512 (two 16-byte chunks per lane per key row in bf16, four in
+    fp32; two query heads per attention pass) on a sliding and a full view,
+    one sequence (CUDA-core head) and a batch (bf16: tensor-core head)."""
+    m = synth.ModelSpec(d_t=1024, d_a=512, n_blocks=2, n_q_heads=4, head_dim=512, n_kv_heads=2, d_ff=1024,
+                        vocab=2000, dtype=dtype, block_view=(0, 1))
+    views = [synth.ViewSpec(cap=64, window=48, rope_theta=1e4), synth.ViewSpec(cap=300, window=0, rope_theta=1e6)]
+    w = synth.make_draft_workload("hd512", m, views, B, 3, [70, 200, 33][:B], 51 + B, hist_len=4)
+    _, d, h, z = run_gpu_draft(w)
+    check_draft_parity(w, d, h, z, seqs=range(B))

@@ -299,3 +299,11 @@ def test_quantised_projections(wquant, B):
     kv, nc = [0, 5, 9, 2][:B], [1, 0, 2, 2][:B]
     w = synth.make_nextn_workload("q-nextn", m, B, 3, 2, kv, nc, 50 + B)
     check(w, run(w))
+
+
+def test_head_dim_512():
+    m = synth.NextnSpec(d=1024, n_q_heads=4, head_dim=512, n_kv_heads=2, d_ff=1024, vocab=2000, dtype="bf16",
+                        rope_theta=1e4)
+    for B in (1, 3):
+        w = synth.make_nextn_workload("hd512-nextn", m, B, 3, 2, [9, 0, 30][:B], [2, 1, 0][:B], 60 + B)
+        check(w, run(w))
