@@ -340,3 +340,19 @@ def test_head_dim_512(dtype, B):
     w = synth.make_draft_workload("hd512", m, views, B, 3, [70, 200, 33][:B], 51 + B, hist_len=4)
     _, d, h, z = run_gpu_draft(w)
     check_draft_parity(w, d, h, z, seqs=range(B))
+
+
+@pytest.mark.parametrize("dtype,B", [("f32", 1), ("bf16", 2)])
+def test_api_limits(dtype, B):
+    """The largest shapes the header allows in one call: N = 16 draft steps,
+    MTP_MAX_BLOCKS = 8 blocks over MTP_MAX_VIEWS = 4 views, 16 query heads per
+    KV head."""
+    import mtp_speculative_decoding_gb300 as mtp
+    m = synth.ModelSpec(d_t=256, d_a=128, n_blocks=mtp.MTP_MAX_BLOCKS, n_q_heads=16, head_dim=32, n_kv_heads=1,
+                        d_ff=256, vocab=1500, dtype=dtype, block_view=(0, 1, 2, 3, 3, 2, 1, 0))
+    views = [synth.ViewSpec(cap=40, window=24, rope_theta=1e4), synth.ViewSpec(cap=90, window=0, rope_theta=1e6),
+             synth.ViewSpec(cap=32, window=16, rope_theta=5e3, sink=4), synth.ViewSpec(cap=120, window=0, rope_theta=2e5)]
+    assert len(views) == mtp.MTP_MAX_VIEWS
+    w = synth.make_draft_workload("limits", m, views, B, 16, [77, 30][:B], 70 + B, hist_len=4)
+    _, d, h, z = run_gpu_draft(w)
+    check_draft_parity(w, d, h, z, seqs=range(B))

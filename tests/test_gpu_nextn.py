@@ -307,3 +307,10 @@ def test_head_dim_512():
     for B in (1, 3):
         w = synth.make_nextn_workload("hd512-nextn", m, B, 3, 2, [9, 0, 30][:B], [2, 1, 0][:B], 60 + B)
         check(w, run(w))
+
+
+def test_sixteen_drafts_and_sixteen_heads_per_kv_head():
+    m = synth.NextnSpec(d=256, n_q_heads=16, head_dim=32, n_kv_heads=1, d_ff=512, vocab=1500, dtype="bf16",
+                        rope_theta=1e4)
+    w = synth.make_nextn_workload("limits-nextn", m, 2, 16, 3, [5, 0], [3, 1], 81)
+    check(w, run(w))
