@@ -356,3 +356,11 @@ def test_api_limits(dtype, B):
     w = synth.make_draft_workload("limits", m, views, B, 16, [77, 30][:B], 70 + B, hist_len=4)
     _, d, h, z = run_gpu_draft(w)
     check_draft_parity(w, d, h, z, seqs=range(B))
+
+
+def test_sampled_sixteen_steps_small_batch():
+    """Sampled drafting over N = 16 steps (the penalty set grows to the history
+    plus 15 drafts) at B = 3, bf16: the tensor-core head with the sampler."""
+    w = small_workload("bf16", N=16, seed=17)
+    d, h, z = run_sampled(w, seed=4321, offset=2)
+    check_sampled(w, 4321, 2, d, h, z, seqs=range(w.B))

@@ -314,3 +314,15 @@ def test_sixteen_drafts_and_sixteen_heads_per_kv_head():
                         rope_theta=1e4)
     w = synth.make_nextn_workload("limits-nextn", m, 2, 16, 3, [5, 0], [3, 1], 81)
     check(w, run(w))
+
+
+def test_maximum_catch_up_on_the_tensor_core_path():
+    """Sixteen catch-up iterations through the split-K tensor-core projections
+    (width 1024, SwiGLU 4096, B = 24 bf16: the inputs outgrow shared memory)."""
+    import mtp_speculative_decoding_gb300 as mtp
+    m = synth.NextnSpec(d=1024, n_q_heads=8, head_dim=128, n_kv_heads=2, d_ff=4096, vocab=3000, dtype="bf16",
+                        rope_theta=1e4)
+    B, M = 24, mtp.MTP_MAX_CATCHUP
+    w = synth.make_nextn_workload("tc-catchup", m, B, 2, M, [3 * i for i in range(B)], [(5 * i) % (M + 1) for i in range(B)],
+                                  91)
+    check(w, run(w, want_logits=False), seqs=[0, 3, 16, B - 1])
