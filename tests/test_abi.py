@@ -130,3 +130,33 @@ def test_host_q4_0_quantiser_matches_the_oracle():
     np.testing.assert_array_equal(d1, d2)
     with pytest.raises(mtp.MTPError):
         mtp.quantize_q4_0(np.zeros((2, 48), dtype=np.float32))
+
+
+def test_nextn_host_checks_reject_before_any_device_work():
+    """mtp_nextn_draft's argument checks return before the first CUDA call, so
+    they run without a GPU: a NextN config needs d_a == d_t and one block, the
+    drafter KV a plain view (window 0), at most MTP_MAX_CATCHUP catch-up rows,
+    catch-up arrays when M > 0, and no sampling.  (Placeholder addresses: none
+    is dereferenced.)"""
+    import ctypes as C
+    mtp_build.build()
+    L = mtp.lib()
+    fake = 1 << 20   # 16-byte aligned, never dereferenced
+
+    def call(cfg, view, M=2, cu=True, kv_len=fake):
+        w = mtp.Weights()
+        w.tok_embd = w.norm_e = w.norm_h = w.w_pre = w.final_norm = fake
+        b = w.blk[0]
+        b.attn_norm = b.w_q = b.q_norm = b.k_norm = b.w_o = b.pre_ffn_norm = b.w_gate = b.w_up = b.w_down = fake
+        return L.mtp_nextn_draft(C.byref(cfg), C.byref(w), C.byref(view), kv_len, 1, 3, fake,
+                                 fake if cu else None, fake if cu else None, M, fake, fake, fake, None, None, None,
+                                 fake, 1 << 30, None)
+
+    good_view = mtp.KVView(fake, fake, 4 * 64 * 64, 64 * 64, 64, 64, 0, 1e4, 0)
+    cfg = mtp.make_config(256, 256, 1, 4, 64, 2, 512, 1000)
+    assert call(mtp.make_config(256, 128, 1, 4, 64, 2, 512, 1000), good_view) == mtp.MTP_ERR_ARG      # d_a != d_t
+    assert call(mtp.make_config(256, 256, 2, 4, 64, 2, 512, 1000), good_view) == mtp.MTP_ERR_UNSUPPORTED
+    assert call(cfg, mtp.KVView(fake, fake, 4 * 64 * 64, 64 * 64, 64, 64, 16, 1e4, 0)) == mtp.MTP_ERR_ARG  # window
+    assert call(cfg, good_view, M=mtp.MTP_MAX_CATCHUP + 1) == mtp.MTP_ERR_ARG
+    assert call(cfg, good_view, M=2, cu=False) == mtp.MTP_ERR_ARG                                      # no rows
+    assert call(cfg, good_view, kv_len=None) == mtp.MTP_ERR_ARG                                        # no kv_len
